@@ -1,0 +1,5 @@
+"""Oracle (test infrastructure only): plain CPU restatement of the MoE layer forward.
+
+Only the tests, the smoke check and the bench's CPU-baseline leg import this package.
+"""
+from . import moe_oracle  # noqa: F401

@@ -1,0 +1,13 @@
+"""Seeded synthetic inputs shared by the oracle tests, the GPU tests and the bench.
+
+This package draws random tensors of the workload shapes and nothing else: it
+holds none of the MoE layer's arithmetic.
+"""
+from .moe_inputs import (  # noqa: F401
+    CONFIGS,
+    LayerShape,
+    bf16_bits_from_f32,
+    f32_from_bf16_bits,
+    make_layer,
+    make_tokens,
+)

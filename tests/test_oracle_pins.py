@@ -1,0 +1,373 @@
+"""Pins of the oracle against facts that do not come from the oracle itself.
+
+Each test checks one oracle function against brute force, a closed form, a special
+case that reduces to a library routine, an invariant the method fixes, or the
+hand-worked example in tests/golden/.  A plausible slip (dropped term, wrong sign,
+transposed operand, wrong index) fails at least one of them.
+"""
+import itertools
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+from synth import CONFIGS, f32_from_bf16_bits, make_layer
+
+
+def _bf(b):
+    return f32_from_bf16_bits(b).astype(np.float64)
+
+
+# ---------------------------------------------------------------- top-k selection
+
+def _brute_force_topk(keys_row, k):
+    """Best k-subset: maximise the descending key vector, then the smallest index set."""
+    E = len(keys_row)
+    best = None
+    for subset in itertools.combinations(range(E), k):
+        vec = tuple(sorted((float(keys_row[e]) for e in subset), reverse=True))
+        rank = (tuple(-v for v in vec), subset)
+        if best is None or rank < best[0]:
+            best = (rank, subset)
+    chosen = best[1]
+    return sorted(chosen, key=lambda e: (-float(keys_row[e]), e))
+
+
+@pytest.mark.parametrize("k", [1, 2, 3])
+def test_topk_matches_brute_force_with_ties(k):
+    rng = np.random.default_rng(11)
+    E, T = 8, 200
+    # Few distinct values so that ties are everywhere.
+    scores = rng.choice(np.array([0.25, 0.5, 0.625, 0.75], np.float32), size=(T, E))
+    bias = rng.choice(np.array([0.0, 0.125, -0.125], np.float32), size=E)
+    idx = O.topk_select(scores, bias, k)
+    keys = scores + bias[None, :]
+    for t in range(T):
+        assert list(idx[t]) == _brute_force_topk(keys[t], k)
+
+
+def test_topk_tiny_workload_matches_brute_force():
+    s = CONFIGS["tiny"]
+    L = make_layer(s, "tiny")
+    sc = O.router_scores(L["x"], L["w_router"]).astype(np.float32)
+    idx = O.topk_select(sc, L["bias"], 2)
+    keys = O.selection_keys(sc, L["bias"])
+    for t in range(s.T):
+        assert list(idx[t]) == _brute_force_topk(keys[t], 2)
+
+
+def test_topk_matches_stable_argsort_library():
+    rng = np.random.default_rng(3)
+    scores = rng.random((300, 64)).astype(np.float32)
+    bias = (rng.random(64).astype(np.float32) - 0.5) * np.float32(0.02)
+    keys = (scores + bias).astype(np.float32)
+    lib = np.argsort(-keys, axis=1, kind="stable")[:, :2]
+    assert np.array_equal(O.topk_select(scores, bias, 2), lib)
+
+
+def test_topk_all_equal_keys_picks_lowest_indices():
+    scores = np.full((5, 8), 0.5, np.float32)
+    idx = O.topk_select(scores, np.zeros(8, np.float32), 2)
+    assert (idx == np.array([0, 1])).all()
+
+
+def test_top1_is_first_argmax():
+    rng = np.random.default_rng(5)
+    scores = rng.choice(np.array([0.1, 0.2, 0.3], np.float32), size=(100, 16))
+    idx = O.topk_select(scores, np.zeros(16, np.float32), 1)
+    assert np.array_equal(idx[:, 0], np.argmax(scores, axis=1))
+
+
+def test_bias_steers_selection_only():
+    # A bias that flips the winner must not enter the gate: gates use the raw score.
+    scores = np.array([[0.6, 0.5, 0.1]], np.float32)
+    bias = np.array([0.0, 0.2, 0.0], np.float32)
+    idx = O.topk_select(scores, bias, 1)
+    assert idx[0, 0] == 1
+    g = O.gate_weights(scores, idx, renorm=False)
+    assert g[0, 0] == np.float64(np.float32(0.5))
+
+
+# ---------------------------------------------------------------- router scores
+
+def test_sigmoid_closed_forms_and_orientation():
+    # W_r is a non-symmetric permutation: logit_e = x[sigma(e)].  With x = ln 3 at the
+    # position expert 2 reads and -ln 3 where expert 0 reads, the scores are 3/4 and 1/4.
+    d, E = 4, 4
+    sigma = [3, 0, 1, 2]
+    W = np.zeros((E, d), np.float32)
+    for e in range(E):
+        W[e, sigma[e]] = 1.0
+    x = np.zeros((1, d))
+    x[0, 1] = math.log(3.0)   # expert 2 reads x[1]
+    x[0, 3] = -math.log(3.0)  # expert 0 reads x[3]
+    s = O.router_scores(x, W)
+    assert s[0, 2] == pytest.approx(0.75, abs=1e-15)
+    assert s[0, 0] == pytest.approx(0.25, abs=1e-15)
+    assert s[0, 1] == 0.5 and s[0, 3] == 0.5
+    off = np.array([0.0, math.log(3.0), 0.0, 0.0])
+    assert O.router_scores(np.zeros((1, d)), W, off)[0, 1] == pytest.approx(0.75, abs=1e-15)
+
+
+def test_zero_tokens_give_half_scores_and_lowest_pair():
+    E, d = 8, 64
+    W = np.random.default_rng(0).standard_normal((E, d)).astype(np.float32)
+    s = O.router_scores(np.zeros((3, d)), W)
+    assert (s == 0.5).all()
+    idx = O.topk_select(s.astype(np.float32), np.zeros(E, np.float32), 2)
+    assert (idx == [0, 1]).all()
+    assert (O.gate_weights(s, idx, True) == 0.5).all()
+
+
+def test_router_matches_torch_library():
+    s = CONFIGS["tiny"]
+    L = make_layer(s, "tiny")
+    ref = torch.sigmoid(torch.from_numpy(L["x"]).double() @ torch.from_numpy(L["w_router"]).double().T)
+    assert np.allclose(O.router_scores(L["x"], L["w_router"]), ref.numpy(), rtol=0, atol=1e-14)
+
+
+# ---------------------------------------------------------------- gates and loads
+
+def test_gate_renorm_properties():
+    rng = np.random.default_rng(8)
+    s = rng.random((50, 16))
+    idx = O.topk_select(s.astype(np.float32), np.zeros(16, np.float32), 2)
+    g = O.gate_weights(s, idx, True)
+    assert np.allclose(g.sum(axis=1), 1.0, atol=1e-15)
+    g1 = O.gate_weights(s, O.topk_select(s.astype(np.float32), np.zeros(16, np.float32), 1), True)
+    assert (g1 == 1.0).all()          # top-1 with renormalisation: constant weight
+    g_off = O.gate_weights(s, idx, False)
+    assert np.array_equal(g_off, np.take_along_axis(s, idx, axis=1))
+
+
+def test_load_matches_bincount_and_sums():
+    rng = np.random.default_rng(2)
+    idx = np.stack([rng.permutation(64)[:2] for _ in range(1000)])
+    load = O.expert_load(idx, 64)
+    assert load.sum() == 2000
+    assert np.array_equal(load, np.bincount(idx.ravel(), minlength=64))
+
+
+# ---------------------------------------------------------------- permutation
+
+def test_permutation_invariants_and_library_sort():
+    rng = np.random.default_rng(4)
+    T, E, k = 500, 16, 2
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+    offsets, perm_tok, inv_pos = O.stable_permutation(idx, E)
+    load = np.bincount(idx.ravel(), minlength=E)
+    assert np.array_equal(offsets, np.concatenate([[0], np.cumsum(load)]))
+    assert sorted(perm_tok.tolist()) == sorted(np.repeat(np.arange(T), k).tolist())
+    assert sorted(inv_pos.ravel().tolist()) == list(range(T * k))        # bijection
+    for t in range(T):
+        for j in range(k):
+            p = inv_pos[t, j]
+            assert perm_tok[p] == t
+            assert offsets[idx[t, j]] <= p < offsets[idx[t, j] + 1]
+    for e in range(E):
+        blk = perm_tok[offsets[e]:offsets[e + 1]]
+        assert (np.diff(blk) > 0).all()                                   # ascending tokens
+    order = np.argsort(idx.ravel(), kind="stable")                        # library stable sort
+    assert np.array_equal(perm_tok, order // k)
+    assert np.array_equal(inv_pos.ravel()[order], np.arange(T * k))
+
+
+# ---------------------------------------------------------------- bias update
+
+def _nearest_f32(q: Fraction) -> np.float32:
+    """Nearest fp32 to an exact rational, found by bracketing (ties to even)."""
+    c = np.float32(float(q))
+    lo, hi = np.nextafter(c, np.float32(-np.inf)), np.nextafter(c, np.float32(np.inf))
+    cands = sorted([lo, c, hi], key=lambda v: (abs(Fraction(float(v)) - q),
+                                               int(np.array(v).view(np.uint32)) & 1))
+    return cands[0]
+
+
+def test_bias_update_bitwise_nearest_and_direction():
+    rng = np.random.default_rng(6)
+    E, T, k = 64, 8192, 2
+    bias = rng.uniform(-0.01, 0.01, E).astype(np.float32)
+    bias[:4] = [0.0, 1.0, -1.0, 0.125]
+    load = rng.integers(0, 600, E)
+    load[4] = T * k // E                            # exactly on target: unchanged
+    new = O.bias_update(bias, load, T * k, 1e-3)
+    g = Fraction(float(np.float32(1e-3)))
+    for e in range(E):
+        target_minus = Fraction(T * k, E) - int(load[e])
+        if target_minus == 0:
+            assert new[e] == bias[e]
+            continue
+        step = g if target_minus > 0 else -g       # under-loaded experts go up
+        want = _nearest_f32(Fraction(float(bias[e])) + step)
+        assert new[e].view(np.uint32) == want.view(np.uint32), e
+
+
+def test_bias_update_balanced_loads_leave_bias_unchanged():
+    bias = np.linspace(-0.01, 0.01, 8).astype(np.float32)
+    new = O.bias_update(bias, np.full(8, 16), 64 * 2, 1e-3)
+    assert np.array_equal(new.view(np.uint32), bias.view(np.uint32))
+
+
+def test_bias_update_replicas_equal_full_batch():
+    s = CONFIGS["tiny"].replace(T=96)
+    rng = np.random.default_rng(9)
+    sc = rng.random((s.T, s.E)).astype(np.float32)
+    bias = np.zeros(s.E, np.float32)
+    idx = O.topk_select(sc, bias, s.k)
+    full = O.bias_update(bias, O.expert_load(idx, s.E), s.T * s.k, 1e-3)
+    for n in (2, 3, 4):
+        shards = np.array_split(np.arange(s.T), n)
+        load = sum(O.expert_load(O.topk_select(sc[sh], bias, s.k), s.E) for sh in shards)
+        assert np.array_equal(O.bias_update(bias, load, s.T * s.k, 1e-3).view(np.uint32),
+                              full.view(np.uint32))
+
+
+# ---------------------------------------------------------------- hand-worked fixture
+
+def test_golden_route_permute_bias(golden_dir):
+    G = json.load(open(os.path.join(golden_dir, "route_permute_bias_worked.json")))
+    s = np.array(G["scores"], np.float32)
+    b = np.array(G["bias"], np.float32)
+    idx = O.topk_select(s, b, G["k"])
+    assert idx.tolist() == G["idx"]
+    g = O.gate_weights(s.astype(np.float64), idx, True)
+    for t in range(G["T"]):
+        for j in range(G["k"]):
+            num, den = G["gate_num_den"][t][j]
+            assert g[t, j] == pytest.approx(num / den, abs=1e-15)
+    load = O.expert_load(idx, G["E"])
+    assert load.tolist() == G["load"]
+    off, perm, inv = O.stable_permutation(idx, G["E"])
+    assert off.tolist() == G["offsets"] and perm.tolist() == G["perm_tok"]
+    assert inv.tolist() == G["inv_pos"]
+    nb = O.bias_update(b, load, G["T"] * G["k"], G["gamma"])
+    for e, sg in enumerate(G["bias_sign"]):
+        assert np.sign(float(nb[e]) - float(b[e])) == sg
+
+
+# ---------------------------------------------------------------- bf16 rounding
+
+def test_round_to_bf16_against_torch_and_ties():
+    rng = np.random.default_rng(1)
+    v = (rng.standard_normal(20000) * 3).astype(np.float32)
+    lib = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(O.round_to_bf16(v.astype(np.float64)), lib)
+    assert O.round_to_bf16(np.array([1 + 2 ** -8]))[0] == 1.0                  # tie -> even
+    assert O.round_to_bf16(np.array([1 + 3 * 2 ** -8]))[0] == 1 + 2 ** -6      # tie -> even
+    assert O.round_to_bf16(np.array([1 + 2 ** -8 + 2 ** -20]))[0] == 1 + 2 ** -7
+
+
+# ---------------------------------------------------------------- expert FFN
+
+def test_swiglu_structured_weights_closed_form():
+    # d = f = 5, W_gate = diag(c), W_up = I, W_down a permutation sigma (rows pick hidden
+    # units).  Then y_i = silu(c_s x_s) * x_s with s = sigma(i): this fixes which matrix
+    # gets the activation and the orientation of each matrix.
+    n = 5
+    c = np.array([0.5, -1.0, 2.0, 0.25, 1.5])
+    sigma = [2, 4, 0, 1, 3]
+    Wg = np.diag(c)
+    Wu = np.eye(n)
+    Wd = np.zeros((n, n))
+    for i in range(n):
+        Wd[i, sigma[i]] = 1.0
+    x = np.array([[0.3, -0.7, 1.1, 2.0, -1.5]])
+    y = O.swiglu_ffn(x, Wg, Wu, Wd, round_hidden=False)
+    for i in range(n):
+        s_ = sigma[i]
+        a = c[s_] * x[0, s_]
+        assert y[0, i] == pytest.approx(a / (1 + math.exp(-a)) * x[0, s_], abs=1e-15)
+    # Swapping gate and up changes the result (the activation is on the gate only).
+    y_sw = O.swiglu_ffn(x, Wu, Wg, Wd, round_hidden=False)
+    assert not np.allclose(y, y_sw)
+
+
+def test_dense_swiglu_matches_torch_library():
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((33, 64))
+    Wg, Wu = rng.standard_normal((2, 48, 64)) * 0.1
+    Wd = rng.standard_normal((64, 48)) * 0.1
+    tx = torch.from_numpy(x)
+    ref = (torch.nn.functional.silu(tx @ torch.from_numpy(Wg).T) * (tx @ torch.from_numpy(Wu).T)) \
+        @ torch.from_numpy(Wd).T
+    assert np.allclose(O.swiglu_ffn(x, Wg, Wu, Wd, round_hidden=False), ref.numpy(), atol=1e-12)
+
+
+def _tiny_layer(**override):
+    s = CONFIGS["tiny"]
+    L = make_layer(s, "tiny")
+    P = dict(x=L["x"].astype(np.float64), w_router=L["w_router"], bias=L["bias"],
+             w_gate=_bf(L["w_gate"]), w_up=_bf(L["w_up"]), w_down=_bf(L["w_down"]),
+             s_gate=_bf(L["s_gate"]), s_up=_bf(L["s_up"]), s_down=_bf(L["s_down"]),
+             k=s.k, x_is_bf16=False)
+    P.update(override)
+    return s, P
+
+
+def test_layer_equals_per_token_dense_mixture():
+    # Independent formulation without any permutation: for each token, run the shared
+    # expert and each selected expert directly and add them with the gates.
+    s, P = _tiny_layer()
+    r = O.layer_forward(**P)
+    xb = O.round_to_bf16(P["x"])
+    for t in range(s.T):
+        want = O.swiglu_ffn(xb[t:t + 1], P["s_gate"], P["s_up"], P["s_down"])[0]
+        for j in range(s.k):
+            e = r["idx"][t, j]
+            want = want + r["gate"][t, j] * O.swiglu_ffn(xb[t:t + 1], P["w_gate"][e], P["w_up"][e],
+                                                        P["w_down"][e])[0]
+        assert np.allclose(r["out"][t], want, rtol=0, atol=1e-14)
+
+
+def test_layer_zero_weights_isolate_the_two_branches():
+    s, P = _tiny_layer()
+    r_full = O.layer_forward(**P)
+    r_no_shared = O.layer_forward(**dict(P, s_down=np.zeros_like(P["s_down"])))
+    r_no_routed = O.layer_forward(**dict(P, w_down=np.zeros_like(P["w_down"])))
+    assert np.allclose(r_no_routed["out"], r_full["shared"], atol=0)
+    routed = r_full["out"] - r_full["shared"]
+    assert np.allclose(r_no_shared["out"], routed, atol=1e-15)
+    # The routed branch is linear in W_down.
+    r2 = O.layer_forward(**dict(P, s_down=np.zeros_like(P["s_down"]), w_down=2 * P["w_down"]))
+    assert np.allclose(r2["out"], 2 * r_no_shared["out"], atol=1e-15)
+
+
+def test_layer_invariants_tiny():
+    s, P = _tiny_layer()
+    r = O.layer_forward(**P)
+    assert r["load"].sum() == s.T * s.k
+    for t in range(s.T):
+        assert len(set(r["idx"][t].tolist())) == s.k
+    assert np.allclose(r["gate"].sum(axis=1), 1.0, atol=1e-12)
+    assert set(np.abs(r["bias"] - P["bias"]).tolist()) <= {0.0, float(np.float32(1e-3))}
+
+
+# ---------------------------------------------------------------- int4 container
+
+def test_int4_exact_codes_and_nibble_order():
+    s = np.float32(0.0625)                       # exactly representable in fp16
+    q = np.array([1, -1, 7, -7, 0, 3, -4, 2] * 4, dtype=np.float32)
+    w = (q * s)[None, :]
+    packed, scale, codes = O.quantize_int4_g32(w)
+    assert scale.view(np.float16)[0, 0] == np.float16(s)
+    assert np.array_equal(codes[0], q.astype(np.int8))
+    assert packed[0, 0] == 0xF1 and packed[0, 1] == 0x97     # (1, -1) and (7, -7)
+    assert np.array_equal(O.dequantize_int4_g32(packed, scale), w.astype(np.float64))
+
+
+def test_int4_roundtrip_error_bound_and_zero_group():
+    rng = np.random.default_rng(7)
+    w = (rng.standard_normal((64, 256)) * 0.02).astype(np.float32)
+    w[3, 32:64] = 0.0
+    packed, scale, codes = O.quantize_int4_g32(w)
+    deq = O.dequantize_int4_g32(packed, scale)
+    sc = np.repeat(O.fp16_value_from_bits(scale), 32, axis=1)
+    # |w - q*s| <= s/2 inside the range, plus the fp16 rounding of the scale at the edge.
+    assert (np.abs(deq - w) <= sc / 2 + np.abs(w) * 2 ** -10 + 1e-12).all()
+    assert (codes[3, 32:64] == 0).all() and O.fp16_value_from_bits(scale)[3, 1] == 0.0
+    assert codes.max() <= 7 and codes.min() >= -7
