@@ -1,0 +1,216 @@
+"""ctypes binding of libmoe_gb300.so: argument marshalling only.
+
+Every function here has the name of a C entry point in include/moe_gb300.h, takes
+torch tensors that already live on the GPU (PyTorch supplies device memory and the
+stream) and passes their pointers through.  All computation happens in the library's
+CUDA kernels; there is no other code path.  If the library has not been built the
+first call raises, it never falls back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmoe_gb300.so")
+
+MOE_X_BF16, MOE_X_F32 = 0, 1
+MOE_W_BF16, MOE_W_INT4_G32 = 0, 1
+
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
+                3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT",
+                6: "MOE_ERR_DEVICE"}
+
+# Every symbol the header declares, with (restype, argtypes).
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_F = ctypes.c_float
+
+
+class MoEShape(ctypes.Structure):
+    _fields_ = [("T", _I32), ("d", _I32), ("E", _I32), ("f", _I32), ("F", _I32), ("k", _I32),
+                ("renorm", _I32), ("x_dtype", _I32), ("w_format", _I32)]
+
+
+class MoEWeights(ctypes.Structure):
+    _fields_ = [("w_gate_up", _P), ("w_down", _P), ("scale_gate_up", _P), ("scale_down", _P),
+                ("shared_gate_up", _P), ("shared_down", _P)]
+
+
+class MoEDebug(ctypes.Structure):
+    _fields_ = [("scores", _P), ("idx", _P), ("gate", _P), ("load", _P), ("offsets", _P),
+                ("perm_tok", _P), ("inv_pos", _P)]
+
+
+_SHAPE_P = ctypes.POINTER(MoEShape)
+SIGNATURES = {
+    "moe_abi_version": (_I32, []),
+    "moe_status_string": (ctypes.c_char_p, [_I32]),
+    "moe_gate_up_block": (_I32, [_I32]),
+    "moe_route": (_I32, [_SHAPE_P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_permute_workspace_size": (_SZ, [_SHAPE_P]),
+    "moe_permute": (_I32, [_SHAPE_P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_expert_ffn_workspace_size": (_SZ, [_SHAPE_P]),
+    "moe_expert_ffn": (_I32, [_SHAPE_P, _P, _P, _P, ctypes.POINTER(MoEWeights), _P, _P, _P, _SZ,
+                              _P]),
+    "moe_combine": (_I32, [_SHAPE_P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_bias_update": (_I32, [_I32, _I64, _P, _F, _P, _P]),
+    "moe_layer_workspace_size": (_SZ, [_SHAPE_P]),
+    "moe_layer_fwd": (_I32, [_SHAPE_P, _P, _P, _P, _P, _F, _I32, ctypes.POINTER(MoEWeights), _P,
+                             _P, ctypes.POINTER(MoEDebug), _P, _SZ, _P]),
+    "moe_pack_gate_up": (_I32, [_I32, _I32, _I32, _P, _P, _P, _P]),
+    "moe_quantize_int4": (_I32, [_I64, _I32, _P, _P, _P, _P]),
+    "moe_device_status": (_I32, [_P, ctypes.POINTER(_I32)]),
+    "moe_profile_stage_count": (_I32, []),
+    "moe_profile_stage_name": (ctypes.c_char_p, [_I32]),
+    "moe_profile_start": (_I32, [_I32]),
+    "moe_profile_stop": (_I32, [ctypes.POINTER(_F), ctypes.POINTER(_I32)]),
+}
+
+_lib = None
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(code, code)}")
+        self.code = code
+
+
+def load_library(path: str = LIB_PATH):
+    """Load the shared library once and declare every entry point's signature."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m aux_loss_free_gb300.build`")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(name: str, code: int):
+    if code != 0:
+        raise MoEError(name, code)
+
+
+def make_shape(T, d, E, f, F, k, renorm=True, x_dtype=MOE_X_BF16, w_format=MOE_W_BF16) -> MoEShape:
+    return MoEShape(T, d, E, f, F, k, int(bool(renorm)), x_dtype, w_format)
+
+
+def make_weights(w_gate_up, w_down, shared_gate_up=None, shared_down=None, scale_gate_up=None,
+                 scale_down=None) -> MoEWeights:
+    return MoEWeights(_ptr(w_gate_up), _ptr(w_down), _ptr(scale_gate_up), _ptr(scale_down),
+                      _ptr(shared_gate_up), _ptr(shared_down))
+
+
+def moe_abi_version() -> int:
+    return load_library().moe_abi_version()
+
+
+def moe_gate_up_block(width: int) -> int:
+    return load_library().moe_gate_up_block(width)
+
+
+def moe_route(shape, x, w_router, logit_offset, bias, scores, idx, gate, load, stream=None):
+    _check("moe_route", load_library().moe_route(
+        ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(logit_offset), _ptr(bias), _ptr(scores),
+        _ptr(idx), _ptr(gate), _ptr(load), _stream(stream)))
+
+
+def moe_permute_workspace_size(shape) -> int:
+    return load_library().moe_permute_workspace_size(ctypes.byref(shape))
+
+
+def moe_permute(shape, idx, offsets, perm_tok, inv_pos, workspace, stream=None):
+    _check("moe_permute", load_library().moe_permute(
+        ctypes.byref(shape), _ptr(idx), _ptr(offsets), _ptr(perm_tok), _ptr(inv_pos),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_expert_ffn_workspace_size(shape) -> int:
+    return load_library().moe_expert_ffn_workspace_size(ctypes.byref(shape))
+
+
+def moe_expert_ffn(shape, x, offsets, perm_tok, weights: MoEWeights, y_perm, shared_out, workspace,
+                   stream=None):
+    _check("moe_expert_ffn", load_library().moe_expert_ffn(
+        ctypes.byref(shape), _ptr(x), _ptr(offsets), _ptr(perm_tok), ctypes.byref(weights),
+        _ptr(y_perm), _ptr(shared_out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_combine(shape, y_perm, shared_out, inv_pos, gate, residual, out, stream=None):
+    _check("moe_combine", load_library().moe_combine(
+        ctypes.byref(shape), _ptr(y_perm), _ptr(shared_out), _ptr(inv_pos), _ptr(gate),
+        _ptr(residual), _ptr(out), _stream(stream)))
+
+
+def moe_bias_update(E, tokens_times_k, load, gamma, bias, stream=None):
+    _check("moe_bias_update", load_library().moe_bias_update(
+        E, tokens_times_k, _ptr(load), gamma, _ptr(bias), _stream(stream)))
+
+
+def moe_layer_workspace_size(shape) -> int:
+    return load_library().moe_layer_workspace_size(ctypes.byref(shape))
+
+
+def moe_layer_fwd(shape, x, w_router, logit_offset, bias, gamma, update_bias, weights: MoEWeights,
+                  residual, out, workspace, debug: MoEDebug | None = None, stream=None):
+    _check("moe_layer_fwd", load_library().moe_layer_fwd(
+        ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(logit_offset), _ptr(bias), gamma,
+        int(update_bias), ctypes.byref(weights), _ptr(residual), _ptr(out),
+        ctypes.byref(debug) if debug is not None else None, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def make_debug(scores=None, idx=None, gate=None, load=None, offsets=None, perm_tok=None,
+               inv_pos=None) -> MoEDebug:
+    return MoEDebug(_ptr(scores), _ptr(idx), _ptr(gate), _ptr(load), _ptr(offsets), _ptr(perm_tok),
+                    _ptr(inv_pos))
+
+
+def moe_pack_gate_up(G, width, d, w_gate, w_up, w_gate_up, stream=None):
+    _check("moe_pack_gate_up", load_library().moe_pack_gate_up(
+        G, width, d, _ptr(w_gate), _ptr(w_up), _ptr(w_gate_up), _stream(stream)))
+
+
+def moe_quantize_int4(rows, K, w, q, scale, stream=None):
+    _check("moe_quantize_int4", load_library().moe_quantize_int4(
+        rows, K, _ptr(w), _ptr(q), _ptr(scale), _stream(stream)))
+
+
+def moe_device_status(stream=None) -> int:
+    out = _I32(0)
+    _check("moe_device_status", load_library().moe_device_status(_stream(stream), ctypes.byref(out)))
+    return out.value
+
+
+def moe_profile_start(max_calls: int):
+    _check("moe_profile_start", load_library().moe_profile_start(max_calls))
+
+
+def moe_profile_stop():
+    """-> ({stage name: summed ms}, recorded calls)."""
+    lib = load_library()
+    n = lib.moe_profile_stage_count()
+    ms = (_F * n)()
+    calls = _I32(0)
+    _check("moe_profile_stop", lib.moe_profile_stop(ms, ctypes.byref(calls)))
+    names = [lib.moe_profile_stage_name(i).decode() for i in range(n)]
+    return dict(zip(names, [float(v) for v in ms])), calls.value

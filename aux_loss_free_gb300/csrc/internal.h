@@ -1,0 +1,100 @@
+// Host-side launcher interface shared by the library's translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace moe {
+
+// Device status bits (OR-ed into the library's status word).
+constexpr int kDevTimeout = 1;
+constexpr int kDevCheck = 2;
+
+constexpr int kMaxE = 256;
+constexpr int kMaxK = 8;
+constexpr int kRouterTokens = 32;   // tokens per router block
+
+// Tokens per permutation chunk: a multiple of kRouterTokens chosen so the chunk
+// count table (chunks x E int32) stays within kMaxCountEntries.
+constexpr int kMaxCountEntries = 32768;
+int permute_chunk_tokens(int T, int E);
+
+// Library status word (device), OR-ed by kernels; owned by moe_api.cu.
+int* device_status_ptr();
+
+// ---------------------------------------------------------------- router
+struct RouterArgs {
+  const void* x;
+  int x_is_f32;
+  const float* w_router;
+  const float* logit_offset;
+  const float* bias;
+  float* scores;        // nullable
+  int32_t* idx;
+  float* gate;
+  int32_t* load;        // zeroed by the caller; atomically accumulated
+  int32_t* counts;      // nullable: [chunks][E], zeroed by the caller
+  int chunk_tokens;
+  int T, d, E, k, renorm;
+};
+cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------- permutation
+cudaError_t launch_count(const int32_t* idx, int T, int k, int E, int chunk_tokens,
+                         int32_t* counts, cudaStream_t s);
+// counts [chunks][E] -> bases [chunks][E] (row of each chunk's first pair of
+// each expert), offsets [E+1], optional load [E] and optional bias update.
+cudaError_t launch_scan(const int32_t* counts, int chunks, int E, int32_t* bases,
+                        int32_t* offsets, int32_t* load_out, float* bias, float gamma,
+                        long long tokens_times_k, cudaStream_t s);
+// Scatter pairs to their rows; optionally gather x rows into xp (bf16) and write
+// a bf16 copy of x (xb, for fp32 x) at the same time.
+cudaError_t launch_scatter(const int32_t* idx, const int32_t* bases, int T, int k, int E,
+                           int chunk_tokens, int32_t* perm_tok, int32_t* inv_pos,
+                           const void* x, int x_is_f32, int d, uint16_t* xp, uint16_t* xb,
+                           cudaStream_t s);
+cudaError_t launch_gather(const void* x, int x_is_f32, const int32_t* perm_tok, long long rows,
+                          int d, uint16_t* xp, cudaStream_t s);
+cudaError_t launch_to_bf16(const float* x, long long n, uint16_t* xb, cudaStream_t s);
+cudaError_t launch_bias_update(int E, long long tokens_times_k, const int32_t* load,
+                               float gamma, float* bias, cudaStream_t s);
+cudaError_t launch_combine(const uint16_t* y_perm, const uint16_t* shared_out,
+                           const int32_t* inv_pos, const float* gate, const uint16_t* residual,
+                           uint16_t* out, int T, int k, int d, cudaStream_t s);
+cudaError_t launch_pack_gate_up(int G, int width, int d, int block, const uint16_t* wg,
+                                const uint16_t* wu, uint16_t* wgu, cudaStream_t s);
+
+// ---------------------------------------------------------------- grouped GEMM
+enum EpiMode { EPI_SWIGLU = 0, EPI_STORE = 1, EPI_COMBINE = 2 };
+
+struct GemmOperandSet {
+  const void* a;        // bf16 [a_rows][K]
+  long long a_rows;
+  const void* b;        // bf16 [groups * N][K]
+  int groups;
+  int N, K;
+  void* out;            // bf16 output
+  int ldo;
+  int mode;             // EpiMode
+  int rows;             // shared set: rows of the single group
+};
+struct CombineInputs {
+  const uint16_t* y_perm;
+  const int32_t* inv_pos;
+  const float* gate;
+  const uint16_t* residual;
+  int k;
+};
+// Runs up to two operand sets in one persistent launch: `routed` (E groups with
+// rows from device `offsets`) and `shared` (one group).  Either may be disabled
+// with a null `a`.
+cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* offsets, int E,
+                                const GemmOperandSet& shared, const CombineInputs& comb,
+                                long long max_routed_rows, cudaStream_t s, int* bad_arg);
+
+// ---------------------------------------------------------------- int4 serving
+cudaError_t launch_quantize_int4(long long rows, int K, const uint16_t* w, uint8_t* q,
+                                 uint16_t* scale, cudaStream_t s);
+
+}  // namespace moe

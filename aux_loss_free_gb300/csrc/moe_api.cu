@@ -1,0 +1,477 @@
+// C ABI of the MoE layer library: argument validation, workspace layout and the
+// launch sequence of each call.  Declarations and their contracts: moe_gb300.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+#include "moe_gb300.h"
+
+namespace moe {
+
+__device__ int g_device_status;
+
+int* device_status_ptr() {
+  // One address per device, looked up with that device current.
+  static int* ptrs[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+int permute_chunk_tokens(int T, int E) {
+  long long ct = kRouterTokens;
+  while (((T + ct - 1) / ct) * (long long)E > kMaxCountEntries) ct *= 2;
+  return (int)ct;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kAlign = 1024;
+
+// Bump layout of a workspace: the same code sizes it (base = null) and carves it.
+struct Carver {
+  uint8_t* base;
+  size_t off = 0;
+  explicit Carver(void* b) : base(static_cast<uint8_t*>(b)) {}
+  void* take(size_t bytes) {
+    off = (off + kAlign - 1) / kAlign * kAlign;
+    void* p = base ? base + off : nullptr;
+    off += bytes;
+    return p;
+  }
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------- stage profiler
+constexpr int kStages = 6;
+const char* const kStageNames[kStages] = {"router", "scan", "scatter_gather", "gemm_gate_up",
+                                          "gemm_down_routed", "gemm_down_shared_combine"};
+struct Profiler {
+  std::mutex mu;
+  bool on = false;
+  int max_calls = 0, calls = 0;
+  std::vector<cudaEvent_t> ev;  // (kStages + 1) per call
+} g_prof;
+
+// Marks the start of `stage` (kStages = end of the call) of the current call.
+void prof_mark(int stage, cudaStream_t s) {
+  std::lock_guard<std::mutex> lock(g_prof.mu);
+  if (!g_prof.on || g_prof.calls >= g_prof.max_calls) return;
+  cudaEventRecord(g_prof.ev[(size_t)g_prof.calls * (kStages + 1) + stage], s);
+  if (stage == kStages) ++g_prof.calls;
+}
+
+moe_status_t check_shape(const moe_shape_t* s) {
+  if (!s) return MOE_ERR_INVALID_ARG;
+  if (s->T < 1 || s->d < 1 || s->E < 1 || s->k < 1 || s->f < 1 || s->F < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (s->renorm != 0 && s->renorm != 1) return MOE_ERR_INVALID_ARG;
+  if (s->x_dtype != MOE_X_BF16 && s->x_dtype != MOE_X_F32) return MOE_ERR_INVALID_ARG;
+  if (s->w_format != MOE_W_BF16 && s->w_format != MOE_W_INT4_G32) return MOE_ERR_INVALID_ARG;
+  if (s->T > (1 << 24) || s->d % 64 || s->d < 64 || s->d > 8192) return MOE_ERR_UNSUPPORTED;
+  if (s->E > kMaxE || s->k > kMaxK || s->k > s->E) return MOE_ERR_UNSUPPORTED;
+  if (s->f % 32 || s->f > 8192 || s->F % 32 || s->F > 16384) return MOE_ERR_UNSUPPORTED;
+  if (s->w_format == MOE_W_INT4_G32 && (s->k != 1 || s->T > 256)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+int chunks_of(const moe_shape_t* s, int* chunk_tokens) {
+  *chunk_tokens = permute_chunk_tokens(s->T, s->E);
+  return (s->T + *chunk_tokens - 1) / *chunk_tokens;
+}
+
+struct PermuteWs {
+  int32_t* counts;
+  int32_t* bases;
+};
+PermuteWs carve_permute(Carver& c, const moe_shape_t* s) {
+  int ct;
+  const int chunks = chunks_of(s, &ct);
+  PermuteWs w;
+  w.counts = static_cast<int32_t*>(c.take(sizeof(int32_t) * chunks * s->E));
+  w.bases = static_cast<int32_t*>(c.take(sizeof(int32_t) * chunks * s->E));
+  return w;
+}
+
+struct FfnWs {
+  uint16_t* xp;  // [T*k][d] gathered rows
+  uint16_t* h;   // [T*k][f]
+  uint16_t* hs;  // [T][F]
+  uint16_t* xb;  // [T][d] bf16 copy of fp32 x
+};
+FfnWs carve_ffn(Carver& c, const moe_shape_t* s) {
+  const size_t Tk = (size_t)s->T * s->k;
+  FfnWs w;
+  w.xp = static_cast<uint16_t*>(c.take(2 * Tk * s->d));
+  w.h = static_cast<uint16_t*>(c.take(2 * Tk * s->f));
+  w.hs = s->F ? static_cast<uint16_t*>(c.take(2 * (size_t)s->T * s->F)) : nullptr;
+  w.xb = s->x_dtype == MOE_X_F32 ? static_cast<uint16_t*>(c.take(2 * (size_t)s->T * s->d)) : nullptr;
+  return w;
+}
+
+struct LayerWs {
+  int32_t* idx;
+  float* gate;
+  int32_t* load;
+  int32_t* offsets;
+  int32_t* perm_tok;
+  int32_t* inv_pos;
+  uint16_t* y;
+  PermuteWs perm;
+  FfnWs ffn;
+};
+LayerWs carve_layer(Carver& c, const moe_shape_t* s) {
+  const size_t Tk = (size_t)s->T * s->k;
+  LayerWs w;
+  w.idx = static_cast<int32_t*>(c.take(4 * Tk));
+  w.gate = static_cast<float*>(c.take(4 * Tk));
+  w.load = static_cast<int32_t*>(c.take(4 * (size_t)s->E));
+  w.offsets = static_cast<int32_t*>(c.take(4 * (size_t)(s->E + 1)));
+  w.perm_tok = static_cast<int32_t*>(c.take(4 * Tk));
+  w.inv_pos = static_cast<int32_t*>(c.take(4 * Tk));
+  w.y = static_cast<uint16_t*>(c.take(2 * Tk * s->d));
+  w.perm = carve_permute(c, s);
+  w.ffn = carve_ffn(c, s);
+  return w;
+}
+
+// The two grouped-GEMM launches of the bf16 expert FFN.  Gate/up for routed rows
+// (xp -> h) and the shared expert (x -> hs); then the down projections.  With
+// `comb` set and F > 0, the shared down projection's epilogue adds the gated routed
+// rows and the residual and writes `out` directly.
+moe_status_t run_ffn(const moe_shape_t* s, const void* x_bf16, const int32_t* offsets,
+                     const moe_weights_t* w, const FfnWs& ws, uint16_t* y_perm,
+                     uint16_t* shared_out, const CombineInputs* comb, uint16_t* out,
+                     cudaStream_t st, bool mark = false) {
+  const long long Tk = (long long)s->T * s->k;
+  int bad = 0;
+  GemmOperandSet r1{ws.xp, Tk, w->w_gate_up, s->E, 2 * s->f, s->d, ws.h, s->f, EPI_SWIGLU, 0};
+  GemmOperandSet s1{};
+  if (s->F) s1 = GemmOperandSet{x_bf16, s->T, w->shared_gate_up, 1, 2 * s->F, s->d, ws.hs, s->F,
+                                EPI_SWIGLU, s->T};
+  CombineInputs none{};
+  cudaError_t e = launch_grouped_gemm(r1, offsets, s->E, s1, none, Tk, st, &bad);
+  if (bad) return MOE_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  GemmOperandSet r2{ws.h, Tk, w->w_down, s->E, s->d, s->f, y_perm, s->d, EPI_STORE, 0};
+  GemmOperandSet s2{};
+  if (s->F) {
+    if (comb) s2 = GemmOperandSet{ws.hs, s->T, w->shared_down, 1, s->d, s->F, out, s->d, EPI_COMBINE, s->T};
+    else s2 = GemmOperandSet{ws.hs, s->T, w->shared_down, 1, s->d, s->F, shared_out, s->d, EPI_STORE, s->T};
+  }
+  if (mark) prof_mark(4, st);
+  if (comb && s->F) {
+    // The combine epilogue reads y_perm, so the routed down projection runs first.
+    GemmOperandSet off{};
+    e = launch_grouped_gemm(r2, offsets, s->E, off, none, Tk, st, &bad);
+    if (bad) return MOE_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (mark) prof_mark(5, st);
+    e = launch_grouped_gemm(off, offsets, s->E, s2, *comb, Tk, st, &bad);
+  } else {
+    e = launch_grouped_gemm(r2, offsets, s->E, s2, none, Tk, st, &bad);
+  }
+  if (bad) return MOE_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (comb && !s->F) {
+    if (mark) prof_mark(5, st);
+    e = launch_combine(y_perm, nullptr, comb->inv_pos, comb->gate, comb->residual, out, s->T,
+                       s->k, s->d, st);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+bool weights_ok(const moe_shape_t* s, const moe_weights_t* w) {
+  if (!w || !w->w_gate_up || !w->w_down) return false;
+  if (!aligned16(w->w_gate_up) || !aligned16(w->w_down)) return false;
+  if (s->w_format == MOE_W_INT4_G32) {
+    if (!w->scale_gate_up || !w->scale_down) return false;
+  }
+  if (s->F) {
+    if (!w->shared_gate_up || !w->shared_down) return false;
+    if (!aligned16(w->shared_gate_up) || !aligned16(w->shared_down)) return false;
+  }
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return 1; }
+
+const char* moe_status_string(moe_status_t st) {
+  switch (st) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported size";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_DEVICE: return "device check failed";
+  }
+  return "unknown status";
+}
+
+int32_t moe_gate_up_block(int32_t width) {
+  return width % 128 == 0 ? 128 : (width % 64 == 0 ? 64 : 32);
+}
+
+moe_status_t moe_route(const moe_shape_t* shape, const void* x, const float* w_router,
+                       const float* logit_offset, const float* bias, float* scores, int32_t* idx,
+                       float* gate, int32_t* load, void* stream) {
+  moe_status_t st = check_shape(shape);
+  if (st) return st;
+  if (!x || !w_router || !bias || !idx || !gate || !load) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(load, 0, sizeof(int32_t) * shape->E, s) != cudaSuccess) return MOE_ERR_CUDA;
+  RouterArgs a{x, shape->x_dtype == MOE_X_F32, w_router, logit_offset, bias, scores, idx, gate,
+               load, nullptr, kRouterTokens, shape->T, shape->d, shape->E, shape->k, shape->renorm};
+  return cuda_status(launch_router(a, s));
+}
+
+size_t moe_permute_workspace_size(const moe_shape_t* shape) {
+  if (check_shape(shape)) return 0;
+  Carver c(nullptr);
+  carve_permute(c, shape);
+  return c.off;
+}
+
+moe_status_t moe_permute(const moe_shape_t* shape, const int32_t* idx, int32_t* offsets,
+                         int32_t* perm_tok, int32_t* inv_pos, void* workspace, size_t ws_bytes,
+                         void* stream) {
+  moe_status_t st = check_shape(shape);
+  if (st) return st;
+  if (!idx || !offsets || !perm_tok || !inv_pos || !workspace) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_permute_workspace_size(shape)) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Carver c(workspace);
+  PermuteWs w = carve_permute(c, shape);
+  int ct;
+  const int chunks = chunks_of(shape, &ct);
+  if (cudaMemsetAsync(w.counts, 0, sizeof(int32_t) * chunks * shape->E, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  cudaError_t e = launch_count(idx, shape->T, shape->k, shape->E, ct, w.counts, s);
+  if (e == cudaSuccess)
+    e = launch_scan(w.counts, chunks, shape->E, w.bases, offsets, nullptr, nullptr, 0.f, 0, s);
+  if (e == cudaSuccess)
+    e = launch_scatter(idx, w.bases, shape->T, shape->k, shape->E, ct, perm_tok, inv_pos,
+                       nullptr, 0, shape->d, nullptr, nullptr, s);
+  return cuda_status(e);
+}
+
+size_t moe_expert_ffn_workspace_size(const moe_shape_t* shape) {
+  if (check_shape(shape)) return 0;
+  Carver c(nullptr);
+  carve_ffn(c, shape);
+  return c.off;
+}
+
+moe_status_t moe_expert_ffn(const moe_shape_t* shape, const void* x, const int32_t* offsets,
+                            const int32_t* perm_tok, const moe_weights_t* w, void* y_perm,
+                            void* shared_out, void* workspace, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_shape(shape);
+  if (st) return st;
+  if (shape->w_format != MOE_W_BF16) return MOE_ERR_UNSUPPORTED;
+  if (!x || !offsets || !perm_tok || !y_perm || !workspace || !weights_ok(shape, w))
+    return MOE_ERR_INVALID_ARG;
+  if ((shape->F != 0) != (shared_out != nullptr)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y_perm) || (shared_out && !aligned16(shared_out)))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_expert_ffn_workspace_size(shape)) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Carver c(workspace);
+  FfnWs ws = carve_ffn(c, shape);
+  const long long Tk = (long long)shape->T * shape->k;
+  const int xf = shape->x_dtype == MOE_X_F32;
+  cudaError_t e = launch_gather(x, xf, perm_tok, Tk, shape->d, ws.xp, s);
+  if (e == cudaSuccess && xf && shape->F)
+    e = launch_to_bf16(static_cast<const float*>(x), (long long)shape->T * shape->d, ws.xb, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  const void* xbf = xf ? ws.xb : x;
+  return run_ffn(shape, xbf, offsets, w, ws, static_cast<uint16_t*>(y_perm),
+                 static_cast<uint16_t*>(shared_out), nullptr, nullptr, s);
+}
+
+moe_status_t moe_combine(const moe_shape_t* shape, const void* y_perm, const void* shared_out,
+                         const int32_t* inv_pos, const float* gate, const void* residual, void* out,
+                         void* stream) {
+  moe_status_t st = check_shape(shape);
+  if (st) return st;
+  if (!y_perm || !inv_pos || !gate || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(out) || (shared_out && !aligned16(shared_out)) ||
+      (residual && !aligned16(residual)))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(static_cast<const uint16_t*>(y_perm),
+                                    static_cast<const uint16_t*>(shared_out), inv_pos, gate,
+                                    static_cast<const uint16_t*>(residual),
+                                    static_cast<uint16_t*>(out), shape->T, shape->k, shape->d,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_bias_update(int32_t E, int64_t tokens_times_k, const int32_t* load, float gamma,
+                             float* bias, void* stream) {
+  if (E < 1 || E > kMaxE || tokens_times_k < 0 || !load || !bias) return MOE_ERR_INVALID_ARG;
+  return cuda_status(
+      launch_bias_update(E, tokens_times_k, load, gamma, bias, static_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_layer_workspace_size(const moe_shape_t* shape) {
+  if (check_shape(shape)) return 0;
+  Carver c(nullptr);
+  carve_layer(c, shape);
+  return c.off;
+}
+
+moe_status_t moe_layer_fwd(const moe_shape_t* shape, const void* x, const float* w_router,
+                           const float* logit_offset, float* bias, float gamma,
+                           int32_t update_bias, const moe_weights_t* w, const void* residual,
+                           void* out, const moe_debug_t* dbg, void* workspace, size_t ws_bytes,
+                           void* stream) {
+  moe_status_t st = check_shape(shape);
+  if (st) return st;
+  if (shape->w_format != MOE_W_BF16) return MOE_ERR_UNSUPPORTED;
+  if (!x || !w_router || !bias || !out || !workspace || !weights_ok(shape, w))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(out) ||
+      (residual && !aligned16(residual)))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_layer_workspace_size(shape)) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Carver c(workspace);
+  LayerWs L = carve_layer(c, shape);
+  if (dbg) {
+    if (dbg->idx) L.idx = dbg->idx;
+    if (dbg->gate) L.gate = dbg->gate;
+    if (dbg->load) L.load = dbg->load;
+    if (dbg->offsets) L.offsets = dbg->offsets;
+    if (dbg->perm_tok) L.perm_tok = dbg->perm_tok;
+    if (dbg->inv_pos) L.inv_pos = dbg->inv_pos;
+  }
+  const int T = shape->T, E = shape->E, k = shape->k;
+  int ct;
+  const int chunks = chunks_of(shape, &ct);
+  const int xf = shape->x_dtype == MOE_X_F32;
+
+  prof_mark(0, s);
+  if (cudaMemsetAsync(L.load, 0, sizeof(int32_t) * E, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(L.perm.counts, 0, sizeof(int32_t) * chunks * E, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  RouterArgs ra{x, xf, w_router, logit_offset, bias, dbg ? dbg->scores : nullptr, L.idx, L.gate,
+                L.load, L.perm.counts, ct, T, shape->d, E, k, shape->renorm};
+  cudaError_t e = launch_router(ra, s);
+  prof_mark(1, s);
+  if (e == cudaSuccess)
+    e = launch_scan(L.perm.counts, chunks, E, L.perm.bases, L.offsets, nullptr,
+                    update_bias ? bias : nullptr, gamma, (long long)T * k, s);
+  prof_mark(2, s);
+  if (e == cudaSuccess)
+    e = launch_scatter(L.idx, L.perm.bases, T, k, E, ct, L.perm_tok, L.inv_pos, x, xf, shape->d,
+                       L.ffn.xp, (xf && shape->F) ? L.ffn.xb : nullptr, s);
+  prof_mark(3, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  const void* xbf = xf ? L.ffn.xb : x;
+  CombineInputs comb{L.y, L.inv_pos, L.gate, static_cast<const uint16_t*>(residual), k};
+  const moe_status_t st2 = run_ffn(shape, xbf, L.offsets, w, L.ffn, L.y, nullptr, &comb,
+                                   static_cast<uint16_t*>(out), s, true);
+  prof_mark(kStages, s);
+  return st2;
+}
+
+moe_status_t moe_pack_gate_up(int32_t G, int32_t width, int32_t d, const void* w_gate,
+                              const void* w_up, void* w_gate_up, void* stream) {
+  if (G < 1 || width < 32 || width % 32 || d < 8 || d % 8 || !w_gate || !w_up || !w_gate_up)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_gate_up)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_pack_gate_up(G, width, d, moe_gate_up_block(width),
+                                         static_cast<const uint16_t*>(w_gate),
+                                         static_cast<const uint16_t*>(w_up),
+                                         static_cast<uint16_t*>(w_gate_up),
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_quantize_int4(int64_t rows, int32_t K, const void* w, void* q, void* scale,
+                               void* stream) {
+  if (rows < 1 || K < 32 || K % 32 || !w || !q || !scale) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_quantize_int4(rows, K, static_cast<const uint16_t*>(w),
+                                          static_cast<uint8_t*>(q), static_cast<uint16_t*>(scale),
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+int32_t moe_profile_stage_count(void) { return kStages; }
+
+const char* moe_profile_stage_name(int32_t stage) {
+  return (stage >= 0 && stage < kStages) ? kStageNames[stage] : "";
+}
+
+moe_status_t moe_profile_start(int32_t max_calls) {
+  if (max_calls < 1 || max_calls > (1 << 20)) return MOE_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_prof.mu);
+  for (cudaEvent_t ev : g_prof.ev) cudaEventDestroy(ev);
+  g_prof.ev.assign((size_t)max_calls * (kStages + 1), nullptr);
+  for (auto& ev : g_prof.ev)
+    if (cudaEventCreate(&ev) != cudaSuccess) return MOE_ERR_CUDA;
+  g_prof.max_calls = max_calls;
+  g_prof.calls = 0;
+  g_prof.on = true;
+  return MOE_OK;
+}
+
+moe_status_t moe_profile_stop(float* ms_per_stage, int32_t* calls) {
+  if (!ms_per_stage || !calls) return MOE_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_prof.mu);
+  g_prof.on = false;
+  for (int i = 0; i < kStages; ++i) ms_per_stage[i] = 0.f;
+  *calls = g_prof.calls;
+  for (int c = 0; c < g_prof.calls; ++c) {
+    cudaEvent_t* ev = &g_prof.ev[(size_t)c * (kStages + 1)];
+    if (cudaEventSynchronize(ev[kStages]) != cudaSuccess) return MOE_ERR_CUDA;
+    // Stages a call did not reach keep their previous mark: walk forward from it.
+    int last = 0;
+    for (int i = 1; i <= kStages; ++i) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, ev[last], ev[i]) != cudaSuccess) continue;
+      ms_per_stage[i - 1] += ms;
+      last = i;
+    }
+  }
+  return MOE_OK;
+}
+
+moe_status_t moe_device_status(void* stream, int32_t* device_status) {
+  if (!device_status) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  int* p = device_status_ptr();
+  if (!p) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return MOE_ERR_CUDA;
+  *device_status = (v & kDevTimeout) ? MOE_ERR_TIMEOUT : ((v & kDevCheck) ? MOE_ERR_DEVICE : MOE_OK);
+  return MOE_OK;
+}
+
+}  // extern "C"

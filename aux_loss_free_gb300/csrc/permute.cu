@@ -1,0 +1,320 @@
+// Token permutation (stable counting sort by expert), row gather, combine, bias
+// update and weight packing.
+//
+// Counting sort in three launches: per-chunk expert counts (the router produces
+// them on the fused path), one block that scans the chunk table into per-chunk
+// bases and the expert offsets, and a scatter in which each chunk's pairs are ranked
+// in (token, slot) order with a warp match, which keeps tokens ascending inside
+// every expert's block.  The scatter also gathers the token rows (16-byte vectors)
+// into the permuted activation buffer the grouped GEMM reads.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr unsigned FULL = 0xFFFFFFFFu;
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Copy one token row (d elements) to a bf16 destination row with one warp.
+__device__ __forceinline__ void copy_row_bf16(const void* x, int x_is_f32, long long src_row, int d,
+                                              uint16_t* dst, int lane) {
+  const int nvec = d / 8;  // 8 bf16 = 16 bytes per vector
+  uint4* out = reinterpret_cast<uint4*>(dst);
+  if (x_is_f32) {
+    const float4* in = reinterpret_cast<const float4*>(static_cast<const float*>(x) + src_row * d);
+    for (int v = lane; v < nvec; v += 32) {
+      const float4 a = in[2 * v], b = in[2 * v + 1];
+      out[v] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                          pack_bf16x2(b.z, b.w));
+    }
+  } else {
+    const uint4* in = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + src_row * d);
+    for (int v = lane; v < nvec; v += 32) out[v] = in[v];
+  }
+}
+
+__global__ void count_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int chunk_tokens,
+                             int32_t* __restrict__ counts) {
+  const long long p = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (p >= (long long)T * k) return;
+  const int t = (int)(p / k);
+  atomicAdd(&counts[(long long)(t / chunk_tokens) * E + idx[p]], 1);
+}
+
+// One block.  counts [chunks][E] -> bases [chunks][E] = offsets[e] + sum of the
+// counts of e in earlier chunks.
+__global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ counts, int chunks,
+                                                    int E, int32_t* __restrict__ bases,
+                                                    int32_t* __restrict__ offsets,
+                                                    int32_t* __restrict__ load_out, float* bias,
+                                                    float gamma, long long tokens_times_k) {
+  extern __shared__ int32_t sm[];
+  int32_t* c = sm;                        // [chunks][E]
+  int32_t* segsum = c + chunks * E;       // [nseg][E]
+  __shared__ int32_t total[kMaxE];
+  __shared__ int32_t off[kMaxE + 1];
+  const int tid = threadIdx.x;
+  for (int i = tid; i < chunks * E; i += blockDim.x) c[i] = counts[i];
+  const int nseg = blockDim.x / E;
+  const int L = (chunks + nseg - 1) / nseg;
+  __syncthreads();
+  const int e = tid % E, sg = tid / E;
+  if (sg < nseg) {
+    int sum = 0;
+    const int lo = sg * L, hi = min(chunks, lo + L);
+    for (int ch = lo; ch < hi; ++ch) sum += c[ch * E + e];
+    segsum[sg * E + e] = sum;
+  }
+  __syncthreads();
+  if (tid < E) {
+    int run = 0;
+    for (int s = 0; s < nseg; ++s) {
+      const int v = segsum[s * E + tid];
+      segsum[s * E + tid] = run;
+      run += v;
+    }
+    total[tid] = run;
+  }
+  __syncthreads();
+  if (tid < 32) {  // exclusive scan of total over experts, 32 at a time
+    int carry = 0;
+    for (int b = 0; b < E; b += 32) {
+      const int v = (b + tid < E) ? total[b + tid] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(FULL, incl, o);
+        if (tid >= o) incl += n;
+      }
+      if (b + tid < E) off[b + tid] = carry + incl - v;
+      carry += __shfl_sync(FULL, incl, 31);
+    }
+    if (tid == 0) off[E] = carry;
+  }
+  __syncthreads();
+  if (sg < nseg) {
+    int run = off[e] + segsum[sg * E + e];
+    const int lo = sg * L, hi = min(chunks, lo + L);
+    for (int ch = lo; ch < hi; ++ch) {
+      bases[ch * E + e] = run;
+      run += c[ch * E + e];
+    }
+  }
+  for (int i = tid; i <= E; i += blockDim.x) offsets[i] = off[i];
+  if (tid < E) {
+    if (load_out) load_out[tid] = total[tid];
+    if (bias) {
+      // Aux-loss-free update: sign(T*k - E*load) is sign(target - load), sign(0) = 0.
+      const long long diff = tokens_times_k - (long long)E * total[tid];
+      const float step = diff > 0 ? gamma : (diff < 0 ? -gamma : 0.f);
+      bias[tid] = __fadd_rn(bias[tid], step);
+    }
+  }
+}
+
+constexpr int SC_THREADS = 256;
+constexpr int SC_ROUND = 256;  // pairs ranked per round (8 warp batches)
+
+__global__ void __launch_bounds__(SC_THREADS) scatter_kernel(
+    const int32_t* __restrict__ idx, const int32_t* __restrict__ bases, int T, int k, int E,
+    int chunk_tokens, int32_t* __restrict__ perm_tok, int32_t* __restrict__ inv_pos,
+    const void* __restrict__ x, int x_is_f32, int d, uint16_t* __restrict__ xp,
+    uint16_t* __restrict__ xb) {
+  __shared__ int32_t run[kMaxE];
+  __shared__ int32_t s_pos[SC_ROUND];
+  __shared__ int32_t s_tok[SC_ROUND];
+  const int chunk = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const long long p_begin = (long long)chunk * chunk_tokens * k;
+  const long long p_end = min((long long)T * k, p_begin + (long long)chunk_tokens * k);
+  for (int e = tid; e < E; e += SC_THREADS) run[e] = bases[(long long)chunk * E + e];
+  __syncthreads();
+  for (long long r0 = p_begin; r0 < p_end; r0 += SC_ROUND) {
+    const int n = (int)min((long long)SC_ROUND, p_end - r0);
+    if (warp == 0) {
+      for (int b = 0; b < n; b += 32) {
+        const int q = b + lane;
+        const bool valid = q < n;
+        const int e = valid ? idx[r0 + q] : -1;
+        const unsigned peers = __match_any_sync(FULL, e);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        int pos = 0;
+        if (valid) {
+          pos = run[e] + rank;
+          const long long pr = r0 + q;
+          const int t = (int)(pr / k);
+          perm_tok[pos] = t;
+          inv_pos[pr] = pos;
+          s_pos[q] = pos;
+          s_tok[q] = (pr % k == 0) ? t : -1 - t;  // slot 0 marks the token's first pair
+        }
+        __syncwarp();
+        if (valid && lane == __ffs(peers) - 1) run[e] += __popc(peers);
+        __syncwarp();
+      }
+    }
+    __syncthreads();
+    if (xp) {
+      for (int q = warp; q < n; q += SC_THREADS / 32) {
+        const int st = s_tok[q];
+        const int t = st >= 0 ? st : -1 - st;
+        copy_row_bf16(x, x_is_f32, t, d, xp + (long long)s_pos[q] * d, lane);
+        if (xb && st >= 0) copy_row_bf16(x, x_is_f32, t, d, xb + (long long)t * d, lane);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+__global__ void gather_kernel(const void* __restrict__ x, int x_is_f32,
+                              const int32_t* __restrict__ perm_tok, long long rows, int d,
+                              uint16_t* __restrict__ xp) {
+  const long long r = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  if (r >= rows) return;
+  copy_row_bf16(x, x_is_f32, perm_tok[r], d, xp + r * d, threadIdx.x % 32);
+}
+
+__global__ void to_bf16_kernel(const float* __restrict__ x, long long n8, uint16_t* __restrict__ xb) {
+  const long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (v >= n8) return;
+  const float4 a = reinterpret_cast<const float4*>(x)[2 * v];
+  const float4 b = reinterpret_cast<const float4*>(x)[2 * v + 1];
+  reinterpret_cast<uint4*>(xb)[v] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w),
+                                               pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+}
+
+__global__ void bias_update_kernel(int E, long long tokens_times_k, const int32_t* __restrict__ load,
+                                   float gamma, float* bias) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  const long long diff = tokens_times_k - (long long)E * load[e];
+  const float step = diff > 0 ? gamma : (diff < 0 ? -gamma : 0.f);
+  bias[e] = __fadd_rn(bias[e], step);
+}
+
+// out[t] = residual[t] + shared[t] + sum_j gate[t][j] * y[inv_pos[t][j]]; one thread per
+// 8 output columns, fp32 sum, one rounding to bf16.
+__global__ void combine_kernel(const uint16_t* __restrict__ y, const uint16_t* __restrict__ shared,
+                               const int32_t* __restrict__ inv_pos, const float* __restrict__ gate,
+                               const uint16_t* __restrict__ residual, uint16_t* __restrict__ out,
+                               int T, int k, int d) {
+  const int vpr = d / 8;
+  const long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (v >= (long long)T * vpr) return;
+  const long long t = v / vpr;
+  const int c = (int)(v % vpr);
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  auto add_row = [&](const uint16_t* row, float w) {
+    const uint4 u = reinterpret_cast<const uint4*>(row)[c];
+    const uint32_t ws[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] = fmaf(w, bf16_lo(ws[i]), acc[2 * i]);
+      acc[2 * i + 1] = fmaf(w, bf16_hi(ws[i]), acc[2 * i + 1]);
+    }
+  };
+  if (residual) add_row(residual + t * d, 1.f);
+  if (shared) add_row(shared + t * d, 1.f);
+  for (int j = 0; j < k; ++j) add_row(y + (long long)inv_pos[t * k + j] * d, gate[t * k + j]);
+  reinterpret_cast<uint4*>(out + t * d)[c] =
+      make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                 pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+}
+
+__global__ void pack_gate_up_kernel(int width, int d, int block, const uint16_t* __restrict__ wg,
+                                    const uint16_t* __restrict__ wu, uint16_t* __restrict__ wgu,
+                                    long long total_rows) {
+  const long long r = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  if (r >= total_rows) return;
+  const long long g = r / (2 * width);
+  const int rr = (int)(r % (2 * width));
+  const int blk = rr / (2 * block), within = rr % (2 * block);
+  const bool is_up = within >= block;
+  const long long src_row = g * width + (long long)blk * block + (is_up ? within - block : within);
+  const uint4* src = reinterpret_cast<const uint4*>((is_up ? wu : wg) + src_row * d);
+  uint4* dst = reinterpret_cast<uint4*>(wgu + r * d);
+  for (int v = threadIdx.x % 32; v < d / 8; v += 32) dst[v] = src[v];
+}
+
+}  // namespace
+
+cudaError_t launch_count(const int32_t* idx, int T, int k, int E, int chunk_tokens,
+                         int32_t* counts, cudaStream_t s) {
+  const long long n = (long long)T * k;
+  count_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(idx, T, k, E, chunk_tokens, counts);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scan(const int32_t* counts, int chunks, int E, int32_t* bases,
+                        int32_t* offsets, int32_t* load_out, float* bias, float gamma,
+                        long long tokens_times_k, cudaStream_t s) {
+  const int threads = 1024;
+  const int nseg = threads / E;
+  const size_t dyn = sizeof(int32_t) * ((size_t)chunks * E + (size_t)nseg * E);
+  cudaError_t e =
+      cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  if (e != cudaSuccess) return e;
+  scan_kernel<<<1, threads, dyn, s>>>(counts, chunks, E, bases, offsets, load_out, bias, gamma,
+                                      tokens_times_k);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(const int32_t* idx, const int32_t* bases, int T, int k, int E,
+                           int chunk_tokens, int32_t* perm_tok, int32_t* inv_pos,
+                           const void* x, int x_is_f32, int d, uint16_t* xp, uint16_t* xb,
+                           cudaStream_t s) {
+  const int chunks = (T + chunk_tokens - 1) / chunk_tokens;
+  scatter_kernel<<<chunks, SC_THREADS, 0, s>>>(idx, bases, T, k, E, chunk_tokens, perm_tok,
+                                               inv_pos, x, x_is_f32, d, xp, xb);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const void* x, int x_is_f32, const int32_t* perm_tok, long long rows,
+                          int d, uint16_t* xp, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  gather_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(x, x_is_f32, perm_tok, rows, d, xp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_to_bf16(const float* x, long long n, uint16_t* xb, cudaStream_t s) {
+  const long long n8 = n / 8;
+  if (n8 == 0) return cudaSuccess;
+  to_bf16_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, s>>>(x, n8, xb);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bias_update(int E, long long tokens_times_k, const int32_t* load, float gamma,
+                               float* bias, cudaStream_t s) {
+  bias_update_kernel<<<(E + 255) / 256, 256, 0, s>>>(E, tokens_times_k, load, gamma, bias);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const uint16_t* y_perm, const uint16_t* shared_out,
+                           const int32_t* inv_pos, const float* gate, const uint16_t* residual,
+                           uint16_t* out, int T, int k, int d, cudaStream_t s) {
+  const long long n = (long long)T * (d / 8);
+  combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(y_perm, shared_out, inv_pos, gate,
+                                                               residual, out, T, k, d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_gate_up(int G, int width, int d, int block, const uint16_t* wg,
+                                const uint16_t* wu, uint16_t* wgu, cudaStream_t s) {
+  const long long rows = (long long)G * 2 * width;
+  pack_gate_up_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(width, d, block, wg, wu, wgu,
+                                                                    rows);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,214 @@
+// Router: fp32 logits, sigmoid scores, biased top-k selection, gates and loads.
+//
+// Relay article ("Una carrera de relevos con GPUs alquiladas entrenó el MoE de 2.7B de
+// NanoColibri por $200"), opening section, architecture paragraph: sigmoid-plus-bias
+// router with top-2 routing; section "Entrenamiento por relevos", top-2 paragraph:
+// gates are the winners' scores renormalised over the k winners.
+//
+// One block handles 32 tokens.  Phase 1 is an fp32 tile product (32 tokens x 64
+// experts per pass, each thread a 4 x 4 register tile) with x and W_r staged in shared
+// memory; phase 2 gives each warp whole tokens: every lane holds E/32 experts'
+// scores in registers, the top-k is k rounds of a warp-shuffle arg-max under the
+// order (key descending, expert index ascending), and the gate normalisation is a
+// register sum.  Per-block expert counts go to shared memory, then one atomic per
+// expert to the global load (and to the permutation's chunk table when asked).
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int RT = kRouterTokens;  // tokens per block
+constexpr int KC = 64;             // K chunk staged in shared memory
+constexpr int EB = 64;             // experts per pass
+constexpr int NTHR = 128;
+constexpr int XS_LD = RT + 4;
+constexpr int WS_LD = EB + 4;
+constexpr int MAXC = kMaxE / 32;   // experts per lane in the selection phase
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+template <bool XF32>
+__global__ void __launch_bounds__(NTHR) router_kernel(RouterArgs a) {
+  __shared__ __align__(16) float xs[KC][XS_LD];
+  __shared__ __align__(16) float ws[KC][WS_LD];
+  __shared__ int hist[kMaxE];
+  extern __shared__ float logits[];  // [RT][E + 1]
+
+  const int tid = threadIdx.x;
+  const int t0 = blockIdx.x * RT;
+  const int E = a.E, d = a.d, LD = a.E + 1;
+  for (int e = tid; e < E; e += NTHR) hist[e] = 0;
+
+  const int tx = tid % 16, ty = tid / 16;
+  for (int e0 = 0; e0 < E; e0 += EB) {
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+
+    for (int k0 = 0; k0 < d; k0 += KC) {
+      __syncthreads();
+#pragma unroll
+      for (int pass = 0; pass < RT * KC / 4 / NTHR; ++pass) {
+        const int li = pass * NTHR + tid;
+        const int tok = li / 16, kq = (li % 16) * 4;
+        const int t = t0 + tok;
+        float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
+        if (t < a.T) {
+          if (XF32) {
+            const float4 f =
+                *reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + (size_t)t * d + k0 + kq);
+            v0 = f.x; v1 = f.y; v2 = f.z; v3 = f.w;
+          } else {
+            const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.x) +
+                                                            (size_t)t * d + k0 + kq);
+            v0 = bf16_bits_to_f32(u.x & 0xFFFFu); v1 = bf16_bits_to_f32(u.x >> 16);
+            v2 = bf16_bits_to_f32(u.y & 0xFFFFu); v3 = bf16_bits_to_f32(u.y >> 16);
+          }
+        }
+        xs[kq + 0][tok] = v0; xs[kq + 1][tok] = v1; xs[kq + 2][tok] = v2; xs[kq + 3][tok] = v3;
+      }
+#pragma unroll
+      for (int pass = 0; pass < EB * KC / 4 / NTHR; ++pass) {
+        const int li = pass * NTHR + tid;
+        const int el = li / 16, kq = (li % 16) * 4;
+        const int e = e0 + el;
+        float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (e < E) f = *reinterpret_cast<const float4*>(a.w_router + (size_t)e * d + k0 + kq);
+        ws[kq + 0][el] = f.x; ws[kq + 1][el] = f.y; ws[kq + 2][el] = f.z; ws[kq + 3][el] = f.w;
+      }
+      __syncthreads();
+#pragma unroll 16
+      for (int kk = 0; kk < KC; ++kk) {
+        const float4 xv = *reinterpret_cast<const float4*>(&xs[kk][ty * 4]);
+        const float4 wv = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
+        const float xr[4] = {xv.x, xv.y, xv.z, xv.w};
+        const float wr[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xr[i], wr[j], acc[i][j]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int e = e0 + tx * 4 + j;
+        if (e < E) {
+          const float off = a.logit_offset ? a.logit_offset[e] : 0.f;
+          logits[(ty * 4 + i) * LD + e] = acc[i][j] + off;
+        }
+      }
+  }
+  __syncthreads();
+
+  const int warp = tid / 32, lane = tid % 32;
+  const unsigned FULL = 0xFFFFFFFFu;
+  constexpr int NONE = 0x7FFFFFFF;
+  for (int tok = warp; tok < RT; tok += NTHR / 32) {
+    const int t = t0 + tok;
+    if (t >= a.T) break;  // warp-uniform
+    float sc[MAXC], key[MAXC];
+#pragma unroll
+    for (int i = 0; i < MAXC; ++i) {
+      const int e = lane + 32 * i;
+      sc[i] = 0.f;
+      key[i] = -INFINITY;
+      if (e < E) {
+        const float z = logits[tok * LD + e];
+        const float s = 1.0f / (1.0f + expf(-z));
+        sc[i] = s;
+        key[i] = __fadd_rn(s, a.bias[e]);  // selection key: one fp32 addition
+        if (a.scores) a.scores[(size_t)t * E + e] = s;
+      }
+    }
+    unsigned taken = 0;
+    float sel_s[kMaxK];
+    int sel_e[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      sel_s[j] = 0.f;
+      sel_e[j] = 0;
+      if (j < a.k) {
+        float bk = -INFINITY;
+        int be = NONE;
+#pragma unroll
+        for (int i = 0; i < MAXC; ++i) {
+          const int e = lane + 32 * i;
+          if (e < E && !((taken >> i) & 1u) && (be == NONE || key[i] > bk)) {
+            bk = key[i];
+            be = e;
+          }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const float ok = __shfl_xor_sync(FULL, bk, off);
+          const int oe = __shfl_xor_sync(FULL, be, off);
+          if (oe != NONE && (be == NONE || ok > bk || (ok == bk && oe < be))) {
+            bk = ok;
+            be = oe;
+          }
+        }
+        float sw = 0.f;
+        if ((be & 31) == lane) {
+          taken |= 1u << (be >> 5);
+#pragma unroll
+          for (int i = 0; i < MAXC; ++i)
+            if (i == (be >> 5)) sw = sc[i];
+        }
+        sel_s[j] = __shfl_sync(FULL, sw, be & 31);
+        sel_e[j] = be;
+      }
+    }
+    float denom = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j)
+      if (j < a.k) denom += sel_s[j];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      if (j < a.k && lane == j) {
+        a.idx[(size_t)t * a.k + j] = sel_e[j];
+        a.gate[(size_t)t * a.k + j] = a.renorm ? __fdiv_rn(sel_s[j], denom) : sel_s[j];
+      }
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        if (j < a.k) atomicAdd(&hist[sel_e[j]], 1);
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += NTHR) {
+    const int h = hist[e];
+    if (h) {
+      atomicAdd(&a.load[e], h);
+      if (a.counts) atomicAdd(&a.counts[(size_t)(t0 / a.chunk_tokens) * E + e], h);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_router(const RouterArgs& a, cudaStream_t s) {
+  const int blocks = (a.T + RT - 1) / RT;
+  const size_t dyn = sizeof(float) * RT * (a.E + 1);
+  if (a.x_is_f32) {
+    cudaError_t e = cudaFuncSetAttribute(router_kernel<true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+    if (e != cudaSuccess) return e;
+    router_kernel<true><<<blocks, NTHR, dyn, s>>>(a);
+  } else {
+    cudaError_t e = cudaFuncSetAttribute(router_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+    if (e != cudaSuccess) return e;
+    router_kernel<false><<<blocks, NTHR, dyn, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,87 @@
+"""Device-side layer state: weights uploaded once, packed by the library's kernels.
+
+PyTorch provides the device memory; packing (gate/up interleave, int4 quantisation)
+runs in the library (moe_pack_gate_up, moe_quantize_int4).  `LayerOnDevice.forward`
+is one moe_layer_fwd call.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import _lib as L
+
+
+def to_device_bf16(bits: np.ndarray, device) -> torch.Tensor:
+    """Upload bf16 bit patterns (uint16 numpy) as a torch.bfloat16 tensor."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.to(device).view(torch.bfloat16)
+
+
+def to_device_tokens(x: np.ndarray, device) -> torch.Tensor:
+    if x.dtype == np.uint16:
+        return to_device_bf16(x, device)
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(device)
+
+
+def pack_gate_up(w_gate: torch.Tensor, w_up: torch.Tensor) -> torch.Tensor:
+    """[G][width][d] gate and up (bf16, device) -> interleaved [G][2*width][d]."""
+    G, width, d = w_gate.shape
+    out = torch.empty((G, 2 * width, d), dtype=torch.bfloat16, device=w_gate.device)
+    L.moe_pack_gate_up(G, width, d, w_gate, w_up, out)
+    return out
+
+
+def quantize_int4(w: torch.Tensor):
+    """bf16 [..., K] (device) -> (uint8 codes [..., K/2], fp16-bit scales int16 [..., K/32])."""
+    K = w.shape[-1]
+    rows = w.numel() // K
+    q = torch.empty(w.shape[:-1] + (K // 2,), dtype=torch.uint8, device=w.device)
+    s = torch.empty(w.shape[:-1] + (K // 32,), dtype=torch.int16, device=w.device)
+    L.moe_quantize_int4(rows, K, w, q, s)
+    return q, s
+
+
+class LayerOnDevice:
+    """One MoE layer's parameters on the GPU, in the layouts the library expects."""
+
+    def __init__(self, shape, host: dict, device="cuda", x_dtype=None):
+        self.spec = shape
+        dev = torch.device(device)
+        self.device = dev
+        x_dt = x_dtype if x_dtype is not None else shape.x_dtype
+        self.shape = L.make_shape(shape.T, shape.d, shape.E, shape.f, shape.F, shape.k,
+                                  renorm=shape.renorm,
+                                  x_dtype=L.MOE_X_F32 if x_dt == "f32" else L.MOE_X_BF16,
+                                  w_format=L.MOE_W_INT4_G32 if shape.w_format == "int4" else L.MOE_W_BF16)
+        self.w_router = torch.from_numpy(host["w_router"]).to(dev)
+        self.bias = torch.from_numpy(host["bias"].copy()).to(dev)
+        lo = host.get("logit_offset")
+        self.logit_offset = None if lo is None else torch.from_numpy(lo).to(dev)
+        self.gamma = float(host["gamma"])
+        wg = to_device_bf16(host["w_gate"], dev)
+        wu = to_device_bf16(host["w_up"], dev)
+        self.w_gate_up = pack_gate_up(wg, wu)
+        del wg, wu
+        self.w_down = to_device_bf16(host["w_down"], dev)
+        self.scale_gate_up = self.scale_down = None
+        if shape.w_format == "int4":
+            self.w_gate_up, self.scale_gate_up = quantize_int4(self.w_gate_up)
+            self.w_down, self.scale_down = quantize_int4(self.w_down)
+        self.shared_gate_up = self.shared_down = None
+        if shape.F:
+            sg = to_device_bf16(host["s_gate"], dev)[None]
+            su = to_device_bf16(host["s_up"], dev)[None]
+            self.shared_gate_up = pack_gate_up(sg, su)[0]
+            self.shared_down = to_device_bf16(host["s_down"], dev)
+        self.weights = L.make_weights(self.w_gate_up, self.w_down, self.shared_gate_up,
+                                      self.shared_down, self.scale_gate_up, self.scale_down)
+        self.ws_bytes = L.moe_layer_workspace_size(self.shape)
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+
+    def forward(self, x: torch.Tensor, out: torch.Tensor, update_bias: bool = True,
+                residual: torch.Tensor | None = None, debug=None, stream=None):
+        L.moe_layer_fwd(self.shape, x, self.w_router, self.logit_offset, self.bias, self.gamma,
+                        update_bias, self.weights, residual, out, self.workspace, debug=debug,
+                        stream=stream)
+        return out

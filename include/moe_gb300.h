@@ -1,0 +1,223 @@
+/*
+ * moe_gb300.h -- C ABI of the fine-grained MoE layer forward with aux-loss-free
+ * bias balancing, for NVIDIA GB300 (sm_103a).
+ *
+ * Method source: "Una carrera de relevos con GPUs alquiladas entrenó el MoE de 2.7B
+ * de NanoColibri por $200" (the same article in Chinese and Arabic), called "the
+ * relay article" below.
+ *   - opening section, architecture paragraph: hidden width 1024, 64 routed experts
+ *     of width 512 with top-2 routing, one always-resident shared expert of width
+ *     2048, a sigmoid-plus-bias router, and DeepSeek-V3 load balancing that moves
+ *     each layer's expert bias by gamma times sign(target - load);
+ *   - section "Entrenamiento por relevos", top-2 paragraph: gates are the scores
+ *     renormalised over the winners (at top_k = 1 the weight is the constant 1);
+ *     serving runs one expert per token;
+ *   - opening section, second paragraph: experts stored in an int4 container.
+ * Readings where the article is silent: SwiGLU experts (gate, up, down); ties in
+ * the selection key go to the lower expert index; target load = T*k/E with
+ * sign(0) = 0; the bias selects experts but never enters the gates; the shared
+ * expert is added with weight 1.
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates or frees device memory.  Row-major layouts; every pointer
+ *     must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls only enqueue work; none synchronises the host except
+ *     moe_device_status().
+ *   - Host-side validation happens before any launch and returns
+ *     MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED / MOE_ERR_WORKSPACE with nothing
+ *     enqueued.  A failed launch returns MOE_ERR_CUDA.  Device-side conditions
+ *     (a bounded wait that ran out) set a device status word read by
+ *     moe_device_status(); kernels never trap.
+ *   - bf16 tensors are passed as raw 16-bit patterns (void*), fp16 scales as
+ *     uint16 patterns.
+ */
+#ifndef MOE_GB300_H_
+#define MOE_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, bad size */
+  MOE_ERR_UNSUPPORTED = 2,  /* a size outside the supported envelope */
+  MOE_ERR_WORKSPACE = 3,    /* workspace smaller than the *_workspace_size query */
+  MOE_ERR_CUDA = 4,         /* a CUDA runtime / driver call failed */
+  MOE_ERR_TIMEOUT = 5,      /* device: a bounded wait gave up */
+  MOE_ERR_DEVICE = 6        /* device: an in-kernel check failed */
+} moe_status_t;
+
+enum { MOE_X_BF16 = 0, MOE_X_F32 = 1 };          /* token activation dtype */
+enum { MOE_W_BF16 = 0, MOE_W_INT4_G32 = 1 };     /* routed expert weight format */
+
+/* Sizes of one MoE layer.  T tokens, hidden d, E routed experts of SwiGLU width f,
+ * shared SwiGLU expert of width F (0 = none), top-k routing.
+ * Supported envelope: 1 <= T <= 2^24, 64 <= d <= 8192 with d % 64 == 0,
+ * 1 <= E <= 256, 1 <= k <= min(8, E), f % 32 == 0 (32 <= f <= 8192),
+ * F % 32 == 0 (0 <= F <= 16384).  renorm: 1 = gates renormalised over the k
+ * winners, 0 = gate is the raw sigmoid score.  MOE_W_INT4_G32 additionally needs
+ * k == 1 and T <= 256 (the top-1 serving path). */
+typedef struct {
+  int32_t T, d, E, f, F, k;
+  int32_t renorm;
+  int32_t x_dtype;   /* MOE_X_BF16 | MOE_X_F32 */
+  int32_t w_format;  /* MOE_W_BF16 | MOE_W_INT4_G32 */
+} moe_shape_t;
+
+/* Expert weights (device pointers).
+ *   bf16 format:
+ *     w_gate_up      [E][2f][d]  bf16, gate and up rows interleaved by
+ *                                moe_pack_gate_up (block = moe_gate_up_block(f))
+ *     w_down         [E][d][f]   bf16
+ *   int4 format (moe_quantize_int4 of the bf16 tensors above):
+ *     w_gate_up      [E][2f][d/2]  uint8, two's-complement nibbles, even index low
+ *     scale_gate_up  [E][2f][d/32] fp16, groups of 32 along d
+ *     w_down         [E][d][f/2]   uint8
+ *     scale_down     [E][d][f/32]  fp16, groups of 32 along f
+ *   shared expert (bf16 in every format; NULL when F == 0):
+ *     shared_gate_up [2F][d] bf16, interleaved by moe_pack_gate_up (block for F)
+ *     shared_down    [d][F]  bf16 */
+typedef struct {
+  const void* w_gate_up;
+  const void* w_down;
+  const void* scale_gate_up;
+  const void* scale_down;
+  const void* shared_gate_up;
+  const void* shared_down;
+} moe_weights_t;
+
+/* Optional intermediate outputs of moe_layer_fwd (any field may be NULL). */
+typedef struct {
+  float* scores;      /* [T][E] fp32 sigmoid scores */
+  int32_t* idx;       /* [T][k] */
+  float* gate;        /* [T][k] */
+  int32_t* load;      /* [E] */
+  int32_t* offsets;   /* [E+1] */
+  int32_t* perm_tok;  /* [T*k] */
+  int32_t* inv_pos;   /* [T][k] */
+} moe_debug_t;
+
+/* ABI version; bumped on any incompatible change. */
+int32_t moe_abi_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(moe_status_t status);
+
+/* Rows per gate/up interleave block for an FFN of width `width` (f or F):
+ * 128 if width % 128 == 0, else 64 if width % 64 == 0, else 32. */
+int32_t moe_gate_up_block(int32_t width);
+
+/* Router: relay article, architecture paragraph (sigmoid-plus-bias router, top-k)
+ * and top-2 paragraph (renormalised gates).
+ *   x            [T][d] bf16 or fp32 (shape->x_dtype)
+ *   w_router     [E][d] fp32; logits are fp32 dot products (no reduced precision)
+ *   logit_offset [E] fp32 added to every logit, or NULL (used by the skewed workload)
+ *   bias         [E] fp32, added to the scores for selection only
+ *   scores       [T][E] fp32 sigmoid scores, or NULL to skip writing them
+ *   idx          [T][k] int32: the k experts of largest fl32(score + bias), by
+ *                descending key, ties to the lower index
+ *   gate         [T][k] fp32: score_j / sum of the k winners' scores (renorm),
+ *                else score_j
+ *   load         [E] int32: pairs routed to each expert (overwritten). */
+moe_status_t moe_route(const moe_shape_t* shape, const void* x, const float* w_router,
+                       const float* logit_offset, const float* bias, float* scores,
+                       int32_t* idx, float* gate, int32_t* load, void* stream);
+
+/* Stable counting-sort permutation of the (token, slot) pairs by expert.
+ *   idx       [T][k] int32 from moe_route (values in [0, E), distinct per row)
+ *   offsets   [E+1] int32: expert e owns rows [offsets[e], offsets[e+1])
+ *   perm_tok  [T*k] int32: source token of each row; tokens ascend within a block
+ *   inv_pos   [T][k] int32: row holding pair (t, j)
+ *   workspace scratch of moe_permute_workspace_size(shape) bytes (no state kept). */
+size_t moe_permute_workspace_size(const moe_shape_t* shape);
+moe_status_t moe_permute(const moe_shape_t* shape, const int32_t* idx, int32_t* offsets,
+                         int32_t* perm_tok, int32_t* inv_pos, void* workspace,
+                         size_t ws_bytes, void* stream);
+
+/* Grouped routed-expert FFN and the shared expert (bf16 weights).
+ * Relay article, architecture paragraph (routed experts, always-resident shared
+ * expert); SwiGLU is this library's reading: h = silu(x Wg^T) * (x Wu^T) stored as
+ * bf16, y = h Wd^T; bf16 operands, fp32 accumulation on tcgen05 tensor cores.
+ *   x           [T][d] token activations (bf16, or fp32 rounded to bf16 here)
+ *   offsets, perm_tok from moe_permute
+ *   y_perm      [T*k][d] bf16: routed output of each permuted row
+ *   shared_out  [T][d] bf16: shared-expert output, NULL iff F == 0
+ *   workspace   moe_expert_ffn_workspace_size(shape) bytes of scratch. */
+size_t moe_expert_ffn_workspace_size(const moe_shape_t* shape);
+moe_status_t moe_expert_ffn(const moe_shape_t* shape, const void* x, const int32_t* offsets,
+                            const int32_t* perm_tok, const moe_weights_t* w, void* y_perm,
+                            void* shared_out, void* workspace, size_t ws_bytes,
+                            void* stream);
+
+/* Combine: out[t] = residual[t] + shared[t] + sum_j gate[t][j] * y_perm[inv_pos[t][j]],
+ * summed in fp32 and rounded once to bf16.  residual and shared_out may be NULL. */
+moe_status_t moe_combine(const moe_shape_t* shape, const void* y_perm, const void* shared_out,
+                         const int32_t* inv_pos, const float* gate, const void* residual,
+                         void* out, void* stream);
+
+/* Aux-loss-free bias update, relay article, architecture paragraph (DeepSeek-V3
+ * recipe): bias[e] = fl32(bias[e] + gamma * sign(tokens_times_k - E * load[e])),
+ * i.e. the sign of (target - load) with target = T*k/E and sign(0) = 0.
+ * tokens_times_k is the GLOBAL T*k when `load` was summed over data-parallel
+ * replicas (the only cross-replica exchange of the method). In place on `bias`. */
+moe_status_t moe_bias_update(int32_t E, int64_t tokens_times_k, const int32_t* load,
+                             float gamma, float* bias, void* stream);
+
+/* The whole layer: route, permute, gather, grouped expert FFN, shared expert,
+ * combine and (if update_bias) the bias update, enqueued on one stream with no
+ * host synchronisation.  bias is read for selection and then updated in place.
+ * residual (NULL or [T][d], same dtype as out) is added to the output.  For
+ * MOE_W_INT4_G32 the routed experts run through the int4 dequant-in-GEMM path.
+ *   out        [T][d] bf16
+ *   dbg        NULL or intermediate outputs (see moe_debug_t)
+ *   workspace  moe_layer_workspace_size(shape) bytes of scratch. */
+size_t moe_layer_workspace_size(const moe_shape_t* shape);
+moe_status_t moe_layer_fwd(const moe_shape_t* shape, const void* x, const float* w_router,
+                           const float* logit_offset, float* bias, float gamma,
+                           int32_t update_bias, const moe_weights_t* w, const void* residual,
+                           void* out, const moe_debug_t* dbg, void* workspace,
+                           size_t ws_bytes, void* stream);
+
+/* Weight preparation (off the hot path).
+ * moe_pack_gate_up: for each of G matrices, interleave w_gate [G][width][d] and
+ * w_up [G][width][d] (bf16) into w_gate_up [G][2*width][d] in blocks of
+ * b = moe_gate_up_block(width) rows: block i holds gate rows [i*b, (i+1)*b)
+ * followed by up rows [i*b, (i+1)*b).
+ * moe_quantize_int4: relay article, opening section (int4 container).  w [rows][K]
+ * bf16 -> q [rows][K/2] uint8 (nibbles, even index low) and scale [rows][K/32]
+ * fp16 with scale = fp16(fl32(max|w| / 7)) per group of 32 and
+ * q = clamp(rint(fl32(w / scale)), -7, 7) (0 where scale is 0).  K % 32 == 0. */
+moe_status_t moe_pack_gate_up(int32_t G, int32_t width, int32_t d, const void* w_gate,
+                              const void* w_up, void* w_gate_up, void* stream);
+moe_status_t moe_quantize_int4(int64_t rows, int32_t K, const void* w, void* q, void* scale,
+                               void* stream);
+
+/* Per-stage timing of moe_layer_fwd (profiling aid).  While enabled, every
+ * moe_layer_fwd call records CUDA events on its stream between its stages (router,
+ * permutation scan, scatter + gather, gate/up GEMM, routed down GEMM, shared down
+ * GEMM with the fused combine).  moe_profile_start(max_calls) enables it for up to
+ * max_calls calls (host-side event objects only, no device memory);
+ * moe_profile_stop synchronises, writes the summed milliseconds of each stage over
+ * the recorded calls to ms_per_stage[moe_profile_stage_count()], the number of
+ * recorded calls to *calls, and disables recording. */
+int32_t moe_profile_stage_count(void);
+const char* moe_profile_stage_name(int32_t stage);
+moe_status_t moe_profile_start(int32_t max_calls);
+moe_status_t moe_profile_stop(float* ms_per_stage, int32_t* calls);
+
+/* Synchronises `stream`, returns the device status word accumulated by this
+ * library's kernels since the last call (MOE_OK, MOE_ERR_TIMEOUT or
+ * MOE_ERR_DEVICE) in *device_status, and clears it. */
+moe_status_t moe_device_status(void* stream, int32_t* device_status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H_ */

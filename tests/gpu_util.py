@@ -1,0 +1,39 @@
+"""Helpers shared by the GPU parity tests (host-side comparison only)."""
+import numpy as np
+import torch
+
+from synth import f32_from_bf16_bits
+
+
+def bf64(bits):
+    return f32_from_bf16_bits(bits).astype(np.float64)
+
+
+def tokens64(x):
+    return bf64(x) if x.dtype == np.uint16 else x.astype(np.float64)
+
+
+def bf16_to_np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def rel_l2(got, ref) -> float:
+    ref = np.asarray(ref, np.float64)
+    return float(np.linalg.norm(np.asarray(got, np.float64) - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+# Output tolerance: bf16 operands and outputs with fp32 accumulation.  The relative
+# L2 bound is the contract; the element-wise bound (2e-2 relative plus 2e-2 of the
+# tensor's RMS) catches localised errors that an L2 norm would average away.
+REL_L2 = 2e-2
+
+
+def assert_close_bf16(got, ref, what=""):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    r = rel_l2(got, ref)
+    assert r <= REL_L2, f"{what}: rel L2 {r:.3e}"
+    rms = float(np.sqrt(np.mean(ref ** 2))) if ref.size else 0.0
+    bad = np.abs(got - ref) > 2e-2 * np.abs(ref) + 2e-2 * rms
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements off, first at {np.argwhere(bad)[0]}"
+    return r

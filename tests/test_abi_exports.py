@@ -1,0 +1,69 @@
+"""The C-ABI library builds, loads without a GPU and exports every declared symbol."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import aux_loss_free_gb300 as M
+from aux_loss_free_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_gb300.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib_path():
+    return B.build()
+
+
+def test_header_declares_the_documented_calls():
+    names = declared_functions()
+    for required in ("moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
+                     "moe_bias_update", "moe_layer_fwd"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib_path):
+    lib = ctypes.CDLL(lib_path)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_every_declared_symbol():
+    assert sorted(M.SIGNATURES) == declared_functions()
+
+
+def test_pure_host_entry_points(lib_path):
+    lib = M.load_library(lib_path)
+    assert lib.moe_abi_version() == 1
+    assert lib.moe_status_string(0) == b"ok"
+    assert [lib.moe_gate_up_block(w) for w in (512, 2048, 64, 32, 96)] == [128, 128, 64, 32, 32]
+
+
+def test_host_validation_rejects_bad_shapes_before_any_launch(lib_path):
+    M.load_library(lib_path)
+    bad = [
+        M.make_shape(0, 1024, 64, 512, 2048, 2),      # T = 0
+        M.make_shape(16, 1000, 64, 512, 2048, 2),     # d % 64 != 0
+        M.make_shape(16, 1024, 300, 512, 2048, 2),    # E > 256
+        M.make_shape(16, 1024, 4, 512, 2048, 5),      # k > E
+        M.make_shape(16, 1024, 64, 500, 2048, 2),     # f % 32 != 0
+        M.make_shape(16, 1024, 64, 512, 2048, 2, w_format=M.MOE_W_INT4_G32),  # int4 needs k = 1
+    ]
+    for s in bad:
+        assert M.moe_layer_workspace_size(s) == 0
+        assert M.moe_permute_workspace_size(s) == 0
+    good = M.make_shape(8192, 1024, 64, 512, 2048, 2)
+    assert M.moe_layer_workspace_size(good) > 8192 * 2 * 1024 * 2
+    lib = M.load_library()
+    # Null pointers are rejected on the host (no device touched).
+    assert lib.moe_route(ctypes.byref(good), None, None, None, None, None, None, None, None,
+                         None) == 1
+    assert lib.moe_bias_update(0, 16, None, 1e-3, None, None) == 1
