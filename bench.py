@@ -1,0 +1,409 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE layer forward with its aux-loss-free bias update on GB300.
+
+One step = one moe_layer_fwd call over one batch of synthetic tokens: router, top-k,
+gates, loads, stable permutation and gather, grouped routed-expert SwiGLU GEMMs,
+shared-expert GEMMs, gated combine and the bias update (all in the library's CUDA
+kernels).  Default workload: the Nano-shaped layer, T = 8192 tokens (batch 4 x
+sequence 2048), d = 1024, 64 routed experts of width 512, top-2, shared width 2048.
+
+Timing: W untimed warm-up steps, then K timed steps with a 512 MiB write between
+steps (L2 is 129 MB, so every step starts cold), each step bracketed by CUDA events
+on the launching stream; barrier + synchronize on both sides; max over ranks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload nano|skew|stack|tiny]
+  python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+Prints one JSON line.  Under torchrun (N > 1) every rank runs its own replica on its
+own tokens (weak scaling); the only cross-rank exchange of the method is the sum of
+the per-expert loads before the bias update.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synth import CONFIGS, f32_from_bf16_bits, make_layer, make_tokens  # noqa: E402
+
+METRIC = "MoE-layer fwd tokens/s (T=8192,d=1024,64x512 top-2+2048 shared), % roofline"
+FLUSH_BYTES = 512 << 20
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_gate_up_nano_traffic.txt")
+KERNELS_PER_CALL = 6  # router, scan, scatter+gather, gate/up GEMM, 2 down GEMMs (or combine)
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=["nano", "skew", "stack", "tiny"], default="nano")
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="target CPU time of the oracle baseline sample")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def workload_shape(name):
+    return CONFIGS[name]
+
+
+def config_block(name, n):
+    s = workload_shape(name)
+    cfg = {"workload": {"nano": "nano_moe_layer_fwd_T8192", "skew": "skewed_zipf1.2_moe_layer_fwd_T8192",
+                        "stack": "stack_23_moe_layers_T8192", "tiny": "tiny_moe_layer_fwd_T64"}[name],
+           "T": s.T, "d": s.d, "E": s.E, "f": s.f, "F": s.F, "k": s.k, "renorm": bool(s.renorm),
+           "bias_update": True, "tokens": "batch 4 x seq 2048" if s.T == 8192 else f"{s.T}",
+           "layers": s.layers, "l2": "512 MiB write before every timed step (L2 129 MB)",
+           "parallelism": f"dp{n} replicas, per-expert load all-reduce" if n > 1 else "dp1"}
+    return cfg
+
+
+def layer_algorithmic(s, loads_hit=None):
+    """FLOPs and bytes one layer forward must move (weights of experts hit, x in, out)."""
+    flops = 2 * s.T * s.d * s.E + 2 * 3 * s.d * s.f * s.T * s.k + 2 * 3 * s.d * s.F * s.T
+    hit = s.E if loads_hit is None else int(loads_hit)
+    nbytes = hit * 3 * s.d * s.f * 2 + 3 * s.d * s.F * 2 + s.E * s.d * 4 + 2 * s.T * s.d * 2
+    return flops, nbytes
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as fh:
+            pk = json.load(fh)
+        return pk, "of measured"
+    except (OSError, ValueError):
+        return FALLBACK_PEAKS, "of fallback"
+
+
+def gemm_source_hash():
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "aux_loss_free_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic():
+    """DRAM bytes per gate/up GEMM launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as fh:
+            for line in fh:
+                if ":" in line:
+                    a, b = line.split(":", 1)
+                    kv[a.strip()] = b.strip()
+        if kv.get("kernel_source_sha256_16") != gemm_source_hash():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 20 ms in the background."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20", "-i", str(index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        inside = [p for (t, p) in self.rows if t0 <= t <= t1] or [p for (_, p) in self.rows]
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        mx = [num(p[2]) for p in inside if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside),
+                "power_w_max": max((num(p[3]) or 0.0) for p in inside)}
+
+
+# ----------------------------------------------------------------------------- oracle arm
+
+def oracle_sample_runner(name, seed):
+    """Returns run(ntok) -> seconds for the oracle's layer forward on the first ntok
+    tokens of the workload (fp64 oracle, as it stands)."""
+    from oracle import moe_oracle as O
+
+    s = workload_shape(name)
+    host = make_layer(s, name if name != "stack" else "stack", seed)
+    bf = lambda b: f32_from_bf16_bits(b).astype(np.float64)  # noqa: E731
+    W = {k: bf(host[k]) for k in ("w_gate", "w_up", "w_down", "s_gate", "s_up", "s_down")}
+    x = host["x"]
+    xv = bf(x) if x.dtype == np.uint16 else x.astype(np.float64)
+
+    def run(ntok):
+        t0 = time.perf_counter()
+        O.layer_forward(xv[:ntok], host["w_router"], host["bias"], W["w_gate"], W["w_up"],
+                        W["w_down"], W["s_gate"], W["s_up"], W["s_down"], k=s.k, renorm=s.renorm,
+                        logit_offset=host["logit_offset"], gamma=host["gamma"],
+                        x_is_bf16=x.dtype == np.uint16)
+        return time.perf_counter() - t0
+    return run
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(name, seed, seconds):
+    run = oracle_sample_runner(name, seed)
+    s = workload_shape(name)
+    ntok = min(s.T, 1024)
+    run(min(ntok, 64))  # warm the BLAS threads
+    done, spent = 0, 0.0
+    while spent < seconds and done < 64 * s.T:
+        spent += run(ntok)
+        done += ntok
+    return {"value": done / spent * (1.0 / max(1, s.layers)), "unit": "tokens/s", "cores": cpu_cores(),
+            "kind": "oracle",
+            "sample": f"{done} tokens as {done // ntok} oracle layer forwards of {ntok} tokens of the "
+                      f"{name} workload (fp64 numpy, BLAS on all {cpu_cores()} visible cores), "
+                      f"{spent:.1f} s" + (f"; per stack forward of {s.layers} layers" if s.layers > 1 else "")}
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return
+    run = oracle_sample_runner(args.workload, args.seed)
+    s = workload_shape(args.workload)
+    t_cal = run(256)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    ntok = int(max(32, min(s.T, 256 * budget / max(t_cal, 1e-6))) // 32 * 32)
+    for _ in range(args.warmup):
+        run(ntok)
+    times = [run(ntok) for _ in range(args.steps)]
+    total = sum(times)
+    value = ntok * args.steps / total / max(1, s.layers)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_block(args.workload, world),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "kind": "oracle", "cores": cpu_cores(),
+                             "sample": f"each step: oracle layer forward of {ntok} of the {s.T} tokens"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def gpu_arm(args, rank, world, dist):
+    import torch
+
+    import aux_loss_free_gb300 as M
+    from aux_loss_free_gb300.layer import LayerOnDevice, to_device_tokens
+
+    M.load_library()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    s = workload_shape(args.workload)
+    name = args.workload
+    nlayers = s.layers
+    layers = [LayerOnDevice(s, make_layer(s, name, args.seed, layer=l, with_tokens=False), dev)
+              for l in range(nlayers)]
+    host_x = make_tokens(s, name, args.seed + rank)
+    x0 = to_device_tokens(host_x, dev)
+    acts = [x0] + [torch.empty(s.T, s.d, dtype=torch.bfloat16, device=dev) for _ in range(nlayers)]
+    stream = torch.cuda.current_stream(dev)
+    load = torch.empty(s.E, dtype=torch.int32, device=dev)
+    dbg_load = M.make_debug(load=load)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(x_in):
+        acts[0] = x_in
+        for l, L in enumerate(layers):
+            res = acts[l] if nlayers > 1 else None
+            if world > 1:
+                # Data-parallel replicas: local loads, global sum, identical update.
+                L.forward(acts[l], acts[l + 1], update_bias=False, residual=res, debug=dbg_load)
+                dist.all_reduce(load)
+                M.moe_bias_update(s.E, world * s.T * s.k, load, L.gamma, L.bias)
+            else:
+                L.forward(acts[l], acts[l + 1], update_bias=True, residual=res)
+        return acts[nlayers]
+
+    for _ in range(args.warmup):
+        step(x0)
+    torch.cuda.synchronize(dev)
+    if M.moe_device_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    # ---------------------------------------------------------------- timed region
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    time.sleep(0.1)
+    K = args.steps
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    M.moe_profile_start(K * nlayers)
+    t_wall0 = time.time()
+    for i in range(K):
+        flush.zero_()
+        ev0[i].record(stream)
+        step(x0)
+        ev1[i].record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    if dist:
+        dist.barrier()
+    stages_ms, calls = M.moe_profile_stop()
+    time.sleep(0.05)
+    sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    total_ms = sum(step_ms)
+    if dist:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    status = M.moe_device_status()
+
+    # ---------------------------------------------------------------- end to end
+    # Same step through the public call with host buffers: pinned tokens copied in,
+    # the layer output copied out, both inside the timed region.
+    hx = torch.empty(s.T, s.d, dtype=x0.dtype, pin_memory=True)
+    hx.copy_(x0.cpu())
+    hout = torch.empty(s.T, s.d, dtype=torch.bfloat16, pin_memory=True)
+    xin = torch.empty_like(x0)
+    Ke = max(3, min(K, 100))
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    torch.cuda.synchronize(dev)
+    for i in range(Ke):
+        flush.zero_()
+        e0[i].record(stream)
+        xin.copy_(hx, non_blocking=True)
+        y = step(xin)
+        hout.copy_(y, non_blocking=True)
+        e1[i].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / Ke
+
+    if rank != 0:
+        return
+    peaks, peak_note = load_peaks()
+    flops, nbytes = layer_algorithmic(s)
+    tokens_per_s = world * s.T * K / (total_ms / 1e3)
+    ms_step = total_ms / K
+    roof_s = nlayers * max(flops / (peaks["bf16_tflops"] * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9))
+    gu_flops = 2 * s.T * s.k * s.d * 2 * s.f + 2 * s.T * s.d * 2 * s.F
+    gu_ms = stages_ms["gemm_gate_up"] / max(1, calls)
+    achieved = gu_flops / (gu_ms / 1e3) / 1e12
+    traffic = read_traffic()
+    clocks = sampler.summary(t_wall0, t_wall1)
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_block(name, world),
+        "layer_roofline": {"flops_per_layer": flops, "bytes_per_layer": nbytes,
+                           "roofline_us": roof_s * 1e6, "measured_us": ms_step * 1e3,
+                           "frac": roof_s / (ms_step / 1e3), "peak": peak_note,
+                           "bound": "tensor" if flops / (peaks["bf16_tflops"] * 1e12) >
+                           nbytes / (peaks["hbm_gbs"] * 1e9) else "hbm"},
+        "roofline": {"kernel": "grouped_gemm_kernel (gate/up launch: 64 routed groups + shared)",
+                     "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                     "traffic": traffic, "peak_note": peak_note + " (burst)",
+                     "flops_per_launch": gu_flops, "avg_launch_us": gu_ms * 1e3},
+        "stages_us": {k: v * 1e3 / max(1, calls) for k, v in stages_ms.items()},
+        "e2e": {"value": world * s.T / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(hx.numel() * hx.element_size()),
+                "d2h_bytes_per_step": int(hout.numel() * hout.element_size())},
+        "gpu_launches": K * nlayers * KERNELS_PER_CALL,
+        "clocks": clocks,
+        "device_status": status,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(name if nlayers == 1 else "nano", args.seed,
+                                            args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.gpus != world and world == 1 and args.gpus > 1:
+        print(json.dumps({"error": "run N>1 under torch.distributed.run"}), flush=True)
+        sys.exit(2)
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    try:
+        gpu_arm(args, rank, world, dist)
+    finally:
+        if dist:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
