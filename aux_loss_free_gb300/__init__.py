@@ -30,6 +30,7 @@ from ._lib import (  # noqa: F401
     moe_layer_workspace_size,
     moe_pack_gate_up,
     moe_permute,
+    moe_permute_noalloc,
     moe_permute_workspace_size,
     moe_profile_start,
     moe_profile_stop,

@@ -52,6 +52,7 @@ SIGNATURES = {
     "moe_route": (_I32, [_SHAPE_P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_permute_workspace_size": (_SZ, [_SHAPE_P]),
     "moe_permute": (_I32, [_SHAPE_P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_permute_noalloc": (_I32, [_SHAPE_P, _P, _P, _P, _P, _P]),
     "moe_expert_ffn_workspace_size": (_SZ, [_SHAPE_P]),
     "moe_expert_ffn": (_I32, [_SHAPE_P, _P, _P, _P, ctypes.POINTER(MoEWeights), _P, _P, _P, _SZ,
                               _P]),
@@ -141,6 +142,13 @@ def moe_permute(shape, idx, offsets, perm_tok, inv_pos, workspace, stream=None):
     _check("moe_permute", load_library().moe_permute(
         ctypes.byref(shape), _ptr(idx), _ptr(offsets), _ptr(perm_tok), _ptr(inv_pos),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_permute_noalloc(shape, idx, offsets, perm_tok, inv_pos, stream=None):
+    """moe_permute with the library's fixed static scratch instead of a workspace."""
+    _check("moe_permute_noalloc", load_library().moe_permute_noalloc(
+        ctypes.byref(shape), _ptr(idx), _ptr(offsets), _ptr(perm_tok), _ptr(inv_pos),
+        _stream(stream)))
 
 
 def moe_expert_ffn_workspace_size(shape) -> int:

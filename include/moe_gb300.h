@@ -140,6 +140,25 @@ moe_status_t moe_permute(const moe_shape_t* shape, const int32_t* idx, int32_t* 
                          int32_t* perm_tok, int32_t* inv_pos, void* workspace,
                          size_t ws_bytes, void* stream);
 
+/* moe_permute without a workspace, for callers that cannot give the library device
+ * memory: a plugin inside a framework that owns the memory pool, a serving loop
+ * whose device-memory budget was fixed at start-up, or code about to be captured
+ * into a CUDA graph where a new cudaMalloc is not allowed.  The pages have no
+ * counterpart to this call; it computes exactly what moe_permute computes.
+ * Arguments as moe_permute (idx, offsets, perm_tok, inv_pos are caller-owned).
+ * Scratch: a library-owned static device array of 2 x 32768 int32 (256 KiB), held
+ * by every GPU that loads the library until the process exits.  Every supported
+ * shape fits (the chunking keeps each table within 32768 entries); a shape that
+ * would not fit returns MOE_ERR_UNSUPPORTED before any launch.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress, with that
+ * device current) and caches it: make that first call before any stream capture.
+ * The call allocates and frees nothing.  All calls share the one array, which
+ * keeps the previous call's contents (the call clears what must start at zero), so
+ * calls that can overlap on the GPU -- on different streams, or from different
+ * host threads -- race: serialise them. */
+moe_status_t moe_permute_noalloc(const moe_shape_t* shape, const int32_t* idx, int32_t* offsets,
+                                 int32_t* perm_tok, int32_t* inv_pos, void* stream);
+
 /* Grouped routed-expert FFN and the shared expert (bf16 weights).
  * Relay article, architecture paragraph (routed experts, always-resident shared
  * expert); SwiGLU is this library's reading: h = silu(x Wg^T) * (x Wu^T) stored as
