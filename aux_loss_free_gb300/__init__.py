@@ -36,4 +36,5 @@ from ._lib import (  # noqa: F401
     moe_profile_stop,
     moe_quantize_int4,
     moe_route,
+    moe_route_workspace_size,
 )

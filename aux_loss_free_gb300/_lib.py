@@ -49,7 +49,8 @@ SIGNATURES = {
     "moe_abi_version": (_I32, []),
     "moe_status_string": (ctypes.c_char_p, [_I32]),
     "moe_gate_up_block": (_I32, [_I32]),
-    "moe_route": (_I32, [_SHAPE_P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_route_workspace_size": (_SZ, [_SHAPE_P]),
+    "moe_route": (_I32, [_SHAPE_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute_workspace_size": (_SZ, [_SHAPE_P]),
     "moe_permute": (_I32, [_SHAPE_P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute_noalloc": (_I32, [_SHAPE_P, _P, _P, _P, _P, _P]),
@@ -128,10 +129,16 @@ def moe_gate_up_block(width: int) -> int:
     return load_library().moe_gate_up_block(width)
 
 
-def moe_route(shape, x, w_router, logit_offset, bias, scores, idx, gate, load, stream=None):
+def moe_route_workspace_size(shape) -> int:
+    return load_library().moe_route_workspace_size(ctypes.byref(shape))
+
+
+def moe_route(shape, x, w_router, logit_offset, bias, scores, idx, gate, load, workspace=None,
+              stream=None):
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("moe_route", load_library().moe_route(
         ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(logit_offset), _ptr(bias), _ptr(scores),
-        _ptr(idx), _ptr(gate), _ptr(load), _stream(stream)))
+        _ptr(idx), _ptr(gate), _ptr(load), _ptr(workspace), nbytes, _stream(stream)))
 
 
 def moe_permute_workspace_size(shape) -> int:

@@ -1,4 +1,4 @@
-// Grouped expert GEMM on tcgen05 tensor cores (sm_103a).
+// Grouped expert GEMM on tcgen05 tensor cores, CTA-pair (2-SM) version for sm_103a.
 //
 // One persistent launch runs up to two operand sets: the routed experts (E groups,
 // row ranges read from the device offsets of the counting sort, so there is no
@@ -6,22 +6,25 @@
 // article, opening section, architecture paragraph: 64 routed experts plus one
 // always-resident shared expert; SwiGLU is this library's reading of the expert FFN.
 //
-// CTA layout (192 threads, one CTA per SM):
-//   warp 0      TMA producer: A tile 128 x 64 and B tile BN x 64 (bf16, 128-byte
-//               swizzle) per stage into a 4-stage shared-memory ring;
-//   warp 1      owns the TMEM allocation; one thread issues tcgen05.mma
-//               (M = 128, N = BN, K = 16) into one of two 128 x 256 fp32
-//               accumulators, committing stage releases and accumulator-ready
-//               barriers;
-//   warps 2..5  epilogue: tcgen05.ld of their 32 TMEM lanes (rows), then
-//               SWIGLU  h = silu(gate) * up -> bf16   (gate / up rows interleaved
-//                       in the weights so one tile holds matching columns),
-//               STORE   y -> bf16,
-//               COMBINE out = acc + residual + sum_j gate_j * y_perm[inv_pos_j]
-//                       (the shared expert's down projection adds the routed
-//                       outputs of the same token: the layer's combine step).
+// Clusters of two CTAs on two SMs compute 256 x BN output tiles with
+// tcgen05.mma.cta_group::2 (M = 256, N = BN <= 256, K = 16):
+//   - each CTA stages its own 128 rows of A and one half (BN/2 rows) of B per
+//     k-block (128-byte swizzle, 6-stage ring of 32 KB); both CTAs' TMA copies
+//     complete on the leader CTA's "full" barrier;
+//   - one thread of the leader CTA issues the MMAs; the pair's tensor cores read
+//     the peer's half of B over the cluster, so each SM stages half the B bytes a
+//     single-SM 128 x 256 tile would need;
+//   - commits are multicast to both CTAs (stage release, accumulator ready);
+//   - each CTA's accumulator holds its 128 rows x BN fp32 columns in TMEM, double
+//     buffered (2 x 256 columns); 8 epilogue warps per CTA drain it:
+//       SWIGLU  h = silu(gate) * up -> bf16 (gate / up rows interleaved in the
+//               weights so one tile holds matching columns),
+//       STORE   y -> bf16,
+//       COMBINE out = acc + residual + sum_j gate_j * y_perm[inv_pos_j] (the shared
+//               expert's down projection adds the same token's routed outputs:
+//               the layer's combine step).
 // Every barrier wait is bounded (ptx.cuh); on a timeout the CTA records it in the
-// status word, drains its in-flight copies and MMAs, frees TMEM and exits.
+// status word, the pair drains its in-flight copies and MMAs, frees TMEM and exits.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
@@ -34,21 +37,23 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128;
+constexpr int BM = 256;        // rows per CTA-pair tile
+constexpr int HM = 128;        // rows per CTA
 constexpr int BK = 64;
 constexpr int BN_MAX = 256;
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN_MAX * BK * 2;
+constexpr int STAGES = 6;
+constexpr int A_BYTES = HM * BK * 2;            // 16 KB
+constexpr int B_BYTES = (BN_MAX / 2) * BK * 2;  // 16 KB (one half of B)
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARPS = 8;
+constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 2 * BN_MAX;
 constexpr int DYN_SMEM = STAGES * STAGE_BYTES + 1024;
 constexpr unsigned FULL = 0xFFFFFFFFu;
 
 struct OperandSet {
-  CUtensorMap a;
-  CUtensorMap b;
+  CUtensorMap a;  // box 128 rows x 64
+  CUtensorMap b;  // box BN/2 rows x 64
   void* out;
   int ldo, n_total, k_total, bn, mode, enabled, rows, pad;
 };
@@ -67,11 +72,88 @@ struct Params {
 
 struct Tile {
   int set;    // 0 shared, 1 routed
-  int row0;   // first A row (and output row)
-  int rows;   // valid rows in this tile
-  int brow;   // first B row
-  int n0;     // first output column of the accumulator tile
+  int row0;   // first A row of the pair's 256-row tile
+  int rend;   // end (exclusive) of the group's rows
+  int brow;   // first B row of the BN-row weight tile
+  int n0;     // first accumulator column in the output
 };
+
+// ---------------------------------------------------------------- cluster PTX
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// TMA tile load whose completion is counted on a barrier of the CTA pair (here the
+// leader's), given as a shared::cluster address.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void mma_pair_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on the barrier at the same offset in both CTAs once this thread's MMAs finish.
+__device__ __forceinline__ void commit_pair_multicast(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(static_cast<uint16_t>(0x3))
+      : "memory");
+}
+
+__device__ __forceinline__ void commit_pair_local(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// ---------------------------------------------------------------- helpers
 
 __device__ __forceinline__ Tile decode_tile(const Params& p, int tile, int shared_tiles,
                                             const int* s_off, const int* s_cum) {
@@ -81,7 +163,7 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, int tile, int share
     const int m = tile / nt, n = tile % nt;
     t.set = 0;
     t.row0 = m * BM;
-    t.rows = min(BM, p.shared.rows - t.row0);
+    t.rend = p.shared.rows;
     t.n0 = n * p.shared.bn;
     t.brow = t.n0;
   } else {
@@ -97,7 +179,7 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, int tile, int share
     const int m = local / nt, n = local % nt;
     t.set = 1;
     t.row0 = s_off[g] + m * BM;
-    t.rows = min(BM, s_off[g + 1] - t.row0);
+    t.rend = s_off[g + 1];
     t.n0 = n * p.routed.bn;
     t.brow = g * p.routed.n_total + t.n0;
   }
@@ -109,14 +191,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-__device__ __forceinline__ float silu(float a) { return a / (1.0f + __expf(-a)); }
+// silu(a) = a / (1 + e^-a).  The fast division has no special-value slow path; for
+// very negative a the denominator overflows and the quotient is the correct 0.
+__device__ __forceinline__ float silu(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
 
 __device__ __forceinline__ void add_bf16_row32(float (&o)[32], const uint16_t* src, float w) {
   const uint4* s = reinterpret_cast<const uint4*>(src);
+  uint4 u[4];
+#pragma unroll
+  for (int v = 0; v < 4; ++v) u[v] = s[v];
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
-    const uint4 u = s[v];
-    const uint32_t ws[4] = {u.x, u.y, u.z, u.w};
+    const uint32_t ws[4] = {u[v].x, u[v].y, u[v].z, u[v].w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       o[v * 8 + 2 * i] = fmaf(w, __uint_as_float(ws[i] << 16), o[v * 8 + 2 * i]);
@@ -133,12 +219,13 @@ __device__ __forceinline__ void store_bf16_row32(uint16_t* dst, const float (&o)
                       pack_bf16x2(o[8 * v + 4], o[8 * v + 5]), pack_bf16x2(o[8 * v + 6], o[8 * v + 7]));
 }
 
-__global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __grid_constant__ Params p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[STAGES];
-  __shared__ __align__(8) uint64_t empty_bar[STAGES];
-  __shared__ __align__(8) uint64_t tfull_bar[2];
-  __shared__ __align__(8) uint64_t tempty_bar[2];
+  __shared__ __align__(8) uint64_t full_bar[STAGES];   // used in the leader
+  __shared__ __align__(8) uint64_t empty_bar[STAGES];  // both CTAs
+  __shared__ __align__(8) uint64_t tfull_bar[2];       // both CTAs
+  __shared__ __align__(8) uint64_t tempty_bar[2];      // used in the leader
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ uint32_t tmem_holder;
   __shared__ int s_off[kMaxE + 1];
@@ -147,6 +234,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
 
   const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
   const int shared_tiles =
       p.shared.enabled ? ((p.shared.rows + BM - 1) / BM) * (p.shared.n_total / p.shared.bn) : 0;
 
@@ -157,7 +247,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&tfull_bar[a]), 1);
-      mbar_init(smem_u32(&tempty_bar[a]), 4);
+      mbar_init(smem_u32(&tempty_bar[a]), 2 * EPI_WARPS);
     }
     mbar_init(smem_u32(&drain_bar), 1);
     fence_mbar_init();
@@ -171,8 +261,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
     }
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&tmem_holder), TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(&tmem_holder), TMEM_COLS);
+    tmem_relinquish_pair();
   }
   if (warp == 2) {
     // Tile table of the routed groups: s_cum[g] = tiles of groups < g.
@@ -202,32 +292,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
     if (lane == 0) s_total = shared_tiles + carry;
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // barriers of both CTAs are initialised before any remote use
   tc_fence_after();
   const uint32_t tmem_base = tmem_holder;
   const int total = s_total;
 
   if (warp == 0) {
     if (lane == 0) {
-      // ------------------------------------------------ TMA producer
+      // ------------------------------------------------ TMA producer (both CTAs)
       int stage = 0;
       uint32_t phase = 0, issued = 0, last_par = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = cluster; tile < total && ok; tile += nclusters) {
         const Tile t = decode_tile(p, tile, shared_tiles, s_off, s_cum);
         const OperandSet& S = t.set ? p.routed : p.shared;
         const int nkb = (S.k_total + BK - 1) / BK;
-        const uint32_t bytes = A_BYTES + S.bn * BK * 2;
+        const int half = S.bn / 2;
+        const uint32_t pair_bytes = 2u * (A_BYTES + half * BK * 2);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) {
             ok = false;
             break;
           }
           const uint32_t sa = ring + stage * STAGE_BYTES;
-          const uint32_t fb = smem_u32(&full_bar[stage]);
-          mbar_arrive_expect_tx(fb, bytes);
-          tma_load_2d(sa, &S.a, fb, kb * BK, t.row0);
-          tma_load_2d(sa + A_BYTES, &S.b, fb, kb * BK, t.brow);
+          const uint32_t fb = map_to_rank(smem_u32(&full_bar[stage]), 0);
+          if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[stage]), pair_bytes);
+          tma_load_2d_pair(sa, &S.a, fb, kb * BK, t.row0 + HM * (int)rank);
+          tma_load_2d_pair(sa + A_BYTES, &S.b, fb, kb * BK, t.brow + half * (int)rank);
           issued |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -236,17 +327,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           }
         }
       }
-      // Every copy this CTA started must land before the CTA may exit.
-      for (int s = 0; s < STAGES; ++s)
-        if ((issued >> s) & 1u) mbar_wait(smem_u32(&full_bar[s]), (last_par >> s) & 1u, p.status);
+      // The leader's full barriers count both CTAs' copies: wait for all of them.
+      if (leader)
+        for (int s = 0; s < STAGES; ++s)
+          if ((issued >> s) & 1u) mbar_wait(smem_u32(&full_bar[s]), (last_par >> s) & 1u, p.status);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------ MMA issuer
+    if (lane == 0 && leader) {
+      // ------------------------------------------------ MMA issuer (leader only)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = cluster; tile < total && ok; tile += nclusters) {
         const Tile t = decode_tile(p, tile, shared_tiles, s_off, s_cum);
         const OperandSet& S = t.set ? p.routed : p.shared;
         const int nkb = (S.k_total + BK - 1) / BK;
@@ -266,28 +358,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           const int kleft = S.k_total - kb * BK;
           const int nkk = kleft >= BK ? BK / 16 : (kleft + 15) / 16;
           for (int kk = 0; kk < nkk; ++kk)
-            tc_mma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
-          tc_commit(smem_u32(&empty_bar[stage]));
+            mma_pair_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+          commit_pair_multicast(smem_u32(&empty_bar[stage]));
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(smem_u32(&tfull_bar[acc]));
+        commit_pair_multicast(smem_u32(&tfull_bar[acc]));
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
-      // Every MMA this thread issued must finish before TMEM is released.
-      tc_commit(smem_u32(&drain_bar));
+      // Every MMA must finish before TMEM is released.
+      commit_pair_local(smem_u32(&drain_bar));
       mbar_wait(smem_u32(&drain_bar), 0, p.status);
     }
   } else {
-    // -------------------------------------------------- epilogue (warps 2..5)
-    const int q = warp & 3;  // TMEM lanes [32q, 32q + 32) are this warp's rows
+    // -------------------------------------------------- epilogue (warps 2..9)
+    const int q = warp & 3;                 // TMEM lanes [32q, 32q + 32) are this warp's rows
+    const int colh = (warp - 2) / 4;        // which interleaved half of the column chunks
+    const uint32_t tempty_leader0 = map_to_rank(smem_u32(&tempty_bar[0]), 0);
+    const uint32_t tempty_leader1 = map_to_rank(smem_u32(&tempty_bar[1]), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    for (int tile = cluster; tile < total; tile += nclusters) {
       const Tile t = decode_tile(p, tile, shared_tiles, s_off, s_cum);
       const OperandSet& S = t.set ? p.routed : p.shared;
       int ok = 1;
@@ -296,13 +391,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
       if (!ok) break;
       tc_fence_after();
       const int r = q * 32 + lane;
-      const bool valid = r < t.rows;
-      const long long orow = (long long)t.row0 + r;
+      const long long orow = (long long)t.row0 + HM * (int)rank + r;
+      const bool valid = orow < t.rend;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN_MAX;
       uint16_t* out = static_cast<uint16_t*>(S.out);
       if (S.mode == EPI_SWIGLU) {
         const int half = S.bn / 2;
-        for (int c = 0; c < half; c += 32) {
+        for (int c = 32 * colh; c < half; c += 64) {
           uint32_t g[32], u[32];
           tmem_ld32(tbase + c, g);
           tmem_ld32(tbase + half + c, u);
@@ -313,7 +408,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           if (valid) store_bf16_row32(out + orow * S.ldo + t.n0 / 2 + c, h);
         }
       } else if (S.mode == EPI_STORE) {
-        for (int c = 0; c < S.bn; c += 32) {
+        for (int c = 32 * colh; c < S.bn; c += 64) {
           uint32_t v[32];
           tmem_ld32(tbase + c, v);
           tmem_wait_ld();
@@ -334,7 +429,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
             pj[j] = p.inv_pos[orow * p.k + j];
           }
         }
-        for (int c = 0; c < S.bn; c += 32) {
+        for (int c = 32 * colh; c < S.bn; c += 64) {
           uint32_t v[32];
           tmem_ld32(tbase + c, v);
           tmem_wait_ld();
@@ -353,16 +448,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[acc]));
+      if (lane == 0) mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
   }
 
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // neither CTA leaves while the pair still has copies or MMAs in flight
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+  if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
 // ------------------------------------------------------------------ host side
@@ -402,11 +497,24 @@ int choose_bn(int mode, int N) {
   return N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : 64);
 }
 
-int num_sms() {
-  int dev = 0, n = 0;
+// Largest number of co-resident 2-CTA clusters for this kernel on the current device.
+int max_active_pairs() {
+  static int cached[64] = {0};
+  int dev = 0;
   cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 1;
+  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+  int sms = 1;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int pairs = sms / 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = DYN_SMEM;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel, &cfg) == cudaSuccess && n > 0)
+    pairs = std::min(pairs, n);
+  if (dev >= 0 && dev < 64) cached[dev] = pairs;
+  return pairs;
 }
 
 bool fill_set(OperandSet& t, const GemmOperandSet& o) {
@@ -421,8 +529,8 @@ bool fill_set(OperandSet& t, const GemmOperandSet& o) {
   t.rows = o.rows;
   t.out = o.out;
   if (o.N % t.bn != 0) return false;
-  if (!make_map(&t.a, o.a, o.K, o.a_rows, BM)) return false;
-  if (!make_map(&t.b, o.b, o.K, (uint64_t)o.groups * o.N, t.bn)) return false;
+  if (!make_map(&t.a, o.a, o.K, o.a_rows, HM)) return false;
+  if (!make_map(&t.b, o.b, o.K, (uint64_t)o.groups * o.N, t.bn / 2)) return false;
   return true;
 }
 
@@ -449,16 +557,16 @@ cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* off
   p.status = device_status_ptr();
   if (!p.status) return cudaErrorInvalidDevicePointer;
 
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, DYN_SMEM);
+  if (e != cudaSuccess) return e;
   long long tiles = 0;
   if (p.shared.enabled)
     tiles += (long long)((p.shared.rows + BM - 1) / BM) * (p.shared.n_total / p.shared.bn);
   if (p.routed.enabled)
     tiles += ((max_routed_rows + BM - 1) / BM + E) * (long long)(p.routed.n_total / p.routed.bn);
-  const int grid = (int)std::min<long long>(num_sms(), std::max<long long>(tiles, 1));
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, DYN_SMEM);
-  if (e != cudaSuccess) return e;
-  grouped_gemm_kernel<<<grid, NUM_THREADS, DYN_SMEM, s>>>(p);
+  const int pairs = (int)std::min<long long>(max_active_pairs(), std::max<long long>(tiles, 1));
+  grouped_gemm_kernel<<<2 * pairs, NUM_THREADS, DYN_SMEM, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -39,6 +39,11 @@ struct RouterArgs {
   int T, d, E, k, renorm;
 };
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
+// Tensor-core router (bf16 tokens, E in {16, 32, 48, 64, 80}); needs scratch for the
+// three-way bf16 split of the router weight.
+bool router_tc_supported(int E, int x_is_f32);
+size_t router_tc_scratch_bytes(int E, int d);
+cudaError_t launch_router_tc(const RouterArgs& a, void* w3_scratch, cudaStream_t s);
 
 // ---------------------------------------------------------------- permutation
 cudaError_t launch_count(const int32_t* idx, int T, int k, int E, int chunk_tokens,

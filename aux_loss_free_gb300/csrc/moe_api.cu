@@ -93,6 +93,15 @@ moe_status_t check_shape(const moe_shape_t* s) {
 
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+size_t route_scratch_bytes(const moe_shape_t* s) {
+  return router_tc_supported(s->E, s->x_dtype == MOE_X_F32) ? router_tc_scratch_bytes(s->E, s->d) : 0;
+}
+
+cudaError_t run_router(const RouterArgs& a, void* scratch, cudaStream_t s) {
+  if (router_tc_supported(a.E, a.x_is_f32)) return launch_router_tc(a, scratch, s);
+  return launch_router(a, s);
+}
+
 int chunks_of(const moe_shape_t* s, int* chunk_tokens) {
   *chunk_tokens = permute_chunk_tokens(s->T, s->E);
   return (s->T + *chunk_tokens - 1) / *chunk_tokens;
@@ -128,6 +137,7 @@ FfnWs carve_ffn(Carver& c, const moe_shape_t* s) {
 }
 
 struct LayerWs {
+  void* router;
   int32_t* idx;
   float* gate;
   int32_t* load;
@@ -141,6 +151,8 @@ struct LayerWs {
 LayerWs carve_layer(Carver& c, const moe_shape_t* s) {
   const size_t Tk = (size_t)s->T * s->k;
   LayerWs w;
+  const size_t rb = route_scratch_bytes(s);
+  w.router = rb ? c.take(rb) : nullptr;
   w.idx = static_cast<int32_t*>(c.take(4 * Tk));
   w.gate = static_cast<float*>(c.take(4 * Tk));
   w.load = static_cast<int32_t*>(c.take(4 * (size_t)s->E));
@@ -237,18 +249,27 @@ int32_t moe_gate_up_block(int32_t width) {
   return width % 128 == 0 ? 128 : (width % 64 == 0 ? 64 : 32);
 }
 
+size_t moe_route_workspace_size(const moe_shape_t* shape) {
+  if (check_shape(shape)) return 0;
+  return route_scratch_bytes(shape);
+}
+
 moe_status_t moe_route(const moe_shape_t* shape, const void* x, const float* w_router,
                        const float* logit_offset, const float* bias, float* scores, int32_t* idx,
-                       float* gate, int32_t* load, void* stream) {
+                       float* gate, int32_t* load, void* workspace, size_t ws_bytes, void* stream) {
   moe_status_t st = check_shape(shape);
   if (st) return st;
   if (!x || !w_router || !bias || !idx || !gate || !load) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(w_router)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router) || (scores && !aligned16(scores)))
+    return MOE_ERR_INVALID_ARG;
+  const size_t need = route_scratch_bytes(shape);
+  if (need && (!workspace || !aligned16(workspace))) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(load, 0, sizeof(int32_t) * shape->E, s) != cudaSuccess) return MOE_ERR_CUDA;
   RouterArgs a{x, shape->x_dtype == MOE_X_F32, w_router, logit_offset, bias, scores, idx, gate,
                load, nullptr, kRouterTokens, shape->T, shape->d, shape->E, shape->k, shape->renorm};
-  return cuda_status(launch_router(a, s));
+  return cuda_status(run_router(a, workspace, s));
 }
 
 size_t moe_permute_workspace_size(const moe_shape_t* shape) {
@@ -355,7 +376,8 @@ moe_status_t moe_layer_fwd(const moe_shape_t* shape, const void* x, const float*
   if (!x || !w_router || !bias || !out || !workspace || !weights_ok(shape, w))
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_router) || !aligned16(out) ||
-      (residual && !aligned16(residual)))
+      (residual && !aligned16(residual)) || !aligned16(workspace) ||
+      (dbg && dbg->scores && !aligned16(dbg->scores)))
     return MOE_ERR_INVALID_ARG;
   if (ws_bytes < moe_layer_workspace_size(shape)) return MOE_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -380,7 +402,7 @@ moe_status_t moe_layer_fwd(const moe_shape_t* shape, const void* x, const float*
     return MOE_ERR_CUDA;
   RouterArgs ra{x, xf, w_router, logit_offset, bias, dbg ? dbg->scores : nullptr, L.idx, L.gate,
                 L.load, L.perm.counts, ct, T, shape->d, E, k, shape->renorm};
-  cudaError_t e = launch_router(ra, s);
+  cudaError_t e = run_router(ra, L.router, s);
   prof_mark(1, s);
   if (e == cudaSuccess)
     e = launch_scan(L.perm.counts, chunks, E, L.perm.bases, L.offsets, nullptr,

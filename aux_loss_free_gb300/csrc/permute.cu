@@ -63,7 +63,22 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
   __shared__ int32_t total[kMaxE];
   __shared__ int32_t off[kMaxE + 1];
   const int tid = threadIdx.x;
-  for (int i = tid; i < chunks * E; i += blockDim.x) c[i] = counts[i];
+  {
+    // Issue every load before the first shared-memory store (one memory round trip).
+    constexpr int PER = kMaxCountEntries / 1024;
+    const int n = chunks * E;
+    int v[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int i = j * 1024 + tid;
+      v[j] = i < n ? counts[i] : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int i = j * 1024 + tid;
+      if (i < n) c[i] = v[j];
+    }
+  }
   const int nseg = blockDim.x / E;
   const int L = (chunks + nseg - 1) / nseg;
   __syncthreads();

@@ -1,0 +1,339 @@
+// Router on tcgen05 tensor cores for bf16 tokens.
+//
+// Relay article ("Una carrera de relevos con GPUs alquiladas entrenó el MoE de 2.7B de
+// NanoColibri por $200"), opening section, architecture paragraph: sigmoid-plus-bias
+// router with top-k routing; section "Entrenamiento por relevos", top-2 paragraph:
+// gates renormalised over the winners.
+//
+// The router weight is fp32.  It is split exactly into three bf16 parts,
+// W = W_hi + W_mid + W_lo (each part the bf16 rounding of what the previous parts
+// left), stored as one [3E][d] matrix.  Token values are bf16, so every product
+// x * W_part is exact in fp32 and the tensor core accumulates in fp32: the logits
+// carry fp32 accuracy (no reduced-precision weights, no TF32).  One CTA owns 128
+// tokens: a TMA producer streams 128 x 64 token tiles and 3E x 64 weight tiles
+// through a 4-stage ring, one thread issues tcgen05.mma (M = 128, N = 3E, K = 16)
+// into TMEM, and then each of the 128 threads owns one token: it reads its 3E
+// accumulator columns, forms the E logits, applies the sigmoid, selects the top-k
+// by fl32(score + bias) with ties to the lower index, computes the gates and counts
+// its experts into a per-warp shared-memory histogram.
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int RBM = 128;
+constexpr int RBK = 64;
+constexpr int RSTAGES = 4;
+constexpr int A_BYTES = RBM * RBK * 2;
+constexpr int RTHREADS = 128;
+constexpr unsigned FULL = 0xFFFFFFFFu;
+
+struct RouterTcParams {
+  CUtensorMap x_map;  // [T][d] bf16, box 128 x 64
+  CUtensorMap w_map;  // [3E][d] bf16, box 3E x 64
+  const float* logit_offset;
+  const float* bias;
+  float* scores;
+  int32_t* idx;
+  float* gate;
+  int32_t* load;
+  int32_t* counts;
+  int* status;
+  int chunk_tokens, T, d, k, renorm, stage_bytes;
+};
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+template <int E>
+__global__ void __launch_bounds__(RTHREADS, 1) router_tc_kernel(const __grid_constant__ RouterTcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[RSTAGES];
+  __shared__ __align__(8) uint64_t empty_bar[RSTAGES];
+  __shared__ __align__(8) uint64_t tfull_bar;
+  __shared__ uint32_t tmem_holder;
+  __shared__ float s_bias[E];
+  __shared__ float s_off[E];
+  __shared__ int hist[4][E];
+
+  constexpr int N = 3 * E;
+  constexpr uint32_t TCOLS = N <= 32 ? 32 : (N <= 64 ? 64 : (N <= 128 ? 128 : 256));
+  const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int t0 = blockIdx.x * RBM;
+
+  for (int e = threadIdx.x; e < E; e += RTHREADS) {
+    s_bias[e] = p.bias[e];
+    s_off[e] = p.logit_offset ? p.logit_offset[e] : 0.f;
+  }
+  for (int i = threadIdx.x; i < 4 * E; i += RTHREADS) (&hist[0][0])[i] = 0;
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < RSTAGES; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+    }
+    mbar_init(smem_u32(&tfull_bar), 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&p.x_map);
+    tma_prefetch_desc(&p.w_map);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_holder), TCOLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_holder;
+  const int nkb = p.d / RBK;
+
+  if (warp == 0 && lane == 0) {
+    const uint32_t bytes = A_BYTES + N * RBK * 2;
+    uint32_t issued = 0, last_par = 0;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int kb = 0; kb < nkb; ++kb) {
+      if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) break;
+      const uint32_t sa = ring + stage * p.stage_bytes;
+      const uint32_t fb = smem_u32(&full_bar[stage]);
+      mbar_arrive_expect_tx(fb, bytes);
+      tma_load_2d(sa, &p.x_map, fb, kb * RBK, t0);
+      tma_load_2d(sa + A_BYTES, &p.w_map, fb, kb * RBK, 0);
+      issued |= 1u << stage;
+      last_par = (last_par & ~(1u << stage)) | (phase << stage);
+      if (++stage == RSTAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    for (int s = 0; s < RSTAGES; ++s)
+      if ((issued >> s) & 1u) mbar_wait(smem_u32(&full_bar[s]), (last_par >> s) & 1u, p.status);
+  } else if (warp == 1 && lane == 0) {
+    constexpr uint32_t idesc = idesc_bf16_f32(RBM, N);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int kb = 0; kb < nkb && ok; ++kb) {
+      if (!mbar_wait(smem_u32(&full_bar[stage]), phase, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sa = ring + stage * p.stage_bytes;
+      const uint64_t adesc = sw128_kmajor_desc(sa);
+      const uint64_t bdesc = sw128_kmajor_desc(sa + A_BYTES);
+#pragma unroll
+      for (int kk = 0; kk < RBK / 16; ++kk)
+        tc_mma_bf16(tmem_base, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+      tc_commit(smem_u32(&empty_bar[stage]));
+      if (++stage == RSTAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    tc_commit(smem_u32(&tfull_bar));  // also fires after a partial (timed-out) loop
+  }
+  __syncwarp();
+
+  // ------------------------------------------------------------ per-token epilogue
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait(smem_u32(&tfull_bar), 0, p.status) ? 1 : 0;
+  ok = __shfl_sync(FULL, ok, 0);
+  tc_fence_after();
+  const int row = warp * 32 + lane;
+  const int t = t0 + row;
+  const bool valid = ok && t < p.T;
+  const uint32_t tl = tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
+  float s[E];
+#pragma unroll
+  for (int c = 0; c < E; c += 16) {
+    uint32_t h[16], m[16], l[16];
+    tmem_ld16(tl + c, h);
+    tmem_ld16(tl + E + c, m);
+    tmem_ld16(tl + 2 * E + c, l);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float z = (__uint_as_float(h[i]) + __uint_as_float(m[i])) + __uint_as_float(l[i]) +
+                      s_off[c + i];
+      s[c + i] = 1.0f / (1.0f + expf(-z));
+    }
+  }
+  if (valid) {
+    if (p.scores) {
+      float4* dst = reinterpret_cast<float4*>(p.scores + (size_t)t * E);
+#pragma unroll
+      for (int i = 0; i < E / 4; ++i) dst[i] = make_float4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]);
+    }
+    uint32_t taken[(E + 31) / 32];
+#pragma unroll
+    for (int i = 0; i < (E + 31) / 32; ++i) taken[i] = 0;
+    float sel_s[kMaxK];
+    int sel_e[kMaxK];
+    float denom = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      sel_s[j] = 0.f;
+      sel_e[j] = 0;
+      if (j < p.k) {
+        float bk = -INFINITY, bs = 0.f;
+        int be = -1;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          if (!((taken[e / 32] >> (e % 32)) & 1u)) {
+            const float key = __fadd_rn(s[e], s_bias[e]);
+            if (be < 0 || key > bk) {
+              bk = key;
+              be = e;
+              bs = s[e];
+            }
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < (E + 31) / 32; ++i)
+          if (i == be / 32) taken[i] |= 1u << (be % 32);
+        sel_s[j] = bs;
+        sel_e[j] = be;
+        denom += bs;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      if (j < p.k) {
+        p.idx[(size_t)t * p.k + j] = sel_e[j];
+        p.gate[(size_t)t * p.k + j] = p.renorm ? __fdiv_rn(sel_s[j], denom) : sel_s[j];
+        atomicAdd(&hist[warp][sel_e[j]], 1);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  // Each warp's 32 tokens lie in one permutation chunk (chunks are multiples of 32).
+  for (int i = threadIdx.x; i < 4 * E; i += RTHREADS) {
+    const int w = i / E, e = i % E;
+    const int v = hist[w][e];
+    if (v) {
+      atomicAdd(&p.load[e], v);
+      if (p.counts) atomicAdd(&p.counts[(size_t)((t0 + 32 * w) / p.chunk_tokens) * E + e], v);
+    }
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TCOLS);
+  }
+}
+
+// W (fp32 [E][d]) -> W3 (bf16 [3E][d]): rows [0,E) W_hi, [E,2E) W_mid, [2E,3E) W_lo with
+// W_hi = bf16(W), W_mid = bf16(W - W_hi), W_lo = bf16(W - W_hi - W_mid); each
+// difference is exact in fp32.
+__global__ void split_router_kernel(const float* __restrict__ w, long long n, uint16_t* __restrict__ w3) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float v = w[i];
+  const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+  const float r1 = v - __bfloat162float(hi);
+  const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+  const float r2 = r1 - __bfloat162float(mid);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+  w3[i] = __bfloat16_as_ushort(hi);
+  w3[n + i] = __bfloat16_as_ushort(mid);
+  w3[2 * n + i] = __bfloat16_as_ushort(lo);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(RBK), box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int E>
+cudaError_t launch_e(RouterTcParams& p, int blocks, cudaStream_t s) {
+  const int dyn = RSTAGES * p.stage_bytes + 1024;
+  cudaError_t e = cudaFuncSetAttribute(router_tc_kernel<E>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+  if (e != cudaSuccess) return e;
+  router_tc_kernel<E><<<blocks, RTHREADS, dyn, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool router_tc_supported(int E, int x_is_f32) {
+  return !x_is_f32 && (E == 16 || E == 32 || E == 48 || E == 64 || E == 80);
+}
+
+size_t router_tc_scratch_bytes(int E, int d) { return (size_t)3 * E * d * sizeof(uint16_t); }
+
+cudaError_t launch_router_tc(const RouterArgs& a, void* w3_scratch, cudaStream_t s) {
+  const long long n = (long long)a.E * a.d;
+  uint16_t* w3 = static_cast<uint16_t*>(w3_scratch);
+  split_router_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a.w_router, n, w3);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  RouterTcParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (!make_map(&p.x_map, a.x, a.d, a.T, RBM) || !make_map(&p.w_map, w3, a.d, 3 * a.E, 3 * a.E))
+    return cudaErrorInvalidValue;
+  p.logit_offset = a.logit_offset;
+  p.bias = a.bias;
+  p.scores = a.scores;
+  p.idx = a.idx;
+  p.gate = a.gate;
+  p.load = a.load;
+  p.counts = a.counts;
+  p.status = device_status_ptr();
+  if (!p.status) return cudaErrorInvalidDevicePointer;
+  p.chunk_tokens = a.chunk_tokens;
+  p.T = a.T;
+  p.d = a.d;
+  p.k = a.k;
+  p.renorm = a.renorm;
+  p.stage_bytes = A_BYTES + ((3 * a.E * RBK * 2 + 1023) / 1024) * 1024;
+  const int blocks = (a.T + RBM - 1) / RBM;
+  switch (a.E) {
+    case 16: return launch_e<16>(p, blocks, s);
+    case 32: return launch_e<32>(p, blocks, s);
+    case 48: return launch_e<48>(p, blocks, s);
+    case 64: return launch_e<64>(p, blocks, s);
+    case 80: return launch_e<80>(p, blocks, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace moe

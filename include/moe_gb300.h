@@ -116,7 +116,10 @@ int32_t moe_gate_up_block(int32_t width);
 /* Router: relay article, architecture paragraph (sigmoid-plus-bias router, top-k)
  * and top-2 paragraph (renormalised gates).
  *   x            [T][d] bf16 or fp32 (shape->x_dtype)
- *   w_router     [E][d] fp32; logits are fp32 dot products (no reduced precision)
+ *   w_router     [E][d] fp32; logits carry fp32 accuracy: with bf16 tokens and
+ *                E in {16, 32, 48, 64, 80} the weight is split exactly into three
+ *                bf16 parts and multiplied on the tensor cores with fp32
+ *                accumulation (every product exact); otherwise fp32 FMA on CUDA cores
  *   logit_offset [E] fp32 added to every logit, or NULL (used by the skewed workload)
  *   bias         [E] fp32, added to the scores for selection only
  *   scores       [T][E] fp32 sigmoid scores, or NULL to skip writing them
@@ -124,10 +127,14 @@ int32_t moe_gate_up_block(int32_t width);
  *                descending key, ties to the lower index
  *   gate         [T][k] fp32: score_j / sum of the k winners' scores (renorm),
  *                else score_j
- *   load         [E] int32: pairs routed to each expert (overwritten). */
+ *   load         [E] int32: pairs routed to each expert (overwritten)
+ *   workspace    moe_route_workspace_size(shape) bytes of scratch (may be NULL when
+ *                that size is 0). */
+size_t moe_route_workspace_size(const moe_shape_t* shape);
 moe_status_t moe_route(const moe_shape_t* shape, const void* x, const float* w_router,
                        const float* logit_offset, const float* bias, float* scores,
-                       int32_t* idx, float* gate, int32_t* load, void* stream);
+                       int32_t* idx, float* gate, int32_t* load, void* workspace,
+                       size_t ws_bytes, void* stream);
 
 /* Stable counting-sort permutation of the (token, slot) pairs by expert.
  *   idx       [T][k] int32 from moe_route (values in [0, E), distinct per row)

@@ -64,7 +64,9 @@ def test_route_matches_oracle(name, kw):
     idx = torch.empty(s.T, s.k, dtype=torch.int32, device=DEV)
     gate = torch.empty(s.T, s.k, dtype=torch.float32, device=DEV)
     load = torch.full((s.E,), -7, dtype=torch.int32, device=DEV)
-    M.moe_route(ms, x, wr, lo, bias, scores, idx, gate, load)
+    nws = M.moe_route_workspace_size(ms)
+    ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=DEV) if nws else None
+    M.moe_route(ms, x, wr, lo, bias, scores, idx, gate, load, ws)
     torch.cuda.synchronize()
     sc = scores.cpu().numpy()
     ref_s = O.router_scores(tokens64(host["x"]), host["w_router"], host["logit_offset"])
