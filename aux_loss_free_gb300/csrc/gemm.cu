@@ -9,8 +9,10 @@
 // Clusters of two CTAs on two SMs compute 256 x BN output tiles with
 // tcgen05.mma.cta_group::2 (M = 256, N = BN <= 256, K = 16):
 //   - each CTA stages its own 128 rows of A and one half (BN/2 rows) of B per
-//     k-block (128-byte swizzle, 6-stage ring of 32 KB); both CTAs' TMA copies
-//     complete on the leader CTA's "full" barrier;
+//     128-wide k-block (two 64-wide 128-byte-swizzle atoms each; 3-stage ring of
+//     64 KB); both CTAs' TMA copies complete on the leader CTA's "full" barrier;
+//     eight MMAs per barrier round keep the issuing thread ahead of the tensor
+//     core (one wait per four MMAs measurably starved it);
 //   - one thread of the leader CTA issues the MMAs; the pair's tensor cores read
 //     the peer's half of B over the cluster, so each SM stages half the B bytes a
 //     single-SM 128 x 256 tile would need;
@@ -39,12 +41,14 @@ namespace {
 
 constexpr int BM = 256;        // rows per CTA-pair tile
 constexpr int HM = 128;        // rows per CTA
-constexpr int BK = 64;
+constexpr int AK = 64;         // K width of one 128-byte swizzle atom (bf16)
+constexpr int BK = 2 * AK;     // K per pipeline stage: 8 MMAs per barrier round
 constexpr int BN_MAX = 256;
-constexpr int STAGES = 6;
-constexpr int A_BYTES = HM * BK * 2;            // 16 KB
-constexpr int B_BYTES = (BN_MAX / 2) * BK * 2;  // 16 KB (one half of B)
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int STAGES = 3;
+constexpr int A_ATOM = HM * AK * 2;               // 16 KB: 128 rows x 64
+constexpr int B_ATOM = (BN_MAX / 2) * AK * 2;     // 16 KB: up to 128 rows (half of B) x 64
+constexpr int A_BYTES = 2 * A_ATOM;
+constexpr int STAGE_BYTES = A_BYTES + 2 * B_ATOM; // 64 KB
 constexpr int EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 2 * BN_MAX;
@@ -308,17 +312,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const OperandSet& S = t.set ? p.routed : p.shared;
         const int nkb = (S.k_total + BK - 1) / BK;
         const int half = S.bn / 2;
-        const uint32_t pair_bytes = 2u * (A_BYTES + half * BK * 2);
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) {
+          if (!mbar_wait_spin(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) {
             ok = false;
             break;
           }
+          // Atoms entirely past K are not loaded (and not multiplied).
+          const int natoms = S.k_total - kb * BK > AK ? 2 : 1;
+          const uint32_t pair_bytes = 2u * natoms * (A_ATOM + half * AK * 2);
           const uint32_t sa = ring + stage * STAGE_BYTES;
           const uint32_t fb = map_to_rank(smem_u32(&full_bar[stage]), 0);
           if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[stage]), pair_bytes);
-          tma_load_2d_pair(sa, &S.a, fb, kb * BK, t.row0 + HM * (int)rank);
-          tma_load_2d_pair(sa + A_BYTES, &S.b, fb, kb * BK, t.brow + half * (int)rank);
+          for (int at = 0; at < natoms; ++at) {
+            tma_load_2d_pair(sa + at * A_ATOM, &S.a, fb, kb * BK + at * AK, t.row0 + HM * (int)rank);
+            tma_load_2d_pair(sa + A_BYTES + at * B_ATOM, &S.b, fb, kb * BK + at * AK,
+                             t.brow + half * (int)rank);
+          }
           issued |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -330,7 +339,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       // The leader's full barriers count both CTAs' copies: wait for all of them.
       if (leader)
         for (int s = 0; s < STAGES; ++s)
-          if ((issued >> s) & 1u) mbar_wait(smem_u32(&full_bar[s]), (last_par >> s) & 1u, p.status);
+          if ((issued >> s) & 1u) mbar_wait_spin(smem_u32(&full_bar[s]), (last_par >> s) & 1u, p.status);
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
@@ -343,22 +352,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const OperandSet& S = t.set ? p.routed : p.shared;
         const int nkb = (S.k_total + BK - 1) / BK;
         const uint32_t idesc = idesc_bf16_f32(BM, S.bn);
-        if (!mbar_wait(smem_u32(&tempty_bar[acc]), acc_phase ^ 1u, p.status)) break;
+        if (!mbar_wait_spin(smem_u32(&tempty_bar[acc]), acc_phase ^ 1u, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN_MAX;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(smem_u32(&full_bar[stage]), phase, p.status)) {
+          if (!mbar_wait_spin(smem_u32(&full_bar[stage]), phase, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t sa = ring + stage * STAGE_BYTES;
-          const uint64_t adesc = sw128_kmajor_desc(sa);
-          const uint64_t bdesc = sw128_kmajor_desc(sa + A_BYTES);
           const int kleft = S.k_total - kb * BK;
           const int nkk = kleft >= BK ? BK / 16 : (kleft + 15) / 16;
-          for (int kk = 0; kk < nkk; ++kk)
-            mma_pair_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+          for (int kk = 0; kk < nkk; ++kk) {
+            const int at = kk >> 2, w = kk & 3;
+            const uint64_t adesc = sw128_kmajor_desc(sa + at * A_ATOM);
+            const uint64_t bdesc = sw128_kmajor_desc(sa + A_BYTES + at * B_ATOM);
+            mma_pair_bf16(d_tmem, adesc + 2 * w, bdesc + 2 * w, idesc, (kb | kk) != 0);
+          }
           commit_pair_multicast(smem_u32(&empty_bar[stage]));
           if (++stage == STAGES) {
             stage = 0;
@@ -476,13 +487,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 matrix [outer][inner] row-major, box [box_outer][64] with the 128-byte swizzle.
+// bf16 matrix [outer][inner] row-major, box [box_outer][64] (one swizzle atom) with the
+// 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {inner * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_outer};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(AK), box_outer};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
