@@ -48,17 +48,17 @@ cudaError_t launch_router_tc(const RouterArgs& a, void* w3_scratch, cudaStream_t
 // ---------------------------------------------------------------- permutation
 cudaError_t launch_count(const int32_t* idx, int T, int k, int E, int chunk_tokens,
                          int32_t* counts, cudaStream_t s);
-// counts [chunks][E] -> bases [chunks][E] (row of each chunk's first pair of
-// each expert), offsets [E+1], optional load [E] and optional bias update.
-cudaError_t launch_scan(const int32_t* counts, int chunks, int E, int32_t* bases,
-                        int32_t* offsets, int32_t* load_out, float* bias, float gamma,
-                        long long tokens_times_k, cudaStream_t s);
-// Scatter pairs to their rows; optionally gather x rows into xp (bf16) and write
-// a bf16 copy of x (xb, for fp32 x) at the same time.
-cudaError_t launch_scatter(const int32_t* idx, const int32_t* bases, int T, int k, int E,
-                           int chunk_tokens, int32_t* perm_tok, int32_t* inv_pos,
-                           const void* x, int x_is_f32, int d, uint16_t* xp, uint16_t* xb,
-                           cudaStream_t s);
+// Whole permutation from the per-chunk count table [chunks][E]: expert offsets
+// [E+1], perm_tok, inv_pos; block 0 also writes load_out [E] and applies the bias
+// update when those pointers are set.  Optionally gathers x rows into xp (bf16) and
+// writes a bf16 copy of x into xb (fp32 x).  Blocks of 32 tokens when a chunk holds
+// at most 128 tokens (a block recounts the earlier blocks of its chunk), else one
+// block per chunk.
+cudaError_t launch_scatter(const int32_t* idx, const int32_t* counts, int T, int k, int E,
+                           int chunk_tokens, int32_t* offsets, int32_t* load_out, float* bias,
+                           float gamma, long long tokens_times_k, int32_t* perm_tok,
+                           int32_t* inv_pos, const void* x, int x_is_f32, int d, uint16_t* xp,
+                           uint16_t* xb, cudaStream_t s);
 cudaError_t launch_gather(const void* x, int x_is_f32, const int32_t* perm_tok, long long rows,
                           int d, uint16_t* xp, cudaStream_t s);
 cudaError_t launch_to_bf16(const float* x, long long n, uint16_t* xb, cudaStream_t s);

@@ -59,8 +59,8 @@ struct Carver {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // ---------------------------------------------------------------- stage profiler
-constexpr int kStages = 6;
-const char* const kStageNames[kStages] = {"router", "scan", "scatter_gather", "gemm_gate_up",
+constexpr int kStages = 5;
+const char* const kStageNames[kStages] = {"router", "permute_gather", "gemm_gate_up",
                                           "gemm_down_routed", "gemm_down_shared_combine"};
 struct Profiler {
   std::mutex mu;
@@ -107,16 +107,23 @@ int chunks_of(const moe_shape_t* s, int* chunk_tokens) {
   return (s->T + *chunk_tokens - 1) / *chunk_tokens;
 }
 
+// Layer path: the tensor-core router counts per CTA of 128 tokens, so its chunks are
+// at least 128 tokens (and still keep the count table within kMaxCountEntries).
+int layer_chunks_of(const moe_shape_t* s, int* chunk_tokens) {
+  int ct = permute_chunk_tokens(s->T, s->E);
+  if (router_tc_supported(s->E, s->x_dtype == MOE_X_F32) && ct < 128) ct = 128;
+  *chunk_tokens = ct;
+  return (s->T + ct - 1) / ct;
+}
+
 struct PermuteWs {
-  int32_t* counts;
-  int32_t* bases;
+  int32_t* counts;  // [chunks][E] pairs per (token chunk, expert)
 };
 PermuteWs carve_permute(Carver& c, const moe_shape_t* s) {
   int ct;
   const int chunks = chunks_of(s, &ct);
   PermuteWs w;
   w.counts = static_cast<int32_t*>(c.take(sizeof(int32_t) * chunks * s->E));
-  w.bases = static_cast<int32_t*>(c.take(sizeof(int32_t) * chunks * s->E));
   return w;
 }
 
@@ -190,14 +197,14 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x_bf16, const int32_t* of
     if (comb) s2 = GemmOperandSet{ws.hs, s->T, w->shared_down, 1, s->d, s->F, out, s->d, EPI_COMBINE, s->T};
     else s2 = GemmOperandSet{ws.hs, s->T, w->shared_down, 1, s->d, s->F, shared_out, s->d, EPI_STORE, s->T};
   }
-  if (mark) prof_mark(4, st);
+  if (mark) prof_mark(3, st);
   if (comb && s->F) {
     // The combine epilogue reads y_perm, so the routed down projection runs first.
     GemmOperandSet off{};
     e = launch_grouped_gemm(r2, offsets, s->E, off, none, Tk, st, &bad);
     if (bad) return MOE_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return MOE_ERR_CUDA;
-    if (mark) prof_mark(5, st);
+    if (mark) prof_mark(4, st);
     e = launch_grouped_gemm(off, offsets, s->E, s2, *comb, Tk, st, &bad);
   } else {
     e = launch_grouped_gemm(r2, offsets, s->E, s2, none, Tk, st, &bad);
@@ -205,7 +212,7 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x_bf16, const int32_t* of
   if (bad) return MOE_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (comb && !s->F) {
-    if (mark) prof_mark(5, st);
+    if (mark) prof_mark(4, st);
     e = launch_combine(y_perm, nullptr, comb->inv_pos, comb->gate, comb->residual, out, s->T,
                        s->k, s->d, st);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -295,10 +302,8 @@ moe_status_t moe_permute(const moe_shape_t* shape, const int32_t* idx, int32_t* 
     return MOE_ERR_CUDA;
   cudaError_t e = launch_count(idx, shape->T, shape->k, shape->E, ct, w.counts, s);
   if (e == cudaSuccess)
-    e = launch_scan(w.counts, chunks, shape->E, w.bases, offsets, nullptr, nullptr, 0.f, 0, s);
-  if (e == cudaSuccess)
-    e = launch_scatter(idx, w.bases, shape->T, shape->k, shape->E, ct, perm_tok, inv_pos,
-                       nullptr, 0, shape->d, nullptr, nullptr, s);
+    e = launch_scatter(idx, w.counts, shape->T, shape->k, shape->E, ct, offsets, nullptr, nullptr,
+                       0.f, 0, perm_tok, inv_pos, nullptr, 0, shape->d, nullptr, nullptr, s);
   return cuda_status(e);
 }
 
@@ -393,7 +398,7 @@ moe_status_t moe_layer_fwd(const moe_shape_t* shape, const void* x, const float*
   }
   const int T = shape->T, E = shape->E, k = shape->k;
   int ct;
-  const int chunks = chunks_of(shape, &ct);
+  const int chunks = layer_chunks_of(shape, &ct);
   const int xf = shape->x_dtype == MOE_X_F32;
 
   prof_mark(0, s);
@@ -404,14 +409,14 @@ moe_status_t moe_layer_fwd(const moe_shape_t* shape, const void* x, const float*
                 L.load, L.perm.counts, ct, T, shape->d, E, k, shape->renorm};
   cudaError_t e = run_router(ra, L.router, s);
   prof_mark(1, s);
+  // The scatter launch derives the offsets from the counts and applies the bias
+  // update (after the router has read the bias).
   if (e == cudaSuccess)
-    e = launch_scan(L.perm.counts, chunks, E, L.perm.bases, L.offsets, nullptr,
-                    update_bias ? bias : nullptr, gamma, (long long)T * k, s);
+    e = launch_scatter(L.idx, L.perm.counts, T, k, E, ct, L.offsets, nullptr,
+                       update_bias ? bias : nullptr, gamma, (long long)T * k, L.perm_tok,
+                       L.inv_pos, x, xf, shape->d, L.ffn.xp, (xf && shape->F) ? L.ffn.xb : nullptr,
+                       s);
   prof_mark(2, s);
-  if (e == cudaSuccess)
-    e = launch_scatter(L.idx, L.perm.bases, T, k, E, ct, L.perm_tok, L.inv_pos, x, xf, shape->d,
-                       L.ffn.xp, (xf && shape->F) ? L.ffn.xb : nullptr, s);
-  prof_mark(3, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   const void* xbf = xf ? L.ffn.xb : x;
   CombineInputs comb{L.y, L.inv_pos, L.gate, static_cast<const uint16_t*>(residual), k};

@@ -1,12 +1,11 @@
 // Token permutation (stable counting sort by expert), row gather, combine, bias
 // update and weight packing.
 //
-// Counting sort in three launches: per-chunk expert counts (the router produces
-// them on the fused path), one block that scans the chunk table into per-chunk
-// bases and the expert offsets, and a scatter in which each chunk's pairs are ranked
-// in (token, slot) order with a warp match, which keeps tokens ascending inside
-// every expert's block.  The scatter also gathers the token rows (16-byte vectors)
-// into the permuted activation buffer the grouped GEMM reads.
+// Counting sort in two launches: per-chunk expert counts (the router produces them
+// on the fused path) and one scatter launch in which every block derives its
+// chunk's bases from the count table and ranks its pairs (see scatter_kernel).  The
+// scatter also gathers the token rows into the permuted activation buffer the
+// grouped GEMM reads.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -50,60 +49,73 @@ __global__ void count_kernel(const int32_t* __restrict__ idx, int T, int k, int 
   atomicAdd(&counts[(long long)(t / chunk_tokens) * E + idx[p]], 1);
 }
 
-// One block.  counts [chunks][E] -> bases [chunks][E] = offsets[e] + sum of the
-// counts of e in earlier chunks.
-__global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ counts, int chunks,
-                                                    int E, int32_t* __restrict__ bases,
-                                                    int32_t* __restrict__ offsets,
-                                                    int32_t* __restrict__ load_out, float* bias,
-                                                    float gamma, long long tokens_times_k) {
-  extern __shared__ int32_t sm[];
-  int32_t* c = sm;                        // [chunks][E]
-  int32_t* segsum = c + chunks * E;       // [nseg][E]
-  __shared__ int32_t total[kMaxE];
+constexpr int SC_THREADS = 256;
+constexpr int SC_ROUND = 256;  // pairs ranked per round (8 warp batches)
+
+// One launch does the whole permutation from the per-chunk count table:
+//  1. every block reads the table (a few KB, one batched L2 round trip) and forms,
+//     for each expert, the pairs of earlier chunks and the expert totals; the
+//     totals' exclusive scan gives the expert offsets (block 0 also writes them,
+//     the loads and, if asked, the bias update);
+//  2. a block of 32 tokens adds the pairs of the earlier blocks of its chunk;
+//  3. the block ranks its own pairs in (token, slot) order with a warp match, which
+//     keeps tokens ascending inside every expert's rows, writes perm_tok / inv_pos
+//     and gathers the token rows (16-byte vectors) into the permuted activations.
+__global__ void __launch_bounds__(SC_THREADS) scatter_kernel(
+    const int32_t* __restrict__ idx, const int32_t* __restrict__ counts, int chunks, int T, int k,
+    int E, int chunk_tokens, int32_t* __restrict__ offsets, int32_t* __restrict__ load_out,
+    float* bias, float gamma, long long tokens_times_k, int32_t* __restrict__ perm_tok,
+    int32_t* __restrict__ inv_pos, const void* __restrict__ x, int x_is_f32, int d,
+    uint16_t* __restrict__ xp, uint16_t* __restrict__ xb) {
+  __shared__ int32_t run[kMaxE];
+  __shared__ int32_t tot_e[kMaxE];
   __shared__ int32_t off[kMaxE + 1];
-  const int tid = threadIdx.x;
-  {
-    // Issue every load before the first shared-memory store (one memory round trip).
-    constexpr int PER = kMaxCountEntries / 1024;
-    const int n = chunks * E;
-    int v[PER];
+  __shared__ int32_t part_pre[SC_THREADS];
+  __shared__ int32_t part_tot[SC_THREADS];
+  __shared__ int32_t s_pos[SC_ROUND];
+  __shared__ int32_t s_tok[SC_ROUND];
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int block_tokens = chunk_tokens <= 128 ? 32 : chunk_tokens;
+  const long long t_begin = (long long)blockIdx.x * block_tokens;
+  const long long chunk = t_begin / chunk_tokens;
+  const long long p_begin = t_begin * k;
+  const long long p_end = min((long long)T * k, p_begin + (long long)block_tokens * k);
+
+  // ---- 1. chunk prefix and totals per expert
+  const int parts = SC_THREADS / E;
+  const int e = tid % E, part = tid / E;
+  if (part < parts) {
+    const int L = (chunks + parts - 1) / parts;
+    const int lo = part * L, hi = min(chunks, lo + L);
+    int pre = 0, tot = 0;
+    for (int c0 = lo; c0 < hi; c0 += 16) {
+      int v[16];
 #pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      const int i = j * 1024 + tid;
-      v[j] = i < n ? counts[i] : 0;
-    }
+      for (int j = 0; j < 16; ++j) v[j] = (c0 + j < hi) ? __ldcg(&counts[(long long)(c0 + j) * E + e]) : 0;
 #pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      const int i = j * 1024 + tid;
-      if (i < n) c[i] = v[j];
+      for (int j = 0; j < 16; ++j) {
+        tot += v[j];
+        if (c0 + j < chunk) pre += v[j];
+      }
     }
-  }
-  const int nseg = blockDim.x / E;
-  const int L = (chunks + nseg - 1) / nseg;
-  __syncthreads();
-  const int e = tid % E, sg = tid / E;
-  if (sg < nseg) {
-    int sum = 0;
-    const int lo = sg * L, hi = min(chunks, lo + L);
-    for (int ch = lo; ch < hi; ++ch) sum += c[ch * E + e];
-    segsum[sg * E + e] = sum;
+    part_pre[part * E + e] = pre;
+    part_tot[part * E + e] = tot;
   }
   __syncthreads();
   if (tid < E) {
-    int run = 0;
-    for (int s = 0; s < nseg; ++s) {
-      const int v = segsum[s * E + tid];
-      segsum[s * E + tid] = run;
-      run += v;
+    int pre = 0, tot = 0;
+    for (int q = 0; q < parts; ++q) {
+      pre += part_pre[q * E + tid];
+      tot += part_tot[q * E + tid];
     }
-    total[tid] = run;
+    run[tid] = pre;
+    tot_e[tid] = tot;
   }
   __syncthreads();
-  if (tid < 32) {  // exclusive scan of total over experts, 32 at a time
+  if (tid < 32) {  // exclusive scan of the totals over experts, 32 at a time
     int carry = 0;
     for (int b = 0; b < E; b += 32) {
-      const int v = (b + tid < E) ? total[b + tid] : 0;
+      const int v = (b + tid < E) ? tot_e[b + tid] : 0;
       int incl = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -116,55 +128,38 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
     if (tid == 0) off[E] = carry;
   }
   __syncthreads();
-  if (sg < nseg) {
-    int run = off[e] + segsum[sg * E + e];
-    const int lo = sg * L, hi = min(chunks, lo + L);
-    for (int ch = lo; ch < hi; ++ch) {
-      bases[ch * E + e] = run;
-      run += c[ch * E + e];
+  if (tid < E) run[tid] += off[tid];
+  if (blockIdx.x == 0) {
+    for (int i = tid; i <= E; i += SC_THREADS) offsets[i] = off[i];
+    if (tid < E) {
+      if (load_out) load_out[tid] = tot_e[tid];
+      if (bias) {
+        // Aux-loss-free update: sign(T*k - E*load) is sign(target - load), sign(0) = 0.
+        const long long diff = tokens_times_k - (long long)E * tot_e[tid];
+        const float step = diff > 0 ? gamma : (diff < 0 ? -gamma : 0.f);
+        bias[tid] = __fadd_rn(bias[tid], step);
+      }
     }
   }
-  for (int i = tid; i <= E; i += blockDim.x) offsets[i] = off[i];
-  if (tid < E) {
-    if (load_out) load_out[tid] = total[tid];
-    if (bias) {
-      // Aux-loss-free update: sign(T*k - E*load) is sign(target - load), sign(0) = 0.
-      const long long diff = tokens_times_k - (long long)E * total[tid];
-      const float step = diff > 0 ? gamma : (diff < 0 ? -gamma : 0.f);
-      bias[tid] = __fadd_rn(bias[tid], step);
-    }
-  }
-}
-
-constexpr int SC_THREADS = 256;
-constexpr int SC_ROUND = 256;  // pairs ranked per round (8 warp batches)
-
-__global__ void __launch_bounds__(SC_THREADS) scatter_kernel(
-    const int32_t* __restrict__ idx, const int32_t* __restrict__ bases, int T, int k, int E,
-    int chunk_tokens, int32_t* __restrict__ perm_tok, int32_t* __restrict__ inv_pos,
-    const void* __restrict__ x, int x_is_f32, int d, uint16_t* __restrict__ xp,
-    uint16_t* __restrict__ xb) {
-  __shared__ int32_t run[kMaxE];
-  __shared__ int32_t s_pos[SC_ROUND];
-  __shared__ int32_t s_tok[SC_ROUND];
-  const int chunk = blockIdx.x;
-  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const long long p_begin = (long long)chunk * chunk_tokens * k;
-  const long long p_end = min((long long)T * k, p_begin + (long long)chunk_tokens * k);
-  for (int e = tid; e < E; e += SC_THREADS) run[e] = bases[(long long)chunk * E + e];
   __syncthreads();
+
+  // ---- 2. pairs of the earlier blocks of the same chunk come first
+  for (long long q = chunk * chunk_tokens * k + tid; q < p_begin; q += SC_THREADS)
+    atomicAdd(&run[idx[q]], 1);
+  __syncthreads();
+
+  // ---- 3. rank, scatter, gather
   for (long long r0 = p_begin; r0 < p_end; r0 += SC_ROUND) {
     const int n = (int)min((long long)SC_ROUND, p_end - r0);
     if (warp == 0) {
       for (int b = 0; b < n; b += 32) {
         const int q = b + lane;
         const bool valid = q < n;
-        const int e = valid ? idx[r0 + q] : -1;
-        const unsigned peers = __match_any_sync(FULL, e);
+        const int ex = valid ? idx[r0 + q] : -1;
+        const unsigned peers = __match_any_sync(FULL, ex);
         const int rank = __popc(peers & ((1u << lane) - 1u));
-        int pos = 0;
         if (valid) {
-          pos = run[e] + rank;
+          const int pos = run[ex] + rank;
           const long long pr = r0 + q;
           const int t = (int)(pr / k);
           perm_tok[pos] = t;
@@ -173,7 +168,7 @@ __global__ void __launch_bounds__(SC_THREADS) scatter_kernel(
           s_tok[q] = (pr % k == 0) ? t : -1 - t;  // slot 0 marks the token's first pair
         }
         __syncwarp();
-        if (valid && lane == __ffs(peers) - 1) run[e] += __popc(peers);
+        if (valid && lane == __ffs(peers) - 1) run[ex] += __popc(peers);
         __syncwarp();
       }
     }
@@ -271,26 +266,16 @@ cudaError_t launch_count(const int32_t* idx, int T, int k, int E, int chunk_toke
   return cudaGetLastError();
 }
 
-cudaError_t launch_scan(const int32_t* counts, int chunks, int E, int32_t* bases,
-                        int32_t* offsets, int32_t* load_out, float* bias, float gamma,
-                        long long tokens_times_k, cudaStream_t s) {
-  const int threads = 1024;
-  const int nseg = threads / E;
-  const size_t dyn = sizeof(int32_t) * ((size_t)chunks * E + (size_t)nseg * E);
-  cudaError_t e =
-      cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
-  if (e != cudaSuccess) return e;
-  scan_kernel<<<1, threads, dyn, s>>>(counts, chunks, E, bases, offsets, load_out, bias, gamma,
-                                      tokens_times_k);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_scatter(const int32_t* idx, const int32_t* bases, int T, int k, int E,
-                           int chunk_tokens, int32_t* perm_tok, int32_t* inv_pos,
-                           const void* x, int x_is_f32, int d, uint16_t* xp, uint16_t* xb,
-                           cudaStream_t s) {
+cudaError_t launch_scatter(const int32_t* idx, const int32_t* counts, int T, int k, int E,
+                           int chunk_tokens, int32_t* offsets, int32_t* load_out, float* bias,
+                           float gamma, long long tokens_times_k, int32_t* perm_tok,
+                           int32_t* inv_pos, const void* x, int x_is_f32, int d, uint16_t* xp,
+                           uint16_t* xb, cudaStream_t s) {
   const int chunks = (T + chunk_tokens - 1) / chunk_tokens;
-  scatter_kernel<<<chunks, SC_THREADS, 0, s>>>(idx, bases, T, k, E, chunk_tokens, perm_tok,
+  const int block_tokens = chunk_tokens <= 128 ? 32 : chunk_tokens;
+  const int blocks = (T + block_tokens - 1) / block_tokens;
+  scatter_kernel<<<blocks, SC_THREADS, 0, s>>>(idx, counts, chunks, T, k, E, chunk_tokens, offsets,
+                                               load_out, bias, gamma, tokens_times_k, perm_tok,
                                                inv_pos, x, x_is_f32, d, xp, xb);
   return cudaGetLastError();
 }

@@ -6,10 +6,10 @@
 // not own, a serving loop whose device-memory budget is fixed at start-up, or a
 // caller about to record its launches into a CUDA graph where a fresh cudaMalloc is
 // not allowed.  Those callers still pass their inputs and outputs; the per-chunk
-// count and base tables live in the file-scope array below instead of a workspace.
+// count table lives in the file-scope array below instead of a workspace.
 //
 // The array is a static __device__ symbol: every GPU that loads this library holds
-// its 256 KiB until the process exits.  Host code must not pass the symbol itself
+// its 128 KiB until the process exits.  Host code must not pass the symbol itself
 // to a kernel (on the host it is only a stand-in, not a device address); the device
 // address is looked up once per device with cudaGetSymbolAddress and cached.
 #include <cuda_runtime.h>
@@ -22,8 +22,8 @@
 namespace moe {
 namespace {
 
-// Two tables (counts, bases) of at most kMaxCountEntries int32 each.
-constexpr size_t kNoAllocScratchInts = 2 * (size_t)kMaxCountEntries;
+// The count table: at most kMaxCountEntries int32.
+constexpr size_t kNoAllocScratchInts = (size_t)kMaxCountEntries;
 static __device__ __align__(256) int32_t g_permute_scratch[kNoAllocScratchInts];
 
 // Device address of g_permute_scratch on the current device, looked up on the first
@@ -58,19 +58,16 @@ extern "C" moe_status_t moe_permute_noalloc(const moe_shape_t* shape, const int3
   const int ct = permute_chunk_tokens(shape->T, shape->E);
   const int chunks = (shape->T + ct - 1) / ct;
   const size_t table = (size_t)chunks * shape->E;
-  if (2 * table > kNoAllocScratchInts) return MOE_ERR_UNSUPPORTED;  // beyond the fixed scratch
+  if (table > kNoAllocScratchInts) return MOE_ERR_UNSUPPORTED;  // beyond the fixed scratch
   int32_t* scratch = scratch_on_current_device();
   if (!scratch) return MOE_ERR_CUDA;
   int32_t* counts = scratch;
-  int32_t* bases = scratch + table;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The array keeps the previous call's contents: the count table must start at zero.
   if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * table, s) != cudaSuccess) return MOE_ERR_CUDA;
   cudaError_t e = launch_count(idx, shape->T, shape->k, shape->E, ct, counts, s);
   if (e == cudaSuccess)
-    e = launch_scan(counts, chunks, shape->E, bases, offsets, nullptr, nullptr, 0.f, 0, s);
-  if (e == cudaSuccess)
-    e = launch_scatter(idx, bases, shape->T, shape->k, shape->E, ct, perm_tok, inv_pos, nullptr,
-                       0, shape->d, nullptr, nullptr, s);
+    e = launch_scatter(idx, counts, shape->T, shape->k, shape->E, ct, offsets, nullptr, nullptr,
+                       0.f, 0, perm_tok, inv_pos, nullptr, 0, shape->d, nullptr, nullptr, s);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

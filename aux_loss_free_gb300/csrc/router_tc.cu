@@ -11,11 +11,12 @@
 // x * W_part is exact in fp32 and the tensor core accumulates in fp32: the logits
 // carry fp32 accuracy (no reduced-precision weights, no TF32).  One CTA owns 128
 // tokens: a TMA producer streams 128 x 64 token tiles and 3E x 64 weight tiles
-// through a 4-stage ring, one thread issues tcgen05.mma (M = 128, N = 3E, K = 16)
-// into TMEM, and then each of the 128 threads owns one token: it reads its 3E
-// accumulator columns, forms the E logits, applies the sigmoid, selects the top-k
-// by fl32(score + bias) with ties to the lower index, computes the gates and counts
-// its experts into a per-warp shared-memory histogram.
+// through a 4-stage ring (the CTA's whole token slab is prefetched into L2 first),
+// one thread issues tcgen05.mma (M = 128, N = 3E, K = 16) into TMEM, and then two
+// threads per token read its 3E accumulator columns (one half of the experts
+// each), form the logits, apply the sigmoid, keep their best k by fl32(score +
+// bias) with ties to the lower index, and merge the two lists; the gates and the
+// per-warp shared-memory histogram follow.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -33,7 +34,7 @@ constexpr int RBM = 128;
 constexpr int RBK = 64;
 constexpr int RSTAGES = 4;
 constexpr int A_BYTES = RBM * RBK * 2;
-constexpr int RTHREADS = 128;
+constexpr int RTHREADS = 256;  // 8 warps: two threads per token in the epilogue
 constexpr unsigned FULL = 0xFFFFFFFFu;
 
 struct RouterTcParams {
@@ -71,6 +72,9 @@ __global__ void __launch_bounds__(RTHREADS, 1) router_tc_kernel(const __grid_con
   __shared__ float s_bias[E];
   __shared__ float s_off[E];
   __shared__ int hist[4][E];
+  __shared__ float cand_key[2][RBM][kMaxK];
+  __shared__ int cand_e[2][RBM][kMaxK];
+  __shared__ float cand_s[2][RBM][kMaxK];
 
   constexpr int N = 3 * E;
   constexpr uint32_t TCOLS = N <= 32 ? 32 : (N <= 64 ? 64 : (N <= 128 ? 128 : 256));
@@ -104,12 +108,15 @@ __global__ void __launch_bounds__(RTHREADS, 1) router_tc_kernel(const __grid_con
   const int nkb = p.d / RBK;
 
   if (warp == 0 && lane == 0) {
+    // The token slab is read once, from DRAM: ask for all of it up front so the
+    // ring below is fed from L2 instead of paying DRAM latency per stage.
+    for (int kb = 0; kb < nkb; ++kb) tma_prefetch_l2_2d(&p.x_map, kb * RBK, t0);
     const uint32_t bytes = A_BYTES + N * RBK * 2;
     uint32_t issued = 0, last_par = 0;
     int stage = 0;
     uint32_t phase = 0;
     for (int kb = 0; kb < nkb; ++kb) {
-      if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) break;
+      if (!mbar_wait_spin(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) break;
       const uint32_t sa = ring + stage * p.stage_bytes;
       const uint32_t fb = smem_u32(&full_bar[stage]);
       mbar_arrive_expect_tx(fb, bytes);
@@ -123,14 +130,14 @@ __global__ void __launch_bounds__(RTHREADS, 1) router_tc_kernel(const __grid_con
       }
     }
     for (int s = 0; s < RSTAGES; ++s)
-      if ((issued >> s) & 1u) mbar_wait(smem_u32(&full_bar[s]), (last_par >> s) & 1u, p.status);
+      if ((issued >> s) & 1u) mbar_wait_spin(smem_u32(&full_bar[s]), (last_par >> s) & 1u, p.status);
   } else if (warp == 1 && lane == 0) {
     constexpr uint32_t idesc = idesc_bf16_f32(RBM, N);
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
     for (int kb = 0; kb < nkb && ok; ++kb) {
-      if (!mbar_wait(smem_u32(&full_bar[stage]), phase, p.status)) {
+      if (!mbar_wait_spin(smem_u32(&full_bar[stage]), phase, p.status)) {
         ok = false;
         break;
       }
@@ -152,38 +159,76 @@ __global__ void __launch_bounds__(RTHREADS, 1) router_tc_kernel(const __grid_con
   __syncwarp();
 
   // ------------------------------------------------------------ per-token epilogue
+  // Warps w and w + 4 own the same 32 TMEM lanes (tokens); warp w takes experts
+  // [0, EH), warp w + 4 experts [EH, E).  Each thread forms its experts' scores,
+  // keeps its best k by (key desc, index asc), and the two lists are merged.
   int ok = 1;
   if (lane == 0) ok = mbar_wait(smem_u32(&tfull_bar), 0, p.status) ? 1 : 0;
   ok = __shfl_sync(FULL, ok, 0);
   tc_fence_after();
-  const int row = warp * 32 + lane;
+  constexpr int EH = ((E / 2 + 15) / 16) * 16;
+  const int q = warp & 3, h = warp >> 2;
+  const int row = q * 32 + lane;
   const int t = t0 + row;
   const bool valid = ok && t < p.T;
-  const uint32_t tl = tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
-  float s[E];
+  const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+  const int e_lo = h ? EH : 0, e_hi = h ? E : EH;
+  float s[EH];
 #pragma unroll
-  for (int c = 0; c < E; c += 16) {
-    uint32_t h[16], m[16], l[16];
-    tmem_ld16(tl + c, h);
-    tmem_ld16(tl + E + c, m);
-    tmem_ld16(tl + 2 * E + c, l);
-    tmem_wait_ld();
+  for (int c = 0; c < EH; c += 16) {
+    if (e_lo + c < e_hi) {  // warp-uniform
+      uint32_t hv[16], mv[16], lv[16];
+      tmem_ld16(tl + e_lo + c, hv);
+      tmem_ld16(tl + E + e_lo + c, mv);
+      tmem_ld16(tl + 2 * E + e_lo + c, lv);
+      tmem_wait_ld();
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float z = (__uint_as_float(h[i]) + __uint_as_float(m[i])) + __uint_as_float(l[i]) +
-                      s_off[c + i];
-      s[c + i] = 1.0f / (1.0f + expf(-z));
+      for (int i = 0; i < 16; ++i) {
+        const float z = (__uint_as_float(hv[i]) + __uint_as_float(mv[i])) + __uint_as_float(lv[i]) +
+                        s_off[e_lo + c + i];
+        // Branch-free sigmoid; saturates to exactly 0 / 1 for extreme logits.
+        s[c + i] = __fdividef(1.0f, 1.0f + __expf(-z));
+      }
     }
   }
+  const int nmine = e_hi - e_lo;
+  const int kk = min(p.k, nmine);
   if (valid) {
     if (p.scores) {
-      float4* dst = reinterpret_cast<float4*>(p.scores + (size_t)t * E);
+      float4* dst = reinterpret_cast<float4*>(p.scores + (size_t)t * E + e_lo);
 #pragma unroll
-      for (int i = 0; i < E / 4; ++i) dst[i] = make_float4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]);
+      for (int i = 0; i < EH / 4; ++i)
+        if (4 * i < nmine) dst[i] = make_float4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]);
     }
-    uint32_t taken[(E + 31) / 32];
+    uint64_t taken = 0;
 #pragma unroll
-    for (int i = 0; i < (E + 31) / 32; ++i) taken[i] = 0;
+    for (int j = 0; j < kMaxK; ++j) {
+      if (j < kk) {
+        float bk = -INFINITY, bs = 0.f;
+        int be = -1;
+#pragma unroll
+        for (int i = 0; i < EH; ++i) {
+          if (i < nmine && !((taken >> i) & 1ull)) {
+            const float key = __fadd_rn(s[i], s_bias[e_lo + i]);
+            if (be < 0 || key > bk) {
+              bk = key;
+              be = i;
+              bs = s[i];
+            }
+          }
+        }
+        taken |= 1ull << be;
+        cand_key[h][row][j] = bk;
+        cand_e[h][row][j] = e_lo + be;
+        cand_s[h][row][j] = bs;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (valid && h == 0) {
+    const int na = min(p.k, EH), nb = min(p.k, E - EH);
+    int ia = 0, ib = 0;
     float sel_s[kMaxK];
     int sel_e[kMaxK];
     float denom = 0.f;
@@ -192,25 +237,23 @@ __global__ void __launch_bounds__(RTHREADS, 1) router_tc_kernel(const __grid_con
       sel_s[j] = 0.f;
       sel_e[j] = 0;
       if (j < p.k) {
-        float bk = -INFINITY, bs = 0.f;
-        int be = -1;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          if (!((taken[e / 32] >> (e % 32)) & 1u)) {
-            const float key = __fadd_rn(s[e], s_bias[e]);
-            if (be < 0 || key > bk) {
-              bk = key;
-              be = e;
-              bs = s[e];
-            }
-          }
+        bool take_a;
+        if (ia >= na) take_a = false;
+        else if (ib >= nb) take_a = true;
+        else {
+          const float ka = cand_key[0][row][ia], kb = cand_key[1][row][ib];
+          take_a = ka > kb || (ka == kb && cand_e[0][row][ia] < cand_e[1][row][ib]);
         }
-#pragma unroll
-        for (int i = 0; i < (E + 31) / 32; ++i)
-          if (i == be / 32) taken[i] |= 1u << (be % 32);
-        sel_s[j] = bs;
-        sel_e[j] = be;
-        denom += bs;
+        if (take_a) {
+          sel_e[j] = cand_e[0][row][ia];
+          sel_s[j] = cand_s[0][row][ia];
+          ++ia;
+        } else {
+          sel_e[j] = cand_e[1][row][ib];
+          sel_s[j] = cand_s[1][row][ib];
+          ++ib;
+        }
+        denom += sel_s[j];
       }
     }
 #pragma unroll
@@ -218,11 +261,10 @@ __global__ void __launch_bounds__(RTHREADS, 1) router_tc_kernel(const __grid_con
       if (j < p.k) {
         p.idx[(size_t)t * p.k + j] = sel_e[j];
         p.gate[(size_t)t * p.k + j] = p.renorm ? __fdiv_rn(sel_s[j], denom) : sel_s[j];
-        atomicAdd(&hist[warp][sel_e[j]], 1);
+        atomicAdd(&hist[q][sel_e[j]], 1);
       }
     }
   }
-  tc_fence_before();
   __syncthreads();
   // Each warp's 32 tokens lie in one permutation chunk (chunks are multiples of 32).
   for (int i = threadIdx.x; i < 4 * E; i += RTHREADS) {

@@ -42,7 +42,7 @@ FLUSH_BYTES = 512 << 20
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_gate_up_nano_traffic.txt")
-KERNELS_PER_CALL = 6  # router, scan, scatter+gather, gate/up GEMM, 2 down GEMMs (or combine)
+KERNELS_PER_CALL = 6  # router weight split, router, permute+gather, gate/up GEMM, 2 down GEMMs
 
 
 def parse_args():

@@ -153,9 +153,9 @@ moe_status_t moe_permute(const moe_shape_t* shape, const int32_t* idx, int32_t* 
  * into a CUDA graph where a new cudaMalloc is not allowed.  The pages have no
  * counterpart to this call; it computes exactly what moe_permute computes.
  * Arguments as moe_permute (idx, offsets, perm_tok, inv_pos are caller-owned).
- * Scratch: a library-owned static device array of 2 x 32768 int32 (256 KiB), held
- * by every GPU that loads the library until the process exits.  Every supported
- * shape fits (the chunking keeps each table within 32768 entries); a shape that
+ * Scratch: a library-owned static device array of 32768 int32 (128 KiB), held by
+ * every GPU that loads the library until the process exits.  Every supported shape
+ * fits (the chunking keeps the count table within 32768 entries); a shape that
  * would not fit returns MOE_ERR_UNSUPPORTED before any launch.  The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress, with that
  * device current) and caches it: make that first call before any stream capture.
@@ -226,8 +226,8 @@ moe_status_t moe_quantize_int4(int64_t rows, int32_t K, const void* w, void* q, 
 
 /* Per-stage timing of moe_layer_fwd (profiling aid).  While enabled, every
  * moe_layer_fwd call records CUDA events on its stream between its stages (router,
- * permutation scan, scatter + gather, gate/up GEMM, routed down GEMM, shared down
- * GEMM with the fused combine).  moe_profile_start(max_calls) enables it for up to
+ * permutation + gather, gate/up GEMM, routed down GEMM, shared down GEMM with the
+ * fused combine).  moe_profile_start(max_calls) enables it for up to
  * max_calls calls (host-side event objects only, no device memory);
  * moe_profile_stop synchronises, writes the summed milliseconds of each stage over
  * the recorded calls to ms_per_stage[moe_profile_stage_count()], the number of
