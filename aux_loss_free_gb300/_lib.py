@@ -67,7 +67,7 @@ SIGNATURES = {
     "moe_device_status": (_I32, [_P, ctypes.POINTER(_I32)]),
     "moe_profile_stage_count": (_I32, []),
     "moe_profile_stage_name": (ctypes.c_char_p, [_I32]),
-    "moe_profile_start": (_I32, [_I32]),
+    "moe_profile_start": (_I32, [_I32, _I32]),
     "moe_profile_stop": (_I32, [ctypes.POINTER(_F), ctypes.POINTER(_I32)]),
 }
 
@@ -216,8 +216,8 @@ def moe_device_status(stream=None) -> int:
     return out.value
 
 
-def moe_profile_start(max_calls: int):
-    _check("moe_profile_start", load_library().moe_profile_start(max_calls))
+def moe_profile_start(max_calls: int, period: int = 1):
+    _check("moe_profile_start", load_library().moe_profile_start(max_calls, period))
 
 
 def moe_profile_stop():

@@ -268,6 +268,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     tmem_alloc_pair(smem_u32(&tmem_holder), TMEM_COLS);
     tmem_relinquish_pair();
   }
+  // Set-up above is CTA-local; the offsets and operands come from earlier kernels.
+  pdl_wait();
+  pdl_trigger();
   if (warp == 2) {
     // Tile table of the routed groups: s_cum[g] = tiles of groups < g.
     int carry = 0;
@@ -578,8 +581,7 @@ cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* off
   if (p.routed.enabled)
     tiles += ((max_routed_rows + BM - 1) / BM + E) * (long long)(p.routed.n_total / p.routed.bn);
   const int pairs = (int)std::min<long long>(max_active_pairs(), std::max<long long>(tiles, 1));
-  grouped_gemm_kernel<<<2 * pairs, NUM_THREADS, DYN_SMEM, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(grouped_gemm_kernel, dim3(2 * pairs), dim3(NUM_THREADS), DYN_SMEM, s, p);
 }
 
 }  // namespace moe

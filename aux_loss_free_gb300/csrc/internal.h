@@ -5,7 +5,29 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <utility>
+
 namespace moe {
+
+// Launch with programmatic dependent launch: the kernel may be scheduled while the
+// previous kernel in the stream is still running; it must execute
+// griddepcontrol.wait (pdl_wait) before touching memory that earlier work writes
+// or reads.  This hides the launch gap between the layer's consecutive kernels.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Device status bits (OR-ed into the library's status word).
 constexpr int kDevTimeout = 1;
@@ -43,6 +65,8 @@ cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
 // three-way bf16 split of the router weight.
 bool router_tc_supported(int E, int x_is_f32);
 size_t router_tc_scratch_bytes(int E, int d);
+// Also zeroes a.load [E] and, when set, a.counts [(T / chunk_tokens rounded up) * E]
+// before the router's atomics (no separate memsets in the launch chain).
 cudaError_t launch_router_tc(const RouterArgs& a, void* w3_scratch, cudaStream_t s);
 
 // ---------------------------------------------------------------- permutation

@@ -65,11 +65,19 @@ const char* const kStageNames[kStages] = {"router", "permute_gather", "gemm_gate
 struct Profiler {
   std::mutex mu;
   bool on = false;
-  int max_calls = 0, calls = 0;
-  std::vector<cudaEvent_t> ev;  // (kStages + 1) per call
+  int max_calls = 0, calls = 0, period = 1;
+  long long seen = 0;
+  std::vector<cudaEvent_t> ev;  // (kStages + 1) per recorded call
 } g_prof;
 
-// Marks the start of `stage` (kStages = end of the call) of the current call.
+// Whether the call now starting is recorded (every `period`-th call while enabled).
+bool prof_begin_call() {
+  std::lock_guard<std::mutex> lock(g_prof.mu);
+  if (!g_prof.on || g_prof.calls >= g_prof.max_calls) return false;
+  return (g_prof.seen++ % g_prof.period) == 0;
+}
+
+// Marks the start of `stage` (kStages = end of the call) of a recorded call.
 void prof_mark(int stage, cudaStream_t s) {
   std::lock_guard<std::mutex> lock(g_prof.mu);
   if (!g_prof.on || g_prof.calls >= g_prof.max_calls) return;
@@ -401,14 +409,18 @@ moe_status_t moe_layer_fwd(const moe_shape_t* shape, const void* x, const float*
   const int chunks = layer_chunks_of(shape, &ct);
   const int xf = shape->x_dtype == MOE_X_F32;
 
-  prof_mark(0, s);
-  if (cudaMemsetAsync(L.load, 0, sizeof(int32_t) * E, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cudaMemsetAsync(L.perm.counts, 0, sizeof(int32_t) * chunks * E, s) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  const bool prof = prof_begin_call();
+  if (prof) prof_mark(0, s);
+  // The tensor-core router's first kernel zeroes load and counts itself.
+  if (!router_tc_supported(E, xf)) {
+    if (cudaMemsetAsync(L.load, 0, sizeof(int32_t) * E, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(L.perm.counts, 0, sizeof(int32_t) * chunks * E, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   RouterArgs ra{x, xf, w_router, logit_offset, bias, dbg ? dbg->scores : nullptr, L.idx, L.gate,
                 L.load, L.perm.counts, ct, T, shape->d, E, k, shape->renorm};
   cudaError_t e = run_router(ra, L.router, s);
-  prof_mark(1, s);
+  if (prof) prof_mark(1, s);
   // The scatter launch derives the offsets from the counts and applies the bias
   // update (after the router has read the bias).
   if (e == cudaSuccess)
@@ -416,13 +428,13 @@ moe_status_t moe_layer_fwd(const moe_shape_t* shape, const void* x, const float*
                        update_bias ? bias : nullptr, gamma, (long long)T * k, L.perm_tok,
                        L.inv_pos, x, xf, shape->d, L.ffn.xp, (xf && shape->F) ? L.ffn.xb : nullptr,
                        s);
-  prof_mark(2, s);
+  if (prof) prof_mark(2, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   const void* xbf = xf ? L.ffn.xb : x;
   CombineInputs comb{L.y, L.inv_pos, L.gate, static_cast<const uint16_t*>(residual), k};
   const moe_status_t st2 = run_ffn(shape, xbf, L.offsets, w, L.ffn, L.y, nullptr, &comb,
-                                   static_cast<uint16_t*>(out), s, true);
-  prof_mark(kStages, s);
+                                   static_cast<uint16_t*>(out), s, prof);
+  if (prof) prof_mark(kStages, s);
   return st2;
 }
 
@@ -453,8 +465,8 @@ const char* moe_profile_stage_name(int32_t stage) {
   return (stage >= 0 && stage < kStages) ? kStageNames[stage] : "";
 }
 
-moe_status_t moe_profile_start(int32_t max_calls) {
-  if (max_calls < 1 || max_calls > (1 << 20)) return MOE_ERR_INVALID_ARG;
+moe_status_t moe_profile_start(int32_t max_calls, int32_t period) {
+  if (max_calls < 1 || max_calls > (1 << 20) || period < 1) return MOE_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_prof.mu);
   for (cudaEvent_t ev : g_prof.ev) cudaEventDestroy(ev);
   g_prof.ev.assign((size_t)max_calls * (kStages + 1), nullptr);
@@ -462,6 +474,8 @@ moe_status_t moe_profile_start(int32_t max_calls) {
     if (cudaEventCreate(&ev) != cudaSuccess) return MOE_ERR_CUDA;
   g_prof.max_calls = max_calls;
   g_prof.calls = 0;
+  g_prof.period = period;
+  g_prof.seen = 0;
   g_prof.on = true;
   return MOE_OK;
 }

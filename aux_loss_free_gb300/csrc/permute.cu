@@ -74,6 +74,8 @@ __global__ void __launch_bounds__(SC_THREADS) scatter_kernel(
   __shared__ int32_t part_tot[SC_THREADS];
   __shared__ int32_t s_pos[SC_ROUND];
   __shared__ int32_t s_tok[SC_ROUND];
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // counts / idx come from the router
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int block_tokens = chunk_tokens <= 128 ? 32 : chunk_tokens;
   const long long t_begin = (long long)blockIdx.x * block_tokens;
@@ -274,10 +276,9 @@ cudaError_t launch_scatter(const int32_t* idx, const int32_t* counts, int T, int
   const int chunks = (T + chunk_tokens - 1) / chunk_tokens;
   const int block_tokens = chunk_tokens <= 128 ? 32 : chunk_tokens;
   const int blocks = (T + block_tokens - 1) / block_tokens;
-  scatter_kernel<<<blocks, SC_THREADS, 0, s>>>(idx, counts, chunks, T, k, E, chunk_tokens, offsets,
-                                               load_out, bias, gamma, tokens_times_k, perm_tok,
-                                               inv_pos, x, x_is_f32, d, xp, xb);
-  return cudaGetLastError();
+  return launch_pdl(scatter_kernel, dim3(blocks), dim3(SC_THREADS), 0, s, idx, counts, chunks, T, k,
+                    E, chunk_tokens, offsets, load_out, bias, gamma, tokens_times_k, perm_tok,
+                    inv_pos, x, x_is_f32, d, xp, xb);
 }
 
 cudaError_t launch_gather(const void* x, int x_is_f32, const int32_t* perm_tok, long long rows,

@@ -21,6 +21,7 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -82,10 +83,6 @@ __global__ void __launch_bounds__(RTHREADS, 1) router_tc_kernel(const __grid_con
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int t0 = blockIdx.x * RBM;
 
-  for (int e = threadIdx.x; e < E; e += RTHREADS) {
-    s_bias[e] = p.bias[e];
-    s_off[e] = p.logit_offset ? p.logit_offset[e] : 0.f;
-  }
   for (int i = threadIdx.x; i < 4 * E; i += RTHREADS) (&hist[0][0])[i] = 0;
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < RSTAGES; ++s) {
@@ -100,6 +97,14 @@ __global__ void __launch_bounds__(RTHREADS, 1) router_tc_kernel(const __grid_con
   if (warp == 1) {
     tmem_alloc(smem_u32(&tmem_holder), TCOLS);
     tmem_relinquish();
+  }
+  // Everything above is CTA-local; from here on the kernel reads the bias (updated
+  // by the previous forward), the split weights and the tokens.
+  pdl_wait();
+  pdl_trigger();
+  for (int e = threadIdx.x; e < E; e += RTHREADS) {
+    s_bias[e] = p.bias[e];
+    s_off[e] = p.logit_offset ? p.logit_offset[e] : 0.f;
   }
   tc_fence_before();
   __syncthreads();
@@ -284,8 +289,14 @@ __global__ void __launch_bounds__(RTHREADS, 1) router_tc_kernel(const __grid_con
 // W (fp32 [E][d]) -> W3 (bf16 [3E][d]): rows [0,E) W_hi, [E,2E) W_mid, [2E,3E) W_lo with
 // W_hi = bf16(W), W_mid = bf16(W - W_hi), W_lo = bf16(W - W_hi - W_mid); each
 // difference is exact in fp32.
-__global__ void split_router_kernel(const float* __restrict__ w, long long n, uint16_t* __restrict__ w3) {
+__global__ void split_router_kernel(const float* __restrict__ w, long long n, uint16_t* __restrict__ w3,
+                                    int32_t* __restrict__ zero_a, int na, int32_t* __restrict__ zero_b,
+                                    int nb) {
+  pdl_wait();
+  pdl_trigger();
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < na) zero_a[i] = 0;
+  if (i < nb) zero_b[i] = 0;
   if (i >= n) return;
   const float v = w[i];
   const __nv_bfloat16 hi = __float2bfloat16_rn(v);
@@ -330,8 +341,7 @@ cudaError_t launch_e(RouterTcParams& p, int blocks, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(router_tc_kernel<E>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
   if (e != cudaSuccess) return e;
-  router_tc_kernel<E><<<blocks, RTHREADS, dyn, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(router_tc_kernel<E>, dim3(blocks), dim3(RTHREADS), dyn, s, p);
 }
 
 }  // namespace
@@ -345,8 +355,10 @@ size_t router_tc_scratch_bytes(int E, int d) { return (size_t)3 * E * d * sizeof
 cudaError_t launch_router_tc(const RouterArgs& a, void* w3_scratch, cudaStream_t s) {
   const long long n = (long long)a.E * a.d;
   uint16_t* w3 = static_cast<uint16_t*>(w3_scratch);
-  split_router_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a.w_router, n, w3);
-  cudaError_t e = cudaGetLastError();
+  const int nb = a.counts ? ((a.T + a.chunk_tokens - 1) / a.chunk_tokens) * a.E : 0;
+  const long long nthreads = std::max<long long>(n, std::max(a.E, nb));
+  cudaError_t e = launch_pdl(split_router_kernel, dim3((unsigned)((nthreads + 255) / 256)), dim3(256), 0,
+                             s, a.w_router, n, w3, a.load, a.E, a.counts, nb);
   if (e != cudaSuccess) return e;
   RouterTcParams p;
   std::memset(&p, 0, sizeof(p));

@@ -227,14 +227,15 @@ moe_status_t moe_quantize_int4(int64_t rows, int32_t K, const void* w, void* q, 
 /* Per-stage timing of moe_layer_fwd (profiling aid).  While enabled, every
  * moe_layer_fwd call records CUDA events on its stream between its stages (router,
  * permutation + gather, gate/up GEMM, routed down GEMM, shared down GEMM with the
- * fused combine).  moe_profile_start(max_calls) enables it for up to
- * max_calls calls (host-side event objects only, no device memory);
+ * fused combine).  moe_profile_start(max_calls, period) records every period-th call,
+ * up to max_calls recorded calls (host-side event objects only, no device memory;
+ * each event adds about 2 us to the stream, hence the sampling period);
  * moe_profile_stop synchronises, writes the summed milliseconds of each stage over
  * the recorded calls to ms_per_stage[moe_profile_stage_count()], the number of
  * recorded calls to *calls, and disables recording. */
 int32_t moe_profile_stage_count(void);
 const char* moe_profile_stage_name(int32_t stage);
-moe_status_t moe_profile_start(int32_t max_calls);
+moe_status_t moe_profile_start(int32_t max_calls, int32_t period);
 moe_status_t moe_profile_stop(float* ms_per_stage, int32_t* calls);
 
 /* Synchronises `stream`, returns the device status word accumulated by this
