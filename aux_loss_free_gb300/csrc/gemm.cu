@@ -159,8 +159,17 @@ __device__ __forceinline__ void commit_pair_local(uint32_t bar) {
 
 // ---------------------------------------------------------------- helpers
 
+// Tile order: with both operand sets present, shared-expert tiles (compute bound)
+// and routed tiles (which stream expert weights from DRAM) are interleaved evenly,
+// so every stretch of the launch mixes the two; each set keeps its own order.
 __device__ __forceinline__ Tile decode_tile(const Params& p, int tile, int shared_tiles,
-                                            const int* s_off, const int* s_cum) {
+                                            const int* s_off, const int* s_cum, int total) {
+  const int routed_tiles = total - shared_tiles;
+  if (shared_tiles > 0 && routed_tiles > 0) {
+    const long long r_before = (long long)tile * routed_tiles / total;
+    const long long r_after = (long long)(tile + 1) * routed_tiles / total;
+    tile = (r_after > r_before) ? shared_tiles + (int)r_before : tile - (int)r_before;
+  }
   Tile t;
   if (tile < shared_tiles) {
     const int nt = p.shared.n_total / p.shared.bn;
@@ -311,7 +320,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0, issued = 0, last_par = 0;
       bool ok = true;
       for (int tile = cluster; tile < total && ok; tile += nclusters) {
-        const Tile t = decode_tile(p, tile, shared_tiles, s_off, s_cum);
+        const Tile t = decode_tile(p, tile, shared_tiles, s_off, s_cum, total);
         const OperandSet& S = t.set ? p.routed : p.shared;
         const int nkb = (S.k_total + BK - 1) / BK;
         const int half = S.bn / 2;
@@ -351,7 +360,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = cluster; tile < total && ok; tile += nclusters) {
-        const Tile t = decode_tile(p, tile, shared_tiles, s_off, s_cum);
+        const Tile t = decode_tile(p, tile, shared_tiles, s_off, s_cum, total);
         const OperandSet& S = t.set ? p.routed : p.shared;
         const int nkb = (S.k_total + BK - 1) / BK;
         const uint32_t idesc = idesc_bf16_f32(BM, S.bn);
@@ -397,7 +406,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = cluster; tile < total; tile += nclusters) {
-      const Tile t = decode_tile(p, tile, shared_tiles, s_off, s_cum);
+      const Tile t = decode_tile(p, tile, shared_tiles, s_off, s_cum, total);
       const OperandSet& S = t.set ? p.routed : p.shared;
       int ok = 1;
       if (lane == 0) ok = mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, p.status) ? 1 : 0;

@@ -23,11 +23,24 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Copy one token row (d elements) to a bf16 destination row with one warp.
+// Copy one token row (d elements) to a bf16 destination row with one warp.  For bf16
+// rows every lane issues all of its 16-byte loads before its stores (up to 8 in
+// flight per lane), which the copy needs to reach HBM bandwidth.
 __device__ __forceinline__ void copy_row_bf16(const void* x, int x_is_f32, long long src_row, int d,
                                               uint16_t* dst, int lane) {
   const int nvec = d / 8;  // 8 bf16 = 16 bytes per vector
   uint4* out = reinterpret_cast<uint4*>(dst);
+  if (!x_is_f32 && nvec <= 256) {
+    const uint4* in = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + src_row * d);
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (lane + 32 * j < nvec) v[j] = __ldg(in + lane + 32 * j);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (lane + 32 * j < nvec) out[lane + 32 * j] = v[j];
+    return;
+  }
   if (x_is_f32) {
     const float4* in = reinterpret_cast<const float4*>(static_cast<const float*>(x) + src_row * d);
     for (int v = lane; v < nvec; v += 32) {
@@ -176,6 +189,7 @@ __global__ void __launch_bounds__(SC_THREADS) scatter_kernel(
     }
     __syncthreads();
     if (xp) {
+#pragma unroll 2
       for (int q = warp; q < n; q += SC_THREADS / 32) {
         const int st = s_tok[q];
         const int t = st >= 0 ? st : -1 - st;
