@@ -78,11 +78,13 @@ cudaError_t launch_count(const int32_t* idx, int T, int k, int E, int chunk_toke
 // writes a bf16 copy of x into xb (fp32 x).  Blocks of 32 tokens when a chunk holds
 // at most 128 tokens (a block recounts the earlier blocks of its chunk), else one
 // block per chunk.
+// `active` (nullable, [kMaxE + 1]) receives the ids of the experts with pairs and,
+// at [kMaxE], their count.
 cudaError_t launch_scatter(const int32_t* idx, const int32_t* counts, int T, int k, int E,
                            int chunk_tokens, int32_t* offsets, int32_t* load_out, float* bias,
                            float gamma, long long tokens_times_k, int32_t* perm_tok,
                            int32_t* inv_pos, const void* x, int x_is_f32, int d, uint16_t* xp,
-                           uint16_t* xb, cudaStream_t s);
+                           uint16_t* xb, cudaStream_t s, int32_t* active = nullptr);
 cudaError_t launch_gather(const void* x, int x_is_f32, const int32_t* perm_tok, long long rows,
                           int d, uint16_t* xp, cudaStream_t s);
 cudaError_t launch_to_bf16(const float* x, long long n, uint16_t* xb, cudaStream_t s);
@@ -125,5 +127,12 @@ cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* off
 // ---------------------------------------------------------------- int4 serving
 cudaError_t launch_quantize_int4(long long rows, int K, const uint16_t* w, uint8_t* q,
                                  uint16_t* scale, cudaStream_t s);
+// `active` [kMaxE + 1]: ids of the experts with rows (ascending), count at [kMaxE].
+cudaError_t launch_int4_gate_up(const int32_t* active, const int32_t* offsets, const uint8_t* wq,
+                                const uint16_t* ws, const uint16_t* xp, uint16_t* h, int d, int f,
+                                int block, cudaStream_t s);
+cudaError_t launch_int4_down(const int32_t* active, const int32_t* offsets, const uint8_t* wq,
+                             const uint16_t* ws, const uint16_t* h, uint16_t* y, int d, int f,
+                             cudaStream_t s);
 
 }  // namespace moe

@@ -153,6 +153,7 @@ FfnWs carve_ffn(Carver& c, const moe_shape_t* s) {
 
 struct LayerWs {
   void* router;
+  int32_t* active;  // [kMaxE + 1] experts with rows, count last (int4 serving path)
   int32_t* idx;
   float* gate;
   int32_t* load;
@@ -168,6 +169,7 @@ LayerWs carve_layer(Carver& c, const moe_shape_t* s) {
   LayerWs w;
   const size_t rb = route_scratch_bytes(s);
   w.router = rb ? c.take(rb) : nullptr;
+  w.active = static_cast<int32_t*>(c.take(4 * (size_t)(kMaxE + 1)));
   w.idx = static_cast<int32_t*>(c.take(4 * Tk));
   w.gate = static_cast<float*>(c.take(4 * Tk));
   w.load = static_cast<int32_t*>(c.take(4 * (size_t)s->E));
@@ -226,6 +228,45 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x_bf16, const int32_t* of
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   return MOE_OK;
+}
+
+// Top-1 serving path with int4 routed experts: the shared expert's gate/up on the
+// tensor cores, the routed experts' gate/up and down on the int4 dequantising warps
+// (active experts only), then the shared down projection whose epilogue adds the
+// gated routed rows (and the residual) and writes `out`.
+moe_status_t run_ffn_int4(const moe_shape_t* s, const void* x_bf16, const LayerWs& L,
+                          const moe_weights_t* w, const void* residual, uint16_t* out,
+                          cudaStream_t st, bool mark) {
+  const long long Tk = (long long)s->T * s->k;
+  int bad = 0;
+  GemmOperandSet off{};
+  CombineInputs none{};
+  cudaError_t e = cudaSuccess;
+  if (s->F) {
+    GemmOperandSet s1{x_bf16, s->T, w->shared_gate_up, 1, 2 * s->F, s->d, L.ffn.hs, s->F,
+                      EPI_SWIGLU, s->T};
+    e = launch_grouped_gemm(off, L.offsets, s->E, s1, none, Tk, st, &bad);
+    if (bad) return MOE_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  e = launch_int4_gate_up(L.active, L.offsets, static_cast<const uint8_t*>(w->w_gate_up),
+                          static_cast<const uint16_t*>(w->scale_gate_up), L.ffn.xp, L.ffn.h, s->d,
+                          s->f, moe_gate_up_block(s->f), st);
+  if (e == cudaSuccess)
+    e = launch_int4_down(L.active, L.offsets, static_cast<const uint8_t*>(w->w_down),
+                         static_cast<const uint16_t*>(w->scale_down), L.ffn.h, L.y, s->d, s->f, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (mark) prof_mark(3, st);
+  if (mark) prof_mark(4, st);
+  CombineInputs comb{L.y, L.inv_pos, L.gate, static_cast<const uint16_t*>(residual), s->k};
+  if (s->F) {
+    GemmOperandSet s2{L.ffn.hs, s->T, w->shared_down, 1, s->d, s->F, out, s->d, EPI_COMBINE, s->T};
+    e = launch_grouped_gemm(off, L.offsets, s->E, s2, comb, Tk, st, &bad);
+    if (bad) return MOE_ERR_UNSUPPORTED;
+  } else {
+    e = launch_combine(L.y, nullptr, L.inv_pos, L.gate, comb.residual, out, s->T, s->k, s->d, st);
+  }
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 bool weights_ok(const moe_shape_t* s, const moe_weights_t* w) {
@@ -385,7 +426,8 @@ moe_status_t moe_layer_fwd(const moe_shape_t* shape, const void* x, const float*
                            void* stream) {
   moe_status_t st = check_shape(shape);
   if (st) return st;
-  if (shape->w_format != MOE_W_BF16) return MOE_ERR_UNSUPPORTED;
+  const bool int4 = shape->w_format == MOE_W_INT4_G32;
+  if (int4 && shape->x_dtype != MOE_X_BF16) return MOE_ERR_UNSUPPORTED;
   if (!x || !w_router || !bias || !out || !workspace || !weights_ok(shape, w))
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_router) || !aligned16(out) ||
@@ -427,13 +469,15 @@ moe_status_t moe_layer_fwd(const moe_shape_t* shape, const void* x, const float*
     e = launch_scatter(L.idx, L.perm.counts, T, k, E, ct, L.offsets, nullptr,
                        update_bias ? bias : nullptr, gamma, (long long)T * k, L.perm_tok,
                        L.inv_pos, x, xf, shape->d, L.ffn.xp, (xf && shape->F) ? L.ffn.xb : nullptr,
-                       s);
+                       s, int4 ? L.active : nullptr);
   if (prof) prof_mark(2, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   const void* xbf = xf ? L.ffn.xb : x;
   CombineInputs comb{L.y, L.inv_pos, L.gate, static_cast<const uint16_t*>(residual), k};
-  const moe_status_t st2 = run_ffn(shape, xbf, L.offsets, w, L.ffn, L.y, nullptr, &comb,
-                                   static_cast<uint16_t*>(out), s, prof);
+  const moe_status_t st2 =
+      int4 ? run_ffn_int4(shape, xbf, L, w, residual, static_cast<uint16_t*>(out), s, prof)
+           : run_ffn(shape, xbf, L.offsets, w, L.ffn, L.y, nullptr, &comb,
+                     static_cast<uint16_t*>(out), s, prof);
   if (prof) prof_mark(kStages, s);
   return st2;
 }

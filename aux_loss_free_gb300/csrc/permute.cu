@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(SC_THREADS) scatter_kernel(
     int E, int chunk_tokens, int32_t* __restrict__ offsets, int32_t* __restrict__ load_out,
     float* bias, float gamma, long long tokens_times_k, int32_t* __restrict__ perm_tok,
     int32_t* __restrict__ inv_pos, const void* __restrict__ x, int x_is_f32, int d,
-    uint16_t* __restrict__ xp, uint16_t* __restrict__ xb) {
+    uint16_t* __restrict__ xp, uint16_t* __restrict__ xb, int32_t* __restrict__ active) {
   __shared__ int32_t run[kMaxE];
   __shared__ int32_t tot_e[kMaxE];
   __shared__ int32_t off[kMaxE + 1];
@@ -145,6 +145,16 @@ __global__ void __launch_bounds__(SC_THREADS) scatter_kernel(
   __syncthreads();
   if (tid < E) run[tid] += off[tid];
   if (blockIdx.x == 0) {
+    if (active && tid < 32) {  // compact list of the experts with pairs, ascending
+      int n = 0;
+      for (int b = 0; b < E; b += 32) {
+        const bool has = b + tid < E && tot_e[b + tid] > 0;
+        const unsigned m = __ballot_sync(FULL, has);
+        if (has) active[n + __popc(m & ((1u << tid) - 1u))] = b + tid;
+        n += __popc(m);
+      }
+      if (tid == 0) active[kMaxE] = n;
+    }
     for (int i = tid; i <= E; i += SC_THREADS) offsets[i] = off[i];
     if (tid < E) {
       if (load_out) load_out[tid] = tot_e[tid];
@@ -286,13 +296,13 @@ cudaError_t launch_scatter(const int32_t* idx, const int32_t* counts, int T, int
                            int chunk_tokens, int32_t* offsets, int32_t* load_out, float* bias,
                            float gamma, long long tokens_times_k, int32_t* perm_tok,
                            int32_t* inv_pos, const void* x, int x_is_f32, int d, uint16_t* xp,
-                           uint16_t* xb, cudaStream_t s) {
+                           uint16_t* xb, cudaStream_t s, int32_t* active) {
   const int chunks = (T + chunk_tokens - 1) / chunk_tokens;
   const int block_tokens = chunk_tokens <= 128 ? 32 : chunk_tokens;
   const int blocks = (T + block_tokens - 1) / block_tokens;
   return launch_pdl(scatter_kernel, dim3(blocks), dim3(SC_THREADS), 0, s, idx, counts, chunks, T, k,
                     E, chunk_tokens, offsets, load_out, bias, gamma, tokens_times_k, perm_tok,
-                    inv_pos, x, x_is_f32, d, xp, xb);
+                    inv_pos, x, x_is_f32, d, xp, xb, active);
 }
 
 cudaError_t launch_gather(const void* x, int x_is_f32, const int32_t* perm_tok, long long rows,

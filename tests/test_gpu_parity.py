@@ -270,3 +270,37 @@ def test_skewed_bias_trajectory_bitexact():
         ratios.append(ld.max() / ld.mean())
     assert ratios[0] > 10.0          # the workload is skewed as specified
     assert ratios[-1] < ratios[0]    # and the balancing pulls it back
+
+
+def _dequant_oracle(bits3d):
+    """Oracle int4 round trip of bf16 weights [G][rows][K] (its own quantiser)."""
+    G, R, K = bits3d.shape
+    packed, scale, _ = O.quantize_int4_g32(bf64(bits3d.reshape(-1, K)).astype(np.float32))
+    return O.dequantize_int4_g32(packed, scale).reshape(G, R, K)
+
+
+@pytest.mark.parametrize("T", [1, 8, 64, 200])
+def test_int4_top1_serving_layer_matches_oracle(T):
+    """Top-1 serving with int4 routed experts (dequantised inside the kernels) and the
+    bf16 shared expert: routing bit-exact, gate = raw score, output within tolerance
+    of the oracle run on the oracle's own dequantised weights; no bias update."""
+    s = CONFIGS["decode"].replace(T=T)
+    host = make_layer(s, "decode")
+    layer = LayerOnDevice(s, host, DEV)
+    x = to_device_tokens(host["x"], DEV)
+    scores = torch.empty(s.T, s.E, dtype=torch.float32, device=DEV)
+    idx = torch.empty(s.T, s.k, dtype=torch.int32, device=DEV)
+    gate = torch.empty(s.T, s.k, dtype=torch.float32, device=DEV)
+    dbg = M.make_debug(scores=scores, idx=idx, gate=gate)
+    out = torch.empty(s.T, s.d, dtype=torch.bfloat16, device=DEV)
+    layer.forward(x, out, update_bias=False, debug=dbg)
+    torch.cuda.synchronize()
+    sc = scores.cpu().numpy()
+    ref = O.layer_forward(tokens64(host["x"]), host["w_router"], host["bias"],
+                          _dequant_oracle(host["w_gate"]), _dequant_oracle(host["w_up"]),
+                          _dequant_oracle(host["w_down"]), bf64(host["s_gate"]), bf64(host["s_up"]),
+                          bf64(host["s_down"]), k=1, renorm=False, scores_f32=sc)
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    assert np.abs(gate.cpu().numpy() - ref["gate"]).max() <= 1e-6
+    assert np.array_equal(layer.bias.cpu().numpy().view(np.uint32), host["bias"].view(np.uint32))
+    assert_close_bf16(bf16_to_np(out), ref["out"], "int4 serving out")
