@@ -61,9 +61,9 @@ struct RouterArgs {
   int T, d, E, k, renorm;
 };
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
-// Tensor-core router (bf16 tokens, E in {16, 32, 48, 64, 80}); needs scratch for the
-// three-way bf16 split of the router weight.
-bool router_tc_supported(int E, int x_is_f32);
+// Tensor-core router (bf16 tokens, T >= 128, E in {16, 32, 48, 64, 80}); needs
+// scratch for the three-way bf16 split of the router weight.
+bool router_tc_supported(int T, int E, int x_is_f32);
 size_t router_tc_scratch_bytes(int E, int d);
 // Also zeroes a.load [E] and, when set, a.counts [(T / chunk_tokens rounded up) * E]
 // before the router's atomics (no separate memsets in the launch chain).

@@ -102,11 +102,11 @@ moe_status_t check_shape(const moe_shape_t* s) {
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 size_t route_scratch_bytes(const moe_shape_t* s) {
-  return router_tc_supported(s->E, s->x_dtype == MOE_X_F32) ? router_tc_scratch_bytes(s->E, s->d) : 0;
+  return router_tc_supported(s->T, s->E, s->x_dtype == MOE_X_F32) ? router_tc_scratch_bytes(s->E, s->d) : 0;
 }
 
 cudaError_t run_router(const RouterArgs& a, void* scratch, cudaStream_t s) {
-  if (router_tc_supported(a.E, a.x_is_f32)) return launch_router_tc(a, scratch, s);
+  if (router_tc_supported(a.T, a.E, a.x_is_f32)) return launch_router_tc(a, scratch, s);
   return launch_router(a, s);
 }
 
@@ -119,7 +119,7 @@ int chunks_of(const moe_shape_t* s, int* chunk_tokens) {
 // at least 128 tokens (and still keep the count table within kMaxCountEntries).
 int layer_chunks_of(const moe_shape_t* s, int* chunk_tokens) {
   int ct = permute_chunk_tokens(s->T, s->E);
-  if (router_tc_supported(s->E, s->x_dtype == MOE_X_F32) && ct < 128) ct = 128;
+  if (router_tc_supported(s->T, s->E, s->x_dtype == MOE_X_F32) && ct < 128) ct = 128;
   *chunk_tokens = ct;
   return (s->T + ct - 1) / ct;
 }
@@ -454,7 +454,7 @@ moe_status_t moe_layer_fwd(const moe_shape_t* shape, const void* x, const float*
   const bool prof = prof_begin_call();
   if (prof) prof_mark(0, s);
   // The tensor-core router's first kernel zeroes load and counts itself.
-  if (!router_tc_supported(E, xf)) {
+  if (!router_tc_supported(T, E, xf)) {
     if (cudaMemsetAsync(L.load, 0, sizeof(int32_t) * E, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaMemsetAsync(L.perm.counts, 0, sizeof(int32_t) * chunks * E, s) != cudaSuccess)
       return MOE_ERR_CUDA;

@@ -346,8 +346,10 @@ cudaError_t launch_e(RouterTcParams& p, int blocks, cudaStream_t s) {
 
 }  // namespace
 
-bool router_tc_supported(int E, int x_is_f32) {
-  return !x_is_f32 && (E == 16 || E == 32 || E == 48 || E == 64 || E == 80);
+bool router_tc_supported(int T, int E, int x_is_f32) {
+  // One CTA per 128 tokens: below that the CUDA-core router (fp32 weights read
+  // directly, no split launch) finishes sooner.
+  return !x_is_f32 && T >= 128 && (E == 16 || E == 32 || E == 48 || E == 64 || E == 80);
 }
 
 size_t router_tc_scratch_bytes(int E, int d) { return (size_t)3 * E * d * sizeof(uint16_t); }

@@ -52,7 +52,7 @@ def parse_args():
     p.add_argument("--steps", type=int, default=300)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["nano", "skew", "stack", "tiny"], default="nano")
+    p.add_argument("--workload", choices=sorted(WORKLOADS), default="nano")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -62,26 +62,48 @@ def parse_args():
 
 # ----------------------------------------------------------------------------- helpers
 
+# name -> (case used for the seeds, shape, workload label, metric)
+WORKLOADS = {
+    "nano": ("nano", CONFIGS["nano"], "nano_moe_layer_fwd_T8192", METRIC),
+    "skew": ("skew", CONFIGS["skew"], "skewed_zipf1.2_moe_layer_fwd_T8192_50_steps",
+             "Skewed-load MoE-layer fwd + bias update tokens/s (Zipf 1.2 router offsets), % roofline"),
+    "stack": ("stack", CONFIGS["stack"], "stack_23_moe_layers_T8192",
+              "23-layer MoE stack fwd tokens/s per stack forward, % roofline"),
+    "tiny": ("tiny", CONFIGS["tiny"], "tiny_moe_layer_fwd_T64", "tiny MoE-layer fwd tokens/s"),
+    "decode1": ("decode", CONFIGS["decode"].replace(T=1), "top1_int4_decode_T1",
+                "Top-1 int4 serving decode tokens/s (T=1), % HBM roofline"),
+    "decode8": ("decode", CONFIGS["decode"].replace(T=8), "top1_int4_decode_T8",
+                "Top-1 int4 serving decode tokens/s (T=8), % HBM roofline"),
+    "decode64": ("decode", CONFIGS["decode"].replace(T=64), "top1_int4_decode_T64",
+                 "Top-1 int4 serving decode tokens/s (T=64), % HBM roofline"),
+}
+
+
 def workload_shape(name):
-    return CONFIGS[name]
+    return WORKLOADS[name][1]
 
 
 def config_block(name, n):
     s = workload_shape(name)
-    cfg = {"workload": {"nano": "nano_moe_layer_fwd_T8192", "skew": "skewed_zipf1.2_moe_layer_fwd_T8192",
-                        "stack": "stack_23_moe_layers_T8192", "tiny": "tiny_moe_layer_fwd_T64"}[name],
+    cfg = {"workload": WORKLOADS[name][2],
            "T": s.T, "d": s.d, "E": s.E, "f": s.f, "F": s.F, "k": s.k, "renorm": bool(s.renorm),
-           "bias_update": True, "tokens": "batch 4 x seq 2048" if s.T == 8192 else f"{s.T}",
+           "routed_weights": s.w_format,
+           "bias_update": s.w_format != "int4", "tokens": "batch 4 x seq 2048" if s.T == 8192 else f"{s.T}",
            "layers": s.layers, "l2": "512 MiB write before every timed step (L2 129 MB)",
            "parallelism": f"dp{n} replicas, per-expert load all-reduce" if n > 1 else "dp1"}
     return cfg
 
 
 def layer_algorithmic(s, loads_hit=None):
-    """FLOPs and bytes one layer forward must move (weights of experts hit, x in, out)."""
+    """FLOPs and bytes one layer forward must move (weights of the experts hit, shared
+    and router weights, x in, out)."""
     flops = 2 * s.T * s.d * s.E + 2 * 3 * s.d * s.f * s.T * s.k + 2 * 3 * s.d * s.F * s.T
-    hit = s.E if loads_hit is None else int(loads_hit)
-    nbytes = hit * 3 * s.d * s.f * 2 + 3 * s.d * s.F * 2 + s.E * s.d * 4 + 2 * s.T * s.d * 2
+    hit = min(s.E, s.T * s.k) if loads_hit is None else int(loads_hit)
+    if s.w_format == "int4":
+        expert = 3 * s.d * s.f // 2 + 3 * s.d * s.f // 32 * 2
+    else:
+        expert = 3 * s.d * s.f * 2
+    nbytes = hit * expert + 3 * s.d * s.F * 2 + s.E * s.d * 4 + 2 * s.T * s.d * 2
     return flops, nbytes
 
 
@@ -182,9 +204,16 @@ def oracle_sample_runner(name, seed):
     from oracle import moe_oracle as O
 
     s = workload_shape(name)
-    host = make_layer(s, name if name != "stack" else "stack", seed)
+    host = make_layer(s, WORKLOADS[name][0], seed)
     bf = lambda b: f32_from_bf16_bits(b).astype(np.float64)  # noqa: E731
     W = {k: bf(host[k]) for k in ("w_gate", "w_up", "w_down", "s_gate", "s_up", "s_down")}
+    if s.w_format == "int4":
+        # The serving model's routed experts are the int4 round trip of the bf16 ones
+        # (quantised once, outside the timed calls).
+        for key in ("w_gate", "w_up", "w_down"):
+            G, R, K = W[key].shape
+            packed, scale, _ = O.quantize_int4_g32(W[key].reshape(-1, K).astype(np.float32))
+            W[key] = O.dequantize_int4_g32(packed, scale).reshape(G, R, K)
     x = host["x"]
     xv = bf(x) if x.dtype == np.uint16 else x.astype(np.float64)
 
@@ -226,15 +255,18 @@ def reference_arm(args, rank, world):
         return
     run = oracle_sample_runner(args.workload, args.seed)
     s = workload_shape(args.workload)
-    t_cal = run(256)
+    cal = min(s.T, 256)
+    t_cal = run(cal)
     budget = 150.0 / max(1, args.steps + args.warmup)
-    ntok = int(max(32, min(s.T, 256 * budget / max(t_cal, 1e-6))) // 32 * 32)
+    ntok = int(min(s.T, max(1, cal * budget / max(t_cal, 1e-6))))
+    if ntok >= 32:
+        ntok = ntok // 32 * 32
     for _ in range(args.warmup):
         run(ntok)
     times = [run(ntok) for _ in range(args.steps)]
     total = sum(times)
     value = ntok * args.steps / total / max(1, s.layers)
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+    line = {"impl": "reference", "metric": WORKLOADS[args.workload][3], "value": value, "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -252,6 +284,7 @@ def gpu_arm(args, rank, world, dist):
     import torch
 
     import aux_loss_free_gb300 as M
+    from aux_loss_free_gb300.dp import dp_bias_update
     from aux_loss_free_gb300.layer import LayerOnDevice, to_device_tokens
 
     M.load_library()
@@ -259,10 +292,13 @@ def gpu_arm(args, rank, world, dist):
     torch.cuda.set_device(dev)
     s = workload_shape(args.workload)
     name = args.workload
+    case = WORKLOADS[name][0]
     nlayers = s.layers
-    layers = [LayerOnDevice(s, make_layer(s, name, args.seed, layer=l, with_tokens=False), dev)
+    update = s.w_format != "int4"   # serving does not move the bias
+    layers = [LayerOnDevice(s, make_layer(s, case, args.seed, layer=l, with_tokens=False), dev)
               for l in range(nlayers)]
-    host_x = make_tokens(s, name, args.seed + rank)
+    bias0 = [L.bias.clone() for L in layers]
+    host_x = make_tokens(s, case, args.seed + rank)
     x0 = to_device_tokens(host_x, dev)
     mids = [torch.empty(s.T, s.d, dtype=torch.bfloat16, device=dev) for _ in range(max(0, nlayers - 1))]
     out0 = torch.empty(s.T, s.d, dtype=torch.bfloat16, device=dev)
@@ -277,13 +313,12 @@ def gpu_arm(args, rank, world, dist):
         for l, L in enumerate(layers):
             nxt = out if l == nlayers - 1 else mids[l]
             res = cur if nlayers > 1 else None
-            if world > 1:
+            if world > 1 and update:
                 # Data-parallel replicas: local loads, global sum, identical update.
                 L.forward(cur, nxt, update_bias=False, residual=res, debug=dbg_load)
-                dist.all_reduce(load)
-                M.moe_bias_update(s.E, world * s.T * s.k, load, L.gamma, L.bias)
+                dp_bias_update(load, L.bias, s.T * s.k, L.gamma)
             else:
-                L.forward(cur, nxt, update_bias=True, residual=res)
+                L.forward(cur, nxt, update_bias=update, residual=res)
             cur = nxt
         return out
 
@@ -369,10 +404,24 @@ def gpu_arm(args, rank, world, dist):
     torch.cuda.synchronize(dev)
     e2e_ms = e_start.elapsed_time(e_end) / Ke
 
+    # Load trajectory (skewed workload: the configured 50 steps from the initial bias)
+    # and the number of experts hit, read after the timed region.
+    for L, b in zip(layers, bias0):
+        L.bias.copy_(b)
+    nsteps = max(1, s.steps)
+    loads = torch.empty(nsteps, s.E, dtype=torch.int32, device=dev)
+    for i in range(nsteps):
+        L0 = layers[0]
+        L0.forward(x0, out0 if nlayers == 1 else mids[0], update_bias=update,
+                   residual=x0 if nlayers > 1 else None, debug=M.make_debug(load=loads[i]))
+    ld = loads.cpu().numpy().astype(np.float64)
+    hit = int((ld[0] > 0).sum())
+    traj = (ld.max(axis=1) / ld.mean(axis=1)).tolist()
+
     if rank != 0:
         return
     peaks, peak_note = load_peaks()
-    flops, nbytes = layer_algorithmic(s)
+    flops, nbytes = layer_algorithmic(s, hit)
     tokens_per_s = world * s.T * K / (total_ms / 1e3)
     ms_step = total_ms / K
     roof_s = nlayers * max(flops / (peaks["bf16_tflops"] * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9))
@@ -382,7 +431,7 @@ def gpu_arm(args, rank, world, dist):
     traffic = read_traffic()
     clocks = sampler.summary(t_wall0, t_wall1)
     line = {
-        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "metric": WORKLOADS[name][3], "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_block(name, world),
@@ -401,10 +450,22 @@ def gpu_arm(args, rank, world, dist):
                 "h2d_bytes_per_step": int(hx[0].numel() * hx[0].element_size()),
                 "d2h_bytes_per_step": int(hout[0].numel() * hout[0].element_size()),
                 "copies": "pinned host buffers; H2D and D2H on their own streams overlapped with compute (double-buffered); no L2 flush (weights exceed L2)"},
-        "gpu_launches": K * nlayers * KERNELS_PER_CALL,
+        "gpu_launches": K * nlayers * (KERNELS_PER_CALL + (1 if s.w_format == "int4" else 0)),
         "clocks": clocks,
         "device_status": status,
+        "experts_hit": hit,
     }
+    if s.steps > 1:
+        line["load_max_over_mean"] = {"first": traj[0], "last": traj[-1],
+                                      "per_step": [round(v, 3) for v in traj]}
+        line["step_us"] = {"min": min(step_ms) * 1e3, "median": statistics.median(step_ms) * 1e3,
+                           "max": max(step_ms) * 1e3}
+    if s.w_format == "int4":
+        # Serving is bound by weight bytes: report the HBM roofline of the layer.
+        line["roofline"] = {"kernel": "whole top-1 serving layer", "bound": "hbm",
+                            "achieved": nbytes / (ms_step / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
+                            "unit": "GB/s", "frac": nbytes / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"],
+                            "traffic": None, "peak_note": peak_note, "bytes_per_step": nbytes}
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(name if nlayers == 1 else "nano", args.seed,
                                             args.cpu_seconds)

@@ -116,9 +116,9 @@ int32_t moe_gate_up_block(int32_t width);
 /* Router: relay article, architecture paragraph (sigmoid-plus-bias router, top-k)
  * and top-2 paragraph (renormalised gates).
  *   x            [T][d] bf16 or fp32 (shape->x_dtype)
- *   w_router     [E][d] fp32; logits carry fp32 accuracy: with bf16 tokens and
- *                E in {16, 32, 48, 64, 80} the weight is split exactly into three
- *                bf16 parts and multiplied on the tensor cores with fp32
+ *   w_router     [E][d] fp32; logits carry fp32 accuracy: with bf16 tokens,
+ *                T >= 128 and E in {16, 32, 48, 64, 80} the weight is split exactly
+ *                into three bf16 parts and multiplied on the tensor cores with fp32
  *                accumulation (every product exact); otherwise fp32 FMA on CUDA cores
  *   logit_offset [E] fp32 added to every logit, or NULL (used by the skewed workload)
  *   bias         [E] fp32, added to the scores for selection only

@@ -67,5 +67,6 @@ def test_host_validation_rejects_bad_shapes_before_any_launch(lib_path):
     assert lib.moe_route(ctypes.byref(good), None, None, None, None, None, None, None, None,
                          None, 0, None) == 1
     assert M.moe_route_workspace_size(good) == 3 * 64 * 1024 * 2
+    assert M.moe_route_workspace_size(M.make_shape(64, 1024, 64, 512, 2048, 2)) == 0  # small T: CUDA-core router
     assert M.moe_route_workspace_size(M.make_shape(64, 64, 8, 32, 128, 2, x_dtype=M.MOE_X_F32)) == 0
     assert lib.moe_bias_update(0, 16, None, 1e-3, None, None) == 1
