@@ -173,9 +173,11 @@ def stable_permutation(idx: np.ndarray, E: int):
 
 
 def silu(a: np.ndarray) -> np.ndarray:
-    """silu(a) = a / (1 + exp(-a))."""
+    """silu(a) = a / (1 + exp(-a)).  For a below about -709, exp(-a) overflows to inf
+    and the quotient is the correct limit -0.0 (the overflow warning is silenced)."""
     a = np.asarray(a, dtype=np.float64)
-    return a / (1.0 + np.exp(-a))
+    with np.errstate(over="ignore"):
+        return a / (1.0 + np.exp(-a))
 
 
 def swiglu_ffn(xb: np.ndarray, w_gate: np.ndarray, w_up: np.ndarray, w_down: np.ndarray,

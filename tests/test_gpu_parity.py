@@ -304,3 +304,54 @@ def test_int4_top1_serving_layer_matches_oracle(T):
     assert np.abs(gate.cpu().numpy() - ref["gate"]).max() <= 1e-6
     assert np.array_equal(layer.bias.cpu().numpy().view(np.uint32), host["bias"].view(np.uint32))
     assert_close_bf16(bf16_to_np(out), ref["out"], "int4 serving out")
+
+
+def test_stack_23_layers_with_residual():
+    """Config 4: 23 Nano layers, x_{l+1} = x_l + MoE_l(x_l) in bf16, each layer with its
+    own weights and bias update.  Every layer's routing, loads and updated bias are
+    checked bit for bit; the outputs of 64 sampled tokens are checked at layers 0, 11
+    and 22 against the oracle fed that layer's GPU input (tokens are independent
+    within a layer, so a sample is exact to check)."""
+    s = CONFIGS["stack"]
+    x = to_device_tokens(make_layer(s.replace(f=32, F=32), "stack")["x"], DEV)
+    acts = [x]
+    layers, hosts, dbgs = [], [], []
+    for l in range(s.layers):
+        host = make_layer(s, "stack", layer=l, with_tokens=False)
+        layer = LayerOnDevice(s, host, DEV)
+        scores = torch.empty(s.T, s.E, dtype=torch.float32, device=DEV)
+        load = torch.empty(s.E, dtype=torch.int32, device=DEV)
+        out = torch.empty(s.T, s.d, dtype=torch.bfloat16, device=DEV)
+        layer.forward(acts[-1], out, update_bias=True, residual=acts[-1],
+                      debug=M.make_debug(scores=scores, load=load))
+        acts.append(out)
+        dbgs.append((scores, load))
+        # Keep host weights only for the layers whose outputs are checked.
+        hosts.append(host if l in (0, 11, s.layers - 1) else {"bias": host["bias"]})
+        layers.append(layer)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(23)
+    sample = np.sort(rng.choice(s.T, 64, replace=False))
+    for l in range(s.layers):
+        sc = dbgs[l][0].cpu().numpy()
+        idx = O.topk_select(sc, hosts[l]["bias"], s.k)
+        ld = O.expert_load(idx, s.E)
+        assert np.array_equal(dbgs[l][1].cpu().numpy(), ld), l
+        want_b = O.bias_update(hosts[l]["bias"], ld, s.T * s.k, s.gamma)
+        assert np.array_equal(layers[l].bias.cpu().numpy().view(np.uint32), want_b.view(np.uint32)), l
+        if "w_gate" not in hosts[l]:
+            continue
+        H = hosts[l]
+        xin = bf16_to_np(acts[l])[sample]
+        gidx = idx[sample]
+        gate = O.gate_weights(sc[sample].astype(np.float64), gidx, True)
+        want = xin.copy()
+        for i in range(len(sample)):
+            row = xin[i:i + 1]
+            y = O.swiglu_ffn(row, bf64(H["s_gate"]), bf64(H["s_up"]), bf64(H["s_down"]))[0]
+            for j in range(s.k):
+                e = gidx[i, j]
+                y = y + gate[i, j] * O.swiglu_ffn(row, bf64(H["w_gate"][e]), bf64(H["w_up"][e]),
+                                                  bf64(H["w_down"][e]))[0]
+            want[i] += y
+        assert_close_bf16(bf16_to_np(acts[l + 1])[sample], want, f"stack layer {l}")
