@@ -228,4 +228,4 @@ def moe_profile_stop():
     calls = _I32(0)
     _check("moe_profile_stop", lib.moe_profile_stop(ms, ctypes.byref(calls)))
     names = [lib.moe_profile_stage_name(i).decode() for i in range(n)]
-    return dict(zip(names, [float(v) for v in ms])), calls.value
+    return {nm: float(v) for nm, v in zip(names, ms) if nm}, calls.value

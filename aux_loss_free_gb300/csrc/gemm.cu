@@ -59,7 +59,8 @@ struct OperandSet {
   CUtensorMap a;  // box 128 rows x 64
   CUtensorMap b;  // box BN/2 rows x 64
   void* out;
-  int ldo, n_total, k_total, bn, mode, enabled, rows, pad;
+  int ldo, n_total, k_total, bn, mode, enabled, rows;
+  int v8;  // output rows start on 32-byte boundaries: 256-bit stores allowed
 };
 
 struct Params {
@@ -166,8 +167,10 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, int tile, int share
                                             const int* s_off, const int* s_cum, int total) {
   const int routed_tiles = total - shared_tiles;
   if (shared_tiles > 0 && routed_tiles > 0) {
-    const long long r_before = (long long)tile * routed_tiles / total;
-    const long long r_after = (long long)(tile + 1) * routed_tiles / total;
+    // 32-bit arithmetic (tile counts stay far below 2^15): this runs between tiles on
+    // the MMA thread's critical path.
+    const unsigned r_before = (unsigned)tile * (unsigned)routed_tiles / (unsigned)total;
+    const unsigned r_after = (unsigned)(tile + 1) * (unsigned)routed_tiles / (unsigned)total;
     tile = (r_after > r_before) ? shared_tiles + (int)r_before : tile - (int)r_before;
   }
   Tile t;
@@ -224,12 +227,25 @@ __device__ __forceinline__ void add_bf16_row32(float (&o)[32], const uint16_t* s
   }
 }
 
-__device__ __forceinline__ void store_bf16_row32(uint16_t* dst, const float (&o)[32]) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
+// 32 values -> 64 bytes of bf16.  With v8, two 256-bit stores: half the store
+// instructions of 128-bit ones and whole 32-byte sectors (the epilogue's rows are
+// one per thread, so each warp store touches 32 lines).
+__device__ __forceinline__ void store_bf16_row32(uint16_t* dst, const float (&o)[32], int v8) {
+  uint32_t p[16];
 #pragma unroll
-  for (int v = 0; v < 4; ++v)
-    d[v] = make_uint4(pack_bf16x2(o[8 * v + 0], o[8 * v + 1]), pack_bf16x2(o[8 * v + 2], o[8 * v + 3]),
-                      pack_bf16x2(o[8 * v + 4], o[8 * v + 5]), pack_bf16x2(o[8 * v + 6], o[8 * v + 7]));
+  for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(o[2 * i], o[2 * i + 1]);
+  if (v8) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 16 * h),
+                   "r"(p[8 * h]), "r"(p[8 * h + 1]), "r"(p[8 * h + 2]), "r"(p[8 * h + 3]),
+                   "r"(p[8 * h + 4]), "r"(p[8 * h + 5]), "r"(p[8 * h + 6]), "r"(p[8 * h + 7])
+                   : "memory");
+  } else {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) d[v] = make_uint4(p[4 * v], p[4 * v + 1], p[4 * v + 2], p[4 * v + 3]);
+  }
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
@@ -428,17 +444,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           float h[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) h[i] = silu(__uint_as_float(g[i])) * __uint_as_float(u[i]);
-          if (valid) store_bf16_row32(out + orow * S.ldo + t.n0 / 2 + c, h);
+          if (valid) store_bf16_row32(out + orow * S.ldo + t.n0 / 2 + c, h, S.v8);
         }
       } else if (S.mode == EPI_STORE) {
-        for (int c = 32 * colh; c < S.bn; c += 64) {
-          uint32_t v[32];
+        // Two 32-column chunks per TMEM round trip.
+        for (int c = 32 * colh; c < S.bn; c += 128) {
+          const bool two = c + 64 < S.bn;  // warp-uniform
+          uint32_t v[32], w[32];
           tmem_ld32(tbase + c, v);
+          if (two) tmem_ld32(tbase + c + 64, w);
           tmem_wait_ld();
           float o[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(v[i]);
-          if (valid) store_bf16_row32(out + orow * S.ldo + t.n0 + c, o);
+          if (valid) store_bf16_row32(out + orow * S.ldo + t.n0 + c, o, S.v8);
+          if (two) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(w[i]);
+            if (valid) store_bf16_row32(out + orow * S.ldo + t.n0 + c + 64, o, S.v8);
+          }
         }
       } else {
         float gj[kMaxK];
@@ -465,7 +489,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < kMaxK; ++j)
               if (j < p.k) add_bf16_row32(o, p.y_perm + pj[j] * S.ldo + col, gj[j]);
-            store_bf16_row32(out + orow * S.ldo + col, o);
+            store_bf16_row32(out + orow * S.ldo + col, o, S.v8);
           }
         }
       }
@@ -552,6 +576,7 @@ bool fill_set(OperandSet& t, const GemmOperandSet& o) {
   t.mode = o.mode;
   t.rows = o.rows;
   t.out = o.out;
+  t.v8 = (reinterpret_cast<uintptr_t>(o.out) % 32 == 0) && ((long long)o.ldo * 2) % 32 == 0;
   if (o.N % t.bn != 0) return false;
   if (!make_map(&t.a, o.a, o.K, o.a_rows, HM)) return false;
   if (!make_map(&t.b, o.b, o.K, (uint64_t)o.groups * o.N, t.bn / 2)) return false;
@@ -560,9 +585,17 @@ bool fill_set(OperandSet& t, const GemmOperandSet& o) {
 
 }  // namespace
 
+int gemm_max_pairs() {
+  if (cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           DYN_SMEM) != cudaSuccess)
+    return 1;
+  return max_active_pairs();
+}
+
 cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* offsets, int E,
                                 const GemmOperandSet& shared, const CombineInputs& comb,
-                                long long max_routed_rows, cudaStream_t s, int* bad_arg) {
+                                long long max_routed_rows, cudaStream_t s, int* bad_arg,
+                                int max_pairs) {
   Params p;
   std::memset(&p, 0, sizeof(p));
   *bad_arg = 0;
@@ -589,7 +622,9 @@ cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* off
     tiles += (long long)((p.shared.rows + BM - 1) / BM) * (p.shared.n_total / p.shared.bn);
   if (p.routed.enabled)
     tiles += ((max_routed_rows + BM - 1) / BM + E) * (long long)(p.routed.n_total / p.routed.bn);
-  const int pairs = (int)std::min<long long>(max_active_pairs(), std::max<long long>(tiles, 1));
+  int cap = max_active_pairs();
+  if (max_pairs > 0 && max_pairs < cap) cap = max_pairs;
+  const int pairs = (int)std::min<long long>(cap, std::max<long long>(tiles, 1));
   return launch_pdl(grouped_gemm_kernel, dim3(2 * pairs), dim3(NUM_THREADS), DYN_SMEM, s, p);
 }
 

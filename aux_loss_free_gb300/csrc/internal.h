@@ -120,9 +120,13 @@ struct CombineInputs {
 // Runs up to two operand sets in one persistent launch: `routed` (E groups with
 // rows from device `offsets`) and `shared` (one group).  Either may be disabled
 // with a null `a`.
+// max_pairs > 0 caps the number of 2-SM clusters (leaving SMs to concurrent work).
 cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* offsets, int E,
                                 const GemmOperandSet& shared, const CombineInputs& comb,
-                                long long max_routed_rows, cudaStream_t s, int* bad_arg);
+                                long long max_routed_rows, cudaStream_t s, int* bad_arg,
+                                int max_pairs = 0);
+// Number of co-resident 2-SM clusters of the grouped GEMM on the current device.
+int gemm_max_pairs();
 
 // ---------------------------------------------------------------- int4 serving
 cudaError_t launch_quantize_int4(long long rows, int K, const uint16_t* w, uint8_t* q,

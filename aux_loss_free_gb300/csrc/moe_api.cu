@@ -59,30 +59,62 @@ struct Carver {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // ---------------------------------------------------------------- stage profiler
-constexpr int kStages = 5;
-const char* const kStageNames[kStages] = {"router", "permute_gather", "gemm_gate_up",
-                                          "gemm_down_routed", "gemm_down_shared_combine"};
+// A recorded call places up to kStages + 1 named marks; stage i lasts from mark i to
+// mark i + 1 and carries mark i's name.  Names are static strings.
+constexpr int kStages = 6;
 struct Profiler {
   std::mutex mu;
   bool on = false;
-  int max_calls = 0, calls = 0, period = 1;
+  int max_calls = 0, calls = 0, period = 1, nmarks = 0;
   long long seen = 0;
-  std::vector<cudaEvent_t> ev;  // (kStages + 1) per recorded call
+  std::vector<cudaEvent_t> ev;           // (kStages + 1) per recorded call
+  const char* names[kStages + 1] = {};   // of the first recorded call
 } g_prof;
 
 // Whether the call now starting is recorded (every `period`-th call while enabled).
 bool prof_begin_call() {
   std::lock_guard<std::mutex> lock(g_prof.mu);
   if (!g_prof.on || g_prof.calls >= g_prof.max_calls) return false;
+  g_prof.nmarks = 0;
   return (g_prof.seen++ % g_prof.period) == 0;
 }
 
-// Marks the start of `stage` (kStages = end of the call) of a recorded call.
-void prof_mark(int stage, cudaStream_t s) {
+// Next mark of a recorded call; name == nullptr ends the call.
+void prof_mark(const char* name, cudaStream_t s) {
   std::lock_guard<std::mutex> lock(g_prof.mu);
-  if (!g_prof.on || g_prof.calls >= g_prof.max_calls) return;
-  cudaEventRecord(g_prof.ev[(size_t)g_prof.calls * (kStages + 1) + stage], s);
-  if (stage == kStages) ++g_prof.calls;
+  if (!g_prof.on || g_prof.calls >= g_prof.max_calls || g_prof.nmarks > kStages) return;
+  cudaEventRecord(g_prof.ev[(size_t)g_prof.calls * (kStages + 1) + g_prof.nmarks], s);
+  if (g_prof.calls == 0) g_prof.names[g_prof.nmarks] = name;
+  ++g_prof.nmarks;
+  if (!name) {
+    for (int i = g_prof.nmarks; i <= kStages; ++i)  // unused slots repeat the end mark
+      cudaEventRecord(g_prof.ev[(size_t)g_prof.calls * (kStages + 1) + i], s);
+    ++g_prof.calls;
+  }
+}
+
+// ---------------------------------------------------------------- fork / join
+// moe_layer_fwd runs the routing on a second stream while the shared expert's
+// gate/up GEMM (which needs only x) runs on the caller's stream.  One non-blocking
+// stream and two events per device, created on first use and kept for the process;
+// the mutex serialises enqueues that use them.
+struct AuxStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_aux_mu;
+AuxStream g_aux[64];
+
+AuxStream* aux_for_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  AuxStream& a = g_aux[dev];
+  if (!a.s) {
+    if (cudaStreamCreateWithFlags(&a.s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+  }
+  return &a;
 }
 
 moe_status_t check_shape(const moe_shape_t* s) {
@@ -161,6 +193,7 @@ struct LayerWs {
   int32_t* perm_tok;
   int32_t* inv_pos;
   uint16_t* y;
+  uint16_t* s_out;  // [T][d] shared-expert output (before the combine)
   PermuteWs perm;
   FfnWs ffn;
 };
@@ -177,54 +210,49 @@ LayerWs carve_layer(Carver& c, const moe_shape_t* s) {
   w.perm_tok = static_cast<int32_t*>(c.take(4 * Tk));
   w.inv_pos = static_cast<int32_t*>(c.take(4 * Tk));
   w.y = static_cast<uint16_t*>(c.take(2 * Tk * s->d));
+  w.s_out = s->F ? static_cast<uint16_t*>(c.take(2 * (size_t)s->T * s->d)) : nullptr;
   w.perm = carve_permute(c, s);
   w.ffn = carve_ffn(c, s);
   return w;
 }
 
-// The two grouped-GEMM launches of the bf16 expert FFN.  Gate/up for routed rows
-// (xp -> h) and the shared expert (x -> hs); then the down projections.  With
-// `comb` set and F > 0, the shared down projection's epilogue adds the gated routed
-// rows and the residual and writes `out` directly.
+// The grouped-GEMM launches of the bf16 expert FFN: gate/up for routed rows
+// (xp -> h) and the shared expert (x -> hs) in one launch, both down projections
+// (h -> y_perm, hs -> shared_out) in another; with `comb` set, the combine kernel
+// then writes out = residual + shared_out + sum_j gate_j * y_perm[inv_pos_j].
 moe_status_t run_ffn(const moe_shape_t* s, const void* x_bf16, const int32_t* offsets,
                      const moe_weights_t* w, const FfnWs& ws, uint16_t* y_perm,
                      uint16_t* shared_out, const CombineInputs* comb, uint16_t* out,
-                     cudaStream_t st, bool mark = false) {
+                     cudaStream_t st, bool mark = false, bool shared_gate_up_done = false) {
   const long long Tk = (long long)s->T * s->k;
   int bad = 0;
   GemmOperandSet r1{ws.xp, Tk, w->w_gate_up, s->E, 2 * s->f, s->d, ws.h, s->f, EPI_SWIGLU, 0};
   GemmOperandSet s1{};
-  if (s->F) s1 = GemmOperandSet{x_bf16, s->T, w->shared_gate_up, 1, 2 * s->F, s->d, ws.hs, s->F,
-                                EPI_SWIGLU, s->T};
+  if (s->F && !shared_gate_up_done)
+    s1 = GemmOperandSet{x_bf16, s->T, w->shared_gate_up, 1, 2 * s->F, s->d, ws.hs, s->F,
+                        EPI_SWIGLU, s->T};
   CombineInputs none{};
+  if (mark) prof_mark(shared_gate_up_done ? "routed_gate_up" : "gemm_gate_up", st);
   cudaError_t e = launch_grouped_gemm(r1, offsets, s->E, s1, none, Tk, st, &bad);
   if (bad) return MOE_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   GemmOperandSet r2{ws.h, Tk, w->w_down, s->E, s->d, s->f, y_perm, s->d, EPI_STORE, 0};
   GemmOperandSet s2{};
-  if (s->F) {
-    if (comb) s2 = GemmOperandSet{ws.hs, s->T, w->shared_down, 1, s->d, s->F, out, s->d, EPI_COMBINE, s->T};
-    else s2 = GemmOperandSet{ws.hs, s->T, w->shared_down, 1, s->d, s->F, shared_out, s->d, EPI_STORE, s->T};
-  }
-  if (mark) prof_mark(3, st);
-  if (comb && s->F) {
-    // The combine epilogue reads y_perm, so the routed down projection runs first.
-    GemmOperandSet off{};
-    e = launch_grouped_gemm(r2, offsets, s->E, off, none, Tk, st, &bad);
-    if (bad) return MOE_ERR_UNSUPPORTED;
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-    if (mark) prof_mark(4, st);
-    e = launch_grouped_gemm(off, offsets, s->E, s2, *comb, Tk, st, &bad);
-  } else {
-    e = launch_grouped_gemm(r2, offsets, s->E, s2, none, Tk, st, &bad);
-  }
+  if (s->F)
+    s2 = GemmOperandSet{ws.hs, s->T, w->shared_down, 1, s->d, s->F, shared_out, s->d, EPI_STORE, s->T};
+  if (mark) prof_mark("gemm_down", st);
+  // Both down projections in one launch (their tiles interleave: the routed ones
+  // stream expert weights, the shared ones are compute bound), then the combine.
+  if (comb && s->F)
+    s2 = GemmOperandSet{ws.hs, s->T, w->shared_down, 1, s->d, s->F, shared_out, s->d, EPI_STORE, s->T};
+  e = launch_grouped_gemm(r2, offsets, s->E, s2, none, Tk, st, &bad);
   if (bad) return MOE_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  if (comb && !s->F) {
-    if (mark) prof_mark(4, st);
-    e = launch_combine(y_perm, nullptr, comb->inv_pos, comb->gate, comb->residual, out, s->T,
-                       s->k, s->d, st);
+  if (comb) {
+    if (mark) prof_mark("combine", st);
+    e = launch_combine(y_perm, s->F ? shared_out : nullptr, comb->inv_pos, comb->gate,
+                       comb->residual, out, s->T, s->k, s->d, st);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   return MOE_OK;
@@ -242,6 +270,7 @@ moe_status_t run_ffn_int4(const moe_shape_t* s, const void* x_bf16, const LayerW
   GemmOperandSet off{};
   CombineInputs none{};
   cudaError_t e = cudaSuccess;
+  if (mark) prof_mark("gate_up_and_int4_experts", st);
   if (s->F) {
     GemmOperandSet s1{x_bf16, s->T, w->shared_gate_up, 1, 2 * s->F, s->d, L.ffn.hs, s->F,
                       EPI_SWIGLU, s->T};
@@ -256,8 +285,7 @@ moe_status_t run_ffn_int4(const moe_shape_t* s, const void* x_bf16, const LayerW
     e = launch_int4_down(L.active, L.offsets, static_cast<const uint8_t*>(w->w_down),
                          static_cast<const uint16_t*>(w->scale_down), L.ffn.h, L.y, s->d, s->f, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  if (mark) prof_mark(3, st);
-  if (mark) prof_mark(4, st);
+  if (mark) prof_mark("shared_down_combine", st);
   CombineInputs comb{L.y, L.inv_pos, L.gate, static_cast<const uint16_t*>(residual), s->k};
   if (s->F) {
     GemmOperandSet s2{L.ffn.hs, s->T, w->shared_down, 1, s->d, s->F, out, s->d, EPI_COMBINE, s->T};
@@ -452,33 +480,67 @@ moe_status_t moe_layer_fwd(const moe_shape_t* shape, const void* x, const float*
   const int xf = shape->x_dtype == MOE_X_F32;
 
   const bool prof = prof_begin_call();
-  if (prof) prof_mark(0, s);
+  const bool tc = router_tc_supported(T, E, xf);
+  // Fork: the shared expert's gate/up needs only x, so it runs on the caller's stream
+  // (on most SMs) while the routing runs on a second stream (on the rest).
+  const bool fork = !int4 && !xf && shape->F > 0 && T >= 1024;
+  AuxStream* aux = nullptr;
+  std::unique_lock<std::mutex> aux_lock(g_aux_mu, std::defer_lock);
+  cudaStream_t rs = s;  // stream of the routing kernels
+  if (fork) {
+    aux_lock.lock();
+    aux = aux_for_current_device();
+    if (!aux) return MOE_ERR_CUDA;
+    rs = aux->s;
+    if (prof) prof_mark("shared_gate_up", s);
+    if (cudaEventRecord(aux->fork, s) != cudaSuccess ||
+        cudaStreamWaitEvent(rs, aux->fork, 0) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    const int pairs = gemm_max_pairs();
+    const int reserve = pairs >= 32 ? pairs / 6 : 0;  // SMs left for the routing
+    GemmOperandSet off{}, s1{x, T, w->shared_gate_up, 1, 2 * shape->F, shape->d, L.ffn.hs,
+                             shape->F, EPI_SWIGLU, T};
+    CombineInputs none{};
+    int bad = 0;
+    const cudaError_t eg = launch_grouped_gemm(off, L.offsets, E, s1, none, (long long)T * k, s,
+                                               &bad, pairs - reserve);
+    if (bad) return MOE_ERR_UNSUPPORTED;
+    if (eg != cudaSuccess) return MOE_ERR_CUDA;
+    if (prof) prof_mark("routing_wait", s);
+  } else if (prof) {
+    prof_mark("router", s);
+  }
   // The tensor-core router's first kernel zeroes load and counts itself.
-  if (!router_tc_supported(T, E, xf)) {
-    if (cudaMemsetAsync(L.load, 0, sizeof(int32_t) * E, s) != cudaSuccess) return MOE_ERR_CUDA;
-    if (cudaMemsetAsync(L.perm.counts, 0, sizeof(int32_t) * chunks * E, s) != cudaSuccess)
+  if (!tc) {
+    if (cudaMemsetAsync(L.load, 0, sizeof(int32_t) * E, rs) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(L.perm.counts, 0, sizeof(int32_t) * chunks * E, rs) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
   RouterArgs ra{x, xf, w_router, logit_offset, bias, dbg ? dbg->scores : nullptr, L.idx, L.gate,
                 L.load, L.perm.counts, ct, T, shape->d, E, k, shape->renorm};
-  cudaError_t e = run_router(ra, L.router, s);
-  if (prof) prof_mark(1, s);
+  cudaError_t e = run_router(ra, L.router, rs);
+  if (prof && !fork) prof_mark("permute_gather", s);
   // The scatter launch derives the offsets from the counts and applies the bias
   // update (after the router has read the bias).
   if (e == cudaSuccess)
     e = launch_scatter(L.idx, L.perm.counts, T, k, E, ct, L.offsets, nullptr,
                        update_bias ? bias : nullptr, gamma, (long long)T * k, L.perm_tok,
                        L.inv_pos, x, xf, shape->d, L.ffn.xp, (xf && shape->F) ? L.ffn.xb : nullptr,
-                       s, int4 ? L.active : nullptr);
-  if (prof) prof_mark(2, s);
+                       rs, int4 ? L.active : nullptr);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (fork) {
+    if (cudaEventRecord(aux->join, rs) != cudaSuccess ||
+        cudaStreamWaitEvent(s, aux->join, 0) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    aux_lock.unlock();
+  }
   const void* xbf = xf ? L.ffn.xb : x;
   CombineInputs comb{L.y, L.inv_pos, L.gate, static_cast<const uint16_t*>(residual), k};
   const moe_status_t st2 =
       int4 ? run_ffn_int4(shape, xbf, L, w, residual, static_cast<uint16_t*>(out), s, prof)
-           : run_ffn(shape, xbf, L.offsets, w, L.ffn, L.y, nullptr, &comb,
-                     static_cast<uint16_t*>(out), s, prof);
-  if (prof) prof_mark(kStages, s);
+           : run_ffn(shape, xbf, L.offsets, w, L.ffn, L.y, L.s_out, &comb,
+                     static_cast<uint16_t*>(out), s, prof, fork);
+  if (prof) prof_mark(nullptr, s);
   return st2;
 }
 
@@ -506,7 +568,9 @@ moe_status_t moe_quantize_int4(int64_t rows, int32_t K, const void* w, void* q, 
 int32_t moe_profile_stage_count(void) { return kStages; }
 
 const char* moe_profile_stage_name(int32_t stage) {
-  return (stage >= 0 && stage < kStages) ? kStageNames[stage] : "";
+  if (stage < 0 || stage >= kStages) return "";
+  const char* n = g_prof.names[stage];
+  return n ? n : "";
 }
 
 moe_status_t moe_profile_start(int32_t max_calls, int32_t period) {
@@ -516,6 +580,7 @@ moe_status_t moe_profile_start(int32_t max_calls, int32_t period) {
   g_prof.ev.assign((size_t)max_calls * (kStages + 1), nullptr);
   for (auto& ev : g_prof.ev)
     if (cudaEventCreate(&ev) != cudaSuccess) return MOE_ERR_CUDA;
+  for (auto& n : g_prof.names) n = nullptr;
   g_prof.max_calls = max_calls;
   g_prof.calls = 0;
   g_prof.period = period;
@@ -533,13 +598,9 @@ moe_status_t moe_profile_stop(float* ms_per_stage, int32_t* calls) {
   for (int c = 0; c < g_prof.calls; ++c) {
     cudaEvent_t* ev = &g_prof.ev[(size_t)c * (kStages + 1)];
     if (cudaEventSynchronize(ev[kStages]) != cudaSuccess) return MOE_ERR_CUDA;
-    // Stages a call did not reach keep their previous mark: walk forward from it.
-    int last = 0;
-    for (int i = 1; i <= kStages; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       float ms = 0.f;
-      if (cudaEventElapsedTime(&ms, ev[last], ev[i]) != cudaSuccess) continue;
-      ms_per_stage[i - 1] += ms;
-      last = i;
+      if (cudaEventElapsedTime(&ms, ev[i], ev[i + 1]) == cudaSuccess) ms_per_stage[i] += ms;
     }
   }
   return MOE_OK;

@@ -243,6 +243,8 @@ __global__ void combine_kernel(const uint16_t* __restrict__ y, const uint16_t* _
                                const int32_t* __restrict__ inv_pos, const float* __restrict__ gate,
                                const uint16_t* __restrict__ residual, uint16_t* __restrict__ out,
                                int T, int k, int d) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // y / shared come from the GEMM
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int vpr = d / 8;
   const long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (v >= (long long)T * vpr) return;
@@ -329,9 +331,8 @@ cudaError_t launch_combine(const uint16_t* y_perm, const uint16_t* shared_out,
                            const int32_t* inv_pos, const float* gate, const uint16_t* residual,
                            uint16_t* out, int T, int k, int d, cudaStream_t s) {
   const long long n = (long long)T * (d / 8);
-  combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(y_perm, shared_out, inv_pos, gate,
-                                                               residual, out, T, k, d);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, y_perm,
+                    shared_out, inv_pos, gate, residual, out, T, k, d);
 }
 
 cudaError_t launch_pack_gate_up(int G, int width, int d, int block, const uint16_t* wg,

@@ -196,8 +196,11 @@ moe_status_t moe_bias_update(int32_t E, int64_t tokens_times_k, const int32_t* l
                              float gamma, float* bias, void* stream);
 
 /* The whole layer: route, permute, gather, grouped expert FFN, shared expert,
- * combine and (if update_bias) the bias update, enqueued on one stream with no
- * host synchronisation.  bias is read for selection and then updated in place.
+ * combine and (if update_bias) the bias update, enqueued with no host
+ * synchronisation.  With bf16 tokens, F > 0 and T >= 1024 the routing runs on a
+ * library-owned second stream (one per device, created on first use, joined back
+ * with events) while the shared expert's gate/up GEMM runs on `stream`; all work is
+ * ordered before anything enqueued on `stream` after the call.  bias is read for selection and then updated in place.
  * residual (NULL or [T][d], same dtype as out) is added to the output.  For
  * MOE_W_INT4_G32 the routed experts run through the int4 dequant-in-GEMM path.
  *   out        [T][d] bf16
@@ -225,9 +228,11 @@ moe_status_t moe_quantize_int4(int64_t rows, int32_t K, const void* w, void* q, 
                                void* stream);
 
 /* Per-stage timing of moe_layer_fwd (profiling aid).  While enabled, every
- * moe_layer_fwd call records CUDA events on its stream between its stages (router,
- * permutation + gather, gate/up GEMM, routed down GEMM, shared down GEMM with the
- * fused combine).  moe_profile_start(max_calls, period) records every period-th call,
+ * moe_layer_fwd call records CUDA events on its stream between its stages; after
+ * moe_profile_stop, moe_profile_stage_name(i) names stage i of the recorded calls
+ * ("" for an unused slot).  On the large bf16 path the stages are the shared-expert
+ * gate/up GEMM (while the routing runs on a second stream), the remaining wait for
+ * the routing, the routed gate/up GEMM, the down GEMM and the combine.  moe_profile_start(max_calls, period) records every period-th call,
  * up to max_calls recorded calls (host-side event objects only, no device memory;
  * each event adds about 2 us to the stream, hence the sampling period);
  * moe_profile_stop synchronises, writes the summed milliseconds of each stage over

@@ -355,3 +355,26 @@ def test_stack_23_layers_with_residual():
                                                   bf64(H["w_down"][e]))[0]
             want[i] += y
         assert_close_bf16(bf16_to_np(acts[l + 1])[sample], want, f"stack layer {l}")
+
+
+def test_expert_ffn_outputs_only_16_byte_aligned():
+    """The ABI promises 16-byte alignment only: outputs offset by 16 bytes from a
+    32-byte boundary take the 128-bit store path and must give the same result."""
+    s = CONFIGS["nano"].replace(T=512)
+    host = make_layer(s, "nano")
+    layer = LayerOnDevice(s, host, DEV)
+    x = to_device_tokens(host["x"], DEV)
+    sc = O.router_scores(tokens64(host["x"]), host["w_router"]).astype(np.float32)
+    ref = _oracle_layer(s, host, sc)
+    offsets = torch.from_numpy(ref["offsets"].astype(np.int32)).to(DEV)
+    perm = torch.from_numpy(ref["perm_tok"].astype(np.int32)).to(DEV)
+    ybuf = torch.empty(s.T * s.k * s.d + 8, dtype=torch.bfloat16, device=DEV)
+    sbuf = torch.empty(s.T * s.d + 8, dtype=torch.bfloat16, device=DEV)
+    y = ybuf[8:].view(s.T * s.k, s.d)     # 16 bytes past the allocation's start
+    sh = sbuf[8:].view(s.T, s.d)
+    assert y.data_ptr() % 32 == 16 and sh.data_ptr() % 32 == 16
+    ws = torch.empty(M.moe_expert_ffn_workspace_size(layer.shape), dtype=torch.uint8, device=DEV)
+    M.moe_expert_ffn(layer.shape, x, offsets, perm, layer.weights, y, sh, ws)
+    torch.cuda.synchronize()
+    assert_close_bf16(bf16_to_np(y), ref["Y"], "y_perm (16-byte aligned)")
+    assert_close_bf16(bf16_to_np(sh), ref["shared"], "shared_out (16-byte aligned)")
