@@ -238,26 +238,39 @@ __global__ void bias_update_kernel(int E, long long tokens_times_k, const int32_
 }
 
 // out[t] = residual[t] + shared[t] + sum_j gate[t][j] * y[inv_pos[t][j]]; one thread per
-// 8 output columns, fp32 sum, one rounding to bf16.
+// 16 output columns (32-byte loads and stores when every row starts on a 32-byte
+// boundary, else two 16-byte halves), fp32 sum, one rounding to bf16.
+__device__ __forceinline__ void load16_bf16(const uint16_t* row, int v8, uint32_t (&w)[8]) {
+  if (v8) {
+    asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
+                   "=r"(w[7])
+                 : "l"(row));
+  } else {
+    const uint4 a = reinterpret_cast<const uint4*>(row)[0], b = reinterpret_cast<const uint4*>(row)[1];
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+  }
+}
+
 __global__ void combine_kernel(const uint16_t* __restrict__ y, const uint16_t* __restrict__ shared,
                                const int32_t* __restrict__ inv_pos, const float* __restrict__ gate,
                                const uint16_t* __restrict__ residual, uint16_t* __restrict__ out,
-                               int T, int k, int d) {
+                               int T, int k, int d, int v8) {
   asm volatile("griddepcontrol.wait;" ::: "memory");  // y / shared come from the GEMM
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int vpr = d / 8;
+  const int vpr = d / 16;
   const long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (v >= (long long)T * vpr) return;
   const long long t = v / vpr;
-  const int c = (int)(v % vpr);
-  float acc[8];
+  const int c = (int)(v % vpr) * 16;
+  float acc[16];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
   auto add_row = [&](const uint16_t* row, float w) {
-    const uint4 u = reinterpret_cast<const uint4*>(row)[c];
-    const uint32_t ws[4] = {u.x, u.y, u.z, u.w};
+    uint32_t ws[8];
+    load16_bf16(row + c, v8, ws);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 8; ++i) {
       acc[2 * i] = fmaf(w, bf16_lo(ws[i]), acc[2 * i]);
       acc[2 * i + 1] = fmaf(w, bf16_hi(ws[i]), acc[2 * i + 1]);
     }
@@ -265,9 +278,18 @@ __global__ void combine_kernel(const uint16_t* __restrict__ y, const uint16_t* _
   if (residual) add_row(residual + t * d, 1.f);
   if (shared) add_row(shared + t * d, 1.f);
   for (int j = 0; j < k; ++j) add_row(y + (long long)inv_pos[t * k + j] * d, gate[t * k + j]);
-  reinterpret_cast<uint4*>(out + t * d)[c] =
-      make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                 pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+  uint32_t p[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) p[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+  uint16_t* dst = out + t * d + c;
+  if (v8) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(p[0]),
+                 "r"(p[1]), "r"(p[2]), "r"(p[3]), "r"(p[4]), "r"(p[5]), "r"(p[6]), "r"(p[7])
+                 : "memory");
+  } else {
+    reinterpret_cast<uint4*>(dst)[0] = make_uint4(p[0], p[1], p[2], p[3]);
+    reinterpret_cast<uint4*>(dst)[1] = make_uint4(p[4], p[5], p[6], p[7]);
+  }
 }
 
 __global__ void pack_gate_up_kernel(int width, int d, int block, const uint16_t* __restrict__ wg,
@@ -330,9 +352,13 @@ cudaError_t launch_bias_update(int E, long long tokens_times_k, const int32_t* l
 cudaError_t launch_combine(const uint16_t* y_perm, const uint16_t* shared_out,
                            const int32_t* inv_pos, const float* gate, const uint16_t* residual,
                            uint16_t* out, int T, int k, int d, cudaStream_t s) {
-  const long long n = (long long)T * (d / 8);
+  const long long n = (long long)T * (d / 16);
+  auto a32 = [](const void* p) { return reinterpret_cast<uintptr_t>(p) % 32 == 0; };
+  // d % 64 == 0, so every row starts on a 32-byte boundary when its base does.
+  const int v8 = a32(y_perm) && a32(out) && (!shared_out || a32(shared_out)) &&
+                 (!residual || a32(residual));
   return launch_pdl(combine_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, y_perm,
-                    shared_out, inv_pos, gate, residual, out, T, k, d);
+                    shared_out, inv_pos, gate, residual, out, T, k, d, v8);
 }
 
 cudaError_t launch_pack_gate_up(int G, int width, int d, int block, const uint16_t* wg,

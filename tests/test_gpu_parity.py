@@ -378,3 +378,10 @@ def test_expert_ffn_outputs_only_16_byte_aligned():
     torch.cuda.synchronize()
     assert_close_bf16(bf16_to_np(y), ref["Y"], "y_perm (16-byte aligned)")
     assert_close_bf16(bf16_to_np(sh), ref["shared"], "shared_out (16-byte aligned)")
+    obuf = torch.empty(s.T * s.d + 8, dtype=torch.bfloat16, device=DEV)
+    out = obuf[8:].view(s.T, s.d)
+    inv = torch.from_numpy(ref["inv_pos"].astype(np.int32)).to(DEV)
+    gate = torch.from_numpy(ref["gate"].astype(np.float32)).to(DEV)
+    M.moe_combine(layer.shape, y, sh, inv, gate, None, out)
+    torch.cuda.synchronize()
+    assert_close_bf16(bf16_to_np(out), ref["out"], "combine (16-byte aligned)")
