@@ -42,14 +42,17 @@ namespace {
 constexpr int BM = 256;        // rows per CTA-pair tile
 constexpr int HM = 128;        // rows per CTA
 constexpr int AK = 64;         // K width of one 128-byte swizzle atom (bf16)
-constexpr int BK = 2 * AK;     // K per pipeline stage: 8 MMAs per barrier round
+constexpr int ATOMS = 2;       // swizzle atoms per pipeline stage
+constexpr int BK = ATOMS * AK; // K per pipeline stage: 8 MMAs per barrier round
 constexpr int BN_MAX = 256;
 constexpr int STAGES = 3;
 constexpr int A_ATOM = HM * AK * 2;               // 16 KB: 128 rows x 64
 constexpr int B_ATOM = (BN_MAX / 2) * AK * 2;     // 16 KB: up to 128 rows (half of B) x 64
-constexpr int A_BYTES = 2 * A_ATOM;
-constexpr int STAGE_BYTES = A_BYTES + 2 * B_ATOM; // 64 KB
+constexpr int A_BYTES = ATOMS * A_ATOM;
+constexpr int STAGE_BYTES = A_BYTES + ATOMS * B_ATOM; // 64 KB
 constexpr int EPI_WARPS = 8;
+constexpr int EPI_GROUPS = EPI_WARPS / 4;  // warps per TMEM lane quadrant
+constexpr int CS = 32 * EPI_GROUPS;        // column stride between one warp's chunks
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 2 * BN_MAX;
 constexpr int DYN_SMEM = STAGES * STAGE_BYTES + 1024;
@@ -167,8 +170,7 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, int tile, int share
                                             const int* s_off, const int* s_cum, int total) {
   const int routed_tiles = total - shared_tiles;
   if (shared_tiles > 0 && routed_tiles > 0) {
-    // 32-bit arithmetic (tile counts stay far below 2^15): this runs between tiles on
-    // the MMA thread's critical path.
+    // 32-bit arithmetic (tile counts stay far below 2^15).
     const unsigned r_before = (unsigned)tile * (unsigned)routed_tiles / (unsigned)total;
     const unsigned r_after = (unsigned)(tile + 1) * (unsigned)routed_tiles / (unsigned)total;
     tile = (r_after > r_before) ? shared_tiles + (int)r_before : tile - (int)r_before;
@@ -202,6 +204,18 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, int tile, int share
   return t;
 }
 
+// Which operand set a tile belongs to (1 = routed), by the same interleave as
+// decode_tile: all the MMA issuer needs, without the search over the groups.
+__device__ __forceinline__ int tile_set(int tile, int shared_tiles, int total) {
+  const int routed_tiles = total - shared_tiles;
+  if (shared_tiles > 0 && routed_tiles > 0) {
+    const unsigned r_before = (unsigned)tile * (unsigned)routed_tiles / (unsigned)total;
+    const unsigned r_after = (unsigned)(tile + 1) * (unsigned)routed_tiles / (unsigned)total;
+    return r_after > r_before ? 1 : 0;
+  }
+  return shared_tiles > 0 && tile < shared_tiles ? 0 : 1;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
@@ -211,11 +225,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // very negative a the denominator overflows and the quotient is the correct 0.
 __device__ __forceinline__ float silu(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
 
-__device__ __forceinline__ void add_bf16_row32(float (&o)[32], const uint16_t* src, float w) {
+// 32 bf16 values (64 bytes), cached in L2 only (gathered rows, used once).
+__device__ __forceinline__ void load_row32(const uint16_t* src, uint4 (&u)[4]) {
   const uint4* s = reinterpret_cast<const uint4*>(src);
-  uint4 u[4];
 #pragma unroll
-  for (int v = 0; v < 4; ++v) u[v] = s[v];
+  for (int v = 0; v < 4; ++v) u[v] = __ldcg(s + v);
+}
+
+// o += w * (32 bf16 values in u).
+__device__ __forceinline__ void accumulate_row32(float (&o)[32], const uint4 (&u)[4], float w) {
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
     const uint32_t ws[4] = {u[v].x, u[v].y, u[v].z, u[v].w};
@@ -225,6 +243,12 @@ __device__ __forceinline__ void add_bf16_row32(float (&o)[32], const uint16_t* s
       o[v * 8 + 2 * i + 1] = fmaf(w, __uint_as_float(ws[i] & 0xFFFF0000u), o[v * 8 + 2 * i + 1]);
     }
   }
+}
+
+__device__ __forceinline__ void add_bf16_row32(float (&o)[32], const uint16_t* src, float w) {
+  uint4 u[4];
+  load_row32(src, u);
+  accumulate_row32(o, u, w);
 }
 
 // 32 values -> 64 bytes of bf16.  With v8, two 256-bit stores: half the store
@@ -346,7 +370,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           // Atoms entirely past K are not loaded (and not multiplied).
-          const int natoms = S.k_total - kb * BK > AK ? 2 : 1;
+          const int natoms = min(ATOMS, (S.k_total - kb * BK + AK - 1) / AK);
           const uint32_t pair_bytes = 2u * natoms * (A_ATOM + half * AK * 2);
           const uint32_t sa = ring + stage * STAGE_BYTES;
           const uint32_t fb = map_to_rank(smem_u32(&full_bar[stage]), 0);
@@ -372,14 +396,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ------------------------------------------------ MMA issuer (leader only)
+      // The loop body is kept to the barrier waits and the MMAs: the operand set's
+      // fields are read (as plain kernel-parameter loads) once per tile, not through a
+      // reference into parameter space on every k-block.
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = cluster; tile < total && ok; tile += nclusters) {
-        const Tile t = decode_tile(p, tile, shared_tiles, s_off, s_cum, total);
-        const OperandSet& S = t.set ? p.routed : p.shared;
-        const int nkb = (S.k_total + BK - 1) / BK;
-        const uint32_t idesc = idesc_bf16_f32(BM, S.bn);
+        const int set = tile_set(tile, shared_tiles, total);
+        const int k_total = set ? p.routed.k_total : p.shared.k_total;
+        const int bn = set ? p.routed.bn : p.shared.bn;
+        const int nkb = (k_total + BK - 1) / BK;
+        const int nkk_last = (k_total - (nkb - 1) * BK + 15) / 16;
+        const uint32_t idesc = idesc_bf16_f32(BM, bn);
         if (!mbar_wait_spin(smem_u32(&tempty_bar[acc]), acc_phase ^ 1u, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN_MAX;
@@ -390,13 +419,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           }
           tc_fence_after();
           const uint32_t sa = ring + stage * STAGE_BYTES;
-          const int kleft = S.k_total - kb * BK;
-          const int nkk = kleft >= BK ? BK / 16 : (kleft + 15) / 16;
-          for (int kk = 0; kk < nkk; ++kk) {
-            const int at = kk >> 2, w = kk & 3;
-            const uint64_t adesc = sw128_kmajor_desc(sa + at * A_ATOM);
-            const uint64_t bdesc = sw128_kmajor_desc(sa + A_BYTES + at * B_ATOM);
-            mma_pair_bf16(d_tmem, adesc + 2 * w, bdesc + 2 * w, idesc, (kb | kk) != 0);
+          uint64_t adesc[ATOMS], bdesc[ATOMS];
+#pragma unroll
+          for (int at = 0; at < ATOMS; ++at) {
+            adesc[at] = sw128_kmajor_desc(sa + at * A_ATOM);
+            bdesc[at] = sw128_kmajor_desc(sa + A_BYTES + at * B_ATOM);
+          }
+          if (kb + 1 < nkb) {
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              mma_pair_bf16(d_tmem, adesc[kk >> 2] + 2 * (kk & 3), bdesc[kk >> 2] + 2 * (kk & 3),
+                            idesc, (kb | kk) != 0);
+          } else {
+            for (int kk = 0; kk < nkk_last; ++kk)
+              mma_pair_bf16(d_tmem, adesc[kk >> 2] + 2 * (kk & 3), bdesc[kk >> 2] + 2 * (kk & 3),
+                            idesc, (kb | kk) != 0);
           }
           commit_pair_multicast(smem_u32(&empty_bar[stage]));
           if (++stage == STAGES) {
@@ -416,7 +453,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   } else {
     // -------------------------------------------------- epilogue (warps 2..9)
     const int q = warp & 3;                 // TMEM lanes [32q, 32q + 32) are this warp's rows
-    const int colh = (warp - 2) / 4;        // which interleaved half of the column chunks
+    const int colh = (warp - 2) / 4;        // which interleaved share of the column chunks
     const uint32_t tempty_leader0 = map_to_rank(smem_u32(&tempty_bar[0]), 0);
     const uint32_t tempty_leader1 = map_to_rank(smem_u32(&tempty_bar[1]), 0);
     int acc = 0;
@@ -436,7 +473,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       uint16_t* out = static_cast<uint16_t*>(S.out);
       if (S.mode == EPI_SWIGLU) {
         const int half = S.bn / 2;
-        for (int c = 32 * colh; c < half; c += 64) {
+        for (int c = 32 * colh; c < half; c += CS) {
           uint32_t g[32], u[32];
           tmem_ld32(tbase + c, g);
           tmem_ld32(tbase + half + c, u);
@@ -448,11 +485,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         }
       } else if (S.mode == EPI_STORE) {
         // Two 32-column chunks per TMEM round trip.
-        for (int c = 32 * colh; c < S.bn; c += 128) {
-          const bool two = c + 64 < S.bn;  // warp-uniform
+        for (int c = 32 * colh; c < S.bn; c += 2 * CS) {
+          const bool two = c + CS < S.bn;  // warp-uniform
           uint32_t v[32], w[32];
           tmem_ld32(tbase + c, v);
-          if (two) tmem_ld32(tbase + c + 64, w);
+          if (two) tmem_ld32(tbase + c + CS, w);
           tmem_wait_ld();
           float o[32];
 #pragma unroll
@@ -461,7 +498,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           if (two) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(w[i]);
-            if (valid) store_bf16_row32(out + orow * S.ldo + t.n0 + c + 64, o, S.v8);
+            if (valid) store_bf16_row32(out + orow * S.ldo + t.n0 + c + CS, o, S.v8);
           }
         }
       } else {
@@ -476,18 +513,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             pj[j] = p.inv_pos[orow * p.k + j];
           }
         }
-        for (int c = 32 * colh; c < S.bn; c += 64) {
+        for (int c = 32 * colh; c < S.bn; c += CS) {
           uint32_t v[32];
           tmem_ld32(tbase + c, v);
+          // The residual and the first two routed rows are requested together, and
+          // while the accumulator chunk is read, so their latencies overlap.
+          const long long col = t.n0 + c;
+          uint4 ur[4], u0[4], u1[4];
+          if (valid) {
+            if (p.residual) load_row32(p.residual + orow * S.ldo + col, ur);
+            if (p.k > 0) load_row32(p.y_perm + pj[0] * S.ldo + col, u0);
+            if (p.k > 1) load_row32(p.y_perm + pj[1] * S.ldo + col, u1);
+          }
           tmem_wait_ld();
           float o[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(v[i]);
           if (valid) {
-            const long long col = t.n0 + c;
-            if (p.residual) add_bf16_row32(o, p.residual + orow * S.ldo + col, 1.f);
+            if (p.residual) accumulate_row32(o, ur, 1.f);
+            if (p.k > 0) accumulate_row32(o, u0, gj[0]);
+            if (p.k > 1) accumulate_row32(o, u1, gj[1]);
 #pragma unroll
-            for (int j = 0; j < kMaxK; ++j)
+            for (int j = 2; j < kMaxK; ++j)
               if (j < p.k) add_bf16_row32(o, p.y_perm + pj[j] * S.ldo + col, gj[j]);
             store_bf16_row32(out + orow * S.ldo + col, o, S.v8);
           }
@@ -496,6 +543,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
+
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }

@@ -252,6 +252,10 @@ __device__ __forceinline__ void load16_bf16(const uint16_t* row, int v8, uint32_
   }
 }
 
+// out[t] = residual[t] + shared[t] + sum_j gate[t][j] * y[inv_pos[t][j]], 16 columns
+// per thread.  With KC = k (1 or 2) every row load of a thread is issued before the
+// first use, so only the inv_pos -> y dependency is exposed; KC = 0 loops over k.
+template <int KC>
 __global__ void combine_kernel(const uint16_t* __restrict__ y, const uint16_t* __restrict__ shared,
                                const int32_t* __restrict__ inv_pos, const float* __restrict__ gate,
                                const uint16_t* __restrict__ residual, uint16_t* __restrict__ out,
@@ -266,18 +270,45 @@ __global__ void combine_kernel(const uint16_t* __restrict__ y, const uint16_t* _
   float acc[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-  auto add_row = [&](const uint16_t* row, float w) {
-    uint32_t ws[8];
-    load16_bf16(row + c, v8, ws);
+  auto add = [&](const uint32_t (&ws)[8], float w) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       acc[2 * i] = fmaf(w, bf16_lo(ws[i]), acc[2 * i]);
       acc[2 * i + 1] = fmaf(w, bf16_hi(ws[i]), acc[2 * i + 1]);
     }
   };
-  if (residual) add_row(residual + t * d, 1.f);
-  if (shared) add_row(shared + t * d, 1.f);
-  for (int j = 0; j < k; ++j) add_row(y + (long long)inv_pos[t * k + j] * d, gate[t * k + j]);
+  if (KC > 0) {
+    int pos[KC > 0 ? KC : 1];
+    float g[KC > 0 ? KC : 1];
+#pragma unroll
+    for (int j = 0; j < KC; ++j) {
+      pos[j] = inv_pos[t * KC + j];
+      g[j] = gate[t * KC + j];
+    }
+    uint32_t wr[8], wsh[8], wy[KC > 0 ? KC : 1][8];
+    if (residual) load16_bf16(residual + t * d + c, v8, wr);
+    if (shared) load16_bf16(shared + t * d + c, v8, wsh);
+#pragma unroll
+    for (int j = 0; j < KC; ++j) load16_bf16(y + (long long)pos[j] * d + c, v8, wy[j]);
+    if (residual) add(wr, 1.f);
+    if (shared) add(wsh, 1.f);
+#pragma unroll
+    for (int j = 0; j < KC; ++j) add(wy[j], g[j]);
+  } else {
+    uint32_t ws[8];
+    if (residual) {
+      load16_bf16(residual + t * d + c, v8, ws);
+      add(ws, 1.f);
+    }
+    if (shared) {
+      load16_bf16(shared + t * d + c, v8, ws);
+      add(ws, 1.f);
+    }
+    for (int j = 0; j < k; ++j) {
+      load16_bf16(y + (long long)inv_pos[t * k + j] * d + c, v8, ws);
+      add(ws, gate[t * k + j]);
+    }
+  }
   uint32_t p[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) p[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
@@ -357,8 +388,15 @@ cudaError_t launch_combine(const uint16_t* y_perm, const uint16_t* shared_out,
   // d % 64 == 0, so every row starts on a 32-byte boundary when its base does.
   const int v8 = a32(y_perm) && a32(out) && (!shared_out || a32(shared_out)) &&
                  (!residual || a32(residual));
-  return launch_pdl(combine_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, y_perm,
-                    shared_out, inv_pos, gate, residual, out, T, k, d, v8);
+  const dim3 grid((unsigned)((n + 255) / 256));
+  if (k == 1)
+    return launch_pdl(combine_kernel<1>, grid, dim3(256), 0, s, y_perm, shared_out, inv_pos, gate,
+                      residual, out, T, k, d, v8);
+  if (k == 2)
+    return launch_pdl(combine_kernel<2>, grid, dim3(256), 0, s, y_perm, shared_out, inv_pos, gate,
+                      residual, out, T, k, d, v8);
+  return launch_pdl(combine_kernel<0>, grid, dim3(256), 0, s, y_perm, shared_out, inv_pos, gate,
+                    residual, out, T, k, d, v8);
 }
 
 cudaError_t launch_pack_gate_up(int G, int width, int d, int block, const uint16_t* wg,
