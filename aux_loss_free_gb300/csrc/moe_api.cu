@@ -226,26 +226,31 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x_bf16, const int32_t* of
                      cudaStream_t st, bool mark = false, bool shared_gate_up_done = false) {
   const long long Tk = (long long)s->T * s->k;
   int bad = 0;
+  CombineInputs none{};
   GemmOperandSet r1{ws.xp, Tk, w->w_gate_up, s->E, 2 * s->f, s->d, ws.h, s->f, EPI_SWIGLU, 0};
+  GemmOperandSet sd{};
+  if (s->F)
+    sd = GemmOperandSet{ws.hs, s->T, w->shared_down, 1, s->d, s->F, shared_out, s->d, EPI_STORE, s->T};
+  // Each launch pairs tiles that stream expert weights (memory bound) with shared-
+  // expert tiles (compute bound), interleaved.  With the shared gate/up already done,
+  // the routed gate/up runs beside the shared down projection and the routed down
+  // projection runs alone; otherwise the two gate/up sets share one launch and the
+  // two down projections the next.
   GemmOperandSet s1{};
   if (s->F && !shared_gate_up_done)
     s1 = GemmOperandSet{x_bf16, s->T, w->shared_gate_up, 1, 2 * s->F, s->d, ws.hs, s->F,
                         EPI_SWIGLU, s->T};
-  CombineInputs none{};
-  if (mark) prof_mark(shared_gate_up_done ? "routed_gate_up" : "gemm_gate_up", st);
+  else if (s->F)
+    s1 = sd;
+  if (mark) prof_mark(shared_gate_up_done ? "routed_gate_up_shared_down" : "gemm_gate_up", st);
   cudaError_t e = launch_grouped_gemm(r1, offsets, s->E, s1, none, Tk, st, &bad);
   if (bad) return MOE_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   GemmOperandSet r2{ws.h, Tk, w->w_down, s->E, s->d, s->f, y_perm, s->d, EPI_STORE, 0};
   GemmOperandSet s2{};
-  if (s->F)
-    s2 = GemmOperandSet{ws.hs, s->T, w->shared_down, 1, s->d, s->F, shared_out, s->d, EPI_STORE, s->T};
-  if (mark) prof_mark("gemm_down", st);
-  // Both down projections in one launch (their tiles interleave: the routed ones
-  // stream expert weights, the shared ones are compute bound), then the combine.
-  if (comb && s->F)
-    s2 = GemmOperandSet{ws.hs, s->T, w->shared_down, 1, s->d, s->F, shared_out, s->d, EPI_STORE, s->T};
+  if (s->F && !shared_gate_up_done) s2 = sd;
+  if (mark) prof_mark(shared_gate_up_done ? "routed_down" : "gemm_down", st);
   e = launch_grouped_gemm(r2, offsets, s->E, s2, none, Tk, st, &bad);
   if (bad) return MOE_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return MOE_ERR_CUDA;
