@@ -36,6 +36,7 @@ constexpr int kDevCheck = 2;
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 8;
 constexpr int kRouterTokens = 32;   // tokens per router block
+constexpr int kRouterClusterMaxT = 256;  // up to this T the SIMT router uses CTA clusters
 
 // Tokens per permutation chunk: a multiple of kRouterTokens chosen so the chunk
 // count table (chunks x E int32) stays within kMaxCountEntries.

@@ -30,6 +30,89 @@ constexpr int MAXC = kMaxE / 32;   // experts per lane in the selection phase
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
+// Selection for one token by one warp, from its E logits (offset included): scores,
+// the biased top-k (k rounds of a warp-shuffle arg-max under key descending, expert
+// index ascending), gates, and the pair counts (into the block histogram `hist`, or
+// straight into the global load and chunk table when `hist` is null).
+__device__ __forceinline__ void select_token(const RouterArgs& a, const float* lg, int t, int lane,
+                                             int* hist) {
+  const unsigned FULL = 0xFFFFFFFFu;
+  constexpr int NONE = 0x7FFFFFFF;
+  const int E = a.E;
+  float sc[MAXC], key[MAXC];
+#pragma unroll
+  for (int i = 0; i < MAXC; ++i) {
+    const int e = lane + 32 * i;
+    sc[i] = 0.f;
+    key[i] = -INFINITY;
+    if (e < E) {
+      const float z = lg[e];
+      const float s = 1.0f / (1.0f + expf(-z));
+      sc[i] = s;
+      key[i] = __fadd_rn(s, a.bias[e]);  // selection key: one fp32 addition
+      if (a.scores) a.scores[(size_t)t * E + e] = s;
+    }
+  }
+  unsigned taken = 0;
+  float sel_s[kMaxK];
+  int sel_e[kMaxK];
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    sel_s[j] = 0.f;
+    sel_e[j] = 0;
+    if (j < a.k) {
+      float bk = -INFINITY;
+      int be = NONE;
+#pragma unroll
+      for (int i = 0; i < MAXC; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u) && (be == NONE || key[i] > bk)) {
+          bk = key[i];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ok = __shfl_xor_sync(FULL, bk, off);
+        const int oe = __shfl_xor_sync(FULL, be, off);
+        if (oe != NONE && (be == NONE || ok > bk || (ok == bk && oe < be))) {
+          bk = ok;
+          be = oe;
+        }
+      }
+      float sw = 0.f;
+      if ((be & 31) == lane) {
+        taken |= 1u << (be >> 5);
+#pragma unroll
+        for (int i = 0; i < MAXC; ++i)
+          if (i == (be >> 5)) sw = sc[i];
+      }
+      sel_s[j] = __shfl_sync(FULL, sw, be & 31);
+      sel_e[j] = be;
+    }
+  }
+  float denom = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j)
+    if (j < a.k) denom += sel_s[j];
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    if (j < a.k && lane == j) {
+      a.idx[(size_t)t * a.k + j] = sel_e[j];
+      a.gate[(size_t)t * a.k + j] = a.renorm ? __fdiv_rn(sel_s[j], denom) : sel_s[j];
+      if (!hist) {
+        atomicAdd(&a.load[sel_e[j]], 1);
+        if (a.counts) atomicAdd(&a.counts[(size_t)(t / a.chunk_tokens) * E + sel_e[j]], 1);
+      }
+    }
+  }
+  if (hist && lane == 0) {
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j)
+      if (j < a.k) atomicAdd(&hist[sel_e[j]], 1);
+  }
+}
+
 template <bool XF32>
 __global__ void __launch_bounds__(NTHR) router_kernel(RouterArgs a) {
   __shared__ __align__(16) float xs[KC][XS_LD];
@@ -108,79 +191,10 @@ __global__ void __launch_bounds__(NTHR) router_kernel(RouterArgs a) {
   __syncthreads();
 
   const int warp = tid / 32, lane = tid % 32;
-  const unsigned FULL = 0xFFFFFFFFu;
-  constexpr int NONE = 0x7FFFFFFF;
   for (int tok = warp; tok < RT; tok += NTHR / 32) {
     const int t = t0 + tok;
     if (t >= a.T) break;  // warp-uniform
-    float sc[MAXC], key[MAXC];
-#pragma unroll
-    for (int i = 0; i < MAXC; ++i) {
-      const int e = lane + 32 * i;
-      sc[i] = 0.f;
-      key[i] = -INFINITY;
-      if (e < E) {
-        const float z = logits[tok * LD + e];
-        const float s = 1.0f / (1.0f + expf(-z));
-        sc[i] = s;
-        key[i] = __fadd_rn(s, a.bias[e]);  // selection key: one fp32 addition
-        if (a.scores) a.scores[(size_t)t * E + e] = s;
-      }
-    }
-    unsigned taken = 0;
-    float sel_s[kMaxK];
-    int sel_e[kMaxK];
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      sel_s[j] = 0.f;
-      sel_e[j] = 0;
-      if (j < a.k) {
-        float bk = -INFINITY;
-        int be = NONE;
-#pragma unroll
-        for (int i = 0; i < MAXC; ++i) {
-          const int e = lane + 32 * i;
-          if (e < E && !((taken >> i) & 1u) && (be == NONE || key[i] > bk)) {
-            bk = key[i];
-            be = e;
-          }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          const float ok = __shfl_xor_sync(FULL, bk, off);
-          const int oe = __shfl_xor_sync(FULL, be, off);
-          if (oe != NONE && (be == NONE || ok > bk || (ok == bk && oe < be))) {
-            bk = ok;
-            be = oe;
-          }
-        }
-        float sw = 0.f;
-        if ((be & 31) == lane) {
-          taken |= 1u << (be >> 5);
-#pragma unroll
-          for (int i = 0; i < MAXC; ++i)
-            if (i == (be >> 5)) sw = sc[i];
-        }
-        sel_s[j] = __shfl_sync(FULL, sw, be & 31);
-        sel_e[j] = be;
-      }
-    }
-    float denom = 0.f;
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j)
-      if (j < a.k) denom += sel_s[j];
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      if (j < a.k && lane == j) {
-        a.idx[(size_t)t * a.k + j] = sel_e[j];
-        a.gate[(size_t)t * a.k + j] = a.renorm ? __fdiv_rn(sel_s[j], denom) : sel_s[j];
-      }
-    }
-    if (lane == 0) {
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j)
-        if (j < a.k) atomicAdd(&hist[sel_e[j]], 1);
-    }
+    select_token(a, &logits[tok * LD], t, lane, hist);
   }
   __syncthreads();
   for (int e = tid; e < E; e += NTHR) {
@@ -192,9 +206,104 @@ __global__ void __launch_bounds__(NTHR) router_kernel(RouterArgs a) {
   }
 }
 
+
+// Small-T router: a cluster of CL CTAs per CTPB tokens.  CTA r of the cluster computes
+// the logits of experts [r*EPC, (r+1)*EPC) for the cluster's tokens, one warp per
+// expert row of W_r (read once, coalesced float4) against the tokens staged in shared
+// memory; CTA 0 then gathers all E logits over distributed shared memory and runs the
+// selection, one warp per token.  At T = 1 this spreads the 256 KB of W_r over
+// 64 warps on 8 SMs instead of one block.
+constexpr int CL = 8;
+constexpr int CTPB = 4;
+constexpr int CTHR = 256;
+
+template <bool XF32>
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(CTHR) router_cluster_kernel(RouterArgs a) {
+  extern __shared__ __align__(16) float csm[];
+  uint32_t rank;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int E = a.E, d = a.d;
+  const int EPC = (E + CL - 1) / CL;
+  const int t0 = (blockIdx.x / CL) * CTPB;
+  float* xs = csm;                 // [CTPB][d]
+  float* lg = xs + CTPB * d;       // [CTPB][EPC] this CTA's logits
+  float* all = lg + CTPB * EPC;    // [CTPB][E] (CTA 0)
+  for (int i = tid; i < CTPB * d; i += CTHR) {
+    const int tok = i / d, kk = i % d, t = t0 + tok;
+    float v = 0.f;
+    if (t < a.T) {
+      if (XF32)
+        v = static_cast<const float*>(a.x)[(size_t)t * d + kk];
+      else
+        v = bf16_bits_to_f32(static_cast<const uint16_t*>(a.x)[(size_t)t * d + kk]);
+    }
+    xs[i] = v;
+  }
+  __syncthreads();
+  const int e_begin = (int)rank * EPC, e_end = min(E, e_begin + EPC);
+  for (int e = e_begin + warp; e < e_end; e += CTHR / 32) {
+    float acc[CTPB];
+#pragma unroll
+    for (int tok = 0; tok < CTPB; ++tok) acc[tok] = 0.f;
+    const float* wr = a.w_router + (size_t)e * d;
+    for (int kk = lane * 4; kk < d; kk += 128) {
+      const float4 w = *reinterpret_cast<const float4*>(wr + kk);
+#pragma unroll
+      for (int tok = 0; tok < CTPB; ++tok) {
+        const float4 xv = *reinterpret_cast<const float4*>(xs + tok * d + kk);
+        acc[tok] = fmaf(w.x, xv.x, fmaf(w.y, xv.y, fmaf(w.z, xv.z, fmaf(w.w, xv.w, acc[tok]))));
+      }
+    }
+    const float off = a.logit_offset ? a.logit_offset[e] : 0.f;
+#pragma unroll
+    for (int tok = 0; tok < CTPB; ++tok) {
+      float v = acc[tok];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+      if (lane == 0) lg[tok * EPC + (e - e_begin)] = v + off;
+    }
+  }
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  if (rank == 0) {
+    const uint32_t lg_base = static_cast<uint32_t>(__cvta_generic_to_shared(lg));
+    for (int i = tid; i < CTPB * E; i += CTHR) {
+      const int tok = i / E, e = i % E;
+      const uint32_t src = (uint32_t)(e / EPC);
+      uint32_t remote;
+      const uint32_t local = lg_base + 4u * (uint32_t)(tok * EPC + e % EPC);
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(src));
+      float v;
+      asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+      all[i] = v;
+    }
+    __syncthreads();
+    if (warp < CTPB && t0 + warp < a.T) select_token(a, all + warp * E, t0 + warp, lane, nullptr);
+  }
+  // No CTA leaves while CTA 0 may still read its logits.
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 }  // namespace
 
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s) {
+  if (a.T <= kRouterClusterMaxT) {
+    // Few tokens: spread W_r over a cluster per CTPB tokens.
+    const int clusters = (a.T + CTPB - 1) / CTPB;
+    const int epc = (a.E + CL - 1) / CL;
+    const size_t dyn = sizeof(float) * ((size_t)CTPB * a.d + (size_t)CTPB * epc + (size_t)CTPB * a.E);
+    if (a.x_is_f32) {
+      cudaError_t e = cudaFuncSetAttribute(router_cluster_kernel<true>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+      if (e != cudaSuccess) return e;
+      router_cluster_kernel<true><<<clusters * CL, CTHR, dyn, s>>>(a);
+    } else {
+      cudaError_t e = cudaFuncSetAttribute(router_cluster_kernel<false>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+      if (e != cudaSuccess) return e;
+      router_cluster_kernel<false><<<clusters * CL, CTHR, dyn, s>>>(a);
+    }
+    return cudaGetLastError();
+  }
   const int blocks = (a.T + RT - 1) / RT;
   const size_t dyn = sizeof(float) * RT * (a.E + 1);
   if (a.x_is_f32) {

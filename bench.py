@@ -41,7 +41,7 @@ METRIC = "MoE-layer fwd tokens/s (T=8192,d=1024,64x512 top-2+2048 shared), % roo
 FLUSH_BYTES = 512 << 20
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_gate_up_nano_traffic.txt")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_shared_gate_up_nano_traffic.txt")
 PROFILE_PERIOD = 10
 
 
