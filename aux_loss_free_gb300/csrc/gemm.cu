@@ -633,6 +633,11 @@ bool fill_set(OperandSet& t, const GemmOperandSet& o) {
 
 }  // namespace
 
+bool make_tma_map_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+                       uint32_t box_outer) {
+  return make_map(m, ptr, inner, outer, box_outer);
+}
+
 int gemm_max_pairs() {
   if (cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            DYN_SMEM) != cudaSuccess)

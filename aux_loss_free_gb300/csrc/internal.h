@@ -130,6 +130,18 @@ cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* off
 int gemm_max_pairs();
 
 // ---------------------------------------------------------------- int4 serving
+// TMA descriptor for a bf16 matrix [outer][inner] (row-major), box [box_outer][64],
+// 128-byte swizzle.
+bool make_tma_map_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+                       uint32_t box_outer);
+// Shared-expert projections for T <= kSkinnyMaxT tokens (weights in the MMA's M, tokens
+// in N, K split over an 8-CTA cluster).  mode 0: w = gate/up [rows = 2F][K] interleaved
+// in blocks of 128 -> out = h [T][ldo] (SwiGLU); mode 1: w = down [rows = d][K] -> out
+// [T][ldo], plus comb's residual and gated routed rows when comb is given.
+constexpr int kSkinnyMaxT = 64;
+bool skinny_supported(int mode, int T, int rows, int K, int gate_block);
+cudaError_t launch_skinny(int mode, const uint16_t* w, int rows, int K, const uint16_t* x, int T,
+                          uint16_t* out, int ldo, const CombineInputs* comb, cudaStream_t s);
 cudaError_t launch_quantize_int4(long long rows, int K, const uint16_t* w, uint8_t* q,
                                  uint16_t* scale, cudaStream_t s);
 // `active` [kMaxE + 1]: ids of the experts with rows (ascending), count at [kMaxE].

@@ -276,7 +276,15 @@ moe_status_t run_ffn_int4(const moe_shape_t* s, const void* x_bf16, const LayerW
   CombineInputs none{};
   cudaError_t e = cudaSuccess;
   if (mark) prof_mark("gate_up_and_int4_experts", st);
-  if (s->F) {
+  // A few tokens: the shared expert streams its weights over 8-CTA clusters (weights in
+  // the MMA's M, tokens in N) instead of the 256-token tiles of the grouped GEMM.
+  const bool skinny = s->F && skinny_supported(0, s->T, 2 * s->F, s->d, moe_gate_up_block(s->F)) &&
+                      skinny_supported(1, s->T, s->d, s->F, 0);
+  if (skinny) {
+    e = launch_skinny(0, static_cast<const uint16_t*>(w->shared_gate_up), 2 * s->F, s->d,
+                      static_cast<const uint16_t*>(x_bf16), s->T, L.ffn.hs, s->F, nullptr, st);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  } else if (s->F) {
     GemmOperandSet s1{x_bf16, s->T, w->shared_gate_up, 1, 2 * s->F, s->d, L.ffn.hs, s->F,
                       EPI_SWIGLU, s->T};
     e = launch_grouped_gemm(off, L.offsets, s->E, s1, none, Tk, st, &bad);
@@ -292,7 +300,10 @@ moe_status_t run_ffn_int4(const moe_shape_t* s, const void* x_bf16, const LayerW
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (mark) prof_mark("shared_down_combine", st);
   CombineInputs comb{L.y, L.inv_pos, L.gate, static_cast<const uint16_t*>(residual), s->k};
-  if (s->F) {
+  if (skinny) {
+    e = launch_skinny(1, static_cast<const uint16_t*>(w->shared_down), s->d, s->F, L.ffn.hs, s->T,
+                      out, s->d, &comb, st);
+  } else if (s->F) {
     GemmOperandSet s2{L.ffn.hs, s->T, w->shared_down, 1, s->d, s->F, out, s->d, EPI_COMBINE, s->T};
     e = launch_grouped_gemm(off, L.offsets, s->E, s2, comb, Tk, st, &bad);
     if (bad) return MOE_ERR_UNSUPPORTED;
