@@ -63,54 +63,71 @@ cudaError_t launch_quantize_int4(long long rows, int K, const uint16_t* w, uint8
 // Relay article, "Entrenamiento por relevos", top-2 paragraph: at serving time the
 // engine runs one expert per token; opening section: experts ship as int4.  Only
 // the experts actually hit are read (the permutation's compact active list), each
-// weight row once, which makes the step bound by weight bytes.  Lane l of a warp
-// owns input group g = l, l + 32, ... (32 consecutive inputs, one fp16 scale),
-// dequantises w = q * scale and accumulates against the group's token values;
-// a warp reduction gives the row's dot product for every token of the expert.
+// weight row once, which makes the step bound by weight bytes.  A row's 32-input
+// groups are spread over the lanes; each lane turns its group's nibbles into the
+// integers q (exact in fp32), forms sum_i q_i * x_i for up to DEC_TOK tokens of the
+// expert at a time and scales the sum once by the group's fp16 scale, so a group is
+// dequantised once per pass over the expert's tokens.  A lane-group reduction gives
+// the row's dot products.
 namespace moe {
 namespace {
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  return v;
-}
+constexpr int DEC_WARPS = 8;
+constexpr int DEC_TOK = 4;  // tokens of one expert per pass
 
-// Dequantise one group: 16 bytes of two's-complement nibbles (even index low) and
-// its fp16 scale into 32 floats.
-__device__ __forceinline__ void dequant_group(const uint8_t* codes, uint16_t scale_bits, float (&w)[32]) {
+// Integer codes of one group: 16 bytes of two's-complement nibbles (even index in the
+// low nibble) -> 32 floats.  (c ^ 8) is q + 8 in [0, 15]; 2^23 + (q + 8) is exact in
+// fp32, so subtracting 2^23 + 8 gives q exactly.
+__device__ __forceinline__ void int4_codes(const uint8_t* codes, float (&q)[32]) {
   const uint4 u = *reinterpret_cast<const uint4*>(codes);
-  const float s = __half2float(__ushort_as_half(scale_bits));
   const uint32_t words[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int n = 0; n < 8; ++n) {
-      const int q = static_cast<int>((words[i] >> (4 * n)) & 0xFu);
-      w[8 * i + n] = static_cast<float>(q >= 8 ? q - 16 : q) * s;
+      const uint32_t c = ((words[i] >> (4 * n)) & 0xFu) ^ 0x8u;
+      q[8 * i + n] = __uint_as_float(0x4B000000u | c) - 8388616.0f;
     }
 }
 
-// 32 bf16 values (64 bytes) as floats.
-__device__ __forceinline__ void load_bf16x32(const uint16_t* p, float (&v)[32]) {
-  const uint4* q = reinterpret_cast<const uint4*>(p);
+__device__ __forceinline__ float scale_of(const uint16_t* ws, long long i) {
+  return __half2float(__ushort_as_half(ws[i]));
+}
+
+// sum_i q_i * x_i over the 32 bf16 values at p.
+__device__ __forceinline__ float dot32(const float (&q)[32], const uint16_t* p) {
+  const uint4* v = reinterpret_cast<const uint4*>(p);
+  float acc = 0.f;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint4 u = q[i];
+    const uint4 u = v[i];
     const uint32_t ws[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      v[8 * i + 2 * j] = __uint_as_float(ws[j] << 16);
-      v[8 * i + 2 * j + 1] = __uint_as_float(ws[j] & 0xFFFF0000u);
+      acc = fmaf(q[8 * i + 2 * j], __uint_as_float(ws[j] << 16), acc);
+      acc = fmaf(q[8 * i + 2 * j + 1], __uint_as_float(ws[j] & 0xFFFF0000u), acc);
     }
   }
+  return acc;
+}
+
+// Sum over the `width` lanes of this lane's group (width a power of two <= 32).
+__device__ __forceinline__ float group_sum(float v, int width) {
+  for (int o = width / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
 }
 
 __device__ __forceinline__ uint16_t to_bf16_bits(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
-constexpr int DEC_WARPS = 8;
+// Lanes per weight row: the row's groups spread over 32 lanes, or over fewer (and
+// several rows per warp) when the row has fewer than 32 groups.
+__device__ __forceinline__ int lanes_per_row(int ngroups) {
+  int w = 32;
+  while (w > 1 && w / 2 >= ngroups) w /= 2;
+  return w;
+}
 
 // Gate/up of the routed experts: unit (active expert a, hidden unit j) computes
 // h[p][j] = silu(Wg_e[j] . xp[p]) * (Wu_e[j] . xp[p]) for the expert's rows p.
@@ -121,31 +138,43 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) int4_gate_up_kernel(
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x % 32;
-  const long long units = (long long)active[kMaxE] * f;  // active[kMaxE] holds the count
-  const long long stride = (long long)gridDim.x * DEC_WARPS;
   const int ngroups = d / 32;
+  const int lpr = lanes_per_row(ngroups), rpw = 32 / lpr;
+  const int sub = lane / lpr, gl = lane % lpr;
+  const long long per_expert = (f + rpw - 1) / rpw;
+  const long long units = (long long)active[kMaxE] * per_expert;  // active[kMaxE]: count
+  const long long stride = (long long)gridDim.x * DEC_WARPS;
   for (long long u = (long long)blockIdx.x * DEC_WARPS + threadIdx.x / 32; u < units; u += stride) {
-    const int e = active[u / f];
-    const int j = (int)(u % f);
-    const long long grow = (long long)e * 2 * f + (j / block) * 2 * block + j % block;
+    const int e = active[u / per_expert];
+    const int j = (int)(u % per_expert) * rpw + sub;
+    const bool row_ok = j < f;
+    const int jj = row_ok ? j : f - 1;
+    const long long grow = (long long)e * 2 * f + (jj / block) * 2 * block + jj % block;
     const long long urow = grow + block;
     const int p0 = offsets[e], p1 = offsets[e + 1];
-    for (int p = p0; p < p1; ++p) {
-      float gs = 0.f, us = 0.f;
-      for (int g = lane; g < ngroups; g += 32) {
-        float wg[32], wu[32], xv[32];
-        dequant_group(wq + grow * (d / 2) + g * 16, ws[grow * ngroups + g], wg);
-        dequant_group(wq + urow * (d / 2) + g * 16, ws[urow * ngroups + g], wu);
-        load_bf16x32(xp + (long long)p * d + g * 32, xv);
+    for (int pc = p0; pc < p1; pc += DEC_TOK) {
+      float ag[DEC_TOK], au[DEC_TOK];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          gs = fmaf(wg[i], xv[i], gs);
-          us = fmaf(wu[i], xv[i], us);
-        }
+      for (int m = 0; m < DEC_TOK; ++m) ag[m] = au[m] = 0.f;
+      for (int g = gl; g < ngroups; g += lpr) {
+        float qg[32], qu[32];
+        int4_codes(wq + grow * (d / 2) + g * 16, qg);
+        int4_codes(wq + urow * (d / 2) + g * 16, qu);
+        const float sg = scale_of(ws, grow * ngroups + g), su = scale_of(ws, urow * ngroups + g);
+#pragma unroll
+        for (int m = 0; m < DEC_TOK; ++m)
+          if (pc + m < p1) {
+            const uint16_t* xr = xp + (long long)(pc + m) * d + g * 32;
+            ag[m] = fmaf(sg, dot32(qg, xr), ag[m]);
+            au[m] = fmaf(su, dot32(qu, xr), au[m]);
+          }
       }
-      gs = warp_sum(gs);
-      us = warp_sum(us);
-      if (lane == 0) h[(long long)p * f + j] = to_bf16_bits(gs / (1.0f + __expf(-gs)) * us);
+#pragma unroll
+      for (int m = 0; m < DEC_TOK; ++m) {
+        const float gs = group_sum(ag[m], lpr), us = group_sum(au[m], lpr);
+        if (gl == 0 && row_ok && pc + m < p1)
+          h[(long long)(pc + m) * f + j] = to_bf16_bits(gs / (1.0f + __expf(-gs)) * us);
+      }
     }
   }
 }
@@ -159,25 +188,118 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) int4_down_kernel(
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x % 32;
-  const long long units = (long long)active[kMaxE] * d;
-  const long long stride = (long long)gridDim.x * DEC_WARPS;
   const int ngroups = f / 32;
+  const int lpr = lanes_per_row(ngroups), rpw = 32 / lpr;
+  const int sub = lane / lpr, gl = lane % lpr;
+  const long long per_expert = (d + rpw - 1) / rpw;
+  const long long units = (long long)active[kMaxE] * per_expert;
+  const long long stride = (long long)gridDim.x * DEC_WARPS;
   for (long long u = (long long)blockIdx.x * DEC_WARPS + threadIdx.x / 32; u < units; u += stride) {
-    const int e = active[u / d];
-    const int i = (int)(u % d);
-    const long long row = (long long)e * d + i;
+    const int e = active[u / per_expert];
+    const int i = (int)(u % per_expert) * rpw + sub;
+    const bool row_ok = i < d;
+    const long long row = (long long)e * d + (row_ok ? i : d - 1);
     const int p0 = offsets[e], p1 = offsets[e + 1];
-    for (int p = p0; p < p1; ++p) {
-      float acc = 0.f;
-      for (int g = lane; g < ngroups; g += 32) {
-        float w[32], hv[32];
-        dequant_group(wq + row * (f / 2) + g * 16, ws[row * ngroups + g], w);
-        load_bf16x32(h + (long long)p * f + g * 32, hv);
+    for (int pc = p0; pc < p1; pc += DEC_TOK) {
+      float acc[DEC_TOK];
 #pragma unroll
-        for (int k2 = 0; k2 < 32; ++k2) acc = fmaf(w[k2], hv[k2], acc);
+      for (int m = 0; m < DEC_TOK; ++m) acc[m] = 0.f;
+      for (int g = gl; g < ngroups; g += lpr) {
+        float q[32];
+        int4_codes(wq + row * (f / 2) + g * 16, q);
+        const float sc = scale_of(ws, row * ngroups + g);
+#pragma unroll
+        for (int m = 0; m < DEC_TOK; ++m)
+          if (pc + m < p1) acc[m] = fmaf(sc, dot32(q, h + (long long)(pc + m) * f + g * 32), acc[m]);
       }
-      acc = warp_sum(acc);
-      if (lane == 0) y[(long long)p * d + i] = to_bf16_bits(acc);
+#pragma unroll
+      for (int m = 0; m < DEC_TOK; ++m) {
+        const float v = group_sum(acc[m], lpr);
+        if (gl == 0 && row_ok && pc + m < p1) y[(long long)(pc + m) * d + i] = to_bf16_bits(v);
+      }
+    }
+  }
+}
+
+// Serving with few (token, expert) pairs: the same products straight from the routing
+// result, with no permutation.  Pairs p (= t * k + j) keep their order; a warp's unit
+// is (pair, rows) and only the first pair routed to an expert does the work, for all
+// of that expert's pairs (found by a ballot over idx), so each expert's rows are still
+// read once.  h and y are indexed by pair.
+template <bool GATE_UP>
+__global__ void __launch_bounds__(DEC_WARPS * 32) int4_direct_kernel(
+    const int32_t* __restrict__ idx, int P, int k, const uint8_t* __restrict__ wq,
+    const uint16_t* __restrict__ ws, const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
+    int d, int f, int block) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x % 32;
+  const int K = GATE_UP ? d : f, rows = GATE_UP ? f : d;  // inputs, outputs per expert
+  const int ngroups = K / 32;
+  const int lpr = lanes_per_row(ngroups), rpw = 32 / lpr;
+  const int sub = lane / lpr, gl = lane % lpr;
+  const int ea = lane < P ? idx[lane] : -1, eb = lane + 32 < P ? idx[lane + 32] : -1;
+  const long long per_pair = (rows + rpw - 1) / rpw;
+  const long long units = (long long)P * per_pair;
+  const long long stride = (long long)gridDim.x * DEC_WARPS;
+  for (long long u = (long long)blockIdx.x * DEC_WARPS + threadIdx.x / 32; u < units; u += stride) {
+    const int p = (int)(u / per_pair);
+    const int e = __shfl_sync(0xFFFFFFFFu, p < 32 ? ea : eb, p & 31);
+    const unsigned ma = __ballot_sync(0xFFFFFFFFu, ea == e), mb = __ballot_sync(0xFFFFFFFFu, eb == e);
+    const int first = ma ? __ffs(ma) - 1 : 32 + __ffs(mb) - 1;
+    if (first != p) continue;  // warp-uniform: another unit covers this expert's pairs
+    const int r = (int)(u % per_pair) * rpw + sub;
+    const bool row_ok = r < rows;
+    const int rr = row_ok ? r : rows - 1;
+    long long row_a, row_b = 0;  // gate and up rows (gate/up), or the down row
+    if (GATE_UP) {
+      row_a = (long long)e * 2 * f + (rr / block) * 2 * block + rr % block;
+      row_b = row_a + block;
+    } else {
+      row_a = (long long)e * d + rr;
+    }
+    unsigned long long mask = (unsigned long long)ma | ((unsigned long long)mb << 32);
+    while (mask) {
+      int pp[DEC_TOK], cnt = 0;
+#pragma unroll
+      for (int m = 0; m < DEC_TOK; ++m) {
+        pp[m] = 0;
+        if (mask) {
+          pp[m] = __ffsll((long long)mask) - 1;
+          mask &= mask - 1;
+          cnt = m + 1;
+        }
+      }
+      float aa[DEC_TOK], ab[DEC_TOK];
+#pragma unroll
+      for (int m = 0; m < DEC_TOK; ++m) aa[m] = ab[m] = 0.f;
+      for (int g = gl; g < ngroups; g += lpr) {
+        float qa[32], qb[32];
+        int4_codes(wq + row_a * (K / 2) + g * 16, qa);
+        const float sa = scale_of(ws, row_a * ngroups + g);
+        float sb = 0.f;
+        if (GATE_UP) {
+          int4_codes(wq + row_b * (K / 2) + g * 16, qb);
+          sb = scale_of(ws, row_b * ngroups + g);
+        }
+#pragma unroll
+        for (int m = 0; m < DEC_TOK; ++m)
+          if (m < cnt) {
+            // gate/up reads token pp / k of x; down reads pair pp of h
+            const uint16_t* v = src + (long long)(GATE_UP ? pp[m] / k : pp[m]) * K + g * 32;
+            aa[m] = fmaf(sa, dot32(qa, v), aa[m]);
+            if (GATE_UP) ab[m] = fmaf(sb, dot32(qb, v), ab[m]);
+          }
+      }
+#pragma unroll
+      for (int m = 0; m < DEC_TOK; ++m)
+        if (m < cnt) {
+          const float va = group_sum(aa[m], lpr);
+          const float vb = GATE_UP ? group_sum(ab[m], lpr) : 0.f;
+          if (gl == 0 && row_ok)
+            dst[(long long)pp[m] * rows + r] =
+                to_bf16_bits(GATE_UP ? va / (1.0f + __expf(-va)) * vb : va);
+        }
     }
   }
 }
@@ -196,6 +318,17 @@ cudaError_t launch_int4_gate_up(const int32_t* active, const int32_t* offsets, c
                                 int block, cudaStream_t s) {
   return launch_pdl(int4_gate_up_kernel, dim3(decode_grid()), dim3(DEC_WARPS * 32), 0, s, active,
                     offsets, wq, ws, xp, h, d, f, block);
+}
+
+cudaError_t launch_int4_direct(bool gate_up, const int32_t* idx, int pairs, int k, const uint8_t* wq,
+                               const uint16_t* ws, const uint16_t* src, uint16_t* dst, int d, int f,
+                               int block, cudaStream_t s) {
+  if (pairs < 1 || pairs > kDirectMaxPairs) return cudaErrorInvalidValue;
+  if (gate_up)
+    return launch_pdl(int4_direct_kernel<true>, dim3(decode_grid()), dim3(DEC_WARPS * 32), 0, s, idx,
+                      pairs, k, wq, ws, src, dst, d, f, block);
+  return launch_pdl(int4_direct_kernel<false>, dim3(decode_grid()), dim3(DEC_WARPS * 32), 0, s, idx,
+                    pairs, k, wq, ws, src, dst, d, f, block);
 }
 
 cudaError_t launch_int4_down(const int32_t* active, const int32_t* offsets, const uint8_t* wq,

@@ -56,7 +56,7 @@ struct RouterArgs {
   float* scores;        // nullable
   int32_t* idx;
   float* gate;
-  int32_t* load;        // zeroed by the caller; atomically accumulated
+  int32_t* load;        // nullable (SIMT routers); zeroed by the caller; atomically accumulated
   int32_t* counts;      // nullable: [chunks][E], zeroed by the caller
   int chunk_tokens;
   int T, d, E, k, renorm;
@@ -148,6 +148,12 @@ cudaError_t launch_quantize_int4(long long rows, int K, const uint16_t* w, uint8
 cudaError_t launch_int4_gate_up(const int32_t* active, const int32_t* offsets, const uint8_t* wq,
                                 const uint16_t* ws, const uint16_t* xp, uint16_t* h, int d, int f,
                                 int block, cudaStream_t s);
+// Top-1 serving without the permutation (at most kDirectMaxPairs (token, expert)
+// pairs): gate_up: h[p][f] from x[p / k]; down: y[p][d] from h[p]; p = t * k + j.
+constexpr int kDirectMaxPairs = 64;
+cudaError_t launch_int4_direct(bool gate_up, const int32_t* idx, int pairs, int k, const uint8_t* wq,
+                               const uint16_t* ws, const uint16_t* src, uint16_t* dst, int d, int f,
+                               int block, cudaStream_t s);
 cudaError_t launch_int4_down(const int32_t* active, const int32_t* offsets, const uint8_t* wq,
                              const uint16_t* ws, const uint16_t* h, uint16_t* y, int d, int f,
                              cudaStream_t s);

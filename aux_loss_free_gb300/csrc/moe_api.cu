@@ -205,13 +205,18 @@ LayerWs carve_layer(Carver& c, const moe_shape_t* s) {
   w.active = static_cast<int32_t*>(c.take(4 * (size_t)(kMaxE + 1)));
   w.idx = static_cast<int32_t*>(c.take(4 * Tk));
   w.gate = static_cast<float*>(c.take(4 * Tk));
-  w.load = static_cast<int32_t*>(c.take(4 * (size_t)s->E));
+  w.load = nullptr;  // placed after the count table below (one memset clears both)
   w.offsets = static_cast<int32_t*>(c.take(4 * (size_t)(s->E + 1)));
   w.perm_tok = static_cast<int32_t*>(c.take(4 * Tk));
   w.inv_pos = static_cast<int32_t*>(c.take(4 * Tk));
   w.y = static_cast<uint16_t*>(c.take(2 * Tk * s->d));
   w.s_out = s->F ? static_cast<uint16_t*>(c.take(2 * (size_t)s->T * s->d)) : nullptr;
-  w.perm = carve_permute(c, s);
+  {
+    int ct;
+    const int chunks = layer_chunks_of(s, &ct);
+    w.perm.counts = static_cast<int32_t*>(c.take(4 * ((size_t)chunks * s->E + s->E)));
+    w.load = w.perm.counts + (size_t)chunks * s->E;
+  }
   w.ffn = carve_ffn(c, s);
   return w;
 }
@@ -267,20 +272,30 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x_bf16, const int32_t* of
 // tensor cores, the routed experts' gate/up and down on the int4 dequantising warps
 // (active experts only), then the shared down projection whose epilogue adds the
 // gated routed rows (and the residual) and writes `out`.
+// A few tokens: the shared expert streams its weights over 8-CTA clusters (weights in
+// the MMA's M, tokens in N) instead of the 256-token tiles of the grouped GEMM.
+bool int4_skinny(const moe_shape_t* s) {
+  return s->F && skinny_supported(0, s->T, 2 * s->F, s->d, moe_gate_up_block(s->F)) &&
+         skinny_supported(1, s->T, s->d, s->F, 0);
+}
+
+// shared_gate_up_on: non-null when the shared gate/up already runs on another stream;
+// its completion event, waited for before the shared down projection.
+// direct: the routed experts work from idx without the permutation (h and y by pair).
 moe_status_t run_ffn_int4(const moe_shape_t* s, const void* x_bf16, const LayerWs& L,
                           const moe_weights_t* w, const void* residual, uint16_t* out,
-                          cudaStream_t st, bool mark) {
+                          cudaStream_t st, bool mark, cudaEvent_t shared_gate_up_on = nullptr,
+                          bool direct = false) {
   const long long Tk = (long long)s->T * s->k;
   int bad = 0;
   GemmOperandSet off{};
   CombineInputs none{};
   cudaError_t e = cudaSuccess;
   if (mark) prof_mark("gate_up_and_int4_experts", st);
-  // A few tokens: the shared expert streams its weights over 8-CTA clusters (weights in
-  // the MMA's M, tokens in N) instead of the 256-token tiles of the grouped GEMM.
-  const bool skinny = s->F && skinny_supported(0, s->T, 2 * s->F, s->d, moe_gate_up_block(s->F)) &&
-                      skinny_supported(1, s->T, s->d, s->F, 0);
-  if (skinny) {
+  const bool skinny = int4_skinny(s);
+  if (shared_gate_up_on) {
+    // launched beside the routing
+  } else if (skinny) {
     e = launch_skinny(0, static_cast<const uint16_t*>(w->shared_gate_up), 2 * s->F, s->d,
                       static_cast<const uint16_t*>(x_bf16), s->T, L.ffn.hs, s->F, nullptr, st);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -291,15 +306,29 @@ moe_status_t run_ffn_int4(const moe_shape_t* s, const void* x_bf16, const LayerW
     if (bad) return MOE_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
-  e = launch_int4_gate_up(L.active, L.offsets, static_cast<const uint8_t*>(w->w_gate_up),
-                          static_cast<const uint16_t*>(w->scale_gate_up), L.ffn.xp, L.ffn.h, s->d,
-                          s->f, moe_gate_up_block(s->f), st);
-  if (e == cudaSuccess)
-    e = launch_int4_down(L.active, L.offsets, static_cast<const uint8_t*>(w->w_down),
-                         static_cast<const uint16_t*>(w->scale_down), L.ffn.h, L.y, s->d, s->f, st);
+  if (direct) {
+    e = launch_int4_direct(true, L.idx, (int)Tk, s->k, static_cast<const uint8_t*>(w->w_gate_up),
+                           static_cast<const uint16_t*>(w->scale_gate_up),
+                           static_cast<const uint16_t*>(x_bf16), L.ffn.h, s->d, s->f,
+                           moe_gate_up_block(s->f), st);
+    if (e == cudaSuccess)
+      e = launch_int4_direct(false, L.idx, (int)Tk, s->k, static_cast<const uint8_t*>(w->w_down),
+                             static_cast<const uint16_t*>(w->scale_down), L.ffn.h, L.y, s->d, s->f,
+                             moe_gate_up_block(s->f), st);
+  } else {
+    e = launch_int4_gate_up(L.active, L.offsets, static_cast<const uint8_t*>(w->w_gate_up),
+                            static_cast<const uint16_t*>(w->scale_gate_up), L.ffn.xp, L.ffn.h, s->d,
+                            s->f, moe_gate_up_block(s->f), st);
+    if (e == cudaSuccess)
+      e = launch_int4_down(L.active, L.offsets, static_cast<const uint8_t*>(w->w_down),
+                           static_cast<const uint16_t*>(w->scale_down), L.ffn.h, L.y, s->d, s->f, st);
+  }
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (mark) prof_mark("shared_down_combine", st);
-  CombineInputs comb{L.y, L.inv_pos, L.gate, static_cast<const uint16_t*>(residual), s->k};
+  CombineInputs comb{L.y, direct ? nullptr : L.inv_pos, L.gate,
+                     static_cast<const uint16_t*>(residual), s->k};
+  if (shared_gate_up_on && cudaStreamWaitEvent(st, shared_gate_up_on, 0) != cudaSuccess)
+    return MOE_ERR_CUDA;
   if (skinny) {
     e = launch_skinny(1, static_cast<const uint16_t*>(w->shared_down), s->d, s->F, L.ffn.hs, s->T,
                       out, s->d, &comb, st);
@@ -526,10 +555,52 @@ moe_status_t moe_layer_fwd(const moe_shape_t* shape, const void* x, const float*
   } else if (prof) {
     prof_mark("router", s);
   }
+  // Top-1 serving with few tokens: the shared expert's gate/up needs only x, so it
+  // runs on the second stream beside the routing and the routed int4 experts.
+  const bool int4_fork = int4 && !xf && int4_skinny(shape);
+  if (int4_fork) {
+    aux_lock.lock();
+    aux = aux_for_current_device();
+    if (!aux) return MOE_ERR_CUDA;
+    if (cudaEventRecord(aux->fork, s) != cudaSuccess ||
+        cudaStreamWaitEvent(aux->s, aux->fork, 0) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (launch_skinny(0, static_cast<const uint16_t*>(w->shared_gate_up), 2 * shape->F, shape->d,
+                      static_cast<const uint16_t*>(x), T, L.ffn.hs, shape->F, nullptr,
+                      aux->s) != cudaSuccess ||
+        cudaEventRecord(aux->join, aux->s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  // Top-1 serving with at most kDirectMaxPairs (token, expert) pairs skips the
+  // permutation: the int4 experts read the routing result directly.  The loads are
+  // then counted only when the bias update or the caller needs them.
+  const bool direct = int4 && !xf && (long long)T * k <= kDirectMaxPairs &&
+                      (shape->F == 0 || int4_skinny(shape)) &&
+                      !(dbg && (dbg->offsets || dbg->perm_tok || dbg->inv_pos));
+  const bool need_load = update_bias || (dbg && dbg->load);
+  if (direct) {
+    if (need_load && cudaMemsetAsync(L.load, 0, sizeof(int32_t) * E, rs) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    RouterArgs ra{x, xf, w_router, logit_offset, bias, dbg ? dbg->scores : nullptr, L.idx, L.gate,
+                  need_load ? L.load : nullptr, nullptr, ct, T, shape->d, E, k, shape->renorm};
+    cudaError_t e = run_router(ra, L.router, rs);
+    if (e == cudaSuccess && update_bias)
+      e = launch_bias_update(E, (long long)T * k, L.load, gamma, bias, rs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    const moe_status_t st2 = run_ffn_int4(shape, x, L, w, residual, static_cast<uint16_t*>(out), s,
+                                          prof, int4_fork ? aux->join : nullptr, true);
+    if (prof) prof_mark(nullptr, s);
+    return st2;
+  }
   // The tensor-core router's first kernel zeroes load and counts itself.
   if (!tc) {
-    if (cudaMemsetAsync(L.load, 0, sizeof(int32_t) * E, rs) != cudaSuccess) return MOE_ERR_CUDA;
-    if (cudaMemsetAsync(L.perm.counts, 0, sizeof(int32_t) * chunks * E, rs) != cudaSuccess)
+    // The load vector follows the count table in the workspace: one memset for both,
+    // unless the caller asked for the loads in a buffer of its own.
+    const bool adjacent = L.load == L.perm.counts + (size_t)chunks * E;
+    if (cudaMemsetAsync(L.perm.counts, 0, sizeof(int32_t) * ((size_t)chunks * E + (adjacent ? E : 0)),
+                        rs) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (!adjacent && cudaMemsetAsync(L.load, 0, sizeof(int32_t) * E, rs) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
   RouterArgs ra{x, xf, w_router, logit_offset, bias, dbg ? dbg->scores : nullptr, L.idx, L.gate,
@@ -553,7 +624,8 @@ moe_status_t moe_layer_fwd(const moe_shape_t* shape, const void* x, const float*
   const void* xbf = xf ? L.ffn.xb : x;
   CombineInputs comb{L.y, L.inv_pos, L.gate, static_cast<const uint16_t*>(residual), k};
   const moe_status_t st2 =
-      int4 ? run_ffn_int4(shape, xbf, L, w, residual, static_cast<uint16_t*>(out), s, prof)
+      int4 ? run_ffn_int4(shape, xbf, L, w, residual, static_cast<uint16_t*>(out), s, prof,
+                          int4_fork ? aux->join : nullptr)
            : run_ffn(shape, xbf, L.offsets, w, L.ffn, L.y, L.s_out, &comb,
                      static_cast<uint16_t*>(out), s, prof, fork);
   if (prof) prof_mark(nullptr, s);

@@ -252,8 +252,8 @@ __device__ __forceinline__ void load16_bf16(const uint16_t* row, int v8, uint32_
   }
 }
 
-// out[t] = residual[t] + shared[t] + sum_j gate[t][j] * y[inv_pos[t][j]], 16 columns
-// per thread.  With KC = k (1 or 2) every row load of a thread is issued before the
+// out[t] = residual[t] + shared[t] + sum_j gate[t][j] * y[inv_pos[t][j]] (y[t * k + j]
+// without inv_pos), 16 columns per thread.  With KC = k (1 or 2) every row load of a thread is issued before the
 // first use, so only the inv_pos -> y dependency is exposed; KC = 0 loops over k.
 template <int KC>
 __global__ void combine_kernel(const uint16_t* __restrict__ y, const uint16_t* __restrict__ shared,
@@ -282,7 +282,7 @@ __global__ void combine_kernel(const uint16_t* __restrict__ y, const uint16_t* _
     float g[KC > 0 ? KC : 1];
 #pragma unroll
     for (int j = 0; j < KC; ++j) {
-      pos[j] = inv_pos[t * KC + j];
+      pos[j] = inv_pos ? inv_pos[t * KC + j] : (int)(t * KC + j);
       g[j] = gate[t * KC + j];
     }
     uint32_t wr[8], wsh[8], wy[KC > 0 ? KC : 1][8];
@@ -305,7 +305,7 @@ __global__ void combine_kernel(const uint16_t* __restrict__ y, const uint16_t* _
       add(ws, 1.f);
     }
     for (int j = 0; j < k; ++j) {
-      load16_bf16(y + (long long)inv_pos[t * k + j] * d + c, v8, ws);
+      load16_bf16(y + (long long)(inv_pos ? inv_pos[t * k + j] : t * k + j) * d + c, v8, ws);
       add(ws, gate[t * k + j]);
     }
   }

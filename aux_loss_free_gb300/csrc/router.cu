@@ -101,7 +101,7 @@ __device__ __forceinline__ void select_token(const RouterArgs& a, const float* l
       a.idx[(size_t)t * a.k + j] = sel_e[j];
       a.gate[(size_t)t * a.k + j] = a.renorm ? __fdiv_rn(sel_s[j], denom) : sel_s[j];
       if (!hist) {
-        atomicAdd(&a.load[sel_e[j]], 1);
+        if (a.load) atomicAdd(&a.load[sel_e[j]], 1);
         if (a.counts) atomicAdd(&a.counts[(size_t)(t / a.chunk_tokens) * E + sel_e[j]], 1);
       }
     }
@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(NTHR) router_kernel(RouterArgs a) {
   for (int e = tid; e < E; e += NTHR) {
     const int h = hist[e];
     if (h) {
-      atomicAdd(&a.load[e], h);
+      if (a.load) atomicAdd(&a.load[e], h);
       if (a.counts) atomicAdd(&a.counts[(size_t)(t0 / a.chunk_tokens) * E + e], h);
     }
   }
@@ -247,12 +247,24 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(CTHR) router_cluste
 #pragma unroll
     for (int tok = 0; tok < CTPB; ++tok) acc[tok] = 0.f;
     const float* wr = a.w_router + (size_t)e * d;
-    for (int kk = lane * 4; kk < d; kk += 128) {
-      const float4 w = *reinterpret_cast<const float4*>(wr + kk);
+    // Eight float4 of the row in flight per lane before any is used.
+    for (int k0 = lane * 4; k0 < d; k0 += 128 * 8) {
+      float4 w[8];
 #pragma unroll
-      for (int tok = 0; tok < CTPB; ++tok) {
-        const float4 xv = *reinterpret_cast<const float4*>(xs + tok * d + kk);
-        acc[tok] = fmaf(w.x, xv.x, fmaf(w.y, xv.y, fmaf(w.z, xv.z, fmaf(w.w, xv.w, acc[tok]))));
+      for (int u = 0; u < 8; ++u) {
+        const int kk = k0 + u * 128;
+        w[u] = kk < d ? *reinterpret_cast<const float4*>(wr + kk) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int kk = k0 + u * 128;
+        if (kk < d) {
+#pragma unroll
+          for (int tok = 0; tok < CTPB; ++tok) {
+            const float4 xv = *reinterpret_cast<const float4*>(xs + tok * d + kk);
+            acc[tok] = fmaf(w[u].x, xv.x, fmaf(w[u].y, xv.y, fmaf(w[u].z, xv.z, fmaf(w[u].w, xv.w, acc[tok]))));
+          }
+        }
       }
     }
     const float off = a.logit_offset ? a.logit_offset[e] : 0.f;

@@ -18,7 +18,8 @@
 //           128, one CTA covers one block pair (two accumulators) and writes
 //           h[t][j] = silu(g) * u in bf16;
 //   mode 1 (down):   weights [d][F], writes out[t][n] = acc (+ residual[t][n]
-//           + sum_j gate[t][j] * y_perm[inv_pos[t][j]][n] when combining), bf16.
+//           + sum_j gate[t][j] * y_perm[inv_pos[t][j]][n] when combining; without
+//           inv_pos the routed rows are indexed by pair, t * k + j), bf16.
 // Every wait is bounded; on a timeout the CTA records it in the status word and still
 // reaches both cluster barriers and frees its TMEM.
 #include <cuda.h>
@@ -184,7 +185,8 @@ __global__ void __cluster_dims__(SK_SPLIT, 1, 1) __launch_bounds__(SK_THREADS, 1
       if (p.y_perm)
         for (int j = 0; j < p.k; ++j)
           o = fmaf(p.gate[(size_t)t * p.k + j],
-                   sk_bf16(p.y_perm[(size_t)p.inv_pos[(size_t)t * p.k + j] * p.ldo + col]), o);
+                   sk_bf16(p.y_perm[(p.inv_pos ? (size_t)p.inv_pos[(size_t)t * p.k + j]
+                                               : (size_t)t * p.k + j) * p.ldo + col]), o);
       p.out[(size_t)t * p.ldo + col] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
     }
   }

@@ -50,6 +50,10 @@ def kernels_per_call(s):
     tc_router = s.x_dtype == "bf16" and s.T >= 128 and s.E in (16, 32, 48, 64, 80)
     router = 2 if tc_router else 1                     # weight split + router, or SIMT router
     if s.w_format == "int4":
+        if s.T * s.k <= 64:
+            # no permutation: shared gate/up (second stream), int4 gate/up, int4 down,
+            # shared down + combine (or the combine kernel without a shared expert)
+            return router + 2 + (2 if s.F else 1)
         # permute, shared gate/up, int4 gate/up, int4 down, shared down + combine
         return router + 1 + (4 if s.F else 2) + (0 if s.F else 1)
     # permute, gate/up (one or two launches), down, combine

@@ -13,7 +13,7 @@ import aux_loss_free_gb300 as M
 from aux_loss_free_gb300.layer import LayerOnDevice, to_device_bf16, to_device_tokens
 from gpu_util import assert_close_bf16, bf16_to_np, bf64, tokens64
 from oracle import moe_oracle as O
-from synth import CONFIGS, make_layer
+from synth import CONFIGS, make_layer, make_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -304,6 +304,39 @@ def test_int4_top1_serving_layer_matches_oracle(T):
     assert np.abs(gate.cpu().numpy() - ref["gate"]).max() <= 1e-6
     assert np.array_equal(layer.bias.cpu().numpy().view(np.uint32), host["bias"].view(np.uint32))
     assert_close_bf16(bf16_to_np(out), ref["out"], "int4 serving out")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("T", [3, 64])
+def test_int4_serving_without_permutation_bias_update_and_residual(T):
+    """The serving path that skips the permutation (at most 64 token-expert pairs, no
+    permutation outputs requested): loads bit-exact, the bias update applied from
+    them bit for bit, and the output with a residual within tolerance."""
+    s = CONFIGS["decode"].replace(T=T)
+    host = make_layer(s, "decode")
+    layer = LayerOnDevice(s, host, DEV)
+    x = to_device_tokens(host["x"], DEV)
+    res_bits = make_tokens(s, "decode", seed=7)
+    res = to_device_tokens(res_bits, DEV)
+    scores = torch.empty(s.T, s.E, dtype=torch.float32, device=DEV)
+    idx = torch.empty(s.T, s.k, dtype=torch.int32, device=DEV)
+    load = torch.empty(s.E, dtype=torch.int32, device=DEV)
+    dbg = M.make_debug(scores=scores, idx=idx, load=load)
+    out = torch.empty(s.T, s.d, dtype=torch.bfloat16, device=DEV)
+    layer.forward(x, out, update_bias=True, residual=res, debug=dbg)
+    torch.cuda.synchronize()
+    sc = scores.cpu().numpy()
+    res_np = bf64(res_bits)
+    ref = O.layer_forward(tokens64(host["x"]), host["w_router"], host["bias"],
+                          _dequant_oracle(host["w_gate"]), _dequant_oracle(host["w_up"]),
+                          _dequant_oracle(host["w_down"]), bf64(host["s_gate"]), bf64(host["s_up"]),
+                          bf64(host["s_down"]), k=1, renorm=False, gamma=s.gamma, scores_f32=sc,
+                          residual=res_np)
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    assert np.array_equal(load.cpu().numpy(), O.expert_load(ref["idx"], s.E))
+    want_bias = O.bias_update(host["bias"], O.expert_load(ref["idx"], s.E), s.T * s.k, s.gamma)
+    assert np.array_equal(layer.bias.cpu().numpy().view(np.uint32), want_bias.view(np.uint32))
+    assert_close_bf16(bf16_to_np(out), ref["out"], "int4 serving out with residual")
 
 
 def test_stack_23_layers_with_residual():
