@@ -221,25 +221,50 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) int4_down_kernel(
   }
 }
 
+// 32 bf16 inputs of one group -> floats.
+__device__ __forceinline__ void load_group_xf(const uint16_t* p, float (&x)[32]) {
+  const uint4* v = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 u = v[i];
+    const uint32_t ws[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[8 * i + 2 * j] = __uint_as_float(ws[j] << 16);
+      x[8 * i + 2 * j + 1] = __uint_as_float(ws[j] & 0xFFFF0000u);
+    }
+  }
+}
+
 // Serving with few (token, expert) pairs: the same products straight from the routing
 // result, with no permutation.  Pairs p (= t * k + j) keep their order; a warp's unit
-// is (pair, rows) and only the first pair routed to an expert does the work, for all
-// of that expert's pairs (found by a ballot over idx), so each expert's rows are still
-// read once.  h and y are indexed by pair.
+// is (pair, DIR_RPU row slots) and only the first pair routed to an expert does the
+// work, for all of that expert's pairs (found by a ballot over idx), so each expert's
+// rows are still read once.  Per pass over up to DIR_TOK of the expert's pairs, a lane
+// decodes each of its row groups once (integer codes, exact in fp32), unpacks each
+// pair's inputs once, and accumulates the products; the scale multiplies each group's
+// sum once.  h and y are indexed by pair.
+constexpr int DIR_RPU = 2;
+constexpr int DIR_TOK = 2;
+
 template <bool GATE_UP>
-__global__ void __launch_bounds__(DEC_WARPS * 32) int4_direct_kernel(
+__global__ void __launch_bounds__(DEC_WARPS * 32, 2) int4_direct_kernel(
     const int32_t* __restrict__ idx, int P, int k, const uint8_t* __restrict__ wq,
     const uint16_t* __restrict__ ws, const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
     int d, int f, int block) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  constexpr int NM = GATE_UP ? 2 : 1;  // gate and up rows, or the down row
   const int lane = threadIdx.x % 32;
   const int K = GATE_UP ? d : f, rows = GATE_UP ? f : d;  // inputs, outputs per expert
   const int ngroups = K / 32;
   const int lpr = lanes_per_row(ngroups), rpw = 32 / lpr;
   const int sub = lane / lpr, gl = lane % lpr;
   const int ea = lane < P ? idx[lane] : -1, eb = lane + 32 < P ? idx[lane + 32] : -1;
-  const long long per_pair = (rows + rpw - 1) / rpw;
+  // Fewer pairs leave more warps idle: then each unit covers fewer rows.
+  const int rpu = P >= 16 ? DIR_RPU : 1;
+  const int rows_per_unit = rpw * rpu;
+  const long long per_pair = (rows + rows_per_unit - 1) / rows_per_unit;
   const long long units = (long long)P * per_pair;
   const long long stride = (long long)gridDim.x * DEC_WARPS;
   for (long long u = (long long)blockIdx.x * DEC_WARPS + threadIdx.x / 32; u < units; u += stride) {
@@ -248,21 +273,12 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) int4_direct_kernel(
     const unsigned ma = __ballot_sync(0xFFFFFFFFu, ea == e), mb = __ballot_sync(0xFFFFFFFFu, eb == e);
     const int first = ma ? __ffs(ma) - 1 : 32 + __ffs(mb) - 1;
     if (first != p) continue;  // warp-uniform: another unit covers this expert's pairs
-    const int r = (int)(u % per_pair) * rpw + sub;
-    const bool row_ok = r < rows;
-    const int rr = row_ok ? r : rows - 1;
-    long long row_a, row_b = 0;  // gate and up rows (gate/up), or the down row
-    if (GATE_UP) {
-      row_a = (long long)e * 2 * f + (rr / block) * 2 * block + rr % block;
-      row_b = row_a + block;
-    } else {
-      row_a = (long long)e * d + rr;
-    }
+    const int r_base = (int)(u % per_pair) * rows_per_unit + sub;
     unsigned long long mask = (unsigned long long)ma | ((unsigned long long)mb << 32);
     while (mask) {
-      int pp[DEC_TOK], cnt = 0;
+      int pp[DIR_TOK], cnt = 0;
 #pragma unroll
-      for (int m = 0; m < DEC_TOK; ++m) {
+      for (int m = 0; m < DIR_TOK; ++m) {
         pp[m] = 0;
         if (mask) {
           pp[m] = __ffsll((long long)mask) - 1;
@@ -270,36 +286,51 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) int4_direct_kernel(
           cnt = m + 1;
         }
       }
-      float aa[DEC_TOK], ab[DEC_TOK];
-#pragma unroll
-      for (int m = 0; m < DEC_TOK; ++m) aa[m] = ab[m] = 0.f;
-      for (int g = gl; g < ngroups; g += lpr) {
-        float qa[32], qb[32];
-        int4_codes(wq + row_a * (K / 2) + g * 16, qa);
-        const float sa = scale_of(ws, row_a * ngroups + g);
-        float sb = 0.f;
+      for (int i = 0; i < rpu; ++i) {
+        const int r = r_base + i * rpw;
+        const int rr = min(r, rows - 1);
+        long long wrow[NM];
         if (GATE_UP) {
-          int4_codes(wq + row_b * (K / 2) + g * 16, qb);
-          sb = scale_of(ws, row_b * ngroups + g);
+          wrow[0] = (long long)e * 2 * f + (rr / block) * 2 * block + rr % block;
+          wrow[NM - 1] = wrow[0] + block;
+        } else {
+          wrow[0] = (long long)e * d + rr;
+        }
+        float acc[NM][DIR_TOK];
+#pragma unroll
+        for (int mm = 0; mm < NM; ++mm)
+#pragma unroll
+          for (int m = 0; m < DIR_TOK; ++m) acc[mm][m] = 0.f;
+        for (int g = gl; g < ngroups; g += lpr) {
+          float xf[DIR_TOK][32];
+#pragma unroll
+          for (int m = 0; m < DIR_TOK; ++m)
+            if (m < cnt)  // gate/up reads token pp / k of x; down reads pair pp of h
+              load_group_xf(src + (long long)(GATE_UP ? pp[m] / k : pp[m]) * K + g * 32, xf[m]);
+#pragma unroll
+          for (int mm = 0; mm < NM; ++mm) {
+            float q[32];
+            int4_codes(wq + wrow[mm] * (K / 2) + g * 16, q);
+            const float sc = scale_of(ws, wrow[mm] * ngroups + g);
+#pragma unroll
+            for (int m = 0; m < DIR_TOK; ++m)
+              if (m < cnt) {
+                float part = 0.f;
+#pragma unroll
+                for (int t = 0; t < 32; ++t) part = fmaf(q[t], xf[m][t], part);
+                acc[mm][m] = fmaf(sc, part, acc[mm][m]);
+              }
+          }
         }
 #pragma unroll
-        for (int m = 0; m < DEC_TOK; ++m)
+        for (int m = 0; m < DIR_TOK; ++m)
           if (m < cnt) {
-            // gate/up reads token pp / k of x; down reads pair pp of h
-            const uint16_t* v = src + (long long)(GATE_UP ? pp[m] / k : pp[m]) * K + g * 32;
-            aa[m] = fmaf(sa, dot32(qa, v), aa[m]);
-            if (GATE_UP) ab[m] = fmaf(sb, dot32(qb, v), ab[m]);
+            const float va = group_sum(acc[0][m], lpr);
+            const float vb = GATE_UP ? group_sum(acc[NM - 1][m], lpr) : 0.f;
+            if (gl == 0 && r < rows)
+              dst[(long long)pp[m] * rows + r] = to_bf16_bits(GATE_UP ? va / (1.0f + __expf(-va)) * vb : va);
           }
       }
-#pragma unroll
-      for (int m = 0; m < DEC_TOK; ++m)
-        if (m < cnt) {
-          const float va = group_sum(aa[m], lpr);
-          const float vb = GATE_UP ? group_sum(ab[m], lpr) : 0.f;
-          if (gl == 0 && row_ok)
-            dst[(long long)pp[m] * rows + r] =
-                to_bf16_bits(GATE_UP ? va / (1.0f + __expf(-va)) * vb : va);
-        }
     }
   }
 }
