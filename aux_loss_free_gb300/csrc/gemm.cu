@@ -59,8 +59,14 @@ constexpr int DYN_SMEM = STAGES * STAGE_BYTES + 1024;
 constexpr unsigned FULL = 0xFFFFFFFFu;
 
 struct OperandSet {
-  CUtensorMap a;  // box 128 rows x 64
-  CUtensorMap b;  // box BN/2 rows x 64
+  // With kblock set (K a multiple of 64), both maps view a [rows][K] matrix as (64
+  // columns, rows, K / 64 atoms) so that one copy brings a k-block's two 64-column
+  // atoms: 128 rows x 64 x 2 for A, BN/2 rows for B (TMA's cost per copy makes two
+  // 32 KB copies much faster than four of 16 KB).  Otherwise plain 2-D maps, box
+  // (64, rows), one copy per atom.
+  CUtensorMap a;
+  CUtensorMap b;
+  int kblock;
   void* out;
   int ldo, n_total, k_total, bn, mode, enabled, rows;
   int v8;  // output rows start on 32-byte boundaries: 256-bit stores allowed
@@ -119,6 +125,17 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
+      : "memory");
+}
+
+// One k-block (two 64-column atoms) of a 3-D operand map, completion counted on the
+// pair's (leader's) barrier.
+__device__ __forceinline__ void tma_load_kblock_pair(uint32_t dst, const CUtensorMap* map,
+                                                     uint32_t bar_cluster, int32_t row, int32_t atom) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(atom), "r"(bar_cluster)
       : "memory");
 }
 
@@ -369,16 +386,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
-          // Atoms entirely past K are not loaded (and not multiplied).
-          const int natoms = min(ATOMS, (S.k_total - kb * BK + AK - 1) / AK);
+          // Both atoms of the k-block in one copy per operand (an atom past K arrives
+          // zero-filled and is not multiplied); with 2-D maps, atoms past K are not
+          // loaded at all.
+          const int natoms = S.kblock ? ATOMS : min(ATOMS, (S.k_total - kb * BK + AK - 1) / AK);
           const uint32_t pair_bytes = 2u * natoms * (A_ATOM + half * AK * 2);
           const uint32_t sa = ring + stage * STAGE_BYTES;
           const uint32_t fb = map_to_rank(smem_u32(&full_bar[stage]), 0);
+          const uint32_t b_atom = (uint32_t)half * AK * 2;
           if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[stage]), pair_bytes);
-          for (int at = 0; at < natoms; ++at) {
-            tma_load_2d_pair(sa + at * A_ATOM, &S.a, fb, kb * BK + at * AK, t.row0 + HM * (int)rank);
-            tma_load_2d_pair(sa + A_BYTES + at * B_ATOM, &S.b, fb, kb * BK + at * AK,
-                             t.brow + half * (int)rank);
+          if (S.kblock) {
+            tma_load_kblock_pair(sa, &S.a, fb, t.row0 + HM * (int)rank, kb * ATOMS);
+            tma_load_kblock_pair(sa + A_BYTES, &S.b, fb, t.brow + half * (int)rank, kb * ATOMS);
+          } else {
+            for (int at = 0; at < natoms; ++at) {
+              tma_load_2d_pair(sa + at * A_ATOM, &S.a, fb, kb * BK + at * AK, t.row0 + HM * (int)rank);
+              tma_load_2d_pair(sa + A_BYTES + at * b_atom, &S.b, fb, kb * BK + at * AK,
+                               t.brow + half * (int)rank);
+            }
           }
           issued |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
@@ -408,6 +433,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const int bn = set ? p.routed.bn : p.shared.bn;
         const int nkb = (k_total + BK - 1) / BK;
         const int nkk_last = (k_total - (nkb - 1) * BK + 15) / 16;
+        const uint32_t b_atom = (uint32_t)bn / 2 * AK * 2;
         const uint32_t idesc = idesc_bf16_f32(BM, bn);
         if (!mbar_wait_spin(smem_u32(&tempty_bar[acc]), acc_phase ^ 1u, p.status)) break;
         tc_fence_after();
@@ -423,7 +449,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int at = 0; at < ATOMS; ++at) {
             adesc[at] = sw128_kmajor_desc(sa + at * A_ATOM);
-            bdesc[at] = sw128_kmajor_desc(sa + A_BYTES + at * B_ATOM);
+            bdesc[at] = sw128_kmajor_desc(sa + A_BYTES + at * b_atom);  // b_atom: BN/2 rows x 128 B
           }
           if (kb + 1 < nkb) {
 #pragma unroll
@@ -586,6 +612,23 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
   return r == CUDA_SUCCESS;
 }
 
+// The same matrix as (64 columns, outer rows, inner / 64 atoms), box (64, box_outer, 2):
+// one copy = two consecutive 64-column atoms, each [box_outer][64] with the 128-byte
+// swizzle, the second box_outer * 128 bytes after the first.
+bool make_map_kblock(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+                     uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn || inner % AK != 0) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(AK), outer, inner / AK};
+  const cuuint64_t strides[2] = {inner * 2, static_cast<cuuint64_t>(AK) * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(AK), box_outer, static_cast<cuuint32_t>(ATOMS)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int gate_up_block(int width) { return width % 128 == 0 ? 128 : (width % 64 == 0 ? 64 : 32); }
 
 int choose_bn(int mode, int N) {
@@ -626,8 +669,14 @@ bool fill_set(OperandSet& t, const GemmOperandSet& o) {
   t.out = o.out;
   t.v8 = (reinterpret_cast<uintptr_t>(o.out) % 32 == 0) && ((long long)o.ldo * 2) % 32 == 0;
   if (o.N % t.bn != 0) return false;
-  if (!make_map(&t.a, o.a, o.K, o.a_rows, HM)) return false;
-  if (!make_map(&t.b, o.b, o.K, (uint64_t)o.groups * o.N, t.bn / 2)) return false;
+  t.kblock = o.K % AK == 0;
+  if (t.kblock) {
+    if (!make_map_kblock(&t.a, o.a, o.K, o.a_rows, HM)) return false;
+    if (!make_map_kblock(&t.b, o.b, o.K, (uint64_t)o.groups * o.N, t.bn / 2)) return false;
+  } else {
+    if (!make_map(&t.a, o.a, o.K, o.a_rows, HM)) return false;
+    if (!make_map(&t.b, o.b, o.K, (uint64_t)o.groups * o.N, t.bn / 2)) return false;
+  }
   return true;
 }
 
