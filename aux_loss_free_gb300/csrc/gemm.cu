@@ -18,7 +18,7 @@
 //     single-SM 128 x 256 tile would need;
 //   - commits are multicast to both CTAs (stage release, accumulator ready);
 //   - each CTA's accumulator holds its 128 rows x BN fp32 columns in TMEM, double
-//     buffered (2 x 256 columns); 8 epilogue warps per CTA drain it:
+//     buffered (2 x 256 columns); 4 epilogue warps per CTA (one per TMEM lane quadrant) drain it:
 //       SWIGLU  h = silu(gate) * up -> bf16 (gate / up rows interleaved in the
 //               weights so one tile holds matching columns),
 //       STORE   y -> bf16,
@@ -50,7 +50,7 @@ constexpr int A_ATOM = HM * AK * 2;               // 16 KB: 128 rows x 64
 constexpr int B_ATOM = (BN_MAX / 2) * AK * 2;     // 16 KB: up to 128 rows (half of B) x 64
 constexpr int A_BYTES = ATOMS * A_ATOM;
 constexpr int STAGE_BYTES = A_BYTES + ATOMS * B_ATOM; // 64 KB
-constexpr int EPI_WARPS = 8;
+constexpr int EPI_WARPS = 4;
 constexpr int EPI_GROUPS = EPI_WARPS / 4;  // warps per TMEM lane quadrant
 constexpr int CS = 32 * EPI_GROUPS;        // column stride between one warp's chunks
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
@@ -477,7 +477,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       mbar_wait(smem_u32(&drain_bar), 0, p.status);
     }
   } else {
-    // -------------------------------------------------- epilogue (warps 2..9)
+    // -------------------------------------------------- epilogue (warps 2..5)
     const int q = warp & 3;                 // TMEM lanes [32q, 32q + 32) are this warp's rows
     const int colh = (warp - 2) / 4;        // which interleaved share of the column chunks
     const uint32_t tempty_leader0 = map_to_rank(smem_u32(&tempty_bar[0]), 0);
