@@ -432,6 +432,7 @@ def gpu_arm(args, rank, world, dist):
     ld = loads.cpu().numpy().astype(np.float64)
     hit = int((ld[0] > 0).sum())
     traj = (ld.max(axis=1) / ld.mean(axis=1)).tolist()
+    dead = (ld == 0).mean(axis=1).tolist()  # fraction of experts with no pair, per step
 
     if rank != 0:
         return
@@ -461,12 +462,16 @@ def gpu_arm(args, rank, world, dist):
         "layer_roofline": {"flops_per_layer": flops, "bytes_per_layer": nbytes,
                            "roofline_us": roof_s * 1e6, "measured_us": ms_step * 1e3,
                            "frac": roof_s / (ms_step / 1e3), "peak": peak_note,
+                           "frac_sustained": nlayers * max(
+                               flops / (peaks["bf16_tflops_sustained"] * 1e12),
+                               nbytes / (peaks["hbm_gbs"] * 1e9)) / (ms_step / 1e3),
                            "bound": "tensor" if flops / (peaks["bf16_tflops"] * 1e12) >
                            nbytes / (peaks["hbm_gbs"] * 1e9) else "hbm"},
         "roofline": {"kernel": dom_name,
                      "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
                      "traffic": traffic, "peak_note": peak_note + " (burst)",
+                     "frac_sustained": achieved / peaks["bf16_tflops_sustained"],
                      "flops_per_launch": gu_flops, "avg_launch_us": gu_ms * 1e3},
         "stages_us": {k: v * 1e3 / max(1, calls) for k, v in stages_ms.items()},
         "e2e": {"value": world * s.T / (e2e_ms / 1e3), "unit": "tokens/s",
@@ -481,6 +486,8 @@ def gpu_arm(args, rank, world, dist):
     if s.steps > 1:
         line["load_max_over_mean"] = {"first": traj[0], "last": traj[-1],
                                       "per_step": [round(v, 3) for v in traj]}
+        line["dead_expert_fraction"] = {"first": dead[0], "last": dead[-1],
+                                        "per_step": [round(v, 4) for v in dead]}
         line["step_us"] = {"min": min(step_ms) * 1e3, "median": statistics.median(step_ms) * 1e3,
                            "max": max(step_ms) * 1e3}
     if s.w_format == "int4":

@@ -204,7 +204,9 @@ def test_expert_ffn_and_combine_match_oracle(name, kw):
 LAYER_CASES = [("tiny", {}), ("nano", {}), ("skew", {}), ("nano", {"T": 1000}),
                ("nano", {"T": 77, "F": 0}), ("nano", {"T": 1, "k": 1, "renorm": False}),
                ("tiny", {"T": 200, "E": 16, "k": 4, "f": 64, "F": 96}),
-               ("nano", {"T": 4096, "E": 256, "k": 8, "f": 128, "F": 0})]
+               ("nano", {"T": 4096, "E": 256, "k": 8, "f": 128, "F": 0}),
+               ("nano", {"T": 3000}),                                # second stream, ragged tiles
+               ("nano", {"T": 2500, "d": 512, "f": 256, "F": 1024})]  # second stream, other widths
 
 
 @pytest.mark.parametrize("name,kw", LAYER_CASES)
