@@ -194,7 +194,8 @@ def swiglu_ffn(xb: np.ndarray, w_gate: np.ndarray, w_up: np.ndarray, w_down: np.
     return h @ w_down.T
 
 
-def routed_experts(xb: np.ndarray, offsets, perm_tok, w_gate, w_up, w_down) -> np.ndarray:
+def routed_experts(xb: np.ndarray, offsets, perm_tok, w_gate, w_up, w_down,
+                   round_hidden: bool = True) -> np.ndarray:
     """Y[p] for every permuted row p: expert e's FFN applied to token perm_tok[p]."""
     E = len(offsets) - 1
     d = xb.shape[1]
@@ -204,7 +205,7 @@ def routed_experts(xb: np.ndarray, offsets, perm_tok, w_gate, w_up, w_down) -> n
         if hi == lo:
             continue
         rows = xb[perm_tok[lo:hi]]
-        Y[lo:hi] = swiglu_ffn(rows, w_gate[e], w_up[e], w_down[e])
+        Y[lo:hi] = swiglu_ffn(rows, w_gate[e], w_up[e], w_down[e], round_hidden)
     return Y
 
 
@@ -295,7 +296,8 @@ def dequantize_int4_g32(packed: np.ndarray, scale_bits: np.ndarray) -> np.ndarra
 
 def layer_forward(x, w_router, bias, w_gate, w_up, w_down, s_gate, s_up, s_down, k: int,
                   renorm: bool = True, logit_offset=None, gamma: float = 1e-3,
-                  scores_f32=None, residual=None, x_is_bf16: bool = True):
+                  scores_f32=None, residual=None, x_is_bf16: bool = True,
+                  idx=None, exact_gates: bool = False, round_hidden: bool = True):
     """One MoE layer forward plus the bias update, all in the order the method states.
 
     Token values x and all weights are given as real values (fp64 arrays).  If
@@ -308,14 +310,17 @@ def layer_forward(x, w_router, bias, w_gate, w_up, w_down, s_gate, s_up, s_down,
     T = x.shape[0]
     scores = router_scores(x, w_router, logit_offset)
     sel_scores = scores.astype(np.float32) if scores_f32 is None else np.asarray(scores_f32, np.float32)
-    idx = topk_select(sel_scores, bias, k)
-    gate = gate_weights(sel_scores.astype(np.float64), idx, renorm)
+    if idx is None:
+        idx = topk_select(sel_scores, bias, k)
+    # exact_gates: gates from the fp64 scores (a smooth function of x and W_r, for
+    # derivative checks with the selection held fixed through idx).
+    gate = gate_weights(scores if exact_gates else sel_scores.astype(np.float64), idx, renorm)
     load = expert_load(idx, E)
     offsets, perm_tok, inv_pos = stable_permutation(idx, E)
     xb = x if x_is_bf16 else round_to_bf16(x)
-    Y = routed_experts(xb, offsets, perm_tok, w_gate, w_up, w_down)
+    Y = routed_experts(xb, offsets, perm_tok, w_gate, w_up, w_down, round_hidden)
     if s_gate is not None and s_gate.shape[0] > 0:
-        shared = swiglu_ffn(xb, s_gate, s_up, s_down)
+        shared = swiglu_ffn(xb, s_gate, s_up, s_down, round_hidden)
     else:
         shared = np.zeros_like(xb)
     out = combine(Y, shared, inv_pos, gate, residual)
@@ -323,3 +328,103 @@ def layer_forward(x, w_router, bias, w_gate, w_up, w_down, s_gate, s_up, s_down,
     return dict(scores=scores, idx=idx, gate=gate, load=load, offsets=offsets,
                 perm_tok=perm_tok, inv_pos=inv_pos, Y=Y, shared=shared, out=out,
                 bias=new_bias)
+
+
+def layer_backward(x, w_router, bias, w_gate, w_up, w_down, s_gate, s_up, s_down, dout, k: int,
+                   renorm: bool = True, logit_offset=None, scores_f32=None,
+                   residual: bool = False, x_is_bf16: bool = True, idx=None,
+                   exact_gates: bool = False, round_hidden: bool = True):
+    """Gradients of the layer output (as layer_forward computes it) given dout = dL/dout.
+
+    The relay article states the forward (architecture paragraph, top-2 paragraph) and
+    nothing about its derivatives; these are the chain rule through that forward:
+
+    * the selection (biased top-k) is piecewise constant: no gradient flows through
+      the choice of experts, and the bias gets none (it moves by the balancing rule);
+    * pair (t, j) with expert e = idx[t][j] and gate g: y = Wd_e h, h = silu(a) * b,
+      a = Wg_e x_t, b = Wu_e x_t, out_t += g y;  so dy = g dout_t, dg = <dout_t, y>,
+      dh = Wd_e^T dy, da = dh * b * silu'(a), db = dh * silu(a),
+      dx_t += Wg_e^T da + Wu_e^T db, dWd_e += dy h^T, dWg_e += da x_t^T, dWu_e += db x_t^T;
+    * the shared expert likewise with g = 1;
+    * gates: renormalised, g_j = s_j / S with S = sum of the winners' scores, so
+      ds_j = (dg_j - sum_i dg_i g_i) / S; raw, ds_j = dg_j; then dz_j = ds_j s_j (1 - s_j)
+      for the logit z = x W_r^T (+ offset): dx_t += sum_j dz_j W_r[e_j],
+      dW_r[e_j] += dz_j x_t;
+    * with a residual (out = x + MoE(x)), dx += dout.
+
+    h is taken as stored in bf16 when round_hidden (as in the forward); its rounding is
+    passed through unchanged.  Selection uses scores_f32 (the GPU's scores) when given,
+    as in layer_forward; idx and exact_gates as there.  All arithmetic in fp64.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    dout = np.asarray(dout, dtype=np.float64)
+    E, d = w_router.shape
+    T = x.shape[0]
+    scores = router_scores(x, w_router, logit_offset)
+    sel_scores = scores.astype(np.float32) if scores_f32 is None else np.asarray(scores_f32, np.float32)
+    if idx is None:
+        idx = topk_select(sel_scores, bias, k)
+    s_used = scores if exact_gates else sel_scores.astype(np.float64)
+    gate = gate_weights(s_used, idx, renorm)
+    xb = x if x_is_bf16 else round_to_bf16(x)
+    dx = np.zeros_like(x)
+    dwg = np.zeros_like(w_gate, dtype=np.float64)
+    dwu = np.zeros_like(w_up, dtype=np.float64)
+    dwd = np.zeros_like(w_down, dtype=np.float64)
+    dgate = np.zeros((T, k), dtype=np.float64)
+    for t in range(T):
+        for j in range(k):
+            e = int(idx[t, j])
+            xt = xb[t]
+            a = w_gate[e] @ xt
+            b = w_up[e] @ xt
+            sa = silu(a)
+            h = sa * b
+            if round_hidden:
+                h = round_to_bf16(h)
+            y = w_down[e] @ h
+            dgate[t, j] = dout[t] @ y
+            dy = gate[t, j] * dout[t]
+            dh = w_down[e].T @ dy
+            sig = 1.0 / (1.0 + np.exp(-a))
+            da = dh * b * (sig * (1.0 + a * (1.0 - sig)))  # silu'(a) = s + a s (1 - s)
+            db = dh * sa
+            dx[t] += w_gate[e].T @ da + w_up[e].T @ db
+            dwd[e] += np.outer(dy, h)
+            dwg[e] += np.outer(da, xt)
+            dwu[e] += np.outer(db, xt)
+    if s_gate is not None and s_gate.shape[0] > 0:
+        a = xb @ s_gate.T
+        b = xb @ s_up.T
+        sa = silu(a)
+        h = sa * b
+        if round_hidden:
+            h = round_to_bf16(h)
+        dh = dout @ s_down
+        sig = 1.0 / (1.0 + np.exp(-a))
+        da = dh * b * (sig * (1.0 + a * (1.0 - sig)))
+        db = dh * sa
+        dx += da @ s_gate + db @ s_up
+        dsd = dout.T @ h
+        dsg = da.T @ xb
+        dsu = db.T @ xb
+    else:
+        dsg = dsu = dsd = None
+    # Router: through the gates' scores.
+    dz = np.zeros((T, E), dtype=np.float64)
+    for t in range(T):
+        sel = [int(e) for e in idx[t]]
+        st = np.array([s_used[t, e] for e in sel])
+        if renorm:
+            S = st.sum()
+            dsel = (dgate[t] - (dgate[t] * gate[t]).sum()) / S
+        else:
+            dsel = dgate[t].copy()
+        for j, e in enumerate(sel):
+            dz[t, e] += dsel[j] * st[j] * (1.0 - st[j])
+    dx += dz @ w_router
+    dwr = dz.T @ x
+    if residual:
+        dx += dout
+    return dict(idx=idx, gate=gate, dgate=dgate, dz=dz, dx=dx, dw_gate=dwg, dw_up=dwu,
+                dw_down=dwd, ds_gate=dsg, ds_up=dsu, ds_down=dsd, dw_router=dwr)

@@ -371,3 +371,100 @@ def test_int4_roundtrip_error_bound_and_zero_group():
     assert (np.abs(deq - w) <= sc / 2 + np.abs(w) * 2 ** -10 + 1e-12).all()
     assert (codes[3, 32:64] == 0).all() and O.fp16_value_from_bits(scale)[3, 1] == 0.0
     assert codes.max() <= 7 and codes.min() >= -7
+
+
+# ---------------------------------------------------------------- backward
+
+def _bwd_case(seed, T=6, d=16, E=5, f=8, F=12, k=2):
+    """Small random layer in fp64 with a selection held fixed (top-k of its own
+    scores); the scores are kept away from ties so the selection is stable."""
+    rng = np.random.default_rng(seed)
+    P = dict(x=rng.standard_normal((T, d)), w_router=rng.standard_normal((E, d)) * 0.4,
+             bias=np.zeros(E, np.float32), w_gate=rng.standard_normal((E, f, d)) * 0.3,
+             w_up=rng.standard_normal((E, f, d)) * 0.3, w_down=rng.standard_normal((E, d, f)) * 0.3,
+             s_gate=rng.standard_normal((F, d)) * 0.3, s_up=rng.standard_normal((F, d)) * 0.3,
+             s_down=rng.standard_normal((d, F)) * 0.3, dout=rng.standard_normal((T, d)))
+    sc = O.router_scores(P["x"], P["w_router"])
+    P["idx"] = O.topk_select(sc.astype(np.float32), P["bias"], k)
+    return P
+
+
+def _torch_layer(P, k, renorm, residual):
+    """The layer written densely in PyTorch (CPU, fp64), selection fixed to P['idx'];
+    autograd supplies every gradient independently of the oracle's chain rule."""
+    t = {n: torch.tensor(P[n], dtype=torch.float64, requires_grad=True)
+         for n in ("x", "w_router", "w_gate", "w_up", "w_down", "s_gate", "s_up", "s_down")}
+    idx = torch.tensor(P["idx"].astype(np.int64))
+    s = torch.sigmoid(t["x"] @ t["w_router"].T)
+    ssel = torch.gather(s, 1, idx)
+    g = ssel / ssel.sum(dim=1, keepdim=True) if renorm else ssel
+    out = torch.zeros_like(t["x"])
+    for j in range(k):
+        e = idx[:, j]
+        a = torch.einsum("tfd,td->tf", t["w_gate"][e], t["x"])
+        b = torch.einsum("tfd,td->tf", t["w_up"][e], t["x"])
+        h = torch.nn.functional.silu(a) * b
+        y = torch.einsum("tdf,tf->td", t["w_down"][e], h)
+        out = out + g[:, j:j + 1] * y
+    hs = torch.nn.functional.silu(t["x"] @ t["s_gate"].T) * (t["x"] @ t["s_up"].T)
+    out = out + hs @ t["s_down"].T
+    if residual:
+        out = out + t["x"]
+    (out * torch.tensor(P["dout"])).sum().backward()
+    return {n: v.grad.numpy() for n, v in t.items()}
+
+
+@pytest.mark.parametrize("renorm,residual,k", [(True, False, 2), (False, True, 1), (True, True, 3)])
+def test_backward_matches_torch_autograd(renorm, residual, k):
+    P = _bwd_case(11 + k, k=k)
+    ref = _torch_layer(P, k, renorm, residual)
+    g = O.layer_backward(P["x"], P["w_router"], P["bias"], P["w_gate"], P["w_up"], P["w_down"],
+                         P["s_gate"], P["s_up"], P["s_down"], P["dout"], k=k, renorm=renorm,
+                         residual=residual, idx=P["idx"], exact_gates=True, round_hidden=False)
+    pairs = {"x": "dx", "w_router": "dw_router", "w_gate": "dw_gate", "w_up": "dw_up",
+             "w_down": "dw_down", "s_gate": "ds_gate", "s_up": "ds_up", "s_down": "ds_down"}
+    for n, m in pairs.items():
+        assert np.allclose(g[m], ref[n], rtol=1e-10, atol=1e-12), n
+
+
+def test_backward_directional_finite_differences():
+    """d/de <dout, out(theta + e v)> at e = 0 equals <grad, v> for random directions,
+    from the oracle's own forward (selection fixed, exact gates, H not rounded)."""
+    P = _bwd_case(5)
+    k = 2
+
+    def loss(**over):
+        Q = dict(P, **over)
+        r = O.layer_forward(Q["x"], Q["w_router"], Q["bias"], Q["w_gate"], Q["w_up"], Q["w_down"],
+                            Q["s_gate"], Q["s_up"], Q["s_down"], k=k, renorm=True, idx=P["idx"],
+                            exact_gates=True, round_hidden=False)
+        return float((r["out"] * P["dout"]).sum())
+
+    g = O.layer_backward(P["x"], P["w_router"], P["bias"], P["w_gate"], P["w_up"], P["w_down"],
+                         P["s_gate"], P["s_up"], P["s_down"], P["dout"], k=k, renorm=True,
+                         idx=P["idx"], exact_gates=True, round_hidden=False)
+    rng = np.random.default_rng(99)
+    eps = 1e-6
+    for n, m in (("x", "dx"), ("w_router", "dw_router"), ("w_gate", "dw_gate"), ("w_up", "dw_up"),
+                 ("w_down", "dw_down"), ("s_gate", "ds_gate"), ("s_up", "ds_up"), ("s_down", "ds_down")):
+        v = rng.standard_normal(P[n].shape)
+        fd = (loss(**{n: P[n] + eps * v}) - loss(**{n: P[n] - eps * v})) / (2 * eps)
+        assert abs(fd - float((g[m] * v).sum())) <= 1e-6 * max(1.0, abs(fd)), n
+
+
+def test_backward_gate_gradient_special_cases():
+    """Top-1 with renormalisation: the gate is the constant 1, so no gradient reaches
+    the router (the top-2 paragraph's reason for top-2); without renormalisation the
+    gate is the score and the router gradient is dgate * s (1 - s)."""
+    P = _bwd_case(3, k=1)
+    g = O.layer_backward(P["x"], P["w_router"], P["bias"], P["w_gate"], P["w_up"], P["w_down"],
+                         P["s_gate"], P["s_up"], P["s_down"], P["dout"], k=1, renorm=True,
+                         idx=P["idx"], exact_gates=True)
+    assert np.all(g["gate"] == 1.0) and np.all(g["dz"] == 0.0) and np.all(g["dw_router"] == 0.0)
+    g2 = O.layer_backward(P["x"], P["w_router"], P["bias"], P["w_gate"], P["w_up"], P["w_down"],
+                          P["s_gate"], P["s_up"], P["s_down"], P["dout"], k=1, renorm=False,
+                          idx=P["idx"], exact_gates=True)
+    sc = O.router_scores(P["x"], P["w_router"])
+    for t in range(P["x"].shape[0]):
+        e = int(P["idx"][t, 0])
+        assert np.isclose(g2["dz"][t, e], g2["dgate"][t, 0] * sc[t, e] * (1 - sc[t, e]), rtol=1e-12)
