@@ -330,6 +330,29 @@ def layer_forward(x, w_router, bias, w_gate, w_up, w_down, s_gate, s_up, s_down,
                 bias=new_bias)
 
 
+def shared_expert_backward(xb, s_gate, s_up, s_down, dout, round_hidden: bool = True):
+    """Gradients through the shared expert, out_t += Sd (silu(Sg x_t) * (Su x_t)), gate 1.
+
+    Relay article, architecture paragraph (the always-resident shared expert); the
+    chain rule as for one routed pair in layer_backward.  Returns (dx, dS_gate, dS_up,
+    dS_down) for all tokens at once, fp64.
+    """
+    xb = np.asarray(xb, dtype=np.float64)
+    dout = np.asarray(dout, dtype=np.float64)
+    a = xb @ s_gate.T
+    b = xb @ s_up.T
+    sa = silu(a)
+    h = sa * b
+    if round_hidden:
+        h = round_to_bf16(h)
+    dh = dout @ s_down
+    sig = 1.0 / (1.0 + np.exp(-a))
+    da = dh * b * (sig * (1.0 + a * (1.0 - sig)))
+    db = dh * sa
+    dx = da @ s_gate + db @ s_up
+    return dx, da.T @ xb, db.T @ xb, dout.T @ h
+
+
 def layer_backward(x, w_router, bias, w_gate, w_up, w_down, s_gate, s_up, s_down, dout, k: int,
                    renorm: bool = True, logit_offset=None, scores_f32=None,
                    residual: bool = False, x_is_bf16: bool = True, idx=None,
@@ -394,20 +417,8 @@ def layer_backward(x, w_router, bias, w_gate, w_up, w_down, s_gate, s_up, s_down
             dwg[e] += np.outer(da, xt)
             dwu[e] += np.outer(db, xt)
     if s_gate is not None and s_gate.shape[0] > 0:
-        a = xb @ s_gate.T
-        b = xb @ s_up.T
-        sa = silu(a)
-        h = sa * b
-        if round_hidden:
-            h = round_to_bf16(h)
-        dh = dout @ s_down
-        sig = 1.0 / (1.0 + np.exp(-a))
-        da = dh * b * (sig * (1.0 + a * (1.0 - sig)))
-        db = dh * sa
-        dx += da @ s_gate + db @ s_up
-        dsd = dout.T @ h
-        dsg = da.T @ xb
-        dsu = db.T @ xb
+        dxs, dsg, dsu, dsd = shared_expert_backward(xb, s_gate, s_up, s_down, dout, round_hidden)
+        dx += dxs
     else:
         dsg = dsu = dsd = None
     # Router: through the gates' scores.

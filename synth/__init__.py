@@ -9,5 +9,6 @@ from .moe_inputs import (  # noqa: F401
     bf16_bits_from_f32,
     f32_from_bf16_bits,
     make_layer,
+    make_output_grad,
     make_tokens,
 )

@@ -29,7 +29,7 @@ import numpy as np
 _CASE_ID = {"tiny": 0, "nano": 1, "skew": 2, "decode": 3, "stack": 4}
 _TENSOR_ID = {
     "x": 0, "w_router": 1, "bias": 2, "w_gate": 3, "w_up": 4, "w_down": 5,
-    "s_gate": 6, "s_up": 7, "s_down": 8,
+    "s_gate": 6, "s_up": 7, "s_down": 8, "dout": 9,
 }
 
 
@@ -99,6 +99,11 @@ def make_tokens(shape: LayerShape, case: str, seed: int = 0) -> np.ndarray:
     """Token activations x[T][d]: fp32 array for x_dtype 'f32', else bf16 bits (uint16)."""
     x = _normal(seed, case, 0, "x", (shape.T, shape.d), 1.0)
     return x if shape.x_dtype == "f32" else bf16_bits_from_f32(x)
+
+
+def make_output_grad(shape: LayerShape, case: str, seed: int = 0) -> np.ndarray:
+    """Gradient of a loss with respect to the layer output, dout[T][d] ~ N(0, 1), bf16 bits."""
+    return bf16_bits_from_f32(_normal(seed, case, 0, "dout", (shape.T, shape.d), 1.0))
 
 
 def zipf_logit_offset(E: int, s: float) -> np.ndarray:
