@@ -1,4 +1,4 @@
-"""Fine-grained MoE layer forward with aux-loss-free bias balancing on GB300 (sm_103a).
+"""Fine-grained MoE layer (forward and backward) with aux-loss-free bias balancing on GB300 (sm_103a).
 
 The computation lives in ``libmoe_gb300.so`` (CUDA kernels behind the C ABI declared
 in ``include/moe_gb300.h``); this package is its thin ctypes binding.  Build the
@@ -12,11 +12,13 @@ from ._lib import (  # noqa: F401
     MOE_X_F32,
     SIGNATURES,
     MoEDebug,
+    MoEGrads,
     MoEError,
     MoEShape,
     MoEWeights,
     load_library,
     make_debug,
+    make_grads,
     make_shape,
     make_weights,
     moe_abi_version,
@@ -26,6 +28,8 @@ from ._lib import (  # noqa: F401
     moe_expert_ffn,
     moe_expert_ffn_workspace_size,
     moe_gate_up_block,
+    moe_layer_bwd,
+    moe_layer_bwd_workspace_size,
     moe_layer_fwd,
     moe_layer_workspace_size,
     moe_pack_gate_up,

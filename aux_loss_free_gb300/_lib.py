@@ -44,6 +44,11 @@ class MoEDebug(ctypes.Structure):
                 ("perm_tok", _P), ("inv_pos", _P)]
 
 
+class MoEGrads(ctypes.Structure):
+    _fields_ = [("dx", _P), ("dw_router", _P), ("dw_gate_up", _P), ("dw_down", _P),
+                ("ds_gate_up", _P), ("ds_down", _P), ("dgate", _P)]
+
+
 _SHAPE_P = ctypes.POINTER(MoEShape)
 SIGNATURES = {
     "moe_abi_version": (_I32, []),
@@ -62,6 +67,9 @@ SIGNATURES = {
     "moe_layer_workspace_size": (_SZ, [_SHAPE_P]),
     "moe_layer_fwd": (_I32, [_SHAPE_P, _P, _P, _P, _P, _F, _I32, ctypes.POINTER(MoEWeights), _P,
                              _P, ctypes.POINTER(MoEDebug), _P, _SZ, _P]),
+    "moe_layer_bwd_workspace_size": (_SZ, [_SHAPE_P]),
+    "moe_layer_bwd": (_I32, [_SHAPE_P, _P, _P, ctypes.POINTER(MoEWeights), ctypes.POINTER(MoEDebug),
+                             _P, _I32, ctypes.POINTER(MoEGrads), _P, _SZ, _P]),
     "moe_pack_gate_up": (_I32, [_I32, _I32, _I32, _P, _P, _P, _P]),
     "moe_quantize_int4": (_I32, [_I64, _I32, _P, _P, _P, _P]),
     "moe_device_status": (_I32, [_P, ctypes.POINTER(_I32)]),
@@ -198,6 +206,24 @@ def make_debug(scores=None, idx=None, gate=None, load=None, offsets=None, perm_t
                inv_pos=None) -> MoEDebug:
     return MoEDebug(_ptr(scores), _ptr(idx), _ptr(gate), _ptr(load), _ptr(offsets), _ptr(perm_tok),
                     _ptr(inv_pos))
+
+
+def moe_layer_bwd_workspace_size(shape) -> int:
+    return load_library().moe_layer_bwd_workspace_size(ctypes.byref(shape))
+
+
+def make_grads(dx, dw_router, dw_gate_up, dw_down, ds_gate_up=None, ds_down=None,
+               dgate=None) -> MoEGrads:
+    return MoEGrads(_ptr(dx), _ptr(dw_router), _ptr(dw_gate_up), _ptr(dw_down), _ptr(ds_gate_up),
+                    _ptr(ds_down), _ptr(dgate))
+
+
+def moe_layer_bwd(shape, x, w_router, weights: MoEWeights, saved: MoEDebug, dout, residual,
+                  grads: MoEGrads, workspace, stream=None):
+    _check("moe_layer_bwd", load_library().moe_layer_bwd(
+        ctypes.byref(shape), _ptr(x), _ptr(w_router), ctypes.byref(weights), ctypes.byref(saved),
+        _ptr(dout), int(residual), ctypes.byref(grads), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def moe_pack_gate_up(G, width, d, w_gate, w_up, w_gate_up, stream=None):

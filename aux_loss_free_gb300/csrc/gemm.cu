@@ -70,6 +70,9 @@ struct OperandSet {
   void* out;
   int ldo, n_total, k_total, bn, mode, enabled, rows;
   int v8;  // output rows start on 32-byte boundaries: 256-bit stores allowed
+  // MN-major operands: the map views [K rows][M or N] as (64 elements, K rows, atoms
+  // of 64 along M/N), box (64, BK, atoms per CTA), one copy per operand per k-block.
+  int a_mn, b_mn;
 };
 
 struct Params {
@@ -81,6 +84,12 @@ struct Params {
   const float* gate;
   const uint16_t* residual;
   int* status;
+  // Non-zero: the routed set is grouped along K instead of along the rows: group g
+  // multiplies A[:, koff[g]..koff[g+1]) by B[:, same] (offsets holds koff, each a
+  // multiple of 64) into its own output, out + g * group_stride; groups with an empty
+  // range are skipped.  Used for the weight gradients, K running over tokens.
+  int kgroup;
+  long long group_stride;
   int E, k;
 };
 
@@ -90,6 +99,10 @@ struct Tile {
   int rend;   // end (exclusive) of the group's rows
   int brow;   // first B row of the BN-row weight tile
   int n0;     // first accumulator column in the output
+  int k0;     // first K column (K-grouped sets; else 0)
+  int klen;   // K columns
+  int group;  // K group (K-grouped sets; else 0)
+  int bk;     // first K row of the group's B (MN-major B of an M-grouped set)
 };
 
 // ---------------------------------------------------------------- cluster PTX
@@ -193,6 +206,9 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, int tile, int share
     tile = (r_after > r_before) ? shared_tiles + (int)r_before : tile - (int)r_before;
   }
   Tile t;
+  t.k0 = 0;
+  t.group = 0;
+  t.bk = 0;
   if (tile < shared_tiles) {
     const int nt = p.shared.n_total / p.shared.bn;
     const int m = tile / nt, n = tile % nt;
@@ -201,6 +217,20 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, int tile, int share
     t.rend = p.shared.rows;
     t.n0 = n * p.shared.bn;
     t.brow = t.n0;
+    t.klen = p.shared.k_total;
+  } else if (p.kgroup) {
+    const int r = tile - shared_tiles;
+    const int nt = p.routed.n_total / p.routed.bn;
+    const int tpg = ((p.routed.rows + BM - 1) / BM) * nt;
+    const int g = r / tpg, local = r % tpg;
+    t.set = 1;
+    t.row0 = (local / nt) * BM;
+    t.rend = p.routed.rows;
+    t.n0 = (local % nt) * p.routed.bn;
+    t.brow = t.n0;
+    t.group = g;
+    t.k0 = s_off[g];
+    t.klen = s_off[g + 1] - s_off[g];
   } else {
     const int r = tile - shared_tiles;
     int lo = 0, hi = p.E;  // largest g with s_cum[g] <= r (that group is non-empty)
@@ -217,6 +247,8 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, int tile, int share
     t.rend = s_off[g + 1];
     t.n0 = n * p.routed.bn;
     t.brow = g * p.routed.n_total + t.n0;
+    t.bk = g * p.routed.k_total;
+    t.klen = p.routed.k_total;
   }
   return t;
 }
@@ -340,7 +372,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   if (warp == 2) {
     // Tile table of the routed groups: s_cum[g] = tiles of groups < g.
     int carry = 0;
-    if (p.routed.enabled) {
+    if (p.routed.enabled && p.kgroup) {
+      // K-grouped: a fixed number of tiles per group; s_off holds the K offsets.
+      for (int g = lane; g <= p.E; g += 32) s_off[g] = p.offsets[g];
+      carry = p.E * ((p.routed.rows + BM - 1) / BM) * (p.routed.n_total / p.routed.bn);
+    } else if (p.routed.enabled) {
       const int nt = p.routed.n_total / p.routed.bn;
       for (int b = 0; b < p.E; b += 32) {
         const int g = b + lane;
@@ -379,8 +415,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       for (int tile = cluster; tile < total && ok; tile += nclusters) {
         const Tile t = decode_tile(p, tile, shared_tiles, s_off, s_cum, total);
         const OperandSet& S = t.set ? p.routed : p.shared;
-        const int nkb = (S.k_total + BK - 1) / BK;
+        const int nkb = (t.klen + BK - 1) / BK;  // 0 for an empty K group: nothing loaded
         const int half = S.bn / 2;
+        const int katom0 = t.k0 / AK;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait_spin(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) {
             ok = false;
@@ -388,20 +425,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           }
           // Both atoms of the k-block in one copy per operand (an atom past K arrives
           // zero-filled and is not multiplied); with 2-D maps, atoms past K are not
-          // loaded at all.
-          const int natoms = S.kblock ? ATOMS : min(ATOMS, (S.k_total - kb * BK + AK - 1) / AK);
+          // loaded at all.  MN-major operands: one copy of BK rows (k) by the CTA's
+          // 64-element atoms along M / N; rows past K arrive as zeros or belong to the
+          // next group and meet zero (or unmultiplied) columns of the other operand.
+          const int natoms = S.kblock ? ATOMS : min(ATOMS, (t.klen - kb * BK + AK - 1) / AK);
           const uint32_t pair_bytes = 2u * natoms * (A_ATOM + half * AK * 2);
           const uint32_t sa = ring + stage * STAGE_BYTES;
           const uint32_t fb = map_to_rank(smem_u32(&full_bar[stage]), 0);
           const uint32_t b_atom = (uint32_t)half * AK * 2;
           if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[stage]), pair_bytes);
-          if (S.kblock) {
-            tma_load_kblock_pair(sa, &S.a, fb, t.row0 + HM * (int)rank, kb * ATOMS);
-            tma_load_kblock_pair(sa + A_BYTES, &S.b, fb, t.brow + half * (int)rank, kb * ATOMS);
+          if (S.a_mn | S.b_mn) {
+            const int kk0 = t.k0 + kb * BK;
+            if (S.a_mn)
+              tma_load_kblock_pair(sa, &S.a, fb, kk0, (t.row0 + HM * (int)rank) / AK);
+            else
+              tma_load_kblock_pair(sa, &S.a, fb, t.row0 + HM * (int)rank, katom0 + kb * ATOMS);
+            if (S.b_mn)
+              tma_load_kblock_pair(sa + A_BYTES, &S.b, fb, t.bk + kk0, (t.n0 + half * (int)rank) / AK);
+            else
+              tma_load_kblock_pair(sa + A_BYTES, &S.b, fb, t.brow + half * (int)rank, katom0 + kb * ATOMS);
+          } else if (S.kblock) {
+            tma_load_kblock_pair(sa, &S.a, fb, t.row0 + HM * (int)rank, katom0 + kb * ATOMS);
+            tma_load_kblock_pair(sa + A_BYTES, &S.b, fb, t.brow + half * (int)rank, katom0 + kb * ATOMS);
           } else {
             for (int at = 0; at < natoms; ++at) {
-              tma_load_2d_pair(sa + at * A_ATOM, &S.a, fb, kb * BK + at * AK, t.row0 + HM * (int)rank);
-              tma_load_2d_pair(sa + A_BYTES + at * b_atom, &S.b, fb, kb * BK + at * AK,
+              tma_load_2d_pair(sa + at * A_ATOM, &S.a, fb, t.k0 + kb * BK + at * AK,
+                               t.row0 + HM * (int)rank);
+              tma_load_2d_pair(sa + A_BYTES + at * b_atom, &S.b, fb, t.k0 + kb * BK + at * AK,
                                t.brow + half * (int)rank);
             }
           }
@@ -429,12 +479,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       for (int tile = cluster; tile < total && ok; tile += nclusters) {
         const int set = tile_set(tile, shared_tiles, total);
-        const int k_total = set ? p.routed.k_total : p.shared.k_total;
+        int k_total = set ? p.routed.k_total : p.shared.k_total;
+        if (set && p.kgroup) {  // this tile's K group
+          k_total = decode_tile(p, tile, shared_tiles, s_off, s_cum, total).klen;
+          if (k_total == 0) continue;  // empty group: no MMA, no accumulator hand-off
+        }
         const int bn = set ? p.routed.bn : p.shared.bn;
+        const int a_mn = set ? p.routed.a_mn : p.shared.a_mn;
+        const int b_mn = set ? p.routed.b_mn : p.shared.b_mn;
         const int nkb = (k_total + BK - 1) / BK;
         const int nkk_last = (k_total - (nkb - 1) * BK + 15) / 16;
         const uint32_t b_atom = (uint32_t)bn / 2 * AK * 2;
-        const uint32_t idesc = idesc_bf16_f32(BM, bn);
+        const uint32_t idesc = idesc_bf16_f32(BM, bn, a_mn, b_mn);
+        // Descriptor advance (16-byte units) of K step kk = 4 * x + y: K-major, x picks
+        // the 64-column atom and y moves 32 B inside its rows; MN-major, every step is
+        // two 1024-byte atoms further along K.
+        const uint32_t ax = a_mn ? 512u : (uint32_t)(A_ATOM >> 4), ay = a_mn ? 128u : 2u;
+        const uint32_t bx = b_mn ? 512u : (b_atom >> 4), by = b_mn ? 128u : 2u;
         if (!mbar_wait_spin(smem_u32(&tempty_bar[acc]), acc_phase ^ 1u, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN_MAX;
@@ -445,21 +506,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           }
           tc_fence_after();
           const uint32_t sa = ring + stage * STAGE_BYTES;
-          uint64_t adesc[ATOMS], bdesc[ATOMS];
-#pragma unroll
-          for (int at = 0; at < ATOMS; ++at) {
-            adesc[at] = sw128_kmajor_desc(sa + at * A_ATOM);
-            bdesc[at] = sw128_kmajor_desc(sa + A_BYTES + at * b_atom);  // b_atom: BN/2 rows x 128 B
-          }
+          // MN-major: atom columns (64 elements x BK rows) are BK * 128 B apart.
+          const uint64_t adesc = a_mn ? sw128_mnmajor_desc(sa, BK * 128) : sw128_kmajor_desc(sa);
+          const uint64_t bdesc = b_mn ? sw128_mnmajor_desc(sa + A_BYTES, BK * 128)
+                                      : sw128_kmajor_desc(sa + A_BYTES);
           if (kb + 1 < nkb) {
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
-              mma_pair_bf16(d_tmem, adesc[kk >> 2] + 2 * (kk & 3), bdesc[kk >> 2] + 2 * (kk & 3),
-                            idesc, (kb | kk) != 0);
+              mma_pair_bf16(d_tmem, adesc + (kk >> 2) * ax + (kk & 3) * ay,
+                            bdesc + (kk >> 2) * bx + (kk & 3) * by, idesc, (kb | kk) != 0);
           } else {
             for (int kk = 0; kk < nkk_last; ++kk)
-              mma_pair_bf16(d_tmem, adesc[kk >> 2] + 2 * (kk & 3), bdesc[kk >> 2] + 2 * (kk & 3),
-                            idesc, (kb | kk) != 0);
+              mma_pair_bf16(d_tmem, adesc + (kk >> 2) * ax + (kk & 3) * ay,
+                            bdesc + (kk >> 2) * bx + (kk & 3) * by, idesc, (kb | kk) != 0);
           }
           commit_pair_multicast(smem_u32(&empty_bar[stage]));
           if (++stage == STAGES) {
@@ -487,6 +546,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     for (int tile = cluster; tile < total; tile += nclusters) {
       const Tile t = decode_tile(p, tile, shared_tiles, s_off, s_cum, total);
       const OperandSet& S = t.set ? p.routed : p.shared;
+      if (t.klen == 0) {
+        // Empty K group (an expert without tokens): the issuer skipped it; its fp32
+        // output is zero.
+        const long long orow = (long long)t.row0 + HM * (int)rank + q * 32 + lane;
+        if (S.mode == EPI_STORE_F32 && orow < t.rend) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(S.out) +
+                                                  (long long)t.group * p.group_stride + orow * S.ldo + t.n0);
+          for (int c = 4 * colh; c < S.bn / 4; c += 4 * EPI_GROUPS)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[c + i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        continue;
+      }
       int ok = 1;
       if (lane == 0) ok = mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, p.status) ? 1 : 0;
       ok = __shfl_sync(FULL, ok, 0);
@@ -508,6 +580,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) h[i] = silu(__uint_as_float(g[i])) * __uint_as_float(u[i]);
           if (valid) store_bf16_row32(out + orow * S.ldo + t.n0 / 2 + c, h, S.v8);
+        }
+      } else if (S.mode == EPI_STORE_F32) {
+        // fp32 output (weight gradients); K groups write their own matrices.
+        float* o32 = static_cast<float*>(S.out) + (long long)t.group * p.group_stride;
+        for (int c = 32 * colh; c < S.bn; c += CS) {
+          uint32_t v[32];
+          tmem_ld32(tbase + c, v);
+          tmem_wait_ld();
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(o32 + orow * S.ldo + t.n0 + c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                   __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+          }
         }
       } else if (S.mode == EPI_STORE) {
         // Two 32-column chunks per TMEM round trip.
@@ -612,16 +699,18 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
   return r == CUDA_SUCCESS;
 }
 
-// The same matrix as (64 columns, outer rows, inner / 64 atoms), box (64, box_outer, 2):
-// one copy = two consecutive 64-column atoms, each [box_outer][64] with the 128-byte
-// swizzle, the second box_outer * 128 bytes after the first.
+// The same matrix as (64 columns, outer rows, inner / 64 atoms), box (64, box_outer,
+// box_atoms): one copy = box_atoms consecutive 64-column atoms, each [box_outer][64]
+// with the 128-byte swizzle, box_outer * 128 bytes apart.  K-major operands: inner = K,
+// two atoms = one k-block.  MN-major operands: inner = M or N, outer = K rows,
+// box_outer = BK.
 bool make_map_kblock(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
-                     uint32_t box_outer) {
+                     uint32_t box_outer, uint32_t box_atoms = ATOMS) {
   auto fn = encode_fn();
   if (!fn || inner % AK != 0) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(AK), outer, inner / AK};
   const cuuint64_t strides[2] = {inner * 2, static_cast<cuuint64_t>(AK) * 2};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(AK), box_outer, static_cast<cuuint32_t>(ATOMS)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(AK), box_outer, box_atoms};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -633,6 +722,7 @@ int gate_up_block(int width) { return width % 128 == 0 ? 128 : (width % 64 == 0 
 
 int choose_bn(int mode, int N) {
   if (mode == EPI_SWIGLU) return 2 * gate_up_block(N / 2);
+  if (mode == EPI_STORE_F32) return N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : (N % 64 == 0 ? 64 : 32));
   return N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : 64);
 }
 
@@ -669,6 +759,19 @@ bool fill_set(OperandSet& t, const GemmOperandSet& o) {
   t.out = o.out;
   t.v8 = (reinterpret_cast<uintptr_t>(o.out) % 32 == 0) && ((long long)o.ldo * 2) % 32 == 0;
   if (o.N % t.bn != 0) return false;
+  t.a_mn = o.a_mn ? 1 : 0;
+  t.b_mn = o.b_mn ? 1 : 0;
+  if (t.a_mn || t.b_mn) {
+    // Whole k-blocks of both operands per copy (the expected byte count assumes it).
+    if ((!t.a_mn || !t.b_mn) && o.K % AK != 0) return false;
+    if (t.b_mn && t.bn % 128 != 0) return false;
+    t.kblock = 1;
+    const bool ma = t.a_mn ? make_map_kblock(&t.a, o.a, o.rows, o.K, BK, HM / AK)
+                           : make_map_kblock(&t.a, o.a, o.K, o.a_rows, HM);
+    const bool mb = t.b_mn ? make_map_kblock(&t.b, o.b, o.N, (uint64_t)o.groups * o.K, BK, t.bn / 2 / AK)
+                           : make_map_kblock(&t.b, o.b, o.K, (uint64_t)o.groups * o.N, t.bn / 2);
+    return ma && mb;
+  }
   t.kblock = o.K % AK == 0;
   if (t.kblock) {
     if (!make_map_kblock(&t.a, o.a, o.K, o.a_rows, HM)) return false;
@@ -697,7 +800,7 @@ int gemm_max_pairs() {
 cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* offsets, int E,
                                 const GemmOperandSet& shared, const CombineInputs& comb,
                                 long long max_routed_rows, cudaStream_t s, int* bad_arg,
-                                int max_pairs) {
+                                int max_pairs, long long kgroup_stride) {
   Params p;
   std::memset(&p, 0, sizeof(p));
   *bad_arg = 0;
@@ -713,6 +816,8 @@ cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* off
   p.gate = comb.gate;
   p.residual = comb.residual;
   p.k = comb.k;
+  p.kgroup = kgroup_stride > 0 ? 1 : 0;
+  p.group_stride = kgroup_stride;
   p.status = device_status_ptr();
   if (!p.status) return cudaErrorInvalidDevicePointer;
 
@@ -722,7 +827,9 @@ cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* off
   long long tiles = 0;
   if (p.shared.enabled)
     tiles += (long long)((p.shared.rows + BM - 1) / BM) * (p.shared.n_total / p.shared.bn);
-  if (p.routed.enabled)
+  if (p.routed.enabled && p.kgroup)
+    tiles += (long long)E * ((p.routed.rows + BM - 1) / BM) * (p.routed.n_total / p.routed.bn);
+  else if (p.routed.enabled)
     tiles += ((max_routed_rows + BM - 1) / BM + E) * (long long)(p.routed.n_total / p.routed.bn);
   int cap = max_active_pairs();
   if (max_pairs > 0 && max_pairs < cap) cap = max_pairs;

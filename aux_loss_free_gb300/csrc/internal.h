@@ -98,7 +98,7 @@ cudaError_t launch_pack_gate_up(int G, int width, int d, int block, const uint16
                                 const uint16_t* wu, uint16_t* wgu, cudaStream_t s);
 
 // ---------------------------------------------------------------- grouped GEMM
-enum EpiMode { EPI_SWIGLU = 0, EPI_STORE = 1, EPI_COMBINE = 2 };
+enum EpiMode { EPI_SWIGLU = 0, EPI_STORE = 1, EPI_COMBINE = 2, EPI_STORE_F32 = 3 };
 
 struct GemmOperandSet {
   const void* a;        // bf16 [a_rows][K]
@@ -110,6 +110,13 @@ struct GemmOperandSet {
   int ldo;
   int mode;             // EpiMode
   int rows;             // shared set: rows of the single group
+  // MN-major operands (stored [K][M] / [groups * K][N], the M or N index contiguous),
+  // read through the tensor cores' transpose bits: no transposed copies.  M, N must
+  // be multiples of 128 there (each CTA's half of a 256-wide tile is whole 64-element
+  // atoms), and a K-major A beside an MN-major operand needs K % 64 == 0.  An MN-major
+  // A takes its M extent from `rows` and its K extent from K.
+  int a_mn;
+  int b_mn;
 };
 struct CombineInputs {
   const uint16_t* y_perm;
@@ -122,10 +129,13 @@ struct CombineInputs {
 // rows from device `offsets`) and `shared` (one group).  Either may be disabled
 // with a null `a`.
 // max_pairs > 0 caps the number of 2-SM clusters (leaving SMs to concurrent work).
+// kgroup_stride > 0 groups the routed set along K instead: offsets then holds the
+// E + 1 K offsets (multiples of 64), `routed.rows` is every group's row count, and
+// group g writes out + g * kgroup_stride (EPI_STORE_F32 for fp32 outputs).
 cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* offsets, int E,
                                 const GemmOperandSet& shared, const CombineInputs& comb,
                                 long long max_routed_rows, cudaStream_t s, int* bad_arg,
-                                int max_pairs = 0);
+                                int max_pairs = 0, long long kgroup_stride = 0);
 // Number of co-resident 2-SM clusters of the grouped GEMM on the current device.
 int gemm_max_pairs();
 
@@ -157,5 +167,26 @@ cudaError_t launch_int4_direct(bool gate_up, const int32_t* idx, int pairs, int 
 cudaError_t launch_int4_down(const int32_t* active, const int32_t* offsets, const uint8_t* wq,
                              const uint16_t* ws, const uint16_t* h, uint16_t* y, int d, int f,
                              cudaStream_t s);
+
+// ---------------------------------------------------------------- backward
+// Padded layout of the permuted rows (each expert's rows start on a multiple of 64):
+// poff [E+1], tok_pad [q_max] (-1 = padding), inv_pad [pairs], gperm [q_max] (the
+// gate of each padded row, 0 on padding).
+cudaError_t launch_pad_map(const int32_t* off, const int32_t* perm_tok, const int32_t* idx,
+                           const int32_t* inv_pos, const float* gate, int E, long long pairs,
+                           long long q_max, int32_t* poff, int32_t* tok_pad, int32_t* inv_pad,
+                           float* gperm, cudaStream_t s);
+cudaError_t launch_gather_pad(const uint16_t* x, const uint16_t* dout, const int32_t* tok_pad,
+                              long long q_max, const int32_t* rows_limit, int d, uint16_t* xp,
+                              uint16_t* dp, cudaStream_t s);
+cudaError_t launch_swiglu_bwd(uint16_t* ab, uint16_t* dh, const float* gperm, long long rows,
+                              const int32_t* rows_limit, int w, int block, float* dg, cudaStream_t s);
+cudaError_t launch_router_bwd_dx(const int32_t* idx, const float* gate, const float* scores,
+                                 const int32_t* inv_pad, const float* dgp, const float* w_router,
+                                 const uint16_t* dxp, const uint16_t* dxs, const uint16_t* dout, int T,
+                                 int d, int E, int k, int renorm, float* dzp, float* dgate, uint16_t* dx,
+                                 cudaStream_t s);
+cudaError_t launch_router_wgrad(const float* dzp, const int32_t* off, const int32_t* poff,
+                                const uint16_t* xp, int d, int E, float* dwr, cudaStream_t s);
 
 }  // namespace moe

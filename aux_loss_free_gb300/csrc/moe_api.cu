@@ -632,6 +632,170 @@ moe_status_t moe_layer_fwd(const moe_shape_t* shape, const void* x, const float*
   return st2;
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------- layer backward
+
+namespace {
+
+moe_status_t check_bwd_shape(const moe_shape_t* s) {
+  const moe_status_t st = check_shape(s);
+  if (st != MOE_OK) return st;
+  if (s->x_dtype != MOE_X_BF16 || s->w_format != MOE_W_BF16) return MOE_ERR_UNSUPPORTED;
+  // MN-major operands of the backward GEMMs: whole 128-element halves of a tile.
+  if (s->d % 128 || s->f % 128 || s->F % 128) return MOE_ERR_UNSUPPORTED;
+  if ((long long)s->T * s->k + 63LL * s->E > (1LL << 30)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+// Rows of the padded permuted layout: every pair plus up to 63 padding rows per expert.
+long long bwd_rows(const moe_shape_t* s) { return (long long)s->T * s->k + 63LL * s->E; }
+
+struct BwdWs {
+  int32_t* poff;     // [E+1] padded expert offsets
+  int32_t* tok_pad;  // [Q] source token of each padded row (-1 = padding)
+  int32_t* inv_pad;  // [T*k] padded row of each pair
+  float* gperm;      // [Q] gate of each padded row
+  float* dgp;        // [Q] dL/dgate of each padded row
+  float* dzp;        // [Q] dL/dlogit of each padded row
+  uint16_t* xp;      // [Q][d] gathered tokens
+  uint16_t* dp;      // [Q][d] gathered output gradients
+  uint16_t* ab;      // [Q][2f] gate/up pre-activations, then their gradients
+  uint16_t* dh;      // [Q][f] dout Wd, then gate * h
+  uint16_t* dxp;     // [Q][d] routed input gradient of each row
+  uint16_t* abs;     // [T][2F] shared expert: as ab
+  uint16_t* dhs;     // [T][F] as dh (gate 1)
+  uint16_t* dxs;     // [T][d] shared expert's input gradient
+};
+BwdWs carve_bwd(Carver& c, const moe_shape_t* s) {
+  const size_t Q = (size_t)bwd_rows(s), Tk = (size_t)s->T * s->k, T = (size_t)s->T;
+  BwdWs w;
+  w.poff = static_cast<int32_t*>(c.take(4 * (size_t)(s->E + 1)));
+  w.tok_pad = static_cast<int32_t*>(c.take(4 * Q));
+  w.inv_pad = static_cast<int32_t*>(c.take(4 * Tk));
+  w.gperm = static_cast<float*>(c.take(4 * Q));
+  w.dgp = static_cast<float*>(c.take(4 * Q));
+  w.dzp = static_cast<float*>(c.take(4 * Q));
+  w.xp = static_cast<uint16_t*>(c.take(2 * Q * s->d));
+  w.dp = static_cast<uint16_t*>(c.take(2 * Q * s->d));
+  w.ab = static_cast<uint16_t*>(c.take(2 * Q * 2 * s->f));
+  w.dh = static_cast<uint16_t*>(c.take(2 * Q * s->f));
+  w.dxp = static_cast<uint16_t*>(c.take(2 * Q * s->d));
+  w.abs = s->F ? static_cast<uint16_t*>(c.take(2 * T * 2 * s->F)) : nullptr;
+  w.dhs = s->F ? static_cast<uint16_t*>(c.take(2 * T * s->F)) : nullptr;
+  w.dxs = s->F ? static_cast<uint16_t*>(c.take(2 * T * s->d)) : nullptr;
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_layer_bwd_workspace_size(const moe_shape_t* shape) {
+  if (check_bwd_shape(shape) != MOE_OK) return 0;
+  Carver c(nullptr);
+  carve_bwd(c, shape);
+  return c.off + kAlign;
+}
+
+moe_status_t moe_layer_bwd(const moe_shape_t* shape, const void* x, const float* w_router,
+                           const moe_weights_t* w, const moe_debug_t* saved, const void* dout,
+                           int32_t residual, const moe_grads_t* g, void* workspace, size_t ws_bytes,
+                           void* stream) {
+  const moe_status_t st = check_bwd_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!x || !w_router || !w || !saved || !dout || !g || !workspace) return MOE_ERR_INVALID_ARG;
+  if (residual != 0 && residual != 1) return MOE_ERR_INVALID_ARG;
+  if (!w->w_gate_up || !w->w_down || !saved->scores || !saved->idx || !saved->gate ||
+      !saved->offsets || !saved->perm_tok || !saved->inv_pos || !g->dx || !g->dw_router ||
+      !g->dw_gate_up || !g->dw_down)
+    return MOE_ERR_INVALID_ARG;
+  const bool has_shared = shape->F > 0;
+  if (has_shared != (w->shared_gate_up && w->shared_down && g->ds_gate_up && g->ds_down))
+    return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, w_router, w->w_gate_up, w->w_down, dout, g->dx, g->dw_router,
+                        g->dw_gate_up, g->dw_down, workspace};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
+  if (has_shared && (!aligned16(w->shared_gate_up) || !aligned16(w->shared_down) ||
+                     !aligned16(g->ds_gate_up) || !aligned16(g->ds_down)))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_layer_bwd_workspace_size(shape)) return MOE_ERR_WORKSPACE;
+
+  const int T = shape->T, d = shape->d, E = shape->E, k = shape->k, f = shape->f, F = shape->F;
+  const long long P = (long long)T * k, Q = bwd_rows(shape);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(workspace) + kAlign - 1) / kAlign * kAlign);
+  Carver c(base);
+  const BwdWs b = carve_bwd(c, shape);
+  const uint16_t* xb = static_cast<const uint16_t*>(x);
+  const uint16_t* db = static_cast<const uint16_t*>(dout);
+  int bad = 0;
+  CombineInputs none{};
+  cudaError_t e;
+
+  // Padded permuted layout, then the gathered tokens and output gradients.
+  e = launch_pad_map(saved->offsets, saved->perm_tok, saved->idx, saved->inv_pos, saved->gate, E, P, Q,
+                     b.poff, b.tok_pad, b.inv_pad, b.gperm, s);
+  if (e == cudaSuccess) e = launch_gather_pad(xb, db, b.tok_pad, Q, b.poff + E, d, b.xp, b.dp, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  // (1) Gate/up pre-activations, recomputed: ab = xp Wgu_e^T, abs = x Sgu^T.
+  {
+    GemmOperandSet r{b.xp, Q, w->w_gate_up, E, 2 * f, d, b.ab, 2 * f, EPI_STORE, 0};
+    GemmOperandSet sh{};
+    if (has_shared) sh = GemmOperandSet{x, T, w->shared_gate_up, 1, 2 * F, d, b.abs, 2 * F, EPI_STORE, T};
+    e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad);
+  }
+  // (2) dh = dout Wd_e (B = the stored [d][f] weights, MN-major), dhs = dout Sd.
+  if (e == cudaSuccess) {
+    GemmOperandSet r{b.dp, Q, w->w_down, E, f, d, b.dh, f, EPI_STORE, 0, 0, 1};
+    GemmOperandSet sh{};
+    if (has_shared) sh = GemmOperandSet{dout, T, w->shared_down, 1, F, d, b.dhs, F, EPI_STORE, T, 0, 1};
+    e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad);
+  }
+  // (3) SwiGLU backward in place: ab <- (da, db), dh <- gate * h, dgp = <dout, y>.
+  if (e == cudaSuccess)
+    e = launch_swiglu_bwd(b.ab, b.dh, b.gperm, Q, b.poff + E, f, moe_gate_up_block(f), b.dgp, s);
+  if (e == cudaSuccess && has_shared)
+    e = launch_swiglu_bwd(b.abs, b.dhs, nullptr, T, nullptr, F, moe_gate_up_block(F), nullptr, s);
+  // (4) dxp = (da, db) Wgu_e (B = the stored [2f][d] weights, MN-major), dxs likewise.
+  if (e == cudaSuccess) {
+    GemmOperandSet r{b.ab, Q, w->w_gate_up, E, d, 2 * f, b.dxp, d, EPI_STORE, 0, 0, 1};
+    GemmOperandSet sh{};
+    if (has_shared) sh = GemmOperandSet{b.abs, T, w->shared_gate_up, 1, d, 2 * F, b.dxs, d, EPI_STORE, T, 0, 1};
+    e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad);
+  }
+  // (5) Router backward and dx = sum of the pairs' rows + shared + router (+ dout).
+  if (e == cudaSuccess)
+    e = launch_router_bwd_dx(saved->idx, saved->gate, saved->scores, b.inv_pad, b.dgp, w_router, b.dxp,
+                             has_shared ? b.dxs : nullptr, residual ? db : nullptr, T, d, E, k,
+                             shape->renorm, b.dzp, g->dgate, static_cast<uint16_t*>(g->dx), s);
+  // (6) dWd_e = dp^T (gate * h) over the expert's rows (K-grouped), dSd = dout^T hs.
+  if (e == cudaSuccess) {
+    GemmOperandSet r{b.dp, Q, b.dh, 1, f, (int)Q, g->dw_down, f, EPI_STORE_F32, d, 1, 1};
+    GemmOperandSet sh{};
+    if (has_shared) sh = GemmOperandSet{dout, T, b.dhs, 1, F, T, g->ds_down, F, EPI_STORE_F32, d, 1, 1};
+    e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad, 0, (long long)d * f);
+  }
+  // (7) dWgu_e = (da, db)^T xp (rows interleaved as w_gate_up), dSgu = (das, dbs)^T x.
+  if (e == cudaSuccess) {
+    GemmOperandSet r{b.ab, Q, b.xp, 1, d, (int)Q, g->dw_gate_up, d, EPI_STORE_F32, 2 * f, 1, 1};
+    GemmOperandSet sh{};
+    if (has_shared) sh = GemmOperandSet{b.abs, T, x, 1, d, T, g->ds_gate_up, d, EPI_STORE_F32, 2 * F, 1, 1};
+    e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad, 0, (long long)2 * f * d);
+  }
+  // (8) dW_r[e] = sum over the expert's rows of dz * x.
+  if (e == cudaSuccess) e = launch_router_wgrad(b.dzp, saved->offsets, b.poff, b.xp, d, E, g->dw_router, s);
+  if (bad) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(e);
+}
+
+}  // extern "C"
+
+extern "C" {
+
 moe_status_t moe_pack_gate_up(int32_t G, int32_t width, int32_t d, const void* w_gate,
                               const void* w_up, void* w_gate_up, void* stream) {
   if (G < 1 || width < 32 || width % 32 || d < 8 || d % 8 || !w_gate || !w_up || !w_gate_up)

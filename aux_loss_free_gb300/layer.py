@@ -85,3 +85,56 @@ class LayerOnDevice:
                         update_bias, self.weights, residual, out, self.workspace, debug=debug,
                         stream=stream)
         return out
+
+
+class SavedForward:
+    """The forward's routing state that moe_layer_bwd needs (device tensors)."""
+
+    def __init__(self, T: int, E: int, k: int, device):
+        dev = torch.device(device)
+        self.scores = torch.empty((T, E), dtype=torch.float32, device=dev)
+        self.idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+        self.gate = torch.empty((T, k), dtype=torch.float32, device=dev)
+        self.load = torch.empty(E, dtype=torch.int32, device=dev)
+        self.offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        self.perm_tok = torch.empty(T * k, dtype=torch.int32, device=dev)
+        self.inv_pos = torch.empty((T, k), dtype=torch.int32, device=dev)
+        self.debug = L.make_debug(self.scores, self.idx, self.gate, self.load, self.offsets,
+                                  self.perm_tok, self.inv_pos)
+
+
+class LayerGrads:
+    """Gradient buffers of one layer: bf16 dx, fp32 weight gradients."""
+
+    def __init__(self, layer: "LayerOnDevice", want_dgate: bool = False):
+        s, dev = layer.spec, layer.device
+        self.dx = torch.empty((s.T, s.d), dtype=torch.bfloat16, device=dev)
+        self.dw_router = torch.empty((s.E, s.d), dtype=torch.float32, device=dev)
+        self.dw_gate_up = torch.empty((s.E, 2 * s.f, s.d), dtype=torch.float32, device=dev)
+        self.dw_down = torch.empty((s.E, s.d, s.f), dtype=torch.float32, device=dev)
+        self.ds_gate_up = self.ds_down = None
+        if s.F:
+            self.ds_gate_up = torch.empty((2 * s.F, s.d), dtype=torch.float32, device=dev)
+            self.ds_down = torch.empty((s.d, s.F), dtype=torch.float32, device=dev)
+        self.dgate = torch.empty((s.T, s.k), dtype=torch.float32, device=dev) if want_dgate else None
+        self.struct = L.make_grads(self.dx, self.dw_router, self.dw_gate_up, self.dw_down,
+                                   self.ds_gate_up, self.ds_down, self.dgate)
+
+
+def attach_backward(layer: "LayerOnDevice"):
+    """Allocate the backward workspace of a bf16 layer (once)."""
+    if getattr(layer, "bwd_workspace", None) is None:
+        n = L.moe_layer_bwd_workspace_size(layer.shape)
+        if n == 0:
+            raise L.MoEError("moe_layer_bwd_workspace_size", 2)
+        layer.bwd_workspace = torch.empty(n, dtype=torch.uint8, device=layer.device)
+    return layer
+
+
+def layer_backward(layer: "LayerOnDevice", x: torch.Tensor, saved: SavedForward, dout: torch.Tensor,
+                   grads: LayerGrads, residual: bool = False, stream=None):
+    """One moe_layer_bwd call with the state a forward wrote into `saved`."""
+    attach_backward(layer)
+    L.moe_layer_bwd(layer.shape, x, layer.w_router, layer.weights, saved.debug, dout, residual,
+                    grads.struct, layer.bwd_workspace, stream=stream)
+    return grads

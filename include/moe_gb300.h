@@ -213,6 +213,46 @@ moe_status_t moe_layer_fwd(const moe_shape_t* shape, const void* x, const float*
                            void* out, const moe_debug_t* dbg, void* workspace,
                            size_t ws_bytes, void* stream);
 
+/* Gradients written by moe_layer_bwd (device pointers, caller-owned, overwritten). */
+typedef struct {
+  void* dx;            /* [T][d] bf16: dL/dx */
+  float* dw_router;    /* [E][d] */
+  float* dw_gate_up;   /* [E][2f][d], rows interleaved as w_gate_up */
+  float* dw_down;      /* [E][d][f] */
+  float* ds_gate_up;   /* [2F][d], interleaved as shared_gate_up; NULL iff F == 0 */
+  float* ds_down;      /* [d][F]; NULL iff F == 0 */
+  float* dgate;        /* [T][k] dL/dgate of each pair, or NULL */
+} moe_grads_t;
+
+/* Backward of moe_layer_fwd (bf16 tokens and weights): gradients of a loss L given
+ * dout = dL/dout, by the chain rule through the forward the relay article states
+ * (architecture paragraph: sigmoid router, routed and shared SwiGLU experts; top-2
+ * paragraph: gates renormalised over the winners).  The article says nothing about
+ * the backward; this library's readings: the biased top-k selection is held fixed
+ * (it is piecewise constant) and the bias gets no gradient (it moves only by the
+ * balancing rule); with renormalised gates g_j = s_j / S, ds_j = (dg_j - sum_i dg_i
+ * g_i) / S, else ds_j = dg_j; dz_j = ds_j s_j (1 - s_j) for the logit; the
+ * gate/up pre-activations are recomputed from x (not stored by the forward).
+ *   x, w_router, w  as given to moe_layer_fwd (shape->x_dtype = MOE_X_BF16,
+ *                   shape->w_format = MOE_W_BF16)
+ *   saved           the forward's scores, idx, gate, offsets, perm_tok and inv_pos
+ *                   (moe_debug_t outputs of the same call; all required)
+ *   dout            [T][d] bf16
+ *   residual        1 if the forward added x to its output (dx then includes dout)
+ *   grads           outputs; fp32 weight gradients (zero for an expert without
+ *                   tokens), bf16 dx
+ *   workspace       moe_layer_bwd_workspace_size(shape) bytes of scratch.
+ * Supported: the moe_layer_fwd envelope with d, f and F multiples of 128.  Operands
+ * are bf16 with fp32 accumulation; every GEMM runs on the tensor cores, reading the
+ * weights and the permuted activations in their stored layouts (no transposed
+ * copies); the expert weight gradients are K-grouped GEMMs over each expert's
+ * tokens, padded to multiples of 64 rows in the workspace. */
+size_t moe_layer_bwd_workspace_size(const moe_shape_t* shape);
+moe_status_t moe_layer_bwd(const moe_shape_t* shape, const void* x, const float* w_router,
+                           const moe_weights_t* w, const moe_debug_t* saved, const void* dout,
+                           int32_t residual, const moe_grads_t* grads, void* workspace,
+                           size_t ws_bytes, void* stream);
+
 /* Weight preparation (off the hot path).
  * moe_pack_gate_up: for each of G matrices, interleave w_gate [G][width][d] and
  * w_up [G][width][d] (bf16) into w_gate_up [G][2*width][d] in blocks of
