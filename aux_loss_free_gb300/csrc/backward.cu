@@ -106,136 +106,137 @@ __global__ void gather_pad_kernel(const uint16_t* __restrict__ x, const uint16_t
   reinterpret_cast<uint4*>(dp + q * d)[c] = b;
 }
 
-// SwiGLU backward, one warp per row, in place.  ab: [rows][2w] pre-activations, gate
-// and up columns interleaved in blocks of `block` (as the packed weights' rows);
-// dh: [rows][w] = dout Wd (the gate not yet applied).  With g = gperm[row] (1 when
-// gperm is null), h = silu(a) * b, dh' = g * dh:
-//   ab <- (dh' * b * silu'(a), dh' * silu(a))   (same interleave),
-//   dh <- g * h   (the down projection's weight-gradient operand),
-//   dg[row] = <dh, h>   (when dg is set: the gate's gradient <dout, y>).
-// Rows at or past *rows_limit (when set) are left alone.
-__global__ void swiglu_bwd_kernel(uint16_t* __restrict__ ab, uint16_t* __restrict__ dh,
-                                  const float* __restrict__ gperm, long long rows,
-                                  const int32_t* __restrict__ rows_limit, int w, int block,
-                                  float* __restrict__ dg) {
-  const long long r = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  const int lane = threadIdx.x % 32;
-  if (r >= rows || (rows_limit && r >= *rows_limit)) return;
-  const float g = gperm ? gperm[r] : 1.0f;
-  uint16_t* abr = ab + r * 2 * w;
-  uint16_t* dhr = dh + r * w;
-  float dot = 0.f;
-  for (int j0 = 2 * lane; j0 < w; j0 += 64) {  // pairs of columns (block is even)
-    const int blk = j0 / block, within = j0 % block;
-    const long long cg = (long long)blk * 2 * block + within, cu = cg + block;
-    const __nv_bfloat162 a2 = *reinterpret_cast<const __nv_bfloat162*>(abr + cg);
-    const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(abr + cu);
-    const __nv_bfloat162 d2 = *reinterpret_cast<const __nv_bfloat162*>(dhr + j0);
-    const float a[2] = {__low2float(a2), __high2float(a2)};
-    const float b[2] = {__low2float(b2), __high2float(b2)};
-    const float dd[2] = {__low2float(d2), __high2float(d2)};
-    float da[2], db[2], hg[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const float sig = 1.0f / (1.0f + __expf(-a[i]));
-      const float sa = a[i] * sig;
-      const float h = sa * b[i];
-      dot = fmaf(dd[i], h, dot);
-      const float dhg = g * dd[i];
-      da[i] = dhg * b[i] * (sig * (1.0f + a[i] * (1.0f - sig)));
-      db[i] = dhg * sa;
-      hg[i] = g * h;
-    }
-    *reinterpret_cast<__nv_bfloat162*>(abr + cg) = __floats2bfloat162_rn(da[0], da[1]);
-    *reinterpret_cast<__nv_bfloat162*>(abr + cu) = __floats2bfloat162_rn(db[0], db[1]);
-    *reinterpret_cast<__nv_bfloat162*>(dhr + j0) = __floats2bfloat162_rn(hg[0], hg[1]);
-  }
-  if (dg) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
-    if (lane == 0) dg[r] = dot;
-  }
-}
-
-// Router backward and the input gradient, one block per token:
-//   ds_j = (dg_j - sum_i dg_i g_i) / S (renormalised gates, S = sum of the winners'
-//   scores) or dg_j (raw), dz_j = ds_j s_j (1 - s_j)  -> dzp[padded row of pair j],
-//   dx_t = sum_j dxp[padded row j] + dxs_t + sum_j dz_j W_r[e_j] (+ dout_t),
-// summed in fp32, rounded once to bf16.  dgate (optional) receives dg per pair.
+// Router backward and the input gradient, one warp per token (lane j < k holds pair j):
+//   dg_j = sum of the pair's partial <dh, h> (in order), ds_j = (dg_j - sum_i dg_i g_i)
+//   / S with S the sum of the winners' scores (renormalised gates) or dg_j (raw),
+//   dz_j = ds_j s_j (1 - s_j) -> dzp[padded row of pair j],
+//   dx_t = dxs_t + sum_j (dxp[padded row j] + dz_j W_r[e_j]) (+ dout_t),
+// summed in fp32 (16-byte loads, 8 columns a lane), rounded once to bf16.  dgate
+// (optional) receives dg per pair.
 __global__ void router_bwd_dx_kernel(const int32_t* __restrict__ idx, const float* __restrict__ gate,
                                      const float* __restrict__ scores, const int32_t* __restrict__ inv_pad,
-                                     const float* __restrict__ dgp, const float* __restrict__ w_router,
-                                     const uint16_t* __restrict__ dxp, const uint16_t* __restrict__ dxs,
-                                     const uint16_t* __restrict__ dout, int d, int E, int k, int renorm,
-                                     float* __restrict__ dzp, float* __restrict__ dgate,
-                                     uint16_t* __restrict__ dx) {
-  const int t = blockIdx.x;
-  __shared__ float s_dz[kMaxK];
-  __shared__ int s_e[kMaxK];
-  __shared__ int s_q[kMaxK];
-  if (threadIdx.x == 0) {
-    float dg[kMaxK], g[kMaxK], sc[kMaxK], S = 0.f, dgg = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int e = idx[(size_t)t * k + j];
-      const int q = inv_pad[(size_t)t * k + j];
-      s_e[j] = e;
-      s_q[j] = q;
-      dg[j] = dgp[q];
-      g[j] = gate[(size_t)t * k + j];
-      sc[j] = scores[(size_t)t * E + e];
-      S += sc[j];
-      dgg = fmaf(dg[j], g[j], dgg);
-      if (dgate) dgate[(size_t)t * k + j] = dg[j];
-    }
-    for (int j = 0; j < k; ++j) {
-      const float ds = renorm ? (dg[j] - dgg) / S : dg[j];
-      s_dz[j] = ds * sc[j] * (1.0f - sc[j]);
-      dzp[s_q[j]] = s_dz[j];
-    }
+                                     const float* __restrict__ dgp, int nparts,
+                                     const float* __restrict__ w_router, const uint16_t* __restrict__ dxp,
+                                     const uint16_t* __restrict__ dxs, const uint16_t* __restrict__ dout,
+                                     int T, int d, int E, int k, int renorm, float* __restrict__ dzp,
+                                     float* __restrict__ dgate, uint16_t* __restrict__ dx) {
+  const int lane = threadIdx.x % 32;
+  const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  if (t >= T) return;
+  float dg = 0.f, g = 0.f, sc = 0.f;
+  int e = 0, q = 0;
+  if (lane < k) {
+    e = idx[(size_t)t * k + lane];
+    q = inv_pad[(size_t)t * k + lane];
+    for (int p = 0; p < nparts; ++p) dg += dgp[(size_t)q * nparts + p];
+    g = gate[(size_t)t * k + lane];
+    sc = scores[(size_t)t * E + e];
+    if (dgate) dgate[(size_t)t * k + lane] = dg;
   }
-  __syncthreads();
-  for (int c = 2 * threadIdx.x; c < d; c += 2 * blockDim.x) {
-    float v0 = 0.f, v1 = 0.f;
-    if (dxs) {
-      const __nv_bfloat162 u = *reinterpret_cast<const __nv_bfloat162*>(dxs + (size_t)t * d + c);
-      v0 = __low2float(u);
-      v1 = __high2float(u);
-    }
+  float S = sc, dgg = dg * g;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    S += __shfl_xor_sync(0xFFFFFFFFu, S, o);
+    dgg += __shfl_xor_sync(0xFFFFFFFFu, dgg, o);
+  }
+  const float dz = (renorm ? (dg - dgg) / S : dg) * sc * (1.0f - sc);
+  if (lane < k) dzp[q] = dz;
+  for (int c = 8 * lane; c < d; c += 256) {
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    auto add8 = [&](const uint16_t* src) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(src));
+      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[2 * i] += __uint_as_float(w4[i] << 16);
+        v[2 * i + 1] += __uint_as_float(w4[i] & 0xFFFF0000u);
+      }
+    };
+    if (dxs) add8(dxs + (size_t)t * d + c);
     for (int j = 0; j < k; ++j) {
-      const __nv_bfloat162 u = *reinterpret_cast<const __nv_bfloat162*>(dxp + (size_t)s_q[j] * d + c);
-      const float2 wr = *reinterpret_cast<const float2*>(w_router + (size_t)s_e[j] * d + c);
-      v0 += __low2float(u);
-      v1 += __high2float(u);
-      v0 = fmaf(s_dz[j], wr.x, v0);
-      v1 = fmaf(s_dz[j], wr.y, v1);
+      const int qj = __shfl_sync(0xFFFFFFFFu, q, j);
+      const int ej = __shfl_sync(0xFFFFFFFFu, e, j);
+      const float zj = __shfl_sync(0xFFFFFFFFu, dz, j);
+      add8(dxp + (size_t)qj * d + c);
+      const float4 w0 = __ldg(reinterpret_cast<const float4*>(w_router + (size_t)ej * d + c));
+      const float4 w1 = __ldg(reinterpret_cast<const float4*>(w_router + (size_t)ej * d + c + 4));
+      v[0] = fmaf(zj, w0.x, v[0]);
+      v[1] = fmaf(zj, w0.y, v[1]);
+      v[2] = fmaf(zj, w0.z, v[2]);
+      v[3] = fmaf(zj, w0.w, v[3]);
+      v[4] = fmaf(zj, w1.x, v[4]);
+      v[5] = fmaf(zj, w1.y, v[5]);
+      v[6] = fmaf(zj, w1.z, v[6]);
+      v[7] = fmaf(zj, w1.w, v[7]);
     }
-    if (dout) {
-      const __nv_bfloat162 u = *reinterpret_cast<const __nv_bfloat162*>(dout + (size_t)t * d + c);
-      v0 += __low2float(u);
-      v1 += __high2float(u);
-    }
-    *reinterpret_cast<__nv_bfloat162*>(dx + (size_t)t * d + c) = __floats2bfloat162_rn(v0, v1);
+    if (dout) add8(dout + (size_t)t * d + c);
+    uint4 o;
+    o.x = __bfloat16_as_ushort(__float2bfloat16_rn(v[0])) | ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[1])) << 16);
+    o.y = __bfloat16_as_ushort(__float2bfloat16_rn(v[2])) | ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[3])) << 16);
+    o.z = __bfloat16_as_ushort(__float2bfloat16_rn(v[4])) | ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[5])) << 16);
+    o.w = __bfloat16_as_ushort(__float2bfloat16_rn(v[6])) | ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[7])) << 16);
+    *reinterpret_cast<uint4*>(dx + (size_t)t * d + c) = o;
   }
 }
 
-// dW_r[e][c] = sum over expert e's rows q of dzp[q] * xp[q][c] (padded layout; rows
-// in order, so the sum is deterministic).  Block (e, 512 columns), 2 columns a thread.
+// dW_r[e][c] = sum over expert e's rows q of dzp[q] * xp[q][c] (padded layout).
+// Block (256 columns, expert e), 8 warps: warp w takes rows w, w + 8, ... with 8
+// columns a lane (16-byte loads, four rows in flight); the warps' partial sums are
+// added in warp order through shared memory, so the result is deterministic.
 __global__ void router_wgrad_kernel(const float* __restrict__ dzp, const int32_t* __restrict__ off,
                                     const int32_t* __restrict__ poff, const uint16_t* __restrict__ xp,
                                     int d, float* __restrict__ dwr) {
+  __shared__ float part[8][256];
   const int e = blockIdx.y;
-  const int c = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
-  if (c >= d) return;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int c = blockIdx.x * 256 + 8 * lane;
   const int q0 = poff[e], n = off[e + 1] - off[e];
-  float a0 = 0.f, a1 = 0.f;
-#pragma unroll 8
-  for (int i = 0; i < n; ++i) {
-    const float z = dzp[q0 + i];
-    const __nv_bfloat162 u = *reinterpret_cast<const __nv_bfloat162*>(xp + (size_t)(q0 + i) * d + c);
-    a0 = fmaf(z, __low2float(u), a0);
-    a1 = fmaf(z, __high2float(u), a1);
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  if (c < d) {
+    int r = warp;
+    for (; r + 24 < n; r += 32) {
+      uint4 u[4];
+      float z[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        u[j] = __ldg(reinterpret_cast<const uint4*>(xp + (size_t)(q0 + r + 8 * j) * d + c));
+        z[j] = dzp[q0 + r + 8 * j];
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t w4[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] = fmaf(z[j], __uint_as_float(w4[i] << 16), acc[2 * i]);
+          acc[2 * i + 1] = fmaf(z[j], __uint_as_float(w4[i] & 0xFFFF0000u), acc[2 * i + 1]);
+        }
+      }
+    }
+    for (; r < n; r += 8) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(xp + (size_t)(q0 + r) * d + c));
+      const float z = dzp[q0 + r];
+      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = fmaf(z, __uint_as_float(w4[i] << 16), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(z, __uint_as_float(w4[i] & 0xFFFF0000u), acc[2 * i + 1]);
+      }
+    }
   }
-  *reinterpret_cast<float2*>(dwr + (size_t)e * d + c) = make_float2(a0, a1);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) part[warp][8 * lane + i] = acc[i];
+  __syncthreads();
+  const int col = blockIdx.x * 256 + threadIdx.x;
+  if (col < d) {
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) sum += part[w][threadIdx.x];
+    dwr[(size_t)e * d + col] = sum;
+  }
 }
 
 }  // namespace
@@ -258,26 +259,21 @@ cudaError_t launch_gather_pad(const uint16_t* x, const uint16_t* dout, const int
   return cudaGetLastError();
 }
 
-cudaError_t launch_swiglu_bwd(uint16_t* ab, uint16_t* dh, const float* gperm, long long rows,
-                              const int32_t* rows_limit, int w, int block, float* dg, cudaStream_t s) {
-  swiglu_bwd_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(ab, dh, gperm, rows, rows_limit, w, block, dg);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_router_bwd_dx(const int32_t* idx, const float* gate, const float* scores,
-                                 const int32_t* inv_pad, const float* dgp, const float* w_router,
+                                 const int32_t* inv_pad, const float* dgp, int nparts, const float* w_router,
                                  const uint16_t* dxp, const uint16_t* dxs, const uint16_t* dout, int T,
                                  int d, int E, int k, int renorm, float* dzp, float* dgate, uint16_t* dx,
                                  cudaStream_t s) {
-  router_bwd_dx_kernel<<<T, 128, 0, s>>>(idx, gate, scores, inv_pad, dgp, w_router, dxp, dxs, dout, d, E, k,
-                                         renorm, dzp, dgate, dx);
+  router_bwd_dx_kernel<<<(unsigned)((T + 7) / 8), 256, 0, s>>>(idx, gate, scores, inv_pad, dgp, nparts,
+                                                               w_router, dxp, dxs, dout, T, d, E, k, renorm,
+                                                               dzp, dgate, dx);
   return cudaGetLastError();
 }
 
 cudaError_t launch_router_wgrad(const float* dzp, const int32_t* off, const int32_t* poff,
                                 const uint16_t* xp, int d, int E, float* dwr, cudaStream_t s) {
-  router_wgrad_kernel<<<dim3((unsigned)((d / 2 + 255) / 256), (unsigned)E), 256, 0, s>>>(dzp, off, poff, xp,
-                                                                                       d, dwr);
+  router_wgrad_kernel<<<dim3((unsigned)((d + 255) / 256), (unsigned)E), 256, 0, s>>>(dzp, off, poff, xp, d,
+                                                                                   dwr);
   return cudaGetLastError();
 }
 

@@ -69,10 +69,15 @@ struct OperandSet {
   int kblock;
   void* out;
   int ldo, n_total, k_total, bn, mode, enabled, rows;
-  int v8;  // output rows start on 32-byte boundaries: 256-bit stores allowed
+  int v8;   // output rows start on 32-byte boundaries: 256-bit stores allowed
+  int v8h;  // the same for EPI_SWIGLU_BWD's dh rows
   // MN-major operands: the map views [K rows][M or N] as (64 elements, K rows, atoms
   // of 64 along M/N), box (64, BK, atoms per CTA), one copy per operand per k-block.
   int a_mn, b_mn;
+  // EPI_SWIGLU_BWD operands (see GemmOperandSet).
+  uint16_t* dh;
+  const float* gperm;
+  float* dgpart;
 };
 
 struct Params {
@@ -127,6 +132,15 @@ __device__ __forceinline__ void cluster_sync() {
 
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// Arrive without release semantics: for the accumulator hand-back, which orders only
+// the epilogue's TMEM reads (complete once tcgen05.wait::ld returned) before the next
+// MMAs.  A release here would hold every epilogue thread until its global stores of
+// the tile were acknowledged.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
 
@@ -298,6 +312,35 @@ __device__ __forceinline__ void add_bf16_row32(float (&o)[32], const uint16_t* s
   uint4 u[4];
   load_row32(src, u);
   accumulate_row32(o, u, w);
+}
+
+// 32 fp32 values (raw bits) -> dst: four 256-bit stores with v8, else eight 128-bit.
+__device__ __forceinline__ void store_f32_row32(float* dst, const uint32_t (&v)[32], int v8) {
+  if (v8) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 8 * i),
+                   "r"(v[8 * i]), "r"(v[8 * i + 1]), "r"(v[8 * i + 2]), "r"(v[8 * i + 3]),
+                   "r"(v[8 * i + 4]), "r"(v[8 * i + 5]), "r"(v[8 * i + 6]), "r"(v[8 * i + 7])
+                   : "memory");
+  } else {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  }
+}
+
+// 8 packed bf16 pairs (32 bytes) -> dst: one 256-bit store with v8, else two 128-bit.
+__device__ __forceinline__ void store_packed16(uint16_t* dst, const uint32_t (&p)[8], int v8) {
+  if (v8) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(p[0]),
+                 "r"(p[1]), "r"(p[2]), "r"(p[3]), "r"(p[4]), "r"(p[5]), "r"(p[6]), "r"(p[7])
+                 : "memory");
+  } else {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+    d[0] = make_uint4(p[0], p[1], p[2], p[3]);
+    d[1] = make_uint4(p[4], p[5], p[6], p[7]);
+  }
 }
 
 // 32 values -> 64 bytes of bf16.  With v8, two 256-bit stores: half the store
@@ -581,19 +624,71 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           for (int i = 0; i < 32; ++i) h[i] = silu(__uint_as_float(g[i])) * __uint_as_float(u[i]);
           if (valid) store_bf16_row32(out + orow * S.ldo + t.n0 / 2 + c, h, S.v8);
         }
-      } else if (S.mode == EPI_STORE_F32) {
-        // fp32 output (weight gradients); K groups write their own matrices.
-        float* o32 = static_cast<float*>(S.out) + (long long)t.group * p.group_stride;
-        for (int c = 32 * colh; c < S.bn; c += CS) {
-          uint32_t v[32];
-          tmem_ld32(tbase + c, v);
+      } else if (S.mode == EPI_SWIGLU_BWD) {
+        // SwiGLU backward with the pre-activations in TMEM (gate columns [0, half),
+        // up columns [half, bn) of the tile, as for EPI_SWIGLU): with dh read from
+        // memory and g the row's gate, da = g dh b silu'(a) and db = g dh silu(a) go to
+        // out (the accumulator's column order), g h replaces dh, and the partial
+        // <dh, h> of the tile's columns goes to dgpart.
+        const int half = S.bn / 2, w = S.n_total / 2;
+        const float g = (valid && S.gperm) ? S.gperm[orow] : 1.0f;
+        uint16_t* dhr = S.dh + orow * w + t.n0 / 2;
+        uint16_t* o = out + orow * S.ldo + t.n0;
+        float dot = 0.f;
+        for (int c = 16 * colh; c < half; c += 16 * EPI_GROUPS) {
+          uint32_t va[16], vb[16];
+          tmem_ld16(tbase + c, va);
+          tmem_ld16(tbase + half + c, vb);
+          uint4 u[2];
+          if (valid) {
+            u[0] = __ldcg(reinterpret_cast<const uint4*>(dhr + c));
+            u[1] = __ldcg(reinterpret_cast<const uint4*>(dhr + c) + 1);
+          }
           tmem_wait_ld();
           if (valid) {
-            float4* dst = reinterpret_cast<float4*>(o32 + orow * S.ldo + t.n0 + c);
+            uint32_t pa[8], pb[8], ph[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                   __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+            for (int i = 0; i < 8; ++i) {
+              const uint32_t dw = reinterpret_cast<const uint32_t*>(u)[i];
+              float da2[2], db2[2], h2[2];
+#pragma unroll
+              for (int hlf = 0; hlf < 2; ++hlf) {
+                const float a = __uint_as_float(va[2 * i + hlf]);
+                const float b = __uint_as_float(vb[2 * i + hlf]);
+                const float dh = __uint_as_float(hlf ? (dw & 0xFFFF0000u) : (dw << 16));
+                const float sig = __fdividef(1.0f, 1.0f + __expf(-a));
+                const float sa = a * sig;
+                const float h = sa * b;
+                dot = fmaf(dh, h, dot);
+                const float dhg = g * dh;
+                da2[hlf] = dhg * b * (sig * (1.0f + a * (1.0f - sig)));
+                db2[hlf] = dhg * sa;
+                h2[hlf] = g * h;
+              }
+              pa[i] = pack_bf16x2(da2[0], da2[1]);
+              pb[i] = pack_bf16x2(db2[0], db2[1]);
+              ph[i] = pack_bf16x2(h2[0], h2[1]);
+            }
+            store_packed16(o + c, pa, S.v8);
+            store_packed16(o + half + c, pb, S.v8);
+            store_packed16(dhr + c, ph, S.v8h);
+          }
+        }
+        if (valid && S.dgpart) S.dgpart[orow * (S.n_total / S.bn) + t.n0 / S.bn] = dot;
+      } else if (S.mode == EPI_STORE_F32) {
+        // fp32 output (weight gradients); K groups write their own matrices.  Two
+        // 32-column chunks per TMEM round trip; 256-bit stores (whole 32-byte sectors,
+        // one row per thread) when aligned.
+        float* o32 = static_cast<float*>(S.out) + (long long)t.group * p.group_stride + orow * S.ldo + t.n0;
+        for (int c = 32 * colh; c < S.bn; c += 2 * CS) {
+          const bool two = c + CS < S.bn;  // warp-uniform
+          uint32_t v[32], w[32];
+          tmem_ld32(tbase + c, v);
+          if (two) tmem_ld32(tbase + c + CS, w);
+          tmem_wait_ld();
+          if (valid) {
+            store_f32_row32(o32 + c, v, S.v8);
+            if (two) store_f32_row32(o32 + c + CS, w, S.v8);
           }
         }
       } else if (S.mode == EPI_STORE) {
@@ -655,7 +750,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
+      if (lane == 0) mbar_arrive_cluster_relaxed(acc ? tempty_leader1 : tempty_leader0);
 
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
@@ -723,6 +818,7 @@ int gate_up_block(int width) { return width % 128 == 0 ? 128 : (width % 64 == 0 
 int choose_bn(int mode, int N) {
   if (mode == EPI_SWIGLU) return 2 * gate_up_block(N / 2);
   if (mode == EPI_STORE_F32) return N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : (N % 64 == 0 ? 64 : 32));
+  if (mode == EPI_SWIGLU_BWD) return 2 * gate_up_block(N / 2);
   return N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : 64);
 }
 
@@ -757,7 +853,14 @@ bool fill_set(OperandSet& t, const GemmOperandSet& o) {
   t.mode = o.mode;
   t.rows = o.rows;
   t.out = o.out;
-  t.v8 = (reinterpret_cast<uintptr_t>(o.out) % 32 == 0) && ((long long)o.ldo * 2) % 32 == 0;
+  t.dh = o.dh;
+  t.gperm = o.gperm;
+  t.dgpart = o.dgpart;
+  // 256-bit stores of the h-width rows (EPI_SWIGLU_BWD's dh) need 32-byte alignment too.
+  t.v8h = (reinterpret_cast<uintptr_t>(o.dh) % 32 == 0) && ((long long)o.N / 2 * 2) % 32 == 0;
+  if (o.mode == EPI_SWIGLU_BWD && !o.dh) return false;
+  const int esize = o.mode == EPI_STORE_F32 ? 4 : 2;
+  t.v8 = (reinterpret_cast<uintptr_t>(o.out) % 32 == 0) && ((long long)o.ldo * esize) % 32 == 0;
   if (o.N % t.bn != 0) return false;
   t.a_mn = o.a_mn ? 1 : 0;
   t.b_mn = o.b_mn ? 1 : 0;
@@ -784,6 +887,8 @@ bool fill_set(OperandSet& t, const GemmOperandSet& o) {
 }
 
 }  // namespace
+
+int gemm_tile_n(int mode, int N) { return choose_bn(mode, N); }
 
 bool make_tma_map_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
                        uint32_t box_outer) {
@@ -818,6 +923,7 @@ cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* off
   p.k = comb.k;
   p.kgroup = kgroup_stride > 0 ? 1 : 0;
   p.group_stride = kgroup_stride;
+  if (p.kgroup && kgroup_stride % 8 != 0) p.routed.v8 = 0;  // groups' fp32 outputs off 32 B
   p.status = device_status_ptr();
   if (!p.status) return cudaErrorInvalidDevicePointer;
 

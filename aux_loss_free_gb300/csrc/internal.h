@@ -98,7 +98,7 @@ cudaError_t launch_pack_gate_up(int G, int width, int d, int block, const uint16
                                 const uint16_t* wu, uint16_t* wgu, cudaStream_t s);
 
 // ---------------------------------------------------------------- grouped GEMM
-enum EpiMode { EPI_SWIGLU = 0, EPI_STORE = 1, EPI_COMBINE = 2, EPI_STORE_F32 = 3 };
+enum EpiMode { EPI_SWIGLU = 0, EPI_STORE = 1, EPI_COMBINE = 2, EPI_STORE_F32 = 3, EPI_SWIGLU_BWD = 4 };
 
 struct GemmOperandSet {
   const void* a;        // bf16 [a_rows][K]
@@ -117,7 +117,17 @@ struct GemmOperandSet {
   // A takes its M extent from `rows` and its K extent from K.
   int a_mn;
   int b_mn;
+  // EPI_SWIGLU_BWD: the accumulator holds the gate/up pre-activations (a, b),
+  // interleaved as for EPI_SWIGLU; dh [rows][N / 2] holds dL/dh on entry and receives
+  // gate * h; out [rows][N] receives (da, db) in the accumulator's column order;
+  // dgpart [rows][N / bn] (nullable) the per-tile partial sums of <dh, h>; gperm
+  // [rows] (nullable = 1) is each row's gate.
+  uint16_t* dh;
+  const float* gperm;
+  float* dgpart;
 };
+// Column tile width the grouped GEMM uses for an operand set of this mode and N.
+int gemm_tile_n(int mode, int N);
 struct CombineInputs {
   const uint16_t* y_perm;
   const int32_t* inv_pos;
@@ -179,10 +189,9 @@ cudaError_t launch_pad_map(const int32_t* off, const int32_t* perm_tok, const in
 cudaError_t launch_gather_pad(const uint16_t* x, const uint16_t* dout, const int32_t* tok_pad,
                               long long q_max, const int32_t* rows_limit, int d, uint16_t* xp,
                               uint16_t* dp, cudaStream_t s);
-cudaError_t launch_swiglu_bwd(uint16_t* ab, uint16_t* dh, const float* gperm, long long rows,
-                              const int32_t* rows_limit, int w, int block, float* dg, cudaStream_t s);
+// dgp: [Q][nparts] partial sums of dL/dgate per padded row (summed in order).
 cudaError_t launch_router_bwd_dx(const int32_t* idx, const float* gate, const float* scores,
-                                 const int32_t* inv_pad, const float* dgp, const float* w_router,
+                                 const int32_t* inv_pad, const float* dgp, int nparts, const float* w_router,
                                  const uint16_t* dxp, const uint16_t* dxs, const uint16_t* dout, int T,
                                  int d, int E, int k, int renorm, float* dzp, float* dgate, uint16_t* dx,
                                  cudaStream_t s);

@@ -651,16 +651,19 @@ moe_status_t check_bwd_shape(const moe_shape_t* s) {
 // Rows of the padded permuted layout: every pair plus up to 63 padding rows per expert.
 long long bwd_rows(const moe_shape_t* s) { return (long long)s->T * s->k + 63LL * s->E; }
 
+// Column tiles of the routed dgrad-through-down GEMM: partial sums of dL/dgate per row.
+int bwd_parts(const moe_shape_t* s) { return 2 * s->f / gemm_tile_n(EPI_SWIGLU_BWD, 2 * s->f); }
+
 struct BwdWs {
   int32_t* poff;     // [E+1] padded expert offsets
   int32_t* tok_pad;  // [Q] source token of each padded row (-1 = padding)
   int32_t* inv_pad;  // [T*k] padded row of each pair
   float* gperm;      // [Q] gate of each padded row
-  float* dgp;        // [Q] dL/dgate of each padded row
+  float* dgp;        // [Q][f / tile width] partial dL/dgate of each padded row
   float* dzp;        // [Q] dL/dlogit of each padded row
   uint16_t* xp;      // [Q][d] gathered tokens
   uint16_t* dp;      // [Q][d] gathered output gradients
-  uint16_t* ab;      // [Q][2f] gate/up pre-activations, then their gradients
+  uint16_t* ab;      // [Q][2f] gradients of the gate/up pre-activations
   uint16_t* dh;      // [Q][f] dout Wd, then gate * h
   uint16_t* dxp;     // [Q][d] routed input gradient of each row
   uint16_t* abs;     // [T][2F] shared expert: as ab
@@ -674,7 +677,7 @@ BwdWs carve_bwd(Carver& c, const moe_shape_t* s) {
   w.tok_pad = static_cast<int32_t*>(c.take(4 * Q));
   w.inv_pad = static_cast<int32_t*>(c.take(4 * Tk));
   w.gperm = static_cast<float*>(c.take(4 * Q));
-  w.dgp = static_cast<float*>(c.take(4 * Q));
+  w.dgp = static_cast<float*>(c.take(4 * Q * bwd_parts(s)));
   w.dzp = static_cast<float*>(c.take(4 * Q));
   w.xp = static_cast<uint16_t*>(c.take(2 * Q * s->d));
   w.dp = static_cast<uint16_t*>(c.take(2 * Q * s->d));
@@ -741,25 +744,25 @@ moe_status_t moe_layer_bwd(const moe_shape_t* shape, const void* x, const float*
   if (e == cudaSuccess) e = launch_gather_pad(xb, db, b.tok_pad, Q, b.poff + E, d, b.xp, b.dp, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
-  // (1) Gate/up pre-activations, recomputed: ab = xp Wgu_e^T, abs = x Sgu^T.
+  // (1) dh = dout Wd_e (B = the stored [d][f] weights, MN-major), dhs = dout Sd.
   {
-    GemmOperandSet r{b.xp, Q, w->w_gate_up, E, 2 * f, d, b.ab, 2 * f, EPI_STORE, 0};
-    GemmOperandSet sh{};
-    if (has_shared) sh = GemmOperandSet{x, T, w->shared_gate_up, 1, 2 * F, d, b.abs, 2 * F, EPI_STORE, T};
-    e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad);
-  }
-  // (2) dh = dout Wd_e (B = the stored [d][f] weights, MN-major), dhs = dout Sd.
-  if (e == cudaSuccess) {
     GemmOperandSet r{b.dp, Q, w->w_down, E, f, d, b.dh, f, EPI_STORE, 0, 0, 1};
     GemmOperandSet sh{};
     if (has_shared) sh = GemmOperandSet{dout, T, w->shared_down, 1, F, d, b.dhs, F, EPI_STORE, T, 0, 1};
     e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad);
   }
-  // (3) SwiGLU backward in place: ab <- (da, db), dh <- gate * h, dgp = <dout, y>.
-  if (e == cudaSuccess)
-    e = launch_swiglu_bwd(b.ab, b.dh, b.gperm, Q, b.poff + E, f, moe_gate_up_block(f), b.dgp, s);
-  if (e == cudaSuccess && has_shared)
-    e = launch_swiglu_bwd(b.abs, b.dhs, nullptr, T, nullptr, F, moe_gate_up_block(F), nullptr, s);
+  // (2-3) Gate/up pre-activations recomputed on the tensor cores (xp Wgu_e^T, x Sgu^T)
+  // with the SwiGLU backward in the epilogue: ab <- (da, db), dh <- gate * h,
+  // dgp <- partial <dh, h> (= <dout, y>) per column tile.
+  if (e == cudaSuccess) {
+    GemmOperandSet r{b.xp, Q, w->w_gate_up, E, 2 * f, d, b.ab, 2 * f, EPI_SWIGLU_BWD, 0, 0, 0,
+                     b.dh, b.gperm, b.dgp};
+    GemmOperandSet sh{};
+    if (has_shared)
+      sh = GemmOperandSet{x, T, w->shared_gate_up, 1, 2 * F, d, b.abs, 2 * F, EPI_SWIGLU_BWD, T, 0, 0,
+                          b.dhs, nullptr, nullptr};
+    e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad);
+  }
   // (4) dxp = (da, db) Wgu_e (B = the stored [2f][d] weights, MN-major), dxs likewise.
   if (e == cudaSuccess) {
     GemmOperandSet r{b.ab, Q, w->w_gate_up, E, d, 2 * f, b.dxp, d, EPI_STORE, 0, 0, 1};
@@ -769,7 +772,8 @@ moe_status_t moe_layer_bwd(const moe_shape_t* shape, const void* x, const float*
   }
   // (5) Router backward and dx = sum of the pairs' rows + shared + router (+ dout).
   if (e == cudaSuccess)
-    e = launch_router_bwd_dx(saved->idx, saved->gate, saved->scores, b.inv_pad, b.dgp, w_router, b.dxp,
+    e = launch_router_bwd_dx(saved->idx, saved->gate, saved->scores, b.inv_pad, b.dgp, bwd_parts(shape),
+                             w_router, b.dxp,
                              has_shared ? b.dxs : nullptr, residual ? db : nullptr, T, d, E, k,
                              shape->renorm, b.dzp, g->dgate, static_cast<uint16_t*>(g->dx), s);
   // (6) dWd_e = dp^T (gate * h) over the expert's rows (K-grouped), dSd = dout^T hs.
