@@ -75,6 +75,7 @@ SIGNATURES = {
     "moe_device_status": (_I32, [_P, ctypes.POINTER(_I32)]),
     "moe_profile_stage_count": (_I32, []),
     "moe_profile_stage_name": (ctypes.c_char_p, [_I32]),
+    "moe_profile_stage_calls": (_I32, [_I32]),
     "moe_profile_start": (_I32, [_I32, _I32]),
     "moe_profile_stop": (_I32, [ctypes.POINTER(_F), ctypes.POINTER(_I32)]),
 }
@@ -246,12 +247,16 @@ def moe_profile_start(max_calls: int, period: int = 1):
     _check("moe_profile_start", load_library().moe_profile_start(max_calls, period))
 
 
-def moe_profile_stop():
-    """-> ({stage name: summed ms}, recorded calls)."""
+def moe_profile_stop(per_stage_calls: bool = False):
+    """-> ({stage name: summed ms}, recorded calls); with per_stage_calls, the second
+    item is {stage name: recorded calls that had the stage}."""
     lib = load_library()
     n = lib.moe_profile_stage_count()
     ms = (_F * n)()
     calls = _I32(0)
     _check("moe_profile_stop", lib.moe_profile_stop(ms, ctypes.byref(calls)))
     names = [lib.moe_profile_stage_name(i).decode() for i in range(n)]
-    return {nm: float(v) for nm, v in zip(names, ms) if nm}, calls.value
+    sums = {nm: float(v) for nm, v in zip(names, ms) if nm}
+    if per_stage_calls:
+        return sums, {nm: int(lib.moe_profile_stage_calls(i)) for i, nm in enumerate(names) if nm}
+    return sums, calls.value

@@ -59,16 +59,20 @@ struct Carver {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // ---------------------------------------------------------------- stage profiler
-// A recorded call places up to kStages + 1 named marks; stage i lasts from mark i to
-// mark i + 1 and carries mark i's name.  Names are static strings.
-constexpr int kStages = 6;
+// A recorded call places up to kMarks named marks; stage i lasts from mark i to mark
+// i + 1 and carries mark i's name (names are static strings).  Stages are summed by
+// name over the recorded calls, forward and backward calls alike.
+constexpr int kMarks = 10;
+constexpr int kMaxNames = 16;
 struct Profiler {
   std::mutex mu;
   bool on = false;
   int max_calls = 0, calls = 0, period = 1, nmarks = 0;
   long long seen = 0;
-  std::vector<cudaEvent_t> ev;           // (kStages + 1) per recorded call
-  const char* names[kStages + 1] = {};   // of the first recorded call
+  std::vector<cudaEvent_t> ev;           // kMarks per recorded call
+  std::vector<const char*> call_names;   // kMarks per recorded call (null = unused)
+  const char* names[kMaxNames] = {};     // distinct stage names, first-seen order
+  int name_calls[kMaxNames] = {};        // recorded calls that had the stage
 } g_prof;
 
 // Whether the call now starting is recorded (every `period`-th call while enabled).
@@ -82,13 +86,18 @@ bool prof_begin_call() {
 // Next mark of a recorded call; name == nullptr ends the call.
 void prof_mark(const char* name, cudaStream_t s) {
   std::lock_guard<std::mutex> lock(g_prof.mu);
-  if (!g_prof.on || g_prof.calls >= g_prof.max_calls || g_prof.nmarks > kStages) return;
-  cudaEventRecord(g_prof.ev[(size_t)g_prof.calls * (kStages + 1) + g_prof.nmarks], s);
-  if (g_prof.calls == 0) g_prof.names[g_prof.nmarks] = name;
-  ++g_prof.nmarks;
+  if (!g_prof.on || g_prof.calls >= g_prof.max_calls) return;
+  const size_t base = (size_t)g_prof.calls * kMarks;
+  if (g_prof.nmarks < kMarks - 1 || (!name && g_prof.nmarks < kMarks)) {
+    cudaEventRecord(g_prof.ev[base + g_prof.nmarks], s);
+    g_prof.call_names[base + g_prof.nmarks] = name;
+    ++g_prof.nmarks;
+  }
   if (!name) {
-    for (int i = g_prof.nmarks; i <= kStages; ++i)  // unused slots repeat the end mark
-      cudaEventRecord(g_prof.ev[(size_t)g_prof.calls * (kStages + 1) + i], s);
+    for (int i = g_prof.nmarks; i < kMarks; ++i) {  // unused slots repeat the end mark
+      cudaEventRecord(g_prof.ev[base + i], s);
+      g_prof.call_names[base + i] = nullptr;
+    }
     ++g_prof.calls;
   }
 }
@@ -737,13 +746,19 @@ moe_status_t moe_layer_bwd(const moe_shape_t* shape, const void* x, const float*
   int bad = 0;
   CombineInputs none{};
   cudaError_t e;
+  const bool prof = prof_begin_call();
+  if (prof) prof_mark("bwd_pad_gather", s);
 
   // Padded permuted layout, then the gathered tokens and output gradients.
   e = launch_pad_map(saved->offsets, saved->perm_tok, saved->idx, saved->inv_pos, saved->gate, E, P, Q,
                      b.poff, b.tok_pad, b.inv_pad, b.gperm, s);
   if (e == cudaSuccess) e = launch_gather_pad(xb, db, b.tok_pad, Q, b.poff + E, d, b.xp, b.dp, s);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (e != cudaSuccess) {
+    if (prof) prof_mark(nullptr, s);
+    return MOE_ERR_CUDA;
+  }
 
+  if (prof) prof_mark("bwd_dgrad_down", s);
   // (1) dh = dout Wd_e (B = the stored [d][f] weights, MN-major), dhs = dout Sd.
   {
     GemmOperandSet r{b.dp, Q, w->w_down, E, f, d, b.dh, f, EPI_STORE, 0, 0, 1};
@@ -751,6 +766,7 @@ moe_status_t moe_layer_bwd(const moe_shape_t* shape, const void* x, const float*
     if (has_shared) sh = GemmOperandSet{dout, T, w->shared_down, 1, F, d, b.dhs, F, EPI_STORE, T, 0, 1};
     e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad);
   }
+  if (prof && e == cudaSuccess) prof_mark("bwd_recompute_swiglu", s);
   // (2-3) Gate/up pre-activations recomputed on the tensor cores (xp Wgu_e^T, x Sgu^T)
   // with the SwiGLU backward in the epilogue: ab <- (da, db), dh <- gate * h,
   // dgp <- partial <dh, h> (= <dout, y>) per column tile.
@@ -763,6 +779,7 @@ moe_status_t moe_layer_bwd(const moe_shape_t* shape, const void* x, const float*
                           b.dhs, nullptr, nullptr};
     e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad);
   }
+  if (prof && e == cudaSuccess) prof_mark("bwd_dgrad_gate_up", s);
   // (4) dxp = (da, db) Wgu_e (B = the stored [2f][d] weights, MN-major), dxs likewise.
   if (e == cudaSuccess) {
     GemmOperandSet r{b.ab, Q, w->w_gate_up, E, d, 2 * f, b.dxp, d, EPI_STORE, 0, 0, 1};
@@ -770,12 +787,14 @@ moe_status_t moe_layer_bwd(const moe_shape_t* shape, const void* x, const float*
     if (has_shared) sh = GemmOperandSet{b.abs, T, w->shared_gate_up, 1, d, 2 * F, b.dxs, d, EPI_STORE, T, 0, 1};
     e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad);
   }
+  if (prof && e == cudaSuccess) prof_mark("bwd_router_dx", s);
   // (5) Router backward and dx = sum of the pairs' rows + shared + router (+ dout).
   if (e == cudaSuccess)
     e = launch_router_bwd_dx(saved->idx, saved->gate, saved->scores, b.inv_pad, b.dgp, bwd_parts(shape),
                              w_router, b.dxp,
                              has_shared ? b.dxs : nullptr, residual ? db : nullptr, T, d, E, k,
                              shape->renorm, b.dzp, g->dgate, static_cast<uint16_t*>(g->dx), s);
+  if (prof && e == cudaSuccess) prof_mark("bwd_wgrad_down", s);
   // (6) dWd_e = dp^T (gate * h) over the expert's rows (K-grouped), dSd = dout^T hs.
   if (e == cudaSuccess) {
     GemmOperandSet r{b.dp, Q, b.dh, 1, f, (int)Q, g->dw_down, f, EPI_STORE_F32, d, 1, 1};
@@ -783,6 +802,7 @@ moe_status_t moe_layer_bwd(const moe_shape_t* shape, const void* x, const float*
     if (has_shared) sh = GemmOperandSet{dout, T, b.dhs, 1, F, T, g->ds_down, F, EPI_STORE_F32, d, 1, 1};
     e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad, 0, (long long)d * f);
   }
+  if (prof && e == cudaSuccess) prof_mark("bwd_wgrad_gate_up", s);
   // (7) dWgu_e = (da, db)^T xp (rows interleaved as w_gate_up), dSgu = (das, dbs)^T x.
   if (e == cudaSuccess) {
     GemmOperandSet r{b.ab, Q, b.xp, 1, d, (int)Q, g->dw_gate_up, d, EPI_STORE_F32, 2 * f, 1, 1};
@@ -790,8 +810,10 @@ moe_status_t moe_layer_bwd(const moe_shape_t* shape, const void* x, const float*
     if (has_shared) sh = GemmOperandSet{b.abs, T, x, 1, d, T, g->ds_gate_up, d, EPI_STORE_F32, 2 * F, 1, 1};
     e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad, 0, (long long)2 * f * d);
   }
+  if (prof && e == cudaSuccess) prof_mark("bwd_router_wgrad", s);
   // (8) dW_r[e] = sum over the expert's rows of dz * x.
   if (e == cudaSuccess) e = launch_router_wgrad(b.dzp, saved->offsets, b.poff, b.xp, d, E, g->dw_router, s);
+  if (prof) prof_mark(nullptr, s);
   if (bad) return MOE_ERR_UNSUPPORTED;
   return cuda_status(e);
 }
@@ -821,22 +843,29 @@ moe_status_t moe_quantize_int4(int64_t rows, int32_t K, const void* w, void* q, 
                                           static_cast<cudaStream_t>(stream)));
 }
 
-int32_t moe_profile_stage_count(void) { return kStages; }
+int32_t moe_profile_stage_count(void) { return kMaxNames; }
 
 const char* moe_profile_stage_name(int32_t stage) {
-  if (stage < 0 || stage >= kStages) return "";
+  if (stage < 0 || stage >= kMaxNames) return "";
   const char* n = g_prof.names[stage];
   return n ? n : "";
+}
+
+int32_t moe_profile_stage_calls(int32_t stage) {
+  if (stage < 0 || stage >= kMaxNames) return 0;
+  return g_prof.name_calls[stage];
 }
 
 moe_status_t moe_profile_start(int32_t max_calls, int32_t period) {
   if (max_calls < 1 || max_calls > (1 << 20) || period < 1) return MOE_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_prof.mu);
   for (cudaEvent_t ev : g_prof.ev) cudaEventDestroy(ev);
-  g_prof.ev.assign((size_t)max_calls * (kStages + 1), nullptr);
+  g_prof.ev.assign((size_t)max_calls * kMarks, nullptr);
+  g_prof.call_names.assign((size_t)max_calls * kMarks, nullptr);
   for (auto& ev : g_prof.ev)
     if (cudaEventCreate(&ev) != cudaSuccess) return MOE_ERR_CUDA;
   for (auto& n : g_prof.names) n = nullptr;
+  for (auto& c : g_prof.name_calls) c = 0;
   g_prof.max_calls = max_calls;
   g_prof.calls = 0;
   g_prof.period = period;
@@ -849,14 +878,21 @@ moe_status_t moe_profile_stop(float* ms_per_stage, int32_t* calls) {
   if (!ms_per_stage || !calls) return MOE_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_prof.mu);
   g_prof.on = false;
-  for (int i = 0; i < kStages; ++i) ms_per_stage[i] = 0.f;
+  for (int i = 0; i < kMaxNames; ++i) ms_per_stage[i] = 0.f;
   *calls = g_prof.calls;
   for (int c = 0; c < g_prof.calls; ++c) {
-    cudaEvent_t* ev = &g_prof.ev[(size_t)c * (kStages + 1)];
-    if (cudaEventSynchronize(ev[kStages]) != cudaSuccess) return MOE_ERR_CUDA;
-    for (int i = 0; i < kStages; ++i) {
+    cudaEvent_t* ev = &g_prof.ev[(size_t)c * kMarks];
+    const char* const* nm = &g_prof.call_names[(size_t)c * kMarks];
+    if (cudaEventSynchronize(ev[kMarks - 1]) != cudaSuccess) return MOE_ERR_CUDA;
+    for (int i = 0; i + 1 < kMarks; ++i) {
+      if (!nm[i]) break;
+      int slot = 0;
+      while (slot < kMaxNames && g_prof.names[slot] && g_prof.names[slot] != nm[i]) ++slot;
+      if (slot == kMaxNames) continue;  // more distinct stages than slots: not reported
+      if (!g_prof.names[slot]) g_prof.names[slot] = nm[i];
+      ++g_prof.name_calls[slot];
       float ms = 0.f;
-      if (cudaEventElapsedTime(&ms, ev[i], ev[i + 1]) == cudaSuccess) ms_per_stage[i] += ms;
+      if (cudaEventElapsedTime(&ms, ev[i], ev[i + 1]) == cudaSuccess) ms_per_stage[slot] += ms;
     }
   }
   return MOE_OK;

@@ -11,8 +11,13 @@ Timing: W untimed warm-up steps, then K timed steps with a 512 MiB write between
 steps (L2 is 129 MB, so every step starts cold), each step bracketed by CUDA events
 on the launching stream; barrier + synchronize on both sides; max over ranks.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload nano|skew|stack|tiny]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload nano|skew|stack|tiny|train|...]
   python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+The `train` workload times a training step of the same layer instead: the forward
+(saving its routing state) with the bias update, then moe_layer_bwd for a seeded
+output gradient (dx and fp32 weight gradients of the router, routed and shared
+experts).
 
 Prints one JSON line.  Under torchrun (N > 1) every rank runs its own replica on its
 own tokens (weak scaling); the only cross-rank exchange of the method is the sum of
@@ -35,7 +40,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from synth import CONFIGS, f32_from_bf16_bits, make_layer, make_tokens  # noqa: E402
+from synth import CONFIGS, f32_from_bf16_bits, make_layer, make_output_grad, make_tokens  # noqa: E402
 
 METRIC = "MoE-layer fwd tokens/s (T=8192,d=1024,64x512 top-2+2048 shared), % roofline"
 FLUSH_BYTES = 512 << 20
@@ -59,6 +64,41 @@ def kernels_per_call(s):
     # permute, gate/up (one or two launches), down, combine
     fork = s.x_dtype == "bf16" and s.F > 0 and s.T >= 1024
     return router + 1 + (2 if fork else 1) + 1 + 1
+
+
+# Kernels one moe_layer_bwd launches: padded layout, gather, five grouped GEMMs
+# (dgrad down; gate/up recompute with the SwiGLU backward; dgrad gate/up; two weight
+# gradients), router backward + dx, router weight gradient.
+KERNELS_PER_BWD = 9
+
+
+def train_algorithmic(s):
+    """FLOPs and bytes of one training step of the layer: the forward's, plus the
+    backward's input and weight gradients (twice the expert GEMM FLOPs, and the
+    router's two products over the winners); bytes add the weights read again, the
+    fp32 weight gradients written, dout and x read, dx written."""
+    f_fwd, b_fwd = layer_algorithmic(s)
+    expert_flops = 2 * 3 * s.d * s.f * s.T * s.k + 2 * 3 * s.d * s.F * s.T
+    f_bwd = 2 * expert_flops + 2 * 2 * s.T * s.k * s.d
+    hit = min(s.E, s.T * s.k)
+    w_bytes = hit * 3 * s.d * s.f * 2 + 3 * s.d * s.F * 2 + s.E * s.d * 4
+    g_bytes = (hit * 3 * s.d * s.f + 3 * s.d * s.F + s.E * s.d) * 4
+    b_bwd = w_bytes + g_bytes + 3 * s.T * s.d * 2
+    return f_fwd + f_bwd, b_fwd + b_bwd
+
+
+def bwd_stage_work(s, stage):
+    """(FLOPs, HBM bytes that must move) of one backward GEMM stage, algorithmic."""
+    P, T, d, f, F = s.T * s.k, s.T, s.d, s.f, s.F
+    hit = min(s.E, P)
+    table = {
+        "bwd_dgrad_down": (2 * P * d * f + 2 * T * d * F, (hit * d * f + d * F) * 2),
+        "bwd_recompute_swiglu": (2 * P * d * 2 * f + 2 * T * d * 2 * F, (hit * 2 * f * d + 2 * F * d) * 2),
+        "bwd_dgrad_gate_up": (2 * P * 2 * f * d + 2 * T * 2 * F * d, (hit * 2 * f * d + 2 * F * d) * 2),
+        "bwd_wgrad_down": (2 * P * d * f + 2 * T * d * F, (hit * d * f + d * F) * 4),
+        "bwd_wgrad_gate_up": (2 * P * 2 * f * d + 2 * T * 2 * F * d, (hit * 2 * f * d + 2 * F * d) * 4),
+    }
+    return table.get(stage)
 
 
 def parse_args():
@@ -85,6 +125,9 @@ WORKLOADS = {
     "stack": ("stack", CONFIGS["stack"], "stack_23_moe_layers_T8192",
               "23-layer MoE stack fwd tokens/s per stack forward, % roofline"),
     "tiny": ("tiny", CONFIGS["tiny"], "tiny_moe_layer_fwd_T64", "tiny MoE-layer fwd tokens/s"),
+    "train": ("nano", CONFIGS["nano"], "nano_moe_layer_fwd_bwd_T8192",
+              "MoE-layer training step (fwd + bias update + bwd) tokens/s (T=8192,d=1024,64x512 top-2+2048 "
+              "shared), % roofline"),
     "decode1": ("decode", CONFIGS["decode"].replace(T=1), "top1_int4_decode_T1",
                 "Top-1 int4 serving decode tokens/s (T=1), % HBM roofline"),
     "decode8": ("decode", CONFIGS["decode"].replace(T=8), "top1_int4_decode_T8",
@@ -232,12 +275,18 @@ def oracle_sample_runner(name, seed):
     x = host["x"]
     xv = bf(x) if x.dtype == np.uint16 else x.astype(np.float64)
 
+    dout = bf(make_output_grad(s, WORKLOADS[name][0], seed)) if name == "train" else None
+
     def run(ntok):
         t0 = time.perf_counter()
         O.layer_forward(xv[:ntok], host["w_router"], host["bias"], W["w_gate"], W["w_up"],
                         W["w_down"], W["s_gate"], W["s_up"], W["s_down"], k=s.k, renorm=s.renorm,
                         logit_offset=host["logit_offset"], gamma=host["gamma"],
                         x_is_bf16=x.dtype == np.uint16)
+        if dout is not None:
+            O.layer_backward(xv[:ntok], host["w_router"], host["bias"], W["w_gate"], W["w_up"],
+                             W["w_down"], W["s_gate"], W["s_up"], W["s_down"], dout[:ntok], s.k,
+                             renorm=s.renorm, logit_offset=host["logit_offset"])
         return time.perf_counter() - t0
     return run
 
@@ -252,7 +301,7 @@ def cpu_cores():
 def cpu_baseline(name, seed, seconds):
     run = oracle_sample_runner(name, seed)
     s = workload_shape(name)
-    ntok = min(s.T, 1024)
+    ntok = min(s.T, 128 if name == "train" else 1024)
     run(min(ntok, 64))  # warm the BLAS threads
     done, spent = 0, 0.0
     while spent < seconds and done < 64 * s.T:
@@ -260,7 +309,8 @@ def cpu_baseline(name, seed, seconds):
         done += ntok
     return {"value": done / spent * (1.0 / max(1, s.layers)), "unit": "tokens/s", "cores": cpu_cores(),
             "kind": "oracle",
-            "sample": f"{done} tokens as {done // ntok} oracle layer forwards of {ntok} tokens of the "
+            "sample": f"{done} tokens as {done // ntok} oracle layer "
+                      f"{'forward+backward passes' if name == 'train' else 'forwards'} of {ntok} tokens of the "
                       f"{name} workload (fp64 numpy, BLAS on all {cpu_cores()} visible cores), "
                       f"{spent:.1f} s" + (f"; per stack forward of {s.layers} layers" if s.layers > 1 else "")}
 
@@ -287,7 +337,9 @@ def reference_arm(args, rank, world):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_block(args.workload, world),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "kind": "oracle", "cores": cpu_cores(),
-                             "sample": f"each step: oracle layer forward of {ntok} of the {s.T} tokens"},
+                             "sample": f"each step: oracle layer "
+                                       f"{'forward+backward' if args.workload == 'train' else 'forward'}"
+                                       f" of {ntok} of the {s.T} tokens"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -502,6 +554,149 @@ def gpu_arm(args, rank, world, dist):
     print(json.dumps(line), flush=True)
 
 
+def gpu_train_arm(args, rank, world, dist):
+    """Training step of the Nano layer: forward (routing state saved) with the bias
+    update, then the backward for a seeded output gradient."""
+    import torch
+
+    import aux_loss_free_gb300 as M
+    from aux_loss_free_gb300.dp import dp_bias_update
+    from aux_loss_free_gb300.layer import (LayerGrads, LayerOnDevice, SavedForward, attach_backward,
+                                           layer_backward, to_device_bf16, to_device_tokens)
+
+    M.load_library()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    name = args.workload
+    s = workload_shape(name)
+    case = WORKLOADS[name][0]
+    layer = attach_backward(LayerOnDevice(s, make_layer(s, case, args.seed, with_tokens=False), dev))
+    x0 = to_device_tokens(make_tokens(s, case, args.seed + rank), dev)
+    g0 = to_device_bf16(make_output_grad(s, case, args.seed + rank), dev)
+    saved = SavedForward(s.T, s.E, s.k, dev)
+    grads = LayerGrads(layer)
+    out0 = torch.empty(s.T, s.d, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(x_in, dout, out):
+        if world > 1:
+            layer.forward(x_in, out, update_bias=False, debug=saved.debug)
+            dp_bias_update(saved.load, layer.bias, s.T * s.k, layer.gamma)
+        else:
+            layer.forward(x_in, out, update_bias=True, debug=saved.debug)
+        layer_backward(layer, x_in, saved, dout, grads)
+
+    for _ in range(args.warmup):
+        step(x0, g0, out0)
+    torch.cuda.synchronize(dev)
+    if M.moe_device_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    time.sleep(0.1)
+    K = args.steps
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    # An odd sampling period alternates the recorded calls between forward and backward.
+    period = PROFILE_PERIOD + 1
+    M.moe_profile_start(2 * K // period + 2, period)
+    t_wall0 = time.time()
+    for i in range(K):
+        flush.zero_()
+        ev0[i].record(stream)
+        step(x0, g0, out0)
+        ev1[i].record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    if dist:
+        dist.barrier()
+    stages_ms, stage_calls = M.moe_profile_stop(per_stage_calls=True)
+    time.sleep(0.05)
+    sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    total_ms = sum(step_ms)
+    if dist:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    status = M.moe_device_status()
+
+    # End to end: x and dout in from pinned host memory, dx back, every step inside
+    # the timed region (the weight gradients stay on the device for the optimizer).
+    Ke = max(3, min(K, 50))
+    hx = torch.empty(s.T, s.d, dtype=x0.dtype, pin_memory=True)
+    hx.copy_(x0.cpu())
+    hg = torch.empty(s.T, s.d, dtype=torch.bfloat16, pin_memory=True)
+    hg.copy_(g0.cpu())
+    hdx = torch.empty(s.T, s.d, dtype=torch.bfloat16, pin_memory=True)
+    dx_, dg_ = torch.empty_like(x0), torch.empty_like(g0)
+    torch.cuda.synchronize(dev)
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for _ in range(Ke):
+        dx_.copy_(hx, non_blocking=True)
+        dg_.copy_(hg, non_blocking=True)
+        step(dx_, dg_, out0)
+        hdx.copy_(grads.dx, non_blocking=True)
+    e_end.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e_start.elapsed_time(e_end) / Ke
+
+    if rank != 0:
+        return
+    peaks, peak_note = load_peaks()
+    flops, nbytes = train_algorithmic(s)
+    ms_step = total_ms / K
+    roof_s = max(flops / (peaks["bf16_tflops"] * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9))
+    per_call = {k: v / max(1, stage_calls.get(k, 1)) for k, v in stages_ms.items()}
+    # Dominant kernel: the slowest backward GEMM stage, against the bound its
+    # algorithmic FLOPs and bytes set.
+    cands = [(per_call[k], k) for k in per_call if bwd_stage_work(s, k)]
+    dom_ms, dom = max(cands)
+    fl, by = bwd_stage_work(s, dom)
+    t_fl = fl / (peaks["bf16_tflops"] * 1e12)
+    t_by = by / (peaks["hbm_gbs"] * 1e9)
+    if t_fl >= t_by:
+        roof = {"bound": "tensor", "achieved": fl / (dom_ms / 1e3) / 1e12, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": by / (dom_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof.update({"kernel": f"grouped_gemm_kernel ({dom} launch)", "frac": roof["achieved"] / roof["peak"],
+                 "traffic": None, "peak_note": peak_note + (" (burst)" if roof["unit"] == "TFLOP/s" else ""),
+                 "flops_per_launch": fl, "bytes_per_launch": by, "avg_launch_us": dom_ms * 1e3})
+    fwd_k = kernels_per_call(s)
+    line = {
+        "metric": WORKLOADS[name][3], "value": world * s.T * K / (total_ms / 1e3), "unit": "tokens/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(config_block(name, world), step="fwd + bias update + bwd (dx, fp32 weight grads)"),
+        "layer_roofline": {"flops_per_step": flops, "bytes_per_step": nbytes, "roofline_us": roof_s * 1e6,
+                           "measured_us": ms_step * 1e3, "frac": roof_s / (ms_step / 1e3), "peak": peak_note,
+                           "frac_sustained": max(flops / (peaks["bf16_tflops_sustained"] * 1e12),
+                                                 nbytes / (peaks["hbm_gbs"] * 1e9)) / (ms_step / 1e3),
+                           "bound": "tensor" if flops / (peaks["bf16_tflops"] * 1e12) >
+                           nbytes / (peaks["hbm_gbs"] * 1e9) else "hbm"},
+        "roofline": roof,
+        "stages_us": {k: v * 1e3 for k, v in per_call.items()},
+        "e2e": {"value": world * s.T / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(2 * hx.numel() * hx.element_size()),
+                "d2h_bytes_per_step": int(hdx.numel() * hdx.element_size()),
+                "copies": "x and dout from pinned host memory, dx back, on the compute stream; weight "
+                          "gradients stay on the device"},
+        "gpu_launches": K * (fwd_k + KERNELS_PER_BWD),
+        "clocks": sampler.summary(t_wall0, t_wall1),
+        "device_status": status,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(name, args.seed, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -520,7 +715,7 @@ def main():
         tdist.init_process_group("nccl")
         dist = tdist
     try:
-        gpu_arm(args, rank, world, dist)
+        (gpu_train_arm if args.workload == "train" else gpu_arm)(args, rank, world, dist)
     finally:
         if dist:
             dist.destroy_process_group()

@@ -267,19 +267,23 @@ moe_status_t moe_pack_gate_up(int32_t G, int32_t width, int32_t d, const void* w
 moe_status_t moe_quantize_int4(int64_t rows, int32_t K, const void* w, void* q, void* scale,
                                void* stream);
 
-/* Per-stage timing of moe_layer_fwd (profiling aid).  While enabled, every
- * moe_layer_fwd call records CUDA events on its stream between its stages; after
- * moe_profile_stop, moe_profile_stage_name(i) names stage i of the recorded calls
- * ("" for an unused slot).  On the large bf16 path the stages are the shared-expert
- * gate/up GEMM (while the routing runs on a second stream), the remaining wait for
- * the routing, the routed gate/up GEMM, the down GEMM and the combine.  moe_profile_start(max_calls, period) records every period-th call,
- * up to max_calls recorded calls (host-side event objects only, no device memory;
- * each event adds about 2 us to the stream, hence the sampling period);
- * moe_profile_stop synchronises, writes the summed milliseconds of each stage over
- * the recorded calls to ms_per_stage[moe_profile_stage_count()], the number of
+/* Per-stage timing of moe_layer_fwd and moe_layer_bwd (profiling aid).  While
+ * enabled, every recorded call places CUDA events on its stream between its stages;
+ * after moe_profile_stop, stage slot i (0 <= i < moe_profile_stage_count()) holds the
+ * summed milliseconds of the stage named moe_profile_stage_name(i) ("" for an unused
+ * slot) over the recorded calls that had it, moe_profile_stage_calls(i) of them.
+ * Stages are summed by name, so forward and backward calls can be recorded together.
+ * On the large bf16 forward the stages are the shared-expert gate/up GEMM (while the
+ * routing runs on a second stream), the remaining wait for the routing, the routed
+ * gate/up GEMM, the down GEMM and the combine; the backward's are named after its
+ * launches.  moe_profile_start(max_calls, period) records every period-th call, up to
+ * max_calls recorded calls (host-side event objects only, no device memory; each
+ * event adds about 2 us to the stream, hence the sampling period); moe_profile_stop
+ * synchronises, writes ms_per_stage[moe_profile_stage_count()] and the number of
  * recorded calls to *calls, and disables recording. */
 int32_t moe_profile_stage_count(void);
 const char* moe_profile_stage_name(int32_t stage);
+int32_t moe_profile_stage_calls(int32_t stage);
 moe_status_t moe_profile_start(int32_t max_calls, int32_t period);
 moe_status_t moe_profile_stop(float* ms_per_stage, int32_t* calls);
 
