@@ -21,15 +21,22 @@ namespace {
 // Padded layout of the permuted rows: expert e's n_e rows start at poff[e], the sum
 // of the earlier experts' counts rounded up to multiples of 64, so that every expert's
 // rows form whole 64-row K atoms of the weight-gradient GEMMs (the padding rows are
-// zero in every operand).  Each block derives poff from the offsets in shared memory
-// (one warp, E <= 256); block 0 stores it.  Thread i then writes tok_pad[i] (source
-// token of padded row i, -1 for padding and for rows past poff[E]) for i < q_max and,
-// for pair i < pairs, its padded row inv_pad[i] and gperm[inv_pad[i]] = gate[i].
-__global__ void pad_map_kernel(const int32_t* __restrict__ off, const int32_t* __restrict__ perm_tok,
-                               const int32_t* __restrict__ idx, const int32_t* __restrict__ inv_pos,
-                               const float* __restrict__ gate, int E, long long pairs, long long q_max,
-                               int32_t* __restrict__ poff_out, int32_t* __restrict__ tok_pad,
-                               int32_t* __restrict__ inv_pad, float* __restrict__ gperm) {
+// zero in every operand).  One launch builds it and gathers the rows:
+//   - every block derives poff from the offsets in shared memory (one warp, E <= 256);
+//     block 0 stores it;
+//   - thread i < pairs writes pair i's padded row inv_pad[i] and gperm[inv_pad[i]] =
+//     gate[i];
+//   - block b's warps copy padded rows [64 b, 64 b + 64) below poff[E]: xp[q] = x[tok],
+//     dp[q] = dout[tok] for the row's token, zero rows (and a zero gate) for padding;
+//     a lane keeps all of its 16-byte loads of both rows in flight before storing.
+constexpr int PAD_ROWS = 64;
+
+__global__ void __launch_bounds__(256) pad_gather_kernel(
+    const int32_t* __restrict__ off, const int32_t* __restrict__ perm_tok, const int32_t* __restrict__ idx,
+    const int32_t* __restrict__ inv_pos, const float* __restrict__ gate, int E, long long pairs,
+    const uint16_t* __restrict__ x, const uint16_t* __restrict__ dout, int d, int32_t* __restrict__ poff_out,
+    int32_t* __restrict__ inv_pad, float* __restrict__ gperm, uint16_t* __restrict__ xp,
+    uint16_t* __restrict__ dp) {
   __shared__ int s_off[kMaxE + 1], s_poff[kMaxE + 1];
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
@@ -59,51 +66,56 @@ __global__ void pad_map_kernel(const int32_t* __restrict__ off, const int32_t* _
     if (lane == 31 && E == kMaxE) s_poff[E] = incl;
   }
   __syncthreads();
-  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (blockIdx.x == 0)
     for (int e = threadIdx.x; e <= E; e += blockDim.x) poff_out[e] = s_poff[e];
-  if (i < q_max) {
-    int tok = -1;
-    if (i < s_poff[E]) {
-      int lo = 0, hi = E - 1;  // last expert with s_poff <= i
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s_poff[mid] <= i) lo = mid; else hi = mid - 1;
-      }
-      const long long r = s_off[lo] + (i - s_poff[lo]);
-      if (r < s_off[lo + 1]) tok = perm_tok[r];
-    }
-    tok_pad[i] = tok;
-    if (tok < 0) gperm[i] = 0.f;  // padding rows carry a zero gate (never garbage)
-  }
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i < pairs) {
     const int e = idx[i];
     const int q = s_poff[e] + (inv_pos[i] - s_off[e]);
     inv_pad[i] = q;
     gperm[q] = gate[i];
   }
-}
-
-// xp[q] = x[tok_pad[q]], dp[q] = dout[tok_pad[q]] (zero rows for tok_pad < 0) for
-// q < *rows_limit (= poff[E]), bf16, 16 bytes per thread.
-__global__ void gather_pad_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ dout,
-                                  const int32_t* __restrict__ tok_pad, long long q_max,
-                                  const int32_t* __restrict__ rows_limit, int d,
-                                  uint16_t* __restrict__ xp, uint16_t* __restrict__ dp) {
-  const int vpr = d / 8;  // 16-byte vectors per row
-  const long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (v >= q_max * vpr) return;
-  const long long q = v / vpr;
-  if (q >= *rows_limit) return;  // rows past the padded layout's end are never read
-  const int c = (int)(v % vpr);
-  const int t = tok_pad[q];
-  uint4 a = make_uint4(0, 0, 0, 0), b = a;
-  if (t >= 0) {
-    a = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * d) + c);
-    b = __ldg(reinterpret_cast<const uint4*>(dout + (size_t)t * d) + c);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int vpr = d / 8;  // 16-byte vectors per row (d <= 8192: at most 32 per lane)
+  for (int rr = warp; rr < PAD_ROWS; rr += 8) {
+    const long long q = (long long)blockIdx.x * PAD_ROWS + rr;
+    if (q >= s_poff[E]) break;
+    int lo = 0, hi = E - 1;  // last expert with s_poff <= q
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_poff[mid] <= q) lo = mid; else hi = mid - 1;
+    }
+    const long long r = s_off[lo] + (q - s_poff[lo]);
+    const int tok = r < s_off[lo + 1] ? perm_tok[r] : -1;
+    uint4* xo = reinterpret_cast<uint4*>(xp + q * d);
+    uint4* dq = reinterpret_cast<uint4*>(dp + q * d);
+    if (tok < 0) {
+      if (lane == 0) gperm[q] = 0.f;  // padding rows carry a zero gate (never garbage)
+      for (int v = lane; v < vpr; v += 32) xo[v] = dq[v] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const uint4* xi = reinterpret_cast<const uint4*>(x + (size_t)tok * d);
+    const uint4* di = reinterpret_cast<const uint4*>(dout + (size_t)tok * d);
+    for (int v0 = 0; v0 < vpr; v0 += 128) {  // 4 vectors of each row per lane in flight
+      uint4 a[4], g[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int v = v0 + lane + 32 * j;
+        if (v < vpr) {
+          a[j] = __ldg(xi + v);
+          g[j] = __ldg(di + v);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int v = v0 + lane + 32 * j;
+        if (v < vpr) {
+          xo[v] = a[j];
+          dq[v] = g[j];
+        }
+      }
+    }
   }
-  reinterpret_cast<uint4*>(xp + q * d)[c] = a;
-  reinterpret_cast<uint4*>(dp + q * d)[c] = b;
 }
 
 // Router backward and the input gradient, one warp per token (lane j < k holds pair j):
@@ -113,6 +125,8 @@ __global__ void gather_pad_kernel(const uint16_t* __restrict__ x, const uint16_t
 //   dx_t = dxs_t + sum_j (dxp[padded row j] + dz_j W_r[e_j]) (+ dout_t),
 // summed in fp32 (16-byte loads, 8 columns a lane), rounded once to bf16.  dgate
 // (optional) receives dg per pair.
+// KT: pairs held in registers (k <= KT).
+template <int KT>
 __global__ void router_bwd_dx_kernel(const int32_t* __restrict__ idx, const float* __restrict__ gate,
                                      const float* __restrict__ scores, const int32_t* __restrict__ inv_pad,
                                      const float* __restrict__ dgp, int nparts,
@@ -141,49 +155,85 @@ __global__ void router_bwd_dx_kernel(const int32_t* __restrict__ idx, const floa
   }
   const float dz = (renorm ? (dg - dgg) / S : dg) * sc * (1.0f - sc);
   if (lane < k) dzp[q] = dz;
-  for (int c = 8 * lane; c < d; c += 256) {
-    float v[8];
+  // Every lane's copy of the pairs' rows, experts and dz (shuffles while all lanes are
+  // converged: the column loop below runs a lane-dependent number of steps).
+  int qa[KT], ea[KT];
+  float za[KT];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = 0.f;
-    auto add8 = [&](const uint16_t* src) {
-      const uint4 u = __ldg(reinterpret_cast<const uint4*>(src));
-      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+  for (int j = 0; j < KT; ++j) {
+    qa[j] = __shfl_sync(0xFFFFFFFFu, q, j);
+    ea[j] = __shfl_sync(0xFFFFFFFFu, e, j);
+    za[j] = __shfl_sync(0xFFFFFFFFu, dz, j);
+  }
+  // Two blocks of 8 columns per lane per step, every load of both issued before use.
+  for (int c0 = 8 * lane; c0 < d; c0 += 512) {
+    const bool two = c0 + 256 < d;  // lane-dependent when d is not a multiple of 512
+    float v[2][8];
+    uint4 u_s[2], u_d[2], u_p[2][KT];
+    float4 w_r[2][KT][2];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        v[2 * i] += __uint_as_float(w4[i] << 16);
-        v[2 * i + 1] += __uint_as_float(w4[i] & 0xFFFF0000u);
+    for (int h = 0; h < 2; ++h) {
+      const int c = c0 + 256 * h;
+      if (h == 1 && !two) break;
+      if (dxs) u_s[h] = __ldg(reinterpret_cast<const uint4*>(dxs + (size_t)t * d + c));
+      if (dout) u_d[h] = __ldg(reinterpret_cast<const uint4*>(dout + (size_t)t * d + c));
+#pragma unroll
+      for (int j = 0; j < KT; ++j) {
+        if (j >= k) break;
+        const int qj = qa[j], ej = ea[j];
+        u_p[h][j] = __ldg(reinterpret_cast<const uint4*>(dxp + (size_t)qj * d + c));
+        w_r[h][j][0] = __ldg(reinterpret_cast<const float4*>(w_router + (size_t)ej * d + c));
+        w_r[h][j][1] = __ldg(reinterpret_cast<const float4*>(w_router + (size_t)ej * d + c + 4));
       }
-    };
-    if (dxs) add8(dxs + (size_t)t * d + c);
-    for (int j = 0; j < k; ++j) {
-      const int qj = __shfl_sync(0xFFFFFFFFu, q, j);
-      const int ej = __shfl_sync(0xFFFFFFFFu, e, j);
-      const float zj = __shfl_sync(0xFFFFFFFFu, dz, j);
-      add8(dxp + (size_t)qj * d + c);
-      const float4 w0 = __ldg(reinterpret_cast<const float4*>(w_router + (size_t)ej * d + c));
-      const float4 w1 = __ldg(reinterpret_cast<const float4*>(w_router + (size_t)ej * d + c + 4));
-      v[0] = fmaf(zj, w0.x, v[0]);
-      v[1] = fmaf(zj, w0.y, v[1]);
-      v[2] = fmaf(zj, w0.z, v[2]);
-      v[3] = fmaf(zj, w0.w, v[3]);
-      v[4] = fmaf(zj, w1.x, v[4]);
-      v[5] = fmaf(zj, w1.y, v[5]);
-      v[6] = fmaf(zj, w1.z, v[6]);
-      v[7] = fmaf(zj, w1.w, v[7]);
     }
-    if (dout) add8(dout + (size_t)t * d + c);
-    uint4 o;
-    o.x = __bfloat16_as_ushort(__float2bfloat16_rn(v[0])) | ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[1])) << 16);
-    o.y = __bfloat16_as_ushort(__float2bfloat16_rn(v[2])) | ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[3])) << 16);
-    o.z = __bfloat16_as_ushort(__float2bfloat16_rn(v[4])) | ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[5])) << 16);
-    o.w = __bfloat16_as_ushort(__float2bfloat16_rn(v[6])) | ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[7])) << 16);
-    *reinterpret_cast<uint4*>(dx + (size_t)t * d + c) = o;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int c = c0 + 256 * h;
+      if (h == 1 && !two) break;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[h][i] = 0.f;
+      auto add8 = [&](const uint4& u) {
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v[h][2 * i] += __uint_as_float(w4[i] << 16);
+          v[h][2 * i + 1] += __uint_as_float(w4[i] & 0xFFFF0000u);
+        }
+      };
+      if (dxs) add8(u_s[h]);
+#pragma unroll
+      for (int j = 0; j < KT; ++j) {
+        if (j >= k) break;
+        const float zj = za[j];
+        add8(u_p[h][j]);
+        const float4 w0 = w_r[h][j][0], w1 = w_r[h][j][1];
+        v[h][0] = fmaf(zj, w0.x, v[h][0]);
+        v[h][1] = fmaf(zj, w0.y, v[h][1]);
+        v[h][2] = fmaf(zj, w0.z, v[h][2]);
+        v[h][3] = fmaf(zj, w0.w, v[h][3]);
+        v[h][4] = fmaf(zj, w1.x, v[h][4]);
+        v[h][5] = fmaf(zj, w1.y, v[h][5]);
+        v[h][6] = fmaf(zj, w1.z, v[h][6]);
+        v[h][7] = fmaf(zj, w1.w, v[h][7]);
+      }
+      if (dout) add8(u_d[h]);
+      uint4 o;
+      o.x = __bfloat16_as_ushort(__float2bfloat16_rn(v[h][0])) |
+            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[h][1])) << 16);
+      o.y = __bfloat16_as_ushort(__float2bfloat16_rn(v[h][2])) |
+            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[h][3])) << 16);
+      o.z = __bfloat16_as_ushort(__float2bfloat16_rn(v[h][4])) |
+            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[h][5])) << 16);
+      o.w = __bfloat16_as_ushort(__float2bfloat16_rn(v[h][6])) |
+            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[h][7])) << 16);
+      *reinterpret_cast<uint4*>(dx + (size_t)t * d + c) = o;
+    }
   }
 }
 
 // dW_r[e][c] = sum over expert e's rows q of dzp[q] * xp[q][c] (padded layout).
 // Block (256 columns, expert e), 8 warps: warp w takes rows w, w + 8, ... with 8
-// columns a lane (16-byte loads, four rows in flight); the warps' partial sums are
+// columns a lane (16-byte loads, eight rows in flight); the warps' partial sums are
 // added in warp order through shared memory, so the result is deterministic.
 __global__ void router_wgrad_kernel(const float* __restrict__ dzp, const int32_t* __restrict__ off,
                                     const int32_t* __restrict__ poff, const uint16_t* __restrict__ xp,
@@ -198,16 +248,16 @@ __global__ void router_wgrad_kernel(const float* __restrict__ dzp, const int32_t
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
   if (c < d) {
     int r = warp;
-    for (; r + 24 < n; r += 32) {
-      uint4 u[4];
-      float z[4];
+    for (; r + 56 < n; r += 64) {
+      uint4 u[8];
+      float z[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 8; ++j) {
         u[j] = __ldg(reinterpret_cast<const uint4*>(xp + (size_t)(q0 + r + 8 * j) * d + c));
         z[j] = dzp[q0 + r + 8 * j];
       }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 8; ++j) {
         const uint32_t w4[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -241,21 +291,14 @@ __global__ void router_wgrad_kernel(const float* __restrict__ dzp, const int32_t
 
 }  // namespace
 
-cudaError_t launch_pad_map(const int32_t* off, const int32_t* perm_tok, const int32_t* idx,
-                           const int32_t* inv_pos, const float* gate, int E, long long pairs,
-                           long long q_max, int32_t* poff, int32_t* tok_pad, int32_t* inv_pad,
-                           float* gperm, cudaStream_t s) {
-  const long long n = std::max(q_max, pairs);
-  pad_map_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(off, perm_tok, idx, inv_pos, gate, E, pairs,
-                                                             q_max, poff, tok_pad, inv_pad, gperm);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_gather_pad(const uint16_t* x, const uint16_t* dout, const int32_t* tok_pad,
-                              long long q_max, const int32_t* rows_limit, int d, uint16_t* xp,
-                              uint16_t* dp, cudaStream_t s) {
-  const long long n = q_max * (d / 8);
-  gather_pad_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(x, dout, tok_pad, q_max, rows_limit, d, xp, dp);
+cudaError_t launch_pad_gather(const int32_t* off, const int32_t* perm_tok, const int32_t* idx,
+                              const int32_t* inv_pos, const float* gate, int E, long long pairs,
+                              long long q_max, const uint16_t* x, const uint16_t* dout, int d,
+                              int32_t* poff, int32_t* inv_pad, float* gperm, uint16_t* xp, uint16_t* dp,
+                              cudaStream_t s) {
+  const long long blocks = std::max((q_max + PAD_ROWS - 1) / PAD_ROWS, (pairs + 255) / 256);
+  pad_gather_kernel<<<(unsigned)blocks, 256, 0, s>>>(off, perm_tok, idx, inv_pos, gate, E, pairs, x, dout, d,
+                                                     poff, inv_pad, gperm, xp, dp);
   return cudaGetLastError();
 }
 
@@ -264,9 +307,13 @@ cudaError_t launch_router_bwd_dx(const int32_t* idx, const float* gate, const fl
                                  const uint16_t* dxp, const uint16_t* dxs, const uint16_t* dout, int T,
                                  int d, int E, int k, int renorm, float* dzp, float* dgate, uint16_t* dx,
                                  cudaStream_t s) {
-  router_bwd_dx_kernel<<<(unsigned)((T + 7) / 8), 256, 0, s>>>(idx, gate, scores, inv_pad, dgp, nparts,
-                                                               w_router, dxp, dxs, dout, T, d, E, k, renorm,
-                                                               dzp, dgate, dx);
+  const unsigned blocks = (unsigned)((T + 7) / 8);
+  if (k <= 2)
+    router_bwd_dx_kernel<2><<<blocks, 256, 0, s>>>(idx, gate, scores, inv_pad, dgp, nparts, w_router, dxp, dxs,
+                                                   dout, T, d, E, k, renorm, dzp, dgate, dx);
+  else
+    router_bwd_dx_kernel<kMaxK><<<blocks, 256, 0, s>>>(idx, gate, scores, inv_pad, dgp, nparts, w_router, dxp,
+                                                       dxs, dout, T, d, E, k, renorm, dzp, dgate, dx);
   return cudaGetLastError();
 }
 

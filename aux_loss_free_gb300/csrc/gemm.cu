@@ -421,15 +421,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       carry = p.E * ((p.routed.rows + BM - 1) / BM) * (p.routed.n_total / p.routed.bn);
     } else if (p.routed.enabled) {
       const int nt = p.routed.n_total / p.routed.bn;
+      // All offsets in one round trip, then the counts from shared memory.
+      int ov[(kMaxE + 1 + 31) / 32];
+#pragma unroll
+      for (int i = 0; i < (kMaxE + 1 + 31) / 32; ++i)
+        if (lane + 32 * i <= p.E) ov[i] = p.offsets[lane + 32 * i];
+#pragma unroll
+      for (int i = 0; i < (kMaxE + 1 + 31) / 32; ++i)
+        if (lane + 32 * i <= p.E) s_off[lane + 32 * i] = ov[i];
+      __syncwarp();
       for (int b = 0; b < p.E; b += 32) {
         const int g = b + lane;
         int v = 0;
-        if (g < p.E) {
-          const int o0 = p.offsets[g], o1 = p.offsets[g + 1];
-          s_off[g] = o0;
-          if (g == p.E - 1) s_off[p.E] = o1;
-          v = ((o1 - o0 + BM - 1) / BM) * nt;
-        }
+        if (g < p.E) v = ((s_off[g + 1] - s_off[g] + BM - 1) / BM) * nt;
         int incl = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {

@@ -180,15 +180,13 @@ cudaError_t launch_int4_down(const int32_t* active, const int32_t* offsets, cons
 
 // ---------------------------------------------------------------- backward
 // Padded layout of the permuted rows (each expert's rows start on a multiple of 64):
-// poff [E+1], tok_pad [q_max] (-1 = padding), inv_pad [pairs], gperm [q_max] (the
-// gate of each padded row, 0 on padding).
-cudaError_t launch_pad_map(const int32_t* off, const int32_t* perm_tok, const int32_t* idx,
-                           const int32_t* inv_pos, const float* gate, int E, long long pairs,
-                           long long q_max, int32_t* poff, int32_t* tok_pad, int32_t* inv_pad,
-                           float* gperm, cudaStream_t s);
-cudaError_t launch_gather_pad(const uint16_t* x, const uint16_t* dout, const int32_t* tok_pad,
-                              long long q_max, const int32_t* rows_limit, int d, uint16_t* xp,
-                              uint16_t* dp, cudaStream_t s);
+// poff [E+1], inv_pad [pairs], gperm [q_max] (the gate of each padded row, 0 on
+// padding), and the gathered rows xp, dp [q_max][d] (bf16; rows past poff[E] untouched).
+cudaError_t launch_pad_gather(const int32_t* off, const int32_t* perm_tok, const int32_t* idx,
+                              const int32_t* inv_pos, const float* gate, int E, long long pairs,
+                              long long q_max, const uint16_t* x, const uint16_t* dout, int d,
+                              int32_t* poff, int32_t* inv_pad, float* gperm, uint16_t* xp, uint16_t* dp,
+                              cudaStream_t s);
 // dgp: [Q][nparts] partial sums of dL/dgate per padded row (summed in order).
 cudaError_t launch_router_bwd_dx(const int32_t* idx, const float* gate, const float* scores,
                                  const int32_t* inv_pad, const float* dgp, int nparts, const float* w_router,

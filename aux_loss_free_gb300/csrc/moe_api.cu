@@ -665,7 +665,6 @@ int bwd_parts(const moe_shape_t* s) { return 2 * s->f / gemm_tile_n(EPI_SWIGLU_B
 
 struct BwdWs {
   int32_t* poff;     // [E+1] padded expert offsets
-  int32_t* tok_pad;  // [Q] source token of each padded row (-1 = padding)
   int32_t* inv_pad;  // [T*k] padded row of each pair
   float* gperm;      // [Q] gate of each padded row
   float* dgp;        // [Q][f / tile width] partial dL/dgate of each padded row
@@ -683,7 +682,6 @@ BwdWs carve_bwd(Carver& c, const moe_shape_t* s) {
   const size_t Q = (size_t)bwd_rows(s), Tk = (size_t)s->T * s->k, T = (size_t)s->T;
   BwdWs w;
   w.poff = static_cast<int32_t*>(c.take(4 * (size_t)(s->E + 1)));
-  w.tok_pad = static_cast<int32_t*>(c.take(4 * Q));
   w.inv_pad = static_cast<int32_t*>(c.take(4 * Tk));
   w.gperm = static_cast<float*>(c.take(4 * Q));
   w.dgp = static_cast<float*>(c.take(4 * Q * bwd_parts(s)));
@@ -749,15 +747,13 @@ moe_status_t moe_layer_bwd(const moe_shape_t* shape, const void* x, const float*
   const bool prof = prof_begin_call();
   if (prof) prof_mark("bwd_pad_gather", s);
 
-  // Padded permuted layout, then the gathered tokens and output gradients.
-  e = launch_pad_map(saved->offsets, saved->perm_tok, saved->idx, saved->inv_pos, saved->gate, E, P, Q,
-                     b.poff, b.tok_pad, b.inv_pad, b.gperm, s);
-  if (e == cudaSuccess) e = launch_gather_pad(xb, db, b.tok_pad, Q, b.poff + E, d, b.xp, b.dp, s);
+  // Padded permuted layout and the gathered tokens and output gradients.
+  e = launch_pad_gather(saved->offsets, saved->perm_tok, saved->idx, saved->inv_pos, saved->gate, E, P, Q, xb,
+                        db, d, b.poff, b.inv_pad, b.gperm, b.xp, b.dp, s);
   if (e != cudaSuccess) {
     if (prof) prof_mark(nullptr, s);
     return MOE_ERR_CUDA;
   }
-
   if (prof) prof_mark("bwd_dgrad_down", s);
   // (1) dh = dout Wd_e (B = the stored [d][f] weights, MN-major), dhs = dout Sd.
   {

@@ -47,6 +47,7 @@ FLUSH_BYTES = 512 << 20
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_shared_gate_up_nano_traffic.txt")
+TRAIN_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_wgrad_gate_up_train_traffic.txt")
 PROFILE_PERIOD = 10
 
 
@@ -66,10 +67,10 @@ def kernels_per_call(s):
     return router + 1 + (2 if fork else 1) + 1 + 1
 
 
-# Kernels one moe_layer_bwd launches: padded layout, gather, five grouped GEMMs
+# Kernels one moe_layer_bwd launches: padded layout with the row gather, five grouped GEMMs
 # (dgrad down; gate/up recompute with the SwiGLU backward; dgrad gate/up; two weight
 # gradients), router backward + dx, router weight gradient.
-KERNELS_PER_BWD = 9
+KERNELS_PER_BWD = 8
 
 
 def train_algorithmic(s):
@@ -182,12 +183,12 @@ def gemm_source_hash():
     return h.hexdigest()[:16]
 
 
-def read_traffic():
-    """DRAM bytes per gate/up GEMM launch from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
+def read_traffic(path=TRAFFIC_FILE):
+    """DRAM bytes per launch of the dominant GEMM from the committed ncu summary, if it
+    was taken on the current kernel source (else None)."""
     try:
         kv = {}
-        with open(TRAFFIC_FILE) as fh:
+        with open(path) as fh:
             for line in fh:
                 if ":" in line:
                     a, b = line.split(":", 1)
@@ -601,8 +602,9 @@ def gpu_train_arm(args, rank, world, dist):
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    # An odd sampling period alternates the recorded calls between forward and backward.
-    period = PROFILE_PERIOD + 1
+    # An odd sampling period alternates the recorded calls between forward and backward
+    # (every call of a short run).
+    period = PROFILE_PERIOD + 1 if 2 * K >= 4 * (PROFILE_PERIOD + 1) else 1
     M.moe_profile_start(2 * K // period + 2, period)
     t_wall0 = time.time()
     for i in range(K):
@@ -657,6 +659,8 @@ def gpu_train_arm(args, rank, world, dist):
     # Dominant kernel: the slowest backward GEMM stage, against the bound its
     # algorithmic FLOPs and bytes set.
     cands = [(per_call[k], k) for k in per_call if bwd_stage_work(s, k)]
+    if not cands:
+        raise RuntimeError("no backward stage was recorded")
     dom_ms, dom = max(cands)
     fl, by = bwd_stage_work(s, dom)
     t_fl = fl / (peaks["bf16_tflops"] * 1e12)
@@ -667,7 +671,7 @@ def gpu_train_arm(args, rank, world, dist):
     else:
         roof = {"bound": "hbm", "achieved": by / (dom_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof.update({"kernel": f"grouped_gemm_kernel ({dom} launch)", "frac": roof["achieved"] / roof["peak"],
-                 "traffic": None, "peak_note": peak_note + (" (burst)" if roof["unit"] == "TFLOP/s" else ""),
+                 "traffic": read_traffic(TRAIN_TRAFFIC_FILE) if dom == "bwd_wgrad_gate_up" else None, "peak_note": peak_note + (" (burst)" if roof["unit"] == "TFLOP/s" else ""),
                  "flops_per_launch": fl, "bytes_per_launch": by, "avg_launch_us": dom_ms * 1e3})
     fwd_k = kernels_per_call(s)
     line = {
