@@ -89,15 +89,26 @@ def train_algorithmic(s):
 
 
 def bwd_stage_work(s, stage):
-    """(FLOPs, HBM bytes that must move) of one backward GEMM stage, algorithmic."""
+    """(FLOPs, HBM bytes that must move) of one backward GEMM stage, algorithmic:
+    its weights or fp32 weight gradients, and its activation operands and outputs
+    once (padding rows not counted)."""
     P, T, d, f, F = s.T * s.k, s.T, s.d, s.f, s.F
     hit = min(s.E, P)
+    wd, wgu = hit * d * f + d * F, hit * 2 * f * d + 2 * F * d   # weight elements
     table = {
-        "bwd_dgrad_down": (2 * P * d * f + 2 * T * d * F, (hit * d * f + d * F) * 2),
-        "bwd_recompute_swiglu": (2 * P * d * 2 * f + 2 * T * d * 2 * F, (hit * 2 * f * d + 2 * F * d) * 2),
-        "bwd_dgrad_gate_up": (2 * P * 2 * f * d + 2 * T * 2 * F * d, (hit * 2 * f * d + 2 * F * d) * 2),
-        "bwd_wgrad_down": (2 * P * d * f + 2 * T * d * F, (hit * d * f + d * F) * 4),
-        "bwd_wgrad_gate_up": (2 * P * 2 * f * d + 2 * T * 2 * F * d, (hit * 2 * f * d + 2 * F * d) * 4),
+        # dh = dout Wd (P + T rows of dout in, dh out)
+        "bwd_dgrad_down": (2 * P * d * f + 2 * T * d * F, wd * 2 + (P + T) * d * 2 + (P * f + T * F) * 2),
+        # pre-activations recomputed, SwiGLU backward: x rows and dh in; (da, db) and g h out
+        "bwd_recompute_swiglu": (2 * P * d * 2 * f + 2 * T * d * 2 * F,
+                                 wgu * 2 + (P + T) * d * 2 + (P * f + T * F) * 2 * 2 + (P * 2 * f + T * 2 * F) * 2),
+        # dx rows = (da, db) Wgu
+        "bwd_dgrad_gate_up": (2 * P * 2 * f * d + 2 * T * 2 * F * d,
+                              wgu * 2 + (P * 2 * f + T * 2 * F) * 2 + (P + T) * d * 2),
+        # dWd = dout^T (g h): fp32 gradients out
+        "bwd_wgrad_down": (2 * P * d * f + 2 * T * d * F, wd * 4 + (P + T) * d * 2 + (P * f + T * F) * 2),
+        # dWgu = (da, db)^T x: fp32 gradients out
+        "bwd_wgrad_gate_up": (2 * P * 2 * f * d + 2 * T * 2 * F * d,
+                              wgu * 4 + (P * 2 * f + T * 2 * F) * 2 + (P + T) * d * 2),
     }
     return table.get(stage)
 
