@@ -95,6 +95,10 @@ struct Params {
   // range are skipped.  Used for the weight gradients, K running over tokens.
   int kgroup;
   long long group_stride;
+  // Non-zero: the offsets and both sets' B operands were complete before the previous
+  // kernel in the stream started, so the tile table and the first tile's B copies
+  // may be issued before the dependency wait (the A copies and every output wait).
+  int early;
   int E, k;
 };
 
@@ -410,8 +414,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     tmem_relinquish_pair();
   }
   // Set-up above is CTA-local; the offsets and operands come from earlier kernels.
-  pdl_wait();
-  pdl_trigger();
+  // With `early`, everything up to the first tile's B copies runs before the wait.
+  if (!p.early) {
+    pdl_wait();
+    pdl_trigger();
+  }
   if (warp == 2) {
     // Tile table of the routed groups: s_cum[g] = tiles of groups < g.
     int carry = 0;
@@ -459,6 +466,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0, issued = 0, last_par = 0;
       bool ok = true;
+      // Early start: the first tile's B copies (and the stage's expected bytes) go out
+      // now, into the empty ring; after the wait its first `pre` k-blocks load A only.
+      int pre = 0;
+      if (p.early) {
+        if (cluster < total) {
+          const Tile t = decode_tile(p, cluster, shared_tiles, s_off, s_cum, total);
+          const OperandSet& S = t.set ? p.routed : p.shared;
+          const int nkb = (t.klen + BK - 1) / BK;
+          const int half = S.bn / 2;
+          if (S.kblock) {
+            pre = min(nkb, STAGES);
+            for (int kb = 0; kb < pre; ++kb) {
+              const uint32_t sa = ring + kb * STAGE_BYTES;
+              const uint32_t fb = map_to_rank(smem_u32(&full_bar[kb]), 0);
+              if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[kb]), 2u * ATOMS * (A_ATOM + half * AK * 2));
+              if (S.b_mn)
+                tma_load_kblock_pair(sa + A_BYTES, &S.b, fb, t.bk + t.k0 + kb * BK, (t.n0 + half * (int)rank) / AK);
+              else
+                tma_load_kblock_pair(sa + A_BYTES, &S.b, fb, t.brow + half * (int)rank, t.k0 / AK + kb * ATOMS);
+            }
+          }
+        }
+        pdl_wait();
+        pdl_trigger();
+      }
       for (int tile = cluster; tile < total && ok; tile += nclusters) {
         const Tile t = decode_tile(p, tile, shared_tiles, s_off, s_cum, total);
         const OperandSet& S = t.set ? p.routed : p.shared;
@@ -466,7 +498,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const int half = S.bn / 2;
         const int katom0 = t.k0 / AK;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait_spin(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) {
+          const bool b_done = tile == cluster && kb < pre;  // B (and the byte count) already out
+          if (!b_done && !mbar_wait_spin(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) {
             ok = false;
             break;
           }
@@ -480,20 +513,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const uint32_t sa = ring + stage * STAGE_BYTES;
           const uint32_t fb = map_to_rank(smem_u32(&full_bar[stage]), 0);
           const uint32_t b_atom = (uint32_t)half * AK * 2;
-          if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[stage]), pair_bytes);
+          if (leader && !b_done) mbar_arrive_expect_tx(smem_u32(&full_bar[stage]), pair_bytes);
           if (S.a_mn | S.b_mn) {
             const int kk0 = t.k0 + kb * BK;
             if (S.a_mn)
               tma_load_kblock_pair(sa, &S.a, fb, kk0, (t.row0 + HM * (int)rank) / AK);
             else
               tma_load_kblock_pair(sa, &S.a, fb, t.row0 + HM * (int)rank, katom0 + kb * ATOMS);
-            if (S.b_mn)
+            if (b_done) {
+            } else if (S.b_mn) {
               tma_load_kblock_pair(sa + A_BYTES, &S.b, fb, t.bk + kk0, (t.n0 + half * (int)rank) / AK);
-            else
+            } else {
               tma_load_kblock_pair(sa + A_BYTES, &S.b, fb, t.brow + half * (int)rank, katom0 + kb * ATOMS);
+            }
           } else if (S.kblock) {
             tma_load_kblock_pair(sa, &S.a, fb, t.row0 + HM * (int)rank, katom0 + kb * ATOMS);
-            tma_load_kblock_pair(sa + A_BYTES, &S.b, fb, t.brow + half * (int)rank, katom0 + kb * ATOMS);
+            if (!b_done)
+              tma_load_kblock_pair(sa + A_BYTES, &S.b, fb, t.brow + half * (int)rank, katom0 + kb * ATOMS);
           } else {
             for (int at = 0; at < natoms; ++at) {
               tma_load_2d_pair(sa + at * A_ATOM, &S.a, fb, t.k0 + kb * BK + at * AK,
@@ -590,6 +626,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tempty_leader1 = map_to_rank(smem_u32(&tempty_bar[1]), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
+    if (p.early) pdl_wait();  // outputs and epilogue inputs belong to earlier kernels
     for (int tile = cluster; tile < total; tile += nclusters) {
       const Tile t = decode_tile(p, tile, shared_tiles, s_off, s_cum, total);
       const OperandSet& S = t.set ? p.routed : p.shared;
@@ -909,7 +946,7 @@ int gemm_max_pairs() {
 cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* offsets, int E,
                                 const GemmOperandSet& shared, const CombineInputs& comb,
                                 long long max_routed_rows, cudaStream_t s, int* bad_arg,
-                                int max_pairs, long long kgroup_stride) {
+                                int max_pairs, long long kgroup_stride, int early) {
   Params p;
   std::memset(&p, 0, sizeof(p));
   *bad_arg = 0;
@@ -925,6 +962,7 @@ cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* off
   p.gate = comb.gate;
   p.residual = comb.residual;
   p.k = comb.k;
+  p.early = early ? 1 : 0;
   p.kgroup = kgroup_stride > 0 ? 1 : 0;
   p.group_stride = kgroup_stride;
   if (p.kgroup && kgroup_stride % 8 != 0) p.routed.v8 = 0;  // groups' fp32 outputs off 32 B

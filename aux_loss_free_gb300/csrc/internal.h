@@ -142,10 +142,13 @@ struct CombineInputs {
 // kgroup_stride > 0 groups the routed set along K instead: offsets then holds the
 // E + 1 K offsets (multiples of 64), `routed.rows` is every group's row count, and
 // group g writes out + g * kgroup_stride (EPI_STORE_F32 for fp32 outputs).
+// early: the caller guarantees that the offsets and both sets' B operands were
+// complete before the previous kernel in the stream started (the launch then reads
+// them before its dependency wait).
 cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* offsets, int E,
                                 const GemmOperandSet& shared, const CombineInputs& comb,
                                 long long max_routed_rows, cudaStream_t s, int* bad_arg,
-                                int max_pairs = 0, long long kgroup_stride = 0);
+                                int max_pairs = 0, long long kgroup_stride = 0, int early = 0);
 // Number of co-resident 2-SM clusters of the grouped GEMM on the current device.
 int gemm_max_pairs();
 

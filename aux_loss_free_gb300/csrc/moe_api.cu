@@ -265,7 +265,9 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x_bf16, const int32_t* of
   GemmOperandSet s2{};
   if (s->F && !shared_gate_up_done) s2 = sd;
   if (mark) prof_mark(shared_gate_up_done ? "routed_down" : "gemm_down", st);
-  e = launch_grouped_gemm(r2, offsets, s->E, s2, none, Tk, st, &bad);
+  // The offsets come from before the gate/up launch and B is weights: the down launch
+  // may start its tile table and weight copies before its dependency wait.
+  e = launch_grouped_gemm(r2, offsets, s->E, s2, none, Tk, st, &bad, 0, 0, /*early=*/1);
   if (bad) return MOE_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (comb) {
@@ -556,8 +558,9 @@ moe_status_t moe_layer_fwd(const moe_shape_t* shape, const void* x, const float*
                              shape->F, EPI_SWIGLU, T};
     CombineInputs none{};
     int bad = 0;
+    // Shared-only launch: no offsets, B is the shared expert's weights (early start).
     const cudaError_t eg = launch_grouped_gemm(off, L.offsets, E, s1, none, (long long)T * k, s,
-                                               &bad, pairs - reserve);
+                                               &bad, pairs - reserve, 0, /*early=*/1);
     if (bad) return MOE_ERR_UNSUPPORTED;
     if (eg != cudaSuccess) return MOE_ERR_CUDA;
     if (prof) prof_mark("routing_wait", s);
@@ -773,7 +776,7 @@ moe_status_t moe_layer_bwd(const moe_shape_t* shape, const void* x, const float*
     if (has_shared)
       sh = GemmOperandSet{x, T, w->shared_gate_up, 1, 2 * F, d, b.abs, 2 * F, EPI_SWIGLU_BWD, T, 0, 0,
                           b.dhs, nullptr, nullptr};
-    e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad);
+    e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad, 0, 0, /*early=*/1);
   }
   if (prof && e == cudaSuccess) prof_mark("bwd_dgrad_gate_up", s);
   // (4) dxp = (da, db) Wgu_e (B = the stored [2f][d] weights, MN-major), dxs likewise.
@@ -781,7 +784,7 @@ moe_status_t moe_layer_bwd(const moe_shape_t* shape, const void* x, const float*
     GemmOperandSet r{b.ab, Q, w->w_gate_up, E, d, 2 * f, b.dxp, d, EPI_STORE, 0, 0, 1};
     GemmOperandSet sh{};
     if (has_shared) sh = GemmOperandSet{b.abs, T, w->shared_gate_up, 1, d, 2 * F, b.dxs, d, EPI_STORE, T, 0, 1};
-    e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad);
+    e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad, 0, 0, /*early=*/1);
   }
   if (prof && e == cudaSuccess) prof_mark("bwd_router_dx", s);
   // (5) Router backward and dx = sum of the pairs' rows + shared + router (+ dout).
@@ -796,7 +799,7 @@ moe_status_t moe_layer_bwd(const moe_shape_t* shape, const void* x, const float*
     GemmOperandSet r{b.dp, Q, b.dh, 1, f, (int)Q, g->dw_down, f, EPI_STORE_F32, d, 1, 1};
     GemmOperandSet sh{};
     if (has_shared) sh = GemmOperandSet{dout, T, b.dhs, 1, F, T, g->ds_down, F, EPI_STORE_F32, d, 1, 1};
-    e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad, 0, (long long)d * f);
+    e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad, 0, (long long)d * f, /*early=*/1);
   }
   if (prof && e == cudaSuccess) prof_mark("bwd_wgrad_gate_up", s);
   // (7) dWgu_e = (da, db)^T xp (rows interleaved as w_gate_up), dSgu = (das, dbs)^T x.
@@ -804,7 +807,7 @@ moe_status_t moe_layer_bwd(const moe_shape_t* shape, const void* x, const float*
     GemmOperandSet r{b.ab, Q, b.xp, 1, d, (int)Q, g->dw_gate_up, d, EPI_STORE_F32, 2 * f, 1, 1};
     GemmOperandSet sh{};
     if (has_shared) sh = GemmOperandSet{b.abs, T, x, 1, d, T, g->ds_gate_up, d, EPI_STORE_F32, 2 * F, 1, 1};
-    e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad, 0, (long long)2 * f * d);
+    e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad, 0, (long long)2 * f * d, /*early=*/1);
   }
   if (prof && e == cudaSuccess) prof_mark("bwd_router_wgrad", s);
   // (8) dW_r[e] = sum over the expert's rows of dz * x.

@@ -10,8 +10,10 @@
 // left), stored as one [3E][d] matrix.  Token values are bf16, so every product
 // x * W_part is exact in fp32 and the tensor core accumulates in fp32: the logits
 // carry fp32 accuracy (no reduced-precision weights, no TF32).  One CTA owns 128
-// tokens: a TMA producer streams 128 x 64 token tiles and 3E x 64 weight tiles
-// through a 4-stage ring (the CTA's whole token slab is prefetched into L2 first),
+// tokens: a TMA producer streams 128-wide k-blocks of the tokens (128 x 128) and of
+// the weights (3E x 128), one 3-D copy of two 64-column swizzle atoms per operand,
+// through a 2-stage ring (the CTA's whole token slab is prefetched into L2 first;
+// copies of 32-48 KB cost far less TMA issue time per byte than 16-24 KB ones),
 // one thread issues tcgen05.mma (M = 128, N = 3E, K = 16) into TMEM, and then two
 // threads per token read its 3E accumulator columns (one half of the experts
 // each), form the logits, apply the sigmoid, keep their best k by fl32(score +
@@ -32,15 +34,17 @@ namespace moe {
 namespace {
 
 constexpr int RBM = 128;
-constexpr int RBK = 64;
-constexpr int RSTAGES = 4;
-constexpr int A_BYTES = RBM * RBK * 2;
+constexpr int RAT = 64;           // K width of one 128-byte swizzle atom
+constexpr int RBK = 2 * RAT;      // K per stage: two atoms in one copy per operand
+constexpr int RSTAGES = 2;
+constexpr int A_ATOM = RBM * RAT * 2;
+constexpr int A_BYTES = 2 * A_ATOM;
 constexpr int RTHREADS = 256;  // 8 warps: two threads per token in the epilogue
 constexpr unsigned FULL = 0xFFFFFFFFu;
 
 struct RouterTcParams {
-  CUtensorMap x_map;  // [T][d] bf16, box 128 x 64
-  CUtensorMap w_map;  // [3E][d] bf16, box 3E x 64
+  CUtensorMap x_map;  // [T][d] bf16 as (64, T, d / 64), box (64, 128, 2)
+  CUtensorMap w_map;  // [3E][d] bf16 as (64, 3E, d / 64), box (64, 3E, 2)
   const float* logit_offset;
   const float* bias;
   float* scores;
@@ -110,13 +114,14 @@ __global__ void __launch_bounds__(RTHREADS, 1) router_tc_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = tmem_holder;
-  const int nkb = p.d / RBK;
+  const int nkb = (p.d + RBK - 1) / RBK;  // a ragged last atom arrives zero-filled
+  constexpr uint32_t W_ATOM = (uint32_t)N * RAT * 2;
 
   if (warp == 0 && lane == 0) {
     // The token slab is read once, from DRAM: ask for all of it up front so the
     // ring below is fed from L2 instead of paying DRAM latency per stage.
-    for (int kb = 0; kb < nkb; ++kb) tma_prefetch_l2_2d(&p.x_map, kb * RBK, t0);
-    const uint32_t bytes = A_BYTES + N * RBK * 2;
+    for (int kb = 0; kb < nkb; ++kb) tma_prefetch_l2_3d(&p.x_map, 0, t0, 2 * kb);
+    const uint32_t bytes = A_BYTES + 2 * W_ATOM;
     uint32_t issued = 0, last_par = 0;
     int stage = 0;
     uint32_t phase = 0;
@@ -125,8 +130,8 @@ __global__ void __launch_bounds__(RTHREADS, 1) router_tc_kernel(const __grid_con
       const uint32_t sa = ring + stage * p.stage_bytes;
       const uint32_t fb = smem_u32(&full_bar[stage]);
       mbar_arrive_expect_tx(fb, bytes);
-      tma_load_2d(sa, &p.x_map, fb, kb * RBK, t0);
-      tma_load_2d(sa + A_BYTES, &p.w_map, fb, kb * RBK, 0);
+      tma_load_3d(sa, &p.x_map, fb, 0, t0, 2 * kb);
+      tma_load_3d(sa + A_BYTES, &p.w_map, fb, 0, 0, 2 * kb);
       issued |= 1u << stage;
       last_par = (last_par & ~(1u << stage)) | (phase << stage);
       if (++stage == RSTAGES) {
@@ -151,8 +156,9 @@ __global__ void __launch_bounds__(RTHREADS, 1) router_tc_kernel(const __grid_con
       const uint64_t adesc = sw128_kmajor_desc(sa);
       const uint64_t bdesc = sw128_kmajor_desc(sa + A_BYTES);
 #pragma unroll
-      for (int kk = 0; kk < RBK / 16; ++kk)
-        tc_mma_bf16(tmem_base, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+      for (int kk = 0; kk < RBK / 16; ++kk)  // atom kk / 4, 32 bytes per K step inside it
+        tc_mma_bf16(tmem_base, adesc + (kk >> 2) * (A_ATOM >> 4) + 2 * (kk & 3),
+                    bdesc + (kk >> 2) * (W_ATOM >> 4) + 2 * (kk & 3), idesc, (kb | kk) != 0);
       tc_commit(smem_u32(&empty_bar[stage]));
       if (++stage == RSTAGES) {
         stage = 0;
@@ -323,14 +329,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// bf16 [outer][inner] viewed as (64 columns, outer rows, inner / 64 atoms), box (64,
+// box_outer, 2): one copy = two consecutive 128-byte-swizzled atoms, box_outer * 128
+// bytes apart (an atom past `inner` is zero-filled).
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
   auto fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {inner * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(RBK), box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+  if (!fn || inner % RAT != 0) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(RAT), outer, inner / RAT};
+  const cuuint64_t strides[2] = {inner * 2, static_cast<cuuint64_t>(RAT) * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(RAT), box_outer, 2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -380,7 +389,7 @@ cudaError_t launch_router_tc(const RouterArgs& a, void* w3_scratch, cudaStream_t
   p.d = a.d;
   p.k = a.k;
   p.renorm = a.renorm;
-  p.stage_bytes = A_BYTES + ((3 * a.E * RBK * 2 + 1023) / 1024) * 1024;
+  p.stage_bytes = A_BYTES + 2 * 3 * a.E * RAT * 2;  // multiples of 1024 for E % 16 == 0
   const int blocks = (a.T + RBM - 1) / RBM;
   switch (a.E) {
     case 16: return launch_e<16>(p, blocks, s);
