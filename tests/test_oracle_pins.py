@@ -468,3 +468,51 @@ def test_backward_gate_gradient_special_cases():
     for t in range(P["x"].shape[0]):
         e = int(P["idx"][t, 0])
         assert np.isclose(g2["dz"][t, e], g2["dgate"][t, 0] * sc[t, e] * (1 - sc[t, e]), rtol=1e-12)
+
+
+# ----------------------------------------------------------------- expert cache (LRU)
+
+def test_expert_cache_worked_example():
+    """The least-recently-used reading, worked by hand on a 6-expert, 3-slot cache."""
+    import json
+    import os
+    from oracle import expert_cache as C
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "expert_cache_lru_worked.json")))
+    state = C.lru_cache_state(g["E"], g["slots"])
+    for st in g["steps"]:
+        state, h, m, ev, jobs = C.lru_cache_step(state, np.array(st["idx"]))
+        assert (h, m, ev) == (st["hits"], st["misses"], st["evictions"])
+        assert [list(j) for j in jobs] == st["jobs"]
+        assert state[0].tolist() == st["slot_expert"] and state[2].tolist() == st["stamp"]
+    assert state[1].tolist() == g["final_expert_slot"]
+    with pytest.raises(C.CacheCapacityError):
+        C.lru_cache_step(state, np.array(g["overflow_step_idx"]))
+
+
+def test_expert_cache_invariants_and_textbook_cases():
+    from oracle import expert_cache as C
+    rng = np.random.default_rng(0)
+    E, slots = 16, 6
+    steps = [rng.choice(E, size=rng.integers(1, 4), replace=False) for _ in range(300)]
+    r = C.lru_cache_run(E, slots, steps)
+    state = C.lru_cache_state(E, slots)
+    for s, idx in enumerate(steps):
+        state, h, m, ev, jobs = C.lru_cache_step(state, idx)
+        used = set(int(e) for e in idx)
+        assert h + m == len(used)
+        slot_expert, expert_slot = state[0], state[1]
+        assert all(expert_slot[e] >= 0 and slot_expert[expert_slot[e]] == e for e in used)
+        assert all(slot_expert[expert_slot[e]] == e for e in range(E) if expert_slot[e] >= 0)
+        assert all(expert_slot[slot_expert[c]] == c for c in range(slots) if slot_expert[c] >= 0)
+        assert (h, m, ev) == (r["hits"][s], r["misses"][s], r["evictions"][s])
+    # Enough slots for every expert: one miss per first touch, never an eviction.
+    r2 = C.lru_cache_run(E, E, steps)
+    assert sum(r2["misses"]) == len(set(int(e) for st in steps for e in st)) and sum(r2["evictions"]) == 0
+    # Cycling one expert per step over slots + 1 experts: LRU misses every time.
+    cyc = [np.array([s % (slots + 1)]) for s in range(50)]
+    r3 = C.lru_cache_run(E, slots, cyc)
+    assert all(m == 1 for m in r3["misses"])
+    # A working set that fits: misses only on the first pass.
+    ws = [np.array([s % slots]) for s in range(60)]
+    r4 = C.lru_cache_run(E, slots, ws)
+    assert sum(r4["misses"]) == slots and all(m == 0 for m in r4["misses"][slots:])
