@@ -49,6 +49,11 @@ class MoEGrads(ctypes.Structure):
                 ("ds_gate_up", _P), ("ds_down", _P), ("dgate", _P)]
 
 
+class MoECacheStats(ctypes.Structure):
+    _fields_ = [("steps", _I64), ("hits", _I64), ("misses", _I64), ("evictions", _I64), ("bytes", _I64),
+                ("overflow", _I64)]
+
+
 _SHAPE_P = ctypes.POINTER(MoEShape)
 SIGNATURES = {
     "moe_abi_version": (_I32, []),
@@ -70,6 +75,11 @@ SIGNATURES = {
     "moe_layer_bwd_workspace_size": (_SZ, [_SHAPE_P]),
     "moe_layer_bwd": (_I32, [_SHAPE_P, _P, _P, ctypes.POINTER(MoEWeights), ctypes.POINTER(MoEDebug),
                              _P, _I32, ctypes.POINTER(MoEGrads), _P, _SZ, _P]),
+    "moe_expert_cache_bytes": (_SZ, [_SHAPE_P, _I32]),
+    "moe_expert_cache_init": (_I32, [_SHAPE_P, _I32, _P, _SZ, _P]),
+    "moe_expert_cache_read": (_I32, [_SHAPE_P, _I32, _P, ctypes.POINTER(MoECacheStats), _P, _P, _P, _P]),
+    "moe_layer_fwd_cached": (_I32, [_SHAPE_P, _P, _P, _P, _P, _F, _I32, ctypes.POINTER(MoEWeights), _I32, _P,
+                                    _SZ, _P, _P, ctypes.POINTER(MoEDebug), _P, _SZ, _P]),
     "moe_pack_gate_up": (_I32, [_I32, _I32, _I32, _P, _P, _P, _P]),
     "moe_quantize_int4": (_I32, [_I64, _I32, _P, _P, _P, _P]),
     "moe_device_status": (_I32, [_P, ctypes.POINTER(_I32)]),
@@ -224,6 +234,37 @@ def moe_layer_bwd(shape, x, w_router, weights: MoEWeights, saved: MoEDebug, dout
     _check("moe_layer_bwd", load_library().moe_layer_bwd(
         ctypes.byref(shape), _ptr(x), _ptr(w_router), ctypes.byref(weights), ctypes.byref(saved),
         _ptr(dout), int(residual), ctypes.byref(grads), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_expert_cache_bytes(shape, slots) -> int:
+    return load_library().moe_expert_cache_bytes(ctypes.byref(shape), slots)
+
+
+def moe_expert_cache_init(shape, slots, cache, stream=None):
+    _check("moe_expert_cache_init", load_library().moe_expert_cache_init(
+        ctypes.byref(shape), slots, _ptr(cache), cache.numel() * cache.element_size(), _stream(stream)))
+
+
+def moe_expert_cache_read(shape, slots, cache, stream=None):
+    """-> (stats dict, slot_expert, expert_slot, stamp) as numpy int32 arrays (synchronises)."""
+    import numpy as np
+    st = MoECacheStats()
+    se = np.empty(slots, np.int32)
+    es = np.empty(shape.E, np.int32)
+    sp = np.empty(slots, np.int32)
+    _check("moe_expert_cache_read", load_library().moe_expert_cache_read(
+        ctypes.byref(shape), slots, _ptr(cache), ctypes.byref(st), se.ctypes.data_as(_P),
+        es.ctypes.data_as(_P), sp.ctypes.data_as(_P), _stream(stream)))
+    return {n: getattr(st, n) for n, _ in MoECacheStats._fields_}, se, es, sp
+
+
+def moe_layer_fwd_cached(shape, x, w_router, logit_offset, bias, gamma, update_bias, host_weights: MoEWeights,
+                         slots, cache, residual, out, workspace, debug: MoEDebug | None = None, stream=None):
+    _check("moe_layer_fwd_cached", load_library().moe_layer_fwd_cached(
+        ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(logit_offset), _ptr(bias), gamma, int(update_bias),
+        ctypes.byref(host_weights), slots, _ptr(cache), cache.numel() * cache.element_size(), _ptr(residual),
+        _ptr(out), ctypes.byref(debug) if debug is not None else None, _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 

@@ -134,7 +134,7 @@ __device__ __forceinline__ int lanes_per_row(int ngroups) {
 __global__ void __launch_bounds__(DEC_WARPS * 32) int4_gate_up_kernel(
     const int32_t* __restrict__ active, const int32_t* __restrict__ offsets,
     const uint8_t* __restrict__ wq, const uint16_t* __restrict__ ws, const uint16_t* __restrict__ xp,
-    uint16_t* __restrict__ h, int d, int f, int block) {
+    uint16_t* __restrict__ h, int d, int f, int block, const int32_t* __restrict__ slot) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x % 32;
@@ -149,7 +149,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) int4_gate_up_kernel(
     const int j = (int)(u % per_expert) * rpw + sub;
     const bool row_ok = j < f;
     const int jj = row_ok ? j : f - 1;
-    const long long grow = (long long)e * 2 * f + (jj / block) * 2 * block + jj % block;
+    const long long we = slot ? slot[e] : e;  // the weights' position (a cache slot)
+    const long long grow = we * 2 * f + (jj / block) * 2 * block + jj % block;
     const long long urow = grow + block;
     const int p0 = offsets[e], p1 = offsets[e + 1];
     for (int pc = p0; pc < p1; pc += DEC_TOK) {
@@ -184,7 +185,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) int4_gate_up_kernel(
 __global__ void __launch_bounds__(DEC_WARPS * 32) int4_down_kernel(
     const int32_t* __restrict__ active, const int32_t* __restrict__ offsets,
     const uint8_t* __restrict__ wq, const uint16_t* __restrict__ ws, const uint16_t* __restrict__ h,
-    uint16_t* __restrict__ y, int d, int f) {
+    uint16_t* __restrict__ y, int d, int f, const int32_t* __restrict__ slot) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x % 32;
@@ -198,7 +199,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) int4_down_kernel(
     const int e = active[u / per_expert];
     const int i = (int)(u % per_expert) * rpw + sub;
     const bool row_ok = i < d;
-    const long long row = (long long)e * d + (row_ok ? i : d - 1);
+    const long long row = (long long)(slot ? slot[e] : e) * d + (row_ok ? i : d - 1);
     const int p0 = offsets[e], p1 = offsets[e + 1];
     for (int pc = p0; pc < p1; pc += DEC_TOK) {
       float acc[DEC_TOK];
@@ -251,7 +252,7 @@ template <bool GATE_UP>
 __global__ void __launch_bounds__(DEC_WARPS * 32, 2) int4_direct_kernel(
     const int32_t* __restrict__ idx, int P, int k, const uint8_t* __restrict__ wq,
     const uint16_t* __restrict__ ws, const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
-    int d, int f, int block) {
+    int d, int f, int block, const int32_t* __restrict__ slot) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int NM = GATE_UP ? 2 : 1;  // gate and up rows, or the down row
@@ -274,6 +275,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 2) int4_direct_kernel(
     const int first = ma ? __ffs(ma) - 1 : 32 + __ffs(mb) - 1;
     if (first != p) continue;  // warp-uniform: another unit covers this expert's pairs
     const int r_base = (int)(u % per_pair) * rows_per_unit + sub;
+    const long long we = slot ? slot[e] : e;  // the weights' position (a cache slot)
     unsigned long long mask = (unsigned long long)ma | ((unsigned long long)mb << 32);
     while (mask) {
       int pp[DIR_TOK], cnt = 0;
@@ -291,10 +293,10 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 2) int4_direct_kernel(
         const int rr = min(r, rows - 1);
         long long wrow[NM];
         if (GATE_UP) {
-          wrow[0] = (long long)e * 2 * f + (rr / block) * 2 * block + rr % block;
+          wrow[0] = we * 2 * f + (rr / block) * 2 * block + rr % block;
           wrow[NM - 1] = wrow[0] + block;
         } else {
-          wrow[0] = (long long)e * d + rr;
+          wrow[0] = we * d + rr;
         }
         float acc[NM][DIR_TOK];
 #pragma unroll
@@ -346,27 +348,27 @@ int decode_grid() {
 
 cudaError_t launch_int4_gate_up(const int32_t* active, const int32_t* offsets, const uint8_t* wq,
                                 const uint16_t* ws, const uint16_t* xp, uint16_t* h, int d, int f,
-                                int block, cudaStream_t s) {
+                                int block, cudaStream_t s, const int32_t* slot) {
   return launch_pdl(int4_gate_up_kernel, dim3(decode_grid()), dim3(DEC_WARPS * 32), 0, s, active,
-                    offsets, wq, ws, xp, h, d, f, block);
+                    offsets, wq, ws, xp, h, d, f, block, slot);
 }
 
 cudaError_t launch_int4_direct(bool gate_up, const int32_t* idx, int pairs, int k, const uint8_t* wq,
                                const uint16_t* ws, const uint16_t* src, uint16_t* dst, int d, int f,
-                               int block, cudaStream_t s) {
+                               int block, cudaStream_t s, const int32_t* slot) {
   if (pairs < 1 || pairs > kDirectMaxPairs) return cudaErrorInvalidValue;
   if (gate_up)
     return launch_pdl(int4_direct_kernel<true>, dim3(decode_grid()), dim3(DEC_WARPS * 32), 0, s, idx,
-                      pairs, k, wq, ws, src, dst, d, f, block);
+                      pairs, k, wq, ws, src, dst, d, f, block, slot);
   return launch_pdl(int4_direct_kernel<false>, dim3(decode_grid()), dim3(DEC_WARPS * 32), 0, s, idx,
-                    pairs, k, wq, ws, src, dst, d, f, block);
+                    pairs, k, wq, ws, src, dst, d, f, block, slot);
 }
 
 cudaError_t launch_int4_down(const int32_t* active, const int32_t* offsets, const uint8_t* wq,
                              const uint16_t* ws, const uint16_t* h, uint16_t* y, int d, int f,
-                             cudaStream_t s) {
+                             cudaStream_t s, const int32_t* slot) {
   return launch_pdl(int4_down_kernel, dim3(decode_grid()), dim3(DEC_WARPS * 32), 0, s, active,
-                    offsets, wq, ws, h, y, d, f);
+                    offsets, wq, ws, h, y, d, f, slot);
 }
 
 }  // namespace moe

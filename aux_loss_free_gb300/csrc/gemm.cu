@@ -134,11 +134,6 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-
 // Arrive without release semantics: for the accumulator hand-back, which orders only
 // the epilogue's TMEM reads (complete once tcgen05.wait::ld returned) before the next
 // MMAs.  A release here would hold every epilogue thread until its global stores of

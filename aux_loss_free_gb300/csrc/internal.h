@@ -168,18 +168,20 @@ cudaError_t launch_skinny(int mode, const uint16_t* w, int rows, int K, const ui
 cudaError_t launch_quantize_int4(long long rows, int K, const uint16_t* w, uint8_t* q,
                                  uint16_t* scale, cudaStream_t s);
 // `active` [kMaxE + 1]: ids of the experts with rows (ascending), count at [kMaxE].
+// slot (nullable, [E]): expert e's weights sit at position slot[e] of wq / ws (a cache
+// slot); else at e.
 cudaError_t launch_int4_gate_up(const int32_t* active, const int32_t* offsets, const uint8_t* wq,
                                 const uint16_t* ws, const uint16_t* xp, uint16_t* h, int d, int f,
-                                int block, cudaStream_t s);
+                                int block, cudaStream_t s, const int32_t* slot = nullptr);
 // Top-1 serving without the permutation (at most kDirectMaxPairs (token, expert)
 // pairs): gate_up: h[p][f] from x[p / k]; down: y[p][d] from h[p]; p = t * k + j.
 constexpr int kDirectMaxPairs = 64;
 cudaError_t launch_int4_direct(bool gate_up, const int32_t* idx, int pairs, int k, const uint8_t* wq,
                                const uint16_t* ws, const uint16_t* src, uint16_t* dst, int d, int f,
-                               int block, cudaStream_t s);
+                               int block, cudaStream_t s, const int32_t* slot = nullptr);
 cudaError_t launch_int4_down(const int32_t* active, const int32_t* offsets, const uint8_t* wq,
                              const uint16_t* ws, const uint16_t* h, uint16_t* y, int d, int f,
-                             cudaStream_t s);
+                             cudaStream_t s, const int32_t* slot = nullptr);
 
 // ---------------------------------------------------------------- backward
 // Padded layout of the permuted rows (each expert's rows start on a multiple of 64):
@@ -198,5 +200,34 @@ cudaError_t launch_router_bwd_dx(const int32_t* idx, const float* gate, const fl
                                  cudaStream_t s);
 cudaError_t launch_router_wgrad(const float* dzp, const int32_t* off, const int32_t* poff,
                                 const uint16_t* xp, int d, int E, float* dwr, cudaStream_t s);
+
+// ---------------------------------------------------------------- int4 expert cache
+constexpr int kMaxCacheSlots = 256;
+// Device state of the residency cache (least recently used over `slots` HBM slots).
+struct CacheState {
+  int step;       // serving steps planned so far (the stamp of the next one)
+  int njobs;      // copies the last plan asked for
+  int overflow;   // steps that used more experts than slots (not served)
+  int pad;
+  long long hits, misses, evictions, bytes;
+};
+// The four per-expert weight segments (gate/up codes and scales, down codes and
+// scales): base pointers and bytes per expert.
+struct CacheSegments {
+  uint8_t* base[4];
+  long long bytes[4];
+};
+struct CacheView {
+  CacheState* state;
+  int32_t* slot_expert;  // [slots] expert held, -1 empty
+  int32_t* stamp;        // [slots] step of last use, -1 never
+  int32_t* expert_slot;  // [E] slot, -1 absent
+  int2* jobs;            // [max(E, slots)] (expert, slot) copies of the last plan
+  CacheSegments slots_w; // the slots' weights, expert-major layout with slots as experts
+};
+// Plans one serving step from its routing result idx [pairs] and copies the missing
+// experts from host_src (device-accessible host memory, expert-major) into the slots.
+cudaError_t launch_cache_fetch(const int32_t* idx, int pairs, int E, int slots, const CacheView& v,
+                               const CacheSegments& host_src, long long expert_bytes, cudaStream_t s);
 
 }  // namespace moe

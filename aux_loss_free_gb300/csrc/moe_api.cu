@@ -296,7 +296,7 @@ bool int4_skinny(const moe_shape_t* s) {
 moe_status_t run_ffn_int4(const moe_shape_t* s, const void* x_bf16, const LayerWs& L,
                           const moe_weights_t* w, const void* residual, uint16_t* out,
                           cudaStream_t st, bool mark, cudaEvent_t shared_gate_up_on = nullptr,
-                          bool direct = false) {
+                          bool direct = false, const int32_t* slot = nullptr) {
   const long long Tk = (long long)s->T * s->k;
   int bad = 0;
   GemmOperandSet off{};
@@ -321,18 +321,18 @@ moe_status_t run_ffn_int4(const moe_shape_t* s, const void* x_bf16, const LayerW
     e = launch_int4_direct(true, L.idx, (int)Tk, s->k, static_cast<const uint8_t*>(w->w_gate_up),
                            static_cast<const uint16_t*>(w->scale_gate_up),
                            static_cast<const uint16_t*>(x_bf16), L.ffn.h, s->d, s->f,
-                           moe_gate_up_block(s->f), st);
+                           moe_gate_up_block(s->f), st, slot);
     if (e == cudaSuccess)
       e = launch_int4_direct(false, L.idx, (int)Tk, s->k, static_cast<const uint8_t*>(w->w_down),
                              static_cast<const uint16_t*>(w->scale_down), L.ffn.h, L.y, s->d, s->f,
-                             moe_gate_up_block(s->f), st);
+                             moe_gate_up_block(s->f), st, slot);
   } else {
     e = launch_int4_gate_up(L.active, L.offsets, static_cast<const uint8_t*>(w->w_gate_up),
                             static_cast<const uint16_t*>(w->scale_gate_up), L.ffn.xp, L.ffn.h, s->d,
-                            s->f, moe_gate_up_block(s->f), st);
+                            s->f, moe_gate_up_block(s->f), st, slot);
     if (e == cudaSuccess)
       e = launch_int4_down(L.active, L.offsets, static_cast<const uint8_t*>(w->w_down),
-                           static_cast<const uint16_t*>(w->scale_down), L.ffn.h, L.y, s->d, s->f, st);
+                           static_cast<const uint16_t*>(w->scale_down), L.ffn.h, L.y, s->d, s->f, st, slot);
   }
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (mark) prof_mark("shared_down_combine", st);
@@ -503,15 +503,50 @@ size_t moe_layer_workspace_size(const moe_shape_t* shape) {
   return c.off;
 }
 
+}  // extern "C"
+
+namespace {
+
+// An int4 expert cache taking part in a serving call: the slots' weights stand in for
+// the routed weights, filled from host memory right after the routing.
+struct CacheCtx {
+  CacheView view;
+  CacheSegments host_src;
+  long long expert_bytes;
+  int slots;
+};
+
+moe_status_t layer_fwd_impl(const moe_shape_t* shape, const void* x, const float* w_router,
+                            const float* logit_offset, float* bias, float gamma, int32_t update_bias,
+                            const moe_weights_t* w, const void* residual, void* out, const moe_debug_t* dbg,
+                            void* workspace, size_t ws_bytes, void* stream, const CacheCtx* cache);
+
+}  // namespace
+
+extern "C" {
+
 moe_status_t moe_layer_fwd(const moe_shape_t* shape, const void* x, const float* w_router,
                            const float* logit_offset, float* bias, float gamma,
                            int32_t update_bias, const moe_weights_t* w, const void* residual,
                            void* out, const moe_debug_t* dbg, void* workspace, size_t ws_bytes,
                            void* stream) {
+  return layer_fwd_impl(shape, x, w_router, logit_offset, bias, gamma, update_bias, w, residual, out, dbg,
+                        workspace, ws_bytes, stream, nullptr);
+}
+
+}  // extern "C"
+
+namespace {
+
+moe_status_t layer_fwd_impl(const moe_shape_t* shape, const void* x, const float* w_router,
+                            const float* logit_offset, float* bias, float gamma, int32_t update_bias,
+                            const moe_weights_t* w, const void* residual, void* out, const moe_debug_t* dbg,
+                            void* workspace, size_t ws_bytes, void* stream, const CacheCtx* cache) {
   moe_status_t st = check_shape(shape);
   if (st) return st;
   const bool int4 = shape->w_format == MOE_W_INT4_G32;
   if (int4 && shape->x_dtype != MOE_X_BF16) return MOE_ERR_UNSUPPORTED;
+  if (cache && !int4) return MOE_ERR_UNSUPPORTED;
   if (!x || !w_router || !bias || !out || !workspace || !weights_ok(shape, w))
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_router) || !aligned16(out) ||
@@ -598,9 +633,13 @@ moe_status_t moe_layer_fwd(const moe_shape_t* shape, const void* x, const float*
     cudaError_t e = run_router(ra, L.router, rs);
     if (e == cudaSuccess && update_bias)
       e = launch_bias_update(E, (long long)T * k, L.load, gamma, bias, rs);
+    if (e == cudaSuccess && cache)
+      e = launch_cache_fetch(L.idx, T * k, E, cache->slots, cache->view, cache->host_src,
+                             cache->expert_bytes, rs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     const moe_status_t st2 = run_ffn_int4(shape, x, L, w, residual, static_cast<uint16_t*>(out), s,
-                                          prof, int4_fork ? aux->join : nullptr, true);
+                                          prof, int4_fork ? aux->join : nullptr, true,
+                                          cache ? cache->view.expert_slot : nullptr);
     if (prof) prof_mark(nullptr, s);
     return st2;
   }
@@ -626,6 +665,9 @@ moe_status_t moe_layer_fwd(const moe_shape_t* shape, const void* x, const float*
                        update_bias ? bias : nullptr, gamma, (long long)T * k, L.perm_tok,
                        L.inv_pos, x, xf, shape->d, L.ffn.xp, (xf && shape->F) ? L.ffn.xb : nullptr,
                        rs, int4 ? L.active : nullptr);
+  if (e == cudaSuccess && cache)
+    e = launch_cache_fetch(L.idx, T * k, E, cache->slots, cache->view, cache->host_src, cache->expert_bytes,
+                           rs);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (fork) {
     if (cudaEventRecord(aux->join, rs) != cudaSuccess ||
@@ -637,11 +679,144 @@ moe_status_t moe_layer_fwd(const moe_shape_t* shape, const void* x, const float*
   CombineInputs comb{L.y, L.inv_pos, L.gate, static_cast<const uint16_t*>(residual), k};
   const moe_status_t st2 =
       int4 ? run_ffn_int4(shape, xbf, L, w, residual, static_cast<uint16_t*>(out), s, prof,
-                          int4_fork ? aux->join : nullptr)
+                          int4_fork ? aux->join : nullptr, false, cache ? cache->view.expert_slot : nullptr)
            : run_ffn(shape, xbf, L.offsets, w, L.ffn, L.y, L.s_out, &comb,
                      static_cast<uint16_t*>(out), s, prof, fork);
   if (prof) prof_mark(nullptr, s);
   return st2;
+}
+
+// ---------------------------------------------------------------- int4 expert cache
+
+// Bytes per expert of the four int4 weight segments: gate/up codes, gate/up scales,
+// down codes, down scales.
+long long cache_seg_bytes(const moe_shape_t* s, int i) {
+  switch (i) {
+    case 0: return 2LL * s->f * (s->d / 2);
+    case 1: return 2LL * s->f * (s->d / 32) * 2;
+    case 2: return (long long)s->d * (s->f / 2);
+    default: return (long long)s->d * (s->f / 32) * 2;
+  }
+}
+
+bool cache_shape_ok(const moe_shape_t* s, int slots) {
+  if (check_shape(s) != MOE_OK || s->w_format != MOE_W_INT4_G32) return false;
+  // Every step must fit: at least as many slots as a step can use distinct experts.
+  if (slots < std::min<long long>(s->E, (long long)s->T * s->k) || slots > kMaxCacheSlots) return false;
+  for (int i = 0; i < 4; ++i)
+    if (cache_seg_bytes(s, i) % 16) return false;
+  return true;
+}
+
+CacheView carve_cache(Carver& c, const moe_shape_t* s, int slots) {
+  CacheView v;
+  v.state = static_cast<CacheState*>(c.take(sizeof(CacheState)));
+  v.slot_expert = static_cast<int32_t*>(c.take(4 * (size_t)slots));
+  v.stamp = static_cast<int32_t*>(c.take(4 * (size_t)slots));
+  v.expert_slot = static_cast<int32_t*>(c.take(4 * (size_t)s->E));
+  v.jobs = static_cast<int2*>(c.take(8 * (size_t)std::max(s->E, slots)));
+  for (int i = 0; i < 4; ++i) {
+    v.slots_w.bytes[i] = cache_seg_bytes(s, i);
+    v.slots_w.base[i] = static_cast<uint8_t*>(c.take((size_t)slots * cache_seg_bytes(s, i)));
+  }
+  return v;
+}
+
+void* align_up(void* p) {
+  return reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(p) + kAlign - 1) / kAlign * kAlign);
+}
+
+// Device-accessible address of caller memory holding the experts (pinned or managed
+// host memory, or device memory); null when the GPU cannot read it directly.
+const void* device_view(const void* p) {
+  cudaPointerAttributes a;
+  if (!p || cudaPointerGetAttributes(&a, p) != cudaSuccess) return nullptr;
+  if (a.type == cudaMemoryTypeUnregistered) return nullptr;
+  return a.devicePointer;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_expert_cache_bytes(const moe_shape_t* shape, int32_t slots) {
+  if (!cache_shape_ok(shape, slots)) return 0;
+  Carver c(nullptr);
+  carve_cache(c, shape, slots);
+  return c.off + kAlign;
+}
+
+moe_status_t moe_expert_cache_init(const moe_shape_t* shape, int32_t slots, void* cache, size_t bytes,
+                                   void* stream) {
+  if (!cache_shape_ok(shape, slots)) return MOE_ERR_UNSUPPORTED;
+  if (!cache) return MOE_ERR_INVALID_ARG;
+  if (bytes < moe_expert_cache_bytes(shape, slots)) return MOE_ERR_WORKSPACE;
+  Carver c(align_up(cache));
+  const CacheView v = carve_cache(c, shape, slots);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(v.state, 0, sizeof(CacheState), s) != cudaSuccess ||
+      cudaMemsetAsync(v.slot_expert, 0xFF, 4 * (size_t)slots, s) != cudaSuccess ||
+      cudaMemsetAsync(v.stamp, 0xFF, 4 * (size_t)slots, s) != cudaSuccess ||
+      cudaMemsetAsync(v.expert_slot, 0xFF, 4 * (size_t)shape->E, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t moe_expert_cache_read(const moe_shape_t* shape, int32_t slots, const void* cache,
+                                   moe_cache_stats_t* stats, int32_t* slot_expert, int32_t* expert_slot,
+                                   int32_t* stamp, void* stream) {
+  if (!cache_shape_ok(shape, slots)) return MOE_ERR_UNSUPPORTED;
+  if (!cache) return MOE_ERR_INVALID_ARG;
+  Carver c(align_up(const_cast<void*>(cache)));
+  const CacheView v = carve_cache(c, shape, slots);
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (stats) {
+    CacheState h;
+    if (cudaMemcpy(&h, v.state, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    stats->steps = h.step;
+    stats->hits = h.hits;
+    stats->misses = h.misses;
+    stats->evictions = h.evictions;
+    stats->bytes = h.bytes;
+    stats->overflow = h.overflow;
+  }
+  if (slot_expert && cudaMemcpy(slot_expert, v.slot_expert, 4 * (size_t)slots, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (expert_slot && cudaMemcpy(expert_slot, v.expert_slot, 4 * (size_t)shape->E, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (stamp && cudaMemcpy(stamp, v.stamp, 4 * (size_t)slots, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_fwd_cached(const moe_shape_t* shape, const void* x, const float* w_router,
+                                  const float* logit_offset, float* bias, float gamma, int32_t update_bias,
+                                  const moe_weights_t* host_w, int32_t slots, void* cache, size_t cache_bytes,
+                                  const void* residual, void* out, const moe_debug_t* dbg, void* workspace,
+                                  size_t ws_bytes, void* stream) {
+  if (!cache_shape_ok(shape, slots)) return MOE_ERR_UNSUPPORTED;
+  if (!host_w || !cache) return MOE_ERR_INVALID_ARG;
+  if (cache_bytes < moe_expert_cache_bytes(shape, slots)) return MOE_ERR_WORKSPACE;
+  const void* src[4] = {device_view(host_w->w_gate_up), device_view(host_w->scale_gate_up),
+                        device_view(host_w->w_down), device_view(host_w->scale_down)};
+  CacheCtx ctx;
+  Carver c(align_up(cache));
+  ctx.view = carve_cache(c, shape, slots);
+  ctx.slots = slots;
+  ctx.expert_bytes = 0;
+  for (int i = 0; i < 4; ++i) {
+    if (!src[i] || !aligned16(src[i])) return MOE_ERR_INVALID_ARG;
+    ctx.host_src.base[i] = static_cast<uint8_t*>(const_cast<void*>(src[i]));
+    ctx.host_src.bytes[i] = cache_seg_bytes(shape, i);
+    ctx.expert_bytes += cache_seg_bytes(shape, i);
+  }
+  moe_weights_t wc = *host_w;  // the routed weights come from the slots; shared as given
+  wc.w_gate_up = ctx.view.slots_w.base[0];
+  wc.scale_gate_up = ctx.view.slots_w.base[1];
+  wc.w_down = ctx.view.slots_w.base[2];
+  wc.scale_down = ctx.view.slots_w.base[3];
+  return layer_fwd_impl(shape, x, w_router, logit_offset, bias, gamma, update_bias, &wc, residual, out, dbg,
+                        workspace, ws_bytes, stream, &ctx);
 }
 
 }  // extern "C"

@@ -138,3 +138,42 @@ def layer_backward(layer: "LayerOnDevice", x: torch.Tensor, saved: SavedForward,
     L.moe_layer_bwd(layer.shape, x, layer.w_router, layer.weights, saved.debug, dout, residual,
                     grads.struct, layer.bwd_workspace, stream=stream)
     return grads
+
+
+class ExpertCache:
+    """GPU-side residency cache of a serving layer's int4 routed experts.
+
+    The layer's int4 codes and scales are copied once to pinned host memory (the
+    streaming source); the GPU keeps `slots` experts in HBM and fills them per step
+    inside moe_layer_fwd_cached."""
+
+    def __init__(self, layer: "LayerOnDevice", slots: int):
+        if layer.spec.w_format != "int4":
+            raise ValueError("the expert cache serves int4 layers")
+        self.layer, self.slots = layer, slots
+        self.host = {}
+        for name in ("w_gate_up", "scale_gate_up", "w_down", "scale_down"):
+            t = getattr(layer, name)
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.copy_(t)
+            self.host[name] = h
+        self.host_weights = L.make_weights(self.host["w_gate_up"], self.host["w_down"], layer.shared_gate_up,
+                                           layer.shared_down, self.host["scale_gate_up"], self.host["scale_down"])
+        n = L.moe_expert_cache_bytes(layer.shape, slots)
+        if n == 0:
+            raise L.MoEError("moe_expert_cache_bytes", 2)
+        self.mem = torch.empty(n, dtype=torch.uint8, device=layer.device)
+        self.reset()
+
+    def reset(self, stream=None):
+        L.moe_expert_cache_init(self.layer.shape, self.slots, self.mem, stream=stream)
+
+    def forward(self, x, out, update_bias=False, residual=None, debug=None, stream=None):
+        ly = self.layer
+        L.moe_layer_fwd_cached(ly.shape, x, ly.w_router, ly.logit_offset, ly.bias, ly.gamma, update_bias,
+                               self.host_weights, self.slots, self.mem, residual, out, ly.workspace,
+                               debug=debug, stream=stream)
+        return out
+
+    def read(self, stream=None):
+        return L.moe_expert_cache_read(self.layer.shape, self.slots, self.mem, stream=stream)

@@ -253,6 +253,47 @@ moe_status_t moe_layer_bwd(const moe_shape_t* shape, const void* x, const float*
                            int32_t residual, const moe_grads_t* grads, void* workspace,
                            size_t ws_bytes, void* stream);
 
+/* GPU-side residency cache of the int4 routed experts (top-1 serving).
+ * Relay article, opening section, second paragraph: the int4 experts are streamed from
+ * NVMe through an LRU cache under a memory budget; top-2 paragraph: the skew left after
+ * balancing is what such a cache likes.  Here all experts' int4 weights stay in host
+ * memory the GPU can read (pinned or managed), HBM holds `slots` of them, and
+ * moe_layer_fwd_cached brings each step's experts in on the GPU with no host round
+ * trip: after the routing one block plans the step and a grid copies the missing
+ * experts over the CPU-GPU link into their slots.  Policy (this library's reading of
+ * LRU): the experts a step uses are the distinct entries of its routing result,
+ * ascending; the resident ones are hits and their slots are stamped with the step
+ * number first; then each missing expert, in ascending order, takes the slot with the
+ * smallest stamp among the slots not stamped in this step (empty slots have stamp -1),
+ * ties to the lowest slot, evicting its previous expert.
+ * Shapes: w_format = MOE_W_INT4_G32 (k = 1, T <= 256) and
+ * min(E, T*k) <= slots <= 256, so that every step fits.
+ *   moe_expert_cache_bytes  device bytes of the cache (state + slots), 0 if unsupported
+ *   moe_expert_cache_init   empties the cache (stream-ordered memsets)
+ *   moe_expert_cache_read   synchronises `stream`, then copies the counters and (each
+ *                           output nullable) slot_expert [slots] (-1 empty),
+ *                           expert_slot [E] (-1 absent) and stamp [slots] to the host
+ *   moe_layer_fwd_cached    moe_layer_fwd with the routed int4 weights (w_gate_up,
+ *                           scale_gate_up, w_down, scale_down of host_w) in host memory,
+ *                           layouts as in moe_weights_t; the shared expert's weights are
+ *                           device memory as usual.  The output equals moe_layer_fwd's
+ *                           with the same weights resident, bit for bit. */
+typedef struct {
+  int64_t steps, hits, misses, evictions, bytes, overflow;
+} moe_cache_stats_t;
+
+size_t moe_expert_cache_bytes(const moe_shape_t* shape, int32_t slots);
+moe_status_t moe_expert_cache_init(const moe_shape_t* shape, int32_t slots, void* cache, size_t bytes,
+                                   void* stream);
+moe_status_t moe_expert_cache_read(const moe_shape_t* shape, int32_t slots, const void* cache,
+                                   moe_cache_stats_t* stats, int32_t* slot_expert, int32_t* expert_slot,
+                                   int32_t* stamp, void* stream);
+moe_status_t moe_layer_fwd_cached(const moe_shape_t* shape, const void* x, const float* w_router,
+                                  const float* logit_offset, float* bias, float gamma, int32_t update_bias,
+                                  const moe_weights_t* host_w, int32_t slots, void* cache, size_t cache_bytes,
+                                  const void* residual, void* out, const moe_debug_t* dbg, void* workspace,
+                                  size_t ws_bytes, void* stream);
+
 /* Weight preparation (off the hot path).
  * moe_pack_gate_up: for each of G matrices, interleave w_gate [G][width][d] and
  * w_up [G][width][d] (bf16) into w_gate_up [G][2*width][d] in blocks of
