@@ -633,9 +633,11 @@ moe_status_t layer_fwd_impl(const moe_shape_t* shape, const void* x, const float
     cudaError_t e = run_router(ra, L.router, rs);
     if (e == cudaSuccess && update_bias)
       e = launch_bias_update(E, (long long)T * k, L.load, gamma, bias, rs);
-    if (e == cudaSuccess && cache)
+    if (e == cudaSuccess && cache) {
+      if (prof) prof_mark("cache_fetch", rs);
       e = launch_cache_fetch(L.idx, T * k, E, cache->slots, cache->view, cache->host_src,
                              cache->expert_bytes, rs);
+    }
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     const moe_status_t st2 = run_ffn_int4(shape, x, L, w, residual, static_cast<uint16_t*>(out), s,
                                           prof, int4_fork ? aux->join : nullptr, true,
@@ -665,9 +667,11 @@ moe_status_t layer_fwd_impl(const moe_shape_t* shape, const void* x, const float
                        update_bias ? bias : nullptr, gamma, (long long)T * k, L.perm_tok,
                        L.inv_pos, x, xf, shape->d, L.ffn.xp, (xf && shape->F) ? L.ffn.xb : nullptr,
                        rs, int4 ? L.active : nullptr);
-  if (e == cudaSuccess && cache)
+  if (e == cudaSuccess && cache) {
+    if (prof) prof_mark("cache_fetch", rs);
     e = launch_cache_fetch(L.idx, T * k, E, cache->slots, cache->view, cache->host_src, cache->expert_bytes,
                            rs);
+  }
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (fork) {
     if (cudaEventRecord(aux->join, rs) != cudaSuccess ||

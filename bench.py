@@ -146,7 +146,21 @@ WORKLOADS = {
                 "Top-1 int4 serving decode tokens/s (T=8), % HBM roofline"),
     "decode64": ("decode", CONFIGS["decode"].replace(T=64), "top1_int4_decode_T64",
                  "Top-1 int4 serving decode tokens/s (T=64), % HBM roofline"),
+    "cache8": ("decode", CONFIGS["decode"].replace(T=8, skew_zipf_s=1.2),
+               "top1_int4_decode_T8_expert_cache_16_of_64_zipf1.2",
+               "Top-1 int4 serving tokens/s through the GPU expert cache (T=8, 16 of 64 experts in HBM, "
+               "Zipf 1.2 routing), hit rate"),
+    "cache8u": ("decode", CONFIGS["decode"].replace(T=8),
+                "top1_int4_decode_T8_expert_cache_16_of_64_uniform",
+                "Top-1 int4 serving tokens/s through the GPU expert cache (T=8, 16 of 64 experts in HBM, "
+                "unskewed routing), hit rate"),
+    "cache1": ("decode", CONFIGS["decode"].replace(T=1, skew_zipf_s=1.2),
+               "top1_int4_decode_T1_expert_cache_4_of_64_zipf1.2",
+               "Top-1 int4 serving tokens/s through the GPU expert cache (T=1, 4 of 64 experts in HBM, "
+               "Zipf 1.2 routing), hit rate"),
 }
+CACHE_SLOTS = {"cache8": 16, "cache8u": 16, "cache1": 4}
+CACHE_BATCHES = 64  # distinct resident token batches the timed steps cycle through
 
 
 def workload_shape(name):
@@ -712,6 +726,148 @@ def gpu_train_arm(args, rank, world, dist):
     print(json.dumps(line), flush=True)
 
 
+def gpu_cache_arm(args, rank, world, dist):
+    """Top-1 int4 serving through the GPU expert cache: every step routes a different
+    batch of tokens (cycling through CACHE_BATCHES resident batches), so the cache sees
+    a stream of routing results; the all-resident layer is timed on the same batches."""
+    import torch
+
+    import aux_loss_free_gb300 as M
+    from aux_loss_free_gb300.layer import ExpertCache, LayerOnDevice, to_device_tokens
+
+    M.load_library()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    name = args.workload
+    s = workload_shape(name)
+    case = WORKLOADS[name][0]
+    slots = CACHE_SLOTS[name]
+    layer = LayerOnDevice(s, make_layer(s, case, args.seed, with_tokens=False), dev)
+    cache = ExpertCache(layer, slots)
+    batches = [to_device_tokens(make_tokens(s, case, args.seed + 1000 * rank + b), dev) for b in range(CACHE_BATCHES)]
+    out0 = torch.empty(s.T, s.d, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    expert_bytes = sum(int(t.numel() * t.element_size()) // s.E for t in cache.host.values())
+
+    def run(fn, K, warm, profile=False):
+        for i in range(warm):
+            fn(batches[i % CACHE_BATCHES], out0)
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        if profile:
+            M.moe_profile_start(K + 1, 1)
+        t0 = time.time()
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            fn(batches[(warm + i) % CACHE_BATCHES], out0)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        t1 = time.time()
+        stages = M.moe_profile_stop(per_stage_calls=True) if profile else None
+        return sum(a.elapsed_time(b) for a, b in ev), stages, t0, t1
+
+    K = args.steps
+    run(lambda x, o: layer.forward(x, o, update_bias=False), 0, args.warmup)
+    res_ms, _, _, _ = run(lambda x, o: layer.forward(x, o, update_bias=False), K, 0)
+    cache.reset()
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    time.sleep(0.1)
+    for i in range(args.warmup):
+        cache.forward(batches[i % CACHE_BATCHES], out0)
+    st0, _, _, _ = cache.read()
+    if dist:
+        dist.barrier()
+    total_ms, _, tw0, tw1 = run(lambda x, o: cache.forward(x, o), K, 0)
+    st1, _, _, _ = cache.read()
+    sampler.stop()
+    # Stage times from a separate pass (each stage event adds ~2 us to the stream).
+    _, (stages_ms, stage_calls), _, _ = run(lambda x, o: cache.forward(x, o), min(K, 50), 0, profile=True)
+    if dist:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    status = M.moe_device_status()
+    # Host -> device bandwidth of a plain pinned copy: the fill path's ceiling.
+    hsrc = torch.empty(256 << 20, dtype=torch.uint8, pin_memory=True)
+    ddst = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ddst.copy_(hsrc, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(4):
+        ddst.copy_(hsrc, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    link_gbs = 4 * hsrc.numel() / (e0.elapsed_time(e1) / 1e3) / 1e9
+    # End to end: tokens in from pinned memory, output back, each step.
+    Ke = max(3, min(K, 100))
+    hxs = []
+    for b in batches:  # every step's tokens come from host memory, as served
+        h = torch.empty(s.T, s.d, dtype=b.dtype, pin_memory=True)
+        h.copy_(b.cpu())
+        hxs.append(h)
+    hx = hxs[0]
+    hout = torch.empty(s.T, s.d, dtype=torch.bfloat16, pin_memory=True)
+    din = torch.empty_like(batches[0])
+    torch.cuda.synchronize(dev)
+    ee0, ee1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ee0.record(stream)
+    for i in range(Ke):
+        din.copy_(hxs[i % CACHE_BATCHES], non_blocking=True)
+        cache.forward(din, out0)
+        hout.copy_(out0, non_blocking=True)
+    ee1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = ee0.elapsed_time(ee1) / Ke
+    if rank != 0:
+        return
+    peaks, peak_note = load_peaks()
+    hits, misses = st1["hits"] - st0["hits"], st1["misses"] - st0["misses"]
+    fill_bytes = st1["bytes"] - st0["bytes"]
+    ms_step = total_ms / K
+    fetch_ms = stages_ms.get("cache_fetch", float("nan")) / max(1, stage_calls.get("cache_fetch", 1))
+    fill_gbs = (fill_bytes / K) / (fetch_ms / 1e3) / 1e9 if fetch_ms == fetch_ms and fetch_ms > 0 else None
+    # Weight bytes a step must read: the distinct experts it uses (from HBM slots) and
+    # the shared expert, as in the serving workloads' HBM roofline.
+    used_per_step = (hits + misses) / K
+    flops, _ = layer_algorithmic(s)
+    nbytes = int(used_per_step * (3 * s.d * s.f // 2 + 3 * s.d * s.f // 32 * 2) + 3 * s.d * s.F * 2
+                 + s.E * s.d * 4 + 4 * s.T * s.d)
+    line = {
+        "metric": WORKLOADS[name][3], "value": world * s.T * K / (total_ms / 1e3), "unit": "tokens/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int4 weights, bf16 activations", "data": "synthetic",
+        "config": dict(config_block(name, world), slots=slots, token_batches=CACHE_BATCHES,
+                       weights="int4 experts in pinned host memory, slots in HBM"),
+        "cache": {"hit_rate": hits / max(1, hits + misses), "hits": hits, "misses": misses,
+                  "evictions": st1["evictions"] - st0["evictions"], "bytes_per_step": fill_bytes / K,
+                  "expert_bytes": expert_bytes, "fetch_us_per_step": fetch_ms * 1e3,
+                  "resident_us_per_step": res_ms / K * 1e3,
+                  "overflow": st1["overflow"] - st0["overflow"]},
+        "roofline": {"kernel": "cache fill (plan + copy kernels, host memory -> HBM slots)", "bound": "link",
+                     "achieved": fill_gbs, "peak": link_gbs, "unit": "GB/s",
+                     "frac": (fill_gbs / link_gbs) if fill_gbs else None, "traffic": None,
+                     "peak_note": "of a pinned host-to-device copy measured in this run"},
+        "layer_roofline": {"bytes_per_step": nbytes, "roofline_us": nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6,
+                           "measured_us": ms_step * 1e3,
+                           "frac": nbytes / (peaks["hbm_gbs"] * 1e9) / (ms_step / 1e3), "peak": peak_note,
+                           "bound": "hbm"},
+        "stages_us": {k: v * 1e3 / max(1, stage_calls.get(k, 1)) for k, v in stages_ms.items()},
+        "e2e": {"value": world * s.T / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(hx.numel() * hx.element_size()),
+                "d2h_bytes_per_step": int(hout.numel() * hout.element_size()),
+                "copies": "tokens in from pinned memory and the output back on the compute stream"},
+        "gpu_launches": K * (kernels_per_call(s) + 2),
+        "clocks": sampler.summary(tw0, tw1),
+        "device_status": status,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(name, args.seed, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -730,7 +886,9 @@ def main():
         tdist.init_process_group("nccl")
         dist = tdist
     try:
-        (gpu_train_arm if args.workload == "train" else gpu_arm)(args, rank, world, dist)
+        arm = gpu_train_arm if args.workload == "train" else (
+            gpu_cache_arm if args.workload in CACHE_SLOTS else gpu_arm)
+        arm(args, rank, world, dist)
     finally:
         if dist:
             dist.destroy_process_group()
