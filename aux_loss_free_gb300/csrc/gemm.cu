@@ -25,6 +25,12 @@
 //       COMBINE out = acc + residual + sum_j gate_j * y_perm[inv_pos_j] (the shared
 //               expert's down projection adds the same token's routed outputs:
 //               the layer's combine step).
+// A third, chained operand set may follow the other two in the same launch: routed
+// groups whose A operand is the routed set's output (the down projection reading the
+// h rows the gate/up tiles write).  Its tiles come after all others; each waits until
+// every gate/up tile of its 256-row block has published its rows (a per-block counter:
+// each epilogue warp fences its stores and adds one), so the down projection starts
+// on pairs that are done with their gate/up work instead of after the launch ends.
 // Every barrier wait is bounded (ptx.cuh); on a timeout the CTA records it in the
 // status word, the pair drains its in-flight copies and MMAs, frees TMEM and exits.
 #include <cuda_bf16.h>
@@ -83,6 +89,12 @@ struct OperandSet {
 struct Params {
   OperandSet shared;
   OperandSet routed;
+  // Chained set (enabled or not): routed groups over the same offsets, A = the routed
+  // set's output.  dep[m] counts the epilogue warps that have published routed 256-row
+  // block m; a chained tile of block m waits for dep_target of them.
+  OperandSet chain;
+  int* dep;
+  int dep_target;
   const int32_t* offsets;
   const uint16_t* y_perm;
   const int32_t* inv_pos;
@@ -112,6 +124,7 @@ struct Tile {
   int klen;   // K columns
   int group;  // K group (K-grouped sets; else 0)
   int bk;     // first K row of the group's B (MN-major B of an M-grouped set)
+  int mblk;   // routed 256-row block index (routed and chained tiles)
 };
 
 // ---------------------------------------------------------------- cluster PTX
@@ -209,8 +222,39 @@ __device__ __forceinline__ void commit_pair_local(uint32_t bar) {
 // Tile order: with both operand sets present, shared-expert tiles (compute bound)
 // and routed tiles (which stream expert weights from DRAM) are interleaved evenly,
 // so every stretch of the launch mixes the two; each set keeps its own order.
+// Largest group g with s_cum[g] <= r (that group is non-empty).
+__device__ __forceinline__ int find_group(const int* s_cum, int E, int r) {
+  int lo = 0, hi = E;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_cum[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// `total` here is the end of the shared and routed tiles; chained tiles follow it.
 __device__ __forceinline__ Tile decode_tile(const Params& p, int tile, int shared_tiles,
                                             const int* s_off, const int* s_cum, int total) {
+  if (tile >= total) {
+    // Chained tile: routed 256-row block m (the same blocks as the routed set's, whose
+    // tile table counts nt1 tiles per block), column tile n.
+    const int nt1 = p.routed.n_total / p.routed.bn, nt2 = p.chain.n_total / p.chain.bn;
+    const int r = tile - total;
+    const int m = r / nt2, n = r % nt2;
+    const int g = find_group(s_cum, p.E, m * nt1);
+    Tile t;
+    t.set = 2;
+    t.row0 = s_off[g] + (m - s_cum[g] / nt1) * BM;
+    t.rend = s_off[g + 1];
+    t.n0 = n * p.chain.bn;
+    t.brow = g * p.chain.n_total + t.n0;
+    t.k0 = 0;
+    t.klen = p.chain.k_total;
+    t.group = 0;
+    t.bk = g * p.chain.k_total;
+    t.mblk = m;
+    return t;
+  }
   const int routed_tiles = total - shared_tiles;
   if (shared_tiles > 0 && routed_tiles > 0) {
     // 32-bit arithmetic (tile counts stay far below 2^15).
@@ -222,6 +266,7 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, int tile, int share
   t.k0 = 0;
   t.group = 0;
   t.bk = 0;
+  t.mblk = 0;
   if (tile < shared_tiles) {
     const int nt = p.shared.n_total / p.shared.bn;
     const int m = tile / nt, n = tile % nt;
@@ -246,12 +291,7 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, int tile, int share
     t.klen = s_off[g + 1] - s_off[g];
   } else {
     const int r = tile - shared_tiles;
-    int lo = 0, hi = p.E;  // largest g with s_cum[g] <= r (that group is non-empty)
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_cum[mid] <= r) lo = mid; else hi = mid - 1;
-    }
-    const int g = lo;
+    const int g = find_group(s_cum, p.E, r);
     const int nt = p.routed.n_total / p.routed.bn;
     const int local = r - s_cum[g];
     const int m = local / nt, n = local % nt;
@@ -262,6 +302,7 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, int tile, int share
     t.brow = g * p.routed.n_total + t.n0;
     t.bk = g * p.routed.k_total;
     t.klen = p.routed.k_total;
+    t.mblk = r / nt;  // s_cum[g] is a multiple of nt
   }
   return t;
 }
@@ -269,6 +310,7 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, int tile, int share
 // Which operand set a tile belongs to (1 = routed), by the same interleave as
 // decode_tile: all the MMA issuer needs, without the search over the groups.
 __device__ __forceinline__ int tile_set(int tile, int shared_tiles, int total) {
+  if (tile >= total) return 2;
   const int routed_tiles = total - shared_tiles;
   if (shared_tiles > 0 && routed_tiles > 0) {
     const unsigned r_before = (unsigned)tile * (unsigned)routed_tiles / (unsigned)total;
@@ -363,6 +405,26 @@ __device__ __forceinline__ void store_bf16_row32(uint16_t* dst, const float (&o)
   }
 }
 
+// Waits (acquire, at GPU scope) until *ctr >= target, then orders this thread's later
+// TMA reads (async proxy) after the generic-proxy stores the counter published.
+// Bounded like the barrier waits.
+__device__ __forceinline__ bool dep_wait(const int* ctr, int target, int* status) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (true) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= target) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      return true;
+    }
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(status, kDevTimeout);
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -375,6 +437,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   __shared__ int s_off[kMaxE + 1];
   __shared__ int s_cum[kMaxE + 1];
   __shared__ int s_total;
+  __shared__ int s_t1;  // end of the shared and routed tiles (chained tiles follow)
 
   const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -402,6 +465,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     if (p.routed.enabled) {
       tma_prefetch_desc(&p.routed.a);
       tma_prefetch_desc(&p.routed.b);
+    }
+    if (p.chain.enabled) {
+      tma_prefetch_desc(&p.chain.a);
+      tma_prefetch_desc(&p.chain.b);
     }
   }
   if (warp == 1) {
@@ -447,13 +514,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       }
       if (lane == 0) s_cum[p.E] = carry;
     }
-    if (lane == 0) s_total = shared_tiles + carry;
+    if (lane == 0) {
+      // Chained tiles: one row of nt2 column tiles per routed 256-row block.
+      const int chained = (p.chain.enabled && p.routed.enabled && !p.kgroup)
+                              ? carry / (p.routed.n_total / p.routed.bn) * (p.chain.n_total / p.chain.bn)
+                              : 0;
+      s_t1 = shared_tiles + carry;
+      s_total = shared_tiles + carry + chained;
+    }
   }
   tc_fence_before();
   cluster_sync();  // barriers of both CTAs are initialised before any remote use
   tc_fence_after();
   const uint32_t tmem_base = tmem_holder;
-  const int total = s_total;
+  const int total = s_total, t1 = s_t1;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -465,9 +539,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       // now, into the empty ring; after the wait its first `pre` k-blocks load A only.
       int pre = 0;
       if (p.early) {
-        if (cluster < total) {
-          const Tile t = decode_tile(p, cluster, shared_tiles, s_off, s_cum, total);
-          const OperandSet& S = t.set ? p.routed : p.shared;
+        if (cluster < t1) {
+          const Tile t = decode_tile(p, cluster, shared_tiles, s_off, s_cum, t1);
+          const OperandSet& S = t.set == 2 ? p.chain : (t.set ? p.routed : p.shared);
           const int nkb = (t.klen + BK - 1) / BK;
           const int half = S.bn / 2;
           if (S.kblock) {
@@ -487,8 +561,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         pdl_trigger();
       }
       for (int tile = cluster; tile < total && ok; tile += nclusters) {
-        const Tile t = decode_tile(p, tile, shared_tiles, s_off, s_cum, total);
-        const OperandSet& S = t.set ? p.routed : p.shared;
+        const Tile t = decode_tile(p, tile, shared_tiles, s_off, s_cum, t1);
+        const OperandSet& S = t.set == 2 ? p.chain : (t.set ? p.routed : p.shared);
+        // A chained tile's A rows are written by this launch's gate/up tiles.
+        if (t.set == 2 && !dep_wait(p.dep + t.mblk, p.dep_target, p.status)) {
+          ok = false;
+          break;
+        }
         const int nkb = (t.klen + BK - 1) / BK;  // 0 for an empty K group: nothing loaded
         const int half = S.bn / 2;
         const int katom0 = t.k0 / AK;
@@ -556,15 +635,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = cluster; tile < total && ok; tile += nclusters) {
-        const int set = tile_set(tile, shared_tiles, total);
-        int k_total = set ? p.routed.k_total : p.shared.k_total;
-        if (set && p.kgroup) {  // this tile's K group
-          k_total = decode_tile(p, tile, shared_tiles, s_off, s_cum, total).klen;
+        const int set = tile_set(tile, shared_tiles, t1);
+        int k_total = set == 2 ? p.chain.k_total : (set ? p.routed.k_total : p.shared.k_total);
+        if (set == 1 && p.kgroup) {  // this tile's K group
+          k_total = decode_tile(p, tile, shared_tiles, s_off, s_cum, t1).klen;
           if (k_total == 0) continue;  // empty group: no MMA, no accumulator hand-off
         }
-        const int bn = set ? p.routed.bn : p.shared.bn;
-        const int a_mn = set ? p.routed.a_mn : p.shared.a_mn;
-        const int b_mn = set ? p.routed.b_mn : p.shared.b_mn;
+        const int bn = set == 2 ? p.chain.bn : (set ? p.routed.bn : p.shared.bn);
+        const int a_mn = set == 2 ? p.chain.a_mn : (set ? p.routed.a_mn : p.shared.a_mn);
+        const int b_mn = set == 2 ? p.chain.b_mn : (set ? p.routed.b_mn : p.shared.b_mn);
         const int nkb = (k_total + BK - 1) / BK;
         const int nkk_last = (k_total - (nkb - 1) * BK + 15) / 16;
         const uint32_t b_atom = (uint32_t)bn / 2 * AK * 2;
@@ -623,8 +702,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     uint32_t acc_phase = 0;
     if (p.early) pdl_wait();  // outputs and epilogue inputs belong to earlier kernels
     for (int tile = cluster; tile < total; tile += nclusters) {
-      const Tile t = decode_tile(p, tile, shared_tiles, s_off, s_cum, total);
-      const OperandSet& S = t.set ? p.routed : p.shared;
+      const Tile t = decode_tile(p, tile, shared_tiles, s_off, s_cum, t1);
+      const OperandSet& S = t.set == 2 ? p.chain : (t.set ? p.routed : p.shared);
       if (t.klen == 0) {
         // Empty K group (an expert without tokens): the issuer skipped it; its fp32
         // output is zero.
@@ -786,7 +865,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster_relaxed(acc ? tempty_leader1 : tempty_leader0);
+      if (lane == 0) {
+        mbar_arrive_cluster_relaxed(acc ? tempty_leader1 : tempty_leader0);
+        // Publish the warp's rows of a routed tile to the chained tiles: the stores
+        // above (ordered before this lane by the warp barrier), then the count.
+        if (t.set == 1 && p.dep) {
+          __threadfence();
+          atomicAdd(p.dep + t.mblk, 1);
+        }
+      }
 
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
@@ -941,13 +1028,25 @@ int gemm_max_pairs() {
 cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* offsets, int E,
                                 const GemmOperandSet& shared, const CombineInputs& comb,
                                 long long max_routed_rows, cudaStream_t s, int* bad_arg,
-                                int max_pairs, long long kgroup_stride, int early) {
+                                int max_pairs, long long kgroup_stride, int early,
+                                const GemmOperandSet* chain, int32_t* dep) {
   Params p;
   std::memset(&p, 0, sizeof(p));
   *bad_arg = 0;
-  if (!fill_set(p.shared, shared) || !fill_set(p.routed, routed)) {
+  if (!fill_set(p.shared, shared) || !fill_set(p.routed, routed) ||
+      (chain && !fill_set(p.chain, *chain))) {
     *bad_arg = 1;
     return cudaErrorInvalidValue;
+  }
+  if (p.chain.enabled) {
+    // The chained set reads the routed set's output rows block by block.
+    if (!p.routed.enabled || kgroup_stride > 0 || !dep || chain->groups != E ||
+        chain->a != routed.out || chain->K != routed.ldo || routed.mode != EPI_SWIGLU) {
+      *bad_arg = 1;
+      return cudaErrorInvalidValue;
+    }
+    p.dep = dep;
+    p.dep_target = (p.routed.n_total / p.routed.bn) * 2 * EPI_WARPS;
   }
   if (!p.shared.enabled && !p.routed.enabled) return cudaSuccess;
   p.offsets = offsets;
@@ -974,6 +1073,8 @@ cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* off
     tiles += (long long)E * ((p.routed.rows + BM - 1) / BM) * (p.routed.n_total / p.routed.bn);
   else if (p.routed.enabled)
     tiles += ((max_routed_rows + BM - 1) / BM + E) * (long long)(p.routed.n_total / p.routed.bn);
+  if (p.chain.enabled)
+    tiles += ((max_routed_rows + BM - 1) / BM + E) * (long long)(p.chain.n_total / p.chain.bn);
   int cap = max_active_pairs();
   if (max_pairs > 0 && max_pairs < cap) cap = max_pairs;
   const int pairs = (int)std::min<long long>(cap, std::max<long long>(tiles, 1));

@@ -145,10 +145,16 @@ struct CombineInputs {
 // early: the caller guarantees that the offsets and both sets' B operands were
 // complete before the previous kernel in the stream started (the launch then reads
 // them before its dependency wait).
+// chain (nullable): a third set over the same E groups and offsets whose A is the
+// routed set's output (an EPI_SWIGLU set: chain->a == routed.out, chain->K ==
+// routed.ldo); its tiles run after the others in the same launch, each once the
+// routed tiles of its 256-row block have written their rows.  dep: one zeroed int32
+// per routed 256-row block (max_routed_rows / 256 + E + 1 suffice), left non-zero.
 cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* offsets, int E,
                                 const GemmOperandSet& shared, const CombineInputs& comb,
                                 long long max_routed_rows, cudaStream_t s, int* bad_arg,
-                                int max_pairs = 0, long long kgroup_stride = 0, int early = 0);
+                                int max_pairs = 0, long long kgroup_stride = 0, int early = 0,
+                                const GemmOperandSet* chain = nullptr, int32_t* dep = nullptr);
 // Number of co-resident 2-SM clusters of the grouped GEMM on the current device.
 int gemm_max_pairs();
 

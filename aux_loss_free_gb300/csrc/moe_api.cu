@@ -181,6 +181,7 @@ struct FfnWs {
   uint16_t* h;   // [T*k][f]
   uint16_t* hs;  // [T][F]
   uint16_t* xb;  // [T][d] bf16 copy of fp32 x
+  int32_t* dep;  // [T*k / 256 + E + 1] per routed 256-row block: h rows published
 };
 FfnWs carve_ffn(Carver& c, const moe_shape_t* s) {
   const size_t Tk = (size_t)s->T * s->k;
@@ -189,6 +190,7 @@ FfnWs carve_ffn(Carver& c, const moe_shape_t* s) {
   w.h = static_cast<uint16_t*>(c.take(2 * Tk * s->f));
   w.hs = s->F ? static_cast<uint16_t*>(c.take(2 * (size_t)s->T * s->F)) : nullptr;
   w.xb = s->x_dtype == MOE_X_F32 ? static_cast<uint16_t*>(c.take(2 * (size_t)s->T * s->d)) : nullptr;
+  w.dep = static_cast<int32_t*>(c.take(4 * (Tk / 256 + s->E + 1)));
   return w;
 }
 
@@ -256,20 +258,28 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x_bf16, const int32_t* of
                         EPI_SWIGLU, s->T};
   else if (s->F)
     s1 = sd;
-  if (mark) prof_mark(shared_gate_up_done ? "routed_gate_up_shared_down" : "gemm_gate_up", st);
-  cudaError_t e = launch_grouped_gemm(r1, offsets, s->E, s1, none, Tk, st, &bad);
+  GemmOperandSet r2{ws.h, Tk, w->w_down, s->E, s->d, s->f, y_perm, s->d, EPI_STORE, 0};
+  // With the shared gate/up done, the routed down projection is chained into the same
+  // launch (its tiles follow the others and start block by block as h is written;
+  // ws.dep was zeroed by the caller); otherwise it shares a second launch with the
+  // shared down projection.
+  const bool chained = s->F && shared_gate_up_done;
+  if (mark) prof_mark(chained ? "routed_ffn_shared_down" : "gemm_gate_up", st);
+  cudaError_t e = launch_grouped_gemm(r1, offsets, s->E, s1, none, Tk, st, &bad, 0, 0, 0,
+                                      chained ? &r2 : nullptr, chained ? ws.dep : nullptr);
   if (bad) return MOE_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
-  GemmOperandSet r2{ws.h, Tk, w->w_down, s->E, s->d, s->f, y_perm, s->d, EPI_STORE, 0};
-  GemmOperandSet s2{};
-  if (s->F && !shared_gate_up_done) s2 = sd;
-  if (mark) prof_mark(shared_gate_up_done ? "routed_down" : "gemm_down", st);
-  // The offsets come from before the gate/up launch and B is weights: the down launch
-  // may start its tile table and weight copies before its dependency wait.
-  e = launch_grouped_gemm(r2, offsets, s->E, s2, none, Tk, st, &bad, 0, 0, /*early=*/1);
-  if (bad) return MOE_ERR_UNSUPPORTED;
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (!chained) {
+    GemmOperandSet s2{};
+    if (s->F && !shared_gate_up_done) s2 = sd;
+    if (mark) prof_mark(shared_gate_up_done ? "routed_down" : "gemm_down", st);
+    // The offsets come from before the gate/up launch and B is weights: the down launch
+    // may start its tile table and weight copies before its dependency wait.
+    e = launch_grouped_gemm(r2, offsets, s->E, s2, none, Tk, st, &bad, 0, 0, /*early=*/1);
+    if (bad) return MOE_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
   if (comb) {
     if (mark) prof_mark("combine", st);
     e = launch_combine(y_perm, s->F ? shared_out : nullptr, comb->inv_pos, comb->gate,
@@ -656,6 +666,10 @@ moe_status_t layer_fwd_impl(const moe_shape_t* shape, const void* x, const float
     if (!adjacent && cudaMemsetAsync(L.load, 0, sizeof(int32_t) * E, rs) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
+  // The chained down projection's block counters (run_ffn after the fork).
+  if (fork && cudaMemsetAsync(L.ffn.dep, 0, sizeof(int32_t) * ((size_t)T * k / 256 + E + 1), rs) !=
+                  cudaSuccess)
+    return MOE_ERR_CUDA;
   RouterArgs ra{x, xf, w_router, logit_offset, bias, dbg ? dbg->scores : nullptr, L.idx, L.gate,
                 L.load, L.perm.counts, ct, T, shape->d, E, k, shape->renorm};
   cudaError_t e = run_router(ra, L.router, rs);

@@ -62,9 +62,10 @@ def kernels_per_call(s):
             return router + 2 + (2 if s.F else 1)
         # permute, shared gate/up, int4 gate/up, int4 down, shared down + combine
         return router + 1 + (4 if s.F else 2) + (0 if s.F else 1)
-    # permute, gate/up (one or two launches), down, combine
-    fork = s.x_dtype == "bf16" and s.F > 0 and s.T >= 1024
-    return router + 1 + (2 if fork else 1) + 1 + 1
+    # permute, then either the shared gate/up (second stream) and one launch with the
+    # routed gate/up, shared down and the chained routed down, or a gate/up launch and a
+    # down launch; combine
+    return router + 1 + 2 + 1
 
 
 # Kernels one moe_layer_bwd launches: padded layout with the row gather, five grouped GEMMs
