@@ -61,7 +61,12 @@ constexpr int EPI_GROUPS = EPI_WARPS / 4;  // warps per TMEM lane quadrant
 constexpr int CS = 32 * EPI_GROUPS;        // column stride between one warp's chunks
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 2 * BN_MAX;
-constexpr int DYN_SMEM = STAGES * STAGE_BYTES + 1024;
+// EPI_SWIGLU_BWD stages dh through shared memory: per epilogue warp two buffers of its
+// 32 rows x 32 columns (bf16), filled by TMA.
+constexpr int DH_COLS = 32;
+constexpr int DH_BUF = 32 * DH_COLS * 2;                 // 2 KB
+constexpr int DH_BYTES = EPI_WARPS * 2 * DH_BUF;         // 16 KB
+constexpr int DYN_SMEM = STAGES * STAGE_BYTES + DH_BYTES + 1024;
 constexpr unsigned FULL = 0xFFFFFFFFu;
 
 struct OperandSet {
@@ -80,7 +85,9 @@ struct OperandSet {
   // MN-major operands: the map views [K rows][M or N] as (64 elements, K rows, atoms
   // of 64 along M/N), box (64, BK, atoms per CTA), one copy per operand per k-block.
   int a_mn, b_mn;
-  // EPI_SWIGLU_BWD operands (see GemmOperandSet).
+  // EPI_SWIGLU_BWD operands (see GemmOperandSet); dhm views dh as [rows][n_total / 2]
+  // with a 32 x 32 box.
+  CUtensorMap dhm;
   uint16_t* dh;
   const float* gperm;
   float* dgpart;
@@ -433,6 +440,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   __shared__ __align__(8) uint64_t tfull_bar[2];       // both CTAs
   __shared__ __align__(8) uint64_t tempty_bar[2];      // used in the leader
   __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ __align__(8) uint64_t dh_bar[EPI_WARPS][2];  // dh staging buffers
   __shared__ uint32_t tmem_holder;
   __shared__ int s_off[kMaxE + 1];
   __shared__ int s_cum[kMaxE + 1];
@@ -457,6 +465,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       mbar_init(smem_u32(&tempty_bar[a]), 2 * EPI_WARPS);
     }
     mbar_init(smem_u32(&drain_bar), 1);
+    for (int w = 0; w < EPI_WARPS; ++w) {
+      mbar_init(smem_u32(&dh_bar[w][0]), 1);
+      mbar_init(smem_u32(&dh_bar[w][1]), 1);
+    }
     fence_mbar_init();
     if (p.shared.enabled) {
       tma_prefetch_desc(&p.shared.a);
@@ -470,6 +482,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       tma_prefetch_desc(&p.chain.a);
       tma_prefetch_desc(&p.chain.b);
     }
+    if (p.shared.mode == EPI_SWIGLU_BWD && p.shared.enabled) tma_prefetch_desc(&p.shared.dhm);
+    if (p.routed.mode == EPI_SWIGLU_BWD && p.routed.enabled) tma_prefetch_desc(&p.routed.dhm);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(&tmem_holder), TMEM_COLS);
@@ -700,6 +714,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tempty_leader1 = map_to_rank(smem_u32(&tempty_bar[1]), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
+    uint32_t dh_par = 0;  // parity of this warp's two dh buffers
+    const uint32_t dh_stage = ring + STAGES * STAGE_BYTES + (uint32_t)(warp - 2) * 2 * DH_BUF;
     if (p.early) pdl_wait();  // outputs and epilogue inputs belong to earlier kernels
     for (int tile = cluster; tile < total; tile += nclusters) {
       const Tile t = decode_tile(p, tile, shared_tiles, s_off, s_cum, t1);
@@ -749,47 +765,84 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const float g = (valid && S.gperm) ? S.gperm[orow] : 1.0f;
         uint16_t* dhr = S.dh + orow * w + t.n0 / 2;
         uint16_t* o = out + orow * S.ldo + t.n0;
-        float dot = 0.f;
-        for (int c = 16 * colh; c < half; c += 16 * EPI_GROUPS) {
+        // The element math runs on column pairs with the packed fp32x2 instructions
+        // (the exponential and the reciprocal per element).
+        const float2 one2 = make_float2(1.0f, 1.0f), g2 = make_float2(g, g);
+        float2 dot2 = make_float2(0.f, 0.f);
+        auto chunk = [&](int c, const uint4 (&u)[2]) {
           uint32_t va[16], vb[16];
           tmem_ld16(tbase + c, va);
           tmem_ld16(tbase + half + c, vb);
-          uint4 u[2];
-          if (valid) {
-            u[0] = __ldcg(reinterpret_cast<const uint4*>(dhr + c));
-            u[1] = __ldcg(reinterpret_cast<const uint4*>(dhr + c) + 1);
-          }
           tmem_wait_ld();
-          if (valid) {
-            uint32_t pa[8], pb[8], ph[8];
+          if (!valid) return;
+          uint32_t pa[8], pb[8], ph[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint32_t dw = reinterpret_cast<const uint32_t*>(u)[i];
-              float da2[2], db2[2], h2[2];
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t dw = reinterpret_cast<const uint32_t*>(u)[i];
+            const float2 a = make_float2(__uint_as_float(va[2 * i]), __uint_as_float(va[2 * i + 1]));
+            const float2 b = make_float2(__uint_as_float(vb[2 * i]), __uint_as_float(vb[2 * i + 1]));
+            const float2 dh = make_float2(__uint_as_float(dw << 16), __uint_as_float(dw & 0xFFFF0000u));
+            const float2 den = __fadd2_rn(one2, make_float2(__expf(-a.x), __expf(-a.y)));
+            const float2 sig = make_float2(__fdividef(1.0f, den.x), __fdividef(1.0f, den.y));
+            const float2 sa = __fmul2_rn(a, sig);                       // silu(a)
+            const float2 h = __fmul2_rn(sa, b);
+            dot2 = __ffma2_rn(dh, h, dot2);
+            const float2 dhg = __fmul2_rn(g2, dh);
+            // silu'(a) = sig (1 + a (1 - sig))
+            const float2 oms = __ffma2_rn(sig, make_float2(-1.0f, -1.0f), one2);
+            const float2 ds = __fmul2_rn(sig, __ffma2_rn(a, oms, one2));
+            const float2 da = __fmul2_rn(__fmul2_rn(dhg, b), ds);
+            const float2 db = __fmul2_rn(dhg, sa);
+            const float2 gh = __fmul2_rn(g2, h);
+            pa[i] = pack_bf16x2(da.x, da.y);
+            pb[i] = pack_bf16x2(db.x, db.y);
+            ph[i] = pack_bf16x2(gh.x, gh.y);
+          }
+          store_packed16(o + c, pa, S.v8);
+          store_packed16(o + half + c, pb, S.v8);
+          store_packed16(dhr + c, ph, S.v8h);
+        };
+        // dh arrives by TMA, 32 rows x 32 columns per piece into this warp's two shared
+        // buffers, one piece ahead: read row by row from global memory, each thread's
+        // loads (32 rows per warp instruction) beside its stores cost the epilogue more
+        // than its math.
+        static_assert(EPI_GROUPS == 1, "one epilogue warp per TMEM lane quadrant");
+        const int pieces = half / DH_COLS;  // half is 32, 64 or 128
+        const int wrow = t.row0 + HM * (int)rank + q * 32;
+        auto issue = [&](int pc) {
+          const uint32_t bar = smem_u32(&dh_bar[warp - 2][pc & 1]);
+          mbar_arrive_expect_tx(bar, DH_BUF);
+          tma_load_2d(dh_stage + (pc & 1) * DH_BUF, &S.dhm, bar, t.n0 / 2 + pc * DH_COLS, wrow);
+        };
+        if (lane == 0) {
+          issue(0);
+          if (pieces > 1) issue(1);
+        }
+        bool dh_ok = true;
+        for (int pc = 0; pc < pieces && dh_ok; ++pc) {
+          const int b = pc & 1;
+          dh_ok = mbar_wait(smem_u32(&dh_bar[warp - 2][b]), (dh_par >> b) & 1u, p.status);
+          dh_par ^= 1u << b;
+          if (!dh_ok) break;
+          const uint32_t row = dh_stage + b * DH_BUF + lane * (DH_COLS * 2);
 #pragma unroll
-              for (int hlf = 0; hlf < 2; ++hlf) {
-                const float a = __uint_as_float(va[2 * i + hlf]);
-                const float b = __uint_as_float(vb[2 * i + hlf]);
-                const float dh = __uint_as_float(hlf ? (dw & 0xFFFF0000u) : (dw << 16));
-                const float sig = __fdividef(1.0f, 1.0f + __expf(-a));
-                const float sa = a * sig;
-                const float h = sa * b;
-                dot = fmaf(dh, h, dot);
-                const float dhg = g * dh;
-                da2[hlf] = dhg * b * (sig * (1.0f + a * (1.0f - sig)));
-                db2[hlf] = dhg * sa;
-                h2[hlf] = g * h;
-              }
-              pa[i] = pack_bf16x2(da2[0], da2[1]);
-              pb[i] = pack_bf16x2(db2[0], db2[1]);
-              ph[i] = pack_bf16x2(h2[0], h2[1]);
-            }
-            store_packed16(o + c, pa, S.v8);
-            store_packed16(o + half + c, pb, S.v8);
-            store_packed16(dhr + c, ph, S.v8h);
+          for (int sub = 0; sub < 2; ++sub) {
+            uint4 u[2];
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(u[0].x), "=r"(u[0].y), "=r"(u[0].z), "=r"(u[0].w) : "r"(row + sub * 32));
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(u[1].x), "=r"(u[1].y), "=r"(u[1].z), "=r"(u[1].w) : "r"(row + sub * 32 + 16));
+            chunk(pc * DH_COLS + sub * 16, u);
+          }
+          // Every lane has read buffer b: the next piece may overwrite it.
+          __syncwarp();
+          if (lane == 0 && pc + 2 < pieces) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(pc + 2);
           }
         }
-        if (valid && S.dgpart) S.dgpart[orow * (S.n_total / S.bn) + t.n0 / S.bn] = dot;
+        if (!dh_ok) break;
+        if (valid && S.dgpart) S.dgpart[orow * (S.n_total / S.bn) + t.n0 / S.bn] = dot2.x + dot2.y;
       } else if (S.mode == EPI_STORE_F32) {
         // fp32 output (weight gradients); K groups write their own matrices.  Two
         // 32-column chunks per TMEM round trip; 256-bit stores (whole 32-byte sectors,
@@ -981,7 +1034,20 @@ bool fill_set(OperandSet& t, const GemmOperandSet& o) {
   t.dgpart = o.dgpart;
   // 256-bit stores of the h-width rows (EPI_SWIGLU_BWD's dh) need 32-byte alignment too.
   t.v8h = (reinterpret_cast<uintptr_t>(o.dh) % 32 == 0) && ((long long)o.N / 2 * 2) % 32 == 0;
-  if (o.mode == EPI_SWIGLU_BWD && !o.dh) return false;
+  if (o.mode == EPI_SWIGLU_BWD) {
+    // dh [a_rows][N / 2], 32 x 32 boxes at 32-column offsets (64-byte aligned).
+    if (!o.dh || (o.N / 2) % DH_COLS != 0) return false;
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(o.N / 2), static_cast<cuuint64_t>(o.a_rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(o.N / 2) * 2};
+    const cuuint32_t box[2] = {DH_COLS, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    if (fn(&t.dhm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o.dh, dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
   const int esize = o.mode == EPI_STORE_F32 ? 4 : 2;
   t.v8 = (reinterpret_cast<uintptr_t>(o.out) % 32 == 0) && ((long long)o.ldo * esize) % 32 == 0;
   if (o.N % t.bn != 0) return false;
