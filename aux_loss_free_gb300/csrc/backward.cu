@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(256) pad_gather_kernel(
 //   dg_j = sum of the pair's partial <dh, h> (in order), ds_j = (dg_j - sum_i dg_i g_i)
 //   / S with S the sum of the winners' scores (renormalised gates) or dg_j (raw),
 //   dz_j = ds_j s_j (1 - s_j) -> dzp[padded row of pair j],
-//   dx_t = dxs_t + sum_j (dxp[padded row j] + dz_j W_r[e_j]) (+ dout_t),
+//   dx_t = dxs_t (+ dxs2_t) + sum_j (dxp[padded row j] + dz_j W_r[e_j]) (+ dout_t),
 // summed in fp32 (16-byte loads, 8 columns a lane), rounded once to bf16.  dgate
 // (optional) receives dg per pair.
 // KT: pairs held in registers (k <= KT).
@@ -131,7 +131,8 @@ __global__ void router_bwd_dx_kernel(const int32_t* __restrict__ idx, const floa
                                      const float* __restrict__ scores, const int32_t* __restrict__ inv_pad,
                                      const float* __restrict__ dgp, int nparts,
                                      const float* __restrict__ w_router, const uint16_t* __restrict__ dxp,
-                                     const uint16_t* __restrict__ dxs, const uint16_t* __restrict__ dout,
+                                     const uint16_t* __restrict__ dxs, const uint16_t* __restrict__ dxs2,
+                                     const uint16_t* __restrict__ dout,
                                      int T, int d, int E, int k, int renorm, float* __restrict__ dzp,
                                      float* __restrict__ dgate, uint16_t* __restrict__ dx) {
   const int lane = threadIdx.x % 32;
@@ -169,13 +170,14 @@ __global__ void router_bwd_dx_kernel(const int32_t* __restrict__ idx, const floa
   for (int c0 = 8 * lane; c0 < d; c0 += 512) {
     const bool two = c0 + 256 < d;  // lane-dependent when d is not a multiple of 512
     float v[2][8];
-    uint4 u_s[2], u_d[2], u_p[2][KT];
+    uint4 u_s[2], u_s2[2], u_d[2], u_p[2][KT];
     float4 w_r[2][KT][2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int c = c0 + 256 * h;
       if (h == 1 && !two) break;
       if (dxs) u_s[h] = __ldg(reinterpret_cast<const uint4*>(dxs + (size_t)t * d + c));
+      if (dxs2) u_s2[h] = __ldg(reinterpret_cast<const uint4*>(dxs2 + (size_t)t * d + c));
       if (dout) u_d[h] = __ldg(reinterpret_cast<const uint4*>(dout + (size_t)t * d + c));
 #pragma unroll
       for (int j = 0; j < KT; ++j) {
@@ -201,6 +203,7 @@ __global__ void router_bwd_dx_kernel(const int32_t* __restrict__ idx, const floa
         }
       };
       if (dxs) add8(u_s[h]);
+      if (dxs2) add8(u_s2[h]);
 #pragma unroll
       for (int j = 0; j < KT; ++j) {
         if (j >= k) break;
@@ -304,16 +307,17 @@ cudaError_t launch_pad_gather(const int32_t* off, const int32_t* perm_tok, const
 
 cudaError_t launch_router_bwd_dx(const int32_t* idx, const float* gate, const float* scores,
                                  const int32_t* inv_pad, const float* dgp, int nparts, const float* w_router,
-                                 const uint16_t* dxp, const uint16_t* dxs, const uint16_t* dout, int T,
+                                 const uint16_t* dxp, const uint16_t* dxs, const uint16_t* dxs2,
+                                 const uint16_t* dout, int T,
                                  int d, int E, int k, int renorm, float* dzp, float* dgate, uint16_t* dx,
                                  cudaStream_t s) {
   const unsigned blocks = (unsigned)((T + 7) / 8);
   if (k <= 2)
     router_bwd_dx_kernel<2><<<blocks, 256, 0, s>>>(idx, gate, scores, inv_pad, dgp, nparts, w_router, dxp, dxs,
-                                                   dout, T, d, E, k, renorm, dzp, dgate, dx);
+                                                   dxs2, dout, T, d, E, k, renorm, dzp, dgate, dx);
   else
     router_bwd_dx_kernel<kMaxK><<<blocks, 256, 0, s>>>(idx, gate, scores, inv_pad, dgp, nparts, w_router, dxp,
-                                                       dxs, dout, T, d, E, k, renorm, dzp, dgate, dx);
+                                                       dxs, dxs2, dout, T, d, E, k, renorm, dzp, dgate, dx);
   return cudaGetLastError();
 }
 

@@ -60,6 +60,7 @@ constexpr int EPI_WARPS = 4;
 constexpr int EPI_GROUPS = EPI_WARPS / 4;  // warps per TMEM lane quadrant
 constexpr int CS = 32 * EPI_GROUPS;        // column stride between one warp's chunks
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
+constexpr int KS_BLOCK = 32;  // output tiles per block of a K-split shared set
 constexpr uint32_t TMEM_COLS = 2 * BN_MAX;
 // EPI_SWIGLU_BWD stages dh through shared memory: per epilogue warp two buffers of its
 // 32 rows x 32 columns (bf16), filled by TMA.
@@ -85,6 +86,10 @@ struct OperandSet {
   // MN-major operands: the map views [K rows][M or N] as (64 elements, K rows, atoms
   // of 64 along M/N), box (64, BK, atoms per CTA), one copy per operand per k-block.
   int a_mn, b_mn;
+  // Shared set split along K into ksplit >= 1 parts: EPI_STORE parts write out + part *
+  // part_stride; EPI_STORE_F32 parts add into out in part order (see Params::kdep).
+  int ksplit;
+  long long part_stride;
   // EPI_SWIGLU_BWD operands (see GemmOperandSet); dhm views dh as [rows][n_total / 2]
   // with a 32 x 32 box.
   CUtensorMap dhm;
@@ -102,6 +107,11 @@ struct Params {
   OperandSet chain;
   int* dep;
   int dep_target;
+  // fp32 K parts of the shared set: kdep[tile] counts the epilogue warps that have
+  // written (part 0) or added (later parts) that output tile; part p adds once it
+  // reaches 8 p, so the parts are summed in order and the result does not depend on
+  // timing.  Zeroed by the caller.
+  int* kdep;
   const int32_t* offsets;
   const uint16_t* y_perm;
   const int32_t* inv_pos;
@@ -275,14 +285,24 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, int tile, int share
   t.bk = 0;
   t.mblk = 0;
   if (tile < shared_tiles) {
-    const int nt = p.shared.n_total / p.shared.bn;
-    const int m = tile / nt, n = tile % nt;
+    // K parts in blocks of KS_BLOCK output tiles: the block's part 0 tiles, then its
+    // part 1 tiles, ...: a tile's next part comes about two waves later, when the
+    // previous one is done and its output still in L2.
+    const int nt = p.shared.n_total / p.shared.bn, ks = p.shared.ksplit;
+    const int mn_count = ((p.shared.rows + BM - 1) / BM) * nt;
+    const int blk = tile / (KS_BLOCK * ks), within = tile % (KS_BLOCK * ks);
+    const int nb = min(KS_BLOCK, mn_count - blk * KS_BLOCK);
+    const int part = within / nb, mn = blk * KS_BLOCK + within % nb;
+    const int m = mn / nt, n = mn % nt;
     t.set = 0;
     t.row0 = m * BM;
     t.rend = p.shared.rows;
     t.n0 = n * p.shared.bn;
     t.brow = t.n0;
-    t.klen = p.shared.k_total;
+    t.klen = p.shared.k_total / ks;
+    t.k0 = part * t.klen;
+    t.group = part;
+    t.mblk = mn;
   } else if (p.kgroup) {
     const int r = tile - shared_tiles;
     const int nt = p.routed.n_total / p.routed.bn;
@@ -378,6 +398,16 @@ __device__ __forceinline__ void store_f32_row32(float* dst, const uint32_t (&v)[
   }
 }
 
+// dst[0..32) += 32 fp32 values (raw bits), as eight 128-bit reductions performed in L2.
+__device__ __forceinline__ void red_add_f32_row32(float* dst, const uint32_t (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4 * i), "f"(__uint_as_float(v[4 * i])),
+                 "f"(__uint_as_float(v[4 * i + 1])), "f"(__uint_as_float(v[4 * i + 2])),
+                 "f"(__uint_as_float(v[4 * i + 3]))
+                 : "memory");
+}
+
 // 8 packed bf16 pairs (32 bytes) -> dst: one 256-bit store with v8, else two 128-bit.
 __device__ __forceinline__ void store_packed16(uint16_t* dst, const uint32_t (&p)[8], int v8) {
   if (v8) {
@@ -453,7 +483,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   const bool leader = rank == 0;
   const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
   const int shared_tiles =
-      p.shared.enabled ? ((p.shared.rows + BM - 1) / BM) * (p.shared.n_total / p.shared.bn) : 0;
+      p.shared.enabled ? ((p.shared.rows + BM - 1) / BM) * (p.shared.n_total / p.shared.bn) * p.shared.ksplit
+                       : 0;
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -650,7 +681,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       for (int tile = cluster; tile < total && ok; tile += nclusters) {
         const int set = tile_set(tile, shared_tiles, t1);
-        int k_total = set == 2 ? p.chain.k_total : (set ? p.routed.k_total : p.shared.k_total);
+        int k_total = set == 2 ? p.chain.k_total : (set ? p.routed.k_total : p.shared.k_total / p.shared.ksplit);
         if (set == 1 && p.kgroup) {  // this tile's K group
           k_total = decode_tile(p, tile, shared_tiles, s_off, s_cum, t1).klen;
           if (k_total == 0) continue;  // empty group: no MMA, no accumulator hand-off
@@ -742,7 +773,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const long long orow = (long long)t.row0 + HM * (int)rank + r;
       const bool valid = orow < t.rend;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN_MAX;
-      uint16_t* out = static_cast<uint16_t*>(S.out);
+      uint16_t* out = static_cast<uint16_t*>(S.out) + (t.set == 0 ? t.group * S.part_stride : 0);
       if (S.mode == EPI_SWIGLU) {
         const int half = S.bn / 2;
         for (int c = 32 * colh; c < half; c += CS) {
@@ -847,16 +878,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         // fp32 output (weight gradients); K groups write their own matrices.  Two
         // 32-column chunks per TMEM round trip; 256-bit stores (whole 32-byte sectors,
         // one row per thread) when aligned.
-        float* o32 = static_cast<float*>(S.out) + (long long)t.group * p.group_stride + orow * S.ldo + t.n0;
+        // A later K part of the shared set waits for the earlier ones, then adds.
+        const int part = (t.set == 0 && S.ksplit > 1) ? t.group : 0;
+        if (part > 0) {
+          int ok2 = 1;
+          if (lane == 0) ok2 = dep_wait(p.kdep + t.mblk, 2 * EPI_WARPS * part, p.status) ? 1 : 0;
+          ok2 = __shfl_sync(FULL, ok2, 0);
+          __syncwarp();
+          if (!ok2) break;
+        }
+        float* o32 = static_cast<float*>(S.out) + (t.set == 1 ? (long long)t.group * p.group_stride : 0) +
+                     orow * S.ldo + t.n0;
         for (int c = 32 * colh; c < S.bn; c += 2 * CS) {
           const bool two = c + CS < S.bn;  // warp-uniform
           uint32_t v[32], w[32];
           tmem_ld32(tbase + c, v);
           if (two) tmem_ld32(tbase + c + CS, w);
           tmem_wait_ld();
-          if (valid) {
+          if (valid && part > 0) {
+            red_add_f32_row32(o32 + c, v);
+            if (two) red_add_f32_row32(o32 + c + CS, w);
+          } else if (valid) {
             store_f32_row32(o32 + c, v, S.v8);
             if (two) store_f32_row32(o32 + c + CS, w, S.v8);
+          }
+        }
+        if (t.set == 0 && S.ksplit > 1) {
+          __syncwarp();
+          if (lane == 0) {
+            __threadfence();
+            atomicAdd(p.kdep + t.mblk, 1);
           }
         }
       } else if (S.mode == EPI_STORE) {
@@ -1020,6 +1071,7 @@ int max_active_pairs() {
 
 bool fill_set(OperandSet& t, const GemmOperandSet& o) {
   std::memset(&t, 0, sizeof(t));
+  t.ksplit = 1;
   if (!o.a) return true;
   t.enabled = 1;
   t.bn = choose_bn(o.mode, o.N);
@@ -1029,6 +1081,11 @@ bool fill_set(OperandSet& t, const GemmOperandSet& o) {
   t.mode = o.mode;
   t.rows = o.rows;
   t.out = o.out;
+  t.ksplit = o.ksplit > 1 ? o.ksplit : 1;
+  t.part_stride = o.part_stride;
+  // Every part a whole number of 64-wide K atoms; separate bf16 parts or fp32 sums.
+  if (t.ksplit > 1 && (o.K % (AK * t.ksplit) != 0 || (o.mode != EPI_STORE && o.mode != EPI_STORE_F32)))
+    return false;
   t.dh = o.dh;
   t.gperm = o.gperm;
   t.dgpart = o.dgpart;
@@ -1095,7 +1152,7 @@ cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* off
                                 const GemmOperandSet& shared, const CombineInputs& comb,
                                 long long max_routed_rows, cudaStream_t s, int* bad_arg,
                                 int max_pairs, long long kgroup_stride, int early,
-                                const GemmOperandSet* chain, int32_t* dep) {
+                                const GemmOperandSet* chain, int32_t* dep, int32_t* kdep) {
   Params p;
   std::memset(&p, 0, sizeof(p));
   *bad_arg = 0;
@@ -1113,6 +1170,13 @@ cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* off
     }
     p.dep = dep;
     p.dep_target = (p.routed.n_total / p.routed.bn) * 2 * EPI_WARPS;
+  }
+  if (p.shared.ksplit > 1 && p.shared.mode == EPI_STORE_F32) {
+    if (!kdep) {
+      *bad_arg = 1;
+      return cudaErrorInvalidValue;
+    }
+    p.kdep = kdep;
   }
   if (!p.shared.enabled && !p.routed.enabled) return cudaSuccess;
   p.offsets = offsets;
@@ -1134,7 +1198,7 @@ cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* off
   if (e != cudaSuccess) return e;
   long long tiles = 0;
   if (p.shared.enabled)
-    tiles += (long long)((p.shared.rows + BM - 1) / BM) * (p.shared.n_total / p.shared.bn);
+    tiles += (long long)((p.shared.rows + BM - 1) / BM) * (p.shared.n_total / p.shared.bn) * p.shared.ksplit;
   if (p.routed.enabled && p.kgroup)
     tiles += (long long)E * ((p.routed.rows + BM - 1) / BM) * (p.routed.n_total / p.routed.bn);
   else if (p.routed.enabled)

@@ -125,6 +125,11 @@ struct GemmOperandSet {
   uint16_t* dh;
   const float* gperm;
   float* dgpart;
+  // Shared set only: split K into ksplit equal parts (multiples of 64).  EPI_STORE: part
+  // p writes out + p * part_stride elements and the caller sums the parts.  EPI_STORE_F32:
+  // the parts are added into out in part order (launch_grouped_gemm's kdep).
+  int ksplit;
+  long long part_stride;
 };
 // Column tile width the grouped GEMM uses for an operand set of this mode and N.
 int gemm_tile_n(int mode, int N);
@@ -150,11 +155,13 @@ struct CombineInputs {
 // routed.ldo); its tiles run after the others in the same launch, each once the
 // routed tiles of its 256-row block have written their rows.  dep: one zeroed int32
 // per routed 256-row block (max_routed_rows / 256 + E + 1 suffice), left non-zero.
+// kdep: with an fp32 shared set split along K, one zeroed int32 per output tile of it.
 cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* offsets, int E,
                                 const GemmOperandSet& shared, const CombineInputs& comb,
                                 long long max_routed_rows, cudaStream_t s, int* bad_arg,
                                 int max_pairs = 0, long long kgroup_stride = 0, int early = 0,
-                                const GemmOperandSet* chain = nullptr, int32_t* dep = nullptr);
+                                const GemmOperandSet* chain = nullptr, int32_t* dep = nullptr,
+                                int32_t* kdep = nullptr);
 // Number of co-resident 2-SM clusters of the grouped GEMM on the current device.
 int gemm_max_pairs();
 
@@ -201,7 +208,8 @@ cudaError_t launch_pad_gather(const int32_t* off, const int32_t* perm_tok, const
 // dgp: [Q][nparts] partial sums of dL/dgate per padded row (summed in order).
 cudaError_t launch_router_bwd_dx(const int32_t* idx, const float* gate, const float* scores,
                                  const int32_t* inv_pad, const float* dgp, int nparts, const float* w_router,
-                                 const uint16_t* dxp, const uint16_t* dxs, const uint16_t* dout, int T,
+                                 const uint16_t* dxp, const uint16_t* dxs, const uint16_t* dxs2,
+                                 const uint16_t* dout, int T,
                                  int d, int E, int k, int renorm, float* dzp, float* dgate, uint16_t* dx,
                                  cudaStream_t s);
 cudaError_t launch_router_wgrad(const float* dzp, const int32_t* off, const int32_t* poff,

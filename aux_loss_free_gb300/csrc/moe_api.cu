@@ -859,6 +859,28 @@ long long bwd_rows(const moe_shape_t* s) { return (long long)s->T * s->k + 63LL 
 // Column tiles of the routed dgrad-through-down GEMM: partial sums of dL/dgate per row.
 int bwd_parts(const moe_shape_t* s) { return 2 * s->f / gemm_tile_n(EPI_SWIGLU_BWD, 2 * s->f); }
 
+// The shared expert's input gradient dxs = (das, dbs) Sgu runs over K = 2F: with
+// 2F >= 2048 its tiles are split into two K halves (a K = 4096 tile alone took four
+// times a routed tile and left the launch's end to the pairs holding two of them);
+// the router backward adds the halves.
+int bwd_dxs_parts(const moe_shape_t* s) { return (s->F && 2 * s->F >= 2048 && (2 * s->F) % 128 == 0) ? 2 : 1; }
+
+// The shared expert's down-projection weight gradient runs over K = T tokens in few
+// output tiles ([d][F]: 32 for Nano, so most pairs had none and the launch ended with
+// the K = 8192 tiles): split into up to four parts of >= 2048 tokens, added in order
+// into the fp32 output.  The gate/up one ([2F][d], 64 tiles, one for most pairs) gains
+// less from balance than the extra tiles and reductions cost, and is not split.
+int bwd_wgrad_parts(const moe_shape_t* s) {
+  int ks = std::min(4, s->T / 2048);
+  while (ks > 1 && s->T % (64 * ks) != 0) --ks;
+  return std::max(ks, 1);
+}
+// Output tiles of the shared down-projection weight gradient [d][F].
+int bwd_wgrad_tiles_down(const moe_shape_t* s) {
+  return s->F ? (s->d + 255) / 256 * (s->F / gemm_tile_n(EPI_STORE_F32, s->F)) : 0;
+}
+
+
 struct BwdWs {
   int32_t* poff;     // [E+1] padded expert offsets
   int32_t* inv_pad;  // [T*k] padded row of each pair
@@ -872,7 +894,8 @@ struct BwdWs {
   uint16_t* dxp;     // [Q][d] routed input gradient of each row
   uint16_t* abs;     // [T][2F] shared expert: as ab
   uint16_t* dhs;     // [T][F] as dh (gate 1)
-  uint16_t* dxs;     // [T][d] shared expert's input gradient
+  uint16_t* dxs;     // [bwd_dxs_parts][T][d] shared expert's input gradient (K parts)
+  int32_t* kdep;     // per output tile of dS_down: its K parts added so far
 };
 BwdWs carve_bwd(Carver& c, const moe_shape_t* s) {
   const size_t Q = (size_t)bwd_rows(s), Tk = (size_t)s->T * s->k, T = (size_t)s->T;
@@ -889,7 +912,8 @@ BwdWs carve_bwd(Carver& c, const moe_shape_t* s) {
   w.dxp = static_cast<uint16_t*>(c.take(2 * Q * s->d));
   w.abs = s->F ? static_cast<uint16_t*>(c.take(2 * T * 2 * s->F)) : nullptr;
   w.dhs = s->F ? static_cast<uint16_t*>(c.take(2 * T * s->F)) : nullptr;
-  w.dxs = s->F ? static_cast<uint16_t*>(c.take(2 * T * s->d)) : nullptr;
+  w.dxs = s->F ? static_cast<uint16_t*>(c.take(2 * T * s->d * bwd_dxs_parts(s))) : nullptr;
+  w.kdep = static_cast<int32_t*>(c.take(4 * (size_t)(bwd_wgrad_tiles_down(s) + 1)));
   return w;
 }
 
@@ -942,6 +966,11 @@ moe_status_t moe_layer_bwd(const moe_shape_t* shape, const void* x, const float*
   cudaError_t e;
   const bool prof = prof_begin_call();
   if (prof) prof_mark("bwd_pad_gather", s);
+  const int ksw = has_shared ? bwd_wgrad_parts(shape) : 1;
+  if (ksw > 1 && cudaMemsetAsync(b.kdep, 0, 4 * (size_t)bwd_wgrad_tiles_down(shape), s) != cudaSuccess) {
+    if (prof) prof_mark(nullptr, s);
+    return MOE_ERR_CUDA;
+  }
 
   // Padded permuted layout and the gathered tokens and output gradients.
   e = launch_pad_gather(saved->offsets, saved->perm_tok, saved->idx, saved->inv_pos, saved->gate, E, P, Q, xb,
@@ -976,7 +1005,9 @@ moe_status_t moe_layer_bwd(const moe_shape_t* shape, const void* x, const float*
   if (e == cudaSuccess) {
     GemmOperandSet r{b.ab, Q, w->w_gate_up, E, d, 2 * f, b.dxp, d, EPI_STORE, 0, 0, 1};
     GemmOperandSet sh{};
-    if (has_shared) sh = GemmOperandSet{b.abs, T, w->shared_gate_up, 1, d, 2 * F, b.dxs, d, EPI_STORE, T, 0, 1};
+    if (has_shared)
+      sh = GemmOperandSet{b.abs, T, w->shared_gate_up, 1, d, 2 * F, b.dxs, d, EPI_STORE, T, 0, 1,
+                          nullptr, nullptr, nullptr, bwd_dxs_parts(shape), (long long)T * d};
     e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad, 0, 0, /*early=*/1);
   }
   if (prof && e == cudaSuccess) prof_mark("bwd_router_dx", s);
@@ -984,22 +1015,28 @@ moe_status_t moe_layer_bwd(const moe_shape_t* shape, const void* x, const float*
   if (e == cudaSuccess)
     e = launch_router_bwd_dx(saved->idx, saved->gate, saved->scores, b.inv_pad, b.dgp, bwd_parts(shape),
                              w_router, b.dxp,
-                             has_shared ? b.dxs : nullptr, residual ? db : nullptr, T, d, E, k,
+                             has_shared ? b.dxs : nullptr,
+                             has_shared && bwd_dxs_parts(shape) > 1 ? b.dxs + (size_t)T * d : nullptr,
+                             residual ? db : nullptr, T, d, E, k,
                              shape->renorm, b.dzp, g->dgate, static_cast<uint16_t*>(g->dx), s);
   if (prof && e == cudaSuccess) prof_mark("bwd_wgrad_down", s);
   // (6) dWd_e = dp^T (gate * h) over the expert's rows (K-grouped), dSd = dout^T hs.
   if (e == cudaSuccess) {
     GemmOperandSet r{b.dp, Q, b.dh, 1, f, (int)Q, g->dw_down, f, EPI_STORE_F32, d, 1, 1};
     GemmOperandSet sh{};
-    if (has_shared) sh = GemmOperandSet{dout, T, b.dhs, 1, F, T, g->ds_down, F, EPI_STORE_F32, d, 1, 1};
-    e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad, 0, (long long)d * f, /*early=*/1);
+    if (has_shared)
+      sh = GemmOperandSet{dout, T, b.dhs, 1, F, T, g->ds_down, F, EPI_STORE_F32, d, 1, 1,
+                          nullptr, nullptr, nullptr, ksw, 0};
+    e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad, 0, (long long)d * f, /*early=*/1, nullptr,
+                            nullptr, b.kdep);
   }
   if (prof && e == cudaSuccess) prof_mark("bwd_wgrad_gate_up", s);
   // (7) dWgu_e = (da, db)^T xp (rows interleaved as w_gate_up), dSgu = (das, dbs)^T x.
   if (e == cudaSuccess) {
     GemmOperandSet r{b.ab, Q, b.xp, 1, d, (int)Q, g->dw_gate_up, d, EPI_STORE_F32, 2 * f, 1, 1};
     GemmOperandSet sh{};
-    if (has_shared) sh = GemmOperandSet{b.abs, T, x, 1, d, T, g->ds_gate_up, d, EPI_STORE_F32, 2 * F, 1, 1};
+    if (has_shared)
+      sh = GemmOperandSet{b.abs, T, x, 1, d, T, g->ds_gate_up, d, EPI_STORE_F32, 2 * F, 1, 1};
     e = launch_grouped_gemm(r, b.poff, E, sh, none, Q, s, &bad, 0, (long long)2 * f * d, /*early=*/1);
   }
   if (prof && e == cudaSuccess) prof_mark("bwd_router_wgrad", s);
