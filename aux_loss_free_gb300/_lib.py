@@ -68,6 +68,8 @@ SIGNATURES = {
     "moe_expert_ffn": (_I32, [_SHAPE_P, _P, _P, _P, ctypes.POINTER(MoEWeights), _P, _P, _P, _SZ,
                               _P]),
     "moe_combine": (_I32, [_SHAPE_P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_gather_rows": (_I32, [_I64, _I32, _P, _P, _P, _P]),
+    "moe_ep_regroup": (_I32, [_I32, _I32, _P, _P, _P, _P, _P]),
     "moe_bias_update": (_I32, [_I32, _I64, _P, _F, _P, _P]),
     "moe_layer_workspace_size": (_SZ, [_SHAPE_P]),
     "moe_layer_fwd": (_I32, [_SHAPE_P, _P, _P, _P, _P, _F, _I32, ctypes.POINTER(MoEWeights), _P,
@@ -193,6 +195,16 @@ def moe_combine(shape, y_perm, shared_out, inv_pos, gate, residual, out, stream=
     _check("moe_combine", load_library().moe_combine(
         ctypes.byref(shape), _ptr(y_perm), _ptr(shared_out), _ptr(inv_pos), _ptr(gate),
         _ptr(residual), _ptr(out), _stream(stream)))
+
+
+def moe_gather_rows(rows, d, src, index, dst, stream=None):
+    _check("moe_gather_rows", load_library().moe_gather_rows(
+        rows, d, _ptr(src), _ptr(index), _ptr(dst), _stream(stream)))
+
+
+def moe_ep_regroup(world, experts_local, counts, perm, inv, offsets, stream=None):
+    _check("moe_ep_regroup", load_library().moe_ep_regroup(
+        world, experts_local, _ptr(counts), _ptr(perm), _ptr(inv), _ptr(offsets), _stream(stream)))
 
 
 def moe_bias_update(E, tokens_times_k, load, gamma, bias, stream=None):

@@ -483,6 +483,23 @@ moe_status_t moe_expert_ffn(const moe_shape_t* shape, const void* x, const int32
                  static_cast<uint16_t*>(shared_out), nullptr, nullptr, s);
 }
 
+moe_status_t moe_gather_rows(int64_t rows, int32_t d, const void* src, const int32_t* index, void* dst,
+                             void* stream) {
+  if (rows < 0 || d < 8 || d % 8 || d > 8192 || (rows > 0 && (!src || !index || !dst)))
+    return MOE_ERR_INVALID_ARG;
+  if (rows > 0 && (!aligned16(src) || !aligned16(dst))) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_gather(src, 0, index, rows, d, static_cast<uint16_t*>(dst),
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_ep_regroup(int32_t world, int32_t experts_local, const int32_t* counts, int32_t* perm,
+                            int32_t* inv, int32_t* offsets, void* stream) {
+  if (world < 1 || experts_local < 1 || (long long)world * experts_local > 4096) return MOE_ERR_INVALID_ARG;
+  if (!counts || !perm || !inv || !offsets) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_ep_regroup(world, experts_local, counts, perm, inv, offsets,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 moe_status_t moe_combine(const moe_shape_t* shape, const void* y_perm, const void* shared_out,
                          const int32_t* inv_pos, const float* gate, const void* residual, void* out,
                          void* stream) {

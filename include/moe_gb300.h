@@ -187,6 +187,27 @@ moe_status_t moe_combine(const moe_shape_t* shape, const void* y_perm, const voi
                          const int32_t* inv_pos, const float* gate, const void* residual,
                          void* out, void* stream);
 
+/* Row gather: dst[r] = src[index[r]] for r < rows, rows of d bf16 values (d a
+ * multiple of 8, both buffers 16-byte aligned, index values valid rows of src).
+ * The expert-parallel path sends and receives rows with it (no host round trip). */
+moe_status_t moe_gather_rows(int64_t rows, int32_t d, const void* src, const int32_t* index, void* dst,
+                             void* stream);
+
+/* Expert-parallel regrouping of received rows.  The experts are split over `world`
+ * ranks in contiguous ranges of experts_local; a rank receives, source rank by
+ * source rank, each source's rows for its local experts in the source's permuted
+ * order (by local expert, then token).  Relay article, top-2 paragraph: expert
+ * parallelism is where the leftover per-expert imbalance would show.
+ *   counts   [world][experts_local] int32 device: rows source s sent for local expert e
+ *   perm     [rows] int32 device: received row of each grouped row (grouped = by local
+ *            expert, then source rank, then the source's order); rows = sum of counts
+ *   inv      [rows] int32 device: grouped row of each received row
+ *   offsets  [experts_local + 1] int32 device: local expert e owns grouped rows
+ *            [offsets[e], offsets[e+1])
+ * world * experts_local <= 4096; perm and inv must hold sum(counts) entries. */
+moe_status_t moe_ep_regroup(int32_t world, int32_t experts_local, const int32_t* counts, int32_t* perm,
+                            int32_t* inv, int32_t* offsets, void* stream);
+
 /* Aux-loss-free bias update, relay article, architecture paragraph (DeepSeek-V3
  * recipe): bias[e] = fl32(bias[e] + gamma * sign(tokens_times_k - E * load[e])),
  * i.e. the sign of (target - load) with target = T*k/E and sign(0) = 0.
