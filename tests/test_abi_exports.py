@@ -70,3 +70,19 @@ def test_host_validation_rejects_bad_shapes_before_any_launch(lib_path):
     assert M.moe_route_workspace_size(M.make_shape(64, 1024, 64, 512, 2048, 2)) == 0  # small T: CUDA-core router
     assert M.moe_route_workspace_size(M.make_shape(64, 64, 8, 32, 128, 2, x_dtype=M.MOE_X_F32)) == 0
     assert lib.moe_bias_update(0, 16, None, 1e-3, None, None) == 1
+
+
+def test_expert_parallel_calls_validate_on_the_host(lib_path):
+    """moe_gather_rows and moe_ep_regroup reject bad sizes and null pointers before any
+    launch (MOE_ERR_INVALID_ARG = 1), so this runs without a GPU."""
+    lib = M.load_library(lib_path)
+    p = ctypes.c_void_p(16)  # never dereferenced: every call below fails validation first
+    assert lib.moe_gather_rows(-1, 256, p, p, p, None) == 1     # negative row count
+    assert lib.moe_gather_rows(4, 12, p, p, p, None) == 1       # d not a multiple of 8
+    assert lib.moe_gather_rows(4, 16384, p, p, p, None) == 1    # d too wide
+    assert lib.moe_gather_rows(4, 256, None, p, p, None) == 1   # null source
+    assert lib.moe_gather_rows(4, 256, ctypes.c_void_p(24), p, p, None) == 1  # misaligned source
+    assert lib.moe_ep_regroup(0, 8, p, p, p, p, None) == 1      # no ranks
+    assert lib.moe_ep_regroup(2, 0, p, p, p, p, None) == 1      # no local experts
+    assert lib.moe_ep_regroup(64, 128, p, p, p, p, None) == 1   # count table too large
+    assert lib.moe_ep_regroup(2, 8, p, None, p, p, None) == 1   # null output
