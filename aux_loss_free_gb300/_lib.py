@@ -85,6 +85,7 @@ SIGNATURES = {
     "moe_pack_gate_up": (_I32, [_I32, _I32, _I32, _P, _P, _P, _P]),
     "moe_quantize_int4": (_I32, [_I64, _I32, _P, _P, _P, _P]),
     "moe_device_status": (_I32, [_P, ctypes.POINTER(_I32)]),
+    "moe_selftest_bounded_wait": (_I32, [_I64, ctypes.POINTER(_I32), _P]),
     "moe_profile_stage_count": (_I32, []),
     "moe_profile_stage_name": (ctypes.c_char_p, [_I32]),
     "moe_profile_stage_calls": (_I32, [_I32]),
@@ -293,6 +294,14 @@ def moe_quantize_int4(rows, K, w, q, scale, stream=None):
 def moe_device_status(stream=None) -> int:
     out = _I32(0)
     _check("moe_device_status", load_library().moe_device_status(_stream(stream), ctypes.byref(out)))
+    return out.value
+
+
+def moe_selftest_bounded_wait(limit_ns: int, stream=None) -> int:
+    """Make one bounded device wait run out (see the header); returns 1 if it gave up."""
+    out = _I32(-1)
+    _check("moe_selftest_bounded_wait", load_library().moe_selftest_bounded_wait(
+        limit_ns, ctypes.byref(out), _stream(stream)))
     return out.value
 
 

@@ -446,20 +446,9 @@ __device__ __forceinline__ void store_bf16_row32(uint16_t* dst, const float (&o)
 // TMA reads (async proxy) after the generic-proxy stores the counter published.
 // Bounded like the barrier waits.
 __device__ __forceinline__ bool dep_wait(const int* ctr, int target, int* status) {
-  const unsigned long long t0 = globaltimer_ns();
-  while (true) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
-    if (v >= target) {
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      return true;
-    }
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      atomicOr(status, kDevTimeout);
-      return false;
-    }
-    __nanosleep(64);
-  }
+  if (!wait_counter_geq(ctr, target, status, kWaitLimitNs)) return false;
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)

@@ -86,6 +86,7 @@ cudaError_t launch_scatter(const int32_t* idx, const int32_t* counts, int T, int
                            float gamma, long long tokens_times_k, int32_t* perm_tok,
                            int32_t* inv_pos, const void* x, int x_is_f32, int d, uint16_t* xp,
                            uint16_t* xb, cudaStream_t s, int32_t* active = nullptr);
+cudaError_t run_bounded_wait_selftest(unsigned long long limit_ns, int* gave_up, cudaStream_t s);
 cudaError_t launch_ep_regroup(int world, int el, const int32_t* counts, int32_t* perm, int32_t* inv,
                               int32_t* offsets, cudaStream_t s);
 cudaError_t launch_gather(const void* x, int x_is_f32, const int32_t* perm_tok, long long rows,

@@ -483,6 +483,14 @@ moe_status_t moe_expert_ffn(const moe_shape_t* shape, const void* x, const int32
                  static_cast<uint16_t*>(shared_out), nullptr, nullptr, s);
 }
 
+moe_status_t moe_selftest_bounded_wait(int64_t limit_ns, int32_t* gave_up, void* stream) {
+  if (limit_ns < 1 || limit_ns > 1000000000LL || !gave_up) return MOE_ERR_INVALID_ARG;
+  int g = -1;
+  const cudaError_t e = run_bounded_wait_selftest((unsigned long long)limit_ns, &g, static_cast<cudaStream_t>(stream));
+  *gave_up = g;
+  return cuda_status(e);
+}
+
 moe_status_t moe_gather_rows(int64_t rows, int32_t d, const void* src, const int32_t* index, void* dst,
                              void* stream) {
   if (rows < 0 || d < 8 || d % 8 || d > 8192 || (rows > 0 && (!src || !index || !dst)))

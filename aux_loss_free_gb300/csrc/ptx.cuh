@@ -106,6 +106,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* st
   }
 }
 
+// Acquire-waits (GPU scope) until *ctr >= target, a counter other CTAs raise.  Gives
+// up after limit_ns of wall-clock time, sets the timeout bit in *status and returns
+// false.
+__device__ __forceinline__ bool wait_counter_geq(const int* ctr, int target, int* status,
+                                                 unsigned long long limit_ns) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (true) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= target) return true;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      atomicOr(status, kDevTimeout);
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 
 // 2-D tiled bulk tensor load global -> shared, completion counted on `bar`.

@@ -354,6 +354,14 @@ moe_status_t moe_profile_stop(float* ms_per_stage, int32_t* calls);
  * MOE_ERR_DEVICE) in *device_status, and clears it. */
 moe_status_t moe_device_status(void* stream, int32_t* device_status);
 
+/* Self-test of the failure path (for tests; it faults nothing).  One device thread
+ * waits, through the helper the library's dependency waits use, for a counter that
+ * nothing raises; after limit_ns nanoseconds of wall-clock time (1 .. 1e9) it gives up,
+ * sets the timeout bit of the device status word (read and cleared by
+ * moe_device_status, which then reports MOE_ERR_TIMEOUT) and returns.  *gave_up
+ * (host) receives 1 when the wait gave up.  Synchronises `stream`. */
+moe_status_t moe_selftest_bounded_wait(int64_t limit_ns, int32_t* gave_up, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -86,3 +86,11 @@ def test_expert_parallel_calls_validate_on_the_host(lib_path):
     assert lib.moe_ep_regroup(2, 0, p, p, p, p, None) == 1      # no local experts
     assert lib.moe_ep_regroup(64, 128, p, p, p, p, None) == 1   # count table too large
     assert lib.moe_ep_regroup(2, 8, p, None, p, p, None) == 1   # null output
+
+
+def test_selftest_call_validates_on_the_host(lib_path):
+    lib = M.load_library(lib_path)
+    out = ctypes.c_int32(0)
+    assert lib.moe_selftest_bounded_wait(0, ctypes.byref(out), None) == 1              # no limit
+    assert lib.moe_selftest_bounded_wait(2_000_000_000, ctypes.byref(out), None) == 1  # over 1 s
+    assert lib.moe_selftest_bounded_wait(1000, None, None) == 1                        # no output
