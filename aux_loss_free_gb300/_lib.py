@@ -86,6 +86,8 @@ SIGNATURES = {
     "moe_quantize_int4": (_I32, [_I64, _I32, _P, _P, _P, _P]),
     "moe_device_status": (_I32, [_P, ctypes.POINTER(_I32)]),
     "moe_selftest_bounded_wait": (_I32, [_I64, ctypes.POINTER(_I32), _P]),
+    "moe_last_device_status": (_I32, [_P]),
+    "moe_workspace_size": (_SZ, [_SHAPE_P]),
     "moe_profile_stage_count": (_I32, []),
     "moe_profile_stage_name": (ctypes.c_char_p, [_I32]),
     "moe_profile_stage_calls": (_I32, [_I32]),

@@ -1166,4 +1166,12 @@ moe_status_t moe_device_status(void* stream, int32_t* device_status) {
   return MOE_OK;
 }
 
+moe_status_t moe_last_device_status(void* stream) {
+  int32_t st = MOE_OK;
+  const moe_status_t e = moe_device_status(stream, &st);
+  return e != MOE_OK ? e : static_cast<moe_status_t>(st);
+}
+
+size_t moe_workspace_size(const moe_shape_t* shape) { return moe_layer_workspace_size(shape); }
+
 }  // extern "C"

@@ -315,7 +315,9 @@ moe_status_t moe_layer_fwd_cached(const moe_shape_t* shape, const void* x, const
                                   const void* residual, void* out, const moe_debug_t* dbg, void* workspace,
                                   size_t ws_bytes, void* stream);
 
-/* Weight preparation (off the hot path).
+/* Weight preparation, once per weight update and off the hot path: moe_pack_gate_up
+ * for every bf16 layer, then moe_quantize_int4 on the packed gate/up and the down
+ * weights for int4 serving.
  * moe_pack_gate_up: for each of G matrices, interleave w_gate [G][width][d] and
  * w_up [G][width][d] (bf16) into w_gate_up [G][2*width][d] in blocks of
  * b = moe_gate_up_block(width) rows: block i holds gate rows [i*b, (i+1)*b)
@@ -353,6 +355,15 @@ moe_status_t moe_profile_stop(float* ms_per_stage, int32_t* calls);
  * library's kernels since the last call (MOE_OK, MOE_ERR_TIMEOUT or
  * MOE_ERR_DEVICE) in *device_status, and clears it. */
 moe_status_t moe_device_status(void* stream, int32_t* device_status);
+
+/* The same as one call: synchronises `stream`, reads and clears the device status word
+ * and returns it (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE), or MOE_ERR_CUDA if the
+ * read itself failed. */
+moe_status_t moe_last_device_status(void* stream);
+
+/* moe_layer_workspace_size under the short name: bytes of device workspace one
+ * moe_layer_fwd call needs for this shape (0 for an unsupported shape). */
+size_t moe_workspace_size(const moe_shape_t* shape);
 
 /* Self-test of the failure path (for tests; it faults nothing).  One device thread
  * waits, through the helper the library's dependency waits use, for a counter that

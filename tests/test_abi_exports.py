@@ -94,3 +94,11 @@ def test_selftest_call_validates_on_the_host(lib_path):
     assert lib.moe_selftest_bounded_wait(0, ctypes.byref(out), None) == 1              # no limit
     assert lib.moe_selftest_bounded_wait(2_000_000_000, ctypes.byref(out), None) == 1  # over 1 s
     assert lib.moe_selftest_bounded_wait(1000, None, None) == 1                        # no output
+
+
+def test_short_workspace_name_matches_the_layer_query(lib_path):
+    M.load_library(lib_path)
+    lib = M.load_library()
+    for s in (M.make_shape(8192, 1024, 64, 512, 2048, 2), M.make_shape(64, 64, 8, 32, 128, 2),
+              M.make_shape(0, 1024, 64, 512, 2048, 2)):
+        assert lib.moe_workspace_size(ctypes.byref(s)) == M.moe_layer_workspace_size(s)

@@ -25,6 +25,10 @@ def test_bounded_wait_gives_up_and_reports():
     assert time.monotonic() - t0 < 5.0
     assert M.moe_device_status() == MOE_ERR_TIMEOUT
     assert M.moe_device_status() == 0  # the read cleared it
+    # The one-call form reports the same.
+    assert M.moe_selftest_bounded_wait(1_000_000) == 1
+    assert M.load_library().moe_last_device_status(None) == MOE_ERR_TIMEOUT
+    assert M.load_library().moe_last_device_status(None) == 0
     # The context still runs the layer, and the same forward gives the same bits.
     s = CONFIGS["nano"].replace(T=256, d=256, E=16, f=128, F=128)
     host = make_layer(s, "nano")
