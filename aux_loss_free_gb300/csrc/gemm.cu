@@ -24,7 +24,14 @@
 //       STORE   y -> bf16,
 //       COMBINE out = acc + residual + sum_j gate_j * y_perm[inv_pos_j] (the shared
 //               expert's down projection adds the same token's routed outputs:
-//               the layer's combine step).
+//               the layer's combine step),
+//       STORE_F32  fp32 out (weight gradients),
+//       SWIGLU_BWD the SwiGLU backward from the recomputed pre-activations, dh staged
+//               through shared memory by TMA.
+// For the backward, either operand may be MN-major (the instruction descriptor's
+// transpose bits read stored activations and weights where they are), the routed set
+// may be grouped along K (weight gradients over each expert's rows), and the shared
+// set may be split along K (separate bf16 parts, or fp32 parts added in order).
 // A third, chained operand set may follow the other two in the same launch: routed
 // groups whose A operand is the routed set's output (the down projection reading the
 // h rows the gate/up tiles write).  Its tiles come after all others; each waits until
