@@ -41,7 +41,13 @@ class MoEWeights(ctypes.Structure):
 
 class MoEDebug(ctypes.Structure):
     _fields_ = [("scores", _P), ("idx", _P), ("gate", _P), ("load", _P), ("offsets", _P),
-                ("perm_tok", _P), ("inv_pos", _P)]
+                ("perm_tok", _P), ("inv_pos", _P), ("balance", _P)]
+
+
+# moe_balance_t: int64 pairs, int32 max_load, min_load, dead_experts, float
+# max_over_mean, min_over_mean, dead_fraction (32 bytes).
+BALANCE_BYTES = 32
+MOE_TK_FROM_LOAD = -1
 
 
 class MoEGrads(ctypes.Structure):
@@ -71,6 +77,7 @@ SIGNATURES = {
     "moe_gather_rows": (_I32, [_I64, _I32, _P, _P, _P, _P]),
     "moe_ep_regroup": (_I32, [_I32, _I32, _P, _P, _P, _P, _P]),
     "moe_bias_update": (_I32, [_I32, _I64, _P, _F, _P, _P]),
+    "moe_load_balance": (_I32, [_I32, _P, _P, _P]),
     "moe_layer_workspace_size": (_SZ, [_SHAPE_P]),
     "moe_layer_fwd": (_I32, [_SHAPE_P, _P, _P, _P, _P, _F, _I32, ctypes.POINTER(MoEWeights), _P,
                              _P, ctypes.POINTER(MoEDebug), _P, _SZ, _P]),
@@ -215,6 +222,25 @@ def moe_bias_update(E, tokens_times_k, load, gamma, bias, stream=None):
         E, tokens_times_k, _ptr(load), gamma, _ptr(bias), _stream(stream)))
 
 
+def moe_load_balance(E, load, balance, stream=None):
+    """balance: a device buffer of at least BALANCE_BYTES bytes (see balance_from_bytes)."""
+    _check("moe_load_balance", load_library().moe_load_balance(E, _ptr(load), _ptr(balance), _stream(stream)))
+
+
+def balance_from_bytes(raw) -> dict:
+    """Decode one moe_balance_t from its 32 bytes (a uint8 tensor or bytes on the host)."""
+    import numpy as np
+    b = np.frombuffer(bytes(raw.cpu().numpy().tobytes() if hasattr(raw, "cpu") else raw)[:BALANCE_BYTES],
+                      dtype=np.uint8)
+    return {"pairs": int(b[0:8].view(np.int64)[0]),
+            "max_load": int(b[8:12].view(np.int32)[0]),
+            "min_load": int(b[12:16].view(np.int32)[0]),
+            "dead_experts": int(b[16:20].view(np.int32)[0]),
+            "max_over_mean": b[20:24].view(np.float32)[0],
+            "min_over_mean": b[24:28].view(np.float32)[0],
+            "dead_fraction": b[28:32].view(np.float32)[0]}
+
+
 def moe_layer_workspace_size(shape) -> int:
     return load_library().moe_layer_workspace_size(ctypes.byref(shape))
 
@@ -229,9 +255,9 @@ def moe_layer_fwd(shape, x, w_router, logit_offset, bias, gamma, update_bias, we
 
 
 def make_debug(scores=None, idx=None, gate=None, load=None, offsets=None, perm_tok=None,
-               inv_pos=None) -> MoEDebug:
+               inv_pos=None, balance=None) -> MoEDebug:
     return MoEDebug(_ptr(scores), _ptr(idx), _ptr(gate), _ptr(load), _ptr(offsets), _ptr(perm_tok),
-                    _ptr(inv_pos))
+                    _ptr(inv_pos), _ptr(balance))
 
 
 def moe_layer_bwd_workspace_size(shape) -> int:

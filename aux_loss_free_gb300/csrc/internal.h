@@ -7,7 +7,13 @@
 
 #include <utility>
 
+#include "moe_gb300.h"
+
 namespace moe {
+
+// Host validation of a layer shape (the envelope of moe_gb300.h); every entry point
+// that takes a moe_shape_t returns its status first.
+moe_status_t check_shape(const moe_shape_t* s);
 
 // Launch with programmatic dependent launch: the kernel may be scheduled while the
 // previous kernel in the stream is still running; it must execute
@@ -81,19 +87,26 @@ cudaError_t launch_count(const int32_t* idx, int T, int k, int E, int chunk_toke
 // block per chunk.
 // `active` (nullable, [kMaxE + 1]) receives the ids of the experts with pairs and,
 // at [kMaxE], their count.
+// `balance` (nullable): block 0 writes the loads' balance statistics there.
+// Expert ids outside [0, E) are skipped by the counting and the ranking and set the
+// kDevCheck bit of the status word.
 cudaError_t launch_scatter(const int32_t* idx, const int32_t* counts, int T, int k, int E,
                            int chunk_tokens, int32_t* offsets, int32_t* load_out, float* bias,
                            float gamma, long long tokens_times_k, int32_t* perm_tok,
                            int32_t* inv_pos, const void* x, int x_is_f32, int d, uint16_t* xp,
-                           uint16_t* xb, cudaStream_t s, int32_t* active = nullptr);
+                           uint16_t* xb, cudaStream_t s, int32_t* active = nullptr,
+                           moe_balance_t* balance = nullptr);
 cudaError_t run_bounded_wait_selftest(unsigned long long limit_ns, int* gave_up, cudaStream_t s);
 cudaError_t launch_ep_regroup(int world, int el, const int32_t* counts, int32_t* perm, int32_t* inv,
                               int32_t* offsets, cudaStream_t s);
 cudaError_t launch_gather(const void* x, int x_is_f32, const int32_t* perm_tok, long long rows,
                           int d, uint16_t* xp, cudaStream_t s);
 cudaError_t launch_to_bf16(const float* x, long long n, uint16_t* xb, cudaStream_t s);
+// tokens_times_k < 0: the kernel takes the sum of `load` as the global T*k.  bias
+// (nullable) is updated in place; balance (nullable) receives the loads' statistics.
 cudaError_t launch_bias_update(int E, long long tokens_times_k, const int32_t* load,
-                               float gamma, float* bias, cudaStream_t s);
+                               float gamma, float* bias, cudaStream_t s,
+                               moe_balance_t* balance = nullptr);
 cudaError_t launch_combine(const uint16_t* y_perm, const uint16_t* shared_out,
                            const int32_t* inv_pos, const float* gate, const uint16_t* residual,
                            uint16_t* out, int T, int k, int d, cudaStream_t s);

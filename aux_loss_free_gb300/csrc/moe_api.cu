@@ -35,6 +35,20 @@ int permute_chunk_tokens(int T, int E) {
   return (int)ct;
 }
 
+moe_status_t check_shape(const moe_shape_t* s) {
+  if (!s) return MOE_ERR_INVALID_ARG;
+  if (s->T < 1 || s->d < 1 || s->E < 1 || s->k < 1 || s->f < 1 || s->F < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (s->renorm != 0 && s->renorm != 1) return MOE_ERR_INVALID_ARG;
+  if (s->x_dtype != MOE_X_BF16 && s->x_dtype != MOE_X_F32) return MOE_ERR_INVALID_ARG;
+  if (s->w_format != MOE_W_BF16 && s->w_format != MOE_W_INT4_G32) return MOE_ERR_INVALID_ARG;
+  if (s->T > (1 << 24) || s->d % 64 || s->d < 64 || s->d > 8192) return MOE_ERR_UNSUPPORTED;
+  if (s->E > kMaxE || s->k > kMaxK || s->k > s->E) return MOE_ERR_UNSUPPORTED;
+  if (s->f % 32 || s->f > 8192 || s->F % 32 || s->F > 16384) return MOE_ERR_UNSUPPORTED;
+  if (s->w_format == MOE_W_INT4_G32 && (s->k != 1 || s->T > 256)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -124,20 +138,6 @@ AuxStream* aux_for_current_device() {
     if (cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming) != cudaSuccess) return nullptr;
   }
   return &a;
-}
-
-moe_status_t check_shape(const moe_shape_t* s) {
-  if (!s) return MOE_ERR_INVALID_ARG;
-  if (s->T < 1 || s->d < 1 || s->E < 1 || s->k < 1 || s->f < 1 || s->F < 0)
-    return MOE_ERR_INVALID_ARG;
-  if (s->renorm != 0 && s->renorm != 1) return MOE_ERR_INVALID_ARG;
-  if (s->x_dtype != MOE_X_BF16 && s->x_dtype != MOE_X_F32) return MOE_ERR_INVALID_ARG;
-  if (s->w_format != MOE_W_BF16 && s->w_format != MOE_W_INT4_G32) return MOE_ERR_INVALID_ARG;
-  if (s->T > (1 << 24) || s->d % 64 || s->d < 64 || s->d > 8192) return MOE_ERR_UNSUPPORTED;
-  if (s->E > kMaxE || s->k > kMaxK || s->k > s->E) return MOE_ERR_UNSUPPORTED;
-  if (s->f % 32 || s->f > 8192 || s->F % 32 || s->F > 16384) return MOE_ERR_UNSUPPORTED;
-  if (s->w_format == MOE_W_INT4_G32 && (s->k != 1 || s->T > 256)) return MOE_ERR_UNSUPPORTED;
-  return MOE_OK;
 }
 
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -380,7 +380,7 @@ bool weights_ok(const moe_shape_t* s, const moe_weights_t* w) {
 
 extern "C" {
 
-int32_t moe_abi_version(void) { return 1; }
+int32_t moe_abi_version(void) { return 2; }
 
 const char* moe_status_string(moe_status_t st) {
   switch (st) {
@@ -526,9 +526,16 @@ moe_status_t moe_combine(const moe_shape_t* shape, const void* y_perm, const voi
 
 moe_status_t moe_bias_update(int32_t E, int64_t tokens_times_k, const int32_t* load, float gamma,
                              float* bias, void* stream) {
-  if (E < 1 || E > kMaxE || tokens_times_k < 0 || !load || !bias) return MOE_ERR_INVALID_ARG;
+  if (E < 1 || E > kMaxE || (tokens_times_k < 0 && tokens_times_k != MOE_TK_FROM_LOAD) || !load || !bias)
+    return MOE_ERR_INVALID_ARG;
   return cuda_status(
       launch_bias_update(E, tokens_times_k, load, gamma, bias, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_load_balance(int32_t E, const int32_t* load, moe_balance_t* balance, void* stream) {
+  if (E < 1 || E > kMaxE || !load || !balance || (reinterpret_cast<uintptr_t>(balance) & 7u))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_bias_update(E, 0, load, 0.f, nullptr, static_cast<cudaStream_t>(stream), balance));
 }
 
 size_t moe_layer_workspace_size(const moe_shape_t* shape) {
@@ -586,7 +593,8 @@ moe_status_t layer_fwd_impl(const moe_shape_t* shape, const void* x, const float
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_router) || !aligned16(out) ||
       (residual && !aligned16(residual)) || !aligned16(workspace) ||
-      (dbg && dbg->scores && !aligned16(dbg->scores)))
+      (dbg && dbg->scores && !aligned16(dbg->scores)) ||
+      (dbg && dbg->balance && (reinterpret_cast<uintptr_t>(dbg->balance) & 7u)))
     return MOE_ERR_INVALID_ARG;
   if (ws_bytes < moe_layer_workspace_size(shape)) return MOE_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -659,15 +667,16 @@ moe_status_t layer_fwd_impl(const moe_shape_t* shape, const void* x, const float
   const bool direct = int4 && !xf && (long long)T * k <= kDirectMaxPairs &&
                       (shape->F == 0 || int4_skinny(shape)) &&
                       !(dbg && (dbg->offsets || dbg->perm_tok || dbg->inv_pos));
-  const bool need_load = update_bias || (dbg && dbg->load);
+  moe_balance_t* balance = dbg ? dbg->balance : nullptr;
+  const bool need_load = update_bias || (dbg && dbg->load) || balance;
   if (direct) {
     if (need_load && cudaMemsetAsync(L.load, 0, sizeof(int32_t) * E, rs) != cudaSuccess)
       return MOE_ERR_CUDA;
     RouterArgs ra{x, xf, w_router, logit_offset, bias, dbg ? dbg->scores : nullptr, L.idx, L.gate,
                   need_load ? L.load : nullptr, nullptr, ct, T, shape->d, E, k, shape->renorm};
     cudaError_t e = run_router(ra, L.router, rs);
-    if (e == cudaSuccess && update_bias)
-      e = launch_bias_update(E, (long long)T * k, L.load, gamma, bias, rs);
+    if (e == cudaSuccess && (update_bias || balance))
+      e = launch_bias_update(E, (long long)T * k, L.load, gamma, update_bias ? bias : nullptr, rs, balance);
     if (e == cudaSuccess && cache) {
       if (prof) prof_mark("cache_fetch", rs);
       e = launch_cache_fetch(L.idx, T * k, E, cache->slots, cache->view, cache->host_src,
@@ -705,7 +714,7 @@ moe_status_t layer_fwd_impl(const moe_shape_t* shape, const void* x, const float
     e = launch_scatter(L.idx, L.perm.counts, T, k, E, ct, L.offsets, nullptr,
                        update_bias ? bias : nullptr, gamma, (long long)T * k, L.perm_tok,
                        L.inv_pos, x, xf, shape->d, L.ffn.xp, (xf && shape->F) ? L.ffn.xb : nullptr,
-                       rs, int4 ? L.active : nullptr);
+                       rs, int4 ? L.active : nullptr, balance);
   if (e == cudaSuccess && cache) {
     if (prof) prof_mark("cache_fetch", rs);
     e = launch_cache_fetch(L.idx, T * k, E, cache->slots, cache->view, cache->host_src, cache->expert_bytes,

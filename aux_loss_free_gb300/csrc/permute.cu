@@ -55,11 +55,50 @@ __device__ __forceinline__ void copy_row_bf16(const void* x, int x_is_f32, long 
 }
 
 __global__ void count_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int chunk_tokens,
-                             int32_t* __restrict__ counts) {
+                             int32_t* __restrict__ counts, int* status) {
   const long long p = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (p >= (long long)T * k) return;
   const int t = (int)(p / k);
-  atomicAdd(&counts[(long long)(t / chunk_tokens) * E + idx[p]], 1);
+  const int e = idx[p];
+  if (e < 0 || e >= E) {  // not counted: a bad id must not write past the count table
+    atomicOr(status, kDevCheck);
+    return;
+  }
+  atomicAdd(&counts[(long long)(t / chunk_tokens) * E + e], 1);
+}
+
+// Balance statistics of load[0..E) (moe_balance_t) by one warp; lane 0 writes them.
+// The ratios are the fp32 values nearest to the exact rationals: the fp64 quotient of
+// the two exact integers is correctly rounded, and rounding it again to fp32 gives the
+// nearest fp32 for denominators below 2^28 (the exact quotient then never lies within
+// half an fp64 ulp of an fp32 rounding boundary unless it is one).
+__device__ __forceinline__ void warp_balance(const int32_t* load, int E, moe_balance_t* out, int lane) {
+  int mx = 0, mn = 0x7FFFFFFF, dead = 0;
+  long long sum = 0;
+  for (int e = lane; e < E; e += 32) {
+    const int v = load[e];
+    mx = max(mx, v);
+    mn = min(mn, v);
+    dead += v == 0;
+    sum += v;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mx = max(mx, __shfl_xor_sync(FULL, mx, o));
+    mn = min(mn, __shfl_xor_sync(FULL, mn, o));
+    dead += __shfl_xor_sync(FULL, dead, o);
+    sum += __shfl_xor_sync(FULL, sum, o);
+  }
+  if (lane == 0) {
+    out->pairs = sum;
+    out->max_load = mx;
+    out->min_load = mn;
+    out->dead_experts = dead;
+    const double pe = (double)sum;
+    out->max_over_mean = sum > 0 ? __double2float_rn(__ddiv_rn((double)mx * E, pe)) : 0.f;
+    out->min_over_mean = sum > 0 ? __double2float_rn(__ddiv_rn((double)mn * E, pe)) : 0.f;
+    out->dead_fraction = __double2float_rn(__ddiv_rn((double)dead, (double)E));
+  }
 }
 
 constexpr int SC_THREADS = 256;
@@ -79,7 +118,8 @@ __global__ void __launch_bounds__(SC_THREADS) scatter_kernel(
     int E, int chunk_tokens, int32_t* __restrict__ offsets, int32_t* __restrict__ load_out,
     float* bias, float gamma, long long tokens_times_k, int32_t* __restrict__ perm_tok,
     int32_t* __restrict__ inv_pos, const void* __restrict__ x, int x_is_f32, int d,
-    uint16_t* __restrict__ xp, uint16_t* __restrict__ xb, int32_t* __restrict__ active) {
+    uint16_t* __restrict__ xp, uint16_t* __restrict__ xb, int32_t* __restrict__ active,
+    moe_balance_t* __restrict__ balance, int* status) {
   __shared__ int32_t run[kMaxE];
   __shared__ int32_t tot_e[kMaxE];
   __shared__ int32_t off[kMaxE + 1];
@@ -156,6 +196,7 @@ __global__ void __launch_bounds__(SC_THREADS) scatter_kernel(
       if (tid == 0) active[kMaxE] = n;
     }
     for (int i = tid; i <= E; i += SC_THREADS) offsets[i] = off[i];
+    if (balance && warp == 1) warp_balance(tot_e, E, balance, lane);
     if (tid < E) {
       if (load_out) load_out[tid] = tot_e[tid];
       if (bias) {
@@ -169,8 +210,10 @@ __global__ void __launch_bounds__(SC_THREADS) scatter_kernel(
   __syncthreads();
 
   // ---- 2. pairs of the earlier blocks of the same chunk come first
-  for (long long q = chunk * chunk_tokens * k + tid; q < p_begin; q += SC_THREADS)
-    atomicAdd(&run[idx[q]], 1);
+  for (long long q = chunk * chunk_tokens * k + tid; q < p_begin; q += SC_THREADS) {
+    const int ex = idx[q];
+    if (ex >= 0 && ex < E) atomicAdd(&run[ex], 1);
+  }
   __syncthreads();
 
   // ---- 3. rank, scatter, gather
@@ -179,10 +222,15 @@ __global__ void __launch_bounds__(SC_THREADS) scatter_kernel(
     if (warp == 0) {
       for (int b = 0; b < n; b += 32) {
         const int q = b + lane;
-        const bool valid = q < n;
-        const int ex = valid ? idx[r0 + q] : -1;
+        int ex = q < n ? idx[r0 + q] : -1;
+        if (q < n && (ex < 0 || ex >= E)) {  // a bad id is not ranked (the count skipped it)
+          atomicOr(status, kDevCheck);
+          ex = -1;
+        }
+        const bool valid = ex >= 0;
         const unsigned peers = __match_any_sync(FULL, ex);
         const int rank = __popc(peers & ((1u << lane) - 1u));
+        if (q < n && !valid) s_pos[q] = -1;  // the row gather skips it
         if (valid) {
           const int pos = run[ex] + rank;
           const long long pr = r0 + q;
@@ -201,6 +249,7 @@ __global__ void __launch_bounds__(SC_THREADS) scatter_kernel(
     if (xp) {
 #pragma unroll 2
       for (int q = warp; q < n; q += SC_THREADS / 32) {
+        if (s_pos[q] < 0) continue;
         const int st = s_tok[q];
         const int t = st >= 0 ? st : -1 - st;
         copy_row_bf16(x, x_is_f32, t, d, xp + (long long)s_pos[q] * d, lane);
@@ -228,11 +277,26 @@ __global__ void to_bf16_kernel(const float* __restrict__ x, long long n8, uint16
                                                pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
 }
 
+// One block of 256 threads (E <= 256).  tokens_times_k < 0: the global T*k is the sum
+// of the loads (each token contributes k pairs), taken here so that no host round trip
+// is needed after the loads were summed over replicas.
 __global__ void bias_update_kernel(int E, long long tokens_times_k, const int32_t* __restrict__ load,
-                                   float gamma, float* bias) {
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= E) return;
-  const long long diff = tokens_times_k - (long long)E * load[e];
+                                   float gamma, float* bias, moe_balance_t* balance) {
+  __shared__ long long s_part[8];
+  const int e = threadIdx.x, warp = e / 32, lane = e % 32;
+  const int v = e < E ? load[e] : 0;
+  if (balance && warp == 0) warp_balance(load, E, balance, lane);
+  if (tokens_times_k < 0) {
+    long long s = v;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(FULL, s, o);
+    if (lane == 0) s_part[warp] = s;
+    __syncthreads();
+    tokens_times_k = 0;
+    for (int w = 0; w < (int)(blockDim.x / 32); ++w) tokens_times_k += s_part[w];
+  }
+  if (e >= E || !bias) return;
+  const long long diff = tokens_times_k - (long long)E * v;
   const float step = diff > 0 ? gamma : (diff < 0 ? -gamma : 0.f);
   bias[e] = __fadd_rn(bias[e], step);
 }
@@ -343,7 +407,9 @@ __global__ void pack_gate_up_kernel(int width, int d, int block, const uint16_t*
 cudaError_t launch_count(const int32_t* idx, int T, int k, int E, int chunk_tokens,
                          int32_t* counts, cudaStream_t s) {
   const long long n = (long long)T * k;
-  count_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(idx, T, k, E, chunk_tokens, counts);
+  int* status = device_status_ptr();
+  if (!status) return cudaErrorInvalidDevicePointer;
+  count_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(idx, T, k, E, chunk_tokens, counts, status);
   return cudaGetLastError();
 }
 
@@ -351,13 +417,15 @@ cudaError_t launch_scatter(const int32_t* idx, const int32_t* counts, int T, int
                            int chunk_tokens, int32_t* offsets, int32_t* load_out, float* bias,
                            float gamma, long long tokens_times_k, int32_t* perm_tok,
                            int32_t* inv_pos, const void* x, int x_is_f32, int d, uint16_t* xp,
-                           uint16_t* xb, cudaStream_t s, int32_t* active) {
+                           uint16_t* xb, cudaStream_t s, int32_t* active, moe_balance_t* balance) {
   const int chunks = (T + chunk_tokens - 1) / chunk_tokens;
   const int block_tokens = chunk_tokens <= 128 ? 32 : chunk_tokens;
   const int blocks = (T + block_tokens - 1) / block_tokens;
+  int* status = device_status_ptr();
+  if (!status) return cudaErrorInvalidDevicePointer;
   return launch_pdl(scatter_kernel, dim3(blocks), dim3(SC_THREADS), 0, s, idx, counts, chunks, T, k,
                     E, chunk_tokens, offsets, load_out, bias, gamma, tokens_times_k, perm_tok,
-                    inv_pos, x, x_is_f32, d, xp, xb, active);
+                    inv_pos, x, x_is_f32, d, xp, xb, active, balance, status);
 }
 
 cudaError_t launch_gather(const void* x, int x_is_f32, const int32_t* perm_tok, long long rows,
@@ -375,8 +443,9 @@ cudaError_t launch_to_bf16(const float* x, long long n, uint16_t* xb, cudaStream
 }
 
 cudaError_t launch_bias_update(int E, long long tokens_times_k, const int32_t* load, float gamma,
-                               float* bias, cudaStream_t s) {
-  bias_update_kernel<<<(E + 255) / 256, 256, 0, s>>>(E, tokens_times_k, load, gamma, bias);
+                               float* bias, cudaStream_t s, moe_balance_t* balance) {
+  if (E < 1 || E > 256) return cudaErrorInvalidValue;
+  bias_update_kernel<<<1, 256, 0, s>>>(E, tokens_times_k, load, gamma, bias, balance);
   return cudaGetLastError();
 }
 

@@ -2,11 +2,11 @@
 // workspace.
 //
 // Who needs this: code that cannot hand the library device memory for scratch.
-// Examples are a plugin running inside a host framework whose memory pool it does
-// not own, a serving loop whose device-memory budget is fixed at start-up, or a
-// caller about to record its launches into a CUDA graph where a fresh cudaMalloc is
-// not allowed.  Those callers still pass their inputs and outputs; the per-chunk
-// count table lives in the file-scope array below instead of a workspace.
+// Examples are a plugin running inside a host framework that owns the device memory
+// pool and gives plugins no scratch, or a serving loop whose device-memory budget is
+// fixed at start-up and may not grow.  Those callers still pass their inputs and
+// outputs; the per-chunk count table lives in the file-scope array below instead of
+// a workspace.
 //
 // The array is a static __device__ symbol: every GPU that loads this library holds
 // its 128 KiB until the process exits.  Host code must not pass the symbol itself
@@ -27,7 +27,9 @@ constexpr size_t kNoAllocScratchInts = (size_t)kMaxCountEntries;
 static __device__ __align__(256) int32_t g_permute_scratch[kNoAllocScratchInts];
 
 // Device address of g_permute_scratch on the current device, looked up on the first
-// call made on that device (with it current) and cached; nullptr on failure.
+// call made on that device (with it current) and cached; nullptr on failure.  The
+// address belongs to the device's context as it was then: a cudaDeviceReset would
+// leave it stale, which is why the header rules out use of the library after one.
 int32_t* scratch_on_current_device() {
   static int32_t* ptrs[64] = {nullptr};
   static std::mutex mu;
@@ -51,10 +53,10 @@ using namespace moe;
 extern "C" moe_status_t moe_permute_noalloc(const moe_shape_t* shape, const int32_t* idx,
                                             int32_t* offsets, int32_t* perm_tok,
                                             int32_t* inv_pos, void* stream) {
-  if (!shape || !idx || !offsets || !perm_tok || !inv_pos) return MOE_ERR_INVALID_ARG;
-  if (shape->T < 1 || shape->E < 1 || shape->k < 1) return MOE_ERR_INVALID_ARG;
-  if (shape->T > (1 << 24) || shape->E > kMaxE || shape->k > kMaxK || shape->k > shape->E)
-    return MOE_ERR_UNSUPPORTED;
+  // The same validation, in the same order, as moe_permute.
+  const moe_status_t st = check_shape(shape);
+  if (st) return st;
+  if (!idx || !offsets || !perm_tok || !inv_pos) return MOE_ERR_INVALID_ARG;
   const int ct = permute_chunk_tokens(shape->T, shape->E);
   const int chunks = (shape->T + ct - 1) / ct;
   const size_t table = (size_t)chunks * shape->E;

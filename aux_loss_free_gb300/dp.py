@@ -3,7 +3,10 @@
 Replicas route their own tokens; the method's only cross-replica exchange is the sum
 of the per-expert loads before the bias update, so that every replica applies the
 same update computed from the global load (relay article, architecture paragraph:
-the bias moves by gamma times the sign of target minus load).
+the bias moves by gamma times the sign of target minus load).  The target is the
+global mean load, so it needs the global T*k: the sum of the summed loads, since every
+token adds exactly k pairs.  That holds whatever the shards' sizes (a batch that does
+not divide evenly, ragged batches), where world * (local T*k) would not.
 """
 from __future__ import annotations
 
@@ -19,8 +22,15 @@ def allreduce_load(load: torch.Tensor, group=None) -> int:
     return dist.get_world_size(group)
 
 
-def dp_bias_update(load: torch.Tensor, bias: torch.Tensor, tokens_times_k_local: int, gamma: float,
-                   group=None, stream=None) -> None:
-    """All-reduce the loads, then apply the bias update with the global T*k (device tensors)."""
-    world = allreduce_load(load, group)
-    _lib.moe_bias_update(bias.numel(), world * tokens_times_k_local, load, gamma, bias, stream)
+def global_tokens_times_k(summed_load: torch.Tensor) -> int:
+    """The global T*k from the loads summed over replicas (a host integer; reading a
+    device tensor synchronises with it)."""
+    return int(summed_load.sum(dtype=torch.int64).item())
+
+
+def dp_bias_update(load: torch.Tensor, bias: torch.Tensor, gamma: float, group=None, stream=None) -> None:
+    """All-reduce the loads, then apply the bias update with the global T*k (device
+    tensors).  The update kernel takes the global T*k as the sum of the summed loads
+    itself, so nothing is read back to the host."""
+    allreduce_load(load, group)
+    _lib.moe_bias_update(bias.numel(), _lib.MOE_TK_FROM_LOAD, load, gamma, bias, stream)

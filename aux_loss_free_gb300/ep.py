@@ -29,6 +29,7 @@ from __future__ import annotations
 import torch
 
 from . import _lib as L
+from .dp import allreduce_load, global_tokens_times_k
 from .layer import pack_gate_up, to_device_bf16
 
 
@@ -119,9 +120,10 @@ class EPRank:
         L.moe_combine(self.shape, y_back, s_out, state["inv_pos"], state["gate"], residual, out, stream=stream)
         return out
 
-    # 6. the bias update from the summed loads
-    def bias_update(self, global_load: torch.Tensor, global_tokens_times_k: int, stream=None):
-        L.moe_bias_update(self.spec.E, global_tokens_times_k, global_load, self.gamma, self.bias, stream=stream)
+    # 6. the bias update from the summed loads; tokens_times_k is the global T*k (the sum
+    # of the summed loads), or MOE_TK_FROM_LOAD to have the kernel take that sum itself
+    def bias_update(self, global_load: torch.Tensor, tokens_times_k: int, stream=None):
+        L.moe_bias_update(self.spec.E, tokens_times_k, global_load, self.gamma, self.bias, stream=stream)
 
 
 def rows_per_owner(counts: torch.Tensor) -> list[int]:
@@ -148,8 +150,9 @@ def ep_forward(rank: EPRank, x: torch.Tensor, out: torch.Tensor, update_bias: bo
     rank.combine(st, x, y_back, out, residual)
     if update_bias:
         load = st["load"].clone()
-        dist.all_reduce(load, op=dist.ReduceOp.SUM, group=group)
-        rank.bias_update(load, dist.get_world_size(group) * rank.t * rank.spec.k)
+        allreduce_load(load, group)
+        # The global T*k from the summed loads: right for shards of any sizes.
+        rank.bias_update(load, global_tokens_times_k(load))
     return out
 
 
@@ -177,5 +180,5 @@ def ep_forward_emulated(ranks: list[EPRank], xs: list[torch.Tensor], outs: list[
     if update_bias:
         load = torch.stack([s["load"] for s in st]).sum(dim=0, dtype=torch.int32)
         for r in ranks:
-            r.bias_update(load, world * r.t * r.spec.k)
+            r.bias_update(load, L.MOE_TK_FROM_LOAD)  # global T*k = sum of the summed loads
     return outs

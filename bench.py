@@ -410,7 +410,7 @@ def gpu_arm(args, rank, world, dist):
             if world > 1 and update:
                 # Data-parallel replicas: local loads, global sum, identical update.
                 L.forward(cur, nxt, update_bias=False, residual=res, debug=dbg_load)
-                dp_bias_update(load, L.bias, s.T * s.k, L.gamma)
+                dp_bias_update(load, L.bias, L.gamma)
             else:
                 L.forward(cur, nxt, update_bias=update, residual=res)
             cur = nxt
@@ -609,7 +609,7 @@ def gpu_train_arm(args, rank, world, dist):
     def step(x_in, dout, out):
         if world > 1:
             layer.forward(x_in, out, update_bias=False, debug=saved.debug)
-            dp_bias_update(saved.load, layer.bias, s.T * s.k, layer.gamma)
+            dp_bias_update(saved.load, layer.bias, layer.gamma)
         else:
             layer.forward(x_in, out, update_bias=True, debug=saved.debug)
         layer_backward(layer, x_in, saved, dout, grads)

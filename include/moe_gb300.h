@@ -92,6 +92,22 @@ typedef struct {
   const void* shared_down;
 } moe_weights_t;
 
+/* Expert-balance statistics of one routing result, computed on the device from the
+ * per-expert loads.  Relay article, section "Entrenamiento por relevos": the relay's
+ * dashboard tracks expert balance, and the top-2 paragraph reports that the fraction of
+ * dead experts stayed low.  This library's definitions (the pages give none): the mean
+ * load is pairs / E; an expert is dead when its load is 0.  Each ratio is the fp32
+ * value nearest to the exact rational (ties to even); 0 when pairs is 0. */
+typedef struct {
+  int64_t pairs;        /* sum of the loads: T*k (summed over replicas if the loads were) */
+  int32_t max_load;     /* largest load */
+  int32_t min_load;     /* smallest load */
+  int32_t dead_experts; /* experts with load 0 */
+  float max_over_mean;  /* max_load * E / pairs */
+  float min_over_mean;  /* min_load * E / pairs */
+  float dead_fraction;  /* dead_experts / E */
+} moe_balance_t;
+
 /* Optional intermediate outputs of moe_layer_fwd (any field may be NULL). */
 typedef struct {
   float* scores;      /* [T][E] fp32 sigmoid scores */
@@ -101,6 +117,7 @@ typedef struct {
   int32_t* offsets;   /* [E+1] */
   int32_t* perm_tok;  /* [T*k] */
   int32_t* inv_pos;   /* [T][k] */
+  moe_balance_t* balance;  /* one struct (device, 8-byte aligned): this forward's balance */
 } moe_debug_t;
 
 /* ABI version; bumped on any incompatible change. */
@@ -148,21 +165,26 @@ moe_status_t moe_permute(const moe_shape_t* shape, const int32_t* idx, int32_t* 
                          size_t ws_bytes, void* stream);
 
 /* moe_permute without a workspace, for callers that cannot give the library device
- * memory: a plugin inside a framework that owns the memory pool, a serving loop
- * whose device-memory budget was fixed at start-up, or code about to be captured
- * into a CUDA graph where a new cudaMalloc is not allowed.  The pages have no
- * counterpart to this call; it computes exactly what moe_permute computes.
- * Arguments as moe_permute (idx, offsets, perm_tok, inv_pos are caller-owned).
+ * memory: a plugin inside a framework that owns the device memory pool and hands out
+ * no scratch, or a serving loop whose device-memory budget was fixed at start-up and
+ * may not grow.  The pages have no counterpart to this call; it computes what
+ * moe_permute computes and validates the shape as moe_permute does (same status for
+ * the same shape).  Arguments as moe_permute (idx, offsets, perm_tok, inv_pos are
+ * caller-owned).
  * Scratch: a library-owned static device array of 32768 int32 (128 KiB), held by
  * every GPU that loads the library until the process exits.  Every supported shape
  * fits (the chunking keeps the count table within 32768 entries); a shape that
  * would not fit returns MOE_ERR_UNSUPPORTED before any launch.  The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress, with that
  * device current) and caches it: make that first call before any stream capture.
+ * The cached address belongs to the device's context as it was at that call: after
+ * cudaDeviceReset the library must not be used again in the process.
  * The call allocates and frees nothing.  All calls share the one array, which
  * keeps the previous call's contents (the call clears what must start at zero), so
  * calls that can overlap on the GPU -- on different streams, or from different
- * host threads -- race: serialise them. */
+ * host threads -- race: serialise them.  An expert id outside [0, E) in idx is not
+ * counted; it sets MOE_ERR_DEVICE in the device status word (moe_device_status) and
+ * the outputs are then unspecified. */
 moe_status_t moe_permute_noalloc(const moe_shape_t* shape, const int32_t* idx, int32_t* offsets,
                                  int32_t* perm_tok, int32_t* inv_pos, void* stream);
 
@@ -212,9 +234,18 @@ moe_status_t moe_ep_regroup(int32_t world, int32_t experts_local, const int32_t*
  * recipe): bias[e] = fl32(bias[e] + gamma * sign(tokens_times_k - E * load[e])),
  * i.e. the sign of (target - load) with target = T*k/E and sign(0) = 0.
  * tokens_times_k is the GLOBAL T*k when `load` was summed over data-parallel
- * replicas (the only cross-replica exchange of the method). In place on `bias`. */
+ * replicas (the only cross-replica exchange of the method), or MOE_TK_FROM_LOAD: the
+ * kernel then sums `load` itself, which is the global T*k exactly (every token adds k
+ * pairs), whatever the replicas' shard sizes, with no host round trip.  Other negative
+ * values return MOE_ERR_INVALID_ARG.  In place on `bias`. */
+#define MOE_TK_FROM_LOAD (-1)
 moe_status_t moe_bias_update(int32_t E, int64_t tokens_times_k, const int32_t* load,
                              float gamma, float* bias, void* stream);
+
+/* Expert-balance statistics (moe_balance_t) of `load` [E] int32 (device), written to
+ * *balance (device, 8-byte aligned) by one block.  For loads summed over replicas as
+ * well as a single forward's. */
+moe_status_t moe_load_balance(int32_t E, const int32_t* load, moe_balance_t* balance, void* stream);
 
 /* The whole layer: route, permute, gather, grouped expert FFN, shared expert,
  * combine and (if update_bias) the bias update, enqueued with no host

@@ -246,6 +246,54 @@ def bias_update(bias: np.ndarray, load: np.ndarray, tokens_times_k: int, gamma: 
     return out
 
 
+def nearest_f32(num: int, den: int) -> np.float32:
+    """The fp32 value nearest to the exact rational num / den (ties to even), den > 0.
+
+    Exact arithmetic: the quotient is scaled by a power of two so that its integer part
+    has 25 to 26 bits, the 24-bit significand is chosen by integer rounding (ties to the
+    even significand), and the power of two is put back.  Plain integers only.
+    """
+    if num == 0:
+        return np.float32(0.0)
+    if num < 0:
+        return -nearest_f32(-num, den)
+    # num / den = q * 2^e with 2^23 <= q < 2^24 after rounding.
+    e = num.bit_length() - den.bit_length() - 24
+    while True:
+        n, d = (num, den << e) if e >= 0 else (num << -e, den)
+        if n >= d << 24:
+            e += 1
+        elif n < d << 23:
+            e -= 1
+        else:
+            break
+    q, r = divmod(n, d)
+    if 2 * r > d or (2 * r == d and q % 2 == 1):
+        q += 1
+    return np.float32(np.ldexp(np.float64(q), e))  # q <= 2^24: exact in fp64 and fp32
+
+
+def balance_stats(load, E: int) -> dict:
+    """Expert-balance statistics of one routing result (per-expert loads).
+
+    Relay article, section "Entrenamiento por relevos": the relay's dashboard tracks
+    expert balance, and the top-2 paragraph says the fraction of dead experts stayed
+    low.  The pages define neither; this build's reading: the mean load is pairs / E
+    with pairs = sum of the loads; max/mean = max_load * E / pairs, min/mean likewise;
+    an expert is dead when its load is 0, dead fraction = dead / E.  Each ratio is the
+    fp32 value nearest to the exact rational (0 when pairs is 0).
+    """
+    load = [int(v) for v in np.asarray(load).ravel()]
+    assert len(load) == E
+    pairs = sum(load)
+    mx, mn = max(load), min(load)
+    dead = sum(1 for v in load if v == 0)
+    return dict(pairs=pairs, max_load=mx, min_load=mn, dead_experts=dead,
+                max_over_mean=nearest_f32(mx * E, pairs) if pairs else np.float32(0.0),
+                min_over_mean=nearest_f32(mn * E, pairs) if pairs else np.float32(0.0),
+                dead_fraction=nearest_f32(dead, E))
+
+
 # ---------------------------------------------------------------------------
 # int4 container (symmetric, group 32 along the input dimension, fp16 scales).
 # ---------------------------------------------------------------------------

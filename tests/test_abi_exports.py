@@ -42,7 +42,7 @@ def test_binding_covers_every_declared_symbol():
 
 def test_pure_host_entry_points(lib_path):
     lib = M.load_library(lib_path)
-    assert lib.moe_abi_version() == 1
+    assert lib.moe_abi_version() == 2
     assert lib.moe_status_string(0) == b"ok"
     assert [lib.moe_gate_up_block(w) for w in (512, 2048, 64, 32, 96)] == [128, 128, 64, 32, 32]
 
@@ -70,6 +70,33 @@ def test_host_validation_rejects_bad_shapes_before_any_launch(lib_path):
     assert M.moe_route_workspace_size(M.make_shape(64, 1024, 64, 512, 2048, 2)) == 0  # small T: CUDA-core router
     assert M.moe_route_workspace_size(M.make_shape(64, 64, 8, 32, 128, 2, x_dtype=M.MOE_X_F32)) == 0
     assert lib.moe_bias_update(0, 16, None, 1e-3, None, None) == 1
+    p = ctypes.c_void_p(16)  # never dereferenced: every call below fails validation first
+    assert lib.moe_bias_update(64, -2, p, ctypes.c_float(1e-3), p, None) == 1  # only -1 means "sum the loads"
+    assert lib.moe_load_balance(0, p, p, None) == 1                       # no experts
+    assert lib.moe_load_balance(64, p, ctypes.c_void_p(20), None) == 1    # balance not 8-byte aligned
+    assert lib.moe_load_balance(64, None, p, None) == 1
+
+
+def test_noalloc_permute_validates_like_permute(lib_path):
+    """moe_permute_noalloc returns the status moe_permute returns for every bad shape
+    (both validate before touching the device)."""
+    lib = M.load_library(lib_path)
+    p = ctypes.c_void_p(16)
+    bad = [
+        M.make_shape(0, 1024, 64, 512, 2048, 2),
+        M.make_shape(16, 1000, 64, 512, 2048, 2),
+        M.make_shape(16, 1024, 300, 512, 2048, 2),
+        M.make_shape(16, 1024, 4, 512, 2048, 5),
+        M.make_shape(16, 1024, 64, 500, 2048, 2),
+        M.make_shape(16, 1024, 64, 512, 2048, 2, renorm=True, x_dtype=7),
+        M.make_shape(16, 1024, 64, 512, 2048, 2, w_format=M.MOE_W_INT4_G32),
+    ]
+    for s in bad:
+        want = lib.moe_permute(ctypes.byref(s), p, p, p, p, p, 1 << 20, None)
+        assert want != 0
+        assert lib.moe_permute_noalloc(ctypes.byref(s), p, p, p, p, None) == want
+    good = M.make_shape(64, 1024, 64, 512, 2048, 2)
+    assert lib.moe_permute_noalloc(ctypes.byref(good), None, p, p, p, None) == 1  # null idx
 
 
 def test_expert_parallel_calls_validate_on_the_host(lib_path):

@@ -249,14 +249,16 @@ def test_layer_fwd_matches_oracle(name, kw, with_residual):
 
 def test_skewed_bias_trajectory_bitexact():
     """50 forward + bias-update steps on the Zipf-skewed router: the GPU's bias after
-    every step equals the oracle's, and the max/mean load falls from its start."""
+    every step equals the oracle's, the fused balance statistics equal the oracle's
+    (bit for bit), and the max/mean load falls from its start."""
     s = CONFIGS["skew"]
     host = make_layer(s, "skew")
     layer = LayerOnDevice(s, host, DEV)
     x = to_device_tokens(host["x"], DEV)
     scores = torch.empty(s.T, s.E, dtype=torch.float32, device=DEV)
     load = torch.empty(s.E, dtype=torch.int32, device=DEV)
-    dbg = M.make_debug(scores=scores, load=load)
+    bal = torch.zeros(M.BALANCE_BYTES, dtype=torch.uint8, device=DEV)
+    dbg = M.make_debug(scores=scores, load=load, balance=bal)
     out = torch.empty(s.T, s.d, dtype=torch.bfloat16, device=DEV)
     bias = host["bias"].copy()
     ratios = []
@@ -267,6 +269,10 @@ def test_skewed_bias_trajectory_bitexact():
         idx = O.topk_select(sc, bias, s.k)
         ld = O.expert_load(idx, s.E)
         assert np.array_equal(load.cpu().numpy(), ld), step
+        # The fused balance output (max/mean, min/mean, dead fraction) of every step.
+        got, want = M.balance_from_bytes(bal), O.balance_stats(ld, s.E)
+        for key in want:
+            assert np.float64(got[key]) == np.float64(want[key]), (step, key)
         bias = O.bias_update(bias, ld, s.T * s.k, s.gamma)
         assert np.array_equal(layer.bias.cpu().numpy().view(np.uint32), bias.view(np.uint32)), step
         ratios.append(ld.max() / ld.mean())

@@ -1,9 +1,12 @@
 """Two CPU ranks (gloo) run the data-parallel balancing step on their token shards.
 
 Each rank routes its shard with the oracle, the loads are summed with the package's
-allreduce_load, and each rank applies the bias update with the global T*k.  Every
-rank must end with the bias that the single-process full batch gives, bit for bit,
-and each shard's routing must equal the full batch's routing of those tokens.
+allreduce_load, and each rank applies the bias update with the global T*k that the
+package's global_tokens_times_k takes from the summed loads.  The batch (97 tokens)
+does not split evenly (shards of 49 and 48), so world * (local T*k) would be wrong for
+both ranks.  Every rank must end with the bias that the single-process full batch
+gives, bit for bit, and each shard's routing must equal the full batch's routing of
+those tokens.
 """
 import os
 import socket
@@ -13,7 +16,7 @@ import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
 
-from aux_loss_free_gb300.dp import allreduce_load
+from aux_loss_free_gb300.dp import allreduce_load, global_tokens_times_k
 from oracle import moe_oracle as O
 from synth import CONFIGS, make_layer
 
@@ -25,7 +28,7 @@ def _free_port():
 
 
 def _shape():
-    return CONFIGS["tiny"].replace(T=96, E=16)
+    return CONFIGS["tiny"].replace(T=97, E=16)  # shards of 49 and 48 tokens
 
 
 def _rank_main(rank, world, port, out_dir):
@@ -41,7 +44,9 @@ def _rank_main(rank, world, port, out_dir):
         idx = O.topk_select(scores, bias, s.k)
         load = torch.from_numpy(O.expert_load(idx, s.E).astype(np.int32))
         n = allreduce_load(load)
-        new_bias = O.bias_update(bias, load.numpy(), n * len(shard) * s.k, s.gamma)  # global T*k
+        tk = global_tokens_times_k(load)
+        assert tk == s.T * s.k != n * len(shard) * s.k
+        new_bias = O.bias_update(bias, load.numpy(), tk, s.gamma)
         np.save(os.path.join(out_dir, f"bias_{rank}.npy"), new_bias)
         np.save(os.path.join(out_dir, f"idx_{rank}.npy"), idx)
         np.save(os.path.join(out_dir, f"load_{rank}.npy"), load.numpy())
@@ -61,6 +66,10 @@ def test_two_rank_bias_update_equals_full_batch(tmp_path):
     load = O.expert_load(idx, s.E)
     want = O.bias_update(bias, load, s.T * s.k, s.gamma)
     shards = np.array_split(np.arange(s.T), world)
+    # The case can tell the formulas apart: world * (a shard's T*k) moves some bias
+    # differently from the global T*k (an expert's E * load equals a wrong target).
+    wrong = [O.bias_update(bias, load, world * len(sh) * s.k, s.gamma) for sh in shards]
+    assert any(not np.array_equal(w.view(np.uint32), want.view(np.uint32)) for w in wrong)
     for r in range(world):
         got = np.load(tmp_path / f"bias_{r}.npy")
         assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
@@ -115,7 +124,7 @@ class _OracleRank:
 
 
 def _ep_shape():
-    return CONFIGS["tiny"].replace(T=96, E=16)
+    return CONFIGS["tiny"].replace(T=97, E=16)  # unequal shards: 49 and 48 tokens
 
 
 def _ep_rank_main(rank, world, port, out_dir):

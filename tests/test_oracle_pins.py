@@ -516,3 +516,96 @@ def test_expert_cache_invariants_and_textbook_cases():
     ws = [np.array([s % slots]) for s in range(60)]
     r4 = C.lru_cache_run(E, slots, ws)
     assert sum(r4["misses"]) == slots and all(m == 0 for m in r4["misses"][slots:])
+
+
+# ---------------------------------------------------------------- combine residual
+
+
+def test_golden_combine_with_and_without_residual(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "combine_residual_worked.json")))
+    Y, sh = np.array(g["Y"]), np.array(g["shared"])
+    inv, gate, res = np.array(g["inv_pos"]), np.array(g["gate"]), np.array(g["residual"])
+    assert np.array_equal(O.combine(Y, sh, inv, gate), np.array(g["out_without_residual"]))
+    assert np.array_equal(O.combine(Y, sh, inv, gate, residual=res), np.array(g["out_with_residual"]))
+
+
+def test_combine_residual_is_added_once():
+    # Dyadic values on a coarse grid: every sum below is exact in fp64, so the residual
+    # must appear exactly once (a dropped or doubled residual fails the equality).
+    rng = np.random.default_rng(11)
+    T, k, d = 16, 3, 8
+    Y = rng.integers(-64, 64, (T * k, d)) / 8.0
+    sh = rng.integers(-64, 64, (T, d)) / 8.0
+    res = rng.integers(-64, 64, (T, d)) / 8.0
+    inv = rng.permutation(T * k).reshape(T, k)
+    gate = rng.integers(1, 8, (T, k)) / 8.0
+    base = O.combine(Y, sh, inv, gate)
+    with_res = O.combine(Y, sh, inv, gate, residual=res)
+    assert np.array_equal(with_res - res, base)
+    assert not np.array_equal(with_res, base)
+
+
+def test_layer_with_residual_equals_per_token_dense_mixture_plus_x():
+    s, P = _tiny_layer()
+    xb = O.round_to_bf16(P["x"])
+    r = O.layer_forward(**P, residual=xb)
+    r0 = O.layer_forward(**P)
+    for t in range(s.T):
+        want = xb[t] + O.swiglu_ffn(xb[t:t + 1], P["s_gate"], P["s_up"], P["s_down"])[0]
+        for j in range(s.k):
+            e = r["idx"][t, j]
+            want = want + r["gate"][t, j] * O.swiglu_ffn(xb[t:t + 1], P["w_gate"][e], P["w_up"][e],
+                                                        P["w_down"][e])[0]
+        assert np.allclose(r["out"][t], want, rtol=0, atol=1e-13)
+    assert np.allclose(r["out"] - xb, r0["out"], rtol=0, atol=1e-13)
+
+
+# ---------------------------------------------------------------- balance statistics
+
+
+def test_golden_balance_stats(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "balance_worked.json")))
+    for c in g["cases"]:
+        got = O.balance_stats(c["load"], len(c["load"]))
+        for key in ("pairs", "max_load", "min_load", "dead_experts"):
+            assert got[key] == c[key], (c["load"], key)
+        for key in ("max_over_mean", "min_over_mean", "dead_fraction"):
+            bits = int(np.float32(got[key]).view(np.uint32))
+            assert bits == int(c[key + "_bits"], 16), (c["load"], key, hex(bits))
+
+
+def test_nearest_f32_against_correctly_rounded_division():
+    # Python's int / int is the correctly rounded fp64 quotient (a library routine);
+    # rounding that to fp32 gives the nearest fp32 whenever the denominator is below
+    # 2^28 (the exact quotient cannot lie within half an fp64 ulp of an fp32 rounding
+    # boundary without being one).  Also exact cases and ties.
+    rng = np.random.default_rng(3)
+    for _ in range(20000):
+        a = int(rng.integers(0, 1 << 40))
+        b = int(rng.integers(1, 1 << 27))
+        assert O.nearest_f32(a, b) == np.float32(a / b), (a, b)
+    assert O.nearest_f32(7, 7) == np.float32(1.0)
+    # 1 + 2^-24 is halfway between 1 and the next fp32: ties to the even significand (1).
+    assert O.nearest_f32((1 << 24) + 1, 1 << 24) == np.float32(1.0)
+    # 1 + 3 * 2^-24 is halfway between 1 + 2^-23 and 1 + 2^-22: ties to even (1 + 2^-22).
+    assert O.nearest_f32((1 << 24) + 3, 1 << 24) == np.float32(1.0 + 2.0 ** -22)
+
+
+def test_balance_stats_properties():
+    rng = np.random.default_rng(5)
+    for E in (1, 3, 8, 64, 256):
+        for _ in range(20):
+            load = rng.integers(0, 50, E)
+            load[rng.random(E) < 0.3] = 0
+            st = O.balance_stats(load, E)
+            assert st["pairs"] == int(load.sum())
+            assert st["max_load"] == int(load.max()) and st["min_load"] == int(load.min())
+            assert st["dead_experts"] == int((load == 0).sum())
+            if st["pairs"]:
+                assert st["min_over_mean"] <= 1.0 <= st["max_over_mean"] <= E
+                # Within half an fp32 ulp of the exact ratio.
+                exact = st["max_load"] * E / st["pairs"]
+                assert abs(float(st["max_over_mean"]) - exact) <= np.spacing(np.float32(exact)) / 2 * 1.0000001
+    # Every pair on one expert: max/mean = E, every other expert dead.
+    st = O.balance_stats([0, 0, 12, 0], 4)
+    assert st["max_over_mean"] == 4.0 and st["dead_fraction"] == 0.75 and st["min_over_mean"] == 0.0
