@@ -76,21 +76,6 @@ constexpr int DH_BUF = 32 * DH_COLS * 2;                 // 2 KB
 constexpr int DH_BYTES = EPI_WARPS * 2 * DH_BUF;         // 16 KB
 constexpr int DYN_SMEM = STAGES * STAGE_BYTES + DH_BYTES + 1024;
 constexpr unsigned FULL = 0xFFFFFFFFu;
-// Router and scatter tiles (fused routing) keep their per-CTA working set in the dh
-// staging area, which a launch with fused routing never uses for dh.  Offsets in
-// 4-byte words.
-constexpr int RS_BIAS = 0;     // [64] f32 bias
-constexpr int RS_OFF = 64;     // [64] f32 logit offset
-constexpr int RS_RUN = 128;    // [64] i32 running per-expert counts of the chunk
-constexpr int RS_PRE = 192;    // [128] i32 partial sums over earlier chunks, then [64] totals of them
-constexpr int RS_TOT = 320;    // [128] i32 partial sums over all chunks, then [64] expert totals
-constexpr int RS_EOFF = 448;   // [65] i32 expert offsets
-constexpr int RS_BASE = 520;   // [64] i32 first row of each expert's share of the chunk
-constexpr int RS_IDX = 1024;   // [128 * kMaxK] i32 experts of the chunk's pairs, then their rows
-constexpr int RS_RANK = 2048;  // [128 * kMaxK] i32 rank of each pair inside the chunk
-constexpr int RS_WORDS = 3072;
-static_assert(RS_WORDS * 4 <= DH_BYTES, "fused-routing scratch fits the dh staging area");
-static_assert(HM * kMaxK <= 1024, "one chunk's pairs fit the scratch lists");
 
 struct OperandSet {
   // With kblock set (K a multiple of 64), both maps view a [rows][K] matrix as (64
@@ -151,18 +136,7 @@ struct Params {
   // may be issued before the dependency wait (the A copies and every output wait).
   int early;
   int E, k;
-  // Fused routing (route_tiles > 0; the launch then holds no routed or chained set):
-  // positions [0, route_tiles) are router tiles (256-row block m = position), positions
-  // [scatter_at, scatter_at + route_tiles) scatter tiles (block m = position -
-  // scatter_at), every other position a tile of the shared set, in order.
-  OperandSet route;  // A = tokens, B = split router weight [3E][d], bn = 3E, EPI_ROUTER
-  RouteFusion rf;
-  int route_tiles, scatter_at, route_chunks;
 };
-
-// Tile kinds of the fused-routing launch (Tile::set values beyond the operand sets).
-constexpr int SET_ROUTER = 3;
-constexpr int SET_SCATTER = 4;
 
 struct Tile {
   int set;    // 0 shared, 1 routed
@@ -204,12 +178,6 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
-}
-
-// Arrive on a barrier of either CTA of the pair (shared::cluster address) with release
-// semantics at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // TMA tile load whose completion is counted on a barrier of the CTA pair (here the
@@ -288,50 +256,9 @@ __device__ __forceinline__ int find_group(const int* s_cum, int E, int r) {
   return lo;
 }
 
-// The operand set a tile reads (router tiles: the fused routing's set).
-__device__ __forceinline__ const OperandSet& operand_set(const Params& p, int set) {
-  return set == 2 ? p.chain : (set == 1 ? p.routed : (set >= SET_ROUTER ? p.route : p.shared));
-}
-
-// Kind of position `pos` of a launch with fused routing (SET_ROUTER, SET_SCATTER or 0
-// for the shared set) and its index among the tiles of that kind.
-__device__ __forceinline__ int fused_kind(const Params& p, int pos, int* index) {
-  const int nr = p.route_tiles;
-  if (pos < nr) {
-    *index = pos;
-    return SET_ROUTER;
-  }
-  if (pos >= p.scatter_at && pos < p.scatter_at + nr) {
-    *index = pos - p.scatter_at;
-    return SET_SCATTER;
-  }
-  *index = pos - nr - (pos >= p.scatter_at + nr ? nr : 0);
-  return 0;
-}
-
 // `total` here is the end of the shared and routed tiles; chained tiles follow it.
 __device__ __forceinline__ Tile decode_tile(const Params& p, int tile, int shared_tiles,
                                             const int* s_off, const int* s_cum, int total) {
-  if (p.route_tiles) {
-    int i;
-    const int kind = fused_kind(p, tile, &i);
-    if (kind) {
-      Tile t;
-      t.set = kind;
-      t.row0 = i * BM;
-      t.rend = p.route.rows;
-      t.n0 = 0;
-      t.brow = 0;
-      t.k0 = 0;
-      t.klen = p.route.k_total;
-      t.group = 0;
-      t.bk = 0;
-      t.mblk = i;
-      return t;
-    }
-    tile = i;              // a shared tile
-    total = shared_tiles;  // no routed or chained set beside it
-  }
   if (tile >= total) {
     // Chained tile: routed 256-row block m (the same blocks as the routed set's, whose
     // tile table counts nt1 tiles per block), column tile n.
@@ -416,11 +343,7 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, int tile, int share
 
 // Which operand set a tile belongs to (1 = routed), by the same interleave as
 // decode_tile: all the MMA issuer needs, without the search over the groups.
-__device__ __forceinline__ int tile_set(const Params& p, int tile, int shared_tiles, int total) {
-  if (p.route_tiles) {
-    int i;
-    return fused_kind(p, tile, &i);
-  }
+__device__ __forceinline__ int tile_set(int tile, int shared_tiles, int total) {
   if (tile >= total) return 2;
   const int routed_tiles = total - shared_tiles;
   if (shared_tiles > 0 && routed_tiles > 0) {
@@ -544,9 +467,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   __shared__ __align__(8) uint64_t tempty_bar[2];      // used in the leader
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ __align__(8) uint64_t dh_bar[EPI_WARPS][2];  // dh staging buffers
-  __shared__ __align__(8) uint64_t sfull_bar[STAGES];      // scatter tiles: this CTA's rows landed
-  __shared__ __align__(8) uint64_t sdone_bar[STAGES];      // scatter tiles: both CTAs copied (leader)
-  __shared__ __align__(8) uint64_t egrp_bar;               // the epilogue warps meet (fused routing)
   __shared__ uint32_t tmem_holder;
   __shared__ int s_off[kMaxE + 1];
   __shared__ int s_cum[kMaxE + 1];
@@ -576,16 +496,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       mbar_init(smem_u32(&dh_bar[w][0]), 1);
       mbar_init(smem_u32(&dh_bar[w][1]), 1);
     }
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&sfull_bar[s]), 1);
-      mbar_init(smem_u32(&sdone_bar[s]), 2);
-    }
-    mbar_init(smem_u32(&egrp_bar), EPI_WARPS);
     fence_mbar_init();
-    if (p.route_tiles) {
-      tma_prefetch_desc(&p.route.a);
-      tma_prefetch_desc(&p.route.b);
-    }
     if (p.shared.enabled) {
       tma_prefetch_desc(&p.shared.a);
       tma_prefetch_desc(&p.shared.b);
@@ -649,9 +560,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const int chained = (p.chain.enabled && p.routed.enabled && !p.kgroup)
                               ? carry / (p.routed.n_total / p.routed.bn) * (p.chain.n_total / p.chain.bn)
                               : 0;
-      // Fused routing: a router and a scatter tile per 256-row block of tokens.
-      s_t1 = shared_tiles + carry + 2 * p.route_tiles;
-      s_total = shared_tiles + carry + chained + 2 * p.route_tiles;
+      s_t1 = shared_tiles + carry;
+      s_total = shared_tiles + carry + chained;
     }
   }
   tc_fence_before();
@@ -672,11 +582,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       if (p.early) {
         if (cluster < t1) {
           const Tile t = decode_tile(p, cluster, shared_tiles, s_off, s_cum, t1);
-          const OperandSet& S = operand_set(p, t.set);
+          const OperandSet& S = t.set == 2 ? p.chain : (t.set ? p.routed : p.shared);
           const int nkb = (t.klen + BK - 1) / BK;
           const int half = S.bn / 2;
-          // Router and scatter tiles read what the previous kernel writes: no early copies.
-          if (S.kblock && t.set < SET_ROUTER) {
+          if (S.kblock) {
             pre = min(nkb, STAGES);
             for (int kb = 0; kb < pre; ++kb) {
               const uint32_t sa = ring + kb * STAGE_BYTES;
@@ -692,37 +601,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         pdl_wait();
         pdl_trigger();
       }
-      uint32_t sf_used = 0, sf_last = 0;  // stages with a scatter copy of this CTA, its parity
       for (int tile = cluster; tile < total && ok; tile += nclusters) {
         const Tile t = decode_tile(p, tile, shared_tiles, s_off, s_cum, t1);
-        const OperandSet& S = operand_set(p, t.set);
-        if (t.set == SET_SCATTER) {
-          // This CTA's 128 token rows, k-block by k-block, into the ring for the epilogue
-          // (completion on this CTA's own barrier); the leader completes the stage's full
-          // barrier with a plain arrival so that the MMA issuer passes it in order.
-          const int nkb = (t.klen + BK - 1) / BK;
-          for (int kb = 0; kb < nkb; ++kb) {
-            if (!mbar_wait_spin(smem_u32(&empty_bar[stage]), phase ^ 1u, p.status)) {
-              ok = false;
-              break;
-            }
-            const uint32_t sa = ring + stage * STAGE_BYTES;
-            const uint32_t sb = smem_u32(&sfull_bar[stage]);
-            mbar_arrive_expect_tx(sb, ATOMS * A_ATOM);
-            tma_load_3d(sa, &S.a, sb, 0, t.row0 + HM * (int)rank, kb * ATOMS);
-            if (leader) mbar_arrive(smem_u32(&full_bar[stage]));
-            const uint32_t sp = (sf_used >> stage) & 1u ? ((sf_last >> stage) & 1u) ^ 1u : 0u;
-            sf_used |= 1u << stage;
-            sf_last = (sf_last & ~(1u << stage)) | (sp << stage);
-            issued |= 1u << stage;
-            last_par = (last_par & ~(1u << stage)) | (phase << stage);
-            if (++stage == STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
-          continue;
-        }
+        const OperandSet& S = t.set == 2 ? p.chain : (t.set ? p.routed : p.shared);
         // A chained tile's A rows are written by this launch's gate/up tiles.
         if (t.set == 2 && !dep_wait(p.dep + t.mblk, p.dep_target, p.status)) {
           ok = false;
@@ -784,9 +665,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       if (leader)
         for (int s = 0; s < STAGES; ++s)
           if ((issued >> s) & 1u) mbar_wait_spin(smem_u32(&full_bar[s]), (last_par >> s) & 1u, p.status);
-      // And for this CTA's last scatter copy into each stage.
-      for (int s = 0; s < STAGES; ++s)
-        if ((sf_used >> s) & 1u) mbar_wait_spin(smem_u32(&sfull_bar[s]), (sf_last >> s) & 1u, p.status);
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
@@ -795,43 +673,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       // fields are read (as plain kernel-parameter loads) once per tile, not through a
       // reference into parameter space on every k-block.
       int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0, sd_par = 0;
+      uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = cluster; tile < total && ok; tile += nclusters) {
-        const int set = tile_set(p, tile, shared_tiles, t1);
-        if (set == SET_SCATTER) {
-          // Token rows for the epilogues, no MMA.  The issuer keeps the ring's order and
-          // hands each stage back to both producers itself, once the stage's phase of
-          // the full barrier has completed and both CTAs' epilogues have copied their
-          // rows: a producer could otherwise put the next use's bytes on the leader's
-          // full barrier before the leader has closed this use's phase.
-          const int nkb = (p.route.k_total + BK - 1) / BK;
-          for (int kb = 0; kb < nkb; ++kb) {
-            if (!mbar_wait_spin(smem_u32(&full_bar[stage]), phase, p.status) ||
-                !mbar_wait_spin(smem_u32(&sdone_bar[stage]), (sd_par >> stage) & 1u, p.status)) {
-              ok = false;
-              break;
-            }
-            sd_par ^= 1u << stage;
-            mbar_arrive_cluster(map_to_rank(smem_u32(&empty_bar[stage]), 0));
-            mbar_arrive_cluster(map_to_rank(smem_u32(&empty_bar[stage]), 1));
-            if (++stage == STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
-          continue;
-        }
-        int k_total = set == SET_ROUTER
-                          ? p.route.k_total
-                          : (set == 2 ? p.chain.k_total : (set ? p.routed.k_total : p.shared.k_total / p.shared.ksplit));
+        const int set = tile_set(tile, shared_tiles, t1);
+        int k_total = set == 2 ? p.chain.k_total : (set ? p.routed.k_total : p.shared.k_total / p.shared.ksplit);
         if (set == 1 && p.kgroup) {  // this tile's K group
           k_total = decode_tile(p, tile, shared_tiles, s_off, s_cum, t1).klen;
           if (k_total == 0) continue;  // empty group: no MMA, no accumulator hand-off
         }
-        const int bn = set == SET_ROUTER ? p.route.bn : (set == 2 ? p.chain.bn : (set ? p.routed.bn : p.shared.bn));
-        const int a_mn = set == SET_ROUTER ? 0 : (set == 2 ? p.chain.a_mn : (set ? p.routed.a_mn : p.shared.a_mn));
-        const int b_mn = set == SET_ROUTER ? 0 : (set == 2 ? p.chain.b_mn : (set ? p.routed.b_mn : p.shared.b_mn));
+        const int bn = set == 2 ? p.chain.bn : (set ? p.routed.bn : p.shared.bn);
+        const int a_mn = set == 2 ? p.chain.a_mn : (set ? p.routed.a_mn : p.shared.a_mn);
+        const int b_mn = set == 2 ? p.chain.b_mn : (set ? p.routed.b_mn : p.shared.b_mn);
         const int nkb = (k_total + BK - 1) / BK;
         const int nkk_last = (k_total - (nkb - 1) * BK + 15) / 16;
         const uint32_t b_atom = (uint32_t)bn / 2 * AK * 2;
@@ -890,305 +743,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     uint32_t acc_phase = 0;
     uint32_t dh_par = 0;  // parity of this warp's two dh buffers
     const uint32_t dh_stage = ring + STAGES * STAGE_BYTES + (uint32_t)(warp - 2) * 2 * DH_BUF;
-    // Fused routing state, in one register: bits [0, 2) the ring stage of this pair's
-    // next k-block (where a scatter tile's rows land), [2, 2 + STAGES) the parity of
-    // each stage's next scatter copy, bit 8 the parity of the epilogue-group barrier.
-    uint32_t fstate = 0;
     if (p.early) pdl_wait();  // outputs and epilogue inputs belong to earlier kernels
     for (int tile = cluster; tile < total; tile += nclusters) {
       const Tile t = decode_tile(p, tile, shared_tiles, s_off, s_cum, t1);
-      const OperandSet& S = operand_set(p, t.set);
-      const int kb0 = fstate & 3u;  // stage of this tile's first k-block
-      fstate = (fstate & ~3u) | (uint32_t)((kb0 + (t.klen + BK - 1) / BK) % STAGES);
-      // The four epilogue warps meet (bounded); their shared-memory writes before it are
-      // visible to all of them after it.
-      auto egrp_sync = [&]() -> bool {
-        __syncwarp();
-        int ok2 = 1;
-        if (lane == 0) {
-          mbar_arrive(smem_u32(&egrp_bar));
-          ok2 = mbar_wait(smem_u32(&egrp_bar), (fstate >> 8) & 1u, p.status) ? 1 : 0;
-        }
-        fstate ^= 1u << 8;
-        ok2 = __shfl_sync(FULL, ok2, 0);
-        __syncwarp();
-        return ok2 != 0;
-      };
-      const int ew = warp - 2;  // 0..3: the epilogue warp's index for work not tied to TMEM lanes
-      int* const rsw = reinterpret_cast<int*>(smem_raw + (ring - smem_u32(smem_raw)) + STAGES * STAGE_BYTES);
-      if (t.set == SET_ROUTER) {
-        // ---- router tile: 128 tokens of this CTA, logits of the three weight parts
-        // summed, sigmoid scores, biased top-k (ties to the lower index), gates, the
-        // chunk's expert counts and each pair's rank inside the chunk (the stable
-        // counting sort restricted to the chunk: tokens ascending, then slots).
-        const RouteFusion& R = p.rf;
-        const int E = R.E, kk = R.k, i = ew * 32 + lane;
-        const int r = q * 32 + lane;
-        const int crow = t.row0 + HM * (int)rank;  // first token of this CTA's chunk
-        const long long tok = (long long)crow + r;
-        const bool valid = tok < R.T;
-        const int chunk = crow / HM;
-        float* sbias = reinterpret_cast<float*>(rsw + RS_BIAS);
-        float* soffs = reinterpret_cast<float*>(rsw + RS_OFF);
-        int* srun = rsw + RS_RUN;
-        int* sidx = rsw + RS_IDX;
-        int* srank = rsw + RS_RANK;
-        if (i < E) {
-          sbias[i] = R.bias[i];
-          soffs[i] = R.logit_offset ? R.logit_offset[i] : 0.f;
-          srun[i] = 0;
-        }
-        if (!egrp_sync()) break;
-        int ok = 1;
-        if (lane == 0) ok = mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, p.status) ? 1 : 0;
-        ok = __shfl_sync(FULL, ok, 0);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN_MAX;
-        // The k best experts so far, by descending key; experts arrive in ascending order
-        // and only a strictly larger key moves an earlier one down, so equal keys keep
-        // the lower index first.
-        float sel_k[kMaxK], sel_s[kMaxK];
-        int sel_e[kMaxK];
-#pragma unroll
-        for (int j = 0; j < kMaxK; ++j) {
-          sel_k[j] = 0.f;
-          sel_s[j] = 0.f;
-          sel_e[j] = -1;
-        }
-#pragma unroll 1
-        for (int c = 0; c < E; c += 16) {
-          uint32_t hv[16], mv[16], lv[16];
-          tmem_ld16(tb + c, hv);
-          tmem_ld16(tb + E + c, mv);
-          tmem_ld16(tb + 2 * E + c, lv);
-          tmem_wait_ld();
-          float sc[16];
-#pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const float z = (__uint_as_float(hv[u]) + __uint_as_float(mv[u])) + __uint_as_float(lv[u]) +
-                            soffs[c + u];
-            // Branch-free sigmoid; saturates to exactly 0 / 1 for extreme logits.
-            sc[u] = __fdividef(1.0f, 1.0f + __expf(-z));
-          }
-          if (valid && R.scores) {
-            float4* dst = reinterpret_cast<float4*>(R.scores + tok * E + c);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) dst[u] = make_float4(sc[4 * u], sc[4 * u + 1], sc[4 * u + 2], sc[4 * u + 3]);
-          }
-#pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            float nk = __fadd_rn(sc[u], sbias[c + u]), ns = sc[u];
-            int ne = c + u;
-#pragma unroll
-            for (int j = 0; j < kMaxK; ++j)
-              if (j < kk && ne >= 0 && (sel_e[j] < 0 || nk > sel_k[j])) {
-                const float tk = sel_k[j], ts = sel_s[j];
-                const int te = sel_e[j];
-                sel_k[j] = nk;
-                sel_s[j] = ns;
-                sel_e[j] = ne;
-                nk = tk;
-                ns = ts;
-                ne = te;
-              }
-          }
-        }
-        // The accumulator is free once read: the pair's next MMAs may start.
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster_relaxed(acc ? tempty_leader1 : tempty_leader0);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
-        float denom = 0.f;
-#pragma unroll
-        for (int j = 0; j < kMaxK; ++j)
-          if (j < kk) denom += sel_s[j];
-        if (valid) {
-#pragma unroll
-          for (int j = 0; j < kMaxK; ++j)
-            if (j < kk) {
-              R.idx[tok * kk + j] = sel_e[j];
-              R.gate[tok * kk + j] = R.renorm ? __fdiv_rn(sel_s[j], denom) : sel_s[j];
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < kMaxK; ++j)
-          if (j < kk) sidx[r * kk + j] = valid ? sel_e[j] : -1;
-        if (!egrp_sync()) break;
-        if (ew == 0) {
-          // Ranks in (token, slot) order, 32 pairs at a time.
-          const int np = HM * kk;
-          for (int b = 0; b < np; b += 32) {
-            const int qq = b + lane;
-            const int ex = qq < np ? sidx[qq] : -1;
-            const unsigned peers = __match_any_sync(FULL, ex);
-            const int rk = __popc(peers & ((1u << lane) - 1u));
-            if (ex >= 0) srank[qq] = srun[ex] + rk;
-            __syncwarp();
-            if (ex >= 0 && lane == __ffs(peers) - 1) srun[ex] += __popc(peers);
-            __syncwarp();
-          }
-        }
-        if (!egrp_sync()) break;
-        // The ranks inside the chunk stand in inv_pos until the scatter tile adds the
-        // chunk's base rows.
-        if (valid) {
-#pragma unroll
-          for (int j = 0; j < kMaxK; ++j)
-            if (j < kk) R.inv_pos[tok * kk + j] = srank[r * kk + j];
-        }
-        if (i < E && chunk < p.route_chunks) R.counts[(long long)chunk * E + i] = srun[i];
-        __syncwarp();
-        if (lane == 0) {
-          __threadfence();
-          atomicAdd(R.done, 1);
-        }
-        continue;
-      }
-      if (t.set == SET_SCATTER) {
-        // ---- scatter tile: every router tile has published; expert offsets from the
-        // count table, this chunk's base row per expert, the final rows of its pairs
-        // (perm_tok, inv_pos), chunk 0 also the offsets, loads, bias update and balance
-        // statistics; then the chunk's token rows, which the producer brings into the
-        // ring k-block by k-block, go to their permuted rows.
-        const RouteFusion& R = p.rf;
-        const int E = R.E, kk = R.k, i = ew * 32 + lane;
-        const int crow = t.row0 + HM * (int)rank;
-        const int chunk = crow / HM;
-        int* spre = rsw + RS_PRE;
-        int* stot = rsw + RS_TOT;
-        int* seoff = rsw + RS_EOFF;
-        int* sbase = rsw + RS_BASE;
-        int* spos = rsw + RS_IDX;
-        int ok = 1;
-        if (lane == 0) ok = wait_counter_geq(R.done, 2 * EPI_WARPS * p.route_tiles, p.status, kWaitLimitNs) ? 1 : 0;
-        ok = __shfl_sync(FULL, ok, 0);
-        __syncwarp();
-        if (!ok) break;
-        const int parts = (EPI_WARPS * 32) / E;
-        {
-          const int e = i % E, part = i / E;
-          if (part < parts) {
-            const int L = (p.route_chunks + parts - 1) / parts;
-            const int lo = part * L, hi = min(p.route_chunks, lo + L);
-            int pre = 0, tot = 0;
-            for (int cc = lo; cc < hi; ++cc) {
-              const int v = __ldcg(R.counts + (long long)cc * E + e);
-              tot += v;
-              if (cc < chunk) pre += v;
-            }
-            spre[part * E + e] = pre;
-            stot[part * E + e] = tot;
-          }
-        }
-        if (!egrp_sync()) break;
-        int pre_e = 0, tot_e = 0;
-        if (i < E)
-          for (int u = 0; u < parts; ++u) {
-            pre_e += spre[u * E + i];
-            tot_e += stot[u * E + i];
-          }
-        if (!egrp_sync()) break;
-        if (i < E) {
-          spre[i] = pre_e;
-          stot[i] = tot_e;
-        }
-        if (!egrp_sync()) break;
-        if (ew == 0) {  // exclusive scan of the expert totals, 32 at a time
-          int carry = 0;
-          for (int b = 0; b < E; b += 32) {
-            const int v = (b + lane < E) ? stot[b + lane] : 0;
-            int incl = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const int n = __shfl_up_sync(FULL, incl, o);
-              if (lane >= o) incl += n;
-            }
-            if (b + lane < E) seoff[b + lane] = carry + incl - v;
-            carry += __shfl_sync(FULL, incl, 31);
-          }
-          if (lane == 0) seoff[E] = carry;
-        }
-        if (!egrp_sync()) break;
-        if (i < E) sbase[i] = seoff[i] + spre[i];
-        if (chunk == 0) {
-          if (i <= E) R.offsets[i] = seoff[i];
-          if (i < E) {
-            R.load[i] = stot[i];
-            if (R.update_bias) {
-              // Aux-loss-free update: sign(T*k - E*load) is sign(target - load), sign(0) = 0.
-              const long long diff = (long long)R.T * kk - (long long)E * stot[i];
-              const float step = diff > 0 ? R.gamma : (diff < 0 ? -R.gamma : 0.f);
-              R.bias[i] = __fadd_rn(R.bias[i], step);
-            }
-          }
-          if (R.balance && ew == 1) warp_balance(stot, E, R.balance, lane);
-        }
-        if (!egrp_sync()) break;
-        {
-          const int r = i;  // row of the chunk, by thread (no TMEM here)
-          const long long tok = (long long)crow + r;
-          const bool valid = tok < R.T;
-#pragma unroll
-          for (int j = 0; j < kMaxK; ++j)
-            if (j < kk) {
-              int pos = -1;
-              if (valid) {
-                const int e = __ldcg(R.idx + tok * kk + j);
-                pos = sbase[e] + __ldcg(R.inv_pos + tok * kk + j);
-                R.inv_pos[tok * kk + j] = pos;
-                R.perm_tok[pos] = (int)tok;
-              }
-              spos[r * kk + j] = pos;
-            }
-        }
-        if (!egrp_sync()) break;
-        // The rows: per stage, each warp copies 32 rows, two per instruction (16 lanes x
-        // 16 bytes = one row's 256 bytes of the k-block), to each of the rows' k
-        // permuted positions.  The stage holds two 64-column atoms with the 128-byte
-        // swizzle (16-byte chunk c of row w at chunk c ^ (w % 8)).
-        const int nkb = (R.d + BK - 1) / BK;
-        bool okc = true;
-        for (int kb = 0; kb < nkb; ++kb) {
-          const int st = (kb0 + kb) % STAGES;
-          int ok3 = 1;
-          if (lane == 0) ok3 = mbar_wait(smem_u32(&sfull_bar[st]), (fstate >> (2 + st)) & 1u, p.status) ? 1 : 0;
-          fstate ^= 1u << (2 + st);
-          ok3 = __shfl_sync(FULL, ok3, 0);
-          __syncwarp();
-          if (!ok3) {
-            okc = false;
-            break;
-          }
-          const uint8_t* stg = smem_raw + (ring - smem_u32(smem_raw)) + st * STAGE_BYTES;
-          const int cidx = lane & 15, atom = cidx >> 3, ci = cidx & 7;
-          const int col = kb * BK + cidx * 8;
-          const bool cvalid = col < R.d;
-#pragma unroll 4
-          for (int it = 0; it < 16; ++it) {
-            const int row = ew * 32 + 2 * it + (lane >> 4);
-            const uint4 v = *reinterpret_cast<const uint4*>(stg + atom * A_ATOM + (row >> 3) * 1024 + (row & 7) * 128 +
-                                                            ((ci ^ (row & 7)) << 4));
-            if (cvalid) {
-#pragma unroll
-              for (int j = 0; j < kMaxK; ++j)
-                if (j < kk) {
-                  const int pos = spos[row * kk + j];
-                  if (pos >= 0) *reinterpret_cast<uint4*>(R.xp + (long long)pos * R.d + col) = v;
-                }
-            }
-          }
-          // Every warp has read the stage: tell the issuer, which hands it back.
-          if (!egrp_sync()) {
-            okc = false;
-            break;
-          }
-          if (ew == 0 && lane == 0) mbar_arrive_cluster(map_to_rank(smem_u32(&sdone_bar[st]), 0));
-        }
-        if (!okc) break;
-        continue;
-      }
+      const OperandSet& S = t.set == 2 ? p.chain : (t.set ? p.routed : p.shared);
       if (t.klen == 0) {
         // Empty K group (an expert without tokens): the issuer skipped it; its fp32
         // output is zero.
@@ -1481,7 +1039,6 @@ bool make_map_kblock(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t o
 int gate_up_block(int width) { return width % 128 == 0 ? 128 : (width % 64 == 0 ? 64 : 32); }
 
 int choose_bn(int mode, int N) {
-  if (mode == EPI_ROUTER) return N;  // 3E <= 192 columns: one tile
   if (mode == EPI_SWIGLU) return 2 * gate_up_block(N / 2);
   if (mode == EPI_STORE_F32) return N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : (N % 64 == 0 ? 64 : 32));
   if (mode == EPI_SWIGLU_BWD) return 2 * gate_up_block(N / 2);
@@ -1591,8 +1148,7 @@ cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* off
                                 const GemmOperandSet& shared, const CombineInputs& comb,
                                 long long max_routed_rows, cudaStream_t s, int* bad_arg,
                                 int max_pairs, long long kgroup_stride, int early,
-                                const GemmOperandSet* chain, int32_t* dep, int32_t* kdep,
-                                const RouteFusion* route) {
+                                const GemmOperandSet* chain, int32_t* dep, int32_t* kdep) {
   Params p;
   std::memset(&p, 0, sizeof(p));
   *bad_arg = 0;
@@ -1600,20 +1156,6 @@ cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* off
       (chain && !fill_set(p.chain, *chain))) {
     *bad_arg = 1;
     return cudaErrorInvalidValue;
-  }
-  if (route) {
-    // Fused routing beside a shared-expert gate/up set only (see RouteFusion).
-    const GemmOperandSet ro{route->x, route->T, route->w3, 1, 3 * route->E, route->d, nullptr, 0, EPI_ROUTER,
-                            route->T};
-    if (route->E < 16 || route->E > kFusedMaxE || route->E % 16 || route->k < 1 || route->k > kMaxK ||
-        route->k > route->E || route->d % AK || !p.shared.enabled || p.shared.mode != EPI_SWIGLU ||
-        p.shared.rows != route->T || p.routed.enabled || chain || !route->done || !fill_set(p.route, ro)) {
-      *bad_arg = 1;
-      return cudaErrorInvalidValue;
-    }
-    p.rf = *route;
-    p.route_tiles = (route->T + BM - 1) / BM;
-    p.route_chunks = (route->T + HM - 1) / HM;
   }
   if (p.chain.enabled) {
     // The chained set reads the routed set's output rows block by block.
@@ -1659,18 +1201,9 @@ cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* off
     tiles += ((max_routed_rows + BM - 1) / BM + E) * (long long)(p.routed.n_total / p.routed.bn);
   if (p.chain.enabled)
     tiles += ((max_routed_rows + BM - 1) / BM + E) * (long long)(p.chain.n_total / p.chain.bn);
-  // With fused routing the shared set is the only operand set: `tiles` counts its tiles.
-  const long long shared_tiles = tiles;
-  tiles += 2LL * p.route_tiles;
   int cap = max_active_pairs();
   if (max_pairs > 0 && max_pairs < cap) cap = max_pairs;
   const int pairs = (int)std::min<long long>(cap, std::max<long long>(tiles, 1));
-  if (p.route_tiles) {
-    // Each pair's first tile is its router tile (when there are no more router tiles
-    // than pairs); the scatter tiles follow one round later, so that every router tile
-    // has published by the time a scatter tile waits for it.
-    p.scatter_at = p.route_tiles + (int)std::min<long long>(shared_tiles, std::max(0, pairs - p.route_tiles));
-  }
   return launch_pdl(grouped_gemm_kernel, dim3(2 * pairs), dim3(NUM_THREADS), DYN_SMEM, s, p);
 }
 

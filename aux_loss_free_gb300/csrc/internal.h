@@ -75,10 +75,6 @@ size_t router_tc_scratch_bytes(int E, int d);
 // Also zeroes a.load [E] and, when set, a.counts [(T / chunk_tokens rounded up) * E]
 // before the router's atomics (no separate memsets in the launch chain).
 cudaError_t launch_router_tc(const RouterArgs& a, void* w3_scratch, cudaStream_t s);
-// The three-way bf16 split of the router weight alone (w3 [3E][d]), zeroing
-// zero[0, nzero) in the same launch.
-cudaError_t launch_router_split(const float* w_router, int E, int d, void* w3, int32_t* zero, int nzero,
-                                cudaStream_t s);
 
 // ---------------------------------------------------------------- permutation
 cudaError_t launch_count(const int32_t* idx, int T, int k, int E, int chunk_tokens,
@@ -118,8 +114,7 @@ cudaError_t launch_pack_gate_up(int G, int width, int d, int block, const uint16
                                 const uint16_t* wu, uint16_t* wgu, cudaStream_t s);
 
 // ---------------------------------------------------------------- grouped GEMM
-enum EpiMode { EPI_SWIGLU = 0, EPI_STORE = 1, EPI_COMBINE = 2, EPI_STORE_F32 = 3, EPI_SWIGLU_BWD = 4,
-               EPI_ROUTER = 5 };
+enum EpiMode { EPI_SWIGLU = 0, EPI_STORE = 1, EPI_COMBINE = 2, EPI_STORE_F32 = 3, EPI_SWIGLU_BWD = 4 };
 
 struct GemmOperandSet {
   const void* a;        // bf16 [a_rows][K]
@@ -177,42 +172,12 @@ struct CombineInputs {
 // routed tiles of its 256-row block have written their rows.  dep: one zeroed int32
 // per routed 256-row block (max_routed_rows / 256 + E + 1 suffice), left non-zero.
 // kdep: with an fp32 shared set split along K, one zeroed int32 per output tile of it.
-// The routing of the layer fused into a shared-expert launch (bf16 tokens, E a
-// multiple of 16 up to kFusedMaxE, permutation chunks of 128 tokens): router tiles
-// (the tokens of a 256-row block times the three-way split router weight, N = 3E) go
-// first, their epilogue forms scores, the biased top-k, gates, the per-chunk expert
-// counts and each pair's rank inside its chunk; scatter tiles (one per 256-row block,
-// after every router tile has published) turn the counts into expert offsets, write
-// perm_tok / inv_pos, apply the bias update and the balance statistics (chunk 0), and
-// copy the block's token rows, brought into the operand ring by TMA, to their
-// permuted rows.  The shared set's tiles run around them.
-constexpr int kFusedMaxE = 64;
-struct RouteFusion {
-  const void* w3;            // [3E][d] bf16: the router weight split into three bf16 parts
-  const void* x;             // [T][d] bf16 tokens
-  const float* logit_offset;  // [E] or null
-  float* bias;               // [E]: read for selection; updated in place when update_bias
-  float gamma;
-  int update_bias;
-  float* scores;             // [T][E] or null
-  int32_t* idx;              // [T][k]
-  float* gate;               // [T][k]
-  int32_t* counts;           // [T / 128 rounded up][E], written whole
-  int32_t* load;             // [E]
-  int32_t* offsets;          // [E + 1]
-  int32_t* perm_tok;         // [T * k]
-  int32_t* inv_pos;          // [T][k]
-  uint16_t* xp;              // [T * k][d] permuted token rows
-  moe_balance_t* balance;    // or null
-  int32_t* done;             // one int32, zero before the launch: router tiles published
-  int T, d, E, k, renorm;
-};
 cudaError_t launch_grouped_gemm(const GemmOperandSet& routed, const int32_t* offsets, int E,
                                 const GemmOperandSet& shared, const CombineInputs& comb,
                                 long long max_routed_rows, cudaStream_t s, int* bad_arg,
                                 int max_pairs = 0, long long kgroup_stride = 0, int early = 0,
                                 const GemmOperandSet* chain = nullptr, int32_t* dep = nullptr,
-                                int32_t* kdep = nullptr, const RouteFusion* route = nullptr);
+                                int32_t* kdep = nullptr);
 // Number of co-resident 2-SM clusters of the grouped GEMM on the current device.
 int gemm_max_pairs();
 

@@ -177,15 +177,12 @@ PermuteWs carve_permute(Carver& c, const moe_shape_t* s) {
 }
 
 struct FfnWs {
-  uint16_t* xp;   // [T*k][d] gathered rows
-  uint16_t* h;    // [T*k][f]
-  uint16_t* hs;   // [T][F]
-  uint16_t* xb;   // [T][d] bf16 copy of fp32 x
-  int32_t* done;  // one counter (fused routing: router tiles published), then dep
-  int32_t* dep;   // [T*k / 256 + E + 1] per routed 256-row block: h rows published
+  uint16_t* xp;  // [T*k][d] gathered rows
+  uint16_t* h;   // [T*k][f]
+  uint16_t* hs;  // [T][F]
+  uint16_t* xb;  // [T][d] bf16 copy of fp32 x
+  int32_t* dep;  // [T*k / 256 + E + 1] per routed 256-row block: h rows published
 };
-// Counters zeroed before each layer forward: done and dep, contiguous.
-size_t sync_words(const moe_shape_t* s) { return 1 + (size_t)s->T * s->k / 256 + s->E + 1; }
 FfnWs carve_ffn(Carver& c, const moe_shape_t* s) {
   const size_t Tk = (size_t)s->T * s->k;
   FfnWs w;
@@ -193,8 +190,7 @@ FfnWs carve_ffn(Carver& c, const moe_shape_t* s) {
   w.h = static_cast<uint16_t*>(c.take(2 * Tk * s->f));
   w.hs = s->F ? static_cast<uint16_t*>(c.take(2 * (size_t)s->T * s->F)) : nullptr;
   w.xb = s->x_dtype == MOE_X_F32 ? static_cast<uint16_t*>(c.take(2 * (size_t)s->T * s->d)) : nullptr;
-  w.done = static_cast<int32_t*>(c.take(4 * sync_words(s)));
-  w.dep = w.done + 1;
+  w.dep = static_cast<int32_t*>(c.take(4 * (Tk / 256 + s->E + 1)));
   return w;
 }
 
@@ -622,32 +618,6 @@ moe_status_t layer_fwd_impl(const moe_shape_t* shape, const void* x, const float
   // Fork: the shared expert's gate/up needs only x, so it runs on the caller's stream
   // (on most SMs) while the routing runs on a second stream (on the rest).
   const bool fork = !int4 && !xf && shape->F > 0 && T >= 1024;
-  moe_balance_t* balance = dbg ? dbg->balance : nullptr;
-  // Fused routing (E a multiple of 16 up to 64, chunks of 128 tokens): the router, the
-  // permutation and the row gather run as tiles of the shared expert's gate/up launch
-  // on the whole GPU, after one launch that splits the router weight and zeroes the
-  // launch's counters; then the chained routed FFN launch and the combine.
-  const bool fused = fork && tc && E % 16 == 0 && E <= kFusedMaxE && ct == 128;
-  if (fused) {
-    if (prof) prof_mark("route_shared_gate_up", s);
-    cudaError_t e = launch_router_split(w_router, E, shape->d, L.router, L.ffn.done, (int)sync_words(shape), s);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-    GemmOperandSet off{}, s1{x, T, w->shared_gate_up, 1, 2 * shape->F, shape->d, L.ffn.hs, shape->F, EPI_SWIGLU, T};
-    CombineInputs none{};
-    const RouteFusion rf{L.router, x, logit_offset, bias, gamma, update_bias, dbg ? dbg->scores : nullptr,
-                         L.idx, L.gate, L.perm.counts, L.load, L.offsets, L.perm_tok, L.inv_pos, L.ffn.xp,
-                         balance, L.ffn.done, T, shape->d, E, k, shape->renorm};
-    int bad = 0;
-    e = launch_grouped_gemm(off, L.offsets, E, s1, none, (long long)T * k, s, &bad, 0, 0, /*early=*/1, nullptr,
-                            nullptr, nullptr, &rf);
-    if (bad) return MOE_ERR_UNSUPPORTED;
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-    CombineInputs comb{L.y, L.inv_pos, L.gate, static_cast<const uint16_t*>(residual), k};
-    const moe_status_t st2 = run_ffn(shape, x, L.offsets, w, L.ffn, L.y, L.s_out, &comb, static_cast<uint16_t*>(out),
-                                     s, prof, /*shared_gate_up_done=*/true);
-    if (prof) prof_mark(nullptr, s);
-    return st2;
-  }
   AuxStream* aux = nullptr;
   std::unique_lock<std::mutex> aux_lock(g_aux_mu, std::defer_lock);
   cudaStream_t rs = s;  // stream of the routing kernels
@@ -697,6 +667,7 @@ moe_status_t layer_fwd_impl(const moe_shape_t* shape, const void* x, const float
   const bool direct = int4 && !xf && (long long)T * k <= kDirectMaxPairs &&
                       (shape->F == 0 || int4_skinny(shape)) &&
                       !(dbg && (dbg->offsets || dbg->perm_tok || dbg->inv_pos));
+  moe_balance_t* balance = dbg ? dbg->balance : nullptr;
   const bool need_load = update_bias || (dbg && dbg->load) || balance;
   if (direct) {
     if (need_load && cudaMemsetAsync(L.load, 0, sizeof(int32_t) * E, rs) != cudaSuccess)

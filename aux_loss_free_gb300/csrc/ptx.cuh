@@ -124,42 +124,6 @@ __device__ __forceinline__ bool wait_counter_geq(const int* ctr, int target, int
   }
 }
 
-// ---------------------------------------------------------------- balance statistics
-
-// Balance statistics of load[0..E) (moe_balance_t) by one warp; lane 0 writes them.
-// The ratios are the fp32 values nearest to the exact rationals: the fp64 quotient of
-// the two exact integers is correctly rounded, and rounding it again to fp32 gives the
-// nearest fp32 for denominators below 2^28 (the exact quotient then never lies within
-// half an fp64 ulp of an fp32 rounding boundary unless it is one).
-__device__ __forceinline__ void warp_balance(const int32_t* load, int E, moe_balance_t* out, int lane) {
-  int mx = 0, mn = 0x7FFFFFFF, dead = 0;
-  long long sum = 0;
-  for (int e = lane; e < E; e += 32) {
-    const int v = load[e];
-    mx = max(mx, v);
-    mn = min(mn, v);
-    dead += v == 0;
-    sum += v;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-    mn = min(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
-    dead += __shfl_xor_sync(0xFFFFFFFFu, dead, o);
-    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-  }
-  if (lane == 0) {
-    out->pairs = sum;
-    out->max_load = mx;
-    out->min_load = mn;
-    out->dead_experts = dead;
-    const double pe = (double)sum;
-    out->max_over_mean = sum > 0 ? __double2float_rn(__ddiv_rn((double)mx * E, pe)) : 0.f;
-    out->min_over_mean = sum > 0 ? __double2float_rn(__ddiv_rn((double)mn * E, pe)) : 0.f;
-    out->dead_fraction = __double2float_rn(__ddiv_rn((double)dead, (double)E));
-  }
-}
-
 // ---------------------------------------------------------------- TMA
 
 // 2-D tiled bulk tensor load global -> shared, completion counted on `bar`.

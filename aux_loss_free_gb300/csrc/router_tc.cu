@@ -355,14 +355,6 @@ cudaError_t launch_e(RouterTcParams& p, int blocks, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_router_split(const float* w_router, int E, int d, void* w3, int32_t* zero, int nzero,
-                                cudaStream_t s) {
-  const long long n = (long long)E * d;
-  const long long nthreads = std::max<long long>(n, nzero);
-  return launch_pdl(split_router_kernel, dim3((unsigned)((nthreads + 255) / 256)), dim3(256), 0, s, w_router, n,
-                    static_cast<uint16_t*>(w3), zero, nzero, static_cast<int32_t*>(nullptr), 0);
-}
-
 bool router_tc_supported(int T, int E, int x_is_f32) {
   // One CTA per 128 tokens: below that the CUDA-core router (fp32 weights read
   // directly, no split launch) finishes sooner.
