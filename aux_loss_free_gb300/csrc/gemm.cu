@@ -90,6 +90,7 @@ struct OperandSet {
   int ldo, n_total, k_total, bn, mode, enabled, rows;
   int v8;   // output rows start on 32-byte boundaries: 256-bit stores allowed
   int v8h;  // the same for EPI_SWIGLU_BWD's dh rows
+  int b_stream;  // B is streamed once (expert weights): its lines are the first L2 evicts
   // MN-major operands: the map views [K rows][M or N] as (64 elements, K rows, atoms
   // of 64 along M/N), box (64, BK, atoms per CTA), one copy per operand per k-block.
   int a_mn, b_mn;
@@ -200,6 +201,23 @@ __device__ __forceinline__ void tma_load_kblock_pair(uint32_t dst, const CUtenso
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(atom), "r"(bar_cluster)
       : "memory");
+}
+
+// The same with an L2 cache policy (createpolicy) for the copied lines.
+__device__ __forceinline__ void tma_load_kblock_pair_hint(uint32_t dst, const CUtensorMap* map,
+                                                          uint32_t bar_cluster, int32_t row, int32_t atom,
+                                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(atom), "r"(bar_cluster), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
@@ -573,6 +591,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ TMA producer (both CTAs)
+      const uint64_t evict_first = l2_evict_first_policy();
       int stage = 0;
       uint32_t phase = 0, issued = 0, last_par = 0;
       bool ok = true;
@@ -643,8 +662,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             }
           } else if (S.kblock) {
             tma_load_kblock_pair(sa, &S.a, fb, t.row0 + HM * (int)rank, katom0 + kb * ATOMS);
-            if (!b_done)
+            if (b_done) {
+            } else if (S.b_stream) {
+              tma_load_kblock_pair_hint(sa + A_BYTES, &S.b, fb, t.brow + half * (int)rank, katom0 + kb * ATOMS,
+                                        evict_first);
+            } else {
               tma_load_kblock_pair(sa + A_BYTES, &S.b, fb, t.brow + half * (int)rank, katom0 + kb * ATOMS);
+            }
           } else {
             for (int at = 0; at < natoms; ++at) {
               tma_load_2d_pair(sa + at * A_ATOM, &S.a, fb, t.k0 + kb * BK + at * AK,
@@ -1106,6 +1130,7 @@ bool fill_set(OperandSet& t, const GemmOperandSet& o) {
   if (o.N % t.bn != 0) return false;
   t.a_mn = o.a_mn ? 1 : 0;
   t.b_mn = o.b_mn ? 1 : 0;
+  t.b_stream = o.b_stream ? 1 : 0;
   if (t.a_mn || t.b_mn) {
     // Whole k-blocks of both operands per copy (the expected byte count assumes it).
     if ((!t.a_mn || !t.b_mn) && o.K % AK != 0) return false;

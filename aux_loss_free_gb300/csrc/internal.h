@@ -146,6 +146,10 @@ struct GemmOperandSet {
   // the parts are added into out in part order (launch_grouped_gemm's kdep).
   int ksplit;
   long long part_stride;
+  // Non-zero: B is read once per use and not again soon (the routed experts' weights in
+  // the forward), so its TMA copies carry an L2 evict-first policy and leave the cache
+  // to the activations the launch and the next kernels read again.
+  int b_stream;
 };
 // Column tile width the grouped GEMM uses for an operand set of this mode and N.
 int gemm_tile_n(int mode, int N);

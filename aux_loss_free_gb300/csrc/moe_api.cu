@@ -244,6 +244,7 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x_bf16, const int32_t* of
   int bad = 0;
   CombineInputs none{};
   GemmOperandSet r1{ws.xp, Tk, w->w_gate_up, s->E, 2 * s->f, s->d, ws.h, s->f, EPI_SWIGLU, 0};
+  r1.b_stream = 1;
   GemmOperandSet sd{};
   if (s->F)
     sd = GemmOperandSet{ws.hs, s->T, w->shared_down, 1, s->d, s->F, shared_out, s->d, EPI_STORE, s->T};
@@ -259,6 +260,7 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x_bf16, const int32_t* of
   else if (s->F)
     s1 = sd;
   GemmOperandSet r2{ws.h, Tk, w->w_down, s->E, s->d, s->f, y_perm, s->d, EPI_STORE, 0};
+  r2.b_stream = 1;
   // With the shared gate/up done, the routed down projection is chained into the same
   // launch (its tiles follow the others and start block by block as h is written;
   // ws.dep was zeroed by the caller); otherwise it shares a second launch with the
