@@ -46,7 +46,8 @@ METRIC = "MoE-layer fwd tokens/s (T=8192,d=1024,64x512 top-2+2048 shared), % roo
 FLUSH_BYTES = 512 << 20
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_shared_gate_up_nano_traffic.txt")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_chained_routed_ffn_nano_traffic.txt")
+SHARED_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_shared_gate_up_nano_traffic.txt")
 TRAIN_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_wgrad_gate_up_train_traffic.txt")
 PROFILE_PERIOD = 10
 
@@ -520,18 +521,34 @@ def gpu_arm(args, rank, world, dist):
     tokens_per_s = world * s.T * K / (total_ms / 1e3)
     ms_step = total_ms / K
     roof_s = nlayers * max(flops / (peaks["bf16_tflops"] * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9))
-    # Dominant kernel: the shared-expert gate/up launch when the layer forks the
-    # routing onto a second stream, else the combined gate/up launch.
-    if "shared_gate_up" in stages_ms:
-        dom_name = "grouped_gemm_kernel (shared-expert gate/up launch, concurrent with routing)"
-        gu_flops = 2 * s.T * s.d * 2 * s.F
-        gu_ms = stages_ms["shared_gate_up"] / max(1, calls)
+    # Dominant kernel: the longest stage.  When the layer forks the routing onto a
+    # second stream that is the chained launch (routed gate/up beside the shared down
+    # projection, the routed down projection chained behind); the shared-expert gate/up
+    # launch that runs beside the routing is reported next to it.  Otherwise the
+    # combined gate/up launch.
+    routed_gu = 2 * s.T * s.k * s.d * 2 * s.f
+    routed_dn = 2 * s.T * s.k * s.f * s.d
+    shared_gu = 2 * s.T * s.d * 2 * s.F
+    shared_dn = 2 * s.T * s.F * s.d
+    extra_rooflines = {}
+    if "routed_ffn_shared_down" in stages_ms:
+        dom_name = ("grouped_gemm_kernel (chained launch: routed gate/up + shared down projection, "
+                    "routed down projection chained)")
+        gu_flops = routed_gu + shared_dn + routed_dn
+        gu_ms = stages_ms["routed_ffn_shared_down"] / max(1, calls)
+        sg_ms = stages_ms["shared_gate_up"] / max(1, calls)
+        sg_ach = shared_gu / (sg_ms / 1e3) / 1e12
+        extra_rooflines["shared_gate_up"] = {
+            "kernel": "grouped_gemm_kernel (shared-expert gate/up launch, concurrent with routing)",
+            "bound": "tensor", "achieved": sg_ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": sg_ach / peaks["bf16_tflops"], "traffic": read_traffic(SHARED_TRAFFIC_FILE),
+            "flops_per_launch": shared_gu, "avg_launch_us": sg_ms * 1e3}
     else:
         dom_name = "grouped_gemm_kernel (gate/up launch: routed groups + shared)"
-        gu_flops = 2 * s.T * s.k * s.d * 2 * s.f + 2 * s.T * s.d * 2 * s.F
+        gu_flops = routed_gu + shared_gu
         gu_ms = stages_ms.get("gemm_gate_up", float("nan")) / max(1, calls)
     achieved = gu_flops / (gu_ms / 1e3) / 1e12
-    traffic = read_traffic()
+    traffic = read_traffic() if "routed_ffn_shared_down" in stages_ms else None
     clocks = sampler.summary(t_wall0, t_wall1)
     line = {
         "metric": WORKLOADS[name][3], "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": K,
@@ -553,6 +570,9 @@ def gpu_arm(args, rank, world, dist):
                      "frac_sustained": achieved / peaks["bf16_tflops_sustained"],
                      "flops_per_launch": gu_flops, "avg_launch_us": gu_ms * 1e3},
         "stages_us": {k: v * 1e3 / max(1, calls) for k, v in stages_ms.items()},
+        "other_rooflines": extra_rooflines,
+        "step_us": {"median": statistics.median(step_ms) * 1e3, "min": min(step_ms) * 1e3,
+                    "max": max(step_ms) * 1e3, "note": "per timed step (CUDA events); ms_per_step is the mean"},
         "e2e": {"value": world * s.T / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(hx[0].numel() * hx[0].element_size()),
                 "d2h_bytes_per_step": int(hout[0].numel() * hout[0].element_size()),
@@ -567,8 +587,6 @@ def gpu_arm(args, rank, world, dist):
                                       "per_step": [round(v, 3) for v in traj]}
         line["dead_expert_fraction"] = {"first": dead[0], "last": dead[-1],
                                         "per_step": [round(v, 4) for v in dead]}
-        line["step_us"] = {"min": min(step_ms) * 1e3, "median": statistics.median(step_ms) * 1e3,
-                           "max": max(step_ms) * 1e3}
     if s.w_format == "int4":
         # Serving is bound by weight bytes: report the HBM roofline of the layer.
         line["roofline"] = {"kernel": "whole top-1 serving layer", "bound": "hbm",
