@@ -2,4 +2,4 @@
 
 Only the tests, the smoke check and the bench's CPU-baseline leg import this package.
 """
-from . import moe_oracle  # noqa: F401
+from . import attention_oracle, moe_oracle  # noqa: F401

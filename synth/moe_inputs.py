@@ -26,10 +26,11 @@ import numpy as np
 
 # Case numbers used in the seed: they are fixed so that stored fixtures and
 # bench runs stay reproducible.
-_CASE_ID = {"tiny": 0, "nano": 1, "skew": 2, "decode": 3, "stack": 4}
+_CASE_ID = {"tiny": 0, "nano": 1, "skew": 2, "decode": 3, "stack": 4, "attn": 5, "attn_tiny": 6}
 _TENSOR_ID = {
     "x": 0, "w_router": 1, "bias": 2, "w_gate": 3, "w_up": 4, "w_down": 5,
     "s_gate": 6, "s_up": 7, "s_down": 8, "dout": 9,
+    "w_q": 10, "w_k": 11, "w_v": 12, "w_o": 13,
 }
 
 
@@ -139,4 +140,45 @@ def make_layer(shape: LayerShape, case: str, seed: int = 0, layer: int = 0,
     out["s_up"] = bf16_bits_from_f32(_normal(seed, case, layer, "s_up", (F, d), 0.02))
     out["s_down"] = bf16_bits_from_f32(_normal(seed, case, layer, "s_down", (d, F), 0.02))
     out["gamma"] = shape.gamma
+    return out
+
+
+@dataclasses.dataclass(frozen=True)
+class AttnShape:
+    """Sizes of one attention block: batch x seq tokens, hidden d, n_head query heads sharing
+    n_kv_head key/value heads (grouped-query attention), head width head_dim."""
+
+    batch: int
+    seq: int
+    d: int
+    n_head: int
+    n_kv_head: int
+    head_dim: int = 128
+    eps: float = 1e-6
+
+    @property
+    def T(self) -> int:
+        return self.batch * self.seq
+
+    def replace(self, **kw) -> "AttnShape":
+        return dataclasses.replace(self, **kw)
+
+
+ATTN_CONFIGS: dict[str, AttnShape] = {
+    # The Nano model's attention (hidden 1024, 4x GQA, head width 128), batch 4 x seq 2048.
+    "attn": AttnShape(batch=4, seq=2048, d=1024, n_head=8, n_kv_head=2),
+    # Small, ragged sequences (not a multiple of the 128-token tile), one key/value head.
+    "attn_tiny": AttnShape(batch=2, seq=200, d=512, n_head=4, n_kv_head=1),
+}
+
+
+def make_attention(shape: AttnShape, case: str, seed: int = 0, layer: int = 0) -> dict:
+    """Inputs of one attention block: x bf16 bits [T][d] ~ N(0, 1), w_q [H*hd][d], w_k, w_v
+    [Hkv*hd][d], w_o [d][H*hd] bf16 bits ~ N(0, 0.02)."""
+    hd = shape.head_dim
+    out = {"x": bf16_bits_from_f32(_normal(seed, case, layer, "x", (shape.T, shape.d), 1.0))}
+    out["w_q"] = bf16_bits_from_f32(_normal(seed, case, layer, "w_q", (shape.n_head * hd, shape.d), 0.02))
+    out["w_k"] = bf16_bits_from_f32(_normal(seed, case, layer, "w_k", (shape.n_kv_head * hd, shape.d), 0.02))
+    out["w_v"] = bf16_bits_from_f32(_normal(seed, case, layer, "w_v", (shape.n_kv_head * hd, shape.d), 0.02))
+    out["w_o"] = bf16_bits_from_f32(_normal(seed, case, layer, "w_o", (shape.d, shape.n_head * hd), 0.02))
     return out
