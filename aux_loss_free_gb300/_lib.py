@@ -55,6 +55,11 @@ class MoEGrads(ctypes.Structure):
                 ("ds_gate_up", _P), ("ds_down", _P), ("dgate", _P)]
 
 
+class MoEAttnShape(ctypes.Structure):
+    _fields_ = [("batch", _I32), ("seq", _I32), ("d", _I32), ("n_head", _I32), ("n_kv_head", _I32),
+                ("head_dim", _I32), ("eps", _F)]
+
+
 class MoECacheStats(ctypes.Structure):
     _fields_ = [("steps", _I64), ("hits", _I64), ("misses", _I64), ("evictions", _I64), ("bytes", _I64),
                 ("overflow", _I64)]
@@ -89,6 +94,9 @@ SIGNATURES = {
     "moe_expert_cache_read": (_I32, [_SHAPE_P, _I32, _P, ctypes.POINTER(MoECacheStats), _P, _P, _P, _P]),
     "moe_layer_fwd_cached": (_I32, [_SHAPE_P, _P, _P, _P, _P, _F, _I32, ctypes.POINTER(MoEWeights), _I32, _P,
                                     _SZ, _P, _P, ctypes.POINTER(MoEDebug), _P, _SZ, _P]),
+    "moe_attention_workspace_size": (_SZ, [ctypes.POINTER(MoEAttnShape)]),
+    "moe_attention_fwd": (_I32, [ctypes.POINTER(MoEAttnShape), _P, _P, _P, _I32, _P, _P, _SZ, _P]),
+    "moe_attention_core": (_I32, [ctypes.POINTER(MoEAttnShape), _P, _P, _P]),
     "moe_pack_gate_up": (_I32, [_I32, _I32, _I32, _P, _P, _P, _P]),
     "moe_quantize_int4": (_I32, [_I64, _I32, _P, _P, _P, _P]),
     "moe_device_status": (_I32, [_P, ctypes.POINTER(_I32)]),
@@ -307,6 +315,25 @@ def moe_layer_fwd_cached(shape, x, w_router, logit_offset, bias, gamma, update_b
         ctypes.byref(host_weights), slots, _ptr(cache), cache.numel() * cache.element_size(), _ptr(residual),
         _ptr(out), ctypes.byref(debug) if debug is not None else None, _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def make_attn_shape(batch, seq, d, n_head, n_kv_head, head_dim=128, eps=1e-6) -> MoEAttnShape:
+    return MoEAttnShape(batch, seq, d, n_head, n_kv_head, head_dim, eps)
+
+
+def moe_attention_workspace_size(shape) -> int:
+    return load_library().moe_attention_workspace_size(ctypes.byref(shape))
+
+
+def moe_attention_fwd(shape, x, w_qkv, w_o, residual, out, workspace, stream=None):
+    _check("moe_attention_fwd", load_library().moe_attention_fwd(
+        ctypes.byref(shape), _ptr(x), _ptr(w_qkv), _ptr(w_o), int(residual), _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_attention_core(shape, qkv, o, stream=None):
+    _check("moe_attention_core", load_library().moe_attention_core(
+        ctypes.byref(shape), _ptr(qkv), _ptr(o), _stream(stream)))
 
 
 def moe_pack_gate_up(G, width, d, w_gate, w_up, w_gate_up, stream=None):

@@ -1,0 +1,412 @@
+// Causal grouped-query attention with per-head QK-norm on tcgen05 tensor cores (sm_103a).
+//
+// Relay article ("Una carrera de relevos con GPUs alquiladas entrenó el MoE de 2.7B de
+// NanoColibri por $200"), opening section, architecture paragraph: grouped-query
+// attention with four query heads per key/value head and a per-head QK-norm.  This
+// library's readings: head width 128; the norm is an RMS normalisation of each head's
+// 128 values without a learned scale; scores q.k / sqrt(128), causal within each
+// sequence, no positional encoding.
+//
+// qk_norm_kernel normalises the query and key heads of the projected [T][C] rows in
+// place (C = (n_head + 2 n_kv_head) * 128: query heads, key heads, value heads).
+// gqa_attention_kernel computes one 128-query tile of one head per CTA:
+//   - warp 0 (one thread): TMA copies of the query tile (once) and, per 128-key tile,
+//     the key and value tiles of the head's group into a 2-stage ring;
+//   - warp 1 (one thread): tcgen05.mma, S_j = Q K_j^T into one of two TMEM score
+//     buffers, and O += P_j V_j into the TMEM output (V read MN-major through the
+//     instruction descriptor, no transposed copy); S_{j+1} is issued before P_j V_j so
+//     the tensor core works while the softmax warps do;
+//   - warps 2-5 (one query row per thread, its TMEM lane): the online softmax in the
+//     log2 domain, reading the scores twice (maximum, then exponentials), writing P_j
+//     as bf16 into shared memory with the 128-byte swizzle the MMA reads, and rescaling
+//     the O row in TMEM only when the row's maximum grew by more than 8 (2^8), which
+//     keeps every exponential below 256; at the end O / l rounded to bf16.
+// Every barrier wait is bounded; on a timeout the status word is set and the CTA exits.
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int HD = kAttnHeadDim;              // head width
+constexpr int BQ = 128;                       // query rows per CTA (TMEM lanes)
+constexpr int BKV = 128;                      // keys per tile
+constexpr int AT = 64;                        // columns per 128-byte swizzle atom (bf16)
+constexpr int ATOM_BYTES = 128 * AT * 2;      // 16 KB: 128 rows x 64
+constexpr int TILE_BYTES = 2 * ATOM_BYTES;    // 32 KB: 128 rows x 128
+constexpr int KV_STAGES = 2;
+constexpr int Q_OFF = 0;
+constexpr int KV_OFF = TILE_BYTES;            // stage s: K at KV_OFF + 2 s TILE, V one tile later
+constexpr int P_OFF = KV_OFF + KV_STAGES * 2 * TILE_BYTES;
+constexpr int ATT_SMEM = P_OFF + TILE_BYTES + 1024;
+constexpr int ATT_THREADS = 192;
+constexpr uint32_t S_COL = 0;                 // score buffers: columns [0, 128) and [128, 256)
+constexpr uint32_t O_COL = 256;               // output accumulator: columns [256, 384)
+constexpr uint32_t ATT_TMEM_COLS = 512;
+constexpr unsigned FULL = 0xFFFFFFFFu;
+
+struct AttnParams {
+  CUtensorMap qkv;   // [T][C] bf16 viewed as (64, T, C / 64), box (64, 128, 2)
+  uint16_t* out;     // [T][n_head * HD] bf16
+  int* status;
+  int batch, seq, n_head, n_kv_head, qtiles;
+  float scale_log2;  // log2(e) / sqrt(HD)
+};
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// One warp per (token, head) of the query and key heads: u / sqrt(mean(u^2) + eps) over
+// the head's 128 values, rounded to bf16 in place.
+__global__ void qk_norm_kernel(uint16_t* __restrict__ qkv, long long rows, int C, int heads, float eps) {
+  pdl_wait();
+  pdl_trigger();
+  const long long w = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (w >= rows * heads) return;
+  const long long t = w / heads;
+  const int h = (int)(w % heads);
+  uint2* p = reinterpret_cast<uint2*>(qkv + t * C + (long long)h * HD) + lane;  // 4 values per lane
+  const uint2 v = *p;
+  const float a = __uint_as_float(v.x << 16), b = __uint_as_float(v.x & 0xFFFF0000u);
+  const float c = __uint_as_float(v.y << 16), d = __uint_as_float(v.y & 0xFFFF0000u);
+  float ss = a * a + b * b + c * c + d * d;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
+  const float f = rsqrtf(ss * (1.0f / HD) + eps);
+  *p = make_uint2(pack_bf16x2(a * f, b * f), pack_bf16x2(c * f, d * f));
+}
+
+__global__ void __launch_bounds__(ATT_THREADS, 1) gqa_attention_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t q_full;
+  __shared__ __align__(8) uint64_t kv_full[KV_STAGES];
+  __shared__ __align__(8) uint64_t kv_empty[KV_STAGES];
+  __shared__ __align__(8) uint64_t s_full[2];
+  __shared__ __align__(8) uint64_t s_free[2];
+  __shared__ __align__(8) uint64_t p_full;
+  __shared__ __align__(8) uint64_t pv_done;
+  __shared__ uint32_t tmem_holder;
+
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* const base_ptr = smem_raw + (base - smem_u32(smem_raw));
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // The longest query tiles (most key tiles under the causal mask) go first.
+  const int per_tile = p.n_head * p.batch;
+  const int qi = p.qtiles - 1 - (int)blockIdx.x / per_tile;
+  const int rem = (int)blockIdx.x % per_tile;
+  const int h = rem % p.n_head, b = rem / p.n_head;
+  const int g = h / (p.n_head / p.n_kv_head);
+  const int row0 = b * p.seq + qi * BQ;  // first token row of the query tile
+  const int ntiles = qi + 1;              // key tiles 0..qi
+  const int q_atom = h * (HD / AT), k_atom = (p.n_head + g) * (HD / AT),
+            v_atom = (p.n_head + p.n_kv_head + g) * (HD / AT);
+
+  if (warp == 0 && lane == 0) {
+    mbar_init(smem_u32(&q_full), 1);
+    for (int s = 0; s < KV_STAGES; ++s) {
+      mbar_init(smem_u32(&kv_full[s]), 1);
+      mbar_init(smem_u32(&kv_empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&s_full[s]), 1);
+      mbar_init(smem_u32(&s_free[s]), 4);
+    }
+    mbar_init(smem_u32(&p_full), 4);
+    mbar_init(smem_u32(&pv_done), 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&p.qkv);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_holder), ATT_TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_holder;
+  pdl_wait();  // the projected, normalised rows come from earlier kernels
+  pdl_trigger();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      mbar_arrive_expect_tx(smem_u32(&q_full), TILE_BYTES);
+      tma_load_3d(base + Q_OFF, &p.qkv, smem_u32(&q_full), 0, row0, q_atom);
+      int issued = 0;
+      for (int j = 0; j < ntiles; ++j) {
+        const int st = j % KV_STAGES;
+        const uint32_t ph = (uint32_t)(j / KV_STAGES) & 1u;
+        if (!mbar_wait_spin(smem_u32(&kv_empty[st]), ph ^ 1u, p.status)) break;
+        const uint32_t kv = base + KV_OFF + st * 2 * TILE_BYTES;
+        const uint32_t fb = smem_u32(&kv_full[st]);
+        mbar_arrive_expect_tx(fb, 2 * TILE_BYTES);
+        const int krow = b * p.seq + j * BKV;
+        tma_load_3d(kv, &p.qkv, fb, 0, krow, k_atom);
+        tma_load_3d(kv + TILE_BYTES, &p.qkv, fb, 0, krow, v_atom);
+        issued = j + 1;
+      }
+      // No copy may still be landing when the CTA exits.
+      mbar_wait_spin(smem_u32(&q_full), 0, p.status);
+      for (int j = issued > KV_STAGES ? issued - KV_STAGES : 0; j < issued; ++j)
+        mbar_wait_spin(smem_u32(&kv_full[j % KV_STAGES]), (uint32_t)(j / KV_STAGES) & 1u, p.status);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      constexpr uint32_t id_s = idesc_bf16_f32(BQ, BKV, 0, 0);
+      constexpr uint32_t id_pv = idesc_bf16_f32(BQ, HD, 0, 1);
+      bool ok = mbar_wait_spin(smem_u32(&q_full), 0, p.status);
+      tc_fence_after();
+      const uint64_t qdesc = sw128_kmajor_desc(base + Q_OFF);
+      const uint64_t pdesc = sw128_kmajor_desc(base + P_OFF);
+      for (int j = 0; j <= ntiles && ok; ++j) {
+        if (j < ntiles) {
+          const int st = j % KV_STAGES;
+          const int sb = j & 1;
+          if (!mbar_wait_spin(smem_u32(&kv_full[st]), (uint32_t)(j / KV_STAGES) & 1u, p.status) ||
+              !mbar_wait_spin(smem_u32(&s_free[sb]), ((uint32_t)(j >> 1) & 1u) ^ 1u, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t kdesc = sw128_kmajor_desc(base + KV_OFF + st * 2 * TILE_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk)  // atom kk / 4, 32 bytes per K step inside it
+            tc_mma_bf16(tmem + S_COL + sb * BKV, qdesc + (kk >> 2) * (ATOM_BYTES >> 4) + 2 * (kk & 3),
+                        kdesc + (kk >> 2) * (ATOM_BYTES >> 4) + 2 * (kk & 3), id_s, kk != 0);
+          tc_commit(smem_u32(&s_full[sb]));
+        }
+        if (j >= 1) {
+          const int jp = j - 1, st = jp % KV_STAGES;
+          if (!mbar_wait_spin(smem_u32(&p_full), (uint32_t)jp & 1u, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // V [keys][HD] is the MN-major B of O += P V: 64-column atoms 16 KB apart, a
+          // 16-key step two 1024-byte atoms further.
+          const uint64_t vdesc = sw128_mnmajor_desc(base + KV_OFF + st * 2 * TILE_BYTES + TILE_BYTES, ATOM_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BKV / 16; ++kk)
+            tc_mma_bf16(tmem + O_COL, pdesc + (kk >> 2) * (ATOM_BYTES >> 4) + 2 * (kk & 3), vdesc + kk * 128u,
+                        id_pv, (jp | kk) != 0);
+          tc_commit(smem_u32(&kv_empty[st]));
+          tc_commit(smem_u32(&pv_done));
+        }
+      }
+    }
+  } else {
+    // -------------------------------------------------- softmax warps 2..5
+    const int q4 = warp & 3;             // TMEM lanes [32 q4, 32 q4 + 32)
+    const int r = q4 * 32 + lane;        // query row of the tile
+    const int qpos = qi * BQ + r;        // position in the sequence
+    const bool valid = qpos < p.seq;
+    const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
+    uint8_t* const prow = base_ptr + P_OFF + (r >> 3) * 1024 + (r & 7) * 128;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const int sb = j & 1;
+      int w = 1;
+      if (lane == 0) w = mbar_wait(smem_u32(&s_full[sb]), (uint32_t)(j >> 1) & 1u, p.status) ? 1 : 0;
+      if (!__shfl_sync(FULL, w, 0)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t scol = tl + S_COL + sb * BKV;
+      const int k0 = j * BKV;
+      // Pass 1: the tile's row maximum (masked keys: later than the query or past the
+      // sequence).
+      float tmax = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < BKV / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(scol + 32 * c, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int kp = k0 + 32 * c + i;
+          const float sv = (kp <= qpos && kp < p.seq) ? __uint_as_float(v[i]) * p.scale_log2 : -INFINITY;
+          tmax = fmaxf(tmax, sv);
+        }
+      }
+      // The previous P V product is done: P's buffer is free and O is current.
+      if (j >= 1) {
+        if (lane == 0) w = mbar_wait(smem_u32(&pv_done), (uint32_t)(j - 1) & 1u, p.status) ? 1 : 0;
+        if (!__shfl_sync(FULL, w, 0)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      float factor = 1.0f;
+      bool grow = false;
+      if (j == 0) {
+        m = tmax;
+      } else if (tmax > m + 8.0f) {
+        factor = exp2f(m - tmax);
+        m = tmax;
+        grow = true;
+      }
+      if (__any_sync(FULL, grow)) {
+        // Rescale the O row (lanes whose maximum did not grow use factor 1).
+        l *= factor;
+#pragma unroll 1
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tl + O_COL + 32 * c, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * factor);
+          tmem_st32(tl + O_COL + 32 * c, v);
+        }
+        tmem_wait_st();
+      }
+      // Pass 2: exponentials, the row sum and P (bf16, 128-byte swizzle: key chunk cc of
+      // 8 at chunk cc ^ (r % 8) of the row's line in its 64-key atom).
+#pragma unroll 1
+      for (int c = 0; c < BKV / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(scol + 32 * c, v);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const int kp = k0 + 32 * c + i;
+          const float e0 = (kp <= qpos && kp < p.seq) ? exp2f(__uint_as_float(v[i]) * p.scale_log2 - m) : 0.f;
+          const float e1 =
+              (kp + 1 <= qpos && kp + 1 < p.seq) ? exp2f(__uint_as_float(v[i + 1]) * p.scale_log2 - m) : 0.f;
+          l += e0 + e1;
+          pk[i / 2] = pack_bf16x2(e0, e1);
+        }
+        uint8_t* atom_row = prow + (c >> 1) * ATOM_BYTES;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int cc = (c & 1) * 4 + u;
+          *reinterpret_cast<uint4*>(atom_row + ((cc ^ (r & 7)) << 4)) =
+              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+      // P's generic stores before the MMA's async-proxy reads; the score buffer is free.
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&s_free[sb]));
+        mbar_arrive(smem_u32(&p_full));
+      }
+    }
+    if (ok) {
+      int w = 1;
+      if (lane == 0) w = mbar_wait(smem_u32(&pv_done), (uint32_t)(ntiles - 1) & 1u, p.status) ? 1 : 0;
+      if (__shfl_sync(FULL, w, 0)) {
+        tc_fence_after();
+        const float inv = 1.0f / l;
+        uint16_t* dst = p.out + (long long)(b * p.seq + qpos) * (p.n_head * HD) + h * HD;
+#pragma unroll 1
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tl + O_COL + 32 * c, v);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) d4[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, ATT_TMEM_COLS);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+}  // namespace
+
+cudaError_t launch_qk_norm(uint16_t* qkv, long long rows, int C, int heads, float eps, cudaStream_t s) {
+  const long long warps = rows * heads;
+  if (warps == 0) return cudaSuccess;
+  return launch_pdl(qk_norm_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s, qkv, rows, C, heads, eps);
+}
+
+cudaError_t launch_attention(const uint16_t* qkv, int batch, int seq, int n_head, int n_kv_head, uint16_t* out,
+                             cudaStream_t s) {
+  AttnParams p;
+  std::memset(&p, 0, sizeof(p));
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorInvalidValue;
+  const long long T = (long long)batch * seq;
+  const int C = (n_head + 2 * n_kv_head) * HD;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(AT), static_cast<cuuint64_t>(T),
+                              static_cast<cuuint64_t>(C / AT)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(C) * 2, static_cast<cuuint64_t>(AT) * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(AT), static_cast<cuuint32_t>(BQ), 2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (fn(&p.qkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(qkv), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  p.out = out;
+  p.status = device_status_ptr();
+  if (!p.status) return cudaErrorInvalidDevicePointer;
+  p.batch = batch;
+  p.seq = seq;
+  p.n_head = n_head;
+  p.n_kv_head = n_kv_head;
+  p.qtiles = (seq + BQ - 1) / BQ;
+  p.scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
+  cudaError_t e = cudaFuncSetAttribute(gqa_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ATT_SMEM);
+  if (e != cudaSuccess) return e;
+  const long long blocks = (long long)p.qtiles * n_head * batch;
+  if (blocks == 0) return cudaSuccess;
+  return launch_pdl(gqa_attention_kernel, dim3((unsigned)blocks), dim3(ATT_THREADS), ATT_SMEM, s, p);
+}
+
+}  // namespace moe

@@ -235,6 +235,18 @@ cudaError_t launch_router_bwd_dx(const int32_t* idx, const float* gate, const fl
 cudaError_t launch_router_wgrad(const float* dzp, const int32_t* off, const int32_t* poff,
                                 const uint16_t* xp, int d, int E, float* dwr, cudaStream_t s);
 
+// ---------------------------------------------------------------- attention block
+// Causal grouped-query attention with per-head QK-norm (attention.cu); head width 128.
+constexpr int kAttnHeadDim = 128;
+// In place on qkv [rows][C] bf16: the first `heads` heads of 128 values of every row
+// (the query and key heads) become u / sqrt(mean(u^2) + eps), rounded to bf16.
+cudaError_t launch_qk_norm(uint16_t* qkv, long long rows, int C, int heads, float eps, cudaStream_t s);
+// out [batch * seq][n_head * 128] bf16: softmax(q k^T / sqrt(128), causal) v per query
+// head, with the key/value head h / (n_head / n_kv_head); qkv [batch * seq][C] holds the
+// normalised query heads, the normalised key heads and the value heads, in that order.
+cudaError_t launch_attention(const uint16_t* qkv, int batch, int seq, int n_head, int n_kv_head, uint16_t* out,
+                             cudaStream_t s);
+
 // ---------------------------------------------------------------- int4 expert cache
 constexpr int kMaxCacheSlots = 256;
 // Device state of the residency cache (least recently used over `slots` HBM slots).

@@ -1186,3 +1186,79 @@ moe_status_t moe_last_device_status(void* stream) {
 size_t moe_workspace_size(const moe_shape_t* shape) { return moe_layer_workspace_size(shape); }
 
 }  // extern "C"
+
+namespace {
+
+moe_status_t check_attn(const moe_attn_shape_t* s) {
+  if (!s) return MOE_ERR_INVALID_ARG;
+  if (s->batch < 1 || s->seq < 1 || s->d < 1 || s->n_head < 1 || s->n_kv_head < 1 || !(s->eps > 0.f))
+    return MOE_ERR_INVALID_ARG;
+  if (s->head_dim != kAttnHeadDim || s->n_head % s->n_kv_head || s->n_head * kAttnHeadDim > 8192 ||
+      s->d % 64 || s->d > 8192 || (long long)s->batch * s->seq > (1LL << 24))
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+struct AttnWs {
+  uint16_t* qkv;  // [T][C]
+  uint16_t* o;    // [T][n_head * 128]
+};
+AttnWs carve_attn(Carver& c, const moe_attn_shape_t* s) {
+  const size_t T = (size_t)s->batch * s->seq;
+  AttnWs w;
+  w.qkv = static_cast<uint16_t*>(c.take(2 * T * (size_t)(s->n_head + 2 * s->n_kv_head) * kAttnHeadDim));
+  w.o = static_cast<uint16_t*>(c.take(2 * T * (size_t)s->n_head * kAttnHeadDim));
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_attention_workspace_size(const moe_attn_shape_t* shape) {
+  if (check_attn(shape)) return 0;
+  Carver c(nullptr);
+  carve_attn(c, shape);
+  return c.off;
+}
+
+moe_status_t moe_attention_core(const moe_attn_shape_t* shape, const void* qkv, void* o, void* stream) {
+  const moe_status_t st = check_attn(shape);
+  if (st) return st;
+  if (!qkv || !o || !aligned16(qkv) || !aligned16(o)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_attention(static_cast<const uint16_t*>(qkv), shape->batch, shape->seq, shape->n_head,
+                                      shape->n_kv_head, static_cast<uint16_t*>(o), static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_attention_fwd(const moe_attn_shape_t* shape, const void* x, const void* w_qkv, const void* w_o,
+                               int32_t residual, void* out, void* workspace, size_t ws_bytes, void* stream) {
+  const moe_status_t st = check_attn(shape);
+  if (st) return st;
+  if (!x || !w_qkv || !w_o || !out || !workspace) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_qkv) || !aligned16(w_o) || !aligned16(out) || !aligned16(workspace))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_attention_workspace_size(shape)) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Carver c(workspace);
+  const AttnWs w = carve_attn(c, shape);
+  const int T = shape->batch * shape->seq, hd = kAttnHeadDim;
+  const int C = (shape->n_head + 2 * shape->n_kv_head) * hd, HO = shape->n_head * hd;
+  int bad = 0;
+  CombineInputs none{};
+  // qkv = x w_qkv^T on the tensor cores (one group over all tokens).
+  const GemmOperandSet off{};
+  const GemmOperandSet proj{x, T, w_qkv, 1, C, shape->d, w.qkv, C, EPI_STORE, T};
+  cudaError_t e = launch_grouped_gemm(off, nullptr, 1, proj, none, 0, s, &bad);
+  if (bad) return MOE_ERR_UNSUPPORTED;
+  if (e == cudaSuccess) e = launch_qk_norm(w.qkv, T, C, shape->n_head + shape->n_kv_head, shape->eps, s);
+  if (e == cudaSuccess) e = launch_attention(w.qkv, shape->batch, shape->seq, shape->n_head, shape->n_kv_head, w.o, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  // out = (x +) o w_o^T: the combine epilogue with no routed rows adds the residual.
+  const CombineInputs res{nullptr, nullptr, nullptr, residual ? static_cast<const uint16_t*>(x) : nullptr, 0};
+  const GemmOperandSet oproj{w.o, T, w_o, 1, shape->d, HO, out, shape->d, residual ? EPI_COMBINE : EPI_STORE, T};
+  e = launch_grouped_gemm(off, nullptr, 1, oproj, res, 0, s, &bad);
+  if (bad) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(e);
+}
+
+}  // extern "C"

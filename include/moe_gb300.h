@@ -346,6 +346,37 @@ moe_status_t moe_layer_fwd_cached(const moe_shape_t* shape, const void* x, const
                                   const void* residual, void* out, const moe_debug_t* dbg, void* workspace,
                                   size_t ws_bytes, void* stream);
 
+/* Attention block of the same model: relay article, opening section, architecture
+ * paragraph (grouped-query attention with four query heads per key/value head, a
+ * per-head QK-norm).  The article states nothing else; this library's readings: head
+ * width 128; the QK-norm is an RMS normalisation of each head's 128 values of q and k
+ * without a learned scale, u / sqrt(mean(u^2) + eps); scores q.k / sqrt(128), causal
+ * within each sequence; no positional encoding; projections without biases.
+ * Token rows are batch-major (row b * seq + s).
+ *   x       [batch*seq][d] bf16
+ *   w_qkv   [(n_head + 2 n_kv_head) * 128][d] bf16: the query, key and value
+ *           projections stacked (query heads, then key heads, then value heads)
+ *   w_o     [d][n_head * 128] bf16
+ *   out     [batch*seq][d] bf16 = x (if residual) + o w_o^T, where o [batch*seq]
+ *           [n_head * 128] is the attention output, rounded to bf16
+ * The projections run on the tensor cores with fp32 accumulation; q, k, v are stored
+ * as bf16 after the projection and again after the norm; the attention kernel keeps the
+ * scores and the output accumulator in fp32 (TMEM) and the probabilities in bf16.
+ * Supported: head_dim == 128, 1 <= n_kv_head <= n_head, n_head % n_kv_head == 0,
+ * n_head * 128 <= 8192, d % 64 == 0 (64 <= d <= 8192), batch >= 1, seq >= 1,
+ * batch * seq <= 2^24, eps > 0.
+ * moe_attention_core computes only the attention: qkv [batch*seq][C] (C = (n_head +
+ * 2 n_kv_head) * 128, the query and key heads already normalised) -> o. */
+typedef struct {
+  int32_t batch, seq, d, n_head, n_kv_head, head_dim;
+  float eps;
+} moe_attn_shape_t;
+
+size_t moe_attention_workspace_size(const moe_attn_shape_t* shape);
+moe_status_t moe_attention_fwd(const moe_attn_shape_t* shape, const void* x, const void* w_qkv, const void* w_o,
+                               int32_t residual, void* out, void* workspace, size_t ws_bytes, void* stream);
+moe_status_t moe_attention_core(const moe_attn_shape_t* shape, const void* qkv, void* o, void* stream);
+
 /* Weight preparation, once per weight update and off the hot path: moe_pack_gate_up
  * for every bf16 layer, then moe_quantize_int4 on the packed gate/up and the down
  * weights for int4 serving.

@@ -129,3 +129,21 @@ def test_short_workspace_name_matches_the_layer_query(lib_path):
     for s in (M.make_shape(8192, 1024, 64, 512, 2048, 2), M.make_shape(64, 64, 8, 32, 128, 2),
               M.make_shape(0, 1024, 64, 512, 2048, 2)):
         assert lib.moe_workspace_size(ctypes.byref(s)) == M.moe_layer_workspace_size(s)
+
+
+def test_attention_calls_validate_on_the_host(lib_path):
+    lib = M.load_library(lib_path)
+    p = ctypes.c_void_p(16)
+    good = M.make_attn_shape(4, 2048, 1024, 8, 2)
+    # q, k, v rows [8192][(8 + 2 + 2) * 128] and the attention output [8192][8 * 128], bf16
+    assert M.moe_attention_workspace_size(good) == 2 * 8192 * 12 * 128 + 2 * 8192 * 8 * 128
+    for bad, code in ((M.make_attn_shape(4, 2048, 1024, 8, 2, head_dim=64), 2),   # head width other than 128
+                      (M.make_attn_shape(4, 2048, 1024, 8, 3), 2),                 # 8 heads do not group by 3
+                      (M.make_attn_shape(4, 2048, 1000, 8, 2), 2),                 # d % 64 != 0
+                      (M.make_attn_shape(0, 2048, 1024, 8, 2), 1),                 # no sequences
+                      (M.make_attn_shape(4, 2048, 1024, 8, 2, eps=0.0), 1)):       # eps must be positive
+        assert M.moe_attention_workspace_size(bad) == 0
+        assert lib.moe_attention_fwd(ctypes.byref(bad), p, p, p, 1, p, p, 1 << 30, None) == code
+        assert lib.moe_attention_core(ctypes.byref(bad), p, p, None) == code
+    assert lib.moe_attention_fwd(ctypes.byref(good), None, p, p, 1, p, p, 1 << 30, None) == 1
+    assert lib.moe_attention_fwd(ctypes.byref(good), p, p, p, 1, p, p, 16, None) == 3  # workspace too small
