@@ -8,7 +8,8 @@
 // sequence, no positional encoding.
 //
 // qk_norm_kernel normalises the query and key heads of the projected [T][C] rows in
-// place (C = (n_head + 2 n_kv_head) * 128: query heads, key heads, value heads).
+// place (C = (n_head + 2 n_kv_head) * 128: query heads, key heads, value heads), one
+// warp per row.
 // gqa_attention_kernel computes one 128-query tile of one head per CTA:
 //   - warp 0 (one thread): TMA copies of the query tile (once) and, per 128-key tile,
 //     the key and value tiles of the head's group into a 2-stage ring;
@@ -17,10 +18,11 @@
 //     instruction descriptor, no transposed copy); S_{j+1} is issued before P_j V_j so
 //     the tensor core works while the softmax warps do;
 //   - warps 2-5 (one query row per thread, its TMEM lane): the online softmax in the
-//     log2 domain, reading the scores twice (maximum, then exponentials), writing P_j
-//     as bf16 into shared memory with the 128-byte swizzle the MMA reads, and rescaling
-//     the O row in TMEM only when the row's maximum grew by more than 8 (2^8), which
-//     keeps every exponential below 256; at the end O / l rounded to bf16.
+//     log2 domain on the row's 128 scores held in registers (causal mask on the
+//     diagonal tile only), writing P_j as bf16 into shared memory with the 128-byte
+//     swizzle the MMA reads, and rescaling the O row in TMEM only when the row's
+//     maximum grew by more than 8 (2^8), which keeps every exponential below 256; at
+//     the end O / l rounded to bf16.
 // Every barrier wait is bounded; on a timeout the status word is set and the CTA exits.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -74,30 +76,49 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// 2^x by the hardware's approximate base-2 exponential (relative error near 2^-22;
+// 2^-inf = 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// One warp per (token, head) of the query and key heads: u / sqrt(mean(u^2) + eps) over
-// the head's 128 values, rounded to bf16 in place.
+// One warp per token row: every query and key head of the row (u / sqrt(mean(u^2) +
+// eps) over the head's 128 values, rounded to bf16 in place); all of the row's loads are
+// issued before the first reduction.
+constexpr int QKN_MAX_HEADS = 16;
 __global__ void qk_norm_kernel(uint16_t* __restrict__ qkv, long long rows, int C, int heads, float eps) {
   pdl_wait();
   pdl_trigger();
-  const long long w = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const long long t = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  if (w >= rows * heads) return;
-  const long long t = w / heads;
-  const int h = (int)(w % heads);
-  uint2* p = reinterpret_cast<uint2*>(qkv + t * C + (long long)h * HD) + lane;  // 4 values per lane
-  const uint2 v = *p;
-  const float a = __uint_as_float(v.x << 16), b = __uint_as_float(v.x & 0xFFFF0000u);
-  const float c = __uint_as_float(v.y << 16), d = __uint_as_float(v.y & 0xFFFF0000u);
-  float ss = a * a + b * b + c * c + d * d;
+  if (t >= rows) return;
+  uint2* row = reinterpret_cast<uint2*>(qkv + t * C) + lane;  // 4 values per lane and head
+  for (int h0 = 0; h0 < heads; h0 += QKN_MAX_HEADS) {
+    const int nh = min(QKN_MAX_HEADS, heads - h0);
+    uint2 v[QKN_MAX_HEADS];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
-  const float f = rsqrtf(ss * (1.0f / HD) + eps);
-  *p = make_uint2(pack_bf16x2(a * f, b * f), pack_bf16x2(c * f, d * f));
+    for (int i = 0; i < QKN_MAX_HEADS; ++i)
+      if (i < nh) v[i] = row[(h0 + i) * (HD / 4)];
+#pragma unroll
+    for (int i = 0; i < QKN_MAX_HEADS; ++i) {
+      if (i < nh) {
+        const float a = __uint_as_float(v[i].x << 16), b = __uint_as_float(v[i].x & 0xFFFF0000u);
+        const float c = __uint_as_float(v[i].y << 16), d = __uint_as_float(v[i].y & 0xFFFF0000u);
+        float ss = a * a + b * b + c * c + d * d;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
+        const float f = rsqrtf(ss * (1.0f / HD) + eps);
+        row[(h0 + i) * (HD / 4)] = make_uint2(pack_bf16x2(a * f, b * f), pack_bf16x2(c * f, d * f));
+      }
+    }
+  }
 }
 
 __global__ void __launch_bounds__(ATT_THREADS, 1) gqa_attention_kernel(const __grid_constant__ AttnParams p) {
@@ -240,21 +261,26 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) gqa_attention_kernel(const __g
       tc_fence_after();
       const uint32_t scol = tl + S_COL + sb * BKV;
       const int k0 = j * BKV;
-      // Pass 1: the tile's row maximum (masked keys: later than the query or past the
-      // sequence).
-      float tmax = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < BKV / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(scol + 32 * c, v);
-        tmem_wait_ld();
+      // The row's 128 scores in registers (one read of the buffer), scaled to the log2
+      // domain.  Only the diagonal tile (j == qi) has keys later than some of its
+      // queries or past the sequence's end: mask there alone.
+      uint32_t v[BKV];
+      tmem_ld32(scol, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      tmem_ld32(scol + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[64]));
+      tmem_ld32(scol + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[96]));
+      tmem_wait_ld();
+      if (j == qi) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int kp = k0 + 32 * c + i;
-          const float sv = (kp <= qpos && kp < p.seq) ? __uint_as_float(v[i]) * p.scale_log2 : -INFINITY;
-          tmax = fmaxf(tmax, sv);
+        for (int i = 0; i < BKV; ++i) {
+          const int kp = k0 + i;
+          if (kp > qpos || kp >= p.seq) v[i] = __float_as_uint(-INFINITY);
         }
       }
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < BKV; ++i) tmax = fmaxf(tmax, __uint_as_float(v[i]));
+      tmax *= p.scale_log2;  // the scale is positive: the maximum commutes with it
       // The previous P V product is done: P's buffer is free and O is current.
       if (j >= 1) {
         if (lane == 0) w = mbar_wait(smem_u32(&pv_done), (uint32_t)(j - 1) & 1u, p.status) ? 1 : 0;
@@ -269,7 +295,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) gqa_attention_kernel(const __g
       if (j == 0) {
         m = tmax;
       } else if (tmax > m + 8.0f) {
-        factor = exp2f(m - tmax);
+        factor = ex2(m - tmax);
         m = tmax;
         grow = true;
       }
@@ -278,29 +304,26 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) gqa_attention_kernel(const __g
         l *= factor;
 #pragma unroll 1
         for (int c = 0; c < HD / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tl + O_COL + 32 * c, v);
+          uint32_t o[32];
+          tmem_ld32(tl + O_COL + 32 * c, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * factor);
-          tmem_st32(tl + O_COL + 32 * c, v);
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * factor);
+          tmem_st32(tl + O_COL + 32 * c, o);
         }
         tmem_wait_st();
       }
-      // Pass 2: exponentials, the row sum and P (bf16, 128-byte swizzle: key chunk cc of
-      // 8 at chunk cc ^ (r % 8) of the row's line in its 64-key atom).
-#pragma unroll 1
+      // Exponentials (one FFMA and one ex2 each; masked keys give 2^-inf = 0), the row
+      // sum and P (bf16, 128-byte swizzle: key chunk cc of 8 at chunk cc ^ (r % 8) of
+      // the row's line in its 64-key atom).
+      const float nm = -m;
+#pragma unroll
       for (int c = 0; c < BKV / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(scol + 32 * c, v);
-        tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const int kp = k0 + 32 * c + i;
-          const float e0 = (kp <= qpos && kp < p.seq) ? exp2f(__uint_as_float(v[i]) * p.scale_log2 - m) : 0.f;
-          const float e1 =
-              (kp + 1 <= qpos && kp + 1 < p.seq) ? exp2f(__uint_as_float(v[i + 1]) * p.scale_log2 - m) : 0.f;
+          const float e0 = ex2(fmaf(__uint_as_float(v[32 * c + i]), p.scale_log2, nm));
+          const float e1 = ex2(fmaf(__uint_as_float(v[32 * c + i + 1]), p.scale_log2, nm));
           l += e0 + e1;
           pk[i / 2] = pack_bf16x2(e0, e1);
         }
@@ -371,9 +394,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }  // namespace
 
 cudaError_t launch_qk_norm(uint16_t* qkv, long long rows, int C, int heads, float eps, cudaStream_t s) {
-  const long long warps = rows * heads;
-  if (warps == 0) return cudaSuccess;
-  return launch_pdl(qk_norm_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s, qkv, rows, C, heads, eps);
+  if (rows == 0 || heads == 0) return cudaSuccess;
+  return launch_pdl(qk_norm_kernel, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, s, qkv, rows, C, heads, eps);
 }
 
 cudaError_t launch_attention(const uint16_t* qkv, int batch, int seq, int n_head, int n_kv_head, uint16_t* out,

@@ -1253,11 +1253,15 @@ moe_status_t moe_attention_fwd(const moe_attn_shape_t* shape, const void* x, con
   if (e == cudaSuccess) e = launch_qk_norm(w.qkv, T, C, shape->n_head + shape->n_kv_head, shape->eps, s);
   if (e == cudaSuccess) e = launch_attention(w.qkv, shape->batch, shape->seq, shape->n_head, shape->n_kv_head, w.o, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  // out = (x +) o w_o^T: the combine epilogue with no routed rows adds the residual.
-  const CombineInputs res{nullptr, nullptr, nullptr, residual ? static_cast<const uint16_t*>(x) : nullptr, 0};
-  const GemmOperandSet oproj{w.o, T, w_o, 1, shape->d, HO, out, shape->d, residual ? EPI_COMBINE : EPI_STORE, T};
-  e = launch_grouped_gemm(off, nullptr, 1, oproj, res, 0, s, &bad);
+  // out = o w_o^T; with the residual, the projection goes to the q, k, v region (free
+  // after the attention) and the combine kernel adds x (no routed rows: k = 0).
+  uint16_t* proj_out = residual ? w.qkv : static_cast<uint16_t*>(out);
+  const GemmOperandSet oproj{w.o, T, w_o, 1, shape->d, HO, proj_out, shape->d, EPI_STORE, T};
+  e = launch_grouped_gemm(off, nullptr, 1, oproj, none, 0, s, &bad);
   if (bad) return MOE_ERR_UNSUPPORTED;
+  if (e == cudaSuccess && residual)
+    e = launch_combine(nullptr, proj_out, nullptr, nullptr, static_cast<const uint16_t*>(x),
+                       static_cast<uint16_t*>(out), T, 0, shape->d, s);
   return cuda_status(e);
 }
 

@@ -40,7 +40,8 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from synth import CONFIGS, f32_from_bf16_bits, make_layer, make_output_grad, make_tokens  # noqa: E402
+from synth import (ATTN_CONFIGS, CONFIGS, f32_from_bf16_bits, make_attention, make_layer,  # noqa: E402
+                   make_output_grad, make_tokens)
 
 METRIC = "MoE-layer fwd tokens/s (T=8192,d=1024,64x512 top-2+2048 shared), % roofline"
 FLUSH_BYTES = 512 << 20
@@ -121,7 +122,7 @@ def parse_args():
     p.add_argument("--steps", type=int, default=300)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=sorted(WORKLOADS), default="nano")
+    p.add_argument("--workload", choices=sorted(WORKLOADS) + ["attn"], default="nano")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -165,8 +166,23 @@ CACHE_SLOTS = {"cache8": 16, "cache8u": 16, "cache1": 4}
 CACHE_BATCHES = 64  # distinct resident token batches the timed steps cycle through
 
 
+ATTN_METRIC = ("Attention block fwd tokens/s (4x GQA, per-head QK-norm, batch 4 x seq 2048, d=1024, "
+               "8 query / 2 key-value heads of 128), % roofline")
+
+
 def workload_shape(name):
     return WORKLOADS[name][1]
+
+
+def attn_algorithmic(s):
+    """FLOPs and bytes of one attention block forward: the projections, the causal
+    attention (scores and the weighted values over the causal triangle of each
+    sequence), weights and the tokens in and out."""
+    hd, C, HO = s.head_dim, (s.n_head + 2 * s.n_kv_head) * s.head_dim, s.n_head * s.head_dim
+    proj = 2 * s.T * s.d * C + 2 * s.T * HO * s.d
+    attn = s.batch * s.n_head * 4 * hd * (s.seq * (s.seq + 1) // 2)
+    nbytes = 2 * (C * s.d + s.d * HO) + 2 * 2 * s.T * s.d
+    return proj, attn, nbytes
 
 
 def config_block(name, n):
@@ -887,6 +903,185 @@ def gpu_cache_arm(args, rank, world, dist):
     print(json.dumps(line), flush=True)
 
 
+def gpu_attn_arm(args, rank, world, dist):
+    """Attention block of the Nano model: one step = one moe_attention_fwd (projections,
+    QK-norm, causal grouped-query attention, output projection with the residual)."""
+    import torch
+
+    import aux_loss_free_gb300 as M
+    from aux_loss_free_gb300.layer import to_device_bf16
+
+    M.load_library()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    s = ATTN_CONFIGS["attn"]
+    H = make_attention(s, "attn", args.seed + rank)
+    ms = M.make_attn_shape(s.batch, s.seq, s.d, s.n_head, s.n_kv_head, s.head_dim, s.eps)
+    x0 = to_device_bf16(H["x"], dev)
+    w_qkv = to_device_bf16(np.concatenate([H["w_q"], H["w_k"], H["w_v"]], axis=0), dev)
+    w_o = to_device_bf16(H["w_o"], dev)
+    ws = torch.empty(M.moe_attention_workspace_size(ms), dtype=torch.uint8, device=dev)
+    out0 = torch.empty(s.T, s.d, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    C = (s.n_head + 2 * s.n_kv_head) * s.head_dim
+    qkv = ws[:s.T * C * 2].view(torch.bfloat16).view(s.T, C)   # the workspace's first region
+    o_core = torch.empty(s.T, s.n_head * s.head_dim, dtype=torch.bfloat16, device=dev)
+
+    def step(x_in, out):
+        M.moe_attention_fwd(ms, x_in, w_qkv, w_o, True, out, ws)
+
+    for _ in range(args.warmup):
+        step(x0, out0)
+    torch.cuda.synchronize(dev)
+    if M.moe_device_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    time.sleep(0.1)
+    K = args.steps
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    for i in range(K):
+        flush.zero_()
+        ev0[i].record(stream)
+        step(x0, out0)
+        ev1[i].record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    if dist:
+        dist.barrier()
+    time.sleep(0.05)
+    sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    total_ms = sum(step_ms)
+    if dist:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    # The attention kernel alone (the block's dominant kernel), on the q, k, v rows the
+    # last step left in the workspace, after the same flush.
+    core_ms = []
+    for i in range(max(3, min(K, 50))):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        M.moe_attention_core(ms, qkv, o_core)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        core_ms.append(a.elapsed_time(b))
+    status = M.moe_device_status()
+    # End to end: tokens in from pinned host memory, the block, the output back, each step.
+    Ke = max(3, min(K, 50))
+    hx = torch.empty(s.T, s.d, dtype=torch.bfloat16, pin_memory=True)
+    hx.copy_(x0.cpu())
+    hout = torch.empty(s.T, s.d, dtype=torch.bfloat16, pin_memory=True)
+    din = torch.empty_like(x0)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(Ke):
+        din.copy_(hx, non_blocking=True)
+        step(din, out0)
+        hout.copy_(out0, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / Ke
+    if rank != 0:
+        return
+    peaks, peak_note = load_peaks()
+    proj, attn, nbytes = attn_algorithmic(s)
+    flops = proj + attn
+    ms_step = total_ms / K
+    roof_s = max(flops / (peaks["bf16_tflops"] * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9))
+    core = statistics.median(core_ms)
+    core_ach = attn / (core / 1e3) / 1e12
+    line = {
+        "metric": ATTN_METRIC, "value": world * s.T * K / (total_ms / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "attention_block_gqa4_qknorm_B4_S2048", "batch": s.batch, "seq": s.seq, "d": s.d,
+                   "n_head": s.n_head, "n_kv_head": s.n_kv_head, "head_dim": s.head_dim, "causal": True,
+                   "residual": True, "l2": "512 MiB write before every timed step (L2 129 MB)",
+                   "parallelism": f"dp{world}"},
+        "layer_roofline": {"flops_per_step": flops, "bytes_per_step": nbytes, "roofline_us": roof_s * 1e6,
+                           "measured_us": ms_step * 1e3, "frac": roof_s / (ms_step / 1e3), "peak": peak_note,
+                           "bound": "tensor"},
+        "roofline": {"kernel": "gqa_attention_kernel (causal attention core)", "bound": "tensor",
+                     "achieved": core_ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": core_ach / peaks["bf16_tflops"], "traffic": None,
+                     "peak_note": peak_note + " (burst)", "flops_per_launch": attn, "avg_launch_us": core * 1e3},
+        "stages_us": {"attention_core": core * 1e3, "projections_qknorm": ms_step * 1e3 - core * 1e3},
+        "step_us": {"median": statistics.median(step_ms) * 1e3, "min": min(step_ms) * 1e3,
+                    "max": max(step_ms) * 1e3},
+        "e2e": {"value": world * s.T / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(hx.numel() * 2), "d2h_bytes_per_step": int(hout.numel() * 2),
+                "copies": "pinned host buffers on the compute stream"},
+        "gpu_launches": K * 5,
+        "clocks": sampler.summary(t_wall0, t_wall1),
+        "device_status": status,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = attn_cpu_baseline(args.seed, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def attn_oracle_runner(seed):
+    """run(seq) -> seconds for the oracle's attention block on one sequence of `seq` tokens."""
+    from oracle import attention_oracle as A
+
+    s = ATTN_CONFIGS["attn"]
+    H = make_attention(s, "attn", seed)
+    bf = lambda b: f32_from_bf16_bits(b).astype(np.float64)  # noqa: E731
+    P = {k: bf(v) for k, v in H.items()}
+
+    def run(seq):
+        t0 = time.perf_counter()
+        A.gqa_attention(P["x"][:seq], P["w_q"], P["w_k"], P["w_v"], P["w_o"], 1, seq, s.n_head, s.n_kv_head,
+                        s.head_dim, s.eps)
+        return time.perf_counter() - t0
+    return run
+
+
+def attn_cpu_baseline(seed, seconds):
+    run = attn_oracle_runner(seed)
+    seq = 512
+    run(64)
+    done, spent = 0, 0.0
+    while spent < seconds and done < 64 * seq:
+        spent += run(seq)
+        done += seq
+    return {"value": done / spent, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{done} tokens as {done // seq} oracle attention blocks of one {seq}-token sequence "
+                      f"(fp64 numpy, BLAS on all {cpu_cores()} visible cores), {spent:.1f} s; a shorter "
+                      f"sequence than the workload's 2048 (causal cost grows with the sequence)"}
+
+
+def attn_reference_arm(args, rank, world):
+    if rank != 0:
+        return
+    run = attn_oracle_runner(args.seed)
+    seq = 512
+    for _ in range(args.warmup):
+        run(seq)
+    times = [run(seq) for _ in range(args.steps)]
+    value = seq * args.steps / sum(times)
+    s = ATTN_CONFIGS["attn"]
+    line = {"impl": "reference", "metric": ATTN_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "attention_block_gqa4_qknorm_B4_S2048", "batch": s.batch, "seq": s.seq,
+                       "d": s.d, "n_head": s.n_head, "n_kv_head": s.n_kv_head, "head_dim": s.head_dim},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "kind": "oracle", "cores": cpu_cores(),
+                             "sample": f"each step: the oracle attention block on one {seq}-token sequence"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -895,7 +1090,7 @@ def main():
         print(json.dumps({"error": "run N>1 under torch.distributed.run"}), flush=True)
         sys.exit(2)
     if args.impl == "reference":
-        reference_arm(args, rank, world)
+        (attn_reference_arm if args.workload == "attn" else reference_arm)(args, rank, world)
         return
     dist = None
     if world > 1:
@@ -906,7 +1101,7 @@ def main():
         dist = tdist
     try:
         arm = gpu_train_arm if args.workload == "train" else (
-            gpu_cache_arm if args.workload in CACHE_SLOTS else gpu_arm)
+            gpu_cache_arm if args.workload in CACHE_SLOTS else (gpu_attn_arm if args.workload == "attn" else gpu_arm))
         arm(args, rank, world, dist)
     finally:
         if dist:
