@@ -11,12 +11,16 @@
 // place (C = (n_head + 2 n_kv_head) * 128: query heads, key heads, value heads), one
 // warp per row.
 // gqa_attention_kernel computes one 128-query tile of one head per CTA:
-//   - warp 0 (one thread): TMA copies of the query tile (once) and, per 128-key tile,
-//     the key and value tiles of the head's group into a 2-stage ring;
+//   - warp 0 (one thread): TMA copies of the query tile (once) and of the key tiles of
+//     the head's group into a 2-stage ring, each stage freed as soon as its S MMA is
+//     done, so the key tile two ahead streams in during the softmax; warp 6 (one
+//     thread): the value tiles into their own 2-stage ring, freed by the P V MMA;
 //   - warp 1 (one thread): tcgen05.mma, S_j = Q K_j^T into one of two TMEM score
 //     buffers, and O += P_j V_j into the TMEM output (V read MN-major through the
-//     instruction descriptor, no transposed copy); S_{j+1} is issued before P_j V_j so
-//     the tensor core works while the softmax warps do;
+//     instruction descriptor, no transposed copy) with P_j from one of two shared-memory
+//     buffers; S_{j+1} is issued before P_j V_j, and the softmax of tile j + 1 writes
+//     the other P buffer while P_j V_j runs, so the tensor core and the softmax warps
+//     overlap;
 //   - warps 2-5 (one query row per thread, its TMEM lane): the online softmax in the
 //     log2 domain on the row's 128 scores held in registers (causal mask on the
 //     diagonal tile only), writing P_j as bf16 into shared memory with the 128-byte
@@ -45,10 +49,12 @@ constexpr int ATOM_BYTES = 128 * AT * 2;      // 16 KB: 128 rows x 64
 constexpr int TILE_BYTES = 2 * ATOM_BYTES;    // 32 KB: 128 rows x 128
 constexpr int KV_STAGES = 2;
 constexpr int Q_OFF = 0;
-constexpr int KV_OFF = TILE_BYTES;            // stage s: K at KV_OFF + 2 s TILE, V one tile later
-constexpr int P_OFF = KV_OFF + KV_STAGES * 2 * TILE_BYTES;
-constexpr int ATT_SMEM = P_OFF + TILE_BYTES + 1024;
-constexpr int ATT_THREADS = 192;
+constexpr int K_OFF = TILE_BYTES;                       // key stage s at K_OFF + s TILE
+constexpr int V_OFF = K_OFF + KV_STAGES * TILE_BYTES;   // value stage s at V_OFF + s TILE
+constexpr int P_OFF = V_OFF + KV_STAGES * TILE_BYTES;
+constexpr int P_BUFS = 2;
+constexpr int ATT_SMEM = P_OFF + P_BUFS * TILE_BYTES + 1024;
+constexpr int ATT_THREADS = 224;
 constexpr uint32_t S_COL = 0;                 // score buffers: columns [0, 128) and [128, 256)
 constexpr uint32_t O_COL = 256;               // output accumulator: columns [256, 384)
 constexpr uint32_t ATT_TMEM_COLS = 512;
@@ -124,12 +130,14 @@ __global__ void qk_norm_kernel(uint16_t* __restrict__ qkv, long long rows, int C
 __global__ void __launch_bounds__(ATT_THREADS, 1) gqa_attention_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t q_full;
-  __shared__ __align__(8) uint64_t kv_full[KV_STAGES];
-  __shared__ __align__(8) uint64_t kv_empty[KV_STAGES];
+  __shared__ __align__(8) uint64_t k_full[KV_STAGES];
+  __shared__ __align__(8) uint64_t k_empty[KV_STAGES];
+  __shared__ __align__(8) uint64_t v_full[KV_STAGES];
+  __shared__ __align__(8) uint64_t v_empty[KV_STAGES];
   __shared__ __align__(8) uint64_t s_full[2];
   __shared__ __align__(8) uint64_t s_free[2];
-  __shared__ __align__(8) uint64_t p_full;
-  __shared__ __align__(8) uint64_t pv_done;
+  __shared__ __align__(8) uint64_t p_full[P_BUFS];
+  __shared__ __align__(8) uint64_t pv_done[P_BUFS];
   __shared__ uint32_t tmem_holder;
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -149,15 +157,19 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) gqa_attention_kernel(const __g
   if (warp == 0 && lane == 0) {
     mbar_init(smem_u32(&q_full), 1);
     for (int s = 0; s < KV_STAGES; ++s) {
-      mbar_init(smem_u32(&kv_full[s]), 1);
-      mbar_init(smem_u32(&kv_empty[s]), 1);
+      mbar_init(smem_u32(&k_full[s]), 1);
+      mbar_init(smem_u32(&k_empty[s]), 1);
+      mbar_init(smem_u32(&v_full[s]), 1);
+      mbar_init(smem_u32(&v_empty[s]), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&s_full[s]), 1);
       mbar_init(smem_u32(&s_free[s]), 4);
     }
-    mbar_init(smem_u32(&p_full), 4);
-    mbar_init(smem_u32(&pv_done), 1);
+    for (int s = 0; s < P_BUFS; ++s) {
+      mbar_init(smem_u32(&p_full[s]), 4);
+      mbar_init(smem_u32(&pv_done[s]), 1);
+    }
     fence_mbar_init();
     tma_prefetch_desc(&p.qkv);
   }
@@ -172,28 +184,33 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) gqa_attention_kernel(const __g
   pdl_wait();  // the projected, normalised rows come from earlier kernels
   pdl_trigger();
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 6) {
     if (lane == 0) {
-      // ------------------------------------------------ TMA producer
-      mbar_arrive_expect_tx(smem_u32(&q_full), TILE_BYTES);
-      tma_load_3d(base + Q_OFF, &p.qkv, smem_u32(&q_full), 0, row0, q_atom);
+      // ------------------------------------------------ TMA producers: keys (warp 0,
+      // which also copies the query tile) and values (warp 6)
+      const bool keys = warp == 0;
+      uint64_t* const full = keys ? k_full : v_full;
+      uint64_t* const empty = keys ? k_empty : v_empty;
+      const uint32_t ring = base + (keys ? K_OFF : V_OFF);
+      const int atom = keys ? k_atom : v_atom;
+      if (keys) {
+        mbar_arrive_expect_tx(smem_u32(&q_full), TILE_BYTES);
+        tma_load_3d(base + Q_OFF, &p.qkv, smem_u32(&q_full), 0, row0, q_atom);
+      }
       int issued = 0;
       for (int j = 0; j < ntiles; ++j) {
         const int st = j % KV_STAGES;
         const uint32_t ph = (uint32_t)(j / KV_STAGES) & 1u;
-        if (!mbar_wait_spin(smem_u32(&kv_empty[st]), ph ^ 1u, p.status)) break;
-        const uint32_t kv = base + KV_OFF + st * 2 * TILE_BYTES;
-        const uint32_t fb = smem_u32(&kv_full[st]);
-        mbar_arrive_expect_tx(fb, 2 * TILE_BYTES);
-        const int krow = b * p.seq + j * BKV;
-        tma_load_3d(kv, &p.qkv, fb, 0, krow, k_atom);
-        tma_load_3d(kv + TILE_BYTES, &p.qkv, fb, 0, krow, v_atom);
+        if (!mbar_wait_spin(smem_u32(&empty[st]), ph ^ 1u, p.status)) break;
+        const uint32_t fb = smem_u32(&full[st]);
+        mbar_arrive_expect_tx(fb, TILE_BYTES);
+        tma_load_3d(ring + st * TILE_BYTES, &p.qkv, fb, 0, b * p.seq + j * BKV, atom);
         issued = j + 1;
       }
       // No copy may still be landing when the CTA exits.
-      mbar_wait_spin(smem_u32(&q_full), 0, p.status);
+      if (keys) mbar_wait_spin(smem_u32(&q_full), 0, p.status);
       for (int j = issued > KV_STAGES ? issued - KV_STAGES : 0; j < issued; ++j)
-        mbar_wait_spin(smem_u32(&kv_full[j % KV_STAGES]), (uint32_t)(j / KV_STAGES) & 1u, p.status);
+        mbar_wait_spin(smem_u32(&full[j % KV_STAGES]), (uint32_t)(j / KV_STAGES) & 1u, p.status);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -203,51 +220,53 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) gqa_attention_kernel(const __g
       bool ok = mbar_wait_spin(smem_u32(&q_full), 0, p.status);
       tc_fence_after();
       const uint64_t qdesc = sw128_kmajor_desc(base + Q_OFF);
-      const uint64_t pdesc = sw128_kmajor_desc(base + P_OFF);
       for (int j = 0; j <= ntiles && ok; ++j) {
         if (j < ntiles) {
           const int st = j % KV_STAGES;
           const int sb = j & 1;
-          if (!mbar_wait_spin(smem_u32(&kv_full[st]), (uint32_t)(j / KV_STAGES) & 1u, p.status) ||
+          if (!mbar_wait_spin(smem_u32(&k_full[st]), (uint32_t)(j / KV_STAGES) & 1u, p.status) ||
               !mbar_wait_spin(smem_u32(&s_free[sb]), ((uint32_t)(j >> 1) & 1u) ^ 1u, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t kdesc = sw128_kmajor_desc(base + KV_OFF + st * 2 * TILE_BYTES);
+          const uint64_t kdesc = sw128_kmajor_desc(base + K_OFF + st * TILE_BYTES);
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk)  // atom kk / 4, 32 bytes per K step inside it
             tc_mma_bf16(tmem + S_COL + sb * BKV, qdesc + (kk >> 2) * (ATOM_BYTES >> 4) + 2 * (kk & 3),
                         kdesc + (kk >> 2) * (ATOM_BYTES >> 4) + 2 * (kk & 3), id_s, kk != 0);
+          tc_commit(smem_u32(&k_empty[st]));
           tc_commit(smem_u32(&s_full[sb]));
         }
         if (j >= 1) {
-          const int jp = j - 1, st = jp % KV_STAGES;
-          if (!mbar_wait_spin(smem_u32(&p_full), (uint32_t)jp & 1u, p.status)) {
+          const int jp = j - 1, st = jp % KV_STAGES, pb = jp & 1;
+          if (!mbar_wait_spin(smem_u32(&p_full[pb]), (uint32_t)(jp >> 1) & 1u, p.status) ||
+              !mbar_wait_spin(smem_u32(&v_full[st]), (uint32_t)(jp / KV_STAGES) & 1u, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
           // V [keys][HD] is the MN-major B of O += P V: 64-column atoms 16 KB apart, a
           // 16-key step two 1024-byte atoms further.
-          const uint64_t vdesc = sw128_mnmajor_desc(base + KV_OFF + st * 2 * TILE_BYTES + TILE_BYTES, ATOM_BYTES);
+          const uint64_t vdesc = sw128_mnmajor_desc(base + V_OFF + st * TILE_BYTES, ATOM_BYTES);
+          const uint64_t pdesc = sw128_kmajor_desc(base + P_OFF + pb * TILE_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BKV / 16; ++kk)
             tc_mma_bf16(tmem + O_COL, pdesc + (kk >> 2) * (ATOM_BYTES >> 4) + 2 * (kk & 3), vdesc + kk * 128u,
                         id_pv, (jp | kk) != 0);
-          tc_commit(smem_u32(&kv_empty[st]));
-          tc_commit(smem_u32(&pv_done));
+          tc_commit(smem_u32(&v_empty[st]));
+          tc_commit(smem_u32(&pv_done[pb]));
         }
       }
     }
-  } else {
+  } else if (warp <= 5) {
     // -------------------------------------------------- softmax warps 2..5
     const int q4 = warp & 3;             // TMEM lanes [32 q4, 32 q4 + 32)
     const int r = q4 * 32 + lane;        // query row of the tile
     const int qpos = qi * BQ + r;        // position in the sequence
     const bool valid = qpos < p.seq;
     const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
-    uint8_t* const prow = base_ptr + P_OFF + (r >> 3) * 1024 + (r & 7) * 128;
+    uint8_t* const prow0 = base_ptr + P_OFF + (r >> 3) * 1024 + (r & 7) * 128;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
@@ -270,6 +289,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) gqa_attention_kernel(const __g
       tmem_ld32(scol + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[64]));
       tmem_ld32(scol + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[96]));
       tmem_wait_ld();
+      // The scores are in registers: the buffer can take S_{j+2}.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&s_free[sb]));
       if (j == qi) {
 #pragma unroll
         for (int i = 0; i < BKV; ++i) {
@@ -277,19 +300,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) gqa_attention_kernel(const __g
           if (kp > qpos || kp >= p.seq) v[i] = __float_as_uint(-INFINITY);
         }
       }
-      float tmax = -INFINITY;
+      float mx[8];
 #pragma unroll
-      for (int i = 0; i < BKV; ++i) tmax = fmaxf(tmax, __uint_as_float(v[i]));
+      for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(v[i]);
+#pragma unroll
+      for (int i = 8; i < BKV; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(v[i]));
+      float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       tmax *= p.scale_log2;  // the scale is positive: the maximum commutes with it
-      // The previous P V product is done: P's buffer is free and O is current.
-      if (j >= 1) {
-        if (lane == 0) w = mbar_wait(smem_u32(&pv_done), (uint32_t)(j - 1) & 1u, p.status) ? 1 : 0;
-        if (!__shfl_sync(FULL, w, 0)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-      }
       float factor = 1.0f;
       bool grow = false;
       if (j == 0) {
@@ -299,7 +316,28 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) gqa_attention_kernel(const __g
         m = tmax;
         grow = true;
       }
-      if (__any_sync(FULL, grow)) {
+      const bool any_grow = __any_sync(FULL, grow);
+      // Before P_j is written, the product that last read its buffer (P_{j-2} V_{j-2})
+      // must be done; before O is rescaled, every earlier product (P_{j-1} V_{j-1}).
+      // Every phase of each buffer's barrier is awaited in order, so no parity wait can
+      // be taken for an older phase.
+      if (j >= 2) {
+        if (lane == 0) w = mbar_wait(smem_u32(&pv_done[j & 1]), (uint32_t)((j - 2) >> 1) & 1u, p.status) ? 1 : 0;
+        if (!__shfl_sync(FULL, w, 0)) {
+          ok = false;
+          break;
+        }
+      }
+      if (any_grow && j >= 1) {
+        if (lane == 0)
+          w = mbar_wait(smem_u32(&pv_done[(j - 1) & 1]), (uint32_t)((j - 1) >> 1) & 1u, p.status) ? 1 : 0;
+        if (!__shfl_sync(FULL, w, 0)) {
+          ok = false;
+          break;
+        }
+      }
+      tc_fence_after();
+      if (any_grow) {
         // Rescale the O row (lanes whose maximum did not grow use factor 1).
         l *= factor;
 #pragma unroll 1
@@ -317,6 +355,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) gqa_attention_kernel(const __g
       // sum and P (bf16, 128-byte swizzle: key chunk cc of 8 at chunk cc ^ (r % 8) of
       // the row's line in its 64-key atom).
       const float nm = -m;
+      uint8_t* const prow = prow0 + (j & 1) * TILE_BYTES;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < BKV / 32; ++c) {
         uint32_t pk[16];
@@ -324,7 +364,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) gqa_attention_kernel(const __g
         for (int i = 0; i < 32; i += 2) {
           const float e0 = ex2(fmaf(__uint_as_float(v[32 * c + i]), p.scale_log2, nm));
           const float e1 = ex2(fmaf(__uint_as_float(v[32 * c + i + 1]), p.scale_log2, nm));
-          l += e0 + e1;
+          ls[(i >> 1) & 3] += e0 + e1;
           pk[i / 2] = pack_bf16x2(e0, e1);
         }
         uint8_t* atom_row = prow + (c >> 1) * ATOM_BYTES;
@@ -335,18 +375,17 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) gqa_attention_kernel(const __g
               make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
         }
       }
-      // P's generic stores before the MMA's async-proxy reads; the score buffer is free.
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      // P's generic stores before the MMA's async-proxy reads.
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&s_free[sb]));
-        mbar_arrive(smem_u32(&p_full));
-      }
+      if (lane == 0) mbar_arrive(smem_u32(&p_full[j & 1]));
     }
     if (ok) {
       int w = 1;
-      if (lane == 0) w = mbar_wait(smem_u32(&pv_done), (uint32_t)(ntiles - 1) & 1u, p.status) ? 1 : 0;
+      const int last = ntiles - 1;
+      if (lane == 0) w = mbar_wait(smem_u32(&pv_done[last & 1]), (uint32_t)(last >> 1) & 1u, p.status) ? 1 : 0;
       if (__shfl_sync(FULL, w, 0)) {
         tc_fence_after();
         const float inv = 1.0f / l;
