@@ -17,14 +17,14 @@
 //     thread): the value tiles into their own 2-stage ring, freed by the P V MMA;
 //   - warp 1 (one thread): tcgen05.mma, S_j = Q K_j^T into one of two TMEM score
 //     buffers, and O += P_j V_j into the TMEM output (V read MN-major through the
-//     instruction descriptor, no transposed copy) with P_j from one of two shared-memory
-//     buffers; S_{j+1} is issued before P_j V_j, and the softmax of tile j + 1 writes
-//     the other P buffer while P_j V_j runs, so the tensor core and the softmax warps
-//     overlap;
+//     instruction descriptor, no transposed copy) with P_j read from one of two TMEM
+//     buffers as the MMA's A operand; S_{j+1} is issued before P_j V_j, and the softmax
+//     of tile j + 1 writes the other P buffer while P_j V_j runs, so the tensor core and
+//     the softmax warps overlap;
 //   - warps 2-5 (one query row per thread, its TMEM lane): the online softmax in the
 //     log2 domain on the row's 128 scores held in registers (causal mask on the
-//     diagonal tile only), writing P_j as bf16 into shared memory with the 128-byte
-//     swizzle the MMA reads, and rescaling the O row in TMEM only when the row's
+//     diagonal tile only), writing P_j as bf16 pairs into the row's TMEM lane, and
+//     rescaling the O row in TMEM only when the row's
 //     maximum grew by more than 8 (2^8), which keeps every exponential below 256; at
 //     the end O / l rounded to bf16.
 // Every barrier wait is bounded; on a timeout the status word is set and the CTA exits.
@@ -51,12 +51,12 @@ constexpr int KV_STAGES = 2;
 constexpr int Q_OFF = 0;
 constexpr int K_OFF = TILE_BYTES;                       // key stage s at K_OFF + s TILE
 constexpr int V_OFF = K_OFF + KV_STAGES * TILE_BYTES;   // value stage s at V_OFF + s TILE
-constexpr int P_OFF = V_OFF + KV_STAGES * TILE_BYTES;
+constexpr int ATT_SMEM = V_OFF + KV_STAGES * TILE_BYTES + 1024;
 constexpr int P_BUFS = 2;
-constexpr int ATT_SMEM = P_OFF + P_BUFS * TILE_BYTES + 1024;
 constexpr int ATT_THREADS = 224;
 constexpr uint32_t S_COL = 0;                 // score buffers: columns [0, 128) and [128, 256)
 constexpr uint32_t O_COL = 256;               // output accumulator: columns [256, 384)
+constexpr uint32_t P_COL = 384;               // P buffers, bf16 pairs: columns [384, 448) and [448, 512)
 constexpr uint32_t ATT_TMEM_COLS = 512;
 constexpr unsigned FULL = 0xFFFFFFFFu;
 
@@ -81,6 +81,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] * B[smem], one 128 x N x 16 step with A read from tensor memory:
+// row m of A in lane m, two bf16 values per 32-bit column (the even k in the low half).
+__device__ __forceinline__ void tc_mma_bf16_a_tmem(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                   uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 
 // 2^x by the hardware's approximate base-2 exponential (relative error near 2^-22;
 // 2^-inf = 0).
@@ -141,7 +153,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) gqa_attention_kernel(const __g
   __shared__ uint32_t tmem_holder;
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  uint8_t* const base_ptr = smem_raw + (base - smem_u32(smem_raw));
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // The longest query tiles (most key tiles under the causal mask) go first.
   const int per_tile = p.n_head * p.batch;
@@ -249,11 +260,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) gqa_attention_kernel(const __g
           // V [keys][HD] is the MN-major B of O += P V: 64-column atoms 16 KB apart, a
           // 16-key step two 1024-byte atoms further.
           const uint64_t vdesc = sw128_mnmajor_desc(base + V_OFF + st * TILE_BYTES, ATOM_BYTES);
-          const uint64_t pdesc = sw128_kmajor_desc(base + P_OFF + pb * TILE_BYTES);
+          const uint32_t pcol = tmem + P_COL + pb * (BKV / 2);  // 16 keys = 8 columns per step
 #pragma unroll
           for (int kk = 0; kk < BKV / 16; ++kk)
-            tc_mma_bf16(tmem + O_COL, pdesc + (kk >> 2) * (ATOM_BYTES >> 4) + 2 * (kk & 3), vdesc + kk * 128u,
-                        id_pv, (jp | kk) != 0);
+            tc_mma_bf16_a_tmem(tmem + O_COL, pcol + kk * 8, vdesc + kk * 128u, id_pv, (jp | kk) != 0);
           tc_commit(smem_u32(&v_empty[st]));
           tc_commit(smem_u32(&pv_done[pb]));
         }
@@ -266,7 +276,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) gqa_attention_kernel(const __g
     const int qpos = qi * BQ + r;        // position in the sequence
     const bool valid = qpos < p.seq;
     const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
-    uint8_t* const prow0 = base_ptr + P_OFF + (r >> 3) * 1024 + (r & 7) * 128;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
@@ -352,32 +361,24 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) gqa_attention_kernel(const __g
         tmem_wait_st();
       }
       // Exponentials (one FFMA and one ex2 each; masked keys give 2^-inf = 0), the row
-      // sum and P (bf16, 128-byte swizzle: key chunk cc of 8 at chunk cc ^ (r % 8) of
-      // the row's line in its 64-key atom).
+      // sum and P (bf16 pairs, keys 2c and 2c + 1 in column c of the row's P buffer).
       const float nm = -m;
-      uint8_t* const prow = prow0 + (j & 1) * TILE_BYTES;
+      const uint32_t pcol = tl + P_COL + (j & 1) * (BKV / 2);
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < BKV / 32; ++c) {
-        uint32_t pk[16];
+      for (int c = 0; c < BKV / 64; ++c) {
+        uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float e0 = ex2(fmaf(__uint_as_float(v[32 * c + i]), p.scale_log2, nm));
-          const float e1 = ex2(fmaf(__uint_as_float(v[32 * c + i + 1]), p.scale_log2, nm));
+        for (int i = 0; i < 64; i += 2) {
+          const float e0 = ex2(fmaf(__uint_as_float(v[64 * c + i]), p.scale_log2, nm));
+          const float e1 = ex2(fmaf(__uint_as_float(v[64 * c + i + 1]), p.scale_log2, nm));
           ls[(i >> 1) & 3] += e0 + e1;
           pk[i / 2] = pack_bf16x2(e0, e1);
         }
-        uint8_t* atom_row = prow + (c >> 1) * ATOM_BYTES;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int cc = (c & 1) * 4 + u;
-          *reinterpret_cast<uint4*>(atom_row + ((cc ^ (r & 7)) << 4)) =
-              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-        }
+        tmem_st32(pcol + 32 * c, pk);
       }
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      // P's generic stores before the MMA's async-proxy reads.
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tmem_wait_st();  // P is in TMEM before the MMA may read it
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&p_full[j & 1]));

@@ -5,7 +5,9 @@ C ABI.
 moe_attention_core (the tcgen05 attention kernel alone) is fed the oracle's own
 normalised q, k and v (bf16), so it is checked in isolation; moe_attention_fwd (the
 projections on the tensor cores, the QK-norm kernel, the attention kernel, the output
-projection with the residual) is checked end to end.  Tolerance: the bf16 bound of
+projection with the residual) is checked end to end.  The head groupings (1, 2, 4 and 8
+query heads per key/value head) reach every cluster size of the kernel (key and value
+tiles shared by 1, 2 or 4 CTAs through multicast copies).  Tolerance: the bf16 bound of
 gpu_util (2e-2 relative L2 plus an element-wise bound).
 """
 import numpy as np
@@ -41,6 +43,7 @@ CORE_CASES = [
     ATTN_CONFIGS["attn_tiny"].replace(batch=1, seq=1),                    # one token
     ATTN_CONFIGS["attn_tiny"].replace(batch=2, seq=129, n_head=2, n_kv_head=2, d=256),  # no grouping
     ATTN_CONFIGS["attn_tiny"].replace(batch=1, seq=700, n_head=8, n_kv_head=1, d=1024),  # one shared head
+    ATTN_CONFIGS["attn_tiny"].replace(batch=2, seq=260, n_head=4, n_kv_head=2, d=512),   # pairs of heads
 ]
 
 
