@@ -209,6 +209,36 @@ cudaError_t launch_int4_gate_up(const int32_t* active, const int32_t* offsets, c
 // Top-1 serving without the permutation (at most kDirectMaxPairs (token, expert)
 // pairs): gate_up: h[p][f] from x[p / k]; down: y[p][d] from h[p]; p = t * k + j.
 constexpr int kDirectMaxPairs = 64;
+
+// Top-1 serving with at most kServeMaxPairs (token, expert) pairs in one persistent
+// launch (serve.cu): router, selection, bias update, shared and int4 routed experts,
+// combine.  bf16 tokens and int4 routed weights; x, W_r and the shared expert's
+// weights 16-byte aligned; its shared memory (the CTA's weight slices, x, hs, h, the
+// logits) at most kServeMaxSmem bytes.
+constexpr int kServeMaxPairs = 8;
+constexpr size_t kServeMaxSmem = 200 * 1024;
+struct ServeArgs {
+  const void* x;
+  const float* w_router;
+  const float* logit_offset;
+  float* bias;
+  const moe_weights_t* w;
+  const void* residual;
+  uint16_t* out;
+  float* scores;
+  int32_t* idx;
+  float* gate;
+  int32_t* load;
+  moe_balance_t* balance;
+  void* scratch;  // serve_fused_scratch_bytes(shape)
+  uint16_t* hs;   // [T][F]
+  uint16_t* h;    // [T*k][f]
+  int update_bias;
+  float gamma;
+};
+bool serve_fused_supported(const moe_shape_t* s, const void* x, const float* w_router, const moe_weights_t* w);
+size_t serve_fused_scratch_bytes(const moe_shape_t* s);
+cudaError_t launch_serve_fused(const moe_shape_t* s, const ServeArgs& a, cudaStream_t st);
 cudaError_t launch_int4_direct(bool gate_up, const int32_t* idx, int pairs, int k, const uint8_t* wq,
                                const uint16_t* ws, const uint16_t* src, uint16_t* dst, int d, int f,
                                int block, cudaStream_t s, const int32_t* slot = nullptr);

@@ -205,6 +205,7 @@ struct LayerWs {
   int32_t* inv_pos;
   uint16_t* y;
   uint16_t* s_out;  // [T][d] shared-expert output (before the combine)
+  void* serve;      // fused serving scratch (int4 shapes with at most kServeMaxPairs pairs)
   PermuteWs perm;
   FfnWs ffn;
 };
@@ -229,6 +230,11 @@ LayerWs carve_layer(Carver& c, const moe_shape_t* s) {
     w.load = w.perm.counts + (size_t)chunks * s->E;
   }
   w.ffn = carve_ffn(c, s);
+  // The fused serving launch's logits and sync words: carved from the shape alone, so
+  // the workspace size does not depend on the device.
+  w.serve = (s->w_format == MOE_W_INT4_G32 && s->x_dtype == MOE_X_BF16 && Tk <= (size_t)kServeMaxPairs)
+                ? c.take(serve_fused_scratch_bytes(s))
+                : nullptr;
   return w;
 }
 
@@ -614,6 +620,35 @@ moe_status_t layer_fwd_impl(const moe_shape_t* shape, const void* x, const float
   int ct;
   const int chunks = layer_chunks_of(shape, &ct);
   const int xf = shape->x_dtype == MOE_X_F32;
+  // Top-1 serving of at most kServeMaxPairs pairs: one persistent launch does the whole
+  // layer (not with an expert cache, whose fill runs between routing and experts, nor
+  // when the caller asks for the permutation).
+  if (int4 && !cache && L.serve && !(dbg && (dbg->offsets || dbg->perm_tok || dbg->inv_pos)) &&
+      serve_fused_supported(shape, x, w_router, w)) {
+    ServeArgs a{};
+    a.x = x;
+    a.w_router = w_router;
+    a.logit_offset = logit_offset;
+    a.bias = bias;
+    a.w = w;
+    a.residual = residual;
+    a.out = static_cast<uint16_t*>(out);
+    a.scores = dbg ? dbg->scores : nullptr;
+    a.idx = L.idx;
+    a.gate = L.gate;
+    a.load = dbg ? dbg->load : nullptr;
+    a.balance = dbg ? dbg->balance : nullptr;
+    a.scratch = L.serve;
+    a.hs = L.ffn.hs;
+    a.h = L.ffn.h;
+    a.update_bias = update_bias;
+    a.gamma = gamma;
+    const bool prof = prof_begin_call();
+    if (prof) prof_mark("serve_fused", s);
+    const cudaError_t e = launch_serve_fused(shape, a, s);
+    if (prof) prof_mark(nullptr, s);
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
 
   const bool prof = prof_begin_call();
   const bool tc = router_tc_supported(T, E, xf);

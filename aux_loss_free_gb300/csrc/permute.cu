@@ -9,6 +9,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "select.cuh"
 
 namespace moe {
 namespace {
@@ -65,40 +66,6 @@ __global__ void count_kernel(const int32_t* __restrict__ idx, int T, int k, int 
     return;
   }
   atomicAdd(&counts[(long long)(t / chunk_tokens) * E + e], 1);
-}
-
-// Balance statistics of load[0..E) (moe_balance_t) by one warp; lane 0 writes them.
-// The ratios are the fp32 values nearest to the exact rationals: the fp64 quotient of
-// the two exact integers is correctly rounded, and rounding it again to fp32 gives the
-// nearest fp32 for denominators below 2^28 (the exact quotient then never lies within
-// half an fp64 ulp of an fp32 rounding boundary unless it is one).
-__device__ __forceinline__ void warp_balance(const int32_t* load, int E, moe_balance_t* out, int lane) {
-  int mx = 0, mn = 0x7FFFFFFF, dead = 0;
-  long long sum = 0;
-  for (int e = lane; e < E; e += 32) {
-    const int v = load[e];
-    mx = max(mx, v);
-    mn = min(mn, v);
-    dead += v == 0;
-    sum += v;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    mx = max(mx, __shfl_xor_sync(FULL, mx, o));
-    mn = min(mn, __shfl_xor_sync(FULL, mn, o));
-    dead += __shfl_xor_sync(FULL, dead, o);
-    sum += __shfl_xor_sync(FULL, sum, o);
-  }
-  if (lane == 0) {
-    out->pairs = sum;
-    out->max_load = mx;
-    out->min_load = mn;
-    out->dead_experts = dead;
-    const double pe = (double)sum;
-    out->max_over_mean = sum > 0 ? __double2float_rn(__ddiv_rn((double)mx * E, pe)) : 0.f;
-    out->min_over_mean = sum > 0 ? __double2float_rn(__ddiv_rn((double)mn * E, pe)) : 0.f;
-    out->dead_fraction = __double2float_rn(__ddiv_rn((double)dead, (double)E));
-  }
 }
 
 constexpr int SC_THREADS = 256;
@@ -199,12 +166,8 @@ __global__ void __launch_bounds__(SC_THREADS) scatter_kernel(
     if (balance && warp == 1) warp_balance(tot_e, E, balance, lane);
     if (tid < E) {
       if (load_out) load_out[tid] = tot_e[tid];
-      if (bias) {
-        // Aux-loss-free update: sign(T*k - E*load) is sign(target - load), sign(0) = 0.
-        const long long diff = tokens_times_k - (long long)E * tot_e[tid];
-        const float step = diff > 0 ? gamma : (diff < 0 ? -gamma : 0.f);
-        bias[tid] = __fadd_rn(bias[tid], step);
-      }
+      // Aux-loss-free update: sign(T*k - E*load) is sign(target - load), sign(0) = 0.
+      if (bias) bias[tid] = biased_step(bias[tid], tokens_times_k, E, tot_e[tid], gamma);
     }
   }
   __syncthreads();
@@ -296,9 +259,7 @@ __global__ void bias_update_kernel(int E, long long tokens_times_k, const int32_
     for (int w = 0; w < (int)(blockDim.x / 32); ++w) tokens_times_k += s_part[w];
   }
   if (e >= E || !bias) return;
-  const long long diff = tokens_times_k - (long long)E * v;
-  const float step = diff > 0 ? gamma : (diff < 0 ? -gamma : 0.f);
-  bias[e] = __fadd_rn(bias[e], step);
+  bias[e] = biased_step(bias[e], tokens_times_k, E, v, gamma);
 }
 
 // out[t] = residual[t] + shared[t] + sum_j gate[t][j] * y[inv_pos[t][j]]; one thread per

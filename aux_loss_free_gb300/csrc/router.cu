@@ -16,6 +16,7 @@
 #include <math.h>
 
 #include "internal.h"
+#include "select.cuh"
 
 namespace moe {
 namespace {
@@ -26,92 +27,8 @@ constexpr int EB = 64;             // experts per pass
 constexpr int NTHR = 128;
 constexpr int XS_LD = RT + 4;
 constexpr int WS_LD = EB + 4;
-constexpr int MAXC = kMaxE / 32;   // experts per lane in the selection phase
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
-
-// Selection for one token by one warp, from its E logits (offset included): scores,
-// the biased top-k (k rounds of a warp-shuffle arg-max under key descending, expert
-// index ascending), gates, and the pair counts (into the block histogram `hist`, or
-// straight into the global load and chunk table when `hist` is null).
-__device__ __forceinline__ void select_token(const RouterArgs& a, const float* lg, int t, int lane,
-                                             int* hist) {
-  const unsigned FULL = 0xFFFFFFFFu;
-  constexpr int NONE = 0x7FFFFFFF;
-  const int E = a.E;
-  float sc[MAXC], key[MAXC];
-#pragma unroll
-  for (int i = 0; i < MAXC; ++i) {
-    const int e = lane + 32 * i;
-    sc[i] = 0.f;
-    key[i] = -INFINITY;
-    if (e < E) {
-      const float z = lg[e];
-      const float s = 1.0f / (1.0f + expf(-z));
-      sc[i] = s;
-      key[i] = __fadd_rn(s, a.bias[e]);  // selection key: one fp32 addition
-      if (a.scores) a.scores[(size_t)t * E + e] = s;
-    }
-  }
-  unsigned taken = 0;
-  float sel_s[kMaxK];
-  int sel_e[kMaxK];
-#pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
-    sel_s[j] = 0.f;
-    sel_e[j] = 0;
-    if (j < a.k) {
-      float bk = -INFINITY;
-      int be = NONE;
-#pragma unroll
-      for (int i = 0; i < MAXC; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && (be == NONE || key[i] > bk)) {
-          bk = key[i];
-          be = e;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ok = __shfl_xor_sync(FULL, bk, off);
-        const int oe = __shfl_xor_sync(FULL, be, off);
-        if (oe != NONE && (be == NONE || ok > bk || (ok == bk && oe < be))) {
-          bk = ok;
-          be = oe;
-        }
-      }
-      float sw = 0.f;
-      if ((be & 31) == lane) {
-        taken |= 1u << (be >> 5);
-#pragma unroll
-        for (int i = 0; i < MAXC; ++i)
-          if (i == (be >> 5)) sw = sc[i];
-      }
-      sel_s[j] = __shfl_sync(FULL, sw, be & 31);
-      sel_e[j] = be;
-    }
-  }
-  float denom = 0.f;
-#pragma unroll
-  for (int j = 0; j < kMaxK; ++j)
-    if (j < a.k) denom += sel_s[j];
-#pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
-    if (j < a.k && lane == j) {
-      a.idx[(size_t)t * a.k + j] = sel_e[j];
-      a.gate[(size_t)t * a.k + j] = a.renorm ? __fdiv_rn(sel_s[j], denom) : sel_s[j];
-      if (!hist) {
-        if (a.load) atomicAdd(&a.load[sel_e[j]], 1);
-        if (a.counts) atomicAdd(&a.counts[(size_t)(t / a.chunk_tokens) * E + sel_e[j]], 1);
-      }
-    }
-  }
-  if (hist && lane == 0) {
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j)
-      if (j < a.k) atomicAdd(&hist[sel_e[j]], 1);
-  }
-}
 
 template <bool XF32>
 __global__ void __launch_bounds__(NTHR) router_kernel(RouterArgs a) {
