@@ -222,21 +222,6 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) int4_down_kernel(
   }
 }
 
-// 32 bf16 inputs of one group -> floats.
-__device__ __forceinline__ void load_group_xf(const uint16_t* p, float (&x)[32]) {
-  const uint4* v = reinterpret_cast<const uint4*>(p);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 u = v[i];
-    const uint32_t ws[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      x[8 * i + 2 * j] = __uint_as_float(ws[j] << 16);
-      x[8 * i + 2 * j + 1] = __uint_as_float(ws[j] & 0xFFFF0000u);
-    }
-  }
-}
-
 // Serving with few (token, expert) pairs: the same products straight from the routing
 // result, with no permutation.  Pairs p (= t * k + j) keep their order; a warp's unit
 // is (pair, DIR_RPU row slots) and only the first pair routed to an expert does the
@@ -304,24 +289,18 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 2) int4_direct_kernel(
 #pragma unroll
           for (int m = 0; m < DIR_TOK; ++m) acc[mm][m] = 0.f;
         for (int g = gl; g < ngroups; g += lpr) {
-          float xf[DIR_TOK][32];
-#pragma unroll
-          for (int m = 0; m < DIR_TOK; ++m)
-            if (m < cnt)  // gate/up reads token pp / k of x; down reads pair pp of h
-              load_group_xf(src + (long long)(GATE_UP ? pp[m] / k : pp[m]) * K + g * 32, xf[m]);
 #pragma unroll
           for (int mm = 0; mm < NM; ++mm) {
             float q[32];
             int4_codes(wq + wrow[mm] * (K / 2) + g * 16, q);
             const float sc = scale_of(ws, wrow[mm] * ngroups + g);
+            // Each pair's inputs are read inside its product (gate/up: token pp / k of
+            // x; down: pair pp of h), so only the decoded codes stay live.
 #pragma unroll
             for (int m = 0; m < DIR_TOK; ++m)
-              if (m < cnt) {
-                float part = 0.f;
-#pragma unroll
-                for (int t = 0; t < 32; ++t) part = fmaf(q[t], xf[m][t], part);
-                acc[mm][m] = fmaf(sc, part, acc[mm][m]);
-              }
+              if (m < cnt)
+                acc[mm][m] = fmaf(sc, dot32(q, src + (long long)(GATE_UP ? pp[m] / k : pp[m]) * K + g * 32),
+                                  acc[mm][m]);
           }
         }
 #pragma unroll
