@@ -36,9 +36,12 @@ fl32(b + gamma*sign), whose fp32 rounding is part of the definition, and the int
 quantiser, whose code decisions are taken in fp32 as the GPU takes them.
 
 Parity pins: every function here is checked in tests/test_oracle_pins.py against
-brute force, closed forms, special cases and library routines.  The layer output
-values themselves have no worked example on the pages: beyond those structural
-pins they are "parity unpinned".
+something other than itself: brute force (top-k over all subsets), closed forms
+(structured SwiGLU weights, sigmoid through a one-hot router, exact rational bias
+rounding), library routines (PyTorch SwiGLU, sigmoid and autograd, stable sort,
+bincount), hand-worked fixtures (tests/golden/) and, for the whole layer, an
+independent per-token dense mixture with no permutation.  The pages print no worked
+example of the layer's values, so no pin is a printed number.
 """
 from __future__ import annotations
 
