@@ -125,6 +125,7 @@ def parse_args():
     p.add_argument("--workload", choices=sorted(WORKLOADS) + ["attn"], default="nano")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-sample-worker", default=None, help=argparse.SUPPRESS)
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle baseline sample")
     return p.parse_args()
@@ -342,6 +343,37 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def timed_oracle_sample(name, seed, seconds):
+    """(tokens done, seconds spent, tokens per call) of the oracle on the workload."""
+    run = oracle_sample_runner(name, seed)
+    s = workload_shape(name)
+    ntok = min(s.T, 128 if name == "train" else 1024)
+    run(min(ntok, 64))  # warm the BLAS threads
+    done, spent = 0, 0.0
+    while spent < seconds and done < 64 * s.T:
+        spent += run(ntok)
+        done += ntok
+    return done, spent, ntok
+
+
+def one_thread_baseline(name, seed, seconds):
+    """The same oracle sample on one host thread: a child process (a fresh interpreter,
+    nothing forked from a process that holds a CUDA context) with every BLAS thread
+    pool set to one thread before numpy loads."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", VECLIB_MAXIMUM_THREADS="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-sample-worker", name, "--seed", str(seed),
+           "--cpu-seconds", str(seconds)]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=seconds * 6 + 120)
+        done, spent, ntok = json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as exc:  # the main measurement stands without it
+        return {"error": f"one-thread sample failed: {exc!r}"[:200]}
+    s = workload_shape(name)
+    return {"value": done / spent * (1.0 / max(1, s.layers)), "unit": "tokens/s", "cores": 1,
+            "sample": f"{done} tokens in calls of {ntok}, BLAS on one thread, {spent:.1f} s"}
+
+
 def cpu_baseline(name, seed, seconds):
     run = oracle_sample_runner(name, seed)
     s = workload_shape(name)
@@ -356,7 +388,8 @@ def cpu_baseline(name, seed, seconds):
             "sample": f"{done} tokens as {done // ntok} oracle layer "
                       f"{'forward+backward passes' if name == 'train' else 'forwards'} of {ntok} tokens of the "
                       f"{name} workload (fp64 numpy, BLAS on all {cpu_cores()} visible cores), "
-                      f"{spent:.1f} s" + (f"; per stack forward of {s.layers} layers" if s.layers > 1 else "")}
+                      f"{spent:.1f} s" + (f"; per stack forward of {s.layers} layers" if s.layers > 1 else ""),
+            "one_thread": one_thread_baseline(name, seed, max(2.0, min(8.0, seconds / 2)))}
 
 
 def reference_arm(args, rank, world):
@@ -1084,6 +1117,11 @@ def attn_reference_arm(args, rank, world):
 
 def main():
     args = parse_args()
+    if args.cpu_sample_worker:
+        # Child of one_thread_baseline: the oracle sample only, printed as JSON.
+        print(json.dumps(list(timed_oracle_sample(args.cpu_sample_worker, args.seed, args.cpu_seconds))),
+              flush=True)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.gpus != world and world == 1 and args.gpus > 1:
