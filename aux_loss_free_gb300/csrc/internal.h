@@ -235,6 +235,12 @@ struct ServeArgs {
   uint16_t* h;    // [T*k][f]
   int update_bias;
   float gamma;
+  // Expert cache (or null): the routed weights in w are its slots'; the launch plans
+  // the step and copies the missing experts from cache_src first.
+  const struct CacheView* cache_view;
+  const struct CacheSegments* cache_src;
+  int cache_slots;
+  long long cache_expert_bytes;
 };
 bool serve_fused_supported(const moe_shape_t* s, const void* x, const float* w_router, const moe_weights_t* w);
 size_t serve_fused_scratch_bytes(const moe_shape_t* s);

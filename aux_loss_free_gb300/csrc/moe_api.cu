@@ -621,9 +621,9 @@ moe_status_t layer_fwd_impl(const moe_shape_t* shape, const void* x, const float
   const int chunks = layer_chunks_of(shape, &ct);
   const int xf = shape->x_dtype == MOE_X_F32;
   // Top-1 serving of at most kServeMaxPairs pairs: one persistent launch does the whole
-  // layer (not with an expert cache, whose fill runs between routing and experts, nor
-  // when the caller asks for the permutation).
-  if (int4 && !cache && L.serve && !(dbg && (dbg->offsets || dbg->perm_tok || dbg->inv_pos)) &&
+  // layer, the expert cache's plan and fill included (not when the caller asks for the
+  // permutation).
+  if (int4 && L.serve && !(dbg && (dbg->offsets || dbg->perm_tok || dbg->inv_pos)) &&
       serve_fused_supported(shape, x, w_router, w)) {
     ServeArgs a{};
     a.x = x;
@@ -643,6 +643,12 @@ moe_status_t layer_fwd_impl(const moe_shape_t* shape, const void* x, const float
     a.h = L.ffn.h;
     a.update_bias = update_bias;
     a.gamma = gamma;
+    if (cache) {
+      a.cache_view = &cache->view;
+      a.cache_src = &cache->host_src;
+      a.cache_slots = cache->slots;
+      a.cache_expert_bytes = cache->expert_bytes;
+    }
     const bool prof = prof_begin_call();
     if (prof) prof_mark("serve_fused", s);
     const cudaError_t e = launch_serve_fused(shape, a, s);

@@ -40,6 +40,7 @@
 #include <algorithm>
 #include <atomic>
 
+#include "cache_plan.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "select.cuh"
@@ -74,7 +75,18 @@ struct ServeParams {
   float* logits;              // scratch [T][E]
   uint16_t* hs;               // scratch [T][F]
   uint16_t* h;                // scratch [T*k][f]
-  int* sync;                  // [4]: router count, done count, the 64-bit id of the call that zeroed them
+  int* sync;                  // [8]: router count, done count, the 64-bit id of the call that zeroed
+                              // them, the cache's plan flag and fill count
+  // Expert cache (cached != 0): the routed weights above are the slots' arrays, read
+  // through expert_slot once this launch has planned the step and copied its misses.
+  int cached, slots;
+  CacheState* cstate;
+  int32_t* slot_expert;
+  int32_t* cstamp;
+  int32_t* expert_slot;
+  int2* jobs;
+  CacheSegments host_src, slots_w;
+  long long expert_bytes;
   unsigned long long call_id; // unique per call
   int* status;
   int T, d, E, f, F, k, renorm, update_bias, bf, bF;
@@ -221,8 +233,10 @@ __global__ void __launch_bounds__(SV_THREADS, 1) serve_kernel(const __grid_const
   // Copies: the CTA's W_r rows or shared gate/up rows (a), its shared down rows (d), the
   // tokens (x), its rows of the routed experts' down projections (r).
   __shared__ __align__(8) uint64_t bar_a, bar_d, bar_x, bar_r, bar_g;
-  __shared__ int s_ok, s_nu, s_rarmed, s_garmed;
+  __shared__ int s_ok, s_nu, s_rarmed, s_garmed, s_allhit;
   __shared__ int s_idx[SV_MAXT], s_ue[SV_MAXT], s_pu[SV_MAXT];  // selection; distinct experts; pair -> distinct
+  __shared__ int s_we[SV_MAXT];  // where each distinct expert's weights are: the expert, or its cache slot
+  __shared__ CachePlanScratch plan_sc;
   __shared__ float s_gate[SV_MAXT];
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int c = blockIdx.x, G = gridDim.x;
@@ -240,6 +254,9 @@ __global__ void __launch_bounds__(SV_THREADS, 1) serve_kernel(const __grid_const
   int* const cnt_router = p.sync;
   int* const cnt_done = p.sync + 1;
   unsigned long long* const ready = reinterpret_cast<unsigned long long*>(p.sync + 2);
+  int* const planned = p.sync + 4;
+  int* const cnt_filled = p.sync + 5;
+  int* const plan_njobs = p.sync + 6;
   const uint32_t rd_codes = (uint32_t)(i1 - i0) * (f / 2), rd_bytes = rd_codes + (uint32_t)(i1 - i0) * (f / 16);
   const uint32_t item_bytes = (uint32_t)d + (uint32_t)d / 8;  // gate and up codes (d / 2 each), scales (d / 16 each)
 
@@ -282,6 +299,8 @@ __global__ void __launch_bounds__(SV_THREADS, 1) serve_kernel(const __grid_const
     // The call's counters start at zero; `ready` = this call's id publishes that.
     *cnt_router = 0;
     *cnt_done = 0;
+    *planned = 0;
+    *cnt_filled = 0;
     __threadfence();
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(ready), "l"(p.call_id) : "memory");
   }
@@ -419,21 +438,105 @@ __global__ void __launch_bounds__(SV_THREADS, 1) serve_kernel(const __grid_const
         s_pu[q] = u;
       }
       s_nu = nu;
-      // This CTA's rows of those experts' down projections, for step 5 (copies issued by
-      // the first warp below).
-      mbar_arrive_expect_tx(smem_u32(&bar_r), i1 > i0 ? (uint32_t)nu * rd_bytes : 0u);
+      for (int u = 0; u < nu; ++u) s_we[u] = s_ue[u];
+    }
+    __syncthreads();
+    if (c == 0) {
+      for (int q = tid; q < P; q += SV_THREADS) {
+        p.idx[q] = s_idx[q];
+        p.gate[q] = s_gate[q];
+      }
+      for (int e = tid; e < E; e += SV_THREADS)
+        if (p.load) p.load[e] = hist[e];
+      if (p.balance && warp == SV_WARPS - 1) warp_balance(hist, E, p.balance, lane);
+    }
+    __syncthreads();
+  }
+
+  // ---------------------------------------------------------------- 3b. expert cache
+  // Every CTA reads where the step's experts are in the tables as the call found them:
+  // CTA 0 writes the step's new tables back only after the last grid barrier, so all
+  // CTAs see the same table and take the same branch.  A hit's slot cannot change in its
+  // own step.  When every expert of the step is resident nothing waits for the plan;
+  // otherwise CTA 0 publishes the plan's copies, every CTA copies its share of the
+  // missing experts from host memory into their slots, and a counted barrier ends the
+  // phase.
+  if (p.cached && ok) {
+    if (tid == 0) {
+      int all = 1;
+      for (int u = 0; u < s_nu; ++u) {
+        s_we[u] = __ldcg(p.expert_slot + s_ue[u]);
+        if (s_we[u] < 0 || s_we[u] >= p.slots) all = 0;
+      }
+      s_allhit = all;
+    }
+    __syncthreads();
+    const bool all_hit = s_allhit != 0;
+    if (c == 0) {
+      if (warp == 0)
+        cache_plan_warp(s_idx, P, E, p.slots, p.cstate, p.slot_expert, p.cstamp, p.expert_slot, p.jobs,
+                        p.expert_bytes, p.status, plan_sc, lane, [] {});
+      if (!all_hit) {
+        __syncthreads();
+        if (tid == 0) {
+          *plan_njobs = plan_sc.next.njobs;
+          __threadfence();
+          asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(planned), "r"(1) : "memory");
+        }
+      }
+    }
+    if (!all_hit) {
+      if (tid == 0) s_ok = spin_geq(planned, 1, p.status) ? 1 : 0;
+      __syncthreads();
+      ok = s_ok;
+      if (ok) {
+        const int njobs = __ldcg(plan_njobs);
+        cache_copy_range(njobs, p.jobs, p.host_src, p.slots_w, (long long)c * SV_THREADS + tid,
+                         (long long)G * SV_THREADS);
+        // The copies are read next by bulk copies (the async proxy) of other CTAs.
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) {
+          atomicAdd(cnt_filled, 1);
+          s_ok = spin_geq(cnt_filled, G, p.status) ? 1 : 0;
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          // The missing experts' slots, from the plan's copies.
+          for (int u = 0; u < s_nu; ++u) {
+            if (s_we[u] >= 0 && s_we[u] < p.slots) continue;
+            s_we[u] = -1;
+            for (int jb = 0; jb < njobs; ++jb) {
+              const int2 job = p.jobs[jb];
+              if (job.x == s_ue[u]) s_we[u] = job.y;
+            }
+            if (s_we[u] < 0 || s_we[u] >= p.slots) {  // not served (the plan ran out of slots)
+              atomicOr(p.status, kDevCheck);
+              s_ok = 0;
+            }
+          }
+        }
+        __syncthreads();
+        ok = s_ok;
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- prefetch of the
+  // routed weights this CTA needs: its routed gate/up items (into the now idle weight
+  // slice region) and its output rows of the experts' down projections
+  if (ok) {
+    if (tid == 0) {
+      mbar_arrive_expect_tx(smem_u32(&bar_r), i1 > i0 ? (uint32_t)s_nu * rd_bytes : 0u);
       s_rarmed = 1;
-      // This CTA's routed gate/up items, all fetched at once into the (now idle) weight
-      // slice region: per item its gate row and up row (codes, then scales).
-      const long long items = (long long)nu * f;
+      const long long items = (long long)s_nu * f;
       const int mine = items > c ? (int)((items - c + G - 1) / G) : 0;
       mbar_arrive_expect_tx(smem_u32(&bar_g), (uint32_t)mine * (uint32_t)item_bytes);
       s_garmed = 1;
     }
+    // The region was last read by generic loads; the copies write it through the async proxy.
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
     {
-      // The region was last read by generic loads; the copies write it through the async proxy.
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       // Item m of this CTA is global item c + G m; thread i issues copy i % 4 of item i / 4.
       const long long items = (long long)s_nu * f;
       const int mine = items > c ? (int)((items - c + G - 1) / G) : 0;
@@ -441,7 +544,7 @@ __global__ void __launch_bounds__(SV_THREADS, 1) serve_kernel(const __grid_const
         const int m = i >> 2, part = i & 3;
         const long long it = c + (long long)G * m;
         const int u = (int)(it / f), j = (int)(it % f);
-        const long long rg = (long long)s_ue[u] * 2 * f + (j / p.bf) * 2 * p.bf + j % p.bf;
+        const long long rg = (long long)s_we[u] * 2 * f + (j / p.bf) * 2 * p.bf + j % p.bf;
         const long long row = (part & 1) ? rg + p.bf : rg;  // gate, up
         // Codes of gate, up at 0, d / 2; scales of gate, up at d, d + d / 16.
         const uint32_t off = (part & 2) ? (uint32_t)d + (part & 1) * (uint32_t)(d / 16) : (part & 1) * (uint32_t)(d / 2);
@@ -454,23 +557,13 @@ __global__ void __launch_bounds__(SV_THREADS, 1) serve_kernel(const __grid_const
     }
     if (warp == 0 && i1 > i0 && lane < 2 * s_nu) {
       const int u = lane >> 1;
-      const long long row = (long long)s_ue[u] * d + i0;
+      const long long row = (long long)s_we[u] * d + i0;
       const uint32_t dst = smem_u32(sm + p.o_rd) + (uint32_t)u * rd_bytes;
       if (lane & 1)
         bulk_load(dst + rd_codes, p.dn_s + row * (f / 32), rd_bytes - rd_codes, smem_u32(&bar_r));
       else
         bulk_load(dst, p.dn_q + row * (f / 2), rd_codes, smem_u32(&bar_r));
     }
-    if (c == 0) {
-      for (int q = tid; q < P; q += SV_THREADS) {
-        p.idx[q] = s_idx[q];
-        p.gate[q] = s_gate[q];
-      }
-      for (int e = tid; e < E; e += SV_THREADS)
-        if (p.load) p.load[e] = hist[e];
-      if (p.balance && warp == SV_WARPS - 1) warp_balance(hist, E, p.balance, lane);
-    }
-    __syncthreads();
   }
 
   // ---------------------------------------------------------------- 4. routed gate/up
@@ -523,6 +616,9 @@ __global__ void __launch_bounds__(SV_THREADS, 1) serve_kernel(const __grid_const
   }
   __syncthreads();
   ok = s_ok;
+  // Every CTA has read the cache's tables for this step: the plan's tables can go in.
+  if (ok && c == 0 && p.cached && warp == 0)
+    cache_plan_write_back(plan_sc, E, p.slots, p.cstate, p.slot_expert, p.cstamp, p.expert_slot, lane);
   // Every CTA has read the bias for its selection: the update can go in.
   if (ok && c == 0 && p.update_bias)
     for (int e = tid; e < E; e += SV_THREADS) p.bias[e] = biased_step(bs[e], (long long)T * k, E, hist[e], p.gamma);
@@ -678,8 +774,8 @@ bool serve_fused_supported(const moe_shape_t* s, const void* x, const float* w_r
 }
 
 size_t serve_fused_scratch_bytes(const moe_shape_t* s) {
-  // logits [T][E] fp32, then the four sync words.
-  return align16((size_t)s->T * s->E * 4) + 16;
+  // logits [T][E] fp32, then the eight sync words.
+  return align16((size_t)s->T * s->E * 4) + 32;
 }
 
 cudaError_t launch_serve_fused(const moe_shape_t* s, const ServeArgs& a, cudaStream_t st) {
@@ -707,6 +803,18 @@ cudaError_t launch_serve_fused(const moe_shape_t* s, const ServeArgs& a, cudaStr
   p.sync = reinterpret_cast<int*>(static_cast<uint8_t*>(a.scratch) + align16((size_t)s->T * s->E * 4));
   p.hs = a.hs;
   p.h = a.h;
+  if (a.cache_view) {
+    p.cached = 1;
+    p.slots = a.cache_slots;
+    p.cstate = a.cache_view->state;
+    p.slot_expert = a.cache_view->slot_expert;
+    p.cstamp = a.cache_view->stamp;
+    p.expert_slot = a.cache_view->expert_slot;
+    p.jobs = a.cache_view->jobs;
+    p.slots_w = a.cache_view->slots_w;
+    p.host_src = *a.cache_src;
+    p.expert_bytes = a.cache_expert_bytes;
+  }
   p.status = device_status_ptr();
   if (!p.status) return cudaErrorInvalidDevicePointer;
   p.T = s->T;

@@ -53,11 +53,29 @@ TRAIN_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_wgrad_gate_up_train_tr
 PROFILE_PERIOD = 10
 
 
+def serve_step_roofline(fill_bytes, hbm_bytes, ms_step, link_gbs, peaks, peak_note):
+    """The single-launch serving step (plan, fill and experts in one kernel): whichever
+    of the host link (the step's fill bytes) and HBM (its weight bytes) bounds it."""
+    link_s = fill_bytes / (link_gbs * 1e9) if link_gbs else 0.0
+    hbm_s = hbm_bytes / (peaks["hbm_gbs"] * 1e9)
+    if link_s > hbm_s:
+        ach = fill_bytes / (ms_step / 1e3) / 1e9
+        return {"kernel": "single-launch serving step (plan, fill from host memory, experts)", "bound": "link",
+                "achieved": ach, "peak": link_gbs, "unit": "GB/s", "frac": ach / link_gbs, "traffic": None,
+                "peak_note": "of a pinned host-to-device copy measured in this run"}
+    ach = hbm_bytes / (ms_step / 1e3) / 1e9
+    return {"kernel": "single-launch serving step (plan, fill from host memory, experts)", "bound": "hbm",
+            "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
+            "traffic": None, "peak_note": peak_note}
+
+
 def kernels_per_call(s):
     """Kernels one moe_layer_fwd launches (the library's own, no memsets or copies)."""
     tc_router = s.x_dtype == "bf16" and s.T >= 128 and s.E in (16, 32, 48, 64, 80)
     router = 2 if tc_router else 1                     # weight split + router, or SIMT router
     if s.w_format == "int4":
+        if s.T * s.k <= 8 and s.x_dtype == "bf16" and s.d % 256 == 0 and s.f % 256 == 0:
+            return 1  # the single-launch serving kernel (with the expert cache's plan and fill)
         if s.T * s.k <= 64:
             # no permutation: shared gate/up (second stream), int4 gate/up, int4 down,
             # shared down + combine (or the combine kernel without a shared expert)
@@ -897,6 +915,7 @@ def gpu_cache_arm(args, rank, world, dist):
     ms_step = total_ms / K
     fetch_ms = stages_ms.get("cache_fetch", float("nan")) / max(1, stage_calls.get("cache_fetch", 1))
     fill_gbs = (fill_bytes / K) / (fetch_ms / 1e3) / 1e9 if fetch_ms == fetch_ms and fetch_ms > 0 else None
+    fused = "serve_fused" in stages_ms  # the plan and the fill run inside the one serving launch
     # Weight bytes a step must read: the distinct experts it uses (from HBM slots) and
     # the shared expert, as in the serving workloads' HBM roofline.
     used_per_step = (hits + misses) / K
@@ -914,10 +933,11 @@ def gpu_cache_arm(args, rank, world, dist):
                   "expert_bytes": expert_bytes, "fetch_us_per_step": fetch_ms * 1e3,
                   "resident_us_per_step": res_ms / K * 1e3,
                   "overflow": st1["overflow"] - st0["overflow"]},
-        "roofline": {"kernel": "cache fill (plan + copy kernels, host memory -> HBM slots)", "bound": "link",
-                     "achieved": fill_gbs, "peak": link_gbs, "unit": "GB/s",
-                     "frac": (fill_gbs / link_gbs) if fill_gbs else None, "traffic": None,
-                     "peak_note": "of a pinned host-to-device copy measured in this run"},
+        "roofline": ({"kernel": "cache fill (plan + copy kernels, host memory -> HBM slots)", "bound": "link",
+                      "achieved": fill_gbs, "peak": link_gbs, "unit": "GB/s",
+                      "frac": (fill_gbs / link_gbs) if fill_gbs else None, "traffic": None,
+                      "peak_note": "of a pinned host-to-device copy measured in this run"} if not fused else
+                     serve_step_roofline(fill_bytes / K, nbytes, ms_step, link_gbs, peaks, peak_note)),
         "layer_roofline": {"bytes_per_step": nbytes, "roofline_us": nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6,
                            "measured_us": ms_step * 1e3,
                            "frac": nbytes / (peaks["hbm_gbs"] * 1e9) / (ms_step / 1e3), "peak": peak_note,
