@@ -320,7 +320,9 @@ moe_status_t moe_layer_bwd(const moe_shape_t* shape, const void* x, const float*
  * memory the GPU can read (pinned or managed), HBM holds `slots` of them, and
  * moe_layer_fwd_cached brings each step's experts in on the GPU with no host round
  * trip: after the routing one block plans the step and a grid copies the missing
- * experts over the CPU-GPU link into their slots.  Policy (this library's reading of
+ * experts over the CPU-GPU link into their slots (with at most 8 tokens, inside the
+ * single serving launch of moe_layer_fwd, where a step whose experts are all resident
+ * waits for no copy).  Policy (this library's reading of
  * LRU): the experts a step uses are the distinct entries of its routing result,
  * ascending; the resident ones are hits and their slots are stamped with the step
  * number first; then each missing expert, in ascending order, takes the slot with the
