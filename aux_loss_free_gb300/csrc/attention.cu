@@ -362,22 +362,24 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) gqa_attention_kernel(const __g
       }
       // Exponentials (one FFMA and one ex2 each; masked keys give 2^-inf = 0), the row
       // sum and P (bf16 pairs, keys 2c and 2c + 1 in column c of the row's P buffer).
-      const float nm = -m;
+      const float2 nm2 = make_float2(-m, -m), sc2 = make_float2(p.scale_log2, p.scale_log2);
       const uint32_t pcol = tl + P_COL + (j & 1) * (BKV / 2);
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int c = 0; c < BKV / 64; ++c) {
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 64; i += 2) {
-          const float e0 = ex2(fmaf(__uint_as_float(v[64 * c + i]), p.scale_log2, nm));
-          const float e1 = ex2(fmaf(__uint_as_float(v[64 * c + i + 1]), p.scale_log2, nm));
-          ls[(i >> 1) & 3] += e0 + e1;
-          pk[i / 2] = pack_bf16x2(e0, e1);
+          // Two scores per packed fp32x2 FMA; the exponentials one by one.
+          const float2 a = __ffma2_rn(make_float2(__uint_as_float(v[64 * c + i]), __uint_as_float(v[64 * c + i + 1])),
+                                      sc2, nm2);
+          const float2 e = make_float2(ex2(a.x), ex2(a.y));
+          ls[(i >> 1) & 1] = __fadd2_rn(ls[(i >> 1) & 1], e);
+          pk[i / 2] = pack_bf16x2(e.x, e.y);
         }
         tmem_st32(pcol + 32 * c, pk);
       }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      l += (ls[0].x + ls[0].y) + (ls[1].x + ls[1].y);
       tmem_wait_st();  // P is in TMEM before the MMA may read it
       tc_fence_before();
       __syncwarp();
