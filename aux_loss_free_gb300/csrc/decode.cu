@@ -8,7 +8,11 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
+#include <atomic>
+
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -316,6 +320,237 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 2) int4_direct_kernel(
   }
 }
 
+// The same permutation-free products on the tensor cores (mma.sync m16n8k16: bf16
+// inputs, fp32 sums): weights in M, the expert's pairs in N (8 per pass).  A unit is
+// (expert, row tile); the experts are the distinct ones of the routing result, in the
+// order of their first pair.  The CTA's 8 warps share a unit: gate/up, 16 gate rows and
+// the 16 matching up rows with K split 8 ways; down, two 16-row tiles with K split 4
+// ways.  Each CTA walks its units through a ring of TCD_STAGES shared-memory stages
+// filled by cp.async (a unit's code rows and scale rows, each row padded by 16 bytes so
+// the fragment reads below fall in distinct banks), so the next units' weights stream
+// in while one is multiplied.  Per 32-input group a lane reads one 32-bit word of 8
+// codes (word l%4) of each of its rows l/4 and l/4 + 8 and forms bf16 pairs of nibbles
+// (i, i + 4) (`q_pair`).  The sum over k may run in any order as long as both operands
+// follow it, so the lane's B fragment holds the inputs at those same positions: its 8
+// consecutive bf16 of the pair's row, re-paired (`input_pairs`).  A group's two 16-deep
+// steps accumulate from zero and its fp16 scale multiplies that partial once (every
+// product q * x exact, as in the CUDA-core path); the warps' partials are summed in a
+// fixed order through shared memory.
+constexpr int TCD_WARPS = 8;
+constexpr int TCD_STAGES = 4;
+
+template <bool GATE_UP>
+struct TcdShape {
+  static constexpr int NM = GATE_UP ? 2 : 1;  // row sets: gate and up, or the down rows
+  static constexpr int RT = GATE_UP ? 1 : 2;  // 16-row tiles per unit
+  static constexpr int KS = TCD_WARPS / RT;   // K parts per tile, one warp each
+  static constexpr int ROWS = 16 * RT * NM;   // weight rows per unit
+};
+
+// Nibbles i and i + 4 of a code word as a bf16 pair of the integers q.  Each half of
+// (w >> 4i) & 0x000F000F ^ 0x43084308 is the bf16 bit pattern of 128 + (q + 8) (the
+// nibble ^ 8 is q + 8 in [0, 15], and the unit in the last place of 128 is 1), so
+// subtracting 136 leaves q, exactly.
+__device__ __forceinline__ uint32_t q_pair(uint32_t w, int i) {
+  const uint32_t v = ((w >> (4 * i)) & 0x000F000Fu) ^ 0x43084308u;
+  uint32_t r;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(0x43084308u));
+  return r;
+}
+
+// 8 consecutive bf16 inputs x0..x7 as the pairs (x0, x4), (x1, x5), (x2, x6), (x3, x7).
+__device__ __forceinline__ void input_pairs(const uint4& u, uint32_t (&b)[4]) {
+  b[0] = __byte_perm(u.x, u.z, 0x5410);
+  b[1] = __byte_perm(u.x, u.z, 0x7632);
+  b[2] = __byte_perm(u.y, u.w, 0x5410);
+  b[3] = __byte_perm(u.y, u.w, 0x7632);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+template <bool GATE_UP>
+__global__ void __launch_bounds__(TCD_WARPS * 32, GATE_UP ? 2 : 4) int4_tc_direct_kernel(
+    const int32_t* __restrict__ idx, int P, int k, const uint8_t* __restrict__ wq,
+    const uint16_t* __restrict__ ws, const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
+    int d, int f, int block, const int32_t* __restrict__ slot) {
+  using S = TcdShape<GATE_UP>;
+  extern __shared__ __align__(16) uint8_t tcd_smem[];
+  const int K = GATE_UP ? d : f, rows = GATE_UP ? f : d;
+  const int ngroups = K / 32, gpw = ngroups / S::KS;
+  const int cstride = K / 2 + 16, sstride = ngroups * 2 + 16;  // padded row strides (bytes)
+  const int stage_bytes = S::ROWS * (cstride + sstride);
+  float(*red)[S::NM][4][32] = reinterpret_cast<float(*)[S::NM][4][32]>(tcd_smem + TCD_STAGES * stage_bytes);
+  int(*plist)[kDirectMaxPairs] = reinterpret_cast<int(*)[kDirectMaxPairs]>(red + TCD_WARPS);
+  int* dexp = plist[TCD_WARPS];  // the distinct experts, in the order of their first pair
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int rt = warp / S::KS, kp = warp % S::KS;
+  const int tiles = rows / (16 * S::RT);
+  // The distinct experts: pairs whose expert no earlier pair has (every warp alike).
+  const bool va = lane < P, vb = lane + 32 < P;
+  const int ea = va ? idx[lane] : -1 - lane, eb = vb ? idx[lane + 32] : -1 - lane;
+  const unsigned below = (1u << lane) - 1u;
+  bool b_seen_in_a = false;
+  for (int q = 0; q < 32; ++q) b_seen_in_a |= __shfl_sync(0xFFFFFFFFu, ea, q) == eb;
+  // Every lane takes part in both matches (full-mask warp primitives; none of them may
+  // sit behind a short-circuit test that some lanes skip).
+  const unsigned same_a = __match_any_sync(0xFFFFFFFFu, ea), same_b = __match_any_sync(0xFFFFFFFFu, eb);
+  const unsigned first_lo = __ballot_sync(0xFFFFFFFFu, va && !(same_a & below));
+  const unsigned first_hi = __ballot_sync(0xFFFFFFFFu, vb && !b_seen_in_a && !(same_b & below));
+  if (warp == 0) {
+    if ((first_lo >> lane) & 1u) dexp[__popc(first_lo & below)] = ea;
+    if ((first_hi >> lane) & 1u) dexp[__popc(first_lo) + __popc(first_hi & below)] = eb;
+  }
+  __syncthreads();
+  const int nunits = (__popc(first_lo) + __popc(first_hi)) * tiles;
+  const int mine = (int)blockIdx.x < nunits ? (nunits - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const uint32_t smem0 = smem_u32(tcd_smem);
+  auto expert_of = [&](int unit) { return dexp[unit / tiles]; };
+  // Global row (in the code and scale tensors) of row r of a unit.
+  auto weight_row = [&](long long we, int tile, int r) -> long long {
+    if (GATE_UP) {
+      const int j = tile * 16 + (r & 15);
+      return we * 2 * f + (j / block) * 2 * block + j % block + (r >= 16 ? block : 0);
+    }
+    return we * d + tile * 32 + r;
+  };
+  // All threads: copy unit `unit`'s code and scale rows into stage `st`, 8 threads per
+  // row (each row's address computed once), 16-byte chunks.
+  static_assert(S::ROWS * 8 == TCD_WARPS * 32, "8 copying threads per row");
+  const int crow_r = tid >> 3, csub = tid & 7;
+  auto issue = [&](int unit, int st) {
+    const int e = expert_of(unit), tile = unit % tiles;
+    const long long row = weight_row(slot ? slot[e] : e, tile, crow_r);
+    const uint8_t* cs = wq + row * (K / 2) + csub * 16;
+    uint32_t cd = smem0 + st * stage_bytes + crow_r * cstride + csub * 16;
+    for (int q = csub; q < K / 32; q += 8, cs += 128, cd += 128) cp_async16(cd, cs);
+    const uint8_t* ss = reinterpret_cast<const uint8_t*>(ws) + row * (K / 16) + csub * 16;
+    uint32_t sd = smem0 + st * stage_bytes + S::ROWS * cstride + crow_r * sstride + csub * 16;
+    for (int q = csub; q < K / 256; q += 8, ss += 128, sd += 128) cp_async16(sd, ss);
+  };
+#pragma unroll 1
+  for (int i = 0; i < TCD_STAGES - 1; ++i) {
+    if (i < mine) issue((int)blockIdx.x + i * (int)gridDim.x, i);
+    cp_async_commit();
+  }
+  int* pl = plist[warp];
+#pragma unroll 1
+  for (int i = 0; i < mine; ++i) {
+    const int unit = (int)blockIdx.x + i * (int)gridDim.x;
+    if (i + TCD_STAGES - 1 < mine) issue(unit + (TCD_STAGES - 1) * (int)gridDim.x, (i + TCD_STAGES - 1) % TCD_STAGES);
+    cp_async_commit();
+    const int e = expert_of(unit), tile = unit % tiles;
+    const unsigned ma = __ballot_sync(0xFFFFFFFFu, ea == e), mb = __ballot_sync(0xFFFFFFFFu, eb == e);
+    const int cnt = __popc(ma) + __popc(mb);
+    // The expert's pairs in order (each warp keeps its own copy).
+    if ((ma >> lane) & 1u) pl[__popc(ma & below)] = lane;
+    if ((mb >> lane) & 1u) pl[__popc(ma) + __popc(mb & below)] = lane + 32;
+    __syncwarp();
+    const uint8_t* stage = tcd_smem + (i % TCD_STAGES) * stage_bytes;
+    const int g0 = kp * gpw;
+    // This lane's rows r0 = m*16 + rt*16 + l/4 and r0 + 8 of each set, at group g0.
+    const uint8_t* cp0 = stage + (rt * 16 + g) * cstride + g0 * 16 + 4 * t;
+    const uint8_t* sp0 = stage + S::ROWS * cstride + (rt * 16 + g) * sstride + g0 * 2;
+    bool waited = false;
+#pragma unroll 1
+    for (int n0 = 0; n0 < cnt; n0 += 8) {
+      const int pn = n0 + g;  // this lane's column of B
+      const bool col_ok = pn < cnt;
+      const uint16_t* xr = src + (long long)(col_ok ? (GATE_UP ? pl[pn] / k : pl[pn]) : 0) * K + g0 * 32 + 8 * t;
+      float acc[S::NM][4];
+#pragma unroll
+      for (int m = 0; m < S::NM; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
+#pragma unroll 1
+      for (int j0 = 0; j0 < gpw; j0 += 4) {
+        uint4 xv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          xv[j] = (col_ok && j0 + j < gpw) ? *reinterpret_cast<const uint4*>(xr + (j0 + j) * 32)
+                                           : make_uint4(0, 0, 0, 0);
+        if (!waited) {  // the unit's rows have landed (this thread's copies, then everyone's)
+          cp_async_wait<TCD_STAGES - 1>();
+          __syncthreads();
+          waited = true;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (j0 + j >= gpw) break;
+          const int jj = j0 + j;
+          uint32_t b[4];
+          input_pairs(xv[j], b);
+#pragma unroll
+          for (int m = 0; m < S::NM; ++m) {
+            const uint8_t* c0 = cp0 + m * 16 * cstride + jj * 16;
+            const uint8_t* s0p = sp0 + m * 16 * sstride + jj * 2;
+            const uint32_t w0 = *reinterpret_cast<const uint32_t*>(c0);
+            const uint32_t w1 = *reinterpret_cast<const uint32_t*>(c0 + 8 * cstride);
+            const float s0 = __half2float(*reinterpret_cast<const __half*>(s0p));
+            const float s1 = __half2float(*reinterpret_cast<const __half*>(s0p + 8 * sstride));
+            float part[4] = {0.f, 0.f, 0.f, 0.f};
+            mma16816(part, q_pair(w0, 0), q_pair(w1, 0), q_pair(w0, 1), q_pair(w1, 1), b[0], b[1]);
+            mma16816(part, q_pair(w0, 2), q_pair(w1, 2), q_pair(w0, 3), q_pair(w1, 3), b[2], b[3]);
+            acc[m][0] = fmaf(s0, part[0], acc[m][0]);
+            acc[m][1] = fmaf(s0, part[1], acc[m][1]);
+            acc[m][2] = fmaf(s1, part[2], acc[m][2]);
+            acc[m][3] = fmaf(s1, part[3], acc[m][3]);
+          }
+        }
+      }
+      if (n0 > 0) __syncthreads();  // the previous pass's sums have been read
+#pragma unroll
+      for (int m = 0; m < S::NM; ++m)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) red[warp][m][c][lane] = acc[m][c];
+      __syncthreads();
+      // Cells (tile row r, column n) summed over the K parts in order.  Lane l/4 holds
+      // rows l/4 and l/4 + 8 (c / 2), columns 2(l%4) + c%2.
+      constexpr int CELLS = 16 * S::RT * 8;
+      for (int cell = tid; cell < CELLS; cell += TCD_WARPS * 32) {
+        const int n = cell / (16 * S::RT), rr = cell % (16 * S::RT);
+        const int tt = rr / 16, r = rr % 16;
+        const int cl = (r % 8) * 4 + n / 2, cc = (r / 8) * 2 + (n & 1);
+        float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+        for (int q = 0; q < S::KS; ++q) {
+          v0 += red[tt * S::KS + q][0][cc][cl];
+          if (GATE_UP) v1 += red[tt * S::KS + q][S::NM - 1][cc][cl];
+        }
+        if (n0 + n < cnt) {
+          const long long o = (long long)pl[n0 + n] * rows + (long long)tile * 16 * S::RT + rr;
+          dst[o] = to_bf16_bits(GATE_UP ? v0 / (1.0f + __expf(-v0)) * v1 : v0);
+        }
+      }
+    }
+    // The next copies reuse this unit's stage, the next sums this unit's `red`.
+    __syncthreads();
+  }
+  cp_async_wait<0>();
+}
+
+template <bool GATE_UP>
+size_t tcd_smem_bytes(int d, int f) {
+  using S = TcdShape<GATE_UP>;
+  const int K = GATE_UP ? d : f;
+  return (size_t)TCD_STAGES * S::ROWS * (K / 2 + 16 + K / 16 + 16) + sizeof(float) * TCD_WARPS * S::NM * 4 * 32 +
+         sizeof(int) * (TCD_WARPS + 1) * kDirectMaxPairs;
+}
+
+// Two gate/up CTAs or four down CTAs per SM.
+constexpr int kTcdMaxSmemGateUp = 110 * 1024, kTcdMaxSmemDown = 54 * 1024;
+
+bool tc_direct_supported(bool gate_up, int d, int f, const void* wq, const void* ws, const void* src) {
+  const bool aligned = ((reinterpret_cast<uintptr_t>(wq) | reinterpret_cast<uintptr_t>(ws) |
+                         reinterpret_cast<uintptr_t>(src)) & 15u) == 0;
+  return aligned && gate_up ? (d % 256 == 0 && f % 16 == 0 && tcd_smem_bytes<true>(d, f) <= (size_t)kTcdMaxSmemGateUp)
+                 : (f % 256 == 0 && d % 32 == 0 && tcd_smem_bytes<false>(d, f) <= (size_t)kTcdMaxSmemDown);
+}
+
 int decode_grid() {
   int dev = 0, sms = 1;
   cudaGetDevice(&dev);
@@ -336,6 +571,32 @@ cudaError_t launch_int4_direct(bool gate_up, const int32_t* idx, int pairs, int 
                                const uint16_t* ws, const uint16_t* src, uint16_t* dst, int d, int f,
                                int block, cudaStream_t s, const int32_t* slot) {
   if (pairs < 1 || pairs > kDirectMaxPairs) return cudaErrorInvalidValue;
+  if (tc_direct_supported(gate_up, d, f, wq, ws, src)) {
+    // At most `pairs` distinct experts; one resident wave of CTAs walks the units.
+    const long long units = (long long)pairs * (gate_up ? f / 16 : d / 32);
+    const int grid = (int)std::min<long long>(units, decode_grid() / 4 * (gate_up ? 2 : 4));
+    const size_t smem = gate_up ? tcd_smem_bytes<true>(d, f) : tcd_smem_bytes<false>(d, f);
+    // The kernels' shared-memory limits, raised once per device to the largest size
+    // the support check admits.
+    static std::atomic<bool> attr_set[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_relaxed)) {
+      e = cudaFuncSetAttribute(int4_tc_direct_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kTcdMaxSmemGateUp);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(int4_tc_direct_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kTcdMaxSmemDown);
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_relaxed);
+    }
+    if (gate_up)
+      return launch_pdl(int4_tc_direct_kernel<true>, dim3(grid), dim3(TCD_WARPS * 32), smem, s, idx, pairs, k,
+                        wq, ws, src, dst, d, f, block, slot);
+    return launch_pdl(int4_tc_direct_kernel<false>, dim3(grid), dim3(TCD_WARPS * 32), smem, s, idx, pairs, k,
+                      wq, ws, src, dst, d, f, block, slot);
+  }
   if (gate_up)
     return launch_pdl(int4_direct_kernel<true>, dim3(decode_grid()), dim3(DEC_WARPS * 32), 0, s, idx,
                       pairs, k, wq, ws, src, dst, d, f, block, slot);

@@ -176,19 +176,6 @@ __device__ __forceinline__ bool spin_eq64(const unsigned long long* w, unsigned 
   }
 }
 
-// D += A B for one 16 x 8 x 16 tile: A 16 x 16 bf16 (row-major, rows in M), B 16 x 8
-// bf16 (column-major: each of the 8 columns stored as 16 consecutive k), fp32 D.  Lane
-// l holds A rows l/4 and l/4 + 8 at k = 2(l%4) + {0, 1, 8, 9}, B column l/4 at the same
-// k, and D rows l/4, l/4 + 8 at columns 2(l%4) + {0, 1}.
-__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 __device__ __forceinline__ uint32_t ld_pair(const uint16_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
 
 // This warp's share of C[m][n] = sum_k A[m][k] B[n][k] for m < 16 * MT (rows past `rows_a`

@@ -145,7 +145,7 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample-worker", default=None, help=argparse.SUPPRESS)
     p.add_argument("--cpu-seconds", type=float, default=12.0,
-                   help="target CPU time of the oracle baseline sample")
+                   help="target CPU time of the oracle baseline sample (0: none)")
     return p.parse_args()
 
 
@@ -393,6 +393,8 @@ def one_thread_baseline(name, seed, seconds):
 
 
 def cpu_baseline(name, seed, seconds):
+    if seconds <= 0:  # --cpu-seconds 0: no oracle timing (profiling runs)
+        return None
     run = oracle_sample_runner(name, seed)
     s = workload_shape(name)
     ntok = min(s.T, 128 if name == "train" else 1024)
@@ -1101,6 +1103,8 @@ def attn_oracle_runner(seed):
 
 
 def attn_cpu_baseline(seed, seconds):
+    if seconds <= 0:
+        return None
     run = attn_oracle_runner(seed)
     seq = 512
     run(64)
