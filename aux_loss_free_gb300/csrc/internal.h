@@ -68,6 +68,12 @@ struct RouterArgs {
   int T, d, E, k, renorm;
 };
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
+// Router of the permutation-free serving path (bf16 tokens, T <= kDirectMaxPairs, no
+// chunk counts): writes the loads outright (no clearing); zeroes its own counter in
+// the scratch of router_small_scratch_bytes(T, E).
+bool router_small_supported(const RouterArgs& a);
+size_t router_small_scratch_bytes(int T, int E);
+cudaError_t launch_router_small(const RouterArgs& a, void* scratch, cudaStream_t s);
 // Tensor-core router (bf16 tokens, T >= 128, E in {16, 32, 48, 64, 80}); needs
 // scratch for the three-way bf16 split of the router weight.
 bool router_tc_supported(int T, int E, int x_is_f32);

@@ -206,6 +206,7 @@ struct LayerWs {
   uint16_t* y;
   uint16_t* s_out;  // [T][d] shared-expert output (before the combine)
   void* serve;      // fused serving scratch (int4 shapes with at most kServeMaxPairs pairs)
+  void* small_router;  // logits and counter of the permutation-free path's router
   PermuteWs perm;
   FfnWs ffn;
 };
@@ -235,6 +236,9 @@ LayerWs carve_layer(Carver& c, const moe_shape_t* s) {
   w.serve = (s->w_format == MOE_W_INT4_G32 && s->x_dtype == MOE_X_BF16 && Tk <= (size_t)kServeMaxPairs)
                 ? c.take(serve_fused_scratch_bytes(s))
                 : nullptr;
+  w.small_router = (s->w_format == MOE_W_INT4_G32 && s->x_dtype == MOE_X_BF16 && Tk <= (size_t)kDirectMaxPairs)
+                       ? c.take(router_small_scratch_bytes(s->T, s->E))
+                       : nullptr;
   return w;
 }
 
@@ -713,11 +717,16 @@ moe_status_t layer_fwd_impl(const moe_shape_t* shape, const void* x, const float
   moe_balance_t* balance = dbg ? dbg->balance : nullptr;
   const bool need_load = update_bias || (dbg && dbg->load) || balance;
   if (direct) {
-    if (need_load && cudaMemsetAsync(L.load, 0, sizeof(int32_t) * E, rs) != cudaSuccess)
-      return MOE_ERR_CUDA;
     RouterArgs ra{x, xf, w_router, logit_offset, bias, dbg ? dbg->scores : nullptr, L.idx, L.gate,
                   need_load ? L.load : nullptr, nullptr, ct, T, shape->d, E, k, shape->renorm};
-    cudaError_t e = run_router(ra, L.router, rs);
+    cudaError_t e = cudaSuccess;
+    if (L.small_router && router_small_supported(ra)) {
+      e = launch_router_small(ra, L.small_router, rs);  // writes the loads outright
+    } else {
+      if (need_load && cudaMemsetAsync(L.load, 0, sizeof(int32_t) * E, rs) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      e = run_router(ra, L.router, rs);
+    }
     if (e == cudaSuccess && (update_bias || balance))
       e = launch_bias_update(E, (long long)T * k, L.load, gamma, update_bias ? bias : nullptr, rs, balance);
     if (e == cudaSuccess && cache) {

@@ -15,7 +15,10 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <algorithm>
+
 #include "internal.h"
+#include "ptx.cuh"
 #include "select.cuh"
 
 namespace moe {
@@ -212,6 +215,141 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(CTHR) router_cluste
   // No CTA leaves while CTA 0 may still read its logits.
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+
+// Router of the permutation-free serving path (at most 64 tokens, bf16 tokens).  CTA
+// (eb, tb) computes the logits of experts [4 eb, 4 eb + 4) for tokens [8 tb, 8 tb + 8),
+// two warps per expert row of W_r, each against 4 tokens staged in shared memory, in
+// the cluster router's summation order (the logits are the same bits), and writes them
+// to scratch.  The last CTA of each token block (an atomic count per block) runs the
+// selection for the block's tokens, one warp per token, and publishes the block's
+// histogram; the last of those (a second count) adds the histograms into the loads,
+// written outright, so they need no clearing.  The launcher zeroes the counters in the
+// same stream.
+constexpr int SR_EB = 4;   // experts per CTA (two warps each)
+constexpr int SR_TB = 8;   // tokens per CTA (four per warp)
+constexpr int SR_THR = 256;
+
+__global__ void __launch_bounds__(SR_THR, 1) router_small_kernel(RouterArgs a, float* lgs, int* bhist,
+                                                                unsigned* ctr) {
+  extern __shared__ __align__(16) float ssm[];
+  __shared__ int s_last;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int E = a.E, d = a.d, T = a.T;
+  const int neb = (E + SR_EB - 1) / SR_EB;
+  const int eb = (int)blockIdx.x % neb, t0 = ((int)blockIdx.x / neb) * SR_TB;
+  const int e = eb * SR_EB + warp / 2, tq = (warp & 1) * 4;
+  // The first 1024 inputs of this warp's W_r row, before the dependency wait: no
+  // kernel writes the router weight.
+  float4 w[8];
+  const float* wr = a.w_router + (size_t)min(e, E - 1) * d;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int kk = lane * 4 + u * 128;
+    w[u] = kk < d ? *reinterpret_cast<const float4*>(wr + kk) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  pdl_wait();
+  pdl_trigger();
+  float* xs = ssm;  // [SR_TB][d]
+  const uint16_t* x = static_cast<const uint16_t*>(a.x);
+  for (int kk = tid * 8; kk < d; kk += SR_THR * 8) {
+    uint4 u[SR_TB];  // every token's chunk in flight before any is stored
+#pragma unroll
+    for (int tok = 0; tok < SR_TB; ++tok)
+      u[tok] = t0 + tok < T ? *reinterpret_cast<const uint4*>(x + (size_t)(t0 + tok) * d + kk) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int tok = 0; tok < SR_TB; ++tok) {
+      float4* o = reinterpret_cast<float4*>(xs + tok * d + kk);
+      o[0] = make_float4(bf16_bits_to_f32(u[tok].x & 0xFFFFu), bf16_bits_to_f32(u[tok].x >> 16),
+                         bf16_bits_to_f32(u[tok].y & 0xFFFFu), bf16_bits_to_f32(u[tok].y >> 16));
+      o[1] = make_float4(bf16_bits_to_f32(u[tok].z & 0xFFFFu), bf16_bits_to_f32(u[tok].z >> 16),
+                         bf16_bits_to_f32(u[tok].w & 0xFFFFu), bf16_bits_to_f32(u[tok].w >> 16));
+    }
+  }
+  __syncthreads();
+  if (e < E) {  // warp-uniform
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k0 = lane * 4; k0 < d; k0 += 128 * 8) {
+      if (k0 != lane * 4) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int kk = k0 + u * 128;
+          w[u] = kk < d ? *reinterpret_cast<const float4*>(wr + kk) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int kk = k0 + u * 128;
+        if (kk < d) {
+#pragma unroll
+          for (int tok = 0; tok < 4; ++tok) {
+            const float4 xv = *reinterpret_cast<const float4*>(xs + (tq + tok) * d + kk);
+            acc[tok] = fmaf(w[u].x, xv.x, fmaf(w[u].y, xv.y, fmaf(w[u].z, xv.z, fmaf(w[u].w, xv.w, acc[tok]))));
+          }
+        }
+      }
+    }
+    const float off = a.logit_offset ? a.logit_offset[e] : 0.f;
+#pragma unroll
+    for (int tok = 0; tok < 4; ++tok) {
+      float v = acc[tok];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+      const int t = t0 + tq + tok;
+      if (lane == 0 && t < T) lgs[(size_t)t * E + e] = v + off;
+    }
+    if (lane == 0) __threadfence();  // this warp's logits before the count below
+  }
+  __syncthreads();
+  const int ntb = (T + SR_TB - 1) / SR_TB, tb = t0 / SR_TB;
+  if (tid == 0) {
+    __threadfence();
+    s_last = atomicAdd(&ctr[tb], 1u) == (unsigned)neb - 1;
+    if (s_last) __threadfence();
+  }
+  __syncthreads();
+  if (!s_last) return;
+  // The block's last CTA: its tokens' logits (one load per thread in flight), then one
+  // warp per token.
+  float* lb = ssm;  // [SR_TB][E]
+  int* hist = reinterpret_cast<int*>(lb + SR_TB * E);
+  const int nt = min(SR_TB, T - t0);
+  {
+    float v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = tid + j * SR_THR;
+      v[j] = i < nt * E ? __ldcg(lgs + (size_t)t0 * E + i) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (tid + j * SR_THR < nt * E) lb[tid + j * SR_THR] = v[j];
+    for (int i = tid + 4 * SR_THR; i < nt * E; i += SR_THR) lb[i] = __ldcg(lgs + (size_t)t0 * E + i);
+  }
+  for (int i = tid; i < E; i += SR_THR) hist[i] = 0;
+  __syncthreads();
+  if (warp < nt) select_token(a, lb + (size_t)warp * E, t0 + warp, lane, hist);
+  if (!a.load) return;  // the same for the whole CTA
+  __syncthreads();
+  for (int i = tid; i < E; i += SR_THR) bhist[(size_t)tb * E + i] = hist[i];
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    s_last = atomicAdd(&ctr[ntb], 1u) == (unsigned)ntb - 1;
+    if (s_last) __threadfence();
+  }
+  __syncthreads();
+  if (!s_last) return;
+  for (int i = tid; i < E; i += SR_THR) {
+    int sum = 0;
+    for (int b = 0; b < ntb; ++b) sum += __ldcg(bhist + (size_t)b * E + i);
+    a.load[i] = sum;
+  }
+}
+
+size_t router_small_smem(int T, int E, int d) {
+  (void)T;
+  return std::max((size_t)SR_TB * d * 4, (size_t)SR_TB * E * 4 + (size_t)E * 4);
+}
 }  // namespace
 
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s) {
@@ -247,6 +385,33 @@ cudaError_t launch_router(const RouterArgs& a, cudaStream_t s) {
     router_kernel<false><<<blocks, NTHR, dyn, s>>>(a);
   }
   return cudaGetLastError();
+}
+
+
+bool router_small_supported(const RouterArgs& a) {
+  return !a.x_is_f32 && !a.counts && a.T >= 1 && a.T <= kDirectMaxPairs && a.E >= 1 && a.E <= kMaxE &&
+         a.k >= 1 && a.k <= kMaxK && a.d % 8 == 0 && router_small_smem(a.T, a.E, a.d) <= 48 * 1024 &&
+         (reinterpret_cast<uintptr_t>(a.x) & 15u) == 0 && (reinterpret_cast<uintptr_t>(a.w_router) & 15u) == 0;
+}
+
+// Scratch: logits [T][E] fp32, block histograms [T/8][E] int32, counters [T/8 + 1].
+size_t router_small_scratch_bytes(int T, int E) {
+  const size_t ntb = (T + SR_TB - 1) / SR_TB;
+  return ((size_t)T * E * 4 + 15) / 16 * 16 + (ntb * E * 4 + 15) / 16 * 16 + ((ntb + 1) * 4 + 15) / 16 * 16;
+}
+
+cudaError_t launch_router_small(const RouterArgs& a, void* scratch, cudaStream_t s) {
+  if (!router_small_supported(a)) return cudaErrorInvalidValue;
+  const size_t ntb = (a.T + SR_TB - 1) / SR_TB;
+  uint8_t* p = static_cast<uint8_t*>(scratch);
+  float* lgs = reinterpret_cast<float*>(p);
+  int* bhist = reinterpret_cast<int*>(p + ((size_t)a.T * a.E * 4 + 15) / 16 * 16);
+  auto* ctr = reinterpret_cast<unsigned*>(reinterpret_cast<uint8_t*>(bhist) + (ntb * a.E * 4 + 15) / 16 * 16);
+  cudaError_t e = cudaMemsetAsync(ctr, 0, (ntb + 1) * sizeof(unsigned), s);
+  if (e != cudaSuccess) return e;
+  const int grid = ((a.E + SR_EB - 1) / SR_EB) * (int)ntb;
+  return launch_pdl(router_small_kernel, dim3(grid), dim3(SR_THR), router_small_smem(a.T, a.E, a.d), s, a, lgs, bhist,
+                    ctr);
 }
 
 }  // namespace moe
