@@ -377,7 +377,8 @@ template <bool GATE_UP>
 __global__ void __launch_bounds__(TCD_WARPS * 32, GATE_UP ? 2 : 4) int4_tc_direct_kernel(
     const int32_t* __restrict__ idx, int P, int k, const uint8_t* __restrict__ wq,
     const uint16_t* __restrict__ ws, const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
-    int d, int f, int block, const int32_t* __restrict__ slot) {
+    int d, int f, int block, const int32_t* __restrict__ slot, const uint16_t* __restrict__ comb_s,
+    const float* __restrict__ comb_gate) {
   using S = TcdShape<GATE_UP>;
   extern __shared__ __align__(16) uint8_t tcd_smem[];
   const int K = GATE_UP ? d : f, rows = GATE_UP ? f : d;
@@ -522,8 +523,14 @@ __global__ void __launch_bounds__(TCD_WARPS * 32, GATE_UP ? 2 : 4) int4_tc_direc
           if (GATE_UP) v1 += red[tt * S::KS + q][S::NM - 1][cc][cl];
         }
         if (n0 + n < cnt) {
-          const long long o = (long long)pl[n0 + n] * rows + (long long)tile * 16 * S::RT + rr;
-          dst[o] = to_bf16_bits(GATE_UP ? v0 / (1.0f + __expf(-v0)) * v1 : v0);
+          const int pr = pl[n0 + n];
+          const long long o = (long long)pr * rows + (long long)tile * 16 * S::RT + rr;
+          if (GATE_UP)
+            dst[o] = to_bf16_bits(v0 / (1.0f + __expf(-v0)) * v1);
+          else if (comb_s)  // top-1 combine: pair pr is token pr
+            dst[o] = to_bf16_bits(fmaf(comb_gate[pr], v0, __uint_as_float((uint32_t)comb_s[o] << 16)));
+          else
+            dst[o] = to_bf16_bits(v0);
         }
       }
     }
@@ -547,7 +554,8 @@ constexpr int kTcdMaxSmemGateUp = 110 * 1024, kTcdMaxSmemDown = 54 * 1024;
 bool tc_direct_supported(bool gate_up, int d, int f, const void* wq, const void* ws, const void* src) {
   const bool aligned = ((reinterpret_cast<uintptr_t>(wq) | reinterpret_cast<uintptr_t>(ws) |
                          reinterpret_cast<uintptr_t>(src)) & 15u) == 0;
-  return aligned && gate_up ? (d % 256 == 0 && f % 16 == 0 && tcd_smem_bytes<true>(d, f) <= (size_t)kTcdMaxSmemGateUp)
+  if (!aligned) return false;
+  return gate_up ? (d % 256 == 0 && f % 16 == 0 && tcd_smem_bytes<true>(d, f) <= (size_t)kTcdMaxSmemGateUp)
                  : (f % 256 == 0 && d % 32 == 0 && tcd_smem_bytes<false>(d, f) <= (size_t)kTcdMaxSmemDown);
 }
 
@@ -557,6 +565,26 @@ int decode_grid() {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   return 4 * sms;
 }
+
+// The tensor-core kernels' shared-memory limits, raised once per device to the largest
+// size the support check admits.
+cudaError_t tcd_raise_smem_limits() {
+  static std::atomic<bool> attr_set[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_relaxed)) {
+    e = cudaFuncSetAttribute(int4_tc_direct_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kTcdMaxSmemGateUp);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(int4_tc_direct_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kTcdMaxSmemDown);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_relaxed);
+  }
+  return cudaSuccess;
+}
+
 
 }  // namespace
 
@@ -576,32 +604,38 @@ cudaError_t launch_int4_direct(bool gate_up, const int32_t* idx, int pairs, int 
     const long long units = (long long)pairs * (gate_up ? f / 16 : d / 32);
     const int grid = (int)std::min<long long>(units, decode_grid() / 4 * (gate_up ? 2 : 4));
     const size_t smem = gate_up ? tcd_smem_bytes<true>(d, f) : tcd_smem_bytes<false>(d, f);
-    // The kernels' shared-memory limits, raised once per device to the largest size
-    // the support check admits.
-    static std::atomic<bool> attr_set[64];
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_relaxed)) {
-      e = cudaFuncSetAttribute(int4_tc_direct_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kTcdMaxSmemGateUp);
-      if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(int4_tc_direct_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kTcdMaxSmemDown);
-      if (e != cudaSuccess) return e;
-      if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_relaxed);
-    }
+    const cudaError_t ea = tcd_raise_smem_limits();
+    if (ea != cudaSuccess) return ea;
+    const uint16_t* no_s = nullptr;
+    const float* no_g = nullptr;
     if (gate_up)
       return launch_pdl(int4_tc_direct_kernel<true>, dim3(grid), dim3(TCD_WARPS * 32), smem, s, idx, pairs, k,
-                        wq, ws, src, dst, d, f, block, slot);
+                        wq, ws, src, dst, d, f, block, slot, no_s, no_g);
     return launch_pdl(int4_tc_direct_kernel<false>, dim3(grid), dim3(TCD_WARPS * 32), smem, s, idx, pairs, k,
-                      wq, ws, src, dst, d, f, block, slot);
+                      wq, ws, src, dst, d, f, block, slot, no_s, no_g);
   }
   if (gate_up)
     return launch_pdl(int4_direct_kernel<true>, dim3(decode_grid()), dim3(DEC_WARPS * 32), 0, s, idx,
                       pairs, k, wq, ws, src, dst, d, f, block, slot);
   return launch_pdl(int4_direct_kernel<false>, dim3(decode_grid()), dim3(DEC_WARPS * 32), 0, s, idx,
                     pairs, k, wq, ws, src, dst, d, f, block, slot);
+}
+
+bool int4_direct_down_combine_supported(int d, int f, int k, const void* wq, const void* ws, const void* h) {
+  return k == 1 && tc_direct_supported(false, d, f, wq, ws, h);
+}
+
+cudaError_t launch_int4_direct_down_combine(const int32_t* idx, int pairs, const uint8_t* wq, const uint16_t* ws,
+                                            const uint16_t* h, const uint16_t* s_in, const float* gate,
+                                            uint16_t* out, int d, int f, cudaStream_t s, const int32_t* slot) {
+  if (pairs < 1 || pairs > kDirectMaxPairs || !int4_direct_down_combine_supported(d, f, 1, wq, ws, h) || !s_in ||
+      !gate)
+    return cudaErrorInvalidValue;
+  const cudaError_t ea = tcd_raise_smem_limits();
+  if (ea != cudaSuccess) return ea;
+  const int grid = (int)std::min<long long>((long long)pairs * (d / 32), decode_grid());
+  return launch_pdl(int4_tc_direct_kernel<false>, dim3(grid), dim3(TCD_WARPS * 32), tcd_smem_bytes<false>(d, f), s,
+                    idx, pairs, 1, wq, ws, h, out, d, f, 0, slot, s_in, gate);
 }
 
 cudaError_t launch_int4_down(const int32_t* active, const int32_t* offsets, const uint8_t* wq,

@@ -254,6 +254,13 @@ cudaError_t launch_serve_fused(const moe_shape_t* s, const ServeArgs& a, cudaStr
 cudaError_t launch_int4_direct(bool gate_up, const int32_t* idx, int pairs, int k, const uint8_t* wq,
                                const uint16_t* ws, const uint16_t* src, uint16_t* dst, int d, int f,
                                int block, cudaStream_t s, const int32_t* slot = nullptr);
+// The permutation-free down projection with the combine in its epilogue (one expert
+// per token, tensor-core shapes): out[t][n] = bf16(s_in[t][n] + gate[t] * y[t][n]),
+// y the routed row in fp32, s_in the shared expert's output (residual included).
+bool int4_direct_down_combine_supported(int d, int f, int k, const void* wq, const void* ws, const void* h);
+cudaError_t launch_int4_direct_down_combine(const int32_t* idx, int pairs, const uint8_t* wq, const uint16_t* ws,
+                                            const uint16_t* h, const uint16_t* s_in, const float* gate,
+                                            uint16_t* out, int d, int f, cudaStream_t s, const int32_t* slot);
 cudaError_t launch_int4_down(const int32_t* active, const int32_t* offsets, const uint8_t* wq,
                              const uint16_t* ws, const uint16_t* h, uint16_t* y, int d, int f,
                              cudaStream_t s, const int32_t* slot = nullptr);

@@ -315,10 +315,12 @@ bool int4_skinny(const moe_shape_t* s) {
 // shared_gate_up_on: non-null when the shared gate/up already runs on another stream;
 // its completion event, waited for before the shared down projection.
 // direct: the routed experts work from idx without the permutation (h and y by pair).
+// shared_on_aux: the second stream also ran the shared down projection into L.s_out
+// (with the residual); the routed down projection then adds it in its epilogue.
 moe_status_t run_ffn_int4(const moe_shape_t* s, const void* x_bf16, const LayerWs& L,
                           const moe_weights_t* w, const void* residual, uint16_t* out,
                           cudaStream_t st, bool mark, cudaEvent_t shared_gate_up_on = nullptr,
-                          bool direct = false, const int32_t* slot = nullptr) {
+                          bool direct = false, const int32_t* slot = nullptr, bool shared_on_aux = false) {
   const long long Tk = (long long)s->T * s->k;
   int bad = 0;
   GemmOperandSet off{};
@@ -344,6 +346,14 @@ moe_status_t run_ffn_int4(const moe_shape_t* s, const void* x_bf16, const LayerW
                            static_cast<const uint16_t*>(w->scale_gate_up),
                            static_cast<const uint16_t*>(x_bf16), L.ffn.h, s->d, s->f,
                            moe_gate_up_block(s->f), st, slot);
+    if (e == cudaSuccess && shared_on_aux) {
+      if (mark) prof_mark("int4_down_combine", st);
+      if (cudaStreamWaitEvent(st, shared_gate_up_on, 0) != cudaSuccess) return MOE_ERR_CUDA;
+      e = launch_int4_direct_down_combine(L.idx, (int)Tk, static_cast<const uint8_t*>(w->w_down),
+                                          static_cast<const uint16_t*>(w->scale_down), L.ffn.h, L.s_out, L.gate,
+                                          out, s->d, s->f, st, slot);
+      return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    }
     if (e == cudaSuccess)
       e = launch_int4_direct(false, L.idx, (int)Tk, s->k, static_cast<const uint8_t*>(w->w_down),
                              static_cast<const uint16_t*>(w->scale_down), L.ffn.h, L.y, s->d, s->f,
@@ -695,6 +705,18 @@ moe_status_t layer_fwd_impl(const moe_shape_t* shape, const void* x, const float
   // Top-1 serving with few tokens: the shared expert's gate/up needs only x, so it
   // runs on the second stream beside the routing and the routed int4 experts.
   const bool int4_fork = int4 && !xf && int4_skinny(shape);
+  // Top-1 serving with at most kDirectMaxPairs (token, expert) pairs skips the
+  // permutation: the int4 experts read the routing result directly.  The loads are
+  // then counted only when the bias update or the caller needs them.
+  const bool direct = int4 && !xf && (long long)T * k <= kDirectMaxPairs &&
+                      (shape->F == 0 || int4_skinny(shape)) &&
+                      !(dbg && (dbg->offsets || dbg->perm_tok || dbg->inv_pos));
+  // With one expert per token on the tensor-core kernels, the shared down projection
+  // also runs on the second stream (into s_out, residual included) and the routed down
+  // projection adds it: the shared expert leaves the critical path.
+  const bool shared_on_aux = int4_fork && direct && k == 1 && L.s_out &&
+                             int4_direct_down_combine_supported(shape->d, shape->f, k, w->w_down, w->scale_down,
+                                                                L.ffn.h);
   if (int4_fork) {
     aux_lock.lock();
     aux = aux_for_current_device();
@@ -704,16 +726,16 @@ moe_status_t layer_fwd_impl(const moe_shape_t* shape, const void* x, const float
       return MOE_ERR_CUDA;
     if (launch_skinny(0, static_cast<const uint16_t*>(w->shared_gate_up), 2 * shape->F, shape->d,
                       static_cast<const uint16_t*>(x), T, L.ffn.hs, shape->F, nullptr,
-                      aux->s) != cudaSuccess ||
-        cudaEventRecord(aux->join, aux->s) != cudaSuccess)
+                      aux->s) != cudaSuccess)
       return MOE_ERR_CUDA;
+    if (shared_on_aux) {
+      CombineInputs res_only{nullptr, nullptr, nullptr, static_cast<const uint16_t*>(residual), k};
+      if (launch_skinny(1, static_cast<const uint16_t*>(w->shared_down), shape->d, shape->F, L.ffn.hs, T, L.s_out,
+                        shape->d, &res_only, aux->s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    }
+    if (cudaEventRecord(aux->join, aux->s) != cudaSuccess) return MOE_ERR_CUDA;
   }
-  // Top-1 serving with at most kDirectMaxPairs (token, expert) pairs skips the
-  // permutation: the int4 experts read the routing result directly.  The loads are
-  // then counted only when the bias update or the caller needs them.
-  const bool direct = int4 && !xf && (long long)T * k <= kDirectMaxPairs &&
-                      (shape->F == 0 || int4_skinny(shape)) &&
-                      !(dbg && (dbg->offsets || dbg->perm_tok || dbg->inv_pos));
   moe_balance_t* balance = dbg ? dbg->balance : nullptr;
   const bool need_load = update_bias || (dbg && dbg->load) || balance;
   if (direct) {
@@ -737,7 +759,7 @@ moe_status_t layer_fwd_impl(const moe_shape_t* shape, const void* x, const float
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     const moe_status_t st2 = run_ffn_int4(shape, x, L, w, residual, static_cast<uint16_t*>(out), s,
                                           prof, int4_fork ? aux->join : nullptr, true,
-                                          cache ? cache->view.expert_slot : nullptr);
+                                          cache ? cache->view.expert_slot : nullptr, shared_on_aux);
     if (prof) prof_mark(nullptr, s);
     return st2;
   }
