@@ -77,8 +77,9 @@ def kernels_per_call(s):
         if s.T * s.k <= 8 and s.x_dtype == "bf16" and s.d % 256 == 0 and s.f % 256 == 0:
             return 1  # the single-launch serving kernel (with the expert cache's plan and fill)
         if s.T * s.k <= 64:
-            # no permutation: shared gate/up (second stream), int4 gate/up, int4 down,
-            # shared down + combine (or the combine kernel without a shared expert)
+            # no permutation: shared gate/up and down (second stream), int4 gate/up, int4
+            # down with the combine (or, off the tensor-core shapes, the shared down with
+            # the combine; the combine kernel without a shared expert)
             return router + 2 + (2 if s.F else 1)
         # permute, shared gate/up, int4 gate/up, int4 down, shared down + combine
         return router + 1 + (4 if s.F else 2) + (0 if s.F else 1)
