@@ -388,6 +388,7 @@ __global__ void __launch_bounds__(TCD_WARPS * 32, GATE_UP ? 2 : 4) int4_tc_direc
   float(*red)[S::NM][4][32] = reinterpret_cast<float(*)[S::NM][4][32]>(tcd_smem + TCD_STAGES * stage_bytes);
   int(*plist)[kDirectMaxPairs] = reinterpret_cast<int(*)[kDirectMaxPairs]>(red + TCD_WARPS);
   int* dexp = plist[TCD_WARPS];  // the distinct experts, in the order of their first pair
+  int* goff = dexp + kDirectMaxPairs;  // gate/up: each tile's first gate row within an expert
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
@@ -408,25 +409,35 @@ __global__ void __launch_bounds__(TCD_WARPS * 32, GATE_UP ? 2 : 4) int4_tc_direc
     if ((first_lo >> lane) & 1u) dexp[__popc(first_lo & below)] = ea;
     if ((first_hi >> lane) & 1u) dexp[__popc(first_lo) + __popc(first_hi & below)] = eb;
   }
+  if (GATE_UP)
+    for (int tl = tid; tl < tiles; tl += TCD_WARPS * 32) goff[tl] = (tl * 16 / block) * 2 * block + tl * 16 % block;
   __syncthreads();
   const int nunits = (__popc(first_lo) + __popc(first_hi)) * tiles;
   const int mine = (int)blockIdx.x < nunits ? (nunits - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
   const uint32_t smem0 = smem_u32(tcd_smem);
-  auto expert_of = [&](int unit) { return dexp[unit / tiles]; };
-  // Global row (in the code and scale tensors) of row r of a unit.
+  // Global row (in the code and scale tensors) of row r of a unit (the tile's 16 gate rows
+  // sit inside one interleave block: block is a multiple of 16).
   auto weight_row = [&](long long we, int tile, int r) -> long long {
-    if (GATE_UP) {
-      const int j = tile * 16 + (r & 15);
-      return we * 2 * f + (j / block) * 2 * block + j % block + (r >= 16 ? block : 0);
-    }
+    if (GATE_UP) return we * 2 * f + goff[tile] + (r & 15) + (r >= 16 ? block : 0);
     return we * d + tile * 32 + r;
+  };
+  // A CTA's units are blockIdx.x + i * gridDim.x; walk their (expert, tile) without
+  // dividing per unit.
+  const int step_q = (int)gridDim.x / tiles, step_r = (int)gridDim.x % tiles;
+  auto advance = [&](int& ue, int& tl) {
+    tl += step_r;
+    ue += step_q;
+    if (tl >= tiles) {
+      tl -= tiles;
+      ++ue;
+    }
   };
   // All threads: copy unit `unit`'s code and scale rows into stage `st`, 8 threads per
   // row (each row's address computed once), 16-byte chunks.
   static_assert(S::ROWS * 8 == TCD_WARPS * 32, "8 copying threads per row");
   const int crow_r = tid >> 3, csub = tid & 7;
-  auto issue = [&](int unit, int st) {
-    const int e = expert_of(unit), tile = unit % tiles;
+  auto issue = [&](int ue, int tile, int st) {
+    const int e = dexp[ue];
     const long long row = weight_row(slot ? slot[e] : e, tile, crow_r);
     const uint8_t* cs = wq + row * (K / 2) + csub * 16;
     uint32_t cd = smem0 + st * stage_bytes + crow_r * cstride + csub * 16;
@@ -435,18 +446,22 @@ __global__ void __launch_bounds__(TCD_WARPS * 32, GATE_UP ? 2 : 4) int4_tc_direc
     uint32_t sd = smem0 + st * stage_bytes + S::ROWS * cstride + crow_r * sstride + csub * 16;
     for (int q = csub; q < K / 256; q += 8, ss += 128, sd += 128) cp_async16(sd, ss);
   };
+  int cur_ue = (int)blockIdx.x / tiles, cur_tl = (int)blockIdx.x % tiles;  // unit i
+  int nxt_ue = cur_ue, nxt_tl = cur_tl;                                      // unit i + stages - 1
 #pragma unroll 1
   for (int i = 0; i < TCD_STAGES - 1; ++i) {
-    if (i < mine) issue((int)blockIdx.x + i * (int)gridDim.x, i);
+    if (i < mine) issue(nxt_ue, nxt_tl, i);
     cp_async_commit();
+    advance(nxt_ue, nxt_tl);
   }
   int* pl = plist[warp];
 #pragma unroll 1
   for (int i = 0; i < mine; ++i) {
-    const int unit = (int)blockIdx.x + i * (int)gridDim.x;
-    if (i + TCD_STAGES - 1 < mine) issue(unit + (TCD_STAGES - 1) * (int)gridDim.x, (i + TCD_STAGES - 1) % TCD_STAGES);
+    if (i + TCD_STAGES - 1 < mine) issue(nxt_ue, nxt_tl, (i + TCD_STAGES - 1) % TCD_STAGES);
     cp_async_commit();
-    const int e = expert_of(unit), tile = unit % tiles;
+    advance(nxt_ue, nxt_tl);
+    const int e = dexp[cur_ue], tile = cur_tl;
+    advance(cur_ue, cur_tl);
     const unsigned ma = __ballot_sync(0xFFFFFFFFu, ea == e), mb = __ballot_sync(0xFFFFFFFFu, eb == e);
     const int cnt = __popc(ma) + __popc(mb);
     // The expert's pairs in order (each warp keeps its own copy).
@@ -463,7 +478,8 @@ __global__ void __launch_bounds__(TCD_WARPS * 32, GATE_UP ? 2 : 4) int4_tc_direc
     for (int n0 = 0; n0 < cnt; n0 += 8) {
       const int pn = n0 + g;  // this lane's column of B
       const bool col_ok = pn < cnt;
-      const uint16_t* xr = src + (long long)(col_ok ? (GATE_UP ? pl[pn] / k : pl[pn]) : 0) * K + g0 * 32 + 8 * t;
+      const int srow = col_ok ? (GATE_UP && k != 1 ? pl[pn] / k : pl[pn]) : 0;
+      const uint16_t* xr = src + (long long)srow * K + g0 * 32 + 8 * t;
       float acc[S::NM][4];
 #pragma unroll
       for (int m = 0; m < S::NM; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
@@ -545,17 +561,17 @@ size_t tcd_smem_bytes(int d, int f) {
   using S = TcdShape<GATE_UP>;
   const int K = GATE_UP ? d : f;
   return (size_t)TCD_STAGES * S::ROWS * (K / 2 + 16 + K / 16 + 16) + sizeof(float) * TCD_WARPS * S::NM * 4 * 32 +
-         sizeof(int) * (TCD_WARPS + 1) * kDirectMaxPairs;
+         sizeof(int) * (TCD_WARPS + 1) * kDirectMaxPairs + (GATE_UP ? sizeof(int) * (f / 16) : 0);
 }
 
 // Two gate/up CTAs or four down CTAs per SM.
 constexpr int kTcdMaxSmemGateUp = 110 * 1024, kTcdMaxSmemDown = 54 * 1024;
 
-bool tc_direct_supported(bool gate_up, int d, int f, const void* wq, const void* ws, const void* src) {
+bool tc_direct_supported(bool gate_up, int d, int f, int block, const void* wq, const void* ws, const void* src) {
   const bool aligned = ((reinterpret_cast<uintptr_t>(wq) | reinterpret_cast<uintptr_t>(ws) |
                          reinterpret_cast<uintptr_t>(src)) & 15u) == 0;
   if (!aligned) return false;
-  return gate_up ? (d % 256 == 0 && f % 16 == 0 && tcd_smem_bytes<true>(d, f) <= (size_t)kTcdMaxSmemGateUp)
+  return gate_up ? (d % 256 == 0 && f % 16 == 0 && block % 16 == 0 && tcd_smem_bytes<true>(d, f) <= (size_t)kTcdMaxSmemGateUp)
                  : (f % 256 == 0 && d % 32 == 0 && tcd_smem_bytes<false>(d, f) <= (size_t)kTcdMaxSmemDown);
 }
 
@@ -599,7 +615,7 @@ cudaError_t launch_int4_direct(bool gate_up, const int32_t* idx, int pairs, int 
                                const uint16_t* ws, const uint16_t* src, uint16_t* dst, int d, int f,
                                int block, cudaStream_t s, const int32_t* slot) {
   if (pairs < 1 || pairs > kDirectMaxPairs) return cudaErrorInvalidValue;
-  if (tc_direct_supported(gate_up, d, f, wq, ws, src)) {
+  if (tc_direct_supported(gate_up, d, f, block, wq, ws, src)) {
     // At most `pairs` distinct experts; one resident wave of CTAs walks the units.
     const long long units = (long long)pairs * (gate_up ? f / 16 : d / 32);
     const int grid = (int)std::min<long long>(units, decode_grid() / 4 * (gate_up ? 2 : 4));
@@ -622,7 +638,7 @@ cudaError_t launch_int4_direct(bool gate_up, const int32_t* idx, int pairs, int 
 }
 
 bool int4_direct_down_combine_supported(int d, int f, int k, const void* wq, const void* ws, const void* h) {
-  return k == 1 && tc_direct_supported(false, d, f, wq, ws, h);
+  return k == 1 && tc_direct_supported(false, d, f, 16, wq, ws, h);
 }
 
 cudaError_t launch_int4_direct_down_combine(const int32_t* idx, int pairs, const uint8_t* wq, const uint16_t* ws,
