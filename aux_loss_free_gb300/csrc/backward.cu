@@ -238,7 +238,7 @@ __global__ void router_bwd_dx_kernel(const int32_t* __restrict__ idx, const floa
 // Block (256 columns, expert e), 8 warps: warp w takes rows w, w + 8, ... with 8
 // columns a lane (16-byte loads, eight rows in flight); the warps' partial sums are
 // added in warp order through shared memory, so the result is deterministic.
-__global__ void router_wgrad_kernel(const float* __restrict__ dzp, const int32_t* __restrict__ off,
+__global__ void __launch_bounds__(256, 2) router_wgrad_kernel(const float* __restrict__ dzp, const int32_t* __restrict__ off,
                                     const int32_t* __restrict__ poff, const uint16_t* __restrict__ xp,
                                     int d, float* __restrict__ dwr) {
   __shared__ float part[8][256];
@@ -251,6 +251,26 @@ __global__ void router_wgrad_kernel(const float* __restrict__ dzp, const int32_t
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
   if (c < d) {
     int r = warp;
+    // Sixteen rows of a warp in flight per step, then eight, then one at a time: each
+    // warp still adds its rows warp, warp + 8, ... in ascending order.
+    for (; r + 120 < n; r += 128) {
+      uint4 u[16];
+      float z[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        u[j] = __ldg(reinterpret_cast<const uint4*>(xp + (size_t)(q0 + r + 8 * j) * d + c));
+        z[j] = dzp[q0 + r + 8 * j];
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t w4[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] = fmaf(z[j], __uint_as_float(w4[i] << 16), acc[2 * i]);
+          acc[2 * i + 1] = fmaf(z[j], __uint_as_float(w4[i] & 0xFFFF0000u), acc[2 * i + 1]);
+        }
+      }
+    }
     for (; r + 56 < n; r += 64) {
       uint4 u[8];
       float z[8];
