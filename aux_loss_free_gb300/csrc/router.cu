@@ -297,12 +297,11 @@ __global__ void __launch_bounds__(SR_THR, 1) router_small_kernel(RouterArgs a, f
       const int t = t0 + tq + tok;
       if (lane == 0 && t < T) lgs[(size_t)t * E + e] = v + off;
     }
-    if (lane == 0) __threadfence();  // this warp's logits before the count below
   }
   __syncthreads();
   const int ntb = (T + SR_TB - 1) / SR_TB, tb = t0 / SR_TB;
   if (tid == 0) {
-    __threadfence();
+    __threadfence();  // the CTA's logits, ordered before this thread by the barrier
     s_last = atomicAdd(&ctr[tb], 1u) == (unsigned)neb - 1;
     if (s_last) __threadfence();
   }
@@ -331,9 +330,9 @@ __global__ void __launch_bounds__(SR_THR, 1) router_small_kernel(RouterArgs a, f
   if (!a.load) return;  // the same for the whole CTA
   __syncthreads();
   for (int i = tid; i < E; i += SR_THR) bhist[(size_t)tb * E + i] = hist[i];
-  __threadfence();
   __syncthreads();
   if (tid == 0) {
+    __threadfence();  // the CTA's writes, ordered before this thread by the barrier
     s_last = atomicAdd(&ctr[ntb], 1u) == (unsigned)ntb - 1;
     if (s_last) __threadfence();
   }

@@ -31,9 +31,12 @@ def _gpu():
 
 
 CASES = [
-    # few pairs: the permutation-free path (int4_direct_kernel); Zipf-skewed routing
+    # at most 8 pairs: the single serving launch (plan and fill inside it); Zipf-skewed routing
     ("direct, skewed", dict(T=8, skew_zipf_s=1.2), 12, 40),
     ("direct, one token", dict(T=1, skew_zipf_s=1.2), 3, 30),
+    # 9 to 64 pairs: the permutation-free path (router of small CTAs, tensor-core int4
+    # kernels reading the experts from their slots)
+    ("direct, 32 tokens", dict(T=32, skew_zipf_s=1.2), 40, 12),
     # more pairs: the permutation path (active experts); more experts than slots
     ("permuted", dict(T=100, E=160, d=256, f=128, F=256, skew_zipf_s=0.8), 120, 12),
 ]
