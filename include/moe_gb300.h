@@ -254,7 +254,10 @@ moe_status_t moe_load_balance(int32_t E, const int32_t* load, moe_balance_t* bal
  * with events) while the shared expert's gate/up GEMM runs on `stream`; all work is
  * ordered before anything enqueued on `stream` after the call.  bias is read for selection and then updated in place.
  * residual (NULL or [T][d], same dtype as out) is added to the output.  For
- * MOE_W_INT4_G32 the routed experts run through the int4 dequant-in-GEMM path.
+ * MOE_W_INT4_G32 the routed experts run through the int4 dequant-in-GEMM path; with
+ * 9 to 64 tokens (top-1, no permutation outputs asked for in dbg) they work straight
+ * from the routing result and the shared expert runs on the same library-owned second
+ * stream, joined back with an event.
  * Top-1 int4 serving of at most 8 tokens (bf16 tokens, d and f multiples of 256, the
  * weights 16-byte aligned, no permutation outputs asked for in dbg) runs as one
  * persistent launch with one CTA per SM whose CTAs wait on one another (section
@@ -262,7 +265,7 @@ moe_status_t moe_load_balance(int32_t E, const int32_t* load, moe_balance_t* bal
  * it needs every SM free at once, and a wait that does not end within 2 s (other
  * kernels holding SMs that long) sets MOE_ERR_TIMEOUT in the device status word and
  * leaves the outputs unspecified.  The workspace needs no clearing between calls, but
- * two calls must not use the same workspace at the same time. 
+ * two calls must not use the same workspace at the same time.
  *   out        [T][d] bf16
  *   dbg        NULL or intermediate outputs (see moe_debug_t)
  *   workspace  moe_layer_workspace_size(shape) bytes of scratch. */
