@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 2) int4_direct_kernel(
 // (expert, row tile); the experts are the distinct ones of the routing result, in the
 // order of their first pair.  The CTA's 8 warps share a unit: gate/up, 16 gate rows and
 // the 16 matching up rows with K split 8 ways; down, two 16-row tiles with K split 4
-// ways.  Each CTA walks its units through a ring of TCD_STAGES shared-memory stages
+// ways.  Each CTA walks its units through a ring of tcd_stages<GATE_UP>() shared-memory stages
 // filled by cp.async (a unit's code rows and scale rows, each row padded by 16 bytes so
 // the fragment reads below fall in distinct banks), so the next units' weights stream
 // in while one is multiplied.  Per 32-input group a lane reads one 32-bit word of 8
@@ -337,7 +337,9 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 2) int4_direct_kernel(
 // product q * x exact, as in the CUDA-core path); the warps' partials are summed in a
 // fixed order through shared memory.
 constexpr int TCD_WARPS = 8;
-constexpr int TCD_STAGES = 4;
+// Ring depth: three stages let three gate/up CTAs share an SM, four down CTAs.
+template <bool GATE_UP>
+__host__ __device__ constexpr int tcd_stages() { return GATE_UP ? 3 : 4; }
 
 template <bool GATE_UP>
 struct TcdShape {
@@ -374,7 +376,7 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 template <bool GATE_UP>
-__global__ void __launch_bounds__(TCD_WARPS * 32, GATE_UP ? 2 : 4) int4_tc_direct_kernel(
+__global__ void __launch_bounds__(TCD_WARPS * 32, GATE_UP ? 3 : 4) int4_tc_direct_kernel(
     const int32_t* __restrict__ idx, int P, int k, const uint8_t* __restrict__ wq,
     const uint16_t* __restrict__ ws, const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
     int d, int f, int block, const int32_t* __restrict__ slot, const uint16_t* __restrict__ comb_s,
@@ -385,7 +387,7 @@ __global__ void __launch_bounds__(TCD_WARPS * 32, GATE_UP ? 2 : 4) int4_tc_direc
   const int ngroups = K / 32, gpw = ngroups / S::KS;
   const int cstride = K / 2 + 16, sstride = ngroups * 2 + 16;  // padded row strides (bytes)
   const int stage_bytes = S::ROWS * (cstride + sstride);
-  float(*red)[S::NM][4][32] = reinterpret_cast<float(*)[S::NM][4][32]>(tcd_smem + TCD_STAGES * stage_bytes);
+  float(*red)[S::NM][4][32] = reinterpret_cast<float(*)[S::NM][4][32]>(tcd_smem + tcd_stages<GATE_UP>() * stage_bytes);
   int(*plist)[kDirectMaxPairs] = reinterpret_cast<int(*)[kDirectMaxPairs]>(red + TCD_WARPS);
   int* dexp = plist[TCD_WARPS];  // the distinct experts, in the order of their first pair
   int* goff = dexp + kDirectMaxPairs;  // gate/up: each tile's first gate row within an expert
@@ -449,7 +451,7 @@ __global__ void __launch_bounds__(TCD_WARPS * 32, GATE_UP ? 2 : 4) int4_tc_direc
   int cur_ue = (int)blockIdx.x / tiles, cur_tl = (int)blockIdx.x % tiles;  // unit i
   int nxt_ue = cur_ue, nxt_tl = cur_tl;                                      // unit i + stages - 1
 #pragma unroll 1
-  for (int i = 0; i < TCD_STAGES - 1; ++i) {
+  for (int i = 0; i < tcd_stages<GATE_UP>() - 1; ++i) {
     if (i < mine) issue(nxt_ue, nxt_tl, i);
     cp_async_commit();
     advance(nxt_ue, nxt_tl);
@@ -457,7 +459,7 @@ __global__ void __launch_bounds__(TCD_WARPS * 32, GATE_UP ? 2 : 4) int4_tc_direc
   int* pl = plist[warp];
 #pragma unroll 1
   for (int i = 0; i < mine; ++i) {
-    if (i + TCD_STAGES - 1 < mine) issue(nxt_ue, nxt_tl, (i + TCD_STAGES - 1) % TCD_STAGES);
+    if (i + tcd_stages<GATE_UP>() - 1 < mine) issue(nxt_ue, nxt_tl, (i + tcd_stages<GATE_UP>() - 1) % tcd_stages<GATE_UP>());
     cp_async_commit();
     advance(nxt_ue, nxt_tl);
     const int e = dexp[cur_ue], tile = cur_tl;
@@ -468,7 +470,7 @@ __global__ void __launch_bounds__(TCD_WARPS * 32, GATE_UP ? 2 : 4) int4_tc_direc
     if ((ma >> lane) & 1u) pl[__popc(ma & below)] = lane;
     if ((mb >> lane) & 1u) pl[__popc(ma) + __popc(mb & below)] = lane + 32;
     __syncwarp();
-    const uint8_t* stage = tcd_smem + (i % TCD_STAGES) * stage_bytes;
+    const uint8_t* stage = tcd_smem + (i % tcd_stages<GATE_UP>()) * stage_bytes;
     const int g0 = kp * gpw;
     // This lane's rows r0 = m*16 + rt*16 + l/4 and r0 + 8 of each set, at group g0.
     const uint8_t* cp0 = stage + (rt * 16 + g) * cstride + g0 * 16 + 4 * t;
@@ -491,7 +493,7 @@ __global__ void __launch_bounds__(TCD_WARPS * 32, GATE_UP ? 2 : 4) int4_tc_direc
           xv[j] = (col_ok && j0 + j < gpw) ? *reinterpret_cast<const uint4*>(xr + (j0 + j) * 32)
                                            : make_uint4(0, 0, 0, 0);
         if (!waited) {  // the unit's rows have landed (this thread's copies, then everyone's)
-          cp_async_wait<TCD_STAGES - 1>();
+          cp_async_wait<tcd_stages<GATE_UP>() - 1>();
           __syncthreads();
           waited = true;
         }
@@ -560,11 +562,11 @@ template <bool GATE_UP>
 size_t tcd_smem_bytes(int d, int f) {
   using S = TcdShape<GATE_UP>;
   const int K = GATE_UP ? d : f;
-  return (size_t)TCD_STAGES * S::ROWS * (K / 2 + 16 + K / 16 + 16) + sizeof(float) * TCD_WARPS * S::NM * 4 * 32 +
+  return (size_t)tcd_stages<GATE_UP>() * S::ROWS * (K / 2 + 16 + K / 16 + 16) + sizeof(float) * TCD_WARPS * S::NM * 4 * 32 +
          sizeof(int) * (TCD_WARPS + 1) * kDirectMaxPairs + (GATE_UP ? sizeof(int) * (f / 16) : 0);
 }
 
-// Two gate/up CTAs or four down CTAs per SM.
+// Three gate/up CTAs or four down CTAs per SM at the Nano shapes (the limits admit larger ones at lower occupancy).
 constexpr int kTcdMaxSmemGateUp = 110 * 1024, kTcdMaxSmemDown = 54 * 1024;
 
 bool tc_direct_supported(bool gate_up, int d, int f, int block, const void* wq, const void* ws, const void* src) {
@@ -618,7 +620,7 @@ cudaError_t launch_int4_direct(bool gate_up, const int32_t* idx, int pairs, int 
   if (tc_direct_supported(gate_up, d, f, block, wq, ws, src)) {
     // At most `pairs` distinct experts; one resident wave of CTAs walks the units.
     const long long units = (long long)pairs * (gate_up ? f / 16 : d / 32);
-    const int grid = (int)std::min<long long>(units, decode_grid() / 4 * (gate_up ? 2 : 4));
+    const int grid = (int)std::min<long long>(units, decode_grid() / 4 * (gate_up ? 3 : 4));
     const size_t smem = gate_up ? tcd_smem_bytes<true>(d, f) : tcd_smem_bytes<false>(d, f);
     const cudaError_t ea = tcd_raise_smem_limits();
     if (ea != cudaSuccess) return ea;
