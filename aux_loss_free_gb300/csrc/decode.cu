@@ -337,9 +337,10 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 2) int4_direct_kernel(
 // product q * x exact, as in the CUDA-core path); the warps' partials are summed in a
 // fixed order through shared memory.
 constexpr int TCD_WARPS = 8;
-// Ring depth: three stages let three gate/up CTAs share an SM, four down CTAs.
+// Ring depth: two stages let four gate/up CTAs share an SM (more warps to hide latency
+// beat a deeper ring); four for the down projection, also four CTAs per SM.
 template <bool GATE_UP>
-__host__ __device__ constexpr int tcd_stages() { return GATE_UP ? 3 : 4; }
+__host__ __device__ constexpr int tcd_stages() { return GATE_UP ? 2 : 4; }
 
 template <bool GATE_UP>
 struct TcdShape {
@@ -376,7 +377,7 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 template <bool GATE_UP>
-__global__ void __launch_bounds__(TCD_WARPS * 32, GATE_UP ? 3 : 4) int4_tc_direct_kernel(
+__global__ void __launch_bounds__(TCD_WARPS * 32, 4) int4_tc_direct_kernel(
     const int32_t* __restrict__ idx, int P, int k, const uint8_t* __restrict__ wq,
     const uint16_t* __restrict__ ws, const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
     int d, int f, int block, const int32_t* __restrict__ slot, const uint16_t* __restrict__ comb_s,
@@ -566,7 +567,7 @@ size_t tcd_smem_bytes(int d, int f) {
          sizeof(int) * (TCD_WARPS + 1) * kDirectMaxPairs + (GATE_UP ? sizeof(int) * (f / 16) : 0);
 }
 
-// Three gate/up CTAs or four down CTAs per SM at the Nano shapes (the limits admit larger ones at lower occupancy).
+// Four CTAs per SM at the Nano shapes (the limits admit larger ones at lower occupancy).
 constexpr int kTcdMaxSmemGateUp = 110 * 1024, kTcdMaxSmemDown = 54 * 1024;
 
 bool tc_direct_supported(bool gate_up, int d, int f, int block, const void* wq, const void* ws, const void* src) {
@@ -620,7 +621,7 @@ cudaError_t launch_int4_direct(bool gate_up, const int32_t* idx, int pairs, int 
   if (tc_direct_supported(gate_up, d, f, block, wq, ws, src)) {
     // At most `pairs` distinct experts; one resident wave of CTAs walks the units.
     const long long units = (long long)pairs * (gate_up ? f / 16 : d / 32);
-    const int grid = (int)std::min<long long>(units, decode_grid() / 4 * (gate_up ? 3 : 4));
+    const int grid = (int)std::min<long long>(units, decode_grid());  // four resident CTAs per SM
     const size_t smem = gate_up ? tcd_smem_bytes<true>(d, f) : tcd_smem_bytes<false>(d, f);
     const cudaError_t ea = tcd_raise_smem_limits();
     if (ea != cudaSuccess) return ea;
