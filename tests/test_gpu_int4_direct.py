@@ -75,7 +75,13 @@ CASES = [
     (64, {}, True),
     (64, dict(skew_zipf_s=1.2), False),
     (64, dict(d=512, f=256, F=512), True),
+    # with a shared expert and d = 256 (the skinny shared-expert kernels want d a multiple
+    # of 512) the layer takes the permutation path instead: checked here all the same
     (24, dict(d=256, f=128, F=256, E=16), False),
+    # no shared expert: the CUDA-core kernels where the tensor-core ones do not apply
+    # (d = 192: gate/up and down; f = 128: the down projection)
+    (24, dict(d=192, f=128, F=0, E=16), True),
+    (40, dict(d=256, f=128, F=0, E=16), False),
 ]
 
 
