@@ -380,7 +380,8 @@ moe_status_t run_ffn_int4(const moe_shape_t* s, const void* x_bf16, const LayerW
     e = launch_grouped_gemm(off, L.offsets, s->E, s2, comb, Tk, st, &bad);
     if (bad) return MOE_ERR_UNSUPPORTED;
   } else {
-    e = launch_combine(L.y, nullptr, L.inv_pos, L.gate, comb.residual, out, s->T, s->k, s->d, st);
+    // Without the permutation comb.inv_pos is null: the routed rows are indexed by pair.
+    e = launch_combine(L.y, nullptr, comb.inv_pos, L.gate, comb.residual, out, s->T, s->k, s->d, st);
   }
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
