@@ -629,27 +629,37 @@ __global__ void __launch_bounds__(SV_THREADS, 1) serve_kernel(const __grid_const
                            lane);
     __syncthreads();
     const int ng = f / 32;
+    // Each half-warp takes one token of the row at a time (two in flight per warp): its 16
+    // lanes share the row's groups and reduce among themselves.  The token loop is the
+    // same for the whole warp, so every lane reaches each shuffle.
+    const int half = lane >> 4, hl = lane & 15;
     for (int r = i0 + warp; r < i1; r += SV_WARPS) {
 #pragma unroll 1
-      for (int t = 0; t < T; ++t) {
+      for (int t0 = 0; t0 < T; t0 += 2) {
+        const int t = t0 + half;
+        const bool tv = t < T;
         float o = 0.f;
-        if (F > 0)
+        if (F > 0 && tv)
           for (int w = 0; w < SV_WARPS; ++w) o += red[w * 128 + (r - i0) * 8 + t];
 #pragma unroll 1
         for (int j = 0; j < k; ++j) {
-          const int q = t * k + j;
+          const int q = (tv ? t : 0) * k + j;
           const uint8_t* rows = sm + p.o_rd + s_pu[q] * rd_bytes;  // this expert's prefetched rows
           const uint8_t* codes = rows + (r - i0) * (f / 2);
           const uint16_t* scales = reinterpret_cast<const uint16_t*>(rows + rd_codes) + (r - i0) * ng;
           float acc = 0.f;
 #pragma unroll 1
-          for (int g = lane; g < ng; g += 32)
-            acc = fmaf(__half2float(__ushort_as_half(scales[g])),
-                       group_qdot(*reinterpret_cast<const uint4*>(codes + g * 16), hh + (long long)q * f + g * 32), acc);
-          const float y = bf16_round(warp_sum(acc));  // the routed output is stored in bf16
+          for (int g = hl; g < ng; g += 16)
+            if (tv)
+              acc = fmaf(__half2float(__ushort_as_half(scales[g])),
+                         group_qdot(*reinterpret_cast<const uint4*>(codes + g * 16), hh + (long long)q * f + g * 32),
+                         acc);
+#pragma unroll
+          for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(FULLM, acc, off);
+          const float y = bf16_round(acc);  // the routed output is stored in bf16
           o = fmaf(s_gate[q], y, o);
         }
-        if (lane == 0) {
+        if (hl == 0 && tv) {
           if (p.residual) o += __bfloat162float(__ushort_as_bfloat16(p.residual[(long long)t * d + r]));
           p.out[(long long)t * d + r] = bf16_bits(o);
         }
