@@ -950,7 +950,8 @@ def gpu_cache_arm(args, rank, world, dist):
                 "h2d_bytes_per_step": int(hx.numel() * hx.element_size()),
                 "d2h_bytes_per_step": int(hout.numel() * hout.element_size()),
                 "copies": "tokens in from pinned memory and the output back on the compute stream"},
-        "gpu_launches": K * (kernels_per_call(s) + 2),
+        # the cache's plan and copy kernels, unless they ran inside the single serving launch
+        "gpu_launches": K * (kernels_per_call(s) + (0 if fused else 2)),
         "clocks": sampler.summary(tw0, tw1),
         "device_status": status,
     }
