@@ -414,18 +414,17 @@ __global__ void __launch_bounds__(SV_THREADS, 1) serve_kernel(const __grid_const
       if (lane < k && p.renorm) s_gate[t * k + lane] = __fdiv_rn(s_gate[t * k + lane], denom);
     }
     __syncthreads();
-    if (tid == 0) {
-      // Distinct experts in order of first appearance; each pair's distinct index.
-      int nu = 0;
-      for (int q = 0; q < P; ++q) {
-        const int e = s_idx[q];
-        int u = 0;
-        while (u < nu && s_ue[u] != e) ++u;
-        if (u == nu) s_ue[nu++] = e;
-        s_pu[q] = u;
-      }
-      s_nu = nu;
-      for (int u = 0; u < nu; ++u) s_we[u] = s_ue[u];
+    if (warp == 0) {
+      // Distinct experts in order of first appearance; each pair's distinct index (pair q
+      // in lane q, P <= 32; every lane takes part in the match and the ballot).
+      const int e = lane < P ? s_idx[lane] : -1 - lane;
+      const unsigned same = __match_any_sync(FULLM, e);
+      const int first = __ffs(same) - 1;  // the first pair with this lane's expert
+      const unsigned firsts = __ballot_sync(FULLM, lane < P && first == lane);
+      const int u = __popc(firsts & ((1u << first) - 1u));
+      if (lane < P) s_pu[lane] = u;
+      if (lane < P && first == lane) s_ue[u] = s_we[u] = e;
+      if (lane == 0) s_nu = __popc(firsts);
     }
     __syncthreads();
     if (c == 0) {
