@@ -325,17 +325,18 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 2) int4_direct_kernel(
 // (expert, row tile); the experts are the distinct ones of the routing result, in the
 // order of their first pair.  The CTA's 8 warps share a unit: gate/up, 16 gate rows and
 // the 16 matching up rows with K split 8 ways; down, two 16-row tiles with K split 4
-// ways.  Each CTA walks its units through a ring of tcd_stages<GATE_UP>() shared-memory stages
-// filled by cp.async (a unit's code rows and scale rows, each row padded by 16 bytes so
-// the fragment reads below fall in distinct banks), so the next units' weights stream
-// in while one is multiplied.  Per 32-input group a lane reads one 32-bit word of 8
+// ways.  Each CTA walks its units through a ring of shared-memory stages (two for gate/up,
+// four for down) filled by cp.async (a unit's code rows and scale rows, each row padded
+// by 16 bytes so the fragment reads below fall in distinct banks), so the next units'
+// weights stream in while one is multiplied.  Per 32-input group a lane reads one 32-bit word of 8
 // codes (word l%4) of each of its rows l/4 and l/4 + 8 and forms bf16 pairs of nibbles
 // (i, i + 4) (`q_pair`).  The sum over k may run in any order as long as both operands
 // follow it, so the lane's B fragment holds the inputs at those same positions: its 8
 // consecutive bf16 of the pair's row, re-paired (`input_pairs`).  A group's two 16-deep
 // steps accumulate from zero and its fp16 scale multiplies that partial once (every
 // product q * x exact, as in the CUDA-core path); the warps' partials are summed in a
-// fixed order through shared memory.
+// fixed order through shared memory.  With one expert per token the down projection can
+// end with the combine: out = bf16(s + gate * y), y still in fp32 (`comb_s`, `comb_gate`).
 constexpr int TCD_WARPS = 8;
 // Ring depth: two stages let four gate/up CTAs share an SM (more warps to hide latency
 // beat a deeper ring); four for the down projection, also four CTAs per SM.
